@@ -1,0 +1,371 @@
+#!/usr/bin/env python
+"""Benchmark of the drafter hot path on GB300.
+
+Default workload (N = 1): the FlashMap-Qwen3-4B-shaped draft step --
+fm_context_append of 17 feature rows at position 1024 (rewinding to 1024 every
+step, so every step is identical) followed by fm_draft of the 16-slot block at
+position 1041 (1042 cross-attention keys).  One step reads ~1.3 GB (all
+weights, the Q8_0 table, the cache), far more than the 129 MB L2, so no L2
+flush is needed between steps.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle (the only
+reference implementation of this path) on the same workload.
+``--workload`` selects another timed unit: prefill (32768-row context
+injection), dflash (draft/accept cycles), tiny.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft steps/sec + achieved HBM GB/s (16-slot block); context prefill rows/sec"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="flashmap4b", choices=["flashmap4b", "prefill", "dflash", "tiny"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill rows/s figure")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), float(m.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier_max(ws, value):
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as d
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    d.all_reduce(t, op=d.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- workloads
+
+class FlashMapStep:
+    """append(17 rows at 1024) + draft(anchor, 1041) on the FlashMap-4B shape."""
+    name = "flashmap4b_step"
+
+    def __init__(self, torch):
+        import block_speculative_decoding_fm_gb300 as fm
+        import fm_synth as S
+        self.fm, self.S, self.torch = fm, S, torch
+        self.cfg = S.flashmap_4b_config()
+        w = S.gen_weights(self.cfg, 1002)
+        self.mod = S.gen_modulation(self.cfg, 1002)
+        self.h = fm.fm_create(self.cfg, fm.weight_items(w), self.mod)
+        self.raw = {n: t.data for n, t in w.items()}
+        fr = S.streams(1002)["features"]
+        self.ctx = S.gen_features(fr, 1024, self.cfg.feat_dim)
+        self.f17 = S.gen_features(fr, 17, self.cfg.feat_dim)
+        self.anchor = S.gen_anchor(S.streams(1002)["tokens"], self.cfg.vocab)
+        fm.fm_context_append(self.h, 0, torch.from_numpy(self.ctx).cuda(), 1024, 0)
+        self.f17_dev = torch.from_numpy(self.f17).cuda()
+        self.tokens = torch.zeros((1, 16), dtype=torch.int32, device="cuda")
+        self.f17_host = torch.from_numpy(self.f17).pin_memory()
+        self.tok_host = torch.zeros((1, 16), dtype=torch.int32).pin_memory()
+        self.launches = 0
+        c = self.cfg
+        D, F, Ht, L = c.dim, c.ff_dim, c.target_dim, c.n_layers
+        weights = (D * c.feat_dim + D * Ht * 2 + L * (4 * D * D + 4 * D * D + 2 * F * D) + Ht * D) * 2
+        table = c.vocab * (Ht + Ht // 16)
+        kv_read = L * 2 * 1042 * D * 2
+        feats = 17 * c.feat_dim * 4
+        kv_write = L * 2 * 18 * D * 2
+        self.bytes_per_step = weights + table + kv_read + feats + kv_write
+        # the anchor row's K/V projection re-reads the 12 cross K/V matrices
+        self.bytes_per_step_moved = self.bytes_per_step + L * 2 * D * D * 2
+
+    def step(self):
+        fm = self.fm
+        fm.fm_context_append(self.h, 0, self.f17_dev, 17, 1024)
+        self.launches += fm.fm_last_launch_count(self.h)
+        fm.fm_draft(self.h, [0], [self.anchor], [1041], self.tokens)
+        self.launches += fm.fm_last_launch_count(self.h)
+
+    def step_e2e(self):
+        self.f17_dev.copy_(self.f17_host, non_blocking=True)
+        self.step()
+        self.tok_host.copy_(self.tokens, non_blocking=True)
+
+    e2e_h2d = 17 * 12800 * 4
+    e2e_d2h = 16 * 4
+
+    def oracle_setup(self):
+        from oracle import FlashMap
+        o = FlashMap(self.cfg, self.raw, self.mod, True)
+        st = o.new_state()
+        o.context_append(st, self.ctx, 0)
+        return o, st
+
+    def oracle_step(self, o, st):
+        o.context_append(st, self.f17, 1024)
+        o.draft(st, self.anchor, 1041)
+
+
+class PrefillStep:
+    """fm_context_append of 32768 feature rows (12800 wide) from position 0."""
+    name = "prefill_32768"
+
+    def __init__(self, torch, rows=32768):
+        import block_speculative_decoding_fm_gb300 as fm
+        import fm_synth as S
+        self.fm, self.torch, self.rows = fm, torch, rows
+        self.cfg = S.flashmap_4b_config(max_ctx=rows + 64)
+        w = S.gen_weights(self.cfg, 1003)
+        self.h = fm.fm_create(self.cfg, fm.weight_items(w), S.gen_modulation(self.cfg, 1003))
+        self.feats = torch.from_numpy(S.gen_features(S.streams(1003)["features"], rows, self.cfg.feat_dim)).cuda()
+        self.launches = 0
+        c = self.cfg
+        self.flops = 2.0 * rows * c.dim * (c.feat_dim + 2 * c.n_layers * c.dim)
+
+    def step(self):
+        self.fm.fm_context_append(self.h, 0, self.feats, self.rows, 0)
+        self.launches += self.fm.fm_last_launch_count(self.h)
+
+
+def time_steps(torch, fn, k):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(k):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def cpu_baseline(w, budget_s=15.0):
+    o, st = w.oracle_setup()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        w.oracle_step(o, st)
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= 20:
+            break
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- arms
+
+def run_reference(args):
+    ws, rank, _ = dist()
+    if rank != 0:
+        return
+    import torch  # noqa: F401
+    from types import SimpleNamespace
+    w = SimpleNamespace()
+    import fm_synth as S
+    from oracle import FlashMap
+    cfg = S.flashmap_4b_config()
+    wt = S.gen_weights(cfg, 1002)
+    mod = S.gen_modulation(cfg, 1002)
+    fr = S.streams(1002)["features"]
+    ctx = S.gen_features(fr, 1024, cfg.feat_dim)
+    f17 = S.gen_features(fr, 17, cfg.feat_dim)
+    anchor = S.gen_anchor(S.streams(1002)["tokens"], cfg.vocab)
+    o = FlashMap(cfg, {n: t.data for n, t in wt.items()}, mod, True)
+    st = o.new_state()
+    o.context_append(st, ctx, 0)
+    for _ in range(args.warmup):
+        o.context_append(st, f17, 1024)
+        o.draft(st, anchor, 1041)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.context_append(st, f17, 1024)
+        o.draft(st, anchor, 1041)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "flashmap4b_step: append 17 rows at 1024 + 16-slot draft at 1041 (L=1042)",
+                       "global_batch": 16, "seq_len": 1042, "parallelism": "replicas", "l2": "inputs > L2"},
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} full steps after {args.warmup} warm-up steps",
+                             "blas_threads": blas_threads()},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as d
+        d.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from block_speculative_decoding_fm_gb300 import build
+    build.build()
+    import block_speculative_decoding_fm_gb300 as fm
+    hbm, bf16, bf16s, peak_src = peaks()
+
+    w = FlashMapStep(torch)
+    for _ in range(max(3, args.warmup)):
+        w.step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    w.launches = 0
+    with Clocks(local) as clk:
+        ms = time_steps(torch, w.step, args.steps)
+    launches = w.launches
+    ms = barrier_max(ws, ms)
+    steps_s = args.steps * ws / (ms / 1000)
+    hbm_gbs = w.bytes_per_step * steps_s / ws / 1e9
+
+    # end to end through the C ABI with host buffers (H2D of the feature rows,
+    # D2H of the drafted tokens inside the timed region)
+    for _ in range(3):
+        w.step_e2e()
+    ms_e2e = barrier_max(ws, time_steps(torch, w.step_e2e, args.steps))
+    e2e = {"value": args.steps * ws / (ms_e2e / 1000), "unit": "steps/s", "h2d_bytes_per_step": w.e2e_h2d,
+           "d2h_bytes_per_step": w.e2e_d2h}
+
+    # per-kernel device time (events around every launch; a separate pass)
+    fm.fm_set_debug(w.h, fm.FM_DEBUG_PROFILE)
+    for _ in range(20):
+        w.step()
+    prof = fm.fm_profile_read(w.h)
+    fm.fm_set_debug(w.h, 0)
+    top = max(prof.items(), key=lambda kv: kv[1][1])
+    name, (nl, tms, tb) = top
+    per_launch_ms = tms / nl
+    achieved = (tb / nl) / (per_launch_ms / 1000) / 1e9
+    kernels = {k: {"launches": v[0] // 20, "ms_per_step": v[1] / 20,
+                   "gbs": (v[2] / v[0]) / ((v[1] / v[0]) / 1000) / 1e9} for k, v in sorted(prof.items())}
+    roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None, "peak_source": f"{peak_src} burst copy",
+                "bytes_per_launch": tb / nl, "ms_per_launch": per_launch_ms}
+
+    extra = {}
+    if not args.no_prefill and rank == 0:
+        pf = PrefillStep(torch)
+        pf.step()
+        torch.cuda.synchronize()
+        pms = time_steps(torch, pf.step, 2) / 2
+        extra["prefill_rows_per_s"] = pf.rows / (pms / 1000)
+        extra["prefill_tflops"] = pf.flops / (pms / 1000) / 1e12
+        fm.fm_destroy(pf.h)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n, dt = cpu_baseline(w)
+        cpu = {"value": v, "unit": "steps/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"{n} full append+draft steps of the same workload in {dt:.1f} s",
+               "blas_threads": blas_threads()}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": steps_s, "unit": "steps/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, f32 activations", "data": "synthetic",
+                "config": {"workload": "flashmap4b_step: append 17 rows at 1024 + 16-slot draft at 1041 (L=1042), "
+                                       "Q8_0 vocab 151936", "global_batch": 16 * ws, "seq_len": 1042,
+                           "parallelism": "replicas" if ws > 1 else "single", "l2": "inputs > L2 (1.35 GB/step)"},
+                "achieved_hbm_gbs": hbm_gbs, "bytes_per_step": w.bytes_per_step,
+                "e2e": e2e, "gpu_launches": launches, "roofline": roofline, "kernels": kernels,
+                "clocks": clk.summary(), "cpu_baseline": cpu, **extra}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

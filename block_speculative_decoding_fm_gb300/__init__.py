@@ -1,0 +1,244 @@
+"""Python binding of libfm.so (include/fm.h): argument marshalling only.
+
+Every function below has the name of the C entry point it calls and does
+nothing but convert arguments (numpy / torch tensors, streams) and turn a
+non-zero status into an ``FmError``.  All compute runs in the library's CUDA
+kernels; there is no CPU fallback: if the library is missing or cannot load,
+``load_library`` raises.  PyTorch supplies device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Iterable, Optional, Sequence, Tuple
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfm.so")
+
+# status codes (fm_status)
+FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_OOM, FM_ERR_CONTEXT_FULL, FM_ERR_STATE, FM_ERR_CUDA, \
+    FM_ERR_TIMEOUT = range(8)
+FM_VARIANT_FLASHMAP, FM_VARIANT_DFLASH = 0, 1
+FM_LM_BF16, FM_LM_Q8_0 = 0, 1
+FM_DTYPE_BF16, FM_DTYPE_Q8_0, FM_DTYPE_F32 = 0, 1, 2
+FM_DEBUG_HIDDEN, FM_DEBUG_HEAD_OUT, FM_DEBUG_LOGITS, FM_DEBUG_CACHE_K, FM_DEBUG_CACHE_V, FM_DEBUG_H0 = range(6)
+FM_DEBUG_KEEP_HIDDEN = 1
+FM_DEBUG_PROFILE = 2
+
+EXPORTS = ["fm_create", "fm_context_append", "fm_context_append_batched", "fm_draft", "fm_accept",
+           "fm_accept_batched", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
+           "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy"]
+
+
+class FmConfig(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int32), ("dim", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("ff_dim", ctypes.c_int32),
+                ("block", ctypes.c_int32), ("target_dim", ctypes.c_int32), ("n_taps", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("lm_format", ctypes.c_int32), ("max_ctx", ctypes.c_int32),
+                ("max_seqs", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("ln_eps", ctypes.c_float),
+                ("rms_eps", ctypes.c_float), ("qk_eps", ctypes.c_float)]
+
+
+class FmTensor(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("data", ctypes.c_void_p), ("nbytes", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("on_device", ctypes.c_int32)]
+
+
+class FmKernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int32), ("ms", ctypes.c_float),
+                ("bytes", ctypes.c_double)]
+
+
+class FmError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libfm.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run block_speculative_decoding_fm_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "fm_create": (I32, [ctypes.POINTER(FmConfig), ctypes.POINTER(FmTensor), I32, P, P, ctypes.POINTER(P)]),
+        "fm_context_append": (I32, [P, I32, P, I32, I32, P]),
+        "fm_context_append_batched": (I32, [P, I32, P, P, P, P, P]),
+        "fm_draft": (I32, [P, I32, P, P, P, P, P]),
+        "fm_accept": (I32, [P, P, I32, P, P]),
+        "fm_accept_batched": (I32, [P, I32, P, P, P, P, P, P]),
+        "fm_debug_copy": (I32, [P, I32, I32, I32, I64, P, I64, P]),
+        "fm_set_debug": (I32, [P, I32]),
+        "fm_get_length": (I32, [P, I32, ctypes.POINTER(I32)]),
+        "fm_memory_bytes": (I32, [P, ctypes.POINTER(I64)]),
+        "fm_last_launch_count": (I32, [P, ctypes.POINTER(I32)]),
+        "fm_profile_read": (I32, [P, ctypes.POINTER(FmKernelTime), I32, ctypes.POINTER(I32)]),
+        "fm_status_str": (ctypes.c_char_p, [I32]),
+        "fm_last_error": (ctypes.c_char_p, [P]),
+        "fm_destroy": (None, [P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, handle=None):
+    if status != FM_OK:
+        lib = load_library()
+        msg = lib.fm_last_error(handle).decode() if handle is not None else lib.fm_last_error(None).decode()
+        raise FmError(status, f"{lib.fm_status_str(status).decode()}: {msg}")
+
+
+def make_config(cfg) -> FmConfig:
+    """An FmConfig from any object with the fm_config fields."""
+    return FmConfig(cfg.variant, cfg.dim, cfg.n_heads, cfg.head_dim, cfg.n_layers, cfg.ff_dim, cfg.block,
+                    cfg.target_dim, cfg.n_taps, cfg.vocab, cfg.lm_format, cfg.max_ctx, cfg.max_seqs,
+                    cfg.rope_theta, cfg.ln_eps, cfg.rms_eps, cfg.qk_eps)
+
+
+def fm_create(cfg, weights: Iterable[Tuple[str, object, int]], modulation=None, stream=None) -> ctypes.c_void_p:
+    """weights: (name, array, FM_DTYPE_*) triples; arrays are host numpy
+    arrays or CUDA tensors (their raw bytes are passed)."""
+    lib = load_library()
+    items = list(weights)
+    keep = []
+    arr = (FmTensor * max(1, len(items)))()
+    for i, (name, data, dtype) in enumerate(items):
+        on_dev = 0
+        if isinstance(data, np.ndarray):
+            data = np.ascontiguousarray(data)
+            nbytes = data.nbytes
+        else:
+            on_dev = 1 if data.is_cuda else 0
+            nbytes = data.numel() * data.element_size()
+        keep.append(data)
+        bname = name.encode()
+        keep.append(bname)
+        arr[i] = FmTensor(bname, _ptr(data), nbytes, dtype, on_dev)
+    mod = None
+    if modulation is not None:
+        mod = np.ascontiguousarray(modulation, dtype=np.float32)
+        keep.append(mod)
+    c = make_config(cfg)
+    h = ctypes.c_void_p()
+    _check(lib.fm_create(ctypes.byref(c), arr, len(items), _ptr(mod), _stream(stream), ctypes.byref(h)))
+    return h
+
+
+def fm_context_append(h, seq: int, feats, n_rows: int, start_pos: int, stream=None) -> None:
+    lib = load_library()
+    _check(lib.fm_context_append(h, seq, _ptr(feats), n_rows, start_pos, _stream(stream)), h)
+
+
+def fm_context_append_batched(h, seq_ids: Sequence[int], feats, n_rows: Sequence[int], starts: Sequence[int],
+                              stream=None) -> None:
+    lib = load_library()
+    n = len(seq_ids)
+    ids = np.ascontiguousarray(seq_ids, np.int32)
+    nr = np.ascontiguousarray(n_rows, np.int32)
+    st = np.ascontiguousarray(starts, np.int32)
+    _check(lib.fm_context_append_batched(h, n, _ptr(ids), _ptr(feats), _ptr(nr), _ptr(st), _stream(stream)), h)
+
+
+def fm_draft(h, seq_ids: Sequence[int], anchors: Sequence[int], pos: Sequence[int], tokens, stream=None) -> None:
+    """tokens: a CUDA int32 tensor [n_seqs, block] that receives the drafts."""
+    lib = load_library()
+    ids = np.ascontiguousarray(seq_ids, np.int32)
+    an = np.ascontiguousarray(anchors, np.int32)
+    ps = np.ascontiguousarray(pos, np.int32)
+    _check(lib.fm_draft(h, len(ids), _ptr(ids), _ptr(an), _ptr(ps), _ptr(tokens), _stream(stream)), h)
+
+
+def fm_accept(draft: Sequence[int], target: Sequence[int], k: int) -> Tuple[int, int]:
+    lib = load_library()
+    d = np.ascontiguousarray(draft, np.int32)
+    t = np.ascontiguousarray(target, np.int32)
+    acc, bonus = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.fm_accept(_ptr(d), _ptr(t), k, ctypes.byref(acc), ctypes.byref(bonus)))
+    return acc.value, bonus.value
+
+
+def fm_accept_batched(h, draft, target, k, n_accepted, bonus, stream=None) -> None:
+    lib = load_library()
+    _check(lib.fm_accept_batched(h, draft.shape[0], _ptr(draft), _ptr(target), _ptr(k), _ptr(n_accepted),
+                                 _ptr(bonus), _stream(stream)), h)
+
+
+def fm_debug_copy(h, what: int, seq: int, index: int, out: np.ndarray, offset: int = 0, stream=None) -> np.ndarray:
+    lib = load_library()
+    _check(lib.fm_debug_copy(h, what, seq, index, offset, _ptr(out), out.nbytes, _stream(stream)), h)
+    return out
+
+
+def fm_set_debug(h, flags: int) -> None:
+    _check(load_library().fm_set_debug(h, flags), h)
+
+
+def fm_get_length(h, seq: int) -> int:
+    v = ctypes.c_int32()
+    _check(load_library().fm_get_length(h, seq, ctypes.byref(v)), h)
+    return v.value
+
+
+def fm_memory_bytes(h) -> int:
+    v = ctypes.c_int64()
+    _check(load_library().fm_memory_bytes(h, ctypes.byref(v)), h)
+    return v.value
+
+
+def fm_last_launch_count(h) -> int:
+    v = ctypes.c_int32()
+    _check(load_library().fm_last_launch_count(h, ctypes.byref(v)), h)
+    return v.value
+
+
+def fm_profile_read(h):
+    """{kernel name: (launches, total ms, total algorithmic bytes)} since the last read."""
+    lib = load_library()
+    buf = (FmKernelTime * 64)()
+    n = ctypes.c_int32()
+    _check(lib.fm_profile_read(h, buf, 64, ctypes.byref(n)), h)
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].ms, buf[i].bytes) for i in range(min(n.value, 64))}
+
+
+def fm_destroy(h) -> None:
+    if h is not None:
+        load_library().fm_destroy(h)
+
+
+def weight_items(tensors: Dict[str, object]):
+    """(name, array, dtype) triples from name -> object with .data / .dtype."""
+    return [(n, t.data, t.dtype) for n, t in tensors.items()]

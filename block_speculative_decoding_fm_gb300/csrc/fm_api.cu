@@ -1,0 +1,1268 @@
+// fm_api.cu -- host runtime behind the C ABI in include/fm.h: weight intake
+// and repacking, the device buffer plan, and the launch sequences of context
+// injection and drafting.  Every compute step is one of this library's
+// kernels; the host only checks arguments, fills the per-call parameter slot
+// and enqueues launches (chained with programmatic dependent launch).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/fm.h"
+#include "fm_internal.h"
+
+using namespace fm;
+
+namespace {
+
+constexpr int kParamSlots = 64;
+
+struct Seg2 {  // cache pointers of one sequence and layer
+  __half *k, *v;
+};
+
+struct ProfRec {
+  std::string name;
+  cudaEvent_t e0, e1;
+  double bytes;
+};
+
+}  // namespace
+
+struct fm_handle {
+  fm_config cfg{};
+  std::string err;
+  int n_sm = 148;
+  int dev = 0;
+  int64_t bytes = 0;
+  int32_t debug = 0;
+  int32_t last_launches = 0;
+  std::vector<void *> allocs;
+
+  // ---- weights (FlashMap) ----
+  __nv_bfloat16 *w_fc = nullptr, *w_hn = nullptr, *w_ap = nullptr, *b_ap = nullptr, *w_an = nullptr;
+  __nv_bfloat16 *w_sn = nullptr, *w_xe = nullptr, *b_xe = nullptr, *w_head = nullptr, *b_head = nullptr;
+  __nv_bfloat16 *w_kvall = nullptr, *w_ckn = nullptr;
+  std::vector<__nv_bfloat16 *> w_qkv, w_sqn, w_skn, w_so, w_cq, w_cqn, w_co, w_f1, b_f1, w_f2, b_f2;
+  float *mod = nullptr;
+  // ---- weights (DFlash) ----
+  std::vector<__nv_bfloat16 *> w_o, w_gu, w_down;
+  __nv_bfloat16 *attn_norm = nullptr, *ff_norm = nullptr, *ctx_norm = nullptr, *out_norm = nullptr;
+  __nv_bfloat16 *w_c = nullptr, *w_tok = nullptr, *block_pos = nullptr, *w_out = nullptr;
+  float *hinit = nullptr;
+  // ---- token table ----
+  int8_t *tq = nullptr;
+  __half *tsc = nullptr;
+  __nv_bfloat16 *tb = nullptr;
+  int Vpad = 0;
+
+  // ---- state ----
+  __half *cache = nullptr;
+  size_t cache_plane = 0;  // elements of one [H][max_ctx][hd] plane
+  std::vector<int32_t> length;
+  float2 *rope = nullptr;
+  int rope_pos = 0;
+  float *h0 = nullptr;
+
+  // ---- work buffers ----
+  float *X = nullptr, *qkv = nullptr, *qc = nullptr, *attn = nullptr, *u = nullptr, *Y = nullptr;
+  float *ctx = nullptr, *actx = nullptr, *uni = nullptr, *hid = nullptr, *dbg_logits = nullptr;
+  float2 *st_x = nullptr, *st_h0 = nullptr, *st_c = nullptr, *st_a = nullptr, *st_u = nullptr, *st_init = nullptr;
+  float *part_o = nullptr;
+  float2 *part_ml = nullptr, *lm_part = nullptr;
+  int max_splits = 1;
+  int32_t *tickets = nullptr;  // [0, H): self, [H, 2H): cross, [2H]: lm head
+  int32_t *tok_tmp = nullptr;
+
+  // ---- diagnostics ----
+  std::vector<ProfRec> prof;
+  std::vector<cudaEvent_t> ev_pool;
+
+  // ---- per-call parameters ----
+  StepParams *sp_dev = nullptr;
+  StepParams *sp_host = nullptr;  // pinned
+  cudaEvent_t sp_ev[kParamSlots]{};
+  int sp_next = 0;
+
+  Seg2 kv(int seq, int l) const {
+    const size_t base = ((size_t)seq * cfg.n_layers + l) * 2 * cache_plane;
+    return {cache + base, cache + base + cache_plane};
+  }
+};
+
+namespace {
+
+thread_local std::string g_create_error;  // reason of the last failed fm_create on this thread
+
+fm_status fail(fm_handle *h, fm_status s, const char *fmt, ...) {
+  if (h) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    h->err = buf;
+  }
+  return s;
+}
+
+#define CK(expr)                                                                                     \
+  do {                                                                                               \
+    cudaError_t e_ = (expr);                                                                         \
+    if (e_ != cudaSuccess) return fail(h, FM_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));     \
+  } while (0)
+
+// Fault injection for the allocation path (host side only): FM_FAULT_INJECT=alloc:N
+// makes the N-th device allocation of a handle report out-of-memory.
+int fault_alloc_at() {
+  const char *s = getenv("FM_FAULT_INJECT");
+  if (!s || strncmp(s, "alloc:", 6) != 0) return -1;
+  return atoi(s + 6);
+}
+
+template <typename T>
+fm_status dalloc(fm_handle *h, T **p, size_t count) {
+  const int inject = fault_alloc_at();
+  if (inject >= 0 && (int)h->allocs.size() + 1 == inject) {
+    *p = nullptr;
+    return fail(h, FM_ERR_OOM, "injected allocation failure at allocation %d", inject);
+  }
+  const size_t bytes = count * sizeof(T) > 0 ? count * sizeof(T) : 16;
+  void *q = nullptr;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return fail(h, FM_ERR_OOM, "cudaMalloc(%zu bytes): %s", bytes, cudaGetErrorString(e));
+  }
+  h->allocs.push_back(q);
+  h->bytes += (int64_t)bytes;
+  *p = static_cast<T *>(q);
+  return FM_OK;
+}
+
+#define TRY(expr)                    \
+  do {                               \
+    fm_status s_ = (expr);           \
+    if (s_ != FM_OK) return s_;      \
+  } while (0)
+
+struct TensorSet {
+  std::unordered_map<std::string, const fm_tensor *> by_name;
+};
+
+fm_status find(fm_handle *h, const TensorSet &ts, const std::string &name, int64_t nbytes, int32_t dtype,
+               bool required, const fm_tensor **out) {
+  *out = nullptr;
+  auto it = ts.by_name.find(name);
+  if (it == ts.by_name.end()) {
+    if (required) return fail(h, FM_ERR_INVALID_ARG, "missing tensor %s", name.c_str());
+    return FM_OK;
+  }
+  const fm_tensor *t = it->second;
+  if (t->dtype != dtype) return fail(h, FM_ERR_INVALID_ARG, "tensor %s: dtype %d, expected %d", name.c_str(), t->dtype, dtype);
+  if (t->nbytes != nbytes)
+    return fail(h, FM_ERR_INVALID_ARG, "tensor %s: %lld bytes, expected %lld", name.c_str(), (long long)t->nbytes,
+                (long long)nbytes);
+  if (!t->data) return fail(h, FM_ERR_INVALID_ARG, "tensor %s: null data", name.c_str());
+  *out = t;
+  return FM_OK;
+}
+
+// copy a bf16 tensor (required unless `optional`) to dst; absent optional -> zeros
+fm_status put_bf16(fm_handle *h, const TensorSet &ts, const std::string &name, void *dst, int64_t elems,
+                   cudaStream_t s, bool optional = false) {
+  const fm_tensor *t;
+  TRY(find(h, ts, name, elems * 2, FM_DTYPE_BF16, !optional, &t));
+  if (!t) {
+    CK(cudaMemsetAsync(dst, 0, elems * 2, s));
+    return FM_OK;
+  }
+  CK(cudaMemcpyAsync(dst, t->data, elems * 2, cudaMemcpyDefault, s));
+  return FM_OK;
+}
+
+// copy an [in][out] bf16 matrix transposed into dst ([out][in], row stride ldo)
+fm_status put_bf16_t(fm_handle *h, const TensorSet &ts, const std::string &name, int rows, int cols,
+                     __nv_bfloat16 *dst, int ldo, __nv_bfloat16 *tmp, cudaStream_t s) {
+  const fm_tensor *t;
+  TRY(find(h, ts, name, (int64_t)rows * cols * 2, FM_DTYPE_BF16, true, &t));
+  CK(cudaMemcpyAsync(tmp, t->data, (size_t)rows * cols * 2, cudaMemcpyDefault, s));
+  CK(launch_transpose_bf16(tmp, rows, cols, dst, ldo, s));
+  return FM_OK;
+}
+
+StepParams *next_params(fm_handle *h, const StepParams &p, cudaStream_t s, fm_status *st) {
+  const int i = h->sp_next;
+  h->sp_next = (h->sp_next + 1) % kParamSlots;
+  cudaEventSynchronize(h->sp_ev[i]);  // the slot's previous copy has been consumed
+  h->sp_host[i] = p;
+  cudaError_t e = cudaMemcpyAsync(h->sp_dev + i, h->sp_host + i, sizeof(StepParams), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaEventRecord(h->sp_ev[i], s);
+  if (e != cudaSuccess) {
+    *st = fail(h, FM_ERR_CUDA, "parameter upload: %s", cudaGetErrorString(e));
+    return nullptr;
+  }
+  *st = FM_OK;
+  return h->sp_dev + i;
+}
+
+cudaEvent_t pool_event(fm_handle *h) {
+  if (!h->ev_pool.empty()) {
+    cudaEvent_t e = h->ev_pool.back();
+    h->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Optional event bracket around one launch (FM_DEBUG_PROFILE).
+struct ProfScope {
+  fm_handle *h;
+  cudaStream_t s;
+  ProfRec rec;
+  bool on;
+  ProfScope(fm_handle *h_, cudaStream_t s_, const char *name, double bytes) : h(h_), s(s_), on(h_->debug & FM_DEBUG_PROFILE) {
+    if (!on) return;
+    rec.name = name;
+    rec.bytes = bytes;
+    rec.e0 = pool_event(h);
+    rec.e1 = pool_event(h);
+    cudaEventRecord(rec.e0, s);
+  }
+  ~ProfScope() {
+    if (!on) return;
+    cudaEventRecord(rec.e1, s);
+    h->prof.push_back(rec);
+  }
+};
+
+GemvArgs gemv_base(const fm_handle *h, const __nv_bfloat16 *W, int M, int K, int T_const, const StepParams *sp) {
+  GemvArgs a;
+  memset(&a, 0, sizeof a);
+  a.W = W;
+  a.M = M;
+  a.K = K;
+  a.T_const = T_const;
+  a.sp = sp;
+  const int tiles = (M + kTile - 1) / kTile;
+  int ks = 1;
+  while (ks < 8 && K % (64 * ks * 2) == 0 && tiles * ks * 2 <= 2 * h->n_sm) ks *= 2;
+  a.ksplit = ks;
+  a.Kc = K / ks;
+  const int mt = (T_const > 0 && T_const <= 16) ? 1 : 2;
+  a.Kp = a.Kc < (mt == 1 ? 512 : 256) ? a.Kc : (mt == 1 ? 512 : 256);
+  a.hd = h->cfg.head_dim;
+  a.max_ctx = h->cfg.max_ctx;
+  a.rope = h->rope;
+  a.qk_eps = h->cfg.qk_eps;
+  a.eps = h->cfg.rms_eps;
+  a.inv_n = 1.0f / (float)K;
+  return a;
+}
+
+fm_status run_gemv(fm_handle *h, const GemvArgs &a, cudaStream_t s, const char *tag = "gemv", int T = 16) {
+  const int tiles = (a.M + kTile - 1) / kTile;
+  ProfScope ps(h, s, tag, (double)a.M * a.K * 2 + (double)T * (a.K + a.M) * 4);
+  CK(launch_gemv(a, tiles, s, true));
+  ++h->last_launches;
+  return FM_OK;
+}
+
+int attn_splits(const fm_handle *h, int L) {
+  int sp = (L + 127) / 128;
+  if (sp > h->max_splits) sp = h->max_splits;
+  return sp < 1 ? 1 : sp;
+}
+
+fm_status run_attn(fm_handle *h, const float *Q, int ldq, const Seg2 &kv, int T, int L_src, int L_add, int L_now,
+                   const StepParams *sp, float *out, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  AttnArgs a;
+  memset(&a, 0, sizeof a);
+  a.Q = Q;
+  a.ldq = ldq;
+  a.Kc = kv.k;
+  a.Vc = kv.v;
+  a.max_ctx = c.max_ctx;
+  a.n_heads = c.n_heads;
+  a.hd = c.head_dim;
+  a.splits = attn_splits(h, L_now);
+  a.T_const = T;
+  a.L_src = L_src;
+  a.L_add = L_add;
+  a.sp = sp;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  a.part_o = h->part_o;
+  a.part_ml = h->part_ml;
+  a.tickets = h->tickets + c.n_heads;
+  a.out = out;
+  a.ldo = c.dim;
+  ProfScope ps(h, s, "attn.cross", (double)L_now * c.dim * 2 * 2 + 2.0 * T * c.dim * 4);
+  CK(launch_attn(a, s, true));
+  ++h->last_launches;
+  return FM_OK;
+}
+
+fm_status run_lmhead(fm_handle *h, const float *Y, int T, const StepParams *sp, int32_t *tokens, float *logits,
+                     cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  LmArgs a;
+  memset(&a, 0, sizeof a);
+  if (c.lm_format == FM_LM_Q8_0) {
+    a.q8 = h->tq;
+    a.q8s = h->tsc;
+  } else {
+    a.wb = h->tb;
+  }
+  a.V = c.vocab;
+  a.H = c.target_dim;
+  a.T_const = T;
+  a.sp = sp;
+  a.Y = Y;
+  a.ldy = c.target_dim;
+  a.part = h->lm_part;
+  a.ticket = h->tickets + 2 * c.n_heads;
+  a.tokens = tokens;
+  a.logits = logits;
+  const double tb = c.lm_format == FM_LM_Q8_0 ? (double)c.vocab * (c.target_dim + c.target_dim / 16)
+                                               : (double)c.vocab * c.target_dim * 2;
+  ProfScope ps(h, s, "lm_head", tb + (double)T * c.target_dim * 4);
+  CK(launch_lmhead(a, lmhead_grid(a, h->n_sm), s, true));
+  ++h->last_launches;
+  return FM_OK;
+}
+
+// ---------------------------------------------------------------- FlashMap
+
+// fc -> hidden_norm -> all layers' k / v (k_norm + RoPE) -> f16 cache rows
+fm_status flashmap_append_rows(fm_handle *h, int seq, const StepParams *sp, int T, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int D = c.dim, FW = c.n_taps * c.target_dim;
+  GemvArgs a = gemv_base(h, h->w_fc, D, FW, 0, sp);
+  a.amode = A_PLAIN;
+  a.x_from_sp = 1;
+  a.ldx = FW;
+  a.emode = E_STORE;
+  a.Y = h->ctx;
+  a.ldy = D;
+  a.out_st = h->st_c;
+  TRY(run_gemv(h, a, s, "gemv.fc", T));
+
+  GemvArgs b = gemv_base(h, h->w_kvall, c.n_layers * 2 * D, D, 0, sp);
+  b.amode = A_RMS;
+  b.X = h->ctx;
+  b.ldx = D;
+  b.st = h->st_c;
+  b.st_tiles = D / kTile;
+  b.nw = h->w_hn;
+  b.inv_n = 1.0f / D;
+  b.emode = E_SEGS;
+  b.seg_rows = D;
+  b.n_segs = 2 * c.n_layers;
+  b.pos_src = 1;
+  b.pos_add = 0;
+  for (int l = 0; l < c.n_layers; ++l) {
+    Seg2 kv = h->kv(seq, l);
+    b.segs[2 * l] = {SEG_CACHE, 0, 1, 0, h->w_ckn + (size_t)l * c.head_dim, kv.k};
+    b.segs[2 * l + 1] = {SEG_CACHE, 0, 0, 0, nullptr, kv.v};
+  }
+  return run_gemv(h, b, s, "gemv.kv_append", T);
+}
+
+fm_status flashmap_draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int D = c.dim, B = c.block, Ht = c.target_dim, F = c.ff_dim, L = c.n_layers;
+  StepParams p{};
+  p.T = B;
+  p.pos = pos;
+  p.L = pos + 1;
+  p.anchor = anchor;
+  fm_status st;
+  const StepParams *sp = next_params(h, p, s, &st);
+  if (!sp) return st;
+
+  // the anchor's context slot at pos: anchor_proj(E[anchor]) -> anchor_norm -> k / v of every layer
+  GemvArgs a = gemv_base(h, h->w_ap, D, Ht, 1, sp);
+  a.amode = c.lm_format == FM_LM_Q8_0 ? A_ROW_Q8 : A_ROW_BF16;
+  a.tq = h->tq;
+  a.tscale = h->tsc;
+  a.tb = h->tb;
+  a.emode = E_STORE;
+  a.bias = h->b_ap;
+  a.Y = h->actx;
+  a.ldy = D;
+  a.out_st = h->st_a;
+  TRY(run_gemv(h, a, s, "gemv.anchor_proj", 1));
+
+  GemvArgs kvp = gemv_base(h, h->w_kvall, L * 2 * D, D, 1, sp);
+  kvp.amode = A_RMS;
+  kvp.X = h->actx;
+  kvp.ldx = D;
+  kvp.st = h->st_a;
+  kvp.st_tiles = D / kTile;
+  kvp.nw = h->w_an;
+  kvp.inv_n = 1.0f / D;
+  kvp.emode = E_SEGS;
+  kvp.seg_rows = D;
+  kvp.n_segs = 2 * L;
+  kvp.pos_src = 0;
+  for (int l = 0; l < L; ++l) {
+    Seg2 kv = h->kv(seq, l);
+    kvp.segs[2 * l] = {SEG_CACHE, 0, 1, 0, h->w_ckn + (size_t)l * c.head_dim, kv.k};
+    kvp.segs[2 * l + 1] = {SEG_CACHE, 0, 0, 0, nullptr, kv.v};
+  }
+  TRY(run_gemv(h, kvp, s, "gemv.kv_anchor", 1));
+
+  const float attn_scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+  for (int l = 0; l < L; ++l) {
+    const float *m_self = h->mod + (size_t)(3 * l + 0) * 3 * D;
+    const float *m_cross = h->mod + (size_t)(3 * l + 1) * 3 * D;
+    const float *m_mlp = h->mod + (size_t)(3 * l + 2) * 3 * D;
+    const bool first = l == 0;
+    // self-attention: adaLN -> q, k, v (+ q/k norm, RoPE at pos + 1 + t) -> attention tail
+    GemvArgs q = gemv_base(h, h->w_qkv[l], 3 * D, D, B, sp);
+    q.amode = A_LNMOD;
+    q.X = first ? h->h0 : h->X;
+    q.ldx = first ? 0 : D;
+    q.st = first ? h->st_h0 : h->st_x;
+    q.st_bcast = first ? 1 : 0;
+    q.st_tiles = D / kTile;
+    q.sc = m_self;
+    q.sh = m_self + D;
+    q.eps = c.ln_eps;
+    q.inv_n = 1.0f / D;
+    q.emode = E_SEGS;
+    q.Y = h->qkv;
+    q.ldy = 3 * D;
+    q.seg_rows = D;
+    q.n_segs = 3;
+    q.segs[0] = {SEG_F32, 0, 1, 0, h->w_sqn[l], nullptr};
+    q.segs[1] = {SEG_F32, D, 1, 0, h->w_skn[l], nullptr};
+    q.segs[2] = {SEG_F32, 2 * D, 0, 0, nullptr, nullptr};
+    q.pos_src = 0;
+    q.pos_add = 1;
+    q.tickets = h->tickets;
+    q.attn_out = h->attn;
+    q.self_D = D;
+    q.attn_scale = attn_scale;
+    TRY(run_gemv(h, q, s, "gemv.qkv_self"));
+
+    GemvArgs o = gemv_base(h, h->w_so[l], D, D, B, sp);
+    o.amode = A_PLAIN;
+    o.X = h->attn;
+    o.ldx = D;
+    o.emode = E_RESID;
+    o.R = first ? h->h0 : h->X;
+    o.ldr = first ? 0 : D;
+    o.gate = m_self + 2 * D;
+    o.Y = h->X;
+    o.ldy = D;
+    o.out_st = h->st_x;
+    TRY(run_gemv(h, o, s, "gemv.o_self"));
+
+    // cross-attention over cache rows 0 .. pos
+    GemvArgs cq = gemv_base(h, h->w_cq[l], D, D, B, sp);
+    cq.amode = A_LNMOD;
+    cq.X = h->X;
+    cq.ldx = D;
+    cq.st = h->st_x;
+    cq.st_tiles = D / kTile;
+    cq.sc = m_cross;
+    cq.sh = m_cross + D;
+    cq.eps = c.ln_eps;
+    cq.inv_n = 1.0f / D;
+    cq.emode = E_SEGS;
+    cq.Y = h->qc;
+    cq.ldy = D;
+    cq.seg_rows = D;
+    cq.n_segs = 1;
+    cq.segs[0] = {SEG_F32, 0, 1, 0, h->w_cqn[l], nullptr};
+    cq.pos_src = 0;
+    cq.pos_add = 1;
+    TRY(run_gemv(h, cq, s, "gemv.q_cross"));
+
+    TRY(run_attn(h, h->qc, D, h->kv(seq, l), B, 1, 0, pos + 1, sp, h->attn, s));
+
+    GemvArgs co = gemv_base(h, h->w_co[l], D, D, B, sp);
+    co.amode = A_PLAIN;
+    co.X = h->attn;
+    co.ldx = D;
+    co.emode = E_RESID;
+    co.R = h->X;
+    co.ldr = D;
+    co.gate = m_cross + 2 * D;
+    co.Y = h->X;
+    co.ldy = D;
+    co.out_st = h->st_x;
+    TRY(run_gemv(h, co, s, "gemv.o_cross"));
+
+    // MLP: adaLN -> fc1 + bias -> exact GELU -> fc2 + bias -> gated residual
+    GemvArgs f1 = gemv_base(h, h->w_f1[l], F, D, B, sp);
+    f1.amode = A_LNMOD;
+    f1.X = h->X;
+    f1.ldx = D;
+    f1.st = h->st_x;
+    f1.st_tiles = D / kTile;
+    f1.sc = m_mlp;
+    f1.sh = m_mlp + D;
+    f1.eps = c.ln_eps;
+    f1.inv_n = 1.0f / D;
+    f1.emode = E_GELU;
+    f1.bias = h->b_f1[l];
+    f1.Y = h->u;
+    f1.ldy = F;
+    TRY(run_gemv(h, f1, s, "gemv.fc1"));
+
+    GemvArgs f2 = gemv_base(h, h->w_f2[l], D, F, B, sp);
+    f2.amode = A_PLAIN;
+    f2.X = h->u;
+    f2.ldx = F;
+    f2.emode = E_RESID;
+    f2.bias = h->b_f2[l];
+    f2.R = h->X;
+    f2.ldr = D;
+    f2.gate = m_mlp + 2 * D;
+    f2.Y = h->X;
+    f2.ldy = D;
+    f2.out_st = h->st_x;
+    TRY(run_gemv(h, f2, s, "gemv.fc2"));
+
+    if (h->debug & FM_DEBUG_KEEP_HIDDEN) {
+      CK(cudaMemcpyAsync(h->hid + (size_t)l * kMaxT * D, h->X, (size_t)B * D * 4, cudaMemcpyDeviceToDevice, s));
+    }
+  }
+  // final adaLN -> head -> lm_head + argmax
+  const float *m_fin = h->mod + (size_t)(3 * L) * 3 * D;
+  GemvArgs hd = gemv_base(h, h->w_head, Ht, D, B, sp);
+  hd.amode = A_LNMOD;
+  hd.X = h->X;
+  hd.ldx = D;
+  hd.st = h->st_x;
+  hd.st_tiles = D / kTile;
+  hd.sc = m_fin;
+  hd.sh = m_fin + D;
+  hd.eps = c.ln_eps;
+  hd.inv_n = 1.0f / D;
+  hd.emode = E_STORE;
+  hd.bias = h->b_head;
+  hd.Y = h->Y;
+  hd.ldy = Ht;
+  TRY(run_gemv(h, hd, s, "gemv.head"));
+  return run_lmhead(h, h->Y, B, sp, tokens, nullptr, s);
+}
+
+// ---------------------------------------------------------------- DFlash
+
+// Eq 2 and the retained per-layer context K / V (projectContextRows)
+fm_status dflash_append_rows(fm_handle *h, int seq, const StepParams *sp, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int d = c.dim, FW = c.n_taps * c.target_dim;
+  GemvArgs a = gemv_base(h, h->w_c, d, FW, 0, sp);
+  a.amode = A_PLAIN;
+  a.x_from_sp = 1;
+  a.ldx = FW;
+  a.emode = E_STORE;
+  a.Y = h->ctx;
+  a.ldy = d;
+  a.out_st = h->st_c;
+  a.st_w = h->ctx_norm;
+  TRY(run_gemv(h, a, s, "gemv.wc", 32));
+
+  GemvArgs b = gemv_base(h, h->w_kvall, c.n_layers * 2 * d, d, 0, sp);
+  b.amode = A_RMS2;
+  b.X = h->ctx;
+  b.ldx = d;
+  b.st = h->st_c;
+  b.st_tiles = d / kTile;
+  b.nw = h->ctx_norm;
+  b.nw2 = h->attn_norm;
+  b.nw_rows = 2 * d;
+  b.inv_n = 1.0f / d;
+  b.emode = E_SEGS;
+  b.seg_rows = d;
+  b.n_segs = 2 * c.n_layers;
+  b.pos_src = 1;
+  for (int l = 0; l < c.n_layers; ++l) {
+    Seg2 kv = h->kv(seq, l);
+    b.segs[2 * l] = {SEG_CACHE, 0, 0, 0, nullptr, kv.k};
+    b.segs[2 * l + 1] = {SEG_CACHE, 0, 0, 0, nullptr, kv.v};
+  }
+  return run_gemv(h, b, s, "gemv.kv_append", 32);
+}
+
+fm_status dflash_draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int d = c.dim, G = c.block, H = c.target_dim, F = c.ff_dim, L = c.n_layers;
+  StepParams p{};
+  p.T = G;
+  p.pos = pos;
+  p.L = pos;  // context rows 0 .. pos-1; the block's own keys go to rows pos .. pos+G-1
+  p.anchor = anchor;
+  fm_status st;
+  const StepParams *sp = next_params(h, p, s, &st);
+  if (!sp) return st;
+
+  // block row 0 = tok_proj(E[anchor]) + block_pos[0]; rows 1.. are constants
+  GemvArgs a = gemv_base(h, h->w_tok, d, H, 1, sp);
+  a.amode = c.lm_format == FM_LM_Q8_0 ? A_ROW_Q8 : A_ROW_BF16;
+  a.tq = h->tq;
+  a.tscale = h->tsc;
+  a.tb = h->tb;
+  a.emode = E_STORE;
+  a.bias = h->block_pos;
+  a.Y = h->hinit;
+  a.ldy = d;
+  a.out_st = h->st_init;
+  TRY(run_gemv(h, a, s, "gemv.tok_proj", 1));
+
+  for (int l = 0; l < L; ++l) {
+    const bool first = l == 0;
+    Seg2 kv = h->kv(seq, l);
+    GemvArgs q = gemv_base(h, h->w_qkv[l], 3 * d, d, G, sp);
+    q.amode = A_RMS;
+    q.X = first ? h->hinit : h->X;
+    q.ldx = d;
+    q.st = first ? h->st_init : h->st_x;
+    q.st_tiles = d / kTile;
+    q.nw = h->attn_norm + (size_t)l * d;
+    q.inv_n = 1.0f / d;
+    q.emode = E_SEGS;
+    q.Y = h->qc;
+    q.ldy = d;
+    q.seg_rows = d;
+    q.n_segs = 3;
+    q.segs[0] = {SEG_F32, 0, 0, 0, nullptr, nullptr};
+    q.segs[1] = {SEG_CACHE, 0, 0, 0, nullptr, kv.k};
+    q.segs[2] = {SEG_CACHE, 0, 0, 0, nullptr, kv.v};
+    q.pos_src = 2;
+    q.pos_add = 0;
+    TRY(run_gemv(h, q, s, "gemv.qkv", G));
+
+    TRY(run_attn(h, h->qc, d, kv, G, 0, G, pos + G, sp, h->attn, s));
+
+    GemvArgs o = gemv_base(h, h->w_o[l], d, d, G, sp);
+    o.amode = A_PLAIN;
+    o.X = h->attn;
+    o.ldx = d;
+    o.emode = E_RESID;
+    o.R = first ? h->hinit : h->X;
+    o.ldr = d;
+    o.Y = h->X;
+    o.ldy = d;
+    o.out_st = h->st_x;
+    TRY(run_gemv(h, o, s, "gemv.o", G));
+
+    GemvArgs gu = gemv_base(h, h->w_gu[l], 2 * F, d, G, sp);
+    gu.amode = A_RMS;
+    gu.X = h->X;
+    gu.ldx = d;
+    gu.st = h->st_x;
+    gu.st_tiles = d / kTile;
+    gu.nw = h->ff_norm + (size_t)l * d;
+    gu.inv_n = 1.0f / d;
+    gu.emode = E_GEGLU;
+    gu.Y = h->u;
+    gu.ldy = F;
+    TRY(run_gemv(h, gu, s, "gemv.gate_up", G));
+
+    GemvArgs dn = gemv_base(h, h->w_down[l], d, F, G, sp);
+    dn.amode = A_PLAIN;
+    dn.X = h->u;
+    dn.ldx = F;
+    dn.emode = E_RESID;
+    dn.R = h->X;
+    dn.ldr = d;
+    dn.Y = h->X;
+    dn.ldy = d;
+    dn.out_st = h->st_x;
+    TRY(run_gemv(h, dn, s, "gemv.down", G));
+
+    if (h->debug & FM_DEBUG_KEEP_HIDDEN) {
+      CK(cudaMemcpyAsync(h->hid + (size_t)l * kMaxT * d, h->X, (size_t)G * d * 4, cudaMemcpyDeviceToDevice, s));
+    }
+  }
+  GemvArgs op = gemv_base(h, h->w_out, H, d, G, sp);
+  op.amode = A_RMS;
+  op.X = h->X;
+  op.ldx = d;
+  op.st = h->st_x;
+  op.st_tiles = d / kTile;
+  op.nw = h->out_norm;
+  op.inv_n = 1.0f / d;
+  op.emode = E_STORE;
+  op.Y = h->Y;
+  op.ldy = H;
+  TRY(run_gemv(h, op, s, "gemv.out_proj", G));
+  return run_lmhead(h, h->Y, G, sp, tokens, nullptr, s);
+}
+
+// ---------------------------------------------------------------- create
+
+fm_status check_config(fm_handle *h, const fm_config &c) {
+  if (c.variant != FM_VARIANT_FLASHMAP && c.variant != FM_VARIANT_DFLASH)
+    return fail(h, FM_ERR_INVALID_ARG, "unknown variant %d", c.variant);
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(h, FM_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c.n_heads < 1 || c.n_heads * c.head_dim != c.dim) return fail(h, FM_ERR_INVALID_ARG, "dim != n_heads * head_dim");
+  if (c.dim % kTile || c.ff_dim % kTile || c.dim < kTile)
+    return fail(h, FM_ERR_UNSUPPORTED, "dim and ff_dim must be multiples of 128");
+  if (c.target_dim % 64 || c.target_dim < 64) return fail(h, FM_ERR_UNSUPPORTED, "target_dim must be a multiple of 64");
+  if (c.n_taps < 1) return fail(h, FM_ERR_INVALID_ARG, "n_taps < 1");
+  if (c.n_layers < 1 || c.n_layers > kMaxSegs / 2)
+    return fail(h, FM_ERR_UNSUPPORTED, "n_layers must be in 1..%d", kMaxSegs / 2);
+  if (c.block < 1 || c.block > 16) return fail(h, FM_ERR_UNSUPPORTED, "block must be in 1..16");
+  if (c.vocab < 1) return fail(h, FM_ERR_INVALID_ARG, "vocab < 1");
+  if (c.lm_format != FM_LM_BF16 && c.lm_format != FM_LM_Q8_0) return fail(h, FM_ERR_INVALID_ARG, "lm_format");
+  if (c.max_seqs < 1) return fail(h, FM_ERR_INVALID_ARG, "max_seqs < 1");
+  if (c.max_ctx < c.block + 2) return fail(h, FM_ERR_INVALID_ARG, "max_ctx < block + 2");
+  if (c.target_dim + 32 > 16000) return fail(h, FM_ERR_UNSUPPORTED, "target_dim too large for the lm_head tile");
+  return FM_OK;
+}
+
+fm_status create_common(fm_handle *h, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int D = c.dim, Ht = c.target_dim, F = c.ff_dim;
+  h->length.assign(c.max_seqs, 0);
+  h->cache_plane = (size_t)c.n_heads * c.max_ctx * c.head_dim;
+  TRY(dalloc(h, &h->cache, (size_t)c.max_seqs * c.n_layers * 2 * h->cache_plane));
+  CK(cudaMemsetAsync(h->cache, 0, (size_t)c.max_seqs * c.n_layers * 2 * h->cache_plane * 2, s));
+  h->rope_pos = c.max_ctx + c.block + 2;
+  TRY(dalloc(h, &h->rope, (size_t)h->rope_pos * c.head_dim / 2));
+  CK(launch_rope_table(h->rope, h->rope_pos, c.head_dim, c.rope_theta, s));
+  const int wmax = 3 * D > F ? (3 * D > Ht ? 3 * D : Ht) : (F > Ht ? F : Ht);
+  TRY(dalloc(h, &h->X, (size_t)kMaxT * D));
+  TRY(dalloc(h, &h->qkv, (size_t)kMaxT * 3 * D));
+  TRY(dalloc(h, &h->qc, (size_t)kMaxT * D));
+  TRY(dalloc(h, &h->attn, (size_t)kMaxT * D));
+  TRY(dalloc(h, &h->u, (size_t)kMaxT * (F > wmax ? F : wmax)));
+  TRY(dalloc(h, &h->Y, (size_t)kMaxT * Ht));
+  TRY(dalloc(h, &h->ctx, (size_t)kMaxT * D));
+  TRY(dalloc(h, &h->actx, (size_t)kMaxT * D));
+  TRY(dalloc(h, &h->hid, (size_t)c.n_layers * kMaxT * D));
+  CK(cudaMemsetAsync(h->X, 0, (size_t)kMaxT * D * 4, s));
+  CK(cudaMemsetAsync(h->hid, 0, (size_t)c.n_layers * kMaxT * D * 4, s));
+  const int tiles_max = (wmax + kTile - 1) / kTile + 64;
+  float2 **sts[] = {&h->st_x, &h->st_h0, &h->st_c, &h->st_a, &h->st_u, &h->st_init};
+  for (float2 **p : sts) {
+    TRY(dalloc(h, p, (size_t)tiles_max * kMaxT));
+    CK(cudaMemsetAsync(*p, 0, (size_t)tiles_max * kMaxT * sizeof(float2), s));
+  }
+  h->max_splits = 2 * h->n_sm / c.n_heads;
+  if (h->max_splits < 1) h->max_splits = 1;
+  TRY(dalloc(h, &h->part_o, (size_t)c.n_heads * h->max_splits * kMaxT * c.head_dim));
+  TRY(dalloc(h, &h->part_ml, (size_t)c.n_heads * h->max_splits * kMaxT));
+  TRY(dalloc(h, &h->lm_part, (size_t)h->n_sm * kMaxT));
+  TRY(dalloc(h, &h->tickets, (size_t)2 * c.n_heads + 8));
+  CK(cudaMemsetAsync(h->tickets, 0, ((size_t)2 * c.n_heads + 8) * 4, s));
+  TRY(dalloc(h, &h->tok_tmp, (size_t)kMaxT));
+  TRY(dalloc(h, &h->sp_dev, kParamSlots));
+  CK(cudaMallocHost(&h->sp_host, sizeof(StepParams) * kParamSlots));
+  memset(h->sp_host, 0, sizeof(StepParams) * kParamSlots);
+  for (int i = 0; i < kParamSlots; ++i) CK(cudaEventCreateWithFlags(&h->sp_ev[i], cudaEventDisableTiming));
+  return FM_OK;
+}
+
+fm_status create_table(fm_handle *h, const TensorSet &ts, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int V = c.vocab, H = c.target_dim;
+  h->Vpad = (V + kTile - 1) / kTile * kTile;
+  if (c.lm_format == FM_LM_Q8_0) {
+    const fm_tensor *t;
+    TRY(find(h, ts, "token_embd.weight", (int64_t)V * (H / 32) * 34, FM_DTYPE_Q8_0, true, &t));
+    uint8_t *raw;
+    TRY(dalloc(h, &raw, (size_t)V * (H / 32) * 34));
+    CK(cudaMemcpyAsync(raw, t->data, (size_t)V * (H / 32) * 34, cudaMemcpyDefault, s));
+    TRY(dalloc(h, &h->tq, (size_t)h->Vpad * H));
+    TRY(dalloc(h, &h->tsc, (size_t)h->Vpad * (H / 32)));
+    CK(launch_q8_repack(raw, V, H, h->tq, h->tsc, h->Vpad, s));
+    CK(cudaStreamSynchronize(s));
+    CK(cudaFree(raw));
+    h->allocs.erase(std::find(h->allocs.begin(), h->allocs.end(), (void *)raw));
+    h->bytes -= (int64_t)V * (H / 32) * 34;
+  } else {
+    TRY(dalloc(h, &h->tb, (size_t)V * H));
+    TRY(put_bf16(h, ts, "token_embd.weight", h->tb, (int64_t)V * H, s));
+  }
+  return FM_OK;
+}
+
+fm_status create_flashmap(fm_handle *h, const TensorSet &ts, const float *modulation, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int D = c.dim, Ht = c.target_dim, F = c.ff_dim, L = c.n_layers, hd = c.head_dim;
+  const int FW = c.n_taps * Ht;
+  if (!modulation) return fail(h, FM_ERR_INVALID_ARG, "FlashMap needs the modulation table");
+  TRY(create_table(h, ts, s));
+  TRY(dalloc(h, &h->w_fc, (size_t)D * FW));
+  TRY(put_bf16(h, ts, "fc.weight", h->w_fc, (int64_t)D * FW, s));
+  TRY(dalloc(h, &h->w_hn, D));
+  TRY(put_bf16(h, ts, "hidden_norm.weight", h->w_hn, D, s));
+  TRY(dalloc(h, &h->w_ap, (size_t)D * Ht));
+  TRY(put_bf16(h, ts, "anchor_proj.weight", h->w_ap, (int64_t)D * Ht, s));
+  TRY(dalloc(h, &h->b_ap, D));
+  TRY(put_bf16(h, ts, "anchor_proj.bias", h->b_ap, D, s, true));
+  TRY(dalloc(h, &h->w_an, D));
+  TRY(put_bf16(h, ts, "anchor_norm.weight", h->w_an, D, s));
+  TRY(dalloc(h, &h->w_sn, Ht));
+  TRY(put_bf16(h, ts, "state_norm.weight", h->w_sn, Ht, s));
+  TRY(dalloc(h, &h->w_xe, (size_t)D * Ht));
+  TRY(put_bf16(h, ts, "x_embed.weight", h->w_xe, (int64_t)D * Ht, s));
+  TRY(dalloc(h, &h->b_xe, D));
+  TRY(put_bf16(h, ts, "x_embed.bias", h->b_xe, D, s, true));
+  TRY(dalloc(h, &h->w_head, (size_t)Ht * D));
+  TRY(put_bf16(h, ts, "head.weight", h->w_head, (int64_t)Ht * D, s));
+  TRY(dalloc(h, &h->b_head, Ht));
+  TRY(put_bf16(h, ts, "head.bias", h->b_head, Ht, s, true));
+  TRY(dalloc(h, &h->w_kvall, (size_t)L * 2 * D * D));
+  TRY(dalloc(h, &h->w_ckn, (size_t)L * hd));
+  const size_t DD = (size_t)D * D;
+  for (int l = 0; l < L; ++l) {
+    const std::string p = "layers." + std::to_string(l) + ".";
+    __nv_bfloat16 *w;
+    TRY(dalloc(h, &w, 3 * DD));
+    TRY(put_bf16(h, ts, p + "self_attn.q_proj.weight", w, DD, s));
+    TRY(put_bf16(h, ts, p + "self_attn.k_proj.weight", w + DD, DD, s));
+    TRY(put_bf16(h, ts, p + "self_attn.v_proj.weight", w + 2 * DD, DD, s));
+    h->w_qkv.push_back(w);
+    TRY(dalloc(h, &w, hd));
+    TRY(put_bf16(h, ts, p + "self_attn.q_norm.weight", w, hd, s));
+    h->w_sqn.push_back(w);
+    TRY(dalloc(h, &w, hd));
+    TRY(put_bf16(h, ts, p + "self_attn.k_norm.weight", w, hd, s));
+    h->w_skn.push_back(w);
+    TRY(dalloc(h, &w, DD));
+    TRY(put_bf16(h, ts, p + "self_attn.o_proj.weight", w, DD, s));
+    h->w_so.push_back(w);
+    TRY(dalloc(h, &w, DD));
+    TRY(put_bf16(h, ts, p + "cross_attn.q_proj.weight", w, DD, s));
+    h->w_cq.push_back(w);
+    TRY(put_bf16(h, ts, p + "cross_attn.k_proj.weight", h->w_kvall + (size_t)(2 * l) * DD, DD, s));
+    TRY(put_bf16(h, ts, p + "cross_attn.v_proj.weight", h->w_kvall + (size_t)(2 * l + 1) * DD, DD, s));
+    TRY(dalloc(h, &w, hd));
+    TRY(put_bf16(h, ts, p + "cross_attn.q_norm.weight", w, hd, s));
+    h->w_cqn.push_back(w);
+    TRY(put_bf16(h, ts, p + "cross_attn.k_norm.weight", h->w_ckn + (size_t)l * hd, hd, s));
+    TRY(dalloc(h, &w, DD));
+    TRY(put_bf16(h, ts, p + "cross_attn.o_proj.weight", w, DD, s));
+    h->w_co.push_back(w);
+    TRY(dalloc(h, &w, (size_t)F * D));
+    TRY(put_bf16(h, ts, p + "mlp.fc1.weight", w, (int64_t)F * D, s));
+    h->w_f1.push_back(w);
+    TRY(dalloc(h, &w, F));
+    TRY(put_bf16(h, ts, p + "mlp.fc1.bias", w, F, s, true));
+    h->b_f1.push_back(w);
+    TRY(dalloc(h, &w, (size_t)D * F));
+    TRY(put_bf16(h, ts, p + "mlp.fc2.weight", w, (int64_t)D * F, s));
+    h->w_f2.push_back(w);
+    TRY(dalloc(h, &w, D));
+    TRY(put_bf16(h, ts, p + "mlp.fc2.bias", w, D, s, true));
+    h->b_f2.push_back(w);
+  }
+  const size_t nmod = (size_t)(3 * L + 1) * 3 * D;
+  TRY(dalloc(h, &h->mod, nmod));
+  CK(cudaMemcpyAsync(h->mod, modulation, nmod * 4, cudaMemcpyDefault, s));
+  TRY(create_common(h, s));
+
+  // h0 = x_embed(state_norm(mean row of E)) + bias, and its row statistics
+  TRY(dalloc(h, &h->h0, D));
+  TRY(dalloc(h, &h->uni, Ht));
+  if (c.lm_format == FM_LM_Q8_0)
+    CK(launch_colmean_q8(h->tq, h->tsc, c.vocab, Ht, h->uni, s));
+  else
+    CK(launch_colmean_bf16(h->tb, c.vocab, Ht, h->uni, s));
+  CK(launch_row_stats(h->uni, 1, Ht, h->st_u, s));
+  StepParams p{};
+  p.T = 1;
+  fm_status st;
+  const StepParams *sp = next_params(h, p, s, &st);
+  if (!sp) return st;
+  GemvArgs a = gemv_base(h, h->w_xe, D, Ht, 1, sp);
+  a.amode = A_RMS;
+  a.X = h->uni;
+  a.ldx = Ht;
+  a.st = h->st_u;
+  a.st_tiles = (Ht + kTile - 1) / kTile;
+  a.nw = h->w_sn;
+  a.inv_n = 1.0f / Ht;
+  a.emode = E_STORE;
+  a.bias = h->b_xe;
+  a.Y = h->h0;
+  a.ldy = D;
+  a.out_st = h->st_h0;
+  CK(launch_gemv(a, (D + kTile - 1) / kTile, s, false));
+  return FM_OK;
+}
+
+fm_status create_dflash(fm_handle *h, const TensorSet &ts, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int d = c.dim, H = c.target_dim, F = c.ff_dim, L = c.n_layers, G = c.block;
+  const int mH = c.n_taps * H;
+  TRY(create_table(h, ts, s));
+  size_t tmp_elems = (size_t)mH * d;
+  if ((size_t)d * F > tmp_elems) tmp_elems = (size_t)d * F;
+  if ((size_t)H * d > tmp_elems) tmp_elems = (size_t)H * d;
+  __nv_bfloat16 *tmp, *tmp2;
+  TRY(dalloc(h, &tmp, tmp_elems));
+  TRY(dalloc(h, &tmp2, (size_t)d * F));
+  const size_t dd = (size_t)d * d;
+  TRY(dalloc(h, &h->attn_norm, (size_t)L * d));
+  TRY(dalloc(h, &h->ff_norm, (size_t)L * d));
+  TRY(dalloc(h, &h->w_kvall, (size_t)L * 2 * dd));
+  for (int l = 0; l < L; ++l) {
+    const std::string p = "bb." + std::to_string(l) + ".";
+    TRY(put_bf16(h, ts, p + "attn_norm", h->attn_norm + (size_t)l * d, d, s));
+    TRY(put_bf16(h, ts, p + "ff_norm", h->ff_norm + (size_t)l * d, d, s));
+    __nv_bfloat16 *w;
+    TRY(dalloc(h, &w, 3 * dd));
+    TRY(put_bf16_t(h, ts, p + "q", d, d, w, d, tmp, s));
+    TRY(put_bf16_t(h, ts, p + "k", d, d, w + dd, d, tmp, s));
+    TRY(put_bf16_t(h, ts, p + "v", d, d, w + 2 * dd, d, tmp, s));
+    CK(cudaMemcpyAsync(h->w_kvall + (size_t)(2 * l) * dd, w + dd, 2 * dd * 2, cudaMemcpyDeviceToDevice, s));
+    h->w_qkv.push_back(w);
+    TRY(dalloc(h, &w, dd));
+    TRY(put_bf16_t(h, ts, p + "o", d, d, w, d, tmp, s));
+    h->w_o.push_back(w);
+    // gate / up interleaved per 64 features: tile j = gate rows 64j.. then up rows 64j..
+    TRY(dalloc(h, &w, (size_t)2 * F * d));
+    TRY(put_bf16_t(h, ts, p + "gate", d, F, tmp2, d, tmp, s));
+    for (int j = 0; j < F / 64; ++j)
+      CK(cudaMemcpyAsync(w + (size_t)(128 * j) * d, tmp2 + (size_t)(64 * j) * d, (size_t)64 * d * 2,
+                         cudaMemcpyDeviceToDevice, s));
+    TRY(put_bf16_t(h, ts, p + "up", d, F, tmp2, d, tmp, s));
+    for (int j = 0; j < F / 64; ++j)
+      CK(cudaMemcpyAsync(w + (size_t)(128 * j + 64) * d, tmp2 + (size_t)(64 * j) * d, (size_t)64 * d * 2,
+                         cudaMemcpyDeviceToDevice, s));
+    h->w_gu.push_back(w);
+    TRY(dalloc(h, &w, (size_t)d * F));
+    TRY(put_bf16_t(h, ts, p + "down", F, d, w, F, tmp, s));
+    h->w_down.push_back(w);
+  }
+  TRY(dalloc(h, &h->w_c, (size_t)d * mH));
+  TRY(put_bf16_t(h, ts, "W_c", mH, d, h->w_c, mH, tmp, s));
+  TRY(dalloc(h, &h->ctx_norm, d));
+  TRY(put_bf16(h, ts, "ctx_norm", h->ctx_norm, d, s));
+  TRY(dalloc(h, &h->w_tok, (size_t)d * H));
+  TRY(put_bf16_t(h, ts, "tok_proj", H, d, h->w_tok, H, tmp, s));
+  __nv_bfloat16 *mask_emb;
+  TRY(dalloc(h, &mask_emb, (size_t)(G > 1 ? G - 1 : 1) * d));
+  if (G > 1) TRY(put_bf16(h, ts, "mask_emb", mask_emb, (int64_t)(G - 1) * d, s));
+  TRY(dalloc(h, &h->block_pos, (size_t)G * d));
+  TRY(put_bf16(h, ts, "block_pos", h->block_pos, (int64_t)G * d, s));
+  TRY(dalloc(h, &h->out_norm, d));
+  TRY(put_bf16(h, ts, "out_norm", h->out_norm, d, s));
+  TRY(dalloc(h, &h->w_out, (size_t)H * d));
+  TRY(put_bf16_t(h, ts, "out_proj", d, H, h->w_out, d, tmp, s));
+  TRY(create_common(h, s));
+  TRY(dalloc(h, &h->hinit, (size_t)kMaxT * d));
+  CK(cudaMemsetAsync(h->hinit, 0, (size_t)kMaxT * d * 4, s));
+  CK(launch_block_consts(mask_emb, h->block_pos, G, d, h->hinit, h->st_init, s));
+  CK(cudaStreamSynchronize(s));
+  return FM_OK;
+}
+
+fm_status check_seq(fm_handle *h, int32_t seq) {
+  if (seq < 0 || seq >= h->cfg.max_seqs) return fail(h, FM_ERR_INVALID_ARG, "seq %d outside [0, %d)", seq, h->cfg.max_seqs);
+  return FM_OK;
+}
+
+fm_status append_checks(fm_handle *h, int32_t seq, const float *feats, int32_t n, int32_t start) {
+  TRY(check_seq(h, seq));
+  if (n < 0) return fail(h, FM_ERR_INVALID_ARG, "n_rows < 0");
+  if (n > 0 && !feats) return fail(h, FM_ERR_INVALID_ARG, "null feature rows");
+  if (n > 0 && (reinterpret_cast<uintptr_t>(feats) & 15)) return fail(h, FM_ERR_INVALID_ARG, "feature rows not 16-byte aligned");
+  if (start < 0 || start > h->length[seq])
+    return fail(h, FM_ERR_STATE, "start %d outside [0, length %d]", start, h->length[seq]);
+  if ((int64_t)start + n + h->cfg.block + 1 > h->cfg.max_ctx)
+    return fail(h, FM_ERR_CONTEXT_FULL, "context full: %d + %d + %d + 1 > %d", start, n, h->cfg.block, h->cfg.max_ctx);
+  return FM_OK;
+}
+
+fm_status append_one(fm_handle *h, int32_t seq, const float *feats, int32_t n, int32_t start, cudaStream_t s) {
+  const int FW = h->cfg.n_taps * h->cfg.target_dim;
+  for (int r0 = 0; r0 < n; r0 += kMaxT) {
+    const int rows = n - r0 < kMaxT ? n - r0 : kMaxT;
+    StepParams p{};
+    p.T = rows;
+    p.start = start + r0;
+    p.feats = feats + (size_t)r0 * FW;
+    fm_status st;
+    const StepParams *sp = next_params(h, p, s, &st);
+    if (!sp) return st;
+    if (h->cfg.variant == FM_VARIANT_FLASHMAP)
+      TRY(flashmap_append_rows(h, seq, sp, rows, s));
+    else
+      TRY(dflash_append_rows(h, seq, sp, s));
+  }
+  h->length[seq] = start + n;
+  return FM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fm_status fm_create(const fm_config *cfg, const fm_tensor *weights, int32_t n_weights, const float *modulation,
+                    void *stream, fm_handle **out) {
+  if (!out) return FM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || (!weights && n_weights > 0) || n_weights < 0) return FM_ERR_INVALID_ARG;
+  fm_handle *h = new (std::nothrow) fm_handle();
+  if (!h) return FM_ERR_OOM;
+  h->cfg = *cfg;
+  fm_status st = check_config(h, *cfg);
+  if (st != FM_OK) {
+    g_create_error = h->err;
+    fm_destroy(h);
+    return st;
+  }
+  cudaGetDevice(&h->dev);
+  cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->dev);
+  TensorSet ts;
+  for (int i = 0; i < n_weights; ++i) {
+    if (!weights[i].name) {
+      fm_destroy(h);
+      return FM_ERR_INVALID_ARG;
+    }
+    ts.by_name[weights[i].name] = &weights[i];
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = cfg->variant == FM_VARIANT_FLASHMAP ? create_flashmap(h, ts, modulation, s) : create_dflash(h, ts, s);
+  if (st == FM_OK) {
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) st = fail(h, FM_ERR_CUDA, "create: %s", cudaGetErrorString(e));
+  }
+  if (st != FM_OK) {
+    g_create_error = h->err;
+    fm_destroy(h);
+    return st;
+  }
+  g_create_error.clear();
+  *out = h;
+  return FM_OK;
+}
+
+fm_status fm_context_append(fm_handle *h, int32_t seq, const float *feats, int32_t n_rows, int32_t start_pos,
+                            void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  TRY(append_checks(h, seq, feats, n_rows, start_pos));
+  return append_one(h, seq, feats, n_rows, start_pos, static_cast<cudaStream_t>(stream));
+}
+
+fm_status fm_context_append_batched(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const float *feats,
+                                    const int32_t *n_rows, const int32_t *start, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  if (n_seqs < 1 || n_seqs > h->cfg.max_seqs || !seq_ids || !n_rows || !start)
+    return fail(h, FM_ERR_INVALID_ARG, "bad batched append arguments");
+  std::vector<char> seen(h->cfg.max_seqs, 0);
+  size_t off = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    TRY(append_checks(h, seq_ids[i], feats ? feats + off : nullptr, n_rows[i], start[i]));
+    if (seen[seq_ids[i]]) return fail(h, FM_ERR_INVALID_ARG, "repeated seq id %d", seq_ids[i]);
+    seen[seq_ids[i]] = 1;
+    off += (size_t)n_rows[i] * h->cfg.n_taps * h->cfg.target_dim;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  off = 0;
+  int total = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    const int launches = h->last_launches;
+    TRY(append_one(h, seq_ids[i], feats + off, n_rows[i], start[i], s));
+    total = h->last_launches;
+    (void)launches;
+    off += (size_t)n_rows[i] * h->cfg.n_taps * h->cfg.target_dim;
+  }
+  h->last_launches = total;
+  return FM_OK;
+}
+
+fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const int32_t *anchors, const int32_t *pos,
+                   int32_t *tokens, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  if (n_seqs < 1 || n_seqs > h->cfg.max_seqs || !seq_ids || !anchors || !pos || !tokens)
+    return fail(h, FM_ERR_INVALID_ARG, "bad draft arguments");
+  std::vector<char> seen(h->cfg.max_seqs, 0);
+  for (int i = 0; i < n_seqs; ++i) {
+    TRY(check_seq(h, seq_ids[i]));
+    if (seen[seq_ids[i]]) return fail(h, FM_ERR_INVALID_ARG, "repeated seq id %d", seq_ids[i]);
+    seen[seq_ids[i]] = 1;
+    if (anchors[i] < 0 || anchors[i] >= h->cfg.vocab)
+      return fail(h, FM_ERR_INVALID_ARG, "anchor %d outside [0, %d)", anchors[i], h->cfg.vocab);
+    if (pos[i] != h->length[seq_ids[i]])
+      return fail(h, FM_ERR_STATE, "pos %d != length %d", pos[i], h->length[seq_ids[i]]);
+    if ((int64_t)pos[i] + h->cfg.block + 1 > h->cfg.max_ctx)
+      return fail(h, FM_ERR_CONTEXT_FULL, "context full at pos %d", pos[i]);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < n_seqs; ++i) {
+    int32_t *tk = tokens + (size_t)i * h->cfg.block;
+    if (h->cfg.variant == FM_VARIANT_FLASHMAP)
+      TRY(flashmap_draft_one(h, seq_ids[i], anchors[i], pos[i], tk, s));
+    else
+      TRY(dflash_draft_one(h, seq_ids[i], anchors[i], pos[i], tk, s));
+  }
+  return FM_OK;
+}
+
+fm_status fm_accept(const int32_t *draft, const int32_t *target, int32_t k, int32_t *n_accepted, int32_t *bonus) {
+  if (!draft || !target || !n_accepted || !bonus || k < 0) return FM_ERR_INVALID_ARG;
+  int32_t a = 0;
+  while (a < k && draft[a] == target[a]) ++a;
+  *n_accepted = a;
+  *bonus = target[a];
+  return FM_OK;
+}
+
+fm_status fm_accept_batched(fm_handle *h, int32_t n_seqs, const int32_t *draft, const int32_t *target,
+                            const int32_t *k, int32_t *acc, int32_t *bonus, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  if (n_seqs < 1 || !draft || !target || !k || !acc || !bonus) return fail(h, FM_ERR_INVALID_ARG, "bad accept arguments");
+  CK(launch_accept(n_seqs, h->cfg.block, draft, target, k, acc, bonus, static_cast<cudaStream_t>(stream)));
+  return FM_OK;
+}
+
+fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, int64_t offset, void *dst,
+                        int64_t nbytes, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  if (!dst || nbytes < 0 || offset < 0) return fail(h, FM_ERR_INVALID_ARG, "bad debug copy arguments");
+  const fm_config &c = h->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void *src = nullptr;
+  int64_t size = 0;
+  switch (what) {
+    case FM_DEBUG_HIDDEN:
+      if (index < 0 || index >= c.n_layers) return fail(h, FM_ERR_INVALID_ARG, "layer %d", index);
+      src = h->hid + (size_t)index * kMaxT * c.dim;
+      size = (int64_t)c.block * c.dim * 4;
+      break;
+    case FM_DEBUG_HEAD_OUT:
+      src = h->Y;
+      size = (int64_t)c.block * c.target_dim * 4;
+      break;
+    case FM_DEBUG_LOGITS: {
+      if (!h->dbg_logits) TRY(dalloc(h, &h->dbg_logits, (size_t)kMaxT * c.vocab));
+      StepParams p{};
+      p.T = c.block;
+      fm_status st;
+      const StepParams *sp = next_params(h, p, s, &st);
+      if (!sp) return st;
+      TRY(run_lmhead(h, h->Y, c.block, sp, h->tok_tmp, h->dbg_logits, s));
+      src = h->dbg_logits;
+      size = (int64_t)c.block * c.vocab * 4;
+      break;
+    }
+    case FM_DEBUG_CACHE_K:
+    case FM_DEBUG_CACHE_V: {
+      TRY(check_seq(h, seq));
+      if (index < 0 || index >= c.n_layers) return fail(h, FM_ERR_INVALID_ARG, "layer %d", index);
+      Seg2 kv = h->kv(seq, index);
+      src = what == FM_DEBUG_CACHE_K ? kv.k : kv.v;
+      size = (int64_t)h->cache_plane * 2;
+      break;
+    }
+    case FM_DEBUG_H0:
+      if (!h->h0) return fail(h, FM_ERR_INVALID_ARG, "no h0 for this variant");
+      src = h->h0;
+      size = (int64_t)c.dim * 4;
+      break;
+    default:
+      return fail(h, FM_ERR_INVALID_ARG, "unknown debug selector %d", what);
+  }
+  if (offset + nbytes > size) return fail(h, FM_ERR_INVALID_ARG, "range beyond the buffer (%lld bytes)", (long long)size);
+  CK(cudaMemcpyAsync(dst, static_cast<const char *>(src) + offset, nbytes, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  return FM_OK;
+}
+
+fm_status fm_set_debug(fm_handle *h, int32_t flags) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->debug = flags;
+  return FM_OK;
+}
+
+fm_status fm_profile_read(fm_handle *h, fm_kernel_time *out, int32_t cap, int32_t *n) {
+  if (!h || !n || cap < 0 || (cap > 0 && !out)) return FM_ERR_INVALID_ARG;
+  std::vector<fm_kernel_time> agg;
+  for (ProfRec &r : h->prof) {
+    CK(cudaEventSynchronize(r.e1));
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, r.e0, r.e1));
+    fm_kernel_time *k = nullptr;
+    for (auto &a : agg)
+      if (r.name == a.name) k = &a;
+    if (!k) {
+      agg.emplace_back();
+      k = &agg.back();
+      memset(k, 0, sizeof *k);
+      snprintf(k->name, sizeof k->name, "%s", r.name.c_str());
+    }
+    k->launches += 1;
+    k->ms += ms;
+    k->bytes += r.bytes;
+    h->ev_pool.push_back(r.e0);
+    h->ev_pool.push_back(r.e1);
+  }
+  h->prof.clear();
+  *n = (int32_t)agg.size();
+  for (int i = 0; i < (int)agg.size() && i < cap; ++i) out[i] = agg[i];
+  return FM_OK;
+}
+
+fm_status fm_get_length(const fm_handle *h, int32_t seq, int32_t *length) {
+  if (!h || !length || seq < 0 || seq >= h->cfg.max_seqs) return FM_ERR_INVALID_ARG;
+  *length = h->length[seq];
+  return FM_OK;
+}
+
+fm_status fm_memory_bytes(const fm_handle *h, int64_t *bytes) {
+  if (!h || !bytes) return FM_ERR_INVALID_ARG;
+  *bytes = h->bytes;
+  return FM_OK;
+}
+
+fm_status fm_last_launch_count(const fm_handle *h, int32_t *count) {
+  if (!h || !count) return FM_ERR_INVALID_ARG;
+  *count = h->last_launches;
+  return FM_OK;
+}
+
+const char *fm_status_str(fm_status s) {
+  switch (s) {
+    case FM_OK: return "ok";
+    case FM_ERR_INVALID_ARG: return "invalid argument";
+    case FM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FM_ERR_OOM: return "out of memory";
+    case FM_ERR_CONTEXT_FULL: return "context full";
+    case FM_ERR_STATE: return "bad sequence state";
+    case FM_ERR_CUDA: return "CUDA error";
+    case FM_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+// With a null handle: the reason the last fm_create on this thread failed.
+const char *fm_last_error(const fm_handle *h) { return h ? h->err.c_str() : g_create_error.c_str(); }
+
+void fm_destroy(fm_handle *h) {
+  if (!h) return;
+  for (void *p : h->allocs) cudaFree(p);
+  if (h->sp_host) cudaFreeHost(h->sp_host);
+  for (int i = 0; i < kParamSlots; ++i)
+    if (h->sp_ev[i]) cudaEventDestroy(h->sp_ev[i]);
+  for (ProfRec &r : h->prof) {
+    cudaEventDestroy(r.e0);
+    cudaEventDestroy(r.e1);
+  }
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+  delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+// fm_internal.h -- kernel argument blocks and launcher declarations shared by
+// the host runtime (fm_api.cu) and the kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace fm {
+
+constexpr int kMaxT = 32;        // rows a skinny GEMV carries (two m16 MMA tiles)
+constexpr int kTile = 128;       // output rows per GEMV tile (one 128-wide head)
+constexpr int kMaxSegs = 16;     // row segments a GEMV epilogue distinguishes
+
+// Device-resident per-call values.  The host fills one slot before each call
+// so that launches (and captured graphs) stay fixed while positions move.
+struct StepParams {
+  int32_t T;        // rows in this chain: draft = block, append = n_rows
+  int32_t pos;      // draft: the anchor's position
+  int32_t L;        // cross-attention keys
+  int32_t anchor;   // draft: anchor token id
+  int32_t start;    // append: first position
+  int32_t pad0, pad1, pad2;
+  const float *feats;  // append: feature rows [T][feat_dim]
+};
+
+// --- skinny GEMV: Y[t][m] = sum_k A[t][k] W[m][k] for t < T <= 32 ----------
+enum AMode : int32_t {
+  A_PLAIN = 0,     // A = X
+  A_RMS = 1,       // A = X * w[k] * rsqrt(mean(x^2) + eps)         (RMSNorm)
+  A_LNMOD = 2,     // A = (X - mu) * rstd * (1 + scale[k]) + shift[k] (adaLN)
+  A_ROW_Q8 = 3,    // A row 0 = dequantised table row sp->anchor (Q8_0)
+  A_ROW_BF16 = 4,  // A row 0 = table row sp->anchor (bf16)
+  A_RMS2 = 5,      // A = RMSNorm(RMSNorm(X; nw); nw2): stats are (sum x^2, sum (x nw)^2)
+};
+
+enum SegKind : int32_t {
+  SEG_F32 = 0,     // store f32 rows into Y (optionally head RMSNorm + RoPE)
+  SEG_CACHE = 1,   // store f16 into a head-major cache [H][max_ctx][hd] (optionally norm + RoPE)
+};
+
+enum EMode : int32_t {
+  E_STORE = 0,     // Y = y + b (out stats optional)
+  E_GELU = 1,      // Y = gelu_erf(y + b)
+  E_RESID = 2,     // Y = R + gate * (y + b)  (gate null -> 1), out stats
+  E_SEGS = 3,      // per-segment f32 / cache stores with per-head RMSNorm + RoPE
+  E_GEGLU = 4,     // tile = 64 gate rows + 64 up rows: Y[f] = gelu_tanh(g) * u
+};
+
+struct SegDesc {
+  int32_t kind;                 // SegKind
+  int32_t y_col;                // SEG_F32: column offset of the segment in Y
+  int32_t rope;                 // apply RoPE after the norm
+  int32_t pad;
+  const __nv_bfloat16 *norm_w;  // per-head RMSNorm weight [hd] (null = none)
+  __half *cache;                // SEG_CACHE: [n_heads][max_ctx][hd]
+};
+
+struct GemvArgs {
+  const __nv_bfloat16 *W;  // [M][K] row-major, bf16
+  int32_t M, K, Kc, Kp;    // rows, cols, cols per CTA, cols per staged A piece
+  int32_t ksplit;          // CTAs (one cluster) sharing a row tile
+  int32_t T_const;         // > 0: fixed T, else sp->T
+  const StepParams *sp;
+
+  // prologue
+  int32_t amode;
+  const float *X;          // input rows X[t * ldx + k] (ldx 0 = one row broadcast)
+  int32_t ldx;
+  int32_t x_from_sp;       // X = sp->feats
+  const float2 *st;        // input row stats: st[i * kMaxT + t] = (sum, sumsq), i < st_tiles
+  int32_t st_tiles;
+  int32_t st_bcast;        // stats of row 0 serve every row
+  const __nv_bfloat16 *nw; // RMS weight (A_RMS, first weight of A_RMS2)
+  const __nv_bfloat16 *nw2;// A_RMS2 second weight; + (m0 / nw_rows) * K for per-layer weights
+  int32_t nw_rows;         // rows sharing one second norm weight (0 = one weight for all)
+  const float *sc, *sh;    // A_LNMOD scale / shift [K]
+  float eps, inv_n;
+  const int8_t *tq;        // A_ROW_Q8: int8 plane [V][K]
+  const __half *tscale;    // A_ROW_Q8: scales [V / 128][K / 32][128]
+  const __nv_bfloat16 *tb; // A_ROW_BF16: rows [V][K]
+
+  // epilogue
+  int32_t emode;
+  const __nv_bfloat16 *bias;  // [M] or null
+  float *Y;
+  int32_t ldy;
+  float2 *out_st;             // [M / 128][kMaxT] (sum, sumsq) of the stored rows, or null
+  const __nv_bfloat16 *st_w;  // if set, out_st holds (sum v^2, sum (v st_w)^2) instead
+  const float *gate;          // E_RESID gate [M] (null = 1)
+  const float *R;             // E_RESID residual source R[t * ldr + m]
+  int32_t ldr;
+  // E_SEGS
+  int32_t seg_rows, n_segs, hd, max_ctx;
+  int32_t pos_src;            // 0: sp->pos, 1: sp->start, 2: sp->L
+  int32_t pos_add;            // position of row t = base + pos_add + t
+  const float2 *rope;         // [positions][hd / 2] (cos, sin)
+  float qk_eps;
+  SegDesc segs[kMaxSegs];
+  // self-attention handoff: after the q/k/v segments of a head are stored, the
+  // last CTA to finish one computes that head's attention over the T rows.
+  int32_t *tickets;           // [n_heads] zero-initialised, self-resetting
+  float *attn_out;            // [T][D]
+  int32_t self_D;             // width of one of q / k / v (0 = no attention tail)
+  float attn_scale;
+};
+
+// --- flash-decode cross attention over a head-major f16 cache --------------
+struct AttnArgs {
+  const float *Q;          // [T][ldq] f32 queries (head h at column h * hd)
+  int32_t ldq;
+  const __half *Kc, *Vc;   // [n_heads][max_ctx][hd]
+  int32_t max_ctx, n_heads, hd;
+  int32_t splits;          // CTAs per head
+  int32_t T_const;
+  int32_t L_src;           // 0: sp->L, 1: sp->pos + 1 (FlashMap keys 0..pos)
+  int32_t L_add;
+  const StepParams *sp;
+  float scale_log2;        // log2(e) / sqrt(hd)
+  float *part_o;           // [n_heads][splits][kMaxT][hd]
+  float2 *part_ml;         // [n_heads][splits][kMaxT] (max (log2 domain), sum)
+  int32_t *tickets;        // [n_heads]
+  float *out;              // [T][ldo]
+  int32_t ldo;
+};
+
+// --- lm_head GEMV fused with the per-row argmax -----------------------------
+struct LmArgs {
+  const int8_t *q8;          // Q8_0 int8 plane [Vpad][H]
+  const __half *q8s;         // scales [Vpad / 128][H / 32][128]
+  const __nv_bfloat16 *wb;   // bf16 table [V][H]
+  int32_t V, H;
+  int32_t T_const;
+  const StepParams *sp;
+  const float *Y;            // [T][H]
+  int32_t ldy;
+  float2 *part;              // [gridDim.x][kMaxT] (value, index-as-float bits)
+  int32_t *ticket;           // [1]
+  int32_t *tokens;           // [T]
+  float *logits;             // optional [T][V] store (debug), null in the hot path
+};
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t s, bool pdl);
+size_t gemv_smem_bytes(const GemvArgs &a, int mt);
+cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s, bool pdl);
+cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t s, bool pdl);
+int lmhead_grid(const LmArgs &a, int n_sm);
+
+// set-up and small kernels
+cudaError_t launch_q8_repack(const uint8_t *raw, int32_t V, int32_t H, int8_t *q, __half *scales,
+                             int32_t Vpad, cudaStream_t s);
+cudaError_t launch_colmean_q8(const int8_t *q, const __half *scales, int32_t V, int32_t H, float *out,
+                              cudaStream_t s);
+cudaError_t launch_colmean_bf16(const __nv_bfloat16 *w, int32_t V, int32_t H, float *out, cudaStream_t s);
+cudaError_t launch_rope_table(float2 *tab, int32_t n_pos, int32_t hd, float theta, cudaStream_t s);
+cudaError_t launch_transpose_bf16(const __nv_bfloat16 *in, int32_t rows, int32_t cols, __nv_bfloat16 *out,
+                                  int32_t ldo, cudaStream_t s);
+cudaError_t launch_block_consts(const __nv_bfloat16 *mask_emb, const __nv_bfloat16 *block_pos, int32_t gamma,
+                                int32_t d, float *out, float2 *st, cudaStream_t s);
+cudaError_t launch_row_stats(const float *x, int32_t rows, int32_t d, float2 *st, cudaStream_t s);
+cudaError_t launch_accept(int32_t n, int32_t block, const int32_t *draft, const int32_t *target,
+                          const int32_t *k, int32_t *acc, int32_t *bonus, cudaStream_t s);
+cudaError_t launch_fill_f32(float *p, size_t n, float v, cudaStream_t s);
+
+}  // namespace fm

@@ -1,0 +1,504 @@
+// k_gemv.cu -- the skinny weight-streaming GEMV of the drafter:
+//   Y[t][m] = sum_k A[t][k] W[m][k],  t < T <= 32,  W bf16 [M][K] row-major.
+//
+// The pages run this product as gemvT17 / gemmBf16 in WGSL (flashmap_drafter.js,
+// ``gemvT``: one weight read, token sums in registers).  On sm_103a:
+//   * weights stream once from HBM through a cp.async ring of 128 x 64 tiles;
+//     the first stages are issued before griddepcontrol.wait, so a kernel's
+//     weights are in flight while its predecessor is still finishing;
+//   * the activations are transformed on the way in (RMSNorm, adaLN LayerNorm
+//     modulate, a table row) and split into bf16 hi + lo, so the bf16 tensor
+//     cores see f32-accurate operands: A*W = hi*W + lo*W, f32 accumulate;
+//   * the T rows are the MMA's M side (m16 tiles), 8 weight rows its N side;
+//     K is permuted inside each 64-wide chunk so that one 128-bit shared load
+//     gives a thread its fragments for four k16 steps;
+//   * split-K across a thread-block cluster; the partial tiles are summed
+//     through distributed shared memory in a fixed order (deterministic);
+//   * fused epilogues: bias, exact GELU, gated residual + row statistics for
+//     the next norm, per-head RMSNorm + interleaved-pair RoPE, f16 cache store,
+//     gated GELU(tanh) FFN, and the block self-attention tail.
+#include <cooperative_groups.h>
+
+#include "dev_common.cuh"
+#include "fm_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace fm {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kChunk = 64;                       // k per pipeline stage
+constexpr int kStageBytes = kTile * kChunk * 2;  // 16 KB of bf16 weights
+constexpr int kCsStride = kTile + 8;             // f32 partial tile row stride
+
+__host__ __device__ constexpr int a_stride(int kp) { return kp + 32; }  // bf16 elements; 64-byte pad
+
+struct Smem {
+  uint32_t ring, ahi, alo, cs;  // shared-space byte addresses
+  float *cs_ptr;
+  float *stat_mu, *stat_rs;     // [kMaxT]
+};
+
+// weight tile: row r (0..127) of chunk, 16-byte unit u (0..7) -> swizzled slot
+__device__ __forceinline__ uint32_t wslot(int r, int u) { return r * 128 + ((u ^ ((r & 1) << 2)) << 4); }
+
+__device__ __forceinline__ void issue_chunk(const GemvArgs &a, uint32_t ring, int stage, int m0, int k) {
+  const uint32_t base = ring + stage * kStageBytes;
+  // 1024 16-byte pieces: row = i / 8, unit = i % 8
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = threadIdx.x + j * kThreads;
+    const int r = i >> 3, u = i & 7;
+    const int m = m0 + r;
+    const bool ok = m < a.M;
+    const __nv_bfloat16 *src = a.W + (size_t)(ok ? m : 0) * a.K + k + u * 8;
+    cp_async16(base + wslot(r, u), src, ok ? 16u : 0u);
+  }
+}
+
+// Row statistics of the input rows (sum over the producer's tiles, in double).
+__device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
+  const int t = threadIdx.x;
+  if (t < kMaxT) {
+    float m = 0.f, r = 1.f;
+    if (t < T && (a.amode == A_RMS || a.amode == A_LNMOD || a.amode == A_RMS2)) {
+      const int ts = a.st_bcast ? 0 : t;
+      double s1 = 0.0, s2 = 0.0;
+      for (int i = 0; i < a.st_tiles; ++i) {
+        const float2 v = __ldcg(a.st + i * kMaxT + ts);
+        s1 += v.x;
+        s2 += v.y;
+      }
+      if (a.amode == A_RMS) {
+        r = (float)(1.0 / sqrt(s2 * a.inv_n + (double)a.eps));
+      } else if (a.amode == A_RMS2) {
+        const double r1 = 1.0 / sqrt(s1 * a.inv_n + (double)a.eps);
+        const double r2 = 1.0 / sqrt(r1 * r1 * s2 * a.inv_n + (double)a.eps);
+        m = (float)r1;   // A_RMS2 keeps r1 in the mean slot
+        r = (float)r2;
+      } else {
+        const double mean = s1 * a.inv_n;
+        double var = s2 * a.inv_n - mean * mean;
+        if (var < 0.0) var = 0.0;
+        m = (float)mean;
+        r = (float)(1.0 / sqrt(var + (double)a.eps));
+      }
+    }
+    mu[t] = m;
+    rs[t] = r;
+  }
+}
+
+// Stage A[t][k0 .. k0 + kp) for all 16 * MT rows as bf16 hi / lo.
+template <int MT>
+__device__ void stage_a(const GemvArgs &a, const Smem &s, int T, int m0, int k0, int kp) {
+  const int rows = 16 * MT;
+  const int lda = a_stride(a.Kp);
+  const int quads = kp >> 2;
+  const float *X = a.x_from_sp ? a.sp->feats : a.X;
+  const __nv_bfloat16 *nw = a.nw;
+  const __nv_bfloat16 *nw2 = a.nw2;
+  if (a.amode == A_RMS2 && a.nw_rows > 0) nw2 += (size_t)(m0 / a.nw_rows) * a.K;
+  for (int i = threadIdx.x; i < rows * quads; i += kThreads) {
+    const int t = i / quads, kq = (i - t * quads) * 4;
+    const int k = k0 + kq;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (t < T) {
+      if (a.amode == A_ROW_Q8 || a.amode == A_ROW_BF16) {
+        if (t == 0) {
+          const int r = a.sp->anchor;
+          if (a.amode == A_ROW_Q8) {
+            const char4 q = *reinterpret_cast<const char4 *>(a.tq + (size_t)r * a.K + k);
+            const float d = __half2float(a.tscale[((size_t)(r >> 7) * (a.K >> 5) + (k >> 5)) * 128 + (r & 127)]);
+            v[0] = d * q.x; v[1] = d * q.y; v[2] = d * q.z; v[3] = d * q.w;
+          } else {
+            const __nv_bfloat16 *p = a.tb + (size_t)r * a.K + k;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = __bfloat162float(p[e]);
+          }
+        }
+      } else {
+        const float4 x = __ldcg(reinterpret_cast<const float4 *>(X + (size_t)t * a.ldx + k));
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        if (a.amode == A_RMS) {
+          const float r = s.stat_rs[t];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = v[e] * r * __bfloat162float(nw[k + e]);
+        } else if (a.amode == A_RMS2) {
+          const float r1 = s.stat_mu[t], r2 = s.stat_rs[t];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            v[e] = (v[e] * r1 * __bfloat162float(nw[k + e])) * r2 * __bfloat162float(nw2[k + e]);
+        } else if (a.amode == A_LNMOD) {
+          const float mu = s.stat_mu[t], r = s.stat_rs[t];
+          const float4 sc = *reinterpret_cast<const float4 *>(a.sc + k);
+          const float4 sh = *reinterpret_cast<const float4 *>(a.sh + k);
+          v[0] = (v[0] - mu) * r * (1.f + sc.x) + sh.x;
+          v[1] = (v[1] - mu) * r * (1.f + sc.y) + sh.y;
+          v[2] = (v[2] - mu) * r * (1.f + sc.z) + sh.z;
+          v[3] = (v[3] - mu) * r * (1.f + sc.w) + sh.w;
+        }
+      }
+    }
+    __nv_bfloat16 h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
+    const uint32_t off = (uint32_t)(t * lda + kq) * 2;
+    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s.ahi + off), "r"(pack_bf16(h[0], h[1])),
+                 "r"(pack_bf16(h[2], h[3])));
+    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s.alo + off), "r"(pack_bf16(l[0], l[1])),
+                 "r"(pack_bf16(l[2], l[3])));
+  }
+}
+
+// One 64-wide chunk: warp w owns weight rows 16w .. 16w+15 (two n8 tiles).
+template <int MT>
+__device__ __forceinline__ void compute_chunk(uint32_t wst, const Smem &s, int lda, int acol,
+                                              float (&acc)[MT][2][4]) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  uint4 blo[2], bhi[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int r = 16 * w + 8 * j + g;
+    blo[j] = lds128(wst + wslot(r, q));
+    bhi[j] = lds128(wst + wslot(r, 4 + q));
+  }
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const uint32_t r0 = (uint32_t)((16 * mt + g) * lda + acol + 8 * q) * 2;
+    const uint32_t r1 = r0 + 8 * lda * 2;
+    const uint4 h0 = lds128(s.ahi + r0), h1 = lds128(s.ahi + r1);
+    const uint4 h2 = lds128(s.ahi + r0 + 64), h3 = lds128(s.ahi + r1 + 64);
+    const uint4 l0 = lds128(s.alo + r0), l1 = lds128(s.alo + r1);
+    const uint4 l2 = lds128(s.alo + r0 + 64), l3 = lds128(s.alo + r1 + 64);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        mma_bf16(acc[mt][j], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj),
+                 word(bhi[j], jj));
+        mma_bf16(acc[mt][j], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj),
+                 word(bhi[j], jj));
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int row_pos(const GemvArgs &a, int t) {
+  const int base = a.pos_src == 0 ? a.sp->pos : a.pos_src == 1 ? a.sp->start : a.sp->L;
+  return base + a.pos_add + t;
+}
+
+// Epilogue for one (token t, 128-row tile): lane holds rows 4 * lane .. + 3.
+__device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], int tile) {
+  const int lane = threadIdx.x & 31;
+  const int mrow = m0 + 4 * lane;
+  const bool live = mrow < a.M;  // M is a multiple of 4
+  if (a.bias && live) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] += __bfloat162float(a.bias[mrow + e]);
+  }
+  switch (a.emode) {
+    case E_STORE:
+    case E_GELU:
+    case E_RESID: {
+      if (a.emode == E_GELU) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = gelu_erf(v[e]);
+      } else if (a.emode == E_RESID && live) {
+        const float4 r = __ldcg(reinterpret_cast<const float4 *>(a.R + (size_t)t * a.ldr + mrow));
+        float gt[4] = {1.f, 1.f, 1.f, 1.f};
+        if (a.gate) {
+          const float4 gg = *reinterpret_cast<const float4 *>(a.gate + mrow);
+          gt[0] = gg.x; gt[1] = gg.y; gt[2] = gg.z; gt[3] = gg.w;
+        }
+        v[0] = r.x + gt[0] * v[0];
+        v[1] = r.y + gt[1] * v[1];
+        v[2] = r.z + gt[2] * v[2];
+        v[3] = r.w + gt[3] * v[3];
+      }
+      if (live)
+        __stcg(reinterpret_cast<float4 *>(a.Y + (size_t)t * a.ldy + mrow), make_float4(v[0], v[1], v[2], v[3]));
+      if (a.out_st) {
+        float s1 = 0.f, s2 = 0.f;
+        if (live) {
+          if (a.st_w) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float vw = v[e] * __bfloat162float(a.st_w[mrow + e]);
+              s1 += v[e] * v[e];
+              s2 += vw * vw;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { s1 += v[e]; s2 += v[e] * v[e]; }
+          }
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        if (lane == 0) a.out_st[tile * kMaxT + t] = make_float2(s1, s2);
+      }
+      break;
+    }
+    case E_GEGLU: {
+      // rows 0..63 of the tile are gate rows f0 .. f0+63, rows 64..127 the up rows
+      const float other0 = __shfl_xor_sync(0xffffffffu, v[0], 16);
+      const float other1 = __shfl_xor_sync(0xffffffffu, v[1], 16);
+      const float other2 = __shfl_xor_sync(0xffffffffu, v[2], 16);
+      const float other3 = __shfl_xor_sync(0xffffffffu, v[3], 16);
+      if (lane < 16) {
+        const int f = (m0 >> 1) + 4 * lane;
+        float4 o;
+        o.x = gelu_tanh(v[0]) * other0;
+        o.y = gelu_tanh(v[1]) * other1;
+        o.z = gelu_tanh(v[2]) * other2;
+        o.w = gelu_tanh(v[3]) * other3;
+        __stcg(reinterpret_cast<float4 *>(a.Y + (size_t)t * a.ldy + f), o);
+      }
+      break;
+    }
+    case E_SEGS: {
+      const int seg = m0 / a.seg_rows;
+      const SegDesc &sd = a.segs[seg];
+      const int mseg = mrow - seg * a.seg_rows;   // row inside the segment
+      const int hd = a.hd;
+      const int lanes_per_head = hd >> 2;
+      if (sd.norm_w) {
+        float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+        ss = group_sum(ss, lanes_per_head);
+        const float r = rsqrtf(ss / (float)hd + a.qk_eps);
+        const int d0 = mseg % hd;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = v[e] * r * __bfloat162float(sd.norm_w[d0 + e]);
+        if (sd.rope) {
+          const int p = row_pos(a, t);
+          const float2 cs0 = a.rope[(size_t)p * (hd >> 1) + (d0 >> 1)];
+          const float2 cs1 = a.rope[(size_t)p * (hd >> 1) + (d0 >> 1) + 1];
+          const float x0 = v[0], x1 = v[1], x2 = v[2], x3 = v[3];
+          v[0] = x0 * cs0.x - x1 * cs0.y;
+          v[1] = x1 * cs0.x + x0 * cs0.y;
+          v[2] = x2 * cs1.x - x3 * cs1.y;
+          v[3] = x3 * cs1.x + x2 * cs1.y;
+        }
+      }
+      if (sd.kind == SEG_F32) {
+        __stcg(reinterpret_cast<float4 *>(a.Y + (size_t)t * a.ldy + sd.y_col + mseg),
+               make_float4(v[0], v[1], v[2], v[3]));
+      } else {
+        const int p = row_pos(a, t);
+        const int head = mseg / hd, d0 = mseg % hd;
+        __half2 lo = __floats2half2_rn(v[0], v[1]);
+        __half2 hi = __floats2half2_rn(v[2], v[3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t *>(&lo);
+        pk.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(sd.cache + ((size_t)head * a.max_ctx + p) * hd + d0) = pk;
+      }
+      break;
+    }
+  }
+}
+
+// Attention of the block over itself for one head (rows t < T, unmasked):
+// O = softmax(q k^T * scale) v from the q/k/v segments in Y.
+__device__ void self_attention_head(const GemvArgs &a, int head, int T, float *sm) {
+  const int hd = a.hd, D = a.self_D;
+  const int ks = hd + 1;  // padded row stride in shared memory
+  float *qq = sm, *kk = sm + kMaxT * ks, *vv = sm + 2 * kMaxT * ks;
+  for (int i = threadIdx.x; i < T * hd; i += kThreads) {
+    const int t = i / hd, d = i - t * hd;
+    const float *row = a.Y + (size_t)t * a.ldy + head * hd + d;
+    qq[t * ks + d] = __ldcg(row);
+    kk[t * ks + d] = __ldcg(row + D);
+    vv[t * ks + d] = __ldcg(row + 2 * D);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int t = w; t < T; t += kThreads / 32) {
+    float sc = -INFINITY;
+    if (lane < T) {
+      float s = 0.f;
+      for (int d = 0; d < hd; ++d) s += qq[t * ks + d] * kk[lane * ks + d];
+      sc = s * a.attn_scale;
+    }
+    const float mx = warp_max(sc);
+    const float p = lane < T ? __expf(sc - mx) : 0.f;
+    const float den = warp_sum(p);
+    for (int d = lane; d < hd; d += 32) {
+      float o = 0.f;
+      for (int j = 0; j < T; ++j) o += __shfl_sync(0xffffffffu, p, j) * vv[j * ks + d];
+      a.attn_out[(size_t)t * D + head * hd + d] = o / den;
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+template <int MT, int S>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tile = blockIdx.x;
+  const int m0 = tile * kTile;
+  const int split = blockIdx.y;
+  const int k_begin = split * a.Kc;
+  const int nchunks = a.Kc / kChunk;
+  const int lda = a_stride(a.Kp);
+
+  Smem s;
+  s.ring = smem_u32(smem);
+  const uint32_t a_bytes = (uint32_t)(16 * MT) * lda * 2;
+  s.ahi = s.ring + S * kStageBytes;
+  s.alo = s.ahi + a_bytes;
+  s.cs = s.alo + a_bytes;
+  s.cs_ptr = reinterpret_cast<float *>(smem + S * kStageBytes + 2 * a_bytes);
+  s.stat_mu = s.cs_ptr + 16 * MT * kCsStride;
+  s.stat_rs = s.stat_mu + kMaxT;
+
+  // weights do not depend on earlier kernels: start streaming them now
+#pragma unroll
+  for (int c = 0; c < S - 1; ++c) {
+    if (c < nchunks) issue_chunk(a, s.ring, c, m0, k_begin + c * kChunk);
+    cp_async_commit();
+  }
+  pdl_trigger();
+  pdl_wait();
+
+  const int T = a.T_const > 0 ? a.T_const : a.sp->T;
+  load_row_stats(a, T, s.stat_mu, s.stat_rs);
+  __syncthreads();
+
+  float acc[MT][2][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
+
+  const int cpp = a.Kp / kChunk;  // chunks per A piece
+  for (int c = 0; c < nchunks; ++c) {
+    if (c % cpp == 0) {
+      if (c) __syncthreads();
+      const int kp = min(a.Kp, a.Kc - c * kChunk);
+      stage_a<MT>(a, s, T, m0, k_begin + c * kChunk, kp);
+      __syncthreads();
+    }
+    if (c + S - 1 < nchunks) issue_chunk(a, s.ring, (c + S - 1) % S, m0, k_begin + (c + S - 1) * kChunk);
+    cp_async_commit();
+    cp_async_wait<S - 1>();
+    __syncthreads();
+    compute_chunk<MT>(s.ring + (c % S) * kStageBytes, s, lda, (c % cpp) * kChunk, acc);
+    __syncthreads();
+  }
+
+  // partial tile -> shared memory
+  {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = 16 * w + 8 * j + 2 * q;
+        const int t0 = 16 * mt + g;
+        *reinterpret_cast<float2 *>(s.cs_ptr + t0 * kCsStride + col) = make_float2(acc[mt][j][0], acc[mt][j][1]);
+        *reinterpret_cast<float2 *>(s.cs_ptr + (t0 + 8) * kCsStride + col) =
+            make_float2(acc[mt][j][2], acc[mt][j][3]);
+      }
+  }
+  __syncthreads();
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int ks = a.ksplit;
+  const int rank = ks > 1 ? (int)cluster.block_rank() : 0;
+  if (ks > 1) cluster.sync();
+
+  {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int t = rank + ks * w; t < T; t += ks * (kThreads / 32)) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int r = 0; r < ks; ++r) {
+        const float *src = ks > 1 ? cluster.map_shared_rank(s.cs_ptr, r) : s.cs_ptr;
+        const float4 x = *reinterpret_cast<const float4 *>(src + t * kCsStride + 4 * lane);
+        v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+      }
+      epilogue_unit(a, t, m0, v, tile);
+    }
+  }
+  if (ks > 1) cluster.sync();
+
+  // self-attention tail: the last CTA to finish a head's q, k and v computes it
+  if (a.self_D > 0) {
+    __shared__ int s_last[4];
+    const int D = a.self_D;
+    const int mseg = m0 % D;
+    const int heads_in_tile = kTile / a.hd;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < heads_in_tile; ++i) {
+        const int h = mseg / a.hd + i;
+        const int old = atomicAdd(a.tickets + h, 1);
+        const bool last = old == 3 * ks - 1;
+        if (last) atomicExch(a.tickets + h, 0);
+        s_last[i] = last ? h : -1;
+      }
+    }
+    __syncthreads();
+    for (int i = 0; i < heads_in_tile; ++i) {
+      if (s_last[i] >= 0) {
+        __threadfence();
+        self_attention_head(a, s_last[i], T, reinterpret_cast<float *>(smem));
+      }
+    }
+  }
+}
+
+size_t gemv_smem_bytes(const GemvArgs &a, int mt) {
+  const int S = mt == 1 ? 4 : 3;
+  const size_t a_bytes = (size_t)(16 * mt) * a_stride(a.Kp) * 2;
+  size_t bytes = (size_t)S * kStageBytes + 2 * a_bytes + (size_t)(16 * mt) * kCsStride * 4 + 2 * kMaxT * 4;
+  const size_t attn = a.self_D > 0 ? (size_t)3 * kMaxT * (a.hd + 1) * 4 : 0;
+  return bytes > attn ? bytes : attn;
+}
+
+cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t st, bool pdl) {
+  const int T = a.T_const > 0 ? a.T_const : kMaxT;
+  const int mt = (a.T_const > 0 && a.T_const <= 16) ? 1 : 2;
+  (void)T;
+  const size_t smem = gemv_smem_bytes(a, mt);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_tiles, a.ksplit, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = 1;
+  attr[na].val.clusterDim.y = a.ksplit;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e;
+  if (mt == 1) {
+    e = cudaFuncSetAttribute(gemv_kernel<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<1, 4>, a);
+  }
+  e = cudaFuncSetAttribute(gemv_kernel<2, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<2, 3>, a);
+}
+
+}  // namespace fm

@@ -1,0 +1,205 @@
+// k_setup.cu -- one-time set-up kernels run by fm_create, and small kernels.
+#include "dev_common.cuh"
+#include "fm_internal.h"
+
+namespace fm {
+
+namespace {
+
+// GGUF Q8_0 rows [V][nb * 34] -> int8 plane [Vpad][H] and scale plane
+// [Vpad / 128][nb][128] (the MTP loader on ternary_bonsai_2_mtp.js splits the
+// 34-byte blocks the same way; the scale plane is tiled by 128 rows here so a
+// vocab tile's scales are contiguous).  Padding rows get zeros.
+__global__ void q8_repack_kernel(const uint8_t *raw, int V, int H, int8_t *q, __half *scales, int Vpad) {
+  const int nb = H / 32;
+  const long long id = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (id >= (long long)Vpad * nb) return;
+  const int r = (int)(id / nb), b = (int)(id - (long long)r * nb);
+  int8_t *qd = q + (size_t)r * H + b * 32;
+  __half *sd = scales + ((size_t)(r >> 7) * nb + b) * 128 + (r & 127);
+  if (r >= V) {
+    for (int i = 0; i < 32; ++i) qd[i] = 0;
+    *sd = __ushort_as_half(0);
+    return;
+  }
+  const uint8_t *src = raw + (size_t)r * nb * 34 + b * 34;
+  const unsigned short d = (unsigned short)src[0] | ((unsigned short)src[1] << 8);
+  *sd = __ushort_as_half(d);
+  for (int i = 0; i < 32; ++i) qd[i] = (int8_t)src[2 + i];
+}
+
+// column sums in double over a slab of rows; partial[slab][col]
+__global__ void colsum_q8_kernel(const int8_t *q, const __half *scales, int V, int H, int rows_per_slab,
+                                 double *partial) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= H) return;
+  const int r0 = blockIdx.y * rows_per_slab, r1 = min(V, r0 + rows_per_slab);
+  double s = 0.0;
+  for (int r = r0; r < r1; ++r) {
+    const float d = __half2float(scales[((size_t)(r >> 7) * (H >> 5) + (c >> 5)) * 128 + (r & 127)]);
+    s += (double)(d * (float)q[(size_t)r * H + c]);
+  }
+  partial[(size_t)blockIdx.y * H + c] = s;
+}
+
+__global__ void colsum_bf16_kernel(const __nv_bfloat16 *w, int V, int H, int rows_per_slab, double *partial) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= H) return;
+  const int r0 = blockIdx.y * rows_per_slab, r1 = min(V, r0 + rows_per_slab);
+  double s = 0.0;
+  for (int r = r0; r < r1; ++r) s += (double)__bfloat162float(w[(size_t)r * H + c]);
+  partial[(size_t)blockIdx.y * H + c] = s;
+}
+
+__global__ void colmean_finish_kernel(const double *partial, int slabs, int H, int V, float *out) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= H) return;
+  double s = 0.0;
+  for (int i = 0; i < slabs; ++i) s += partial[(size_t)i * H + c];
+  out[c] = (float)(s / (double)V);
+}
+
+// (cos, sin) of p * theta^(-2i / hd), angles in double
+__global__ void rope_table_kernel(float2 *tab, int n_pos, int hd, double theta) {
+  const int half = hd / 2;
+  const long long id = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (id >= (long long)n_pos * half) return;
+  const int p = (int)(id / half), i = (int)(id - (long long)p * half);
+  const double inv = pow(theta, -2.0 * (double)i / (double)hd);
+  double s, c;
+  sincos((double)p * inv, &s, &c);
+  tab[id] = make_float2((float)c, (float)s);
+}
+
+__global__ void transpose_bf16_kernel(const __nv_bfloat16 *in, int rows, int cols, __nv_bfloat16 *out, int ldo) {
+  __shared__ __nv_bfloat16 t[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) t[i][threadIdx.x] = in[(size_t)r * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[(size_t)c * ldo + r] = t[threadIdx.x][i];
+  }
+}
+
+// DFlash block rows 1 .. gamma-1: mask_emb[j-1] + block_pos[j] (module-dflash.ts #buildBlock)
+__global__ void block_consts_kernel(const __nv_bfloat16 *mask_emb, const __nv_bfloat16 *block_pos, int gamma, int d,
+                                    float *out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= gamma * d) return;
+  const int j = i / d, k = i - j * d;
+  out[i] = j == 0 ? 0.f : __bfloat162float(mask_emb[(size_t)(j - 1) * d + k]) + __bfloat162float(block_pos[i]);
+}
+
+// (sum, sumsq) of each row over each 128-column tile: st[tile * kMaxT + row]
+__global__ void row_stats_kernel(const float *x, int rows, int d, float2 *st) {
+  const int tile = blockIdx.x, row = blockIdx.y;
+  const int lane = threadIdx.x;
+  float s1 = 0.f, s2 = 0.f;
+  for (int c = tile * kTile + lane; c < min(d, (tile + 1) * kTile); c += 32) {
+    const float v = x[(size_t)row * d + c];
+    s1 += v;
+    s2 += v * v;
+  }
+  s1 = warp_sum(s1);
+  s2 = warp_sum(s2);
+  if (lane == 0 && row < rows) st[tile * kMaxT + row] = make_float2(s1, s2);
+}
+
+__global__ void accept_kernel(int n, int block, const int32_t *draft, const int32_t *target, const int32_t *k,
+                              int32_t *acc, int32_t *bonus) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  int kk = k[i];
+  kk = kk < 0 ? 0 : (kk > block ? block : kk);
+  const int32_t *d = draft + (size_t)i * block, *t = target + (size_t)i * (block + 1);
+  int a = 0;
+  while (a < kk && d[a] == t[a]) ++a;
+  acc[i] = a;
+  bonus[i] = t[a];
+}
+
+__global__ void fill_kernel(float *p, size_t n, float v) {
+  const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (i < n) p[i] = v;
+}
+
+}  // namespace
+
+cudaError_t launch_q8_repack(const uint8_t *raw, int32_t V, int32_t H, int8_t *q, __half *scales, int32_t Vpad,
+                             cudaStream_t s) {
+  const long long n = (long long)Vpad * (H / 32);
+  q8_repack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(raw, V, H, q, scales, Vpad);
+  return cudaGetLastError();
+}
+
+static cudaError_t colmean_common(const void *a, const __half *sc, bool q8, int32_t V, int32_t H, float *out,
+                                  cudaStream_t s) {
+  const int slabs = 128;
+  const int rps = (V + slabs - 1) / slabs;
+  double *partial = nullptr;
+  cudaError_t e = cudaMallocAsync(&partial, sizeof(double) * slabs * H, s);
+  if (e != cudaSuccess) return e;
+  dim3 grid((H + 127) / 128, slabs);
+  if (q8)
+    colsum_q8_kernel<<<grid, 128, 0, s>>>(static_cast<const int8_t *>(a), sc, V, H, rps, partial);
+  else
+    colsum_bf16_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16 *>(a), V, H, rps, partial);
+  colmean_finish_kernel<<<(H + 127) / 128, 128, 0, s>>>(partial, slabs, H, V, out);
+  e = cudaGetLastError();
+  cudaFreeAsync(partial, s);
+  return e;
+}
+
+cudaError_t launch_colmean_q8(const int8_t *q, const __half *scales, int32_t V, int32_t H, float *out,
+                              cudaStream_t s) {
+  return colmean_common(q, scales, true, V, H, out, s);
+}
+
+cudaError_t launch_colmean_bf16(const __nv_bfloat16 *w, int32_t V, int32_t H, float *out, cudaStream_t s) {
+  return colmean_common(w, nullptr, false, V, H, out, s);
+}
+
+cudaError_t launch_rope_table(float2 *tab, int32_t n_pos, int32_t hd, float theta, cudaStream_t s) {
+  const long long n = (long long)n_pos * (hd / 2);
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(tab, n_pos, hd, (double)theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16(const __nv_bfloat16 *in, int32_t rows, int32_t cols, __nv_bfloat16 *out,
+                                  int32_t ldo, cudaStream_t s) {
+  dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
+  transpose_bf16_kernel<<<grid, block, 0, s>>>(in, rows, cols, out, ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_consts(const __nv_bfloat16 *mask_emb, const __nv_bfloat16 *block_pos, int32_t gamma,
+                                int32_t d, float *out, float2 *st, cudaStream_t s) {
+  block_consts_kernel<<<(gamma * d + 255) / 256, 256, 0, s>>>(mask_emb, block_pos, gamma, d, out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_row_stats(out, gamma, d, st, s);
+}
+
+cudaError_t launch_row_stats(const float *x, int32_t rows, int32_t d, float2 *st, cudaStream_t s) {
+  dim3 grid((d + kTile - 1) / kTile, rows);
+  row_stats_kernel<<<grid, 32, 0, s>>>(x, rows, d, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_accept(int32_t n, int32_t block, const int32_t *draft, const int32_t *target, const int32_t *k,
+                          int32_t *acc, int32_t *bonus, cudaStream_t s) {
+  accept_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, block, draft, target, k, acc, bonus);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_f32(float *p, size_t n, float v, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  fill_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, n, v);
+  return cudaGetLastError();
+}
+
+}  // namespace fm

@@ -1,0 +1,244 @@
+/*
+ * fm.h -- C ABI of libfm.so, a GB300 (sm_103a) implementation of the forward
+ * pass of a block-parallel speculative-decoding drafter of the FlashMap /
+ * DFlash kind.  One process, one GPU; every compute step runs in the
+ * library's own CUDA kernels.
+ *
+ * Sources (page title, file, section):
+ *   [FM]  diskformer 0.5.4 -> 0.6.6, package/engines/flashmap_drafter.js
+ *   [MTP] diskformer 0.5.3 -> 0.6.4, package/engines/ternary_bonsai_2_mtp.js
+ *   [DF]  mlx-bun 0.4.0 -> 1.0.0, package/src/spec/dspark/module-dflash.ts
+ *
+ * Conventions
+ *   - Pointers named *_dev are device pointers; *_host are host pointers.
+ *     "stream" is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Every call checks its arguments on the host before it launches anything
+ *     and returns an fm_status; nothing aborts and no C++ exception crosses the
+ *     ABI.  On failure fm_last_error(h) holds a one-line reason.
+ *   - All device work is ordered on the given stream; no call synchronises the
+ *     host except fm_debug_copy (it copies to host memory) and fm_create.
+ *   - A handle is not thread-safe: one host thread at a time per handle.
+ */
+#ifndef FM_H_
+#define FM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FM_ABI_VERSION 1
+
+/* exported from libfm.so; everything else in the library is hidden */
+#if defined(__GNUC__)
+#define FM_API __attribute__((visibility("default")))
+#else
+#define FM_API
+#endif
+
+typedef enum fm_status {
+  FM_OK = 0,
+  FM_ERR_INVALID_ARG = 1,   /* a null/misaligned pointer, a size or index out of range, a bad tensor */
+  FM_ERR_UNSUPPORTED = 2,   /* a configuration the kernels do not handle (see fm_config) */
+  FM_ERR_OOM = 3,           /* a device or pinned-host allocation failed */
+  FM_ERR_CONTEXT_FULL = 4,  /* start + n_rows + block + 1 > max_ctx ([FM] extendContext's check) */
+  FM_ERR_STATE = 5,         /* the call does not fit the sequence state (pos != length, start > length) */
+  FM_ERR_CUDA = 6,          /* a CUDA runtime error; fm_last_error has the CUDA message */
+  FM_ERR_TIMEOUT = 7        /* a bounded device-side wait gave up (reported, never hung) */
+} fm_status;
+
+/* fm_config.variant */
+#define FM_VARIANT_FLASHMAP 0 /* adaLN DiT drafter with context injection [FM] */
+#define FM_VARIANT_DFLASH 1   /* KV-injection drafter, Eq 2 / Eq 3 [DF] */
+
+/* fm_config.lm_format: storage of the tied token table E [vocab][target_dim] */
+#define FM_LM_BF16 0
+#define FM_LM_Q8_0 1 /* GGUF Q8_0: per 32 values a little-endian f16 scale then 32 int8 (34 bytes) [MTP] */
+
+/* fm_tensor.dtype */
+#define FM_DTYPE_BF16 0
+#define FM_DTYPE_Q8_0 1
+#define FM_DTYPE_F32 2
+
+typedef struct fm_config {
+  int32_t variant;     /* FM_VARIANT_* */
+  int32_t dim;         /* draft width D (multiple of 128) */
+  int32_t n_heads;     /* D = n_heads * head_dim */
+  int32_t head_dim;    /* 64 or 128 */
+  int32_t n_layers;    /* DiT / backbone layers (1..64) */
+  int32_t ff_dim;      /* MLP width (multiple of 128) */
+  int32_t block;       /* draft slots: 16 for [FM], gamma for [DF]; 1..16 */
+  int32_t target_dim;  /* the target's hidden width Ht (multiple of 64) */
+  int32_t n_taps;      /* tapped target layers; feature rows are n_taps * target_dim wide */
+  int32_t vocab;       /* rows of the token table */
+  int32_t lm_format;   /* FM_LM_* */
+  int32_t max_ctx;     /* cache rows per sequence (positions 0 .. max_ctx-1) */
+  int32_t max_seqs;    /* independent sequences the handle holds caches for (>= 1) */
+  float rope_theta;    /* RoPE base ([FM] CFG.theta) */
+  float ln_eps;        /* adaLN LayerNorm eps ([FM] CFG.lnEps) */
+  float rms_eps;       /* RMSNorm eps ([FM] CFG.rmsEps; [DF] the target's eps) */
+  float qk_eps;        /* per-head q/k RMSNorm eps ([FM] CFG.qkEps) */
+} fm_config;
+
+/*
+ * One named weight.  Names, shapes and layouts ([out][in] for [FM], [in][out]
+ * for [DF]) are those of the drafter checkpoints:
+ *   [FM]: fc.weight, hidden_norm.weight, anchor_proj.{weight,bias},
+ *         anchor_norm.weight, state_norm.weight, x_embed.{weight,bias},
+ *         layers.{l}.{self_attn,cross_attn}.{q,k,v,o}_proj.weight,
+ *         layers.{l}.{self_attn,cross_attn}.{q,k}_norm.weight,
+ *         layers.{l}.mlp.fc{1,2}.{weight,bias}, head.{weight,bias},
+ *         token_embd.weight (the tied table; FM_DTYPE_Q8_0 or FM_DTYPE_BF16).
+ *         A missing bias is read as zero.
+ *   [DF]: bb.{i}.{attn_norm,q,k,v,o,ff_norm,gate,up,down}, W_c, ctx_norm,
+ *         tok_proj, mask_emb, block_pos, out_norm, out_proj, token_embd.weight.
+ * data is host memory (on_device = 0) or device memory (on_device = 1); the
+ * library copies (and repacks) every tensor during fm_create, so the caller may
+ * free it when fm_create returns.  nbytes must equal the tensor's size.
+ */
+typedef struct fm_tensor {
+  const char *name;
+  const void *data;
+  int64_t nbytes;
+  int32_t dtype;      /* FM_DTYPE_* */
+  int32_t on_device;  /* 0 host, 1 device */
+} fm_tensor;
+
+typedef struct fm_handle fm_handle;
+
+/*
+ * fm_create -- take the configuration and the weights, build the device state
+ * ([FM] FlashMapDrafter.load / upload / init; [DF] DflashDrafter.load).
+ *   modulation_host: [FM] the adaLN table [(3*n_layers+1) * 3 * dim] f32 in
+ *     blocks [scale dim | shift dim | gate dim] for (self, cross, mlp) of every
+ *     layer and the final norm ([FM] timeConditioning output); NULL for [DF].
+ *   On success *out owns: the repacked weights, per-sequence caches of max_ctx
+ *   rows, work buffers, and the constant start row h0 = x_embed(state_norm(
+ *   mean row of E)) ([FM] init).  Synchronises the stream before returning.
+ * Errors: FM_ERR_INVALID_ARG (null pointer, unknown/missing/mis-sized tensor,
+ *   wrong dtype), FM_ERR_UNSUPPORTED (dims outside the limits above), FM_ERR_OOM,
+ *   FM_ERR_CUDA.  *out is NULL on failure.
+ */
+FM_API fm_status fm_create(const fm_config *cfg, const fm_tensor *weights, int32_t n_weights,
+                    const float *modulation_host, void *stream, fm_handle **out);
+
+/*
+ * fm_context_append -- context injection ([FM] extendContext; [DF] Eq 2 and
+ * projectContextRows): the target's tapped feature rows feats_dev
+ * [n_rows][n_taps * target_dim] f32 (device, row-major, 16-byte aligned)
+ * become cache rows start_pos .. start_pos + n_rows - 1 of sequence seq.
+ *   [FM]: c = fc(f); cn = RMSNorm(c; hidden_norm); per layer k = RoPE(k_norm(
+ *         k_proj cn)) at the row's position, v = v_proj cn; stored as f16.
+ *   [DF]: H = RMSNorm(f W_c; ctx_norm); per layer K = attn_norm(H) W_k,
+ *         V = attn_norm(H) W_v; stored as f16.
+ * start_pos <= length is required; writing below the length rewinds (the
+ * verify step re-appends from the anchor slot).  Afterwards length =
+ * start_pos + n_rows.  n_rows may be 0 (only moves the length).
+ * Errors: FM_ERR_INVALID_ARG (seq out of range, n_rows < 0, null feats with
+ *   n_rows > 0), FM_ERR_STATE (start_pos > length or < 0),
+ *   FM_ERR_CONTEXT_FULL (start_pos + n_rows + block + 1 > max_ctx), FM_ERR_CUDA.
+ */
+FM_API fm_status fm_context_append(fm_handle *h, int32_t seq, const float *feats_dev, int32_t n_rows,
+                            int32_t start_pos, void *stream);
+
+/*
+ * fm_context_append_batched -- fm_context_append for several sequences in one
+ * pass (the rows of all sequences share each weight read).  feats_dev holds
+ * the rows of seq_ids[0], then seq_ids[1], ...; n_rows_host[i] and
+ * start_host[i] are per sequence (host arrays of n_seqs).  Same checks per
+ * sequence; nothing is launched if any check fails.  Sequence ids must be
+ * distinct.
+ */
+FM_API fm_status fm_context_append_batched(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids_host,
+                                    const float *feats_dev, const int32_t *n_rows_host,
+                                    const int32_t *start_host, void *stream);
+
+/*
+ * fm_draft -- draft `block` tokens after each anchor ([FM] draft; [DF]
+ * forwardRows with the greedy argmax).  For sequence seq_ids[i] the anchor
+ * token anchors[i] sits at position pos[i], which must equal that sequence's
+ * length.  [FM] writes the anchor's own context slot (cache row pos) as the
+ * page does; the length is unchanged (a later append from pos overwrites it).
+ * tokens_dev: device int32 [n_seqs][block], written in stream order.
+ * Host arrays: seq_ids, anchors, pos (n_seqs each; distinct seq ids).
+ * Errors: FM_ERR_INVALID_ARG (anchor outside [0, vocab), bad seq id, n_seqs
+ *   outside [1, max_seqs], null tokens), FM_ERR_STATE (pos != length),
+ *   FM_ERR_CONTEXT_FULL (pos + block + 1 > max_ctx), FM_ERR_CUDA.
+ */
+FM_API fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids_host, const int32_t *anchors_host,
+                   const int32_t *pos_host, int32_t *tokens_dev, void *stream);
+
+/*
+ * fm_accept -- greedy acceptance ([FM] specGenerate verify step; [MTP] the
+ * same rule): n_accepted = the longest prefix i < k with draft[i] == target[i];
+ * bonus = target[n_accepted].  draft_host has k entries, target_host k + 1.
+ * Pure host function.  Errors: FM_ERR_INVALID_ARG (null pointer, k < 0).
+ */
+FM_API fm_status fm_accept(const int32_t *draft_host, const int32_t *target_host, int32_t k, int32_t *n_accepted,
+                    int32_t *bonus);
+
+/*
+ * fm_accept_batched -- fm_accept for n_seqs sequences on the device:
+ * draft_dev [n_seqs][block], target_dev [n_seqs][block + 1], k_dev [n_seqs]
+ * (each clamped to [0, block]); writes n_accepted_dev[n_seqs], bonus_dev[n_seqs].
+ * Errors: FM_ERR_INVALID_ARG (null pointer, n_seqs < 1), FM_ERR_CUDA.
+ */
+FM_API fm_status fm_accept_batched(fm_handle *h, int32_t n_seqs, const int32_t *draft_dev, const int32_t *target_dev,
+                            const int32_t *k_dev, int32_t *n_accepted_dev, int32_t *bonus_dev, void *stream);
+
+/* fm_debug_copy selectors ([FM] readOut / peek: look at working buffers) */
+#define FM_DEBUG_HIDDEN 0   /* index = layer: the block's hidden rows after that layer [block][dim] f32 (last draft) */
+#define FM_DEBUG_HEAD_OUT 1 /* the head output Y [block][target_dim] f32 (last draft of seq) */
+#define FM_DEBUG_LOGITS 2   /* logits [block][vocab] f32 of the last draft's Y, recomputed without argmax */
+#define FM_DEBUG_CACHE_K 3  /* index = layer: cache K of seq, [n_heads][max_ctx][head_dim] as f16 bits */
+#define FM_DEBUG_CACHE_V 4  /* index = layer: cache V, same layout */
+#define FM_DEBUG_H0 5       /* [FM] the constant start row h0 [dim] f32 */
+
+/*
+ * fm_debug_copy -- copy nbytes of the selected buffer, starting at byte
+ * offset, to dst_host.  Synchronises the stream.  Errors: FM_ERR_INVALID_ARG
+ * (unknown selector, index or range outside the buffer), FM_ERR_CUDA.
+ */
+FM_API fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, int64_t offset, void *dst_host,
+                        int64_t nbytes, void *stream);
+
+/* fm_set_debug flags */
+#define FM_DEBUG_KEEP_HIDDEN 1 /* keep every layer's block hidden rows for FM_DEBUG_HIDDEN (adds copies) */
+#define FM_DEBUG_PROFILE 2     /* bracket every kernel launch with CUDA events (serialises the chain) */
+
+/* Debug switches for later calls (0 = the plain hot path).  Errors: FM_ERR_INVALID_ARG. */
+FM_API fm_status fm_set_debug(fm_handle *h, int32_t flags);
+
+/* Per-kernel timings gathered while FM_DEBUG_PROFILE is set: one entry per
+ * kernel name, with the launches, their summed device time and the summed
+ * algorithmic bytes they move (weights once, activations once).  Reading
+ * synchronises the stream of the recorded launches and resets the record.
+ * Errors: FM_ERR_INVALID_ARG (null pointers, cap < 0), FM_ERR_CUDA. */
+typedef struct fm_kernel_time {
+  char name[32];
+  int32_t launches;
+  float ms;
+  double bytes;
+} fm_kernel_time;
+FM_API fm_status fm_profile_read(fm_handle *h, fm_kernel_time *out, int32_t cap, int32_t *n);
+
+/* Current context length of a sequence.  Errors: FM_ERR_INVALID_ARG. */
+FM_API fm_status fm_get_length(const fm_handle *h, int32_t seq, int32_t *length);
+
+/* Device bytes the handle holds ([FM] gpuBytes). */
+FM_API fm_status fm_memory_bytes(const fm_handle *h, int64_t *bytes);
+
+/* Kernel launches issued by the last fm_context_append / fm_draft / batched call. */
+FM_API fm_status fm_last_launch_count(const fm_handle *h, int32_t *count);
+
+FM_API const char *fm_status_str(fm_status s);
+FM_API const char *fm_last_error(const fm_handle *h);   /* never NULL; "" when no error; NULL h: the last failed fm_create on this thread */
+
+/* Free everything the handle owns.  NULL is ignored. */
+FM_API void fm_destroy(fm_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FM_H_ */

@@ -1,0 +1,98 @@
+"""The C ABI library loads and exports every entry point include/fm.h declares;
+host-only logic (argument checks that run before any device work, the pure
+host acceptance rule) behaves as documented.  No GPU needed."""
+from __future__ import annotations
+
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import block_speculative_decoding_fm_gb300 as fm
+import fm_synth as S
+from block_speculative_decoding_fm_gb300 import build as fmbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fmbuild.build()
+    return fm.load_library()
+
+
+def declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "fm.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(fm_[a-z_]+)\s*\(", txt)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("fm_create", "fm_context_append", "fm_draft", "fm_accept", "fm_accept_batched", "fm_debug_copy",
+              "fm_destroy", "fm_status_str", "fm_last_error"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+    assert set(declared_symbols()) <= set(fm.EXPORTS)
+
+
+def test_no_internal_symbols_exported(lib):
+    out = os.popen(f"nm -D --defined-only {fm.LIB_PATH}").read()
+    names = [l.split()[-1] for l in out.splitlines() if " T " in l]
+    assert names and all(n.startswith("fm_") for n in names), names
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.fm_status_str(s)
+    assert lib.fm_status_str(99) == b"unknown status"
+
+
+def test_accept_host_rule_brute_force(lib):
+    for k in range(5):
+        for d in itertools.product(range(3), repeat=4):
+            for t in itertools.product(range(3), repeat=5):
+                acc, bonus = fm.fm_accept(d, t, k)
+                want = next((i for i in range(k) if d[i] != t[i]), k)
+                assert (acc, bonus) == (want, t[want])
+
+
+def test_accept_rejects_bad_arguments(lib):
+    acc, bonus = ctypes.c_int32(), ctypes.c_int32()
+    d = np.zeros(4, np.int32)
+    assert lib.fm_accept(None, d.ctypes.data, 2, ctypes.byref(acc), ctypes.byref(bonus)) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_accept(d.ctypes.data, d.ctypes.data, -1, ctypes.byref(acc), ctypes.byref(bonus)) == \
+        fm.FM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 96, fm.FM_ERR_UNSUPPORTED),
+    ("dim", 200, fm.FM_ERR_INVALID_ARG),
+    ("block", 17, fm.FM_ERR_UNSUPPORTED),
+    ("n_layers", 0, fm.FM_ERR_UNSUPPORTED),
+    ("lm_format", 7, fm.FM_ERR_INVALID_ARG),
+    ("max_seqs", 0, fm.FM_ERR_INVALID_ARG),
+    ("variant", 3, fm.FM_ERR_INVALID_ARG),
+    ("target_dim", 100, fm.FM_ERR_UNSUPPORTED),
+])
+def test_create_rejects_bad_configs_before_device_work(lib, field, value, status):
+    cfg = S.tiny_config().replace(**{field: value})
+    with pytest.raises(fm.FmError) as e:
+        fm.fm_create(cfg, [], None)
+    assert e.value.status == status
+    assert lib.fm_last_error(None)
+
+
+def test_null_handle_calls_are_rejected(lib):
+    assert lib.fm_context_append(None, 0, None, 0, 0, None) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_draft(None, 1, None, None, None, None, None) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_debug_copy(None, 0, 0, 0, 0, None, 0, None) == fm.FM_ERR_INVALID_ARG
+    lib.fm_destroy(None)
+    assert lib.fm_last_error(None) is not None

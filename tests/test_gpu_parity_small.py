@@ -1,0 +1,188 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle on small
+workloads that span several tiles and ragged tails: the tiny FlashMap-shaped
+drafter (both table formats), a small DFlash drafter, ragged append sizes,
+rewinds, the empty-context draft, and acceptance."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import fm_synth as S
+from gpu_common import REL_L2, Pair, rel_l2, tokens_match
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_speculative_decoding_fm_gb300 import build
+    build.build()
+
+
+def small_dflash(**kw):
+    c = S.DrafterConfig(S.VARIANT_DFLASH, dim=256, n_heads=2, head_dim=128, n_layers=2, ff_dim=512, block=5,
+                        target_dim=320, n_taps=2, vocab=4096, lm_format=S.LM_BF16, max_ctx=160)
+    return c.replace(**kw)
+
+
+def check_draft(p: Pair, got, ref, layers=True):
+    if layers:
+        for l in range(p.cfg.n_layers):
+            e = rel_l2(p.hidden(l), ref.hidden[l])
+            assert e < REL_L2, (l, e)
+    e = rel_l2(p.head_out(), ref.head_out)
+    assert e < REL_L2, e
+    lg = p.logits()
+    e = rel_l2(lg, ref.logits)
+    assert e < REL_L2, e
+    assert tokens_match(got, ref.tokens, ref.logits), (got, ref.tokens)
+    # the fused argmax agrees with the argmax of the recomputed logits
+    assert np.array_equal(got, np.argmax(lg, axis=-1))
+
+
+def check_cache(p: Pair, seq, rows):
+    st = p.state(seq)
+    for l in range(p.cfg.n_layers):
+        for which, ref in (("k", st.k[l]), ("v", st.v[l])):
+            got = p.cache(seq, l, which)[:rows]
+            want = ref[:rows]
+            assert rel_l2(got, want) < 1e-3, (l, which, rel_l2(got, want))
+            # the f16 store matches the oracle's f16 rounding up to one step
+            step = np.abs(want) * 2.0 ** -10 + 2.0 ** -24
+            assert np.all(np.abs(got - want) <= step + 1e-7), (l, which)
+
+
+@pytest.mark.parametrize("lm", [S.LM_BF16, S.LM_Q8_0])
+def test_tiny_flashmap_one_step(lm):
+    cfg = S.tiny_config(max_ctx=128).replace(lm_format=lm)
+    p = Pair(cfg, 1001)
+    rng = S.streams(1001)["features"]
+    p.append(0, S.gen_features(rng, 64, cfg.feat_dim), 0)
+    check_cache(p, 0, 64)
+    anchor = S.gen_anchor(S.streams(1001)["tokens"], cfg.vocab)
+    got, ref = p.draft(0, anchor, 64)
+    check_draft(p, got, ref)
+    check_cache(p, 0, 65)
+    p.close()
+
+
+def test_tiny_flashmap_ragged_appends_and_rewind():
+    cfg = S.tiny_config(max_ctx=160)
+    p = Pair(cfg, 1002)
+    rng = S.streams(1002)["features"]
+    feats = S.gen_features(rng, 120, cfg.feat_dim)
+    start = 0
+    for n in (1, 5, 16, 17, 31, 32, 18):   # 120 rows in ragged pieces (33-row pieces below)
+        p.append(0, feats[start:start + n], start)
+        start += n
+    check_cache(p, 0, 120)
+    k_before = [p.cache(0, l, "k").copy() for l in range(cfg.n_layers)]
+    # rewind to 100 and re-append the same rows: bit-identical cache
+    p.append(0, feats[100:120], 100)
+    for l in range(cfg.n_layers):
+        assert np.array_equal(p.cache(0, l, "k")[:120], k_before[l][:120])
+    got, ref = p.draft(0, 7, 120)
+    check_draft(p, got, ref)
+    p.close()
+
+
+def test_tiny_flashmap_long_append_crosses_chunks():
+    cfg = S.tiny_config(max_ctx=160)
+    p = Pair(cfg, 1003)
+    feats = S.gen_features(S.streams(1003)["features"], 97, cfg.feat_dim)
+    p.append(0, feats, 0)                    # 97 rows: three 32-row passes and a tail
+    check_cache(p, 0, 97)
+    got, ref = p.draft(0, 4095, 97)
+    check_draft(p, got, ref)
+    p.close()
+
+
+def test_tiny_flashmap_empty_context_draft():
+    cfg = S.tiny_config(max_ctx=64)
+    p = Pair(cfg, 1004)
+    got, ref = p.draft(0, 11, 0)             # cross keys = the anchor slot alone
+    check_draft(p, got, ref)
+    check_cache(p, 0, 1)
+    p.close()
+
+
+def test_tiny_flashmap_draft_accept_cycles():
+    """Several verify rounds: draft, targets with a seeded flip, accept on host
+    and device, append acc + 1 fresh rows from the anchor slot."""
+    import torch
+    import block_speculative_decoding_fm_gb300 as fm
+    from oracle import accept
+    cfg = S.tiny_config(max_ctx=200)
+    p = Pair(cfg, 1005)
+    fr = S.streams(1005)["features"]
+    tr = S.streams(1005)["tokens"]
+    p.append(0, S.gen_features(fr, 40, cfg.feat_dim), 0)
+    pos, anchor = 40, 3
+    for cycle in range(6):
+        got, ref = p.draft(0, anchor, pos)
+        check_draft(p, got, ref, layers=(cycle == 0))
+        flip = int(tr.integers(0, cfg.block + 1))
+        target = S.targets_with_flip(ref.tokens, cfg.block, flip, cfg.vocab, tr)
+        want = accept(ref.tokens, target, cfg.block)
+        assert fm.fm_accept(ref.tokens.astype(np.int32), target, cfg.block) == want
+        d = torch.from_numpy(ref.tokens.astype(np.int32)[None]).cuda()
+        t = torch.from_numpy(target[None]).cuda()
+        k = torch.full((1,), cfg.block, dtype=torch.int32, device="cuda")
+        acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        bonus = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fm.fm_accept_batched(p.h, d, t, k, acc, bonus)
+        assert (int(acc.item()), int(bonus.item())) == want
+        n = want[0] + 1
+        p.append(0, S.gen_features(fr, n, cfg.feat_dim), pos)
+        pos += n
+        anchor = want[1]
+    check_cache(p, 0, pos)
+    p.close()
+
+
+def test_small_dflash_steps():
+    cfg = small_dflash()
+    p = Pair(cfg, 1006)
+    fr = S.streams(1006)["features"]
+    p.append(0, S.gen_features(fr, 70, cfg.feat_dim), 0)
+    got, ref = p.draft(0, 17, 70)
+    check_draft(p, got, ref)
+    # verify cycle: append acc + 1 rows at the anchor position, draft again
+    p.append(0, S.gen_features(fr, 3, cfg.feat_dim), 70)
+    got, ref = p.draft(0, 99, 73)
+    check_draft(p, got, ref)
+    p.close()
+
+
+def test_small_dflash_empty_context():
+    cfg = small_dflash()
+    p = Pair(cfg, 1007)
+    got, ref = p.draft(0, 5, 0)              # attention over the block alone
+    check_draft(p, got, ref)
+    p.close()
+
+
+def test_errors_are_reported_not_raised_on_device():
+    import block_speculative_decoding_fm_gb300 as fm
+    cfg = S.tiny_config(max_ctx=64)
+    p = Pair(cfg, 1008, keep_hidden=False)
+    feats = S.gen_features(S.streams(1008)["features"], 8, cfg.feat_dim)
+    with pytest.raises(fm.FmError) as e:
+        p.append(0, feats, 3, oracle=False)           # start beyond the length
+    assert e.value.status == fm.FM_ERR_STATE
+    with pytest.raises(fm.FmError) as e:
+        p.append(0, S.gen_features(S.streams(1)["features"], 60, cfg.feat_dim), 0, oracle=False)
+    assert e.value.status == fm.FM_ERR_CONTEXT_FULL
+    with pytest.raises(fm.FmError) as e:
+        p.draft(0, cfg.vocab, 0, oracle=False)        # anchor out of range
+    assert e.value.status == fm.FM_ERR_INVALID_ARG
+    with pytest.raises(fm.FmError) as e:
+        p.draft(0, 1, 5, oracle=False)                # pos != length
+    assert e.value.status == fm.FM_ERR_STATE
+    with pytest.raises(fm.FmError) as e:
+        p.append(1, feats, 0, oracle=False)           # seq beyond max_seqs
+    assert e.value.status == fm.FM_ERR_INVALID_ARG
+    p.close()
