@@ -79,6 +79,16 @@ struct fm_handle {
   int32_t *tickets = nullptr;  // [0, H): self, [H, 2H): cross, [2H]: lm head
   int32_t *tok_tmp = nullptr;
 
+  // ---- captured chains ----
+  struct GraphEntry {
+    cudaGraphExec_t exec = nullptr;
+    StepParams *sp = nullptr;
+    int launches = 0;
+  };
+  std::unordered_map<uint64_t, GraphEntry> graphs;
+  cudaStream_t cap = nullptr;
+  bool use_graphs = true;
+
   // ---- diagnostics ----
   std::vector<ProfRec> prof;
   std::vector<cudaEvent_t> ev_pool;
@@ -210,6 +220,17 @@ StepParams *next_params(fm_handle *h, const StepParams &p, cudaStream_t s, fm_st
   }
   *st = FM_OK;
   return h->sp_dev + i;
+}
+
+// Upload p into a fixed device slot through the pinned ring (stream ordered).
+fm_status upload_params(fm_handle *h, const StepParams &p, StepParams *dst, cudaStream_t s) {
+  const int i = h->sp_next;
+  h->sp_next = (h->sp_next + 1) % kParamSlots;
+  cudaEventSynchronize(h->sp_ev[i]);
+  h->sp_host[i] = p;
+  CK(cudaMemcpyAsync(dst, h->sp_host + i, sizeof(StepParams), cudaMemcpyHostToDevice, s));
+  CK(cudaEventRecord(h->sp_ev[i], s));
+  return FM_OK;
 }
 
 cudaEvent_t pool_event(fm_handle *h) {
@@ -377,17 +398,9 @@ fm_status flashmap_append_rows(fm_handle *h, int seq, const StepParams *sp, int 
   return run_gemv(h, b, s, "gemv.kv_append", T);
 }
 
-fm_status flashmap_draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s) {
+fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams *sp, cudaStream_t s) {
   const fm_config &c = h->cfg;
   const int D = c.dim, B = c.block, Ht = c.target_dim, F = c.ff_dim, L = c.n_layers;
-  StepParams p{};
-  p.T = B;
-  p.pos = pos;
-  p.L = pos + 1;
-  p.anchor = anchor;
-  fm_status st;
-  const StepParams *sp = next_params(h, p, s, &st);
-  if (!sp) return st;
 
   // the anchor's context slot at pos: anchor_proj(E[anchor]) -> anchor_norm -> k / v of every layer
   GemvArgs a = gemv_base(h, h->w_ap, D, Ht, 1, sp);
@@ -556,7 +569,7 @@ fm_status flashmap_draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t
   hd.Y = h->Y;
   hd.ldy = Ht;
   TRY(run_gemv(h, hd, s, "gemv.head"));
-  return run_lmhead(h, h->Y, B, sp, tokens, nullptr, s);
+  return run_lmhead(h, h->Y, B, sp, nullptr, nullptr, s);
 }
 
 // ---------------------------------------------------------------- DFlash
@@ -598,17 +611,9 @@ fm_status dflash_append_rows(fm_handle *h, int seq, const StepParams *sp, cudaSt
   return run_gemv(h, b, s, "gemv.kv_append", 32);
 }
 
-fm_status dflash_draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s) {
+fm_status dflash_draft_launch(fm_handle *h, int seq, int pos, const StepParams *sp, cudaStream_t s) {
   const fm_config &c = h->cfg;
   const int d = c.dim, G = c.block, H = c.target_dim, F = c.ff_dim, L = c.n_layers;
-  StepParams p{};
-  p.T = G;
-  p.pos = pos;
-  p.L = pos;  // context rows 0 .. pos-1; the block's own keys go to rows pos .. pos+G-1
-  p.anchor = anchor;
-  fm_status st;
-  const StepParams *sp = next_params(h, p, s, &st);
-  if (!sp) return st;
 
   // block row 0 = tok_proj(E[anchor]) + block_pos[0]; rows 1.. are constants
   GemvArgs a = gemv_base(h, h->w_tok, d, H, 1, sp);
@@ -701,7 +706,75 @@ fm_status dflash_draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *
   op.Y = h->Y;
   op.ldy = H;
   TRY(run_gemv(h, op, s, "gemv.out_proj", G));
-  return run_lmhead(h, h->Y, G, sp, tokens, nullptr, s);
+  return run_lmhead(h, h->Y, G, sp, nullptr, nullptr, s);
+}
+
+// ---------------------------------------------------------------- chains
+
+// Run one chain of launches.  The first time a key is seen the chain is
+// captured into a CUDA graph on the capture stream (launches read their
+// per-call values from a fixed device slot); later calls upload the values
+// and replay the graph.  With FM_DEBUG_PROFILE the chain is launched directly.
+template <typename Enqueue>
+fm_status run_chain(fm_handle *h, uint64_t key, const StepParams &p, cudaStream_t s, Enqueue &&enqueue) {
+  if (h->use_graphs && !(h->debug & FM_DEBUG_PROFILE)) {
+    auto it = h->graphs.find(key);
+    if (it == h->graphs.end()) {
+      fm_handle::GraphEntry g;
+      TRY(dalloc(h, &g.sp, 1));
+      CK(cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeRelaxed));
+      const int before = h->last_launches;
+      fm_status st = enqueue(g.sp, h->cap);
+      cudaGraph_t graph = nullptr;
+      cudaError_t e = cudaStreamEndCapture(h->cap, &graph);
+      if (st != FM_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+      }
+      CK(e);
+      e = cudaGraphInstantiate(&g.exec, graph, 0);
+      cudaGraphDestroy(graph);
+      CK(e);
+      g.launches = h->last_launches - before;
+      h->last_launches = before;
+      it = h->graphs.emplace(key, g).first;
+    }
+    TRY(upload_params(h, p, it->second.sp, s));
+    CK(cudaGraphLaunch(it->second.exec, s));
+    h->last_launches += it->second.launches;
+    return FM_OK;
+  }
+  fm_status st;
+  const StepParams *sp = next_params(h, p, s, &st);
+  if (!sp) return st;
+  return enqueue(sp, s);
+}
+
+uint64_t chain_key(int kind, int seq, int T, int splits, int debug) {
+  return ((uint64_t)kind << 56) | ((uint64_t)(uint32_t)seq << 24) | ((uint64_t)T << 12) | ((uint64_t)splits << 2) |
+         (uint64_t)(debug & FM_DEBUG_KEEP_HIDDEN);
+}
+
+fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  StepParams p{};
+  p.T = c.block;
+  p.pos = pos;
+  p.anchor = anchor;
+  p.tokens = tokens;
+  int L_now;
+  if (c.variant == FM_VARIANT_FLASHMAP) {
+    p.L = pos + 1;
+    L_now = pos + 1;
+  } else {
+    p.L = pos;  // context rows 0 .. pos-1; the block's own keys go to rows pos .. pos+block-1
+    L_now = pos + c.block;
+  }
+  const uint64_t key = chain_key(1, seq, c.block, attn_splits(h, L_now), h->debug);
+  return run_chain(h, key, p, s, [&](const StepParams *sp, cudaStream_t st) {
+    return c.variant == FM_VARIANT_FLASHMAP ? flashmap_draft_launch(h, seq, pos, sp, st)
+                                            : dflash_draft_launch(h, seq, pos, sp, st);
+  });
 }
 
 // ---------------------------------------------------------------- create
@@ -766,6 +839,9 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   CK(cudaMallocHost(&h->sp_host, sizeof(StepParams) * kParamSlots));
   memset(h->sp_host, 0, sizeof(StepParams) * kParamSlots);
   for (int i = 0; i < kParamSlots; ++i) CK(cudaEventCreateWithFlags(&h->sp_ev[i], cudaEventDisableTiming));
+  CK(cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking));
+  const char *g = getenv("FM_NO_GRAPHS");
+  h->use_graphs = !(g && g[0] == '1');
   return FM_OK;
 }
 
@@ -991,13 +1067,11 @@ fm_status append_one(fm_handle *h, int32_t seq, const float *feats, int32_t n, i
     p.T = rows;
     p.start = start + r0;
     p.feats = feats + (size_t)r0 * FW;
-    fm_status st;
-    const StepParams *sp = next_params(h, p, s, &st);
-    if (!sp) return st;
-    if (h->cfg.variant == FM_VARIANT_FLASHMAP)
-      TRY(flashmap_append_rows(h, seq, sp, rows, s));
-    else
-      TRY(dflash_append_rows(h, seq, sp, s));
+    const uint64_t key = chain_key(2, seq, rows, 0, 0);
+    TRY(run_chain(h, key, p, s, [&](const StepParams *sp, cudaStream_t st) {
+      return h->cfg.variant == FM_VARIANT_FLASHMAP ? flashmap_append_rows(h, seq, sp, rows, st)
+                                                   : dflash_append_rows(h, seq, sp, st);
+    }));
   }
   h->length[seq] = start + n;
   return FM_OK;
@@ -1103,11 +1177,7 @@ fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const i
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int i = 0; i < n_seqs; ++i) {
-    int32_t *tk = tokens + (size_t)i * h->cfg.block;
-    if (h->cfg.variant == FM_VARIANT_FLASHMAP)
-      TRY(flashmap_draft_one(h, seq_ids[i], anchors[i], pos[i], tk, s));
-    else
-      TRY(dflash_draft_one(h, seq_ids[i], anchors[i], pos[i], tk, s));
+    TRY(draft_one(h, seq_ids[i], anchors[i], pos[i], tokens + (size_t)i * h->cfg.block, s));
   }
   return FM_OK;
 }
@@ -1262,6 +1332,9 @@ void fm_destroy(fm_handle *h) {
     cudaEventDestroy(r.e1);
   }
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+  for (auto &kv : h->graphs)
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+  if (h->cap) cudaStreamDestroy(h->cap);
   delete h;
 }
 

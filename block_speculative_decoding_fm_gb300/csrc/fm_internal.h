@@ -23,6 +23,7 @@ struct StepParams {
   int32_t start;    // append: first position
   int32_t pad0, pad1, pad2;
   const float *feats;  // append: feature rows [T][feat_dim]
+  int32_t *tokens;     // draft: where the argmax tokens go [T]
 };
 
 // --- skinny GEMV: Y[t][m] = sum_k A[t][k] W[m][k] for t < T <= 32 ----------
@@ -137,7 +138,7 @@ struct LmArgs {
   int32_t ldy;
   float2 *part;              // [gridDim.x][kMaxT] (value, index-as-float bits)
   int32_t *ticket;           // [1]
-  int32_t *tokens;           // [T]
+  int32_t *tokens;           // [T]; null: sp->tokens
   float *logits;             // optional [T][V] store (debug), null in the hot path
 };
 

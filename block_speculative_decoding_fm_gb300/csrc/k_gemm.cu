@@ -1,0 +1,400 @@
+// k_gemm.cu -- dense context-injection prefill on the 5th-generation tensor
+// cores: D[m][n] = sum_k A[m][k] B[n][k] with A the context rows (f16) and B a
+// weight matrix (f16 copy of the bf16 weights), both K-major.
+//
+// The page runs this as a 16 x 16 tiled WGSL GEMM (flashmap_drafter.js,
+// ``gemmBf16`` via ``runGemm`` for more than 17 rows).  Here it is a persistent,
+// warp-specialised sm_103a kernel:
+//   warp 0      one thread issues TMA (cp.async.bulk.tensor) loads of 128 x 64
+//               A tiles and 256 x 64 B tiles (128-byte swizzle) into a 4-stage
+//               shared-memory ring guarded by mbarriers;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 f32 accumulators) and
+//               one thread issues tcgen05.mma (kind::f16, M 128, N 256, K 16);
+//               tcgen05.commit frees ring stages and publishes accumulators;
+//   warps 2..5  read an accumulator with tcgen05.ld (one row per thread) while
+//               the next tile accumulates into the other buffer, and run the
+//               fused epilogue:
+//                 FC: C' = c * hidden_norm[n] -> f16 and per-row partial sum of
+//                     squares of c (the RMSNorm that follows fc);
+//                 KV: row scale 1/rms(c), per-head RMSNorm (k_norm) and
+//                     interleaved-pair RoPE on K heads, f16 stores into the
+//                     head-major caches of every layer at the row's position.
+// Every mbarrier wait is bounded by a clock budget; on expiry the kernel sets
+// an error flag, drains, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "dev_common.cuh"
+#include "fm_internal.h"
+#include "tc_gemm.h"
+
+namespace fm {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, ST = 4;
+constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE = A_BYTES + B_BYTES;
+constexpr int kThreads = 192;
+constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s) before a wait gives up
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait: false when the budget ran out or another role already gave up
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *err) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (clock64() - t0 > kWaitBudget) {
+      atomicExch(err, 1);
+      return false;
+    }
+    if (*reinterpret_cast<volatile int32_t *>(err)) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row atom
+  d |= (uint64_t)1 << 46;            // descriptor version for sm_100 family
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: D f32, A/B f16, both K-major, M 128, N 256
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+#define FM_TLD32(taddr, v)                                                                                          \
+  asm volatile(                                                                                                     \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19," \
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"                                                  \
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),           \
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),       \
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),     \
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])      \
+      : "r"(taddr))
+
+__device__ __forceinline__ void tld32(uint32_t taddr, float (&f)[32]) {
+  uint32_t v[32];
+  FM_TLD32(taddr, v);
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+}
+
+__device__ __forceinline__ void store_h8(__half *dst, const float *v) {
+  uint4 pk;
+  __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
+  __half2 h2 = __floats2half2_rn(v[4], v[5]), h3 = __floats2half2_rn(v[6], v[7]);
+  pk.x = *reinterpret_cast<uint32_t *>(&h0);
+  pk.y = *reinterpret_cast<uint32_t *>(&h1);
+  pk.z = *reinterpret_cast<uint32_t *>(&h2);
+  pk.w = *reinterpret_cast<uint32_t *>(&h3);
+  *reinterpret_cast<uint4 *>(dst) = pk;
+}
+
+__device__ void epilogue_fc(const TcGemmArgs &a, uint32_t taddr, int row, int n0, int nb) {
+  float ss = 0.f;
+  const bool live = row < a.M;
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    float v[32];
+    tld32(taddr + c0, v);
+    if (!live) continue;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      ss += v[j] * v[j];
+      v[j] *= __bfloat162float(a.colw[n0 + c0 + j]);
+    }
+    __half *dst = a.out16 + (size_t)row * a.ldo + n0 + c0;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) store_h8(dst + j, v + j);
+  }
+  if (live) a.row_st[(size_t)row * a.st_ld + nb] = ss;
+}
+
+__device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
+  const bool live = row < a.M;
+  const int seg = n0 / a.seg_cols;
+  const int layer = seg >> 1, kind = seg & 1;
+  const int hd = a.hd;
+  float rs = 1.f;
+  if (live) {
+    float s = 0.f;
+    for (int i = 0; i < a.in_st_n; ++i) s += a.in_st[(size_t)row * a.in_st_n + i];
+    rs = rsqrtf(s * a.inv_n + a.eps);
+  }
+  const int p = a.start + row;
+  for (int h0 = 0; h0 < BN; h0 += hd) {
+    const int head = ((n0 % a.seg_cols) + h0) / hd;
+    float r2 = 1.f;
+    if (kind == 0) {
+      float ss = 0.f;
+      for (int c0 = 0; c0 < hd; c0 += 32) {
+        float v[32];
+        tld32(taddr + h0 + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ss += (v[j] * rs) * (v[j] * rs);
+      }
+      r2 = rsqrtf(ss / (float)hd + a.qk_eps);
+    }
+    __half *dst = a.cache + (size_t)(layer * 2 + kind) * a.plane + ((size_t)head * a.max_ctx + p) * hd;
+    const __nv_bfloat16 *kw = a.kn_w + (size_t)layer * hd;
+    for (int c0 = 0; c0 < hd; c0 += 32) {
+      float v[32];
+      tld32(taddr + h0 + c0, v);
+      if (!live) continue;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= rs;
+      if (kind == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * __bfloat162float(kw[c0 + j]);
+        const float2 *rp = a.rope + (size_t)p * (hd >> 1) + (c0 >> 1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 cs = rp[i];
+          const float x0 = v[2 * i], x1 = v[2 * i + 1];
+          v[2 * i] = x0 * cs.x - x1 * cs.y;
+          v[2 * i + 1] = x1 * cs.x + x0 * cs.y;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) store_h8(dst + c0 + j, v + j);
+    }
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bars = base + ST * STAGE;
+  auto full = [&](int s) { return bars + 8 * s; };
+  auto empty = [&](int s) { return bars + 8 * (ST + s); };
+  auto tfull = [&](int b) { return bars + 8 * (2 * ST + b); };
+  auto tempty = [&](int b) { return bars + 8 * (2 * ST + 2 + b); };
+  const uint32_t tslot = bars + 8 * (2 * ST + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 128);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(tslot) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = lds32(tslot);
+
+  pdl_trigger();
+  pdl_wait();
+
+  const int n_nb = a.N / BN;
+  const int n_tiles = ((a.M + BM - 1) / BM) * n_nb;
+  const int nk = a.K / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int mb = tile / n_nb, nb = tile - mb * n_nb;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % ST;
+          if (!mbar_wait(empty(s), ((it / ST) & 1) ^ 1, a.err)) { ok = false; break; }
+          const uint32_t sa = base + s * STAGE, sb = sa + A_BYTES;
+          mbar_expect_tx(full(s), STAGE);
+          tma_load_2d(sa, &a.tma_a, kb * BK, mb * BM, full(s));
+          tma_load_2d(sb, &a.tma_b, kb * BK, nb * BN, full(s));
+        }
+      }
+      // drain: the last stages issued must have landed before the CTA leaves
+      for (uint32_t j = it > ST ? it - ST : 0; j < it; ++j) mbar_wait(full(j % ST), (j / ST) & 1, a.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+        const int b = tc & 1;
+        if (!mbar_wait(tempty(b), ((tc >> 1) & 1) ^ 1, a.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * BN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % ST;
+          if (!mbar_wait(full(s), (it / ST) & 1, a.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = base + s * STAGE, sb = sa + A_BYTES;
+          const uint64_t ad = sdesc(sa), bd = sdesc(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) mma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, (kb | kk) ? 1u : 0u);
+          mma_commit(empty(s));
+        }
+        if (ok) mma_commit(tfull(b));
+      }
+    }
+  } else {
+    const int quad = warp & 3;  // TMEM lanes 32 * quad .. + 31 belong to this warp
+    const int rl = quad * 32 + lane;
+    uint32_t tc = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tc) {
+      const int b = tc & 1;
+      if (!mbar_wait(tfull(b), (tc >> 1) & 1, a.err)) break;
+      tc_fence_after();
+      const int mb = tile / n_nb, nb = tile - mb * n_nb;
+      const uint32_t taddr = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
+      if (a.epi == TC_EPI_FC)
+        epilogue_fc(a, taddr, mb * BM + rl, nb * BN, nb);
+      else
+        epilogue_kv(a, taddr, mb * BM + rl, nb * BN);
+      tc_fence_before();
+      mbar_arrive(tempty(b));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
+  }
+}
+
+__global__ void f32_to_f16_kernel(const float4 *__restrict__ in, uint2 *__restrict__ out, size_t n4) {
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  pdl_trigger();
+  pdl_wait();
+  for (; i < n4; i += stride) {
+    const float4 v = __ldcs(in + i);
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t *>(&a);
+    o.y = *reinterpret_cast<uint32_t *>(&b);
+    out[i] = o;
+  }
+}
+
+__global__ void bf16_to_f16_kernel(const __nv_bfloat16 *__restrict__ in, __half *__restrict__ out, size_t n) {
+  const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (i < n) out[i] = __float2half_rn(__bfloat162float(in[i]));
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_tma_f16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+size_t tc_gemm_smem_bytes() { return (size_t)ST * STAGE + 1024 + 256; }
+
+cudaError_t launch_tc_gemm(const TcGemmArgs &a, int n_sm, cudaStream_t s) {
+  const int n_tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
+  const int grid = n_tiles < n_sm ? n_tiles : n_sm;
+  const size_t smem = tc_gemm_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, a);
+}
+
+cudaError_t launch_f32_to_f16(const float *in, __half *out, size_t n, int n_sm, cudaStream_t s) {
+  const size_t n4 = n / 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_sm * 4, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, f32_to_f16_kernel, reinterpret_cast<const float4 *>(in),
+                            reinterpret_cast<uint2 *>(out), n4);
+}
+
+cudaError_t launch_bf16_to_f16(const __nv_bfloat16 *in, __half *out, size_t n, cudaStream_t s) {
+  bf16_to_f16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace fm

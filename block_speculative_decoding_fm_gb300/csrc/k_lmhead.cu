@@ -244,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_kernel(const __grid_consta
       const int pi = __float_as_int(p.y);
       if (better(p.x, pi, v, i)) { v = p.x; i = pi; }
     }
-    a.tokens[t] = i == 0x7fffffff ? -1 : i;
+    int32_t *out = a.tokens ? a.tokens : a.sp->tokens;
+    out[t] = i == 0x7fffffff ? -1 : i;
   }
 }
 
