@@ -15,6 +15,7 @@
 
 #include "../../include/fm.h"
 #include "fm_internal.h"
+#include "tc_gemm.h"
 
 using namespace fm;
 
@@ -79,6 +80,14 @@ struct fm_handle {
   int32_t *tickets = nullptr;  // [0, H): self, [H, 2H): cross, [2H]: lm head
   int32_t *tok_tmp = nullptr;
 
+  // ---- dense prefill (tcgen05) ----
+  __half *w_fc16 = nullptr, *w_kv16 = nullptr;  // f16 copies of fc and the stacked cross K/V
+  __half *pf_a = nullptr, *pf_c = nullptr;       // scratch: f16 feature rows, f16 weighted fc output
+  float *pf_st = nullptr;                         // per-row partial sums of squares
+  int32_t *pf_err = nullptr;
+  int pf_rows = 0;                                // rows the scratch holds
+  CUtensorMap tm_wfc{}, tm_wkv{}, tm_c{};
+
   // ---- captured chains ----
   struct GraphEntry {
     cudaGraphExec_t exec = nullptr;
@@ -88,6 +97,7 @@ struct fm_handle {
   std::unordered_map<uint64_t, GraphEntry> graphs;
   cudaStream_t cap = nullptr;
   bool use_graphs = true;
+  bool use_prefill = true;
 
   // ---- diagnostics ----
   std::vector<ProfRec> prof;
@@ -709,6 +719,102 @@ fm_status dflash_draft_launch(fm_handle *h, int seq, int pos, const StepParams *
   return run_lmhead(h, h->Y, G, sp, nullptr, nullptr, s);
 }
 
+// ---------------------------------------------------------------- dense prefill
+
+constexpr int kPrefillMin = 128;     // appends of at least this many rows use the tensor-core GEMMs
+constexpr int kPrefillChunk = 16384; // rows per pass (bounds the scratch)
+
+fm_status prefill_setup(fm_handle *h, cudaStream_t s) {
+  if (h->pf_rows) return FM_OK;
+  const fm_config &c = h->cfg;
+  const int D = c.dim, FW = c.n_taps * c.target_dim, L = c.n_layers;
+  if (D % 256) return fail(h, FM_ERR_UNSUPPORTED, "dense prefill needs dim % 256 == 0");
+  const int rows = c.max_ctx < kPrefillChunk ? c.max_ctx : kPrefillChunk;
+  TRY(dalloc(h, &h->w_fc16, (size_t)D * FW));
+  TRY(dalloc(h, &h->w_kv16, (size_t)L * 2 * D * D));
+  CK(launch_bf16_to_f16(h->w_fc, h->w_fc16, (size_t)D * FW, s));
+  CK(launch_bf16_to_f16(h->w_kvall, h->w_kv16, (size_t)L * 2 * D * D, s));
+  TRY(dalloc(h, &h->pf_a, (size_t)rows * FW));
+  TRY(dalloc(h, &h->pf_c, (size_t)rows * D));
+  TRY(dalloc(h, &h->pf_st, (size_t)rows * (D / 256)));
+  TRY(dalloc(h, &h->pf_err, 4));
+  CK(cudaMemsetAsync(h->pf_err, 0, 4, s));
+  if (!make_tma_f16(&h->tm_wfc, h->w_fc16, D, FW, 256) || !make_tma_f16(&h->tm_wkv, h->w_kv16, (uint64_t)L * 2 * D, D, 256))
+    return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+  h->pf_rows = rows;
+  return FM_OK;
+}
+
+// fc -> hidden_norm -> all layers' k / v for rows start .. start+n-1 on tcgen05
+fm_status flashmap_prefill(fm_handle *h, int seq, const float *feats, int n, int start, cudaStream_t s) {
+  TRY(prefill_setup(h, s));
+  const fm_config &c = h->cfg;
+  const int D = c.dim, FW = c.n_taps * c.target_dim, L = c.n_layers;
+  for (int r0 = 0; r0 < n; r0 += h->pf_rows) {
+    const int R = n - r0 < h->pf_rows ? n - r0 : h->pf_rows;
+    {
+      ProfScope ps(h, s, "prefill.f32_to_f16", (double)R * FW * 6);
+      CK(launch_f32_to_f16(feats + (size_t)r0 * FW, h->pf_a, (size_t)R * FW, h->n_sm, s));
+      ++h->last_launches;
+    }
+    TcGemmArgs g;
+    memset(&g, 0, sizeof g);
+    if (!make_tma_f16(&g.tma_a, h->pf_a, R, FW, 128)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+    g.tma_b = h->tm_wfc;
+    g.M = R;
+    g.N = D;
+    g.K = FW;
+    g.epi = TC_EPI_FC;
+    g.err = h->pf_err;
+    g.colw = h->w_hn;
+    g.out16 = h->pf_c;
+    g.ldo = D;
+    g.row_st = h->pf_st;
+    g.st_ld = D / 256;
+    {
+      ProfScope ps(h, s, "prefill.gemm_fc", 2.0 * R * D * FW);
+      CK(launch_tc_gemm(g, h->n_sm, s));
+      ++h->last_launches;
+    }
+    TcGemmArgs k;
+    memset(&k, 0, sizeof k);
+    if (!make_tma_f16(&k.tma_a, h->pf_c, R, D, 128)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+    k.tma_b = h->tm_wkv;
+    k.M = R;
+    k.N = L * 2 * D;
+    k.K = D;
+    k.epi = TC_EPI_KV;
+    k.err = h->pf_err;
+    k.in_st = h->pf_st;
+    k.in_st_n = D / 256;
+    k.eps = c.rms_eps;
+    k.inv_n = 1.0f / D;
+    k.seg_cols = D;
+    k.hd = c.head_dim;
+    k.max_ctx = c.max_ctx;
+    k.start = start + r0;
+    k.rope = h->rope;
+    k.qk_eps = c.qk_eps;
+    k.kn_w = h->w_ckn;
+    k.cache = h->kv(seq, 0).k;
+    k.plane = h->cache_plane;
+    {
+      ProfScope ps(h, s, "prefill.gemm_kv", 2.0 * R * D * (2.0 * L * D));
+      CK(launch_tc_gemm(k, h->n_sm, s));
+      ++h->last_launches;
+    }
+  }
+  // a bounded wait that gave up is reported, never hung
+  int32_t flag = 0;
+  CK(cudaMemcpyAsync(&flag, h->pf_err, 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  if (flag) {
+    cudaMemsetAsync(h->pf_err, 0, 4, s);
+    return fail(h, FM_ERR_TIMEOUT, "prefill GEMM: a pipeline wait exceeded its budget");
+  }
+  return FM_OK;
+}
+
 // ---------------------------------------------------------------- chains
 
 // Run one chain of launches.  The first time a key is seen the chain is
@@ -842,6 +948,8 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   CK(cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking));
   const char *g = getenv("FM_NO_GRAPHS");
   h->use_graphs = !(g && g[0] == '1');
+  const char *pf = getenv("FM_NO_TC_PREFILL");
+  h->use_prefill = !(pf && pf[0] == '1');
   return FM_OK;
 }
 
@@ -1061,6 +1169,11 @@ fm_status append_checks(fm_handle *h, int32_t seq, const float *feats, int32_t n
 
 fm_status append_one(fm_handle *h, int32_t seq, const float *feats, int32_t n, int32_t start, cudaStream_t s) {
   const int FW = h->cfg.n_taps * h->cfg.target_dim;
+  if (h->cfg.variant == FM_VARIANT_FLASHMAP && n >= kPrefillMin && h->cfg.dim % 256 == 0 && h->use_prefill) {
+    TRY(flashmap_prefill(h, seq, feats, n, start, s));
+    h->length[seq] = start + n;
+    return FM_OK;
+  }
   for (int r0 = 0; r0 < n; r0 += kMaxT) {
     const int rows = n - r0 < kMaxT ? n - r0 : kMaxT;
     StepParams p{};

@@ -55,8 +55,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// bounded wait: false when the budget ran out or another role already gave up
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *err) {
+// bounded wait: false when the budget ran out or (honor_err) another role already gave up
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *err, bool honor_err = true) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
@@ -64,7 +64,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
       atomicExch(err, 1);
       return false;
     }
-    if (*reinterpret_cast<volatile int32_t *>(err)) return false;
+    if (honor_err && *reinterpret_cast<volatile int32_t *>(err)) return false;
   }
   return true;
 }
@@ -160,7 +160,7 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
   float rs = 1.f;
   if (live) {
     float s = 0.f;
-    for (int i = 0; i < a.in_st_n; ++i) s += a.in_st[(size_t)row * a.in_st_n + i];
+    for (int i = 0; i < a.in_st_n; ++i) s += __ldcg(a.in_st + (size_t)row * a.in_st_n + i);
     rs = rsqrtf(s * a.inv_n + a.eps);
   }
   const int p = a.start + row;
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
       }
       // drain: the last stages issued must have landed before the CTA leaves
-      for (uint32_t j = it > ST ? it - ST : 0; j < it; ++j) mbar_wait(full(j % ST), (j / ST) & 1, a.err);
+      for (uint32_t j = it > ST ? it - ST : 0; j < it; ++j) mbar_wait(full(j % ST), (j / ST) & 1, a.err, false);
     }
   } else if (warp == 1) {
     if (lane == 0) {

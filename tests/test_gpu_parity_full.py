@@ -73,3 +73,24 @@ def test_dflash_cycles_full_size():
         pos += n_acc + 1
         anchor = bonus
     p.close()
+
+
+def test_long_context_prefill_and_draft():
+    """32768 context rows through the dense prefill, then one draft over 32769 keys."""
+    cfg = S.flashmap_4b_config(max_ctx=32768 + 64)
+    p = Pair(cfg, 1003)
+    fr = S.streams(1003)["features"]
+    feats = S.gen_features(fr, 32768, cfg.feat_dim)
+    p.append(0, feats, 0)
+    st = p.state(0)
+    rng = np.random.default_rng(3)
+    rows = np.sort(rng.choice(32768, 64, replace=False))
+    for l in range(cfg.n_layers):
+        for which, want in (("k", st.k[l]), ("v", st.v[l])):
+            got = p.cache(0, l, which)
+            assert rel_l2(got[rows], want[rows]) < 1e-3, (l, which)
+    anchor = S.gen_anchor(S.streams(1003)["tokens"], cfg.vocab)
+    got, ref = p.draft(0, anchor, 32768)
+    assert rel_l2(p.head_out(), ref.head_out) < REL_L2
+    assert tokens_match(got, ref.tokens, ref.logits), (got, ref.tokens)
+    p.close()

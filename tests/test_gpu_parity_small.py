@@ -50,9 +50,12 @@ def check_cache(p: Pair, seq, rows):
             got = p.cache(seq, l, which)[:rows]
             want = ref[:rows]
             assert rel_l2(got, want) < 1e-3, (l, which, rel_l2(got, want))
-            # the f16 store matches the oracle's f16 rounding up to one step
-            step = np.abs(want) * 2.0 ** -10 + 2.0 ** -24
-            assert np.all(np.abs(got - want) <= step + 1e-7), (l, which)
+            # the f16 store matches the oracle's f16 rounding up to one step of the
+            # element plus a small fraction of the row's scale (f32 vs f64 before rounding)
+            rms = np.sqrt(np.mean(want.astype(np.float64) ** 2, axis=1, keepdims=True))
+            step = np.abs(want) * 2.0 ** -10 + 1e-4 * rms + 2.0 ** -24
+            bad = np.abs(got - want) > step
+            assert not bad.any(), (l, which, int(bad.sum()), float(np.abs(got - want)[bad].max()))
 
 
 @pytest.mark.parametrize("lm", [S.LM_BF16, S.LM_Q8_0])
@@ -185,4 +188,22 @@ def test_errors_are_reported_not_raised_on_device():
     with pytest.raises(fm.FmError) as e:
         p.append(1, feats, 0, oracle=False)           # seq beyond max_seqs
     assert e.value.status == fm.FM_ERR_INVALID_ARG
+    p.close()
+
+
+def test_tiny_flashmap_dense_prefill_tcgen05():
+    """Appends of >= 128 rows run the tcgen05 GEMMs (f16 operands): cache rows
+    and the draft that reads them stay within the parity bars."""
+    cfg = S.tiny_config(max_ctx=640)
+    p = Pair(cfg, 1009)
+    feats = S.gen_features(S.streams(1009)["features"], 600, cfg.feat_dim)
+    p.append(0, feats[:300], 0)             # one dense pass with a ragged last M tile (300 = 2 * 128 + 44)
+    p.append(0, feats[300:557], 300)        # a second pass that starts mid-context
+    st = p.state(0)
+    for l in range(cfg.n_layers):
+        for which, want in (("k", st.k[l]), ("v", st.v[l])):
+            got = p.cache(0, l, which)[:557]
+            assert rel_l2(got, want[:557]) < 1e-3, (l, which, rel_l2(got, want[:557]))
+    got, ref = p.draft(0, 123, 557)
+    check_draft(p, got, ref)
     p.close()
