@@ -88,6 +88,9 @@ struct fm_handle {
   int pf_rows = 0;                                // rows the scratch holds
   CUtensorMap tm_wfc{}, tm_wkv{}, tm_c{};
 
+  // ---- deferred K/V projection of the last short append ----
+  int pend_seq = -1, pend_start = 0, pend_n = 0;
+
   // ---- captured chains ----
   struct GraphEntry {
     cudaGraphExec_t exec = nullptr;
@@ -98,6 +101,7 @@ struct fm_handle {
   cudaStream_t cap = nullptr;
   bool use_graphs = true;
   bool use_prefill = true;
+  bool use_defer = true;
 
   // ---- diagnostics ----
   std::vector<ProfRec> prof;
@@ -373,8 +377,8 @@ fm_status run_lmhead(fm_handle *h, const float *Y, int T, const StepParams *sp, 
 
 // ---------------------------------------------------------------- FlashMap
 
-// fc -> hidden_norm -> all layers' k / v (k_norm + RoPE) -> f16 cache rows
-fm_status flashmap_append_rows(fm_handle *h, int seq, const StepParams *sp, int T, cudaStream_t s) {
+// fc (no bias) on the appended feature rows -> ctx rows + their row statistics
+fm_status flashmap_fc_rows(fm_handle *h, const StepParams *sp, int T, cudaStream_t s) {
   const fm_config &c = h->cfg;
   const int D = c.dim, FW = c.n_taps * c.target_dim;
   GemvArgs a = gemv_base(h, h->w_fc, D, FW, 0, sp);
@@ -385,30 +389,50 @@ fm_status flashmap_append_rows(fm_handle *h, int seq, const StepParams *sp, int 
   a.Y = h->ctx;
   a.ldy = D;
   a.out_st = h->st_c;
-  TRY(run_gemv(h, a, s, "gemv.fc", T));
+  return run_gemv(h, a, s, "gemv.fc", T);
+}
 
-  GemvArgs b = gemv_base(h, h->w_kvall, c.n_layers * 2 * D, D, 0, sp);
+// The stacked cross K/V of every layer over normalised rows: rows < split are
+// ctx rows (hidden_norm, positions start + t); with an anchor row (split > 0 and
+// T = split + 1) the last row is the anchor (anchor_norm, position pos).
+GemvArgs flashmap_kv_args(fm_handle *h, int seq, const StepParams *sp, int T_const, int split) {
+  const fm_config &c = h->cfg;
+  const int D = c.dim, L = c.n_layers;
+  GemvArgs b = gemv_base(h, h->w_kvall, L * 2 * D, D, T_const, sp);
   b.amode = A_RMS;
-  b.X = h->ctx;
+  b.X = split > 0 || T_const == 0 ? h->ctx : h->actx;
   b.ldx = D;
-  b.st = h->st_c;
+  b.st = split > 0 || T_const == 0 ? h->st_c : h->st_a;
   b.st_tiles = D / kTile;
-  b.nw = h->w_hn;
+  b.nw = split > 0 || T_const == 0 ? h->w_hn : h->w_an;
   b.inv_n = 1.0f / D;
+  if (split > 0) {
+    b.split = split;
+    b.X2 = h->actx;
+    b.st2 = h->st_a;
+    b.nw_alt = h->w_an;
+    b.pos_src = 3;
+  } else {
+    b.pos_src = T_const == 0 ? 1 : 0;
+  }
   b.emode = E_SEGS;
   b.seg_rows = D;
-  b.n_segs = 2 * c.n_layers;
-  b.pos_src = 1;
-  b.pos_add = 0;
-  for (int l = 0; l < c.n_layers; ++l) {
+  b.n_segs = 2 * L;
+  for (int l = 0; l < L; ++l) {
     Seg2 kv = h->kv(seq, l);
     b.segs[2 * l] = {SEG_CACHE, 0, 1, 0, h->w_ckn + (size_t)l * c.head_dim, kv.k};
     b.segs[2 * l + 1] = {SEG_CACHE, 0, 0, 0, nullptr, kv.v};
   }
-  return run_gemv(h, b, s, "gemv.kv_append", T);
+  return b;
 }
 
-fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams *sp, cudaStream_t s) {
+// fc -> hidden_norm -> all layers' k / v (k_norm + RoPE) -> f16 cache rows
+fm_status flashmap_append_rows(fm_handle *h, int seq, const StepParams *sp, int T, cudaStream_t s) {
+  TRY(flashmap_fc_rows(h, sp, T, s));
+  return run_gemv(h, flashmap_kv_args(h, seq, sp, 0, 0), s, "gemv.kv_append", T);
+}
+
+fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams *sp, int n_pend, cudaStream_t s) {
   const fm_config &c = h->cfg;
   const int D = c.dim, B = c.block, Ht = c.target_dim, F = c.ff_dim, L = c.n_layers;
 
@@ -425,24 +449,9 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
   a.out_st = h->st_a;
   TRY(run_gemv(h, a, s, "gemv.anchor_proj", 1));
 
-  GemvArgs kvp = gemv_base(h, h->w_kvall, L * 2 * D, D, 1, sp);
-  kvp.amode = A_RMS;
-  kvp.X = h->actx;
-  kvp.ldx = D;
-  kvp.st = h->st_a;
-  kvp.st_tiles = D / kTile;
-  kvp.nw = h->w_an;
-  kvp.inv_n = 1.0f / D;
-  kvp.emode = E_SEGS;
-  kvp.seg_rows = D;
-  kvp.n_segs = 2 * L;
-  kvp.pos_src = 0;
-  for (int l = 0; l < L; ++l) {
-    Seg2 kv = h->kv(seq, l);
-    kvp.segs[2 * l] = {SEG_CACHE, 0, 1, 0, h->w_ckn + (size_t)l * c.head_dim, kv.k};
-    kvp.segs[2 * l + 1] = {SEG_CACHE, 0, 0, 0, nullptr, kv.v};
-  }
-  TRY(run_gemv(h, kvp, s, "gemv.kv_anchor", 1));
+  // the pending appended rows (deferred) and the anchor row share one pass over the cross K/V weights
+  GemvArgs kvp = flashmap_kv_args(h, seq, sp, n_pend + 1, n_pend);
+  TRY(run_gemv(h, kvp, s, n_pend ? "gemv.kv_fused" : "gemv.kv_anchor", n_pend + 1));
 
   const float attn_scale = (float)(1.0 / std::sqrt((double)c.head_dim));
   for (int l = 0; l < L; ++l) {
@@ -861,9 +870,34 @@ uint64_t chain_key(int kind, int seq, int T, int splits, int debug) {
          (uint64_t)(debug & FM_DEBUG_KEEP_HIDDEN);
 }
 
+// Project the K/V rows of a deferred append (when no draft of that sequence
+// follows it directly).
+fm_status flush_pending(fm_handle *h, cudaStream_t s) {
+  if (h->pend_seq < 0) return FM_OK;
+  const int seq = h->pend_seq, n = h->pend_n;
+  StepParams p{};
+  p.T = n;
+  p.start = h->pend_start;
+  h->pend_seq = -1;
+  return run_chain(h, chain_key(4, seq, n, 0, 0), p, s, [&](const StepParams *sp, cudaStream_t st) {
+    return run_gemv(h, flashmap_kv_args(h, seq, sp, 0, 0), st, "gemv.kv_append", n);
+  });
+}
+
 fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s) {
   const fm_config &c = h->cfg;
+  int n_pend = 0;
+  if (h->pend_seq >= 0) {
+    if (h->pend_seq == seq && h->pend_start + h->pend_n == pos && c.variant == FM_VARIANT_FLASHMAP &&
+        h->pend_n + 1 <= kMaxT) {
+      n_pend = h->pend_n;
+    } else {
+      TRY(flush_pending(h, s));
+    }
+  }
   StepParams p{};
+  p.start = n_pend ? h->pend_start : 0;
+  if (n_pend) h->pend_seq = -1;
   p.T = c.block;
   p.pos = pos;
   p.anchor = anchor;
@@ -876,9 +910,9 @@ fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens,
     p.L = pos;  // context rows 0 .. pos-1; the block's own keys go to rows pos .. pos+block-1
     L_now = pos + c.block;
   }
-  const uint64_t key = chain_key(1, seq, c.block, attn_splits(h, L_now), h->debug);
+  const uint64_t key = chain_key(1, seq, c.block + 64 * n_pend, attn_splits(h, L_now), h->debug);
   return run_chain(h, key, p, s, [&](const StepParams *sp, cudaStream_t st) {
-    return c.variant == FM_VARIANT_FLASHMAP ? flashmap_draft_launch(h, seq, pos, sp, st)
+    return c.variant == FM_VARIANT_FLASHMAP ? flashmap_draft_launch(h, seq, pos, sp, n_pend, st)
                                             : dflash_draft_launch(h, seq, pos, sp, st);
   });
 }
@@ -948,6 +982,8 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   CK(cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking));
   const char *g = getenv("FM_NO_GRAPHS");
   h->use_graphs = !(g && g[0] == '1');
+  const char *df = getenv("FM_NO_DEFER");
+  h->use_defer = !(df && df[0] == '1');
   const char *pf = getenv("FM_NO_TC_PREFILL");
   h->use_prefill = !(pf && pf[0] == '1');
   return FM_OK;
@@ -1169,6 +1205,22 @@ fm_status append_checks(fm_handle *h, int32_t seq, const float *feats, int32_t n
 
 fm_status append_one(fm_handle *h, int32_t seq, const float *feats, int32_t n, int32_t start, cudaStream_t s) {
   const int FW = h->cfg.n_taps * h->cfg.target_dim;
+  TRY(flush_pending(h, s));
+  if (h->cfg.variant == FM_VARIANT_FLASHMAP && n > 0 && n < kMaxT && h->use_defer) {
+    // fc now; the K/V projection joins the next draft of this sequence
+    StepParams p{};
+    p.T = n;
+    p.start = start;
+    p.feats = feats;
+    TRY(run_chain(h, chain_key(3, seq, n, 0, 0), p, s, [&](const StepParams *sp, cudaStream_t st) {
+      return flashmap_fc_rows(h, sp, n, st);
+    }));
+    h->pend_seq = seq;
+    h->pend_start = start;
+    h->pend_n = n;
+    h->length[seq] = start + n;
+    return FM_OK;
+  }
   if (h->cfg.variant == FM_VARIANT_FLASHMAP && n >= kPrefillMin && h->cfg.dim % 256 == 0 && h->use_prefill) {
     TRY(flashmap_prefill(h, seq, feats, n, start, s));
     h->length[seq] = start + n;
@@ -1345,6 +1397,7 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
     case FM_DEBUG_CACHE_K:
     case FM_DEBUG_CACHE_V: {
       TRY(check_seq(h, seq));
+      TRY(flush_pending(h, s));
       if (index < 0 || index >= c.n_layers) return fail(h, FM_ERR_INVALID_ARG, "layer %d", index);
       Seg2 kv = h->kv(seq, index);
       src = what == FM_DEBUG_CACHE_K ? kv.k : kv.v;

@@ -77,6 +77,12 @@ struct GemvArgs {
   const __nv_bfloat16 *nw2;// A_RMS2 second weight; + (m0 / nw_rows) * K for per-layer weights
   int32_t nw_rows;         // rows sharing one second norm weight (0 = one weight for all)
   const float *sc, *sh;    // A_LNMOD scale / shift [K]
+  // A_RMS with two row sources: rows t >= split come from X2 (row t - split)
+  // with their own statistics st2 and norm weight nw_alt
+  int32_t split;           // 0 = one source
+  const float *X2;
+  const float2 *st2;
+  const __nv_bfloat16 *nw_alt;
   float eps, inv_n;
   const int8_t *tq;        // A_ROW_Q8: int8 plane [V][K]
   const __half *tscale;    // A_ROW_Q8: scales [V / 128][K / 32][128]
@@ -94,7 +100,7 @@ struct GemvArgs {
   int32_t ldr;
   // E_SEGS
   int32_t seg_rows, n_segs, hd, max_ctx;
-  int32_t pos_src;            // 0: sp->pos, 1: sp->start, 2: sp->L
+  int32_t pos_src;            // 0: sp->pos, 1: sp->start, 2: sp->L, 3: t < split ? sp->start + t : sp->pos
   int32_t pos_add;            // position of row t = base + pos_add + t
   const float2 *rope;         // [positions][hd / 2] (cos, sin)
   float qk_eps;

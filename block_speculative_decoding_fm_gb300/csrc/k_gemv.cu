@@ -64,10 +64,12 @@ __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
   if (t < kMaxT) {
     float m = 0.f, r = 1.f;
     if (t < T && (a.amode == A_RMS || a.amode == A_LNMOD || a.amode == A_RMS2)) {
-      const int ts = a.st_bcast ? 0 : t;
+      const bool second = a.split > 0 && t >= a.split;
+      const int ts = a.st_bcast ? 0 : (second ? t - a.split : t);
+      const float2 *stp = second ? a.st2 : a.st;
       double s1 = 0.0, s2 = 0.0;
       for (int i = 0; i < a.st_tiles; ++i) {
-        const float2 v = __ldcg(a.st + i * kMaxT + ts);
+        const float2 v = __ldcg(stp + i * kMaxT + ts);
         s1 += v.x;
         s2 += v.y;
       }
@@ -120,12 +122,15 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, int T, int m0, int k0,
           }
         }
       } else {
-        const float4 x = __ldcg(reinterpret_cast<const float4 *>(X + (size_t)t * a.ldx + k));
+        const bool second = a.split > 0 && t >= a.split;
+        const float *xr = second ? a.X2 + (size_t)(t - a.split) * a.ldx : X + (size_t)t * a.ldx;
+        const float4 x = __ldcg(reinterpret_cast<const float4 *>(xr + k));
         v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
         if (a.amode == A_RMS) {
           const float r = s.stat_rs[t];
+          const __nv_bfloat16 *w = second ? a.nw_alt : nw;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v[e] = v[e] * r * __bfloat162float(nw[k + e]);
+          for (int e = 0; e < 4; ++e) v[e] = v[e] * r * __bfloat162float(w[k + e]);
         } else if (a.amode == A_RMS2) {
           const float r1 = s.stat_mu[t], r2 = s.stat_rs[t];
 #pragma unroll
@@ -188,6 +193,7 @@ __device__ __forceinline__ void compute_chunk(uint32_t wst, const Smem &s, int l
 }
 
 __device__ __forceinline__ int row_pos(const GemvArgs &a, int t) {
+  if (a.pos_src == 3) return t < a.split ? a.sp->start + t : a.sp->pos + (t - a.split);
   const int base = a.pos_src == 0 ? a.sp->pos : a.pos_src == 1 ? a.sp->start : a.sp->L;
   return base + a.pos_add + t;
 }

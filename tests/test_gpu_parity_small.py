@@ -207,3 +207,36 @@ def test_tiny_flashmap_dense_prefill_tcgen05():
     got, ref = p.draft(0, 123, 557)
     check_draft(p, got, ref)
     p.close()
+
+
+def test_tiny_flashmap_batched_sequences():
+    """Several independent sequences with ragged lengths: one batched append
+    and one batched draft match the oracle run per sequence."""
+    import torch
+    import block_speculative_decoding_fm_gb300 as fm
+    cfg = S.tiny_config(max_ctx=200).replace(max_seqs=4)
+    p = Pair(cfg, 1010)
+    fr = S.streams(1010)["features"]
+    lens = [5, 64, 37, 130]
+    for s, n in enumerate(lens):
+        p.append(s, S.gen_features(fr, n, cfg.feat_dim), 0)
+    # batched append of acc + 1 rows per sequence (rows concatenated in sequence order)
+    extra = [1, 17, 3, 9]
+    rows = [S.gen_features(fr, n, cfg.feat_dim) for n in extra]
+    feats = torch.from_numpy(np.concatenate(rows)).cuda()
+    ids = [2, 0, 3, 1]
+    fm.fm_context_append_batched(p.h, ids, feats, [extra[0], extra[1], extra[2], extra[3]],
+                                 [lens[i] for i in ids])
+    for j, s in enumerate(ids):
+        p.oracle.context_append(p.state(s), rows[j], lens[s])
+    pos = [lens[s] + extra[ids.index(s)] for s in range(4)]
+    anchors = [11, 22, 33, 44]
+    tok = torch.zeros((4, cfg.block), dtype=torch.int32, device="cuda")
+    fm.fm_draft(p.h, [0, 1, 2, 3], anchors, pos, tok)
+    torch.cuda.synchronize()
+    got = tok.cpu().numpy()
+    for s in range(4):
+        ref = p.oracle.draft(p.state(s), anchors[s], pos[s])
+        assert tokens_match(got[s], ref.tokens, ref.logits), (s, got[s], ref.tokens)
+        assert fm.fm_get_length(p.h, s) == pos[s]
+    p.close()
