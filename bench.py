@@ -41,6 +41,8 @@ def parse():
     p.add_argument("--workload", default="flashmap4b", choices=["flashmap4b", "prefill", "dflash", "tiny"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill rows/s figure")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    p.add_argument("--no-kprof", action="store_true", help="skip the per-kernel timing pass")
     return p.parse_args()
 
 
@@ -305,27 +307,31 @@ def run_ours(args):
 
     # end to end through the C ABI with host buffers (H2D of the feature rows,
     # D2H of the drafted tokens inside the timed region)
-    for _ in range(3):
-        w.step_e2e()
-    ms_e2e = barrier_max(ws, time_steps(torch, w.step_e2e, args.steps))
-    e2e = {"value": args.steps * ws / (ms_e2e / 1000), "unit": "steps/s", "h2d_bytes_per_step": w.e2e_h2d,
-           "d2h_bytes_per_step": w.e2e_d2h}
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(3):
+            w.step_e2e()
+        ms_e2e = barrier_max(ws, time_steps(torch, w.step_e2e, args.steps))
+        e2e = {"value": args.steps * ws / (ms_e2e / 1000), "unit": "steps/s", "h2d_bytes_per_step": w.e2e_h2d,
+               "d2h_bytes_per_step": w.e2e_d2h}
 
     # per-kernel device time (events around every launch; a separate pass)
-    fm.fm_set_debug(w.h, fm.FM_DEBUG_PROFILE)
-    for _ in range(20):
-        w.step()
-    prof = fm.fm_profile_read(w.h)
-    fm.fm_set_debug(w.h, 0)
-    top = max(prof.items(), key=lambda kv: kv[1][1])
-    name, (nl, tms, tb) = top
-    per_launch_ms = tms / nl
-    achieved = (tb / nl) / (per_launch_ms / 1000) / 1e9
-    kernels = {k: {"launches": v[0] // 20, "ms_per_step": v[1] / 20,
-                   "gbs": (v[2] / v[0]) / ((v[1] / v[0]) / 1000) / 1e9} for k, v in sorted(prof.items())}
-    roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None, "peak_source": f"{peak_src} burst copy",
-                "bytes_per_launch": tb / nl, "ms_per_launch": per_launch_ms}
+    roofline, kernels = None, None
+    if not args.no_kprof:
+        fm.fm_set_debug(w.h, fm.FM_DEBUG_PROFILE)
+        for _ in range(20):
+            w.step()
+        prof = fm.fm_profile_read(w.h)
+        fm.fm_set_debug(w.h, 0)
+        top = max(prof.items(), key=lambda kv: kv[1][1])
+        name, (nl, tms, tb) = top
+        per_launch_ms = tms / nl
+        achieved = (tb / nl) / (per_launch_ms / 1000) / 1e9
+        kernels = {k: {"launches": v[0] // 20, "ms_per_step": v[1] / 20,
+                       "gbs": (v[2] / v[0]) / ((v[1] / v[0]) / 1000) / 1e9} for k, v in sorted(prof.items())}
+        roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm, "traffic": None, "peak_source": f"{peak_src} burst copy",
+                    "bytes_per_launch": tb / nl, "ms_per_launch": per_launch_ms}
 
     extra = {}
     if not args.no_prefill and rank == 0:

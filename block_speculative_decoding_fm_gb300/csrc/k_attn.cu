@@ -204,20 +204,25 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   __syncthreads();
   float *po = a.part_o + ((size_t)(head * a.splits + split) * kMaxT) * HD;
   float2 *pml = a.part_ml + (size_t)(head * a.splits + split) * kMaxT;
-  for (int i = threadIdx.x; i < T * HD; i += kThreads) {
-    const int t = i / HD, d = i - t * HD;
+  for (int i = threadIdx.x; i < T * (HD / 4); i += kThreads) {
+    const int t = i / (HD / 4), d = 4 * (i - t * (HD / 4));
     float M = -INFINITY;
 #pragma unroll
     for (int ww = 0; ww < 4; ++ww) M = fmaxf(M, mml[(ww * 16 + t) * 2]);
-    float acc = 0.f, lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
 #pragma unroll
     for (int ww = 0; ww < 4; ++ww) {
       const float mw = mml[(ww * 16 + t) * 2];
       const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      acc += f * mo[(ww * 16 + t) * HD + d];
+      const float *src = mo + (ww * 16 + t) * HD + d;
+      acc.x += f * src[0];
+      acc.y += f * src[1];
+      acc.z += f * src[2];
+      acc.w += f * src[3];
       lsum += f * mml[(ww * 16 + t) * 2 + 1];
     }
-    __stcg(po + t * HD + d, acc);
+    __stcg(reinterpret_cast<float4 *>(po + t * HD + d), acc);
     if (d == 0) __stcg(pml + t, make_float2(M, lsum));
   }
 
@@ -235,18 +240,45 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   __threadfence();
   const float *pob = a.part_o + (size_t)head * a.splits * kMaxT * HD;
   const float2 *pmb = a.part_ml + (size_t)head * a.splits * kMaxT;
-  for (int i = threadIdx.x; i < T * HD; i += kThreads) {
-    const int t = i / HD, d = i - t * HD;
+  // (max, sum) of every split and row -> shared memory, then per-row weights
+  float *fm_ = merge;                      // [splits][16] weight of split sp for row t
+  float *fl_ = merge + a.splits * 16;      // [splits][16] partial sums
+  for (int i = threadIdx.x; i < a.splits * T; i += kThreads) {
+    const int sp = i / T, t = i - sp * T;
+    const float2 ml = __ldcg(pmb + sp * kMaxT + t);
+    fm_[sp * 16 + t] = ml.x;
+    fl_[sp * 16 + t] = ml.y;
+  }
+  __syncthreads();
+  if (threadIdx.x < T) {
+    const int t = threadIdx.x;
     float M = -INFINITY;
-    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, __ldcg(pmb + sp * kMaxT + t).x);
-    float acc = 0.f, lsum = 0.f;
+    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, fm_[sp * 16 + t]);
+    float lsum = 0.f;
     for (int sp = 0; sp < a.splits; ++sp) {
-      const float2 ml = __ldcg(pmb + sp * kMaxT + t);
-      const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-      acc += f * __ldcg(pob + ((size_t)sp * kMaxT + t) * HD + d);
-      lsum += f * ml.y;
+      const float mw = fm_[sp * 16 + t];
+      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      fm_[sp * 16 + t] = f;
+      lsum += f * fl_[sp * 16 + t];
     }
-    a.out[(size_t)t * a.ldo + head * HD + d] = acc / lsum;
+    const float inv = 1.f / lsum;
+    for (int sp = 0; sp < a.splits; ++sp) fm_[sp * 16 + t] *= inv;
+  }
+  __syncthreads();
+  // out[t][4 d4 .. 4 d4 + 3] = sum over splits of weight * partial O (independent vector loads)
+  for (int i = threadIdx.x; i < T * (HD / 4); i += kThreads) {
+    const int t = i / (HD / 4), d4 = i - t * (HD / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float f = fm_[sp * 16 + t];
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(pob + ((size_t)sp * kMaxT + t) * HD) + d4);
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+    *reinterpret_cast<float4 *>(a.out + (size_t)t * a.ldo + head * HD + 4 * d4) = acc;
   }
 }
 

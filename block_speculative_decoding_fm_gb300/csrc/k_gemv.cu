@@ -312,31 +312,47 @@ __device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], i
 // O = softmax(q k^T * scale) v from the q/k/v segments in Y.
 __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *sm) {
   const int hd = a.hd, D = a.self_D;
-  const int ks = hd + 1;  // padded row stride in shared memory
+  const int ks = hd + 4;  // padded row stride (floats) in shared memory, keeps float4 alignment
   float *qq = sm, *kk = sm + kMaxT * ks, *vv = sm + 2 * kMaxT * ks;
-  for (int i = threadIdx.x; i < T * hd; i += kThreads) {
-    const int t = i / hd, d = i - t * hd;
+  const int q4 = hd / 4;
+  for (int i = threadIdx.x; i < T * q4; i += kThreads) {
+    const int t = i / q4, d = 4 * (i - t * q4);
     const float *row = a.Y + (size_t)t * a.ldy + head * hd + d;
-    qq[t * ks + d] = __ldcg(row);
-    kk[t * ks + d] = __ldcg(row + D);
-    vv[t * ks + d] = __ldcg(row + 2 * D);
+    const float4 q = __ldcg(reinterpret_cast<const float4 *>(row));
+    const float4 k = __ldcg(reinterpret_cast<const float4 *>(row + D));
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(row + 2 * D));
+    *reinterpret_cast<float4 *>(qq + t * ks + d) = q;
+    *reinterpret_cast<float4 *>(kk + t * ks + d) = k;
+    *reinterpret_cast<float4 *>(vv + t * ks + d) = v;
   }
   __syncthreads();
+  // one warp per query row: lane l owns dims 4l .. 4l+3 (lanes beyond hd/4 hold zeros)
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const bool on = lane < q4;
   for (int t = w; t < T; t += kThreads / 32) {
-    float sc = -INFINITY;
-    if (lane < T) {
-      float s = 0.f;
-      for (int d = 0; d < hd; ++d) s += qq[t * ks + d] * kk[lane * ks + d];
-      sc = s * a.attn_scale;
+    const float4 q = on ? *reinterpret_cast<const float4 *>(qq + t * ks + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float sc[kMaxT];
+    float mx = -INFINITY;
+    for (int j = 0; j < T; ++j) {
+      const float4 k = on ? *reinterpret_cast<const float4 *>(kk + j * ks + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float s = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w) * a.attn_scale;
+      sc[j] = s;
+      mx = fmaxf(mx, s);
     }
-    const float mx = warp_max(sc);
-    const float p = lane < T ? __expf(sc - mx) : 0.f;
-    const float den = warp_sum(p);
-    for (int d = lane; d < hd; d += 32) {
-      float o = 0.f;
-      for (int j = 0; j < T; ++j) o += __shfl_sync(0xffffffffu, p, j) * vv[j * ks + d];
-      a.attn_out[(size_t)t * D + head * hd + d] = o / den;
+    float den = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < T; ++j) {
+      const float p = __expf(sc[j] - mx);
+      den += p;
+      if (on) {
+        const float4 v = *reinterpret_cast<const float4 *>(vv + j * ks + 4 * lane);
+        o.x += p * v.x; o.y += p * v.y; o.z += p * v.z; o.w += p * v.w;
+      }
+    }
+    if (on) {
+      const float inv = 1.f / den;
+      *reinterpret_cast<float4 *>(a.attn_out + (size_t)t * D + head * hd + 4 * lane) =
+          make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
     }
   }
   __syncthreads();
@@ -468,7 +484,7 @@ size_t gemv_smem_bytes(const GemvArgs &a, int mt) {
   const int S = mt == 1 ? 4 : 3;
   const size_t a_bytes = (size_t)(16 * mt) * a_stride(a.Kp) * 2;
   size_t bytes = (size_t)S * kStageBytes + 2 * a_bytes + (size_t)(16 * mt) * kCsStride * 4 + 2 * kMaxT * 4;
-  const size_t attn = a.self_D > 0 ? (size_t)3 * kMaxT * (a.hd + 1) * 4 : 0;
+  const size_t attn = a.self_D > 0 ? (size_t)3 * kMaxT * (a.hd + 4) * 4 : 0;
   return bytes > attn ? bytes : attn;
 }
 
