@@ -127,9 +127,71 @@ __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x)));
 }
 
+// byte offset of int8 column k (0..63) of row r (0..127) inside a Q8_0 table chunk
+__host__ __device__ __forceinline__ uint32_t q8_slot(int r, int k) {
+  const int piece = k >> 4;  // 16-byte piece: block k / 32, half (k % 32) / 16
+  return r * 64 + ((piece ^ (((r >> 1) & 1) << 1)) << 4) + (k & 15);
+}
+// byte offset of bf16 column k (0..63) of row r inside a GEMV weight tile
+__host__ __device__ __forceinline__ uint32_t w_slot(int r, int k) {
+  const int u = k >> 3;
+  return r * 128 + ((u ^ ((r & 1) << 2)) << 4) + (k & 7) * 2;
+}
+
 // (value, index) ordering for argmax: larger value wins, ties to the lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
+}
+
+}  // namespace fm
+
+namespace fm {
+
+// ---- mbarrier + bulk async copies (TMA, 1-D) ------------------------------
+constexpr long long kWaitBudgetCycles = 4000000000LL;  // ~2 s at 2 GHz before a wait gives up
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on an mbarrier phase.  Returns false (and raises *err) when the
+// clock budget runs out, or when another thread already raised *err.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int32_t *err) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity)) {
+    if (*reinterpret_cast<volatile int32_t *>(err)) return false;
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      atomicExch(err, 1);
+      return false;
+    }
+  }
+  return true;
+}
+// global -> shared bulk copy (16-byte aligned, size a multiple of 16) completing on an mbarrier
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
 
 }  // namespace fm

@@ -56,10 +56,9 @@ struct fm_handle {
   __nv_bfloat16 *attn_norm = nullptr, *ff_norm = nullptr, *ctx_norm = nullptr, *out_norm = nullptr;
   __nv_bfloat16 *w_c = nullptr, *w_tok = nullptr, *block_pos = nullptr, *w_out = nullptr;
   float *hinit = nullptr;
-  // ---- token table ----
-  int8_t *tq = nullptr;
-  __half *tsc = nullptr;
-  __nv_bfloat16 *tb = nullptr;
+  // ---- token table (Q8_0: lm_head chunk layout; bf16: GEMV tile layout) ----
+  uint8_t *tq8 = nullptr;
+  uint8_t *tb = nullptr;
   int Vpad = 0;
 
   // ---- state ----
@@ -87,6 +86,9 @@ struct fm_handle {
   int32_t *pf_err = nullptr;
   int pf_rows = 0;                                // rows the scratch holds
   CUtensorMap tm_wfc{}, tm_wkv{}, tm_c{};
+
+  int32_t *dev_err = nullptr;     // raised by a device-side bounded wait that gave up
+  std::vector<void *> to_free;    // row-major staging copies released at the end of fm_create
 
   // ---- deferred K/V projection of the last short append ----
   int pend_seq = -1, pend_start = 0, pend_n = 0;
@@ -170,6 +172,12 @@ fm_status dalloc(fm_handle *h, T **p, size_t count) {
   return FM_OK;
 }
 
+void dfree_later(fm_handle *h, void *p) {
+  auto it = std::find(h->allocs.begin(), h->allocs.end(), p);
+  if (it != h->allocs.end()) h->allocs.erase(it);
+  h->to_free.push_back(p);
+}
+
 #define TRY(expr)                    \
   do {                               \
     fm_status s_ = (expr);           \
@@ -218,6 +226,16 @@ fm_status put_bf16_t(fm_handle *h, const TensorSet &ts, const std::string &name,
   TRY(find(h, ts, name, (int64_t)rows * cols * 2, FM_DTYPE_BF16, true, &t));
   CK(cudaMemcpyAsync(tmp, t->data, (size_t)rows * cols * 2, cudaMemcpyDefault, s));
   CK(launch_transpose_bf16(tmp, rows, cols, dst, ldo, s));
+  return FM_OK;
+}
+
+// Replace a row-major [M][K] bf16 weight by its GEMV tile layout (same pointer slot).
+fm_status tile_weight(fm_handle *h, __nv_bfloat16 **w, int M, int K, cudaStream_t s) {
+  uint8_t *t;
+  TRY(dalloc(h, &t, tiled_bytes(M, K)));
+  CK(launch_tile_weights(*w, M, K, t, s));
+  dfree_later(h, *w);
+  *w = reinterpret_cast<__nv_bfloat16 *>(t);
   return FM_OK;
 }
 
@@ -282,7 +300,8 @@ struct ProfScope {
 GemvArgs gemv_base(const fm_handle *h, const __nv_bfloat16 *W, int M, int K, int T_const, const StepParams *sp) {
   GemvArgs a;
   memset(&a, 0, sizeof a);
-  a.W = W;
+  a.Wt = reinterpret_cast<const uint8_t *>(W);  // weight buffers hold the GEMV tile layout
+  a.err = h->dev_err;
   a.M = M;
   a.K = K;
   a.T_const = T_const;
@@ -351,12 +370,11 @@ fm_status run_lmhead(fm_handle *h, const float *Y, int T, const StepParams *sp, 
   const fm_config &c = h->cfg;
   LmArgs a;
   memset(&a, 0, sizeof a);
-  if (c.lm_format == FM_LM_Q8_0) {
-    a.q8 = h->tq;
-    a.q8s = h->tsc;
-  } else {
+  if (c.lm_format == FM_LM_Q8_0)
+    a.q8 = h->tq8;
+  else
     a.wb = h->tb;
-  }
+  a.err = h->dev_err;
   a.V = c.vocab;
   a.H = c.target_dim;
   a.T_const = T;
@@ -439,8 +457,7 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
   // the anchor's context slot at pos: anchor_proj(E[anchor]) -> anchor_norm -> k / v of every layer
   GemvArgs a = gemv_base(h, h->w_ap, D, Ht, 1, sp);
   a.amode = c.lm_format == FM_LM_Q8_0 ? A_ROW_Q8 : A_ROW_BF16;
-  a.tq = h->tq;
-  a.tscale = h->tsc;
+  a.tq8 = h->tq8;
   a.tb = h->tb;
   a.emode = E_STORE;
   a.bias = h->b_ap;
@@ -637,8 +654,7 @@ fm_status dflash_draft_launch(fm_handle *h, int seq, int pos, const StepParams *
   // block row 0 = tok_proj(E[anchor]) + block_pos[0]; rows 1.. are constants
   GemvArgs a = gemv_base(h, h->w_tok, d, H, 1, sp);
   a.amode = c.lm_format == FM_LM_Q8_0 ? A_ROW_Q8 : A_ROW_BF16;
-  a.tq = h->tq;
-  a.tscale = h->tsc;
+  a.tq8 = h->tq8;
   a.tb = h->tb;
   a.emode = E_STORE;
   a.bias = h->block_pos;
@@ -739,10 +755,7 @@ fm_status prefill_setup(fm_handle *h, cudaStream_t s) {
   const int D = c.dim, FW = c.n_taps * c.target_dim, L = c.n_layers;
   if (D % 256) return fail(h, FM_ERR_UNSUPPORTED, "dense prefill needs dim % 256 == 0");
   const int rows = c.max_ctx < kPrefillChunk ? c.max_ctx : kPrefillChunk;
-  TRY(dalloc(h, &h->w_fc16, (size_t)D * FW));
-  TRY(dalloc(h, &h->w_kv16, (size_t)L * 2 * D * D));
-  CK(launch_bf16_to_f16(h->w_fc, h->w_fc16, (size_t)D * FW, s));
-  CK(launch_bf16_to_f16(h->w_kvall, h->w_kv16, (size_t)L * 2 * D * D, s));
+  if (!h->w_fc16) return fail(h, FM_ERR_UNSUPPORTED, "dense prefill weights were not prepared");
   TRY(dalloc(h, &h->pf_a, (size_t)rows * FW));
   TRY(dalloc(h, &h->pf_c, (size_t)rows * D));
   TRY(dalloc(h, &h->pf_st, (size_t)rows * (D / 256)));
@@ -975,6 +988,8 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   TRY(dalloc(h, &h->tickets, (size_t)2 * c.n_heads + 8));
   CK(cudaMemsetAsync(h->tickets, 0, ((size_t)2 * c.n_heads + 8) * 4, s));
   TRY(dalloc(h, &h->tok_tmp, (size_t)kMaxT));
+  TRY(dalloc(h, &h->dev_err, 4));
+  CK(cudaMemsetAsync(h->dev_err, 0, 4, s));
   TRY(dalloc(h, &h->sp_dev, kParamSlots));
   CK(cudaMallocHost(&h->sp_host, sizeof(StepParams) * kParamSlots));
   memset(h->sp_host, 0, sizeof(StepParams) * kParamSlots);
@@ -993,22 +1008,24 @@ fm_status create_table(fm_handle *h, const TensorSet &ts, cudaStream_t s) {
   const fm_config &c = h->cfg;
   const int V = c.vocab, H = c.target_dim;
   h->Vpad = (V + kTile - 1) / kTile * kTile;
+  TRY(dalloc(h, &h->uni, H));
   if (c.lm_format == FM_LM_Q8_0) {
     const fm_tensor *t;
     TRY(find(h, ts, "token_embd.weight", (int64_t)V * (H / 32) * 34, FM_DTYPE_Q8_0, true, &t));
     uint8_t *raw;
     TRY(dalloc(h, &raw, (size_t)V * (H / 32) * 34));
     CK(cudaMemcpyAsync(raw, t->data, (size_t)V * (H / 32) * 34, cudaMemcpyDefault, s));
-    TRY(dalloc(h, &h->tq, (size_t)h->Vpad * H));
-    TRY(dalloc(h, &h->tsc, (size_t)h->Vpad * (H / 32)));
-    CK(launch_q8_repack(raw, V, H, h->tq, h->tsc, h->Vpad, s));
-    CK(cudaStreamSynchronize(s));
-    CK(cudaFree(raw));
-    h->allocs.erase(std::find(h->allocs.begin(), h->allocs.end(), (void *)raw));
-    h->bytes -= (int64_t)V * (H / 32) * 34;
+    TRY(dalloc(h, &h->tq8, q8_table_bytes(V, H)));
+    CK(launch_q8_repack(raw, V, H, h->tq8, s));
+    CK(launch_colmean_q8(raw, V, H, h->uni, s));
+    dfree_later(h, raw);
   } else {
-    TRY(dalloc(h, &h->tb, (size_t)V * H));
-    TRY(put_bf16(h, ts, "token_embd.weight", h->tb, (int64_t)V * H, s));
+    __nv_bfloat16 *tb;
+    TRY(dalloc(h, &tb, (size_t)V * H));
+    TRY(put_bf16(h, ts, "token_embd.weight", tb, (int64_t)V * H, s));
+    CK(launch_colmean_bf16(tb, V, H, h->uni, s));
+    TRY(tile_weight(h, &tb, V, H, s));
+    h->tb = reinterpret_cast<uint8_t *>(tb);
   }
   return FM_OK;
 }
@@ -1089,13 +1106,29 @@ fm_status create_flashmap(fm_handle *h, const TensorSet &ts, const float *modula
   CK(cudaMemcpyAsync(h->mod, modulation, nmod * 4, cudaMemcpyDefault, s));
   TRY(create_common(h, s));
 
+  // f16 row-major copies for the dense prefill, then every GEMV weight to its tile layout
+  if (D % 256 == 0 && c.max_ctx >= 128) {
+    TRY(dalloc(h, &h->w_fc16, (size_t)D * FW));
+    TRY(dalloc(h, &h->w_kv16, (size_t)L * 2 * D * D));
+    CK(launch_bf16_to_f16(h->w_fc, h->w_fc16, (size_t)D * FW, s));
+    CK(launch_bf16_to_f16(h->w_kvall, h->w_kv16, (size_t)L * 2 * D * D, s));
+  }
+  TRY(tile_weight(h, &h->w_fc, D, FW, s));
+  TRY(tile_weight(h, &h->w_ap, D, Ht, s));
+  TRY(tile_weight(h, &h->w_xe, D, Ht, s));
+  TRY(tile_weight(h, &h->w_head, Ht, D, s));
+  TRY(tile_weight(h, &h->w_kvall, L * 2 * D, D, s));
+  for (int l = 0; l < L; ++l) {
+    TRY(tile_weight(h, &h->w_qkv[l], 3 * D, D, s));
+    TRY(tile_weight(h, &h->w_so[l], D, D, s));
+    TRY(tile_weight(h, &h->w_cq[l], D, D, s));
+    TRY(tile_weight(h, &h->w_co[l], D, D, s));
+    TRY(tile_weight(h, &h->w_f1[l], F, D, s));
+    TRY(tile_weight(h, &h->w_f2[l], D, F, s));
+  }
+
   // h0 = x_embed(state_norm(mean row of E)) + bias, and its row statistics
   TRY(dalloc(h, &h->h0, D));
-  TRY(dalloc(h, &h->uni, Ht));
-  if (c.lm_format == FM_LM_Q8_0)
-    CK(launch_colmean_q8(h->tq, h->tsc, c.vocab, Ht, h->uni, s));
-  else
-    CK(launch_colmean_bf16(h->tb, c.vocab, Ht, h->uni, s));
   CK(launch_row_stats(h->uni, 1, Ht, h->st_u, s));
   StepParams p{};
   p.T = 1;
@@ -1182,6 +1215,18 @@ fm_status create_dflash(fm_handle *h, const TensorSet &ts, cudaStream_t s) {
   TRY(dalloc(h, &h->hinit, (size_t)kMaxT * d));
   CK(cudaMemsetAsync(h->hinit, 0, (size_t)kMaxT * d * 4, s));
   CK(launch_block_consts(mask_emb, h->block_pos, G, d, h->hinit, h->st_init, s));
+  for (int l = 0; l < L; ++l) {
+    TRY(tile_weight(h, &h->w_qkv[l], 3 * d, d, s));
+    TRY(tile_weight(h, &h->w_o[l], d, d, s));
+    TRY(tile_weight(h, &h->w_gu[l], 2 * F, d, s));
+    TRY(tile_weight(h, &h->w_down[l], d, F, s));
+  }
+  TRY(tile_weight(h, &h->w_kvall, L * 2 * d, d, s));
+  TRY(tile_weight(h, &h->w_c, d, mH, s));
+  TRY(tile_weight(h, &h->w_tok, d, H, s));
+  TRY(tile_weight(h, &h->w_out, H, d, s));
+  dfree_later(h, tmp);
+  dfree_later(h, tmp2);
   CK(cudaStreamSynchronize(s));
   return FM_OK;
 }
@@ -1276,6 +1321,9 @@ fm_status fm_create(const fm_config *cfg, const fm_tensor *weights, int32_t n_we
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) st = fail(h, FM_ERR_CUDA, "create: %s", cudaGetErrorString(e));
   }
+  cudaStreamSynchronize(s);
+  for (void *p : h->to_free) cudaFree(p);
+  h->to_free.clear();
   if (st != FM_OK) {
     g_create_error = h->err;
     fm_destroy(h);
@@ -1414,7 +1462,10 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
   }
   if (offset + nbytes > size) return fail(h, FM_ERR_INVALID_ARG, "range beyond the buffer (%lld bytes)", (long long)size);
   CK(cudaMemcpyAsync(dst, static_cast<const char *>(src) + offset, nbytes, cudaMemcpyDeviceToHost, s));
+  int32_t flag = 0;
+  CK(cudaMemcpyAsync(&flag, h->dev_err, 4, cudaMemcpyDeviceToHost, s));
   CK(cudaStreamSynchronize(s));
+  if (flag) return fail(h, FM_ERR_TIMEOUT, "a device-side bounded wait gave up in an earlier call");
   return FM_OK;
 }
 
@@ -1490,6 +1541,7 @@ const char *fm_last_error(const fm_handle *h) { return h ? h->err.c_str() : g_cr
 void fm_destroy(fm_handle *h) {
   if (!h) return;
   for (void *p : h->allocs) cudaFree(p);
+  for (void *p : h->to_free) cudaFree(p);
   if (h->sp_host) cudaFreeHost(h->sp_host);
   for (int i = 0; i < kParamSlots; ++i)
     if (h->sp_ev[i]) cudaEventDestroy(h->sp_ev[i]);

@@ -59,7 +59,8 @@ struct SegDesc {
 };
 
 struct GemvArgs {
-  const __nv_bfloat16 *W;  // [M][K] row-major, bf16
+  const uint8_t *Wt;       // weights tiled [ceil(M/128)][K/64][16 KB]: 128 rows x 64 bf16, pre-swizzled
+  int32_t *err;            // raised when a bounded wait gives up
   int32_t M, K, Kc, Kp;    // rows, cols, cols per CTA, cols per staged A piece
   int32_t ksplit;          // CTAs (one cluster) sharing a row tile
   int32_t T_const;         // > 0: fixed T, else sp->T
@@ -84,9 +85,8 @@ struct GemvArgs {
   const float2 *st2;
   const __nv_bfloat16 *nw_alt;
   float eps, inv_n;
-  const int8_t *tq;        // A_ROW_Q8: int8 plane [V][K]
-  const __half *tscale;    // A_ROW_Q8: scales [V / 128][K / 32][128]
-  const __nv_bfloat16 *tb; // A_ROW_BF16: rows [V][K]
+  const uint8_t *tq8;      // A_ROW_Q8: the table in lm_head layout (see LmArgs)
+  const uint8_t *tb;       // A_ROW_BF16: the table in GEMV tile layout
 
   // epilogue
   int32_t emode;
@@ -133,10 +133,14 @@ struct AttnArgs {
 };
 
 // --- lm_head GEMV fused with the per-row argmax -----------------------------
+// Q8_0 table layout: per (128-row tile, 64-column chunk) one contiguous 8704-byte
+// block: 128 rows x 64 int8 (pre-swizzled, q8_slot) then the two 32-column
+// blocks' f16 scales [2][128].  bf16 table: the GEMV tile layout.
+constexpr int kQ8Chunk = kTile * 64 + 2 * kTile * 2;
 struct LmArgs {
-  const int8_t *q8;          // Q8_0 int8 plane [Vpad][H]
-  const __half *q8s;         // scales [Vpad / 128][H / 32][128]
-  const __nv_bfloat16 *wb;   // bf16 table [V][H]
+  const uint8_t *q8;         // Q8_0 table (layout above) or null
+  const uint8_t *wb;         // bf16 table (GEMV tile layout) or null
+  int32_t *err;
   int32_t V, H;
   int32_t T_const;
   const StepParams *sp;
@@ -156,10 +160,9 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t s, bool pdl);
 int lmhead_grid(const LmArgs &a, int n_sm);
 
 // set-up and small kernels
-cudaError_t launch_q8_repack(const uint8_t *raw, int32_t V, int32_t H, int8_t *q, __half *scales,
-                             int32_t Vpad, cudaStream_t s);
-cudaError_t launch_colmean_q8(const int8_t *q, const __half *scales, int32_t V, int32_t H, float *out,
-                              cudaStream_t s);
+cudaError_t launch_q8_repack(const uint8_t *raw, int32_t V, int32_t H, uint8_t *dst, cudaStream_t s);
+size_t q8_table_bytes(int32_t V, int32_t H);
+cudaError_t launch_colmean_q8(const uint8_t *raw, int32_t V, int32_t H, float *out, cudaStream_t s);
 cudaError_t launch_colmean_bf16(const __nv_bfloat16 *w, int32_t V, int32_t H, float *out, cudaStream_t s);
 cudaError_t launch_rope_table(float2 *tab, int32_t n_pos, int32_t hd, float theta, cudaStream_t s);
 cudaError_t launch_transpose_bf16(const __nv_bfloat16 *in, int32_t rows, int32_t cols, __nv_bfloat16 *out,
@@ -170,5 +173,8 @@ cudaError_t launch_row_stats(const float *x, int32_t rows, int32_t d, float2 *st
 cudaError_t launch_accept(int32_t n, int32_t block, const int32_t *draft, const int32_t *target,
                           const int32_t *k, int32_t *acc, int32_t *bonus, cudaStream_t s);
 cudaError_t launch_fill_f32(float *p, size_t n, float v, cudaStream_t s);
+// [M][K] bf16 row-major -> GEMV tile layout (zero rows past M)
+cudaError_t launch_tile_weights(const __nv_bfloat16 *src, int32_t M, int32_t K, uint8_t *dst, cudaStream_t s);
+size_t tiled_bytes(int32_t M, int32_t K);
 
 }  // namespace fm

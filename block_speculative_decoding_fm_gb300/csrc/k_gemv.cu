@@ -3,9 +3,12 @@
 //
 // The pages run this product as gemvT17 / gemmBf16 in WGSL (flashmap_drafter.js,
 // ``gemvT``: one weight read, token sums in registers).  On sm_103a:
-//   * weights stream once from HBM through a cp.async ring of 128 x 64 tiles;
-//     the first stages are issued before griddepcontrol.wait, so a kernel's
-//     weights are in flight while its predecessor is still finishing;
+//   * weights are stored pre-tiled (128 rows x 64 k, 16 KB, already in the
+//     swizzled shared-memory order); a producer warp streams a CTA's tiles with
+//     1-D bulk TMA copies into an mbarrier ring, issuing the first stages before
+//     griddepcontrol.wait so a kernel's weights are in flight while its
+//     predecessor is still finishing; consumer warps never block on each other
+//     inside the main loop;
 //   * the activations are transformed on the way in (RMSNorm, adaLN LayerNorm
 //     modulate, a table row) and split into bf16 hi + lo, so the bf16 tensor
 //     cores see f32-accurate operands: A*W = hi*W + lo*W, f32 accumulate;
@@ -28,7 +31,8 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;   // consumer warps 0..7
+constexpr int kAll = kThreads + 32;  // + the producer warp
 constexpr int kChunk = 64;                       // k per pipeline stage
 constexpr int kStageBytes = kTile * kChunk * 2;  // 16 KB of bf16 weights
 constexpr int kCsStride = kTile + 8;             // f32 partial tile row stride
@@ -43,20 +47,6 @@ struct Smem {
 
 // weight tile: row r (0..127) of chunk, 16-byte unit u (0..7) -> swizzled slot
 __device__ __forceinline__ uint32_t wslot(int r, int u) { return r * 128 + ((u ^ ((r & 1) << 2)) << 4); }
-
-__device__ __forceinline__ void issue_chunk(const GemvArgs &a, uint32_t ring, int stage, int m0, int k) {
-  const uint32_t base = ring + stage * kStageBytes;
-  // 1024 16-byte pieces: row = i / 8, unit = i % 8
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int i = threadIdx.x + j * kThreads;
-    const int r = i >> 3, u = i & 7;
-    const int m = m0 + r;
-    const bool ok = m < a.M;
-    const __nv_bfloat16 *src = a.W + (size_t)(ok ? m : 0) * a.K + k + u * 8;
-    cp_async16(base + wslot(r, u), src, ok ? 16u : 0u);
-  }
-}
 
 // Row statistics of the input rows (sum over the producer's tiles, in double).
 __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
@@ -111,14 +101,20 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, int T, int m0, int k0,
       if (a.amode == A_ROW_Q8 || a.amode == A_ROW_BF16) {
         if (t == 0) {
           const int r = a.sp->anchor;
+          const size_t chunk = (size_t)(r >> 7) * (a.K / 64) + (k >> 6);
+          const int rr = r & 127, kk = k & 63;
           if (a.amode == A_ROW_Q8) {
-            const char4 q = *reinterpret_cast<const char4 *>(a.tq + (size_t)r * a.K + k);
-            const float d = __half2float(a.tscale[((size_t)(r >> 7) * (a.K >> 5) + (k >> 5)) * 128 + (r & 127)]);
+            const uint8_t *base = a.tq8 + chunk * kQ8Chunk;
+            const char4 q = *reinterpret_cast<const char4 *>(base + q8_slot(rr, kk));
+            const float d = __half2float(
+                *reinterpret_cast<const __half *>(base + kTile * 64 + (kk >> 5) * 256 + rr * 2));
             v[0] = d * q.x; v[1] = d * q.y; v[2] = d * q.z; v[3] = d * q.w;
           } else {
-            const __nv_bfloat16 *p = a.tb + (size_t)r * a.K + k;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = __bfloat162float(p[e]);
+            const uint8_t *base = a.tb + chunk * 16384;
+            const uint2 u = *reinterpret_cast<const uint2 *>(base + w_slot(rr, kk));
+            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+            v[0] = __low2float(p0); v[1] = __high2float(p0); v[2] = __low2float(p1); v[3] = __high2float(p1);
           }
         }
       } else {
@@ -315,7 +311,8 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
   const int ks = hd + 4;  // padded row stride (floats) in shared memory, keeps float4 alignment
   float *qq = sm, *kk = sm + kMaxT * ks, *vv = sm + 2 * kMaxT * ks;
   const int q4 = hd / 4;
-  for (int i = threadIdx.x; i < T * q4; i += kThreads) {
+  const bool consumer = threadIdx.x < kThreads;  // the producer warp only joins the barriers
+  for (int i = threadIdx.x; consumer && i < T * q4; i += kThreads) {
     const int t = i / q4, d = 4 * (i - t * q4);
     const float *row = a.Y + (size_t)t * a.ldy + head * hd + d;
     const float4 q = __ldcg(reinterpret_cast<const float4 *>(row));
@@ -329,7 +326,7 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
   // one warp per query row: lane l owns dims 4l .. 4l+3 (lanes beyond hd/4 hold zeros)
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const bool on = lane < q4;
-  for (int t = w; t < T; t += kThreads / 32) {
+  for (int t = w; consumer && t < T; t += kThreads / 32) {
     const float4 q = on ? *reinterpret_cast<const float4 *>(qq + t * ks + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     float sc[kMaxT];
     float mx = -INFINITY;
@@ -360,8 +357,8 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
 
 }  // namespace
 
-template <int MT, int S>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
+template <int MT>
+__global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ GemvArgs a, const int S) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tile = blockIdx.x;
   const int m0 = tile * kTile;
@@ -369,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
   const int k_begin = split * a.Kc;
   const int nchunks = a.Kc / kChunk;
   const int lda = a_stride(a.Kp);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   Smem s;
   s.ring = smem_u32(smem);
@@ -379,18 +377,24 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
   s.cs_ptr = reinterpret_cast<float *>(smem + S * kStageBytes + 2 * a_bytes);
   s.stat_mu = s.cs_ptr + 16 * MT * kCsStride;
   s.stat_rs = s.stat_mu + kMaxT;
+  const uint32_t bars = smem_u32(s.stat_rs + kMaxT);
+  auto full = [&](int i) { return bars + 8 * i; };
+  auto empty = [&](int i) { return bars + 8 * (S + i); };
+  const uint8_t *wsrc = a.Wt + ((size_t)tile * (a.K / kChunk) + k_begin / kChunk) * kStageBytes;
 
-  // weights do not depend on earlier kernels: start streaming them now
-#pragma unroll
-  for (int c = 0; c < S - 1; ++c) {
-    if (c < nchunks) issue_chunk(a, s.ring, c, m0, k_begin + c * kChunk);
-    cp_async_commit();
+  if (threadIdx.x == kThreads) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), kThreads / 32);
+    }
+    mbar_fence_init();
+    // weights do not depend on earlier kernels: start streaming them now
+    for (int c = 0; c < S && c < nchunks; ++c) {
+      mbar_expect_tx(full(c), kStageBytes);
+      bulk_g2s(s.ring + c * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(c));
+    }
   }
   pdl_trigger();
-  pdl_wait();
-
-  const int T = a.T_const > 0 ? a.T_const : a.sp->T;
-  load_row_stats(a, T, s.stat_mu, s.stat_rs);
   __syncthreads();
 
   float acc[MT][2][4];
@@ -401,31 +405,43 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
 
-  const int cpp = a.Kp / kChunk;  // chunks per A piece
-  for (int c = 0; c < nchunks; ++c) {
-    if (c % cpp == 0) {
-      if (c) __syncthreads();
-      const int kp = min(a.Kp, a.Kc - c * kChunk);
-      stage_a<MT>(a, s, T, m0, k_begin + c * kChunk, kp);
-      __syncthreads();
+  pdl_wait();
+  const int T = a.T_const > 0 ? a.T_const : a.sp->T;
+  if (warp == kThreads / 32) {
+    // producer: refill each stage once its 8 consumer warps have released it
+    if (lane == 0) {
+      for (int c = S; c < nchunks; ++c) {
+        const int st = c % S;
+        if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
+        mbar_expect_tx(full(st), kStageBytes);
+        bulk_g2s(s.ring + st * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(st));
+      }
     }
-    if (c + S - 1 < nchunks) issue_chunk(a, s.ring, (c + S - 1) % S, m0, k_begin + (c + S - 1) * kChunk);
-    cp_async_commit();
-    cp_async_wait<S - 1>();
-    __syncthreads();
-    compute_chunk<MT>(s.ring + (c % S) * kStageBytes, s, lda, (c % cpp) * kChunk, acc);
-    __syncthreads();
-  }
-
-  // partial tile -> shared memory
-  {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  } else {
+    load_row_stats(a, T, s.stat_mu, s.stat_rs);
+    named_sync(1, kThreads);
+    const int cpp = a.Kp / kChunk;  // chunks per A piece
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      if (c % cpp == 0) {
+        if (c) named_sync(1, kThreads);
+        const int kp = min(a.Kp, a.Kc - c * kChunk);
+        stage_a<MT>(a, s, T, m0, k_begin + c * kChunk, kp);
+        named_sync(1, kThreads);
+      }
+      const int st = c % S;
+      if (ok && !mbar_wait_bounded(full(st), (c / S) & 1, a.err)) ok = false;
+      if (ok) compute_chunk<MT>(s.ring + st * kStageBytes, s, lda, (c % cpp) * kChunk, acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(st));
+    }
+    // partial tile -> shared memory
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int col = 16 * w + 8 * j + 2 * q;
+        const int col = 16 * warp + 8 * j + 2 * q;
         const int t0 = 16 * mt + g;
         *reinterpret_cast<float2 *>(s.cs_ptr + t0 * kCsStride + col) = make_float2(acc[mt][j][0], acc[mt][j][1]);
         *reinterpret_cast<float2 *>(s.cs_ptr + (t0 + 8) * kCsStride + col) =
@@ -439,9 +455,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
   const int rank = ks > 1 ? (int)cluster.block_rank() : 0;
   if (ks > 1) cluster.sync();
 
-  {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int t = rank + ks * w; t < T; t += ks * (kThreads / 32)) {
+  if (warp < kThreads / 32) {
+    for (int t = rank + ks * warp; t < T; t += ks * (kThreads / 32)) {
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       for (int r = 0; r < ks; ++r) {
         const float *src = ks > 1 ? cluster.map_shared_rank(s.cs_ptr, r) : s.cs_ptr;
@@ -480,22 +495,27 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
   }
 }
 
+static int gemv_stages(const GemvArgs &a, int mt) {
+  const int nchunks = a.Kc / kChunk;
+  const int cap = mt == 1 ? 4 : 3;  // two CTAs per SM
+  return nchunks < cap ? nchunks : cap;
+}
+
 size_t gemv_smem_bytes(const GemvArgs &a, int mt) {
-  const int S = mt == 1 ? 4 : 3;
+  const int S = gemv_stages(a, mt);
   const size_t a_bytes = (size_t)(16 * mt) * a_stride(a.Kp) * 2;
-  size_t bytes = (size_t)S * kStageBytes + 2 * a_bytes + (size_t)(16 * mt) * kCsStride * 4 + 2 * kMaxT * 4;
+  size_t bytes = (size_t)S * kStageBytes + 2 * a_bytes + (size_t)(16 * mt) * kCsStride * 4 + 2 * kMaxT * 4 + 16 * S;
   const size_t attn = a.self_D > 0 ? (size_t)3 * kMaxT * (a.hd + 4) * 4 : 0;
   return bytes > attn ? bytes : attn;
 }
 
 cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t st, bool pdl) {
-  const int T = a.T_const > 0 ? a.T_const : kMaxT;
   const int mt = (a.T_const > 0 && a.T_const <= 16) ? 1 : 2;
-  (void)T;
   const size_t smem = gemv_smem_bytes(a, mt);
+  const int S = gemv_stages(a, mt);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_tiles, a.ksplit, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kAll, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -514,13 +534,13 @@ cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t st, bool pd
   cfg.numAttrs = na;
   cudaError_t e;
   if (mt == 1) {
-    e = cudaFuncSetAttribute(gemv_kernel<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<1, 4>, a);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<1>, a, S);
   }
-  e = cudaFuncSetAttribute(gemv_kernel<2, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<2, 3>, a);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<2>, a, S);
 }
 
 }  // namespace fm

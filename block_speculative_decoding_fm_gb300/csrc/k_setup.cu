@@ -6,38 +6,44 @@ namespace fm {
 
 namespace {
 
-// GGUF Q8_0 rows [V][nb * 34] -> int8 plane [Vpad][H] and scale plane
-// [Vpad / 128][nb][128] (the MTP loader on ternary_bonsai_2_mtp.js splits the
-// 34-byte blocks the same way; the scale plane is tiled by 128 rows here so a
-// vocab tile's scales are contiguous).  Padding rows get zeros.
-__global__ void q8_repack_kernel(const uint8_t *raw, int V, int H, int8_t *q, __half *scales, int Vpad) {
-  const int nb = H / 32;
+// GGUF Q8_0 rows [V][nb * 34] -> the lm_head layout: per (128-row tile, 64-column
+// chunk) 128 x 64 int8 (pre-swizzled) then the chunk's two blocks of f16 scales
+// [2][128] (the MTP loader on ternary_bonsai_2_mtp.js splits the 34-byte blocks
+// into an int8 plane and a scale plane; here both halves of a chunk sit together
+// so one bulk copy fetches them).  Rows past V get zeros.  One thread per block.
+__global__ void q8_repack_kernel(const uint8_t *raw, int V, int H, uint8_t *dst) {
+  const int nb = H / 32, nck = H / 64;
+  const int Vpad = (V + 127) / 128 * 128;
   const long long id = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (id >= (long long)Vpad * nb) return;
   const int r = (int)(id / nb), b = (int)(id - (long long)r * nb);
-  int8_t *qd = q + (size_t)r * H + b * 32;
-  __half *sd = scales + ((size_t)(r >> 7) * nb + b) * 128 + (r & 127);
-  if (r >= V) {
-    for (int i = 0; i < 32; ++i) qd[i] = 0;
-    *sd = __ushort_as_half(0);
-    return;
+  const int tile = r >> 7, rr = r & 127, kc = b >> 1, bb = b & 1;
+  uint8_t *chunk = dst + ((size_t)tile * nck + kc) * kQ8Chunk;
+  uint8_t q[32];
+  unsigned short d = 0;
+  if (r < V) {
+    const uint8_t *src = raw + (size_t)r * nb * 34 + b * 34;
+    d = (unsigned short)src[0] | ((unsigned short)src[1] << 8);
+    for (int i = 0; i < 32; ++i) q[i] = src[2 + i];
+  } else {
+    for (int i = 0; i < 32; ++i) q[i] = 0;
   }
-  const uint8_t *src = raw + (size_t)r * nb * 34 + b * 34;
-  const unsigned short d = (unsigned short)src[0] | ((unsigned short)src[1] << 8);
-  *sd = __ushort_as_half(d);
-  for (int i = 0; i < 32; ++i) qd[i] = (int8_t)src[2 + i];
+  for (int i = 0; i < 32; ++i) chunk[q8_slot(rr, 32 * bb + i)] = q[i];
+  *reinterpret_cast<unsigned short *>(chunk + kTile * 64 + bb * 256 + rr * 2) = d;
 }
 
 // column sums in double over a slab of rows; partial[slab][col]
-__global__ void colsum_q8_kernel(const int8_t *q, const __half *scales, int V, int H, int rows_per_slab,
-                                 double *partial) {
+__global__ void colsum_q8_kernel(const uint8_t *raw, int V, int H, int rows_per_slab, double *partial) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= H) return;
+  const int nb = H / 32;
   const int r0 = blockIdx.y * rows_per_slab, r1 = min(V, r0 + rows_per_slab);
   double s = 0.0;
   for (int r = r0; r < r1; ++r) {
-    const float d = __half2float(scales[((size_t)(r >> 7) * (H >> 5) + (c >> 5)) * 128 + (r & 127)]);
-    s += (double)(d * (float)q[(size_t)r * H + c]);
+    const uint8_t *blk = raw + (size_t)r * nb * 34 + (c >> 5) * 34;
+    const unsigned short db = (unsigned short)blk[0] | ((unsigned short)blk[1] << 8);
+    const float d = __half2float(__ushort_as_half(db));
+    s += (double)(d * (float)(int8_t)blk[2 + (c & 31)]);
   }
   partial[(size_t)blockIdx.y * H + c] = s;
 }
@@ -122,6 +128,23 @@ __global__ void accept_kernel(int n, int block, const int32_t *draft, const int3
   bonus[i] = t[a];
 }
 
+// One 16-byte unit (8 bf16) per thread: row r, unit u of chunk kc of tile
+// -> byte ((tile * nck + kc) * 16384) + r * 128 + ((u ^ ((r & 1) << 2)) << 4),
+// the order the GEMV kernel reads its shared-memory stages in.
+__global__ void tile_weights_kernel(const uint4 *src, int M, int K, uint8_t *dst) {
+  const int nck = K / 64;
+  const long long id = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const int n_tiles = (M + 127) / 128;
+  if (id >= (long long)n_tiles * nck * 1024) return;
+  const int u = (int)(id & 7), r = (int)((id >> 3) & 127);
+  const long long tk = id >> 10;
+  const int kc = (int)(tk % nck), tile = (int)(tk / nck);
+  const int m = tile * 128 + r;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (m < M) v = src[((size_t)m * K + (size_t)kc * 64 + u * 8) / 8];
+  *reinterpret_cast<uint4 *>(dst + (size_t)tk * 16384 + r * 128 + ((u ^ ((r & 1) << 2)) << 4)) = v;
+}
+
 __global__ void fill_kernel(float *p, size_t n, float v) {
   const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   if (i < n) p[i] = v;
@@ -129,10 +152,11 @@ __global__ void fill_kernel(float *p, size_t n, float v) {
 
 }  // namespace
 
-cudaError_t launch_q8_repack(const uint8_t *raw, int32_t V, int32_t H, int8_t *q, __half *scales, int32_t Vpad,
-                             cudaStream_t s) {
-  const long long n = (long long)Vpad * (H / 32);
-  q8_repack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(raw, V, H, q, scales, Vpad);
+size_t q8_table_bytes(int32_t V, int32_t H) { return (size_t)((V + 127) / 128) * (H / 64) * kQ8Chunk; }
+
+cudaError_t launch_q8_repack(const uint8_t *raw, int32_t V, int32_t H, uint8_t *dst, cudaStream_t s) {
+  const long long n = (long long)((V + 127) / 128 * 128) * (H / 32);
+  q8_repack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(raw, V, H, dst);
   return cudaGetLastError();
 }
 
@@ -145,7 +169,7 @@ static cudaError_t colmean_common(const void *a, const __half *sc, bool q8, int3
   if (e != cudaSuccess) return e;
   dim3 grid((H + 127) / 128, slabs);
   if (q8)
-    colsum_q8_kernel<<<grid, 128, 0, s>>>(static_cast<const int8_t *>(a), sc, V, H, rps, partial);
+    colsum_q8_kernel<<<grid, 128, 0, s>>>(static_cast<const uint8_t *>(a), V, H, rps, partial);
   else
     colsum_bf16_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16 *>(a), V, H, rps, partial);
   colmean_finish_kernel<<<(H + 127) / 128, 128, 0, s>>>(partial, slabs, H, V, out);
@@ -154,9 +178,8 @@ static cudaError_t colmean_common(const void *a, const __half *sc, bool q8, int3
   return e;
 }
 
-cudaError_t launch_colmean_q8(const int8_t *q, const __half *scales, int32_t V, int32_t H, float *out,
-                              cudaStream_t s) {
-  return colmean_common(q, scales, true, V, H, out, s);
+cudaError_t launch_colmean_q8(const uint8_t *raw, int32_t V, int32_t H, float *out, cudaStream_t s) {
+  return colmean_common(raw, nullptr, true, V, H, out, s);
 }
 
 cudaError_t launch_colmean_bf16(const __nv_bfloat16 *w, int32_t V, int32_t H, float *out, cudaStream_t s) {
@@ -193,6 +216,14 @@ cudaError_t launch_row_stats(const float *x, int32_t rows, int32_t d, float2 *st
 cudaError_t launch_accept(int32_t n, int32_t block, const int32_t *draft, const int32_t *target, const int32_t *k,
                           int32_t *acc, int32_t *bonus, cudaStream_t s) {
   accept_kernel<<<(n + 127) / 128, 128, 0, s>>>(n, block, draft, target, k, acc, bonus);
+  return cudaGetLastError();
+}
+
+size_t tiled_bytes(int32_t M, int32_t K) { return (size_t)((M + 127) / 128) * (K / 64) * 16384; }
+
+cudaError_t launch_tile_weights(const __nv_bfloat16 *src, int32_t M, int32_t K, uint8_t *dst, cudaStream_t s) {
+  const long long n = (long long)((M + 127) / 128) * (K / 64) * 1024;
+  tile_weights_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(reinterpret_cast<const uint4 *>(src), M, K, dst);
   return cudaGetLastError();
 }
 
