@@ -332,7 +332,8 @@ fm_status run_gemv(fm_handle *h, const GemvArgs &a, cudaStream_t s, const char *
 
 int attn_splits(const fm_handle *h, int L) {
   int sp = (L + 127) / 128;
-  if (sp > h->max_splits) sp = h->max_splits;
+  if (sp > 8) sp = 8;  // one portable thread-block cluster per head
+  (void)h;
   return sp < 1 ? 1 : sp;
 }
 
@@ -354,13 +355,10 @@ fm_status run_attn(fm_handle *h, const float *Q, int ldq, const Seg2 &kv, int T,
   a.L_add = L_add;
   a.sp = sp;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
-  a.part_o = h->part_o;
-  a.part_ml = h->part_ml;
-  a.tickets = h->tickets + c.n_heads;
   a.out = out;
   a.ldo = c.dim;
   ProfScope ps(h, s, "attn.cross", (double)L_now * c.dim * 2 * 2 + 2.0 * T * c.dim * 4);
-  CK(launch_attn(a, s, true));
+  CK(launch_attn(a, L_now, s, true));
   ++h->last_launches;
   return FM_OK;
 }
@@ -911,6 +909,8 @@ fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens,
   StepParams p{};
   p.start = n_pend ? h->pend_start : 0;
   if (n_pend) h->pend_seq = -1;
+  // cache rows no kernel of this draft writes: below the pending rows / the anchor / the block
+  p.stable = n_pend ? p.start : pos;
   p.T = c.block;
   p.pos = pos;
   p.anchor = anchor;

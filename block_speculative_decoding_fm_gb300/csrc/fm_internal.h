@@ -21,7 +21,8 @@ struct StepParams {
   int32_t L;        // cross-attention keys
   int32_t anchor;   // draft: anchor token id
   int32_t start;    // append: first position
-  int32_t pad0, pad1, pad2;
+  int32_t stable;   // cache rows < stable are not written by any kernel of this call
+  int32_t pad1, pad2;
   const float *feats;  // append: feature rows [T][feat_dim]
   int32_t *tokens;     // draft: where the argmax tokens go [T]
 };
@@ -119,15 +120,12 @@ struct AttnArgs {
   int32_t ldq;
   const __half *Kc, *Vc;   // [n_heads][max_ctx][hd]
   int32_t max_ctx, n_heads, hd;
-  int32_t splits;          // CTAs per head
+  int32_t splits;          // CTAs per head (one thread-block cluster, <= 8)
   int32_t T_const;
   int32_t L_src;           // 0: sp->L, 1: sp->pos + 1 (FlashMap keys 0..pos)
   int32_t L_add;
   const StepParams *sp;
   float scale_log2;        // log2(e) / sqrt(hd)
-  float *part_o;           // [n_heads][splits][kMaxT][hd]
-  float2 *part_ml;         // [n_heads][splits][kMaxT] (max (log2 domain), sum)
-  int32_t *tickets;        // [n_heads]
   float *out;              // [T][ldo]
   int32_t ldo;
 };
@@ -155,7 +153,7 @@ struct LmArgs {
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t s, bool pdl);
 size_t gemv_smem_bytes(const GemvArgs &a, int mt);
-cudaError_t launch_attn(const AttnArgs &a, cudaStream_t s, bool pdl);
+cudaError_t launch_attn(const AttnArgs &a, int L_now, cudaStream_t s, bool pdl);
 cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t s, bool pdl);
 int lmhead_grid(const LmArgs &a, int n_sm);
 

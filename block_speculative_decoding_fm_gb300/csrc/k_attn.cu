@@ -4,12 +4,16 @@
 //   O[t] = softmax_j(q_t . k_j / sqrt(hd)) v_j   over cache rows j < L, no mask,
 // as the pages do with one workgroup per (head, row) and all scores in shared
 // memory (flashmap_drafter.js ``attn``, L <= 4096).  Here the keys are split
-// across CTAs (flash-decoding): each (head, split) CTA streams its share of the
-// head-major f16 cache through shared memory with cp.async, computes scores
-// and P.V on the tensor cores (f16 m16n8k16, queries and probabilities split
-// into f16 hi + lo), keeps an online softmax (running max / sum, rescaled as
-// the MTP head's attention kernel does on ternary_bonsai_2_mtp.js), and the
-// last CTA of a head merges the splits in a fixed order.  Any L is handled.
+// across the CTAs of one thread-block cluster per head (flash-decoding): each
+// CTA streams its share of the head-major f16 cache through shared memory with
+// cp.async (rows that no kernel of the current call writes are requested before
+// griddepcontrol.wait), computes scores and P.V on the tensor cores (f16
+// m16n8k16, queries and probabilities split into f16 hi + lo), keeps an online
+// softmax (running max / sum, rescaled as the MTP head attention kernel on
+// ternary_bonsai_2_mtp.js does), and the cluster merges its partial results
+// through distributed shared memory in a fixed order.  Any L is handled.
+#include <cooperative_groups.h>
+
 #include "dev_common.cuh"
 #include "fm_internal.h"
 
@@ -27,13 +31,14 @@ __device__ __forceinline__ uint32_t vslot(int r, int u, int hd) {  // V tile: XO
   return r * hd * 2 + ((u ^ (r & 7)) << 4);
 }
 
+// stage rows [rlo, rhi) of the 64-key tile starting at k0 (rows past kend are zero-filled)
 template <int HD>
 __device__ __forceinline__ void issue_kv(const AttnArgs &a, int head, uint32_t kbuf, uint32_t vbuf, int k0,
-                                         int kend) {
+                                         int kend, int rlo = 0, int rhi = kKeys) {
   constexpr int U = HD / 8;  // 16-byte units per row
   const __half *kb = a.Kc + (size_t)head * a.max_ctx * HD;
   const __half *vb = a.Vc + (size_t)head * a.max_ctx * HD;
-  for (int i = threadIdx.x; i < kKeys * U; i += kThreads) {
+  for (int i = threadIdx.x + rlo * U; i < rhi * U; i += kThreads) {
     const int r = i / U, u = i - r * U;
     const int key = k0 + r;
     const bool ok = key < kend;
@@ -45,7 +50,7 @@ __device__ __forceinline__ void issue_kv(const AttnArgs &a, int head, uint32_t k
 
 }  // namespace
 
-template <int HD>
+template <int HD, int NS>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NT = HD / 8;        // n8 tiles of the output
@@ -56,21 +61,31 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t tile_bytes = kKeys * HD * 2;
-  const uint32_t kb0 = sbase, vb0 = sbase + tile_bytes, kb1 = sbase + 2 * tile_bytes, vb1 = sbase + 3 * tile_bytes;
-  const uint32_t qhi = sbase + 4 * tile_bytes, qlo = qhi + 16 * QS * 2;
+  auto kbuf = [&](int i) { return sbase + 2 * i * tile_bytes; };  // NS stages of (K tile, V tile)
+  auto vbuf = [&](int i) { return sbase + (2 * i + 1) * tile_bytes; };
+  const uint32_t kb0 = kbuf(0), vb0 = vbuf(0);
+  const uint32_t qhi = sbase + 2 * NS * tile_bytes, qlo = qhi + 16 * QS * 2;
   float *merge = reinterpret_cast<float *>(smem);  // reused after the key loop
 
   pdl_trigger();
-  pdl_wait();
-  const int T = a.T_const > 0 ? a.T_const : a.sp->T;
+  // the per-call values were uploaded before the chain started
   const int L = (a.L_src == 0 ? a.sp->L : a.sp->pos + 1) + a.L_add;
   int per = (L + a.splits - 1) / a.splits;
   per = (per + 15) & ~15;
   const int kbeg = min(L, split * per), kend = min(L, kbeg + per);
   const int nst = (kend - kbeg + kKeys - 1) / kKeys;
-
-  if (nst > 0) issue_kv<HD>(a, head, kb0, vb0, kbeg, kend);
+  // rows below `stable` are not written by this call's kernels: fetch them now
+  const int pre = nst > 0 ? max(0, min(kKeys, a.sp->stable - kbeg)) : 0;
+  if (pre > 0) issue_kv<HD>(a, head, kb0, vb0, kbeg, kend, 0, pre);
   cp_async_commit();
+  pdl_wait();
+  const int T = a.T_const > 0 ? a.T_const : a.sp->T;
+  if (nst > 0 && pre < kKeys) issue_kv<HD>(a, head, kb0, vb0, kbeg, kend, pre, kKeys);
+  cp_async_commit();
+  for (int st = 1; st < NS - 1; ++st) {
+    if (st < nst) issue_kv<HD>(a, head, kbuf(st), vbuf(st), kbeg + st * kKeys, kend);
+    cp_async_commit();
+  }
 
   // queries -> f16 hi / lo (rows >= T are zero)
   for (int i = threadIdx.x; i < 16 * HD; i += kThreads) {
@@ -88,10 +103,11 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
 
   for (int st = 0; st < nst; ++st) {
-    const uint32_t kb = (st & 1) ? kb1 : kb0, vb = (st & 1) ? vb1 : vb0;
-    if (st + 1 < nst) issue_kv<HD>(a, head, (st & 1) ? kb0 : kb1, (st & 1) ? vb0 : vb1, kbeg + (st + 1) * kKeys, kend);
+    const uint32_t kb = kbuf(st % NS), vb = vbuf(st % NS);
+    const int nx = st + NS - 1;
+    if (nx < nst) issue_kv<HD>(a, head, kbuf(nx % NS), vbuf(nx % NS), kbeg + nx * kKeys, kend);
     cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<NS - 1>();
     __syncthreads();
 
     // scores for keys 16w .. 16w+15 of this stage
@@ -202,9 +218,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     mml[(w * 16 + g + 8) * 2 + 1] = l_r[1];
   }
   __syncthreads();
-  float *po = a.part_o + ((size_t)(head * a.splits + split) * kMaxT) * HD;
-  float2 *pml = a.part_ml + (size_t)(head * a.splits + split) * kMaxT;
-  for (int i = threadIdx.x; i < T * (HD / 4); i += kThreads) {
+  // this CTA's partial (unnormalised O, running max in the log2 domain, sum) per row
+  float *co = mml + 4 * 16 * 2;            // [16][HD]
+  float *cml = co + 16 * HD;               // [16][2]
+  for (int i = threadIdx.x; i < 16 * (HD / 4); i += kThreads) {
     const int t = i / (HD / 4), d = 4 * (i - t * (HD / 4));
     float M = -INFINITY;
 #pragma unroll
@@ -222,91 +239,73 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       acc.w += f * src[3];
       lsum += f * mml[(ww * 16 + t) * 2 + 1];
     }
-    __stcg(reinterpret_cast<float4 *>(po + t * HD + d), acc);
-    if (d == 0) __stcg(pml + t, make_float2(M, lsum));
+    *reinterpret_cast<float4 *>(co + t * HD + d) = acc;
+    if (d == 0) {
+      cml[t * 2] = M;
+      cml[t * 2 + 1] = lsum;
+    }
   }
-
-  // the last split of this head combines all splits in order
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int old = atomicAdd(a.tickets + head, 1);
-    s_last = old == a.splits - 1;
-    if (s_last) atomicExch(a.tickets + head, 0);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const float *pob = a.part_o + (size_t)head * a.splits * kMaxT * HD;
-  const float2 *pmb = a.part_ml + (size_t)head * a.splits * kMaxT;
-  // (max, sum) of every split and row -> shared memory, then per-row weights
-  float *fm_ = merge;                      // [splits][16] weight of split sp for row t
-  float *fl_ = merge + a.splits * 16;      // [splits][16] partial sums
-  for (int i = threadIdx.x; i < a.splits * T; i += kThreads) {
-    const int sp = i / T, t = i - sp * T;
-    const float2 ml = __ldcg(pmb + sp * kMaxT + t);
-    fm_[sp * 16 + t] = ml.x;
-    fl_[sp * 16 + t] = ml.y;
-  }
-  __syncthreads();
-  if (threadIdx.x < T) {
-    const int t = threadIdx.x;
+  // merge the splits of this head through distributed shared memory: rank r
+  // finishes rows t = r, r + splits, ... reading every CTA's partial in rank order
+  cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+  cluster.sync();
+  const int rank = (int)cluster.block_rank();
+  const int ns = a.splits;
+  constexpr int PL = HD / 32;  // values per lane
+  for (int t = rank + ns * w; t < T; t += ns * (kThreads / 32)) {
     float M = -INFINITY;
-    for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, fm_[sp * 16 + t]);
+    for (int r = 0; r < ns; ++r) M = fmaxf(M, cluster.map_shared_rank(cml, r)[t * 2]);
     float lsum = 0.f;
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float mw = fm_[sp * 16 + t];
-      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      fm_[sp * 16 + t] = f;
-      lsum += f * fl_[sp * 16 + t];
+    float acc[PL];
+#pragma unroll
+    for (int e = 0; e < PL; ++e) acc[e] = 0.f;
+    for (int r = 0; r < ns; ++r) {
+      const float *rml = cluster.map_shared_rank(cml, r);
+      const float mr = rml[t * 2];
+      const float f = mr == -INFINITY ? 0.f : exp2f(mr - M);
+      lsum += f * rml[t * 2 + 1];
+      const float *ro = cluster.map_shared_rank(co, r) + t * HD + PL * lane;
+#pragma unroll
+      for (int e = 0; e < PL; ++e) acc[e] += f * ro[e];
     }
     const float inv = 1.f / lsum;
-    for (int sp = 0; sp < a.splits; ++sp) fm_[sp * 16 + t] *= inv;
+    float *dst = a.out + (size_t)t * a.ldo + head * HD + PL * lane;
+#pragma unroll
+    for (int e = 0; e < PL; ++e) dst[e] = acc[e] * inv;
   }
-  __syncthreads();
-  // out[t][4 d4 .. 4 d4 + 3] = sum over splits of weight * partial O (independent vector loads)
-  for (int i = threadIdx.x; i < T * (HD / 4); i += kThreads) {
-    const int t = i / (HD / 4), d4 = i - t * (HD / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float f = fm_[sp * 16 + t];
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(pob + ((size_t)sp * kMaxT + t) * HD) + d4);
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
-    }
-    *reinterpret_cast<float4 *>(a.out + (size_t)t * a.ldo + head * HD + 4 * d4) = acc;
-  }
+  cluster.sync();
 }
 
-cudaError_t launch_attn(const AttnArgs &a, cudaStream_t st, bool pdl) {
+cudaError_t launch_attn(const AttnArgs &a, int L_now, cudaStream_t st, bool pdl) {
   const int HD = a.hd;
   const size_t tile = (size_t)kKeys * HD * 2;
-  size_t smem = 4 * tile + 2 * 16 * (HD + 32) * 2;
-  const size_t merge = (size_t)4 * 16 * HD * 4 + 4 * 16 * 2 * 4;
+  // deeper ring when each CTA streams many key tiles
+  const int per_cta = (L_now + a.splits - 1) / a.splits;
+  const int NS = per_cta > 4 * kKeys ? 4 : 2;
+  size_t smem = 2 * NS * tile + 2 * 16 * (HD + 32) * 2;
+  const size_t merge = (size_t)4 * 16 * HD * 4 + 4 * 16 * 2 * 4 + (size_t)16 * HD * 4 + 16 * 2 * 4;
   if (merge > smem) smem = merge;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_heads, a.splits, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = a.splits;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e;
-  if (HD == 128) {
-    e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cfg.numAttrs = pdl ? 2 : 1;
+  auto go = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<128>, a);
-  }
-  e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, attn_kernel<64>, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
+  };
+  if (HD == 128) return NS == 4 ? go(attn_kernel<128, 4>) : go(attn_kernel<128, 2>);
+  return NS == 4 ? go(attn_kernel<64, 4>) : go(attn_kernel<64, 2>);
 }
 
 }  // namespace fm
