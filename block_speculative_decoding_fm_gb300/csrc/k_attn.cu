@@ -110,8 +110,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     cp_async_wait<NS - 1>();
     __syncthreads();
 
-    // scores for keys 16w .. 16w+15 of this stage
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // scores for keys 16w .. 16w+15 of this stage (four independent chains per n-tile)
+    float sp[2][4][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sp[j][u][0] = sp[j][u][1] = sp[j][u][2] = sp[j][u][3] = 0.f;
 #pragma unroll
     for (int c = 0; c < HD / 64; ++c) {
       uint4 blo[2], bhi[2];
@@ -128,10 +132,17 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          mma_f16(s[j], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj), word(bhi[j], jj));
-          mma_f16(s[j], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj), word(bhi[j], jj));
+          const int ch = (jj & 1) * 2;
+          mma_f16(sp[j][ch], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj), word(bhi[j], jj));
+          mma_f16(sp[j][ch + 1], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj),
+                  word(bhi[j], jj));
         }
     }
+    float s[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[j][e] = (sp[j][0][e] + sp[j][2][e]) + (sp[j][1][e] + sp[j][3][e]);
     // mask, scale into the log2 domain, online softmax (rows g and g + 8)
     const int key0 = kbeg + st * kKeys + 16 * w;
     float rmax[2] = {-INFINITY, -INFINITY};

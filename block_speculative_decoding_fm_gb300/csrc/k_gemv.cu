@@ -93,40 +93,58 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, int T, int m0, int k0,
   const __nv_bfloat16 *nw = a.nw;
   const __nv_bfloat16 *nw2 = a.nw2;
   if (a.amode == A_RMS2 && a.nw_rows > 0) nw2 += (size_t)(m0 / a.nw_rows) * a.K;
-  for (int i = threadIdx.x; i < rows * quads; i += kThreads) {
-    const int t = i / quads, kq = (i - t * quads) * 4;
-    const int k = k0 + kq;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (t < T) {
-      if (a.amode == A_ROW_Q8 || a.amode == A_ROW_BF16) {
-        if (t == 0) {
-          const int r = a.sp->anchor;
-          const size_t chunk = (size_t)(r >> 7) * (a.K / 64) + (k >> 6);
-          const int rr = r & 127, kk = k & 63;
-          if (a.amode == A_ROW_Q8) {
-            const uint8_t *base = a.tq8 + chunk * kQ8Chunk;
-            const char4 q = *reinterpret_cast<const char4 *>(base + q8_slot(rr, kk));
-            const float d = __half2float(
-                *reinterpret_cast<const __half *>(base + kTile * 64 + (kk >> 5) * 256 + rr * 2));
-            v[0] = d * q.x; v[1] = d * q.y; v[2] = d * q.z; v[3] = d * q.w;
-          } else {
-            const uint8_t *base = a.tb + chunk * 16384;
-            const uint2 u = *reinterpret_cast<const uint2 *>(base + w_slot(rr, kk));
-            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-            v[0] = __low2float(p0); v[1] = __high2float(p0); v[2] = __low2float(p1); v[3] = __high2float(p1);
-          }
-        }
-      } else {
-        const bool second = a.split > 0 && t >= a.split;
-        const float *xr = second ? a.X2 + (size_t)(t - a.split) * a.ldx : X + (size_t)t * a.ldx;
-        const float4 x = __ldcg(reinterpret_cast<const float4 *>(xr + k));
-        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-        if (a.amode == A_RMS) {
-          const float r = s.stat_rs[t];
-          const __nv_bfloat16 *w = second ? a.nw_alt : nw;
+  // each thread handles up to kBatch quads; all of its loads are issued before
+  // any of them is used so the L2 round trips overlap
+  constexpr int kBatch = 8;
+  for (int i0 = threadIdx.x; i0 < rows * quads; i0 += kThreads * kBatch) {
+    float4 xv[kBatch];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v[e] = v[e] * r * __bfloat162float(w[k + e]);
+    for (int bi = 0; bi < kBatch; ++bi) {
+      const int i = i0 + bi * kThreads;
+      xv[bi] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < rows * quads) {
+        const int t = i / quads, k = k0 + (i - t * quads) * 4;
+        if (t < T && a.amode != A_ROW_Q8 && a.amode != A_ROW_BF16) {
+          const bool second = a.split > 0 && t >= a.split;
+          const float *xr = second ? a.X2 + (size_t)(t - a.split) * a.ldx : X + (size_t)t * a.ldx;
+          xv[bi] = __ldcg(reinterpret_cast<const float4 *>(xr + k));
+        }
+      }
+    }
+#pragma unroll
+    for (int bi = 0; bi < kBatch; ++bi) {
+      const int i = i0 + bi * kThreads;
+      if (i >= rows * quads) break;
+      const int t = i / quads, kq = (i - t * quads) * 4;
+      const int k = k0 + kq;
+      float v[4] = {xv[bi].x, xv[bi].y, xv[bi].z, xv[bi].w};
+      if (t < T) {
+        if (a.amode == A_ROW_Q8 || a.amode == A_ROW_BF16) {
+          v[0] = v[1] = v[2] = v[3] = 0.f;
+          if (t == 0) {
+            const int r = a.sp->anchor;
+            const size_t chunk = (size_t)(r >> 7) * (a.K / 64) + (k >> 6);
+            const int rr = r & 127, kk = k & 63;
+            if (a.amode == A_ROW_Q8) {
+              const uint8_t *base = a.tq8 + chunk * kQ8Chunk;
+              const char4 q = *reinterpret_cast<const char4 *>(base + q8_slot(rr, kk));
+              const float d = __half2float(
+                  *reinterpret_cast<const __half *>(base + kTile * 64 + (kk >> 5) * 256 + rr * 2));
+              v[0] = d * q.x; v[1] = d * q.y; v[2] = d * q.z; v[3] = d * q.w;
+            } else {
+              const uint8_t *base = a.tb + chunk * 16384;
+              const uint2 u = *reinterpret_cast<const uint2 *>(base + w_slot(rr, kk));
+              const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+              const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+              v[0] = __low2float(p0); v[1] = __high2float(p0); v[2] = __low2float(p1); v[3] = __high2float(p1);
+            }
+          }
+        } else if (a.amode == A_RMS) {
+          const bool second = a.split > 0 && t >= a.split;
+          const float r = s.stat_rs[t];
+          const __nv_bfloat16 *wv = second ? a.nw_alt : nw;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = v[e] * r * __bfloat162float(wv[k + e]);
         } else if (a.amode == A_RMS2) {
           const float r1 = s.stat_mu[t], r2 = s.stat_rs[t];
 #pragma unroll
@@ -142,22 +160,26 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, int T, int m0, int k0,
           v[3] = (v[3] - mu) * r * (1.f + sc.w) + sh.w;
         }
       }
-    }
-    __nv_bfloat16 h[4], l[4];
+      __nv_bfloat16 h[4], l[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
-    const uint32_t off = (uint32_t)(t * lda + kq) * 2;
-    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s.ahi + off), "r"(pack_bf16(h[0], h[1])),
-                 "r"(pack_bf16(h[2], h[3])));
-    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s.alo + off), "r"(pack_bf16(l[0], l[1])),
-                 "r"(pack_bf16(l[2], l[3])));
+      for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
+      const uint32_t off = (uint32_t)(t * lda + kq) * 2;
+      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s.ahi + off), "r"(pack_bf16(h[0], h[1])),
+                   "r"(pack_bf16(h[2], h[3])));
+      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s.alo + off), "r"(pack_bf16(l[0], l[1])),
+                   "r"(pack_bf16(l[2], l[3])));
+    }
   }
 }
 
 // One 64-wide chunk: warp w owns weight rows 16w .. 16w+15 (two n8 tiles).
+// Legacy mma.sync has a long latency on this part, so the products go to kNC
+// independent accumulator chains per n-tile (hi / lo x even / odd k16 step),
+// summed once at the end of the tile.
+constexpr int kNC = 4;
 template <int MT>
 __device__ __forceinline__ void compute_chunk(uint32_t wst, const Smem &s, int lda, int acol,
-                                              float (&acc)[MT][2][4]) {
+                                              float (&acc)[MT][2][kNC][4]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   uint4 blo[2], bhi[2];
@@ -179,9 +201,10 @@ __device__ __forceinline__ void compute_chunk(uint32_t wst, const Smem &s, int l
     for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        mma_bf16(acc[mt][j], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj),
+        const int ch = (jj & 1) * 2;
+        mma_bf16(acc[mt][j][ch], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj),
                  word(bhi[j], jj));
-        mma_bf16(acc[mt][j], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj),
+        mma_bf16(acc[mt][j][ch + 1], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj),
                  word(bhi[j], jj));
       }
     }
@@ -358,7 +381,7 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
 }  // namespace
 
 template <int MT>
-__global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ GemvArgs a, const int S) {
+__global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a, const int S) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tile = blockIdx.x;
   const int m0 = tile * kTile;
@@ -397,13 +420,15 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
   pdl_trigger();
   __syncthreads();
 
-  float acc[MT][2][4];
+  float acc[MT][2][kNC][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
+      for (int c = 0; c < kNC; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][j][c][e] = 0.f;
 
   pdl_wait();
   const int T = a.T_const > 0 ? a.T_const : a.sp->T;
@@ -443,9 +468,11 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
       for (int j = 0; j < 2; ++j) {
         const int col = 16 * warp + 8 * j + 2 * q;
         const int t0 = 16 * mt + g;
-        *reinterpret_cast<float2 *>(s.cs_ptr + t0 * kCsStride + col) = make_float2(acc[mt][j][0], acc[mt][j][1]);
-        *reinterpret_cast<float2 *>(s.cs_ptr + (t0 + 8) * kCsStride + col) =
-            make_float2(acc[mt][j][2], acc[mt][j][3]);
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = (acc[mt][j][0][e] + acc[mt][j][2][e]) + (acc[mt][j][1][e] + acc[mt][j][3][e]);
+        *reinterpret_cast<float2 *>(s.cs_ptr + t0 * kCsStride + col) = make_float2(v[0], v[1]);
+        *reinterpret_cast<float2 *>(s.cs_ptr + (t0 + 8) * kCsStride + col) = make_float2(v[2], v[3]);
       }
   }
   __syncthreads();
@@ -458,10 +485,18 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
   if (warp < kThreads / 32) {
     for (int t = rank + ks * warp; t < T; t += ks * (kThreads / 32)) {
       float v[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int r = 0; r < ks; ++r) {
-        const float *src = ks > 1 ? cluster.map_shared_rank(s.cs_ptr, r) : s.cs_ptr;
-        const float4 x = *reinterpret_cast<const float4 *>(src + t * kCsStride + 4 * lane);
-        v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+      float4 part[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {  // all partial rows requested before any is summed (ks <= 8)
+        part[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < ks) {
+          const float *src = ks > 1 ? cluster.map_shared_rank(s.cs_ptr, r) : s.cs_ptr;
+          part[r] = *reinterpret_cast<const float4 *>(src + t * kCsStride + 4 * lane);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        v[0] += part[r].x; v[1] += part[r].y; v[2] += part[r].z; v[3] += part[r].w;
       }
       epilogue_unit(a, t, m0, v, tile);
     }

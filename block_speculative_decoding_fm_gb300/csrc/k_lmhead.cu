@@ -144,18 +144,21 @@ __global__ void __launch_bounds__(kAll, 1) lmhead_kernel(const __grid_constant__
               uint32_t wq[4];
               i8x4_to_f16x4(raw.x, wq[0], wq[1]);
               i8x4_to_f16x4(raw.y, wq[2], wq[3]);
-              float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_f16(p0, word(h0, 0), word(h1, 0), word(h0, 1), word(h1, 1), wq[0], wq[1]);
-              mma_f16(p1, word(h0, 2), word(h1, 2), word(h0, 3), word(h1, 3), wq[2], wq[3]);
-              mma_f16(p0, word(l0, 0), word(l1, 0), word(l0, 1), word(l1, 1), wq[0], wq[1]);
-              mma_f16(p1, word(l0, 2), word(l1, 2), word(l0, 3), word(l1, 3), wq[2], wq[3]);
+              // four independent products (k16 step x hi / lo), summed after
+              float p[4][4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) p[u][0] = p[u][1] = p[u][2] = p[u][3] = 0.f;
+              mma_f16(p[0], word(h0, 0), word(h1, 0), word(h0, 1), word(h1, 1), wq[0], wq[1]);
+              mma_f16(p[1], word(h0, 2), word(h1, 2), word(h0, 3), word(h1, 3), wq[2], wq[3]);
+              mma_f16(p[2], word(l0, 0), word(l1, 0), word(l0, 1), word(l1, 1), wq[0], wq[1]);
+              mma_f16(p[3], word(l0, 2), word(l1, 2), word(l0, 3), word(l1, 3), wq[2], wq[3]);
               const uint32_t sw = lds32(buf + soff[j] + b * 256);
               const __half2 d2 = *reinterpret_cast<const __half2 *>(&sw);
               const float d0 = __low2float(d2), d1 = __high2float(d2);
-              acc[j][0] += d0 * (p0[0] + p1[0]);
-              acc[j][1] += d1 * (p0[1] + p1[1]);
-              acc[j][2] += d0 * (p0[2] + p1[2]);
-              acc[j][3] += d1 * (p0[3] + p1[3]);
+              acc[j][0] += d0 * ((p[0][0] + p[1][0]) + (p[2][0] + p[3][0]));
+              acc[j][1] += d1 * ((p[0][1] + p[1][1]) + (p[2][1] + p[3][1]));
+              acc[j][2] += d0 * ((p[0][2] + p[1][2]) + (p[2][2] + p[3][2]));
+              acc[j][3] += d1 * ((p[0][3] + p[1][3]) + (p[2][3] + p[3][3]));
             }
           }
         } else {
@@ -170,15 +173,25 @@ __global__ void __launch_bounds__(kAll, 1) lmhead_kernel(const __grid_constant__
                       h3 = lds128(ahi + r1 + 64);
           const uint4 l0 = lds128(alo + r0), l1 = lds128(alo + r1), l2 = lds128(alo + r0 + 64),
                       l3 = lds128(alo + r1 + 64);
+          float p[2][4][4];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) p[j][u][0] = p[j][u][1] = p[j][u][2] = p[j][u][3] = 0.f;
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-              mma_bf16(acc[j], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj),
+              const int ch = (jj & 1) * 2;
+              mma_bf16(p[j][ch], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj),
                        word(bhi[j], jj));
-              mma_bf16(acc[j], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj),
+              mma_bf16(p[j][ch + 1], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj),
                        word(bhi[j], jj));
             }
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][e] += (p[j][0][e] + p[j][2][e]) + (p[j][1][e] + p[j][3][e]);
         }
       }
       __syncwarp();
