@@ -127,15 +127,74 @@ __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x)));
 }
 
-// byte offset of int8 column k (0..63) of row r (0..127) inside a Q8_0 table chunk
+// byte offset of int8 column k (0..63) of row r (0..127) inside a Q8_0 table
+// chunk: 64-byte rows whose four 16-byte pieces are permuted by (r / 2) % 4, so
+// eight consecutive rows reading the same piece hit eight distinct bank groups
 __host__ __device__ __forceinline__ uint32_t q8_slot(int r, int k) {
   const int piece = k >> 4;  // 16-byte piece: block k / 32, half (k % 32) / 16
-  return r * 64 + ((piece ^ (((r >> 1) & 1) << 1)) << 4) + (k & 15);
+  return r * 64 + ((piece ^ ((r >> 1) & 3)) << 4) + (k & 15);
 }
-// byte offset of bf16 column k (0..63) of row r inside a GEMV weight tile
-__host__ __device__ __forceinline__ uint32_t w_slot(int r, int k) {
-  const int u = k >> 3;
-  return r * 128 + ((u ^ ((r & 1) << 2)) << 4) + (k & 7) * 2;
+// Byte offset of 16-bit column k (0..63) of row r in a K-major tile stored in
+// the tensor cores' 128-byte-swizzle canonical layout: 8-row atoms of 1024
+// bytes, each row 128 bytes whose 16-byte units are permuted by unit ^ (row % 8).
+// GEMV weight tiles (128 x 64) and staged activation tiles use it.
+__host__ __device__ __forceinline__ uint32_t sw128(int r, int k) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 3) ^ r) & 7) << 4) + (k & 7) * 2);
+}
+__host__ __device__ __forceinline__ uint32_t w_slot(int r, int k) { return sw128(r, k); }
+
+// ---- tcgen05 (5th-generation tensor cores, TMEM accumulators) --------------
+// shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row atoms 1024 bytes apart
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row atom
+  d |= (uint64_t)1 << 46;            // descriptor version for the sm_100 family
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  return d;
+}
+// kind::f16 instruction descriptor: D f32, A/B bf16 (or f16), K-major, M x N
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+template <int NCOLS>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(slot), "n"(NCOLS) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+template <int NCOLS>
+__device__ __forceinline__ void tmem_free(uint32_t taddr) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "n"(NCOLS) : "memory");
+}
+// 32 consecutive f32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&f)[32]) {
+  uint32_t v[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
 }
 
 // (value, index) ordering for argmax: larger value wins, ties to the lower index.
@@ -170,15 +229,22 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait on an mbarrier phase.  Returns false (and raises *err) when the
-// clock budget runs out, or when another thread already raised *err.
+// clock budget runs out, or when another thread already raised *err.  The
+// error word lives in global memory, so it is polled only every few thousand
+// cycles: a load per spin would delay noticing the phase by an L2 round trip.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int32_t *err) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
+  long long next = t0 + 8192;
   while (!mbar_try(bar, parity)) {
-    if (*reinterpret_cast<volatile int32_t *>(err)) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
-      atomicExch(err, 1);
-      return false;
+    const long long t = clock64();
+    if (t > next) {
+      if (*reinterpret_cast<volatile int32_t *>(err)) return false;
+      if (t - t0 > kWaitBudgetCycles) {
+        atomicExch(err, 1);
+        return false;
+      }
+      next = t + 8192;
     }
   }
   return true;

@@ -311,8 +311,7 @@ GemvArgs gemv_base(const fm_handle *h, const __nv_bfloat16 *W, int M, int K, int
   while (ks < 8 && K % (64 * ks * 2) == 0 && tiles * ks * 2 <= 2 * h->n_sm) ks *= 2;
   a.ksplit = ks;
   a.Kc = K / ks;
-  const int mt = (T_const > 0 && T_const <= 16) ? 1 : 2;
-  a.Kp = a.Kc < (mt == 1 ? 512 : 256) ? a.Kc : (mt == 1 ? 512 : 256);
+  a.Kp = a.Kc < 256 ? a.Kc : 256;
   a.hd = h->cfg.head_dim;
   a.max_ctx = h->cfg.max_ctx;
   a.rope = h->rope;
@@ -948,7 +947,8 @@ fm_status check_config(fm_handle *h, const fm_config &c) {
   if (c.lm_format != FM_LM_BF16 && c.lm_format != FM_LM_Q8_0) return fail(h, FM_ERR_INVALID_ARG, "lm_format");
   if (c.max_seqs < 1) return fail(h, FM_ERR_INVALID_ARG, "max_seqs < 1");
   if (c.max_ctx < c.block + 2) return fail(h, FM_ERR_INVALID_ARG, "max_ctx < block + 2");
-  if (c.target_dim + 32 > 16000) return fail(h, FM_ERR_UNSUPPORTED, "target_dim too large for the lm_head tile");
+  if (c.target_dim > 3072)
+    return fail(h, FM_ERR_UNSUPPORTED, "target_dim above 3072 (the lm_head keeps the slot rows in shared memory)");
   return FM_OK;
 }
 

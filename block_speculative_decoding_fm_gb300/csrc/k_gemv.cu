@@ -12,9 +12,11 @@
 //   * the activations are transformed on the way in (RMSNorm, adaLN LayerNorm
 //     modulate, a table row) and split into bf16 hi + lo, so the bf16 tensor
 //     cores see f32-accurate operands: A*W = hi*W + lo*W, f32 accumulate;
-//   * the T rows are the MMA's M side (m16 tiles), 8 weight rows its N side;
-//     K is permuted inside each 64-wide chunk so that one 128-bit shared load
-//     gives a thread its fragments for four k16 steps;
+//   * the contraction runs on the 5th-generation tensor cores: one thread
+//     issues tcgen05.mma (M = 128 weight rows, N = the hi rows then the lo rows
+//     of the activations, K = 16) from shared-memory operands in the 128-byte
+//     swizzle layout into a TMEM accumulator; worker warps read it back with
+//     tcgen05.ld;
 //   * split-K across a thread-block cluster; the partial tiles are summed
 //     through distributed shared memory in a fixed order (deterministic);
 //   * fused epilogues: bias, exact GELU, gated residual + row statistics for
@@ -31,26 +33,25 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 256;   // consumer warps 0..7
-constexpr int kAll = kThreads + 32;  // + the producer warp
+constexpr int kWorkers = 128;          // warps 2..5: stage activations, read TMEM, epilogue
+constexpr int kAll = 64 + kWorkers;    // warp 0 streams weights, warp 1 owns TMEM and issues MMAs
+constexpr int kThreads = kWorkers;     // threads that share the epilogue loops
+constexpr int kWorkerBase = 64;        // first worker thread
+__device__ __forceinline__ int wtid() { return (int)threadIdx.x - kWorkerBase; }
 constexpr int kChunk = 64;                       // k per pipeline stage
 constexpr int kStageBytes = kTile * kChunk * 2;  // 16 KB of bf16 weights
 constexpr int kCsStride = kTile + 8;             // f32 partial tile row stride
 
-__host__ __device__ constexpr int a_stride(int kp) { return kp + 32; }  // bf16 elements; 64-byte pad
 
 struct Smem {
-  uint32_t ring, ahi, alo, cs;  // shared-space byte addresses
+  uint32_t bbuf[2];             // staged activation pieces (128-byte swizzle), double buffered
   float *cs_ptr;
   float *stat_mu, *stat_rs;     // [kMaxT]
 };
 
-// weight tile: row r (0..127) of chunk, 16-byte unit u (0..7) -> swizzled slot
-__device__ __forceinline__ uint32_t wslot(int r, int u) { return r * 128 + ((u ^ ((r & 1) << 2)) << 4); }
-
 // Row statistics of the input rows (sum over the producer's tiles, in double).
 __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
-  const int t = threadIdx.x;
+  const int t = wtid();
   if (t < kMaxT) {
     float m = 0.f, r = 1.f;
     if (t < T && (a.amode == A_RMS || a.amode == A_LNMOD || a.amode == A_RMS2)) {
@@ -84,11 +85,14 @@ __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
 }
 
 // Stage A[t][k0 .. k0 + kp) for all 16 * MT rows as bf16 hi / lo.
+// Stage activation columns k0 .. k0 + kp as the MMA's B operand: rows 0 .. 16MT-1
+// hold the bf16 hi parts, rows 16MT .. 32MT-1 the lo parts, one 64-column chunk
+// after another (each chunk 32MT rows x 128 bytes, 128-byte swizzle).
 template <int MT>
-__device__ void stage_a(const GemvArgs &a, const Smem &s, int T, int m0, int k0, int kp) {
+__device__ void stage_a(const GemvArgs &a, const Smem &s, uint32_t dst, int T, int m0, int k0, int kp) {
   const int rows = 16 * MT;
-  const int lda = a_stride(a.Kp);
   const int quads = kp >> 2;
+  constexpr int kThreads = kWorkers;
   const float *X = a.x_from_sp ? a.sp->feats : a.X;
   const __nv_bfloat16 *nw = a.nw;
   const __nv_bfloat16 *nw2 = a.nw2;
@@ -96,7 +100,7 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, int T, int m0, int k0,
   // each thread handles up to kBatch quads; all of its loads are issued before
   // any of them is used so the L2 round trips overlap
   constexpr int kBatch = 8;
-  for (int i0 = threadIdx.x; i0 < rows * quads; i0 += kThreads * kBatch) {
+  for (int i0 = wtid(); i0 < rows * quads; i0 += kThreads * kBatch) {
     float4 xv[kBatch];
 #pragma unroll
     for (int bi = 0; bi < kBatch; ++bi) {
@@ -163,50 +167,12 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, int T, int m0, int k0,
       __nv_bfloat16 h[4], l[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
-      const uint32_t off = (uint32_t)(t * lda + kq) * 2;
-      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s.ahi + off), "r"(pack_bf16(h[0], h[1])),
+      const uint32_t cbase = dst + (uint32_t)(kq >> 6) * (32 * MT * 128);
+      const int kk = kq & 63;
+      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(t, kk)), "r"(pack_bf16(h[0], h[1])),
                    "r"(pack_bf16(h[2], h[3])));
-      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(s.alo + off), "r"(pack_bf16(l[0], l[1])),
+      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(rows + t, kk)), "r"(pack_bf16(l[0], l[1])),
                    "r"(pack_bf16(l[2], l[3])));
-    }
-  }
-}
-
-// One 64-wide chunk: warp w owns weight rows 16w .. 16w+15 (two n8 tiles).
-// Legacy mma.sync has a long latency on this part, so the products go to kNC
-// independent accumulator chains per n-tile (hi / lo x even / odd k16 step),
-// summed once at the end of the tile.
-constexpr int kNC = 4;
-template <int MT>
-__device__ __forceinline__ void compute_chunk(uint32_t wst, const Smem &s, int lda, int acol,
-                                              float (&acc)[MT][2][kNC][4]) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = lane >> 2, q = lane & 3;
-  uint4 blo[2], bhi[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int r = 16 * w + 8 * j + g;
-    blo[j] = lds128(wst + wslot(r, q));
-    bhi[j] = lds128(wst + wslot(r, 4 + q));
-  }
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const uint32_t r0 = (uint32_t)((16 * mt + g) * lda + acol + 8 * q) * 2;
-    const uint32_t r1 = r0 + 8 * lda * 2;
-    const uint4 h0 = lds128(s.ahi + r0), h1 = lds128(s.ahi + r1);
-    const uint4 h2 = lds128(s.ahi + r0 + 64), h3 = lds128(s.ahi + r1 + 64);
-    const uint4 l0 = lds128(s.alo + r0), l1 = lds128(s.alo + r1);
-    const uint4 l2 = lds128(s.alo + r0 + 64), l3 = lds128(s.alo + r1 + 64);
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int ch = (jj & 1) * 2;
-        mma_bf16(acc[mt][j][ch], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj),
-                 word(bhi[j], jj));
-        mma_bf16(acc[mt][j][ch + 1], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj),
-                 word(bhi[j], jj));
-      }
     }
   }
 }
@@ -334,8 +300,8 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
   const int ks = hd + 4;  // padded row stride (floats) in shared memory, keeps float4 alignment
   float *qq = sm, *kk = sm + kMaxT * ks, *vv = sm + 2 * kMaxT * ks;
   const int q4 = hd / 4;
-  const bool consumer = threadIdx.x < kThreads;  // the producer warp only joins the barriers
-  for (int i = threadIdx.x; consumer && i < T * q4; i += kThreads) {
+  const bool consumer = wtid() >= 0;  // the weight and MMA warps only join the barriers
+  for (int i = wtid(); consumer && i < T * q4; i += kThreads) {
     const int t = i / q4, d = 4 * (i - t * q4);
     const float *row = a.Y + (size_t)t * a.ldy + head * hd + d;
     const float4 q = __ldcg(reinterpret_cast<const float4 *>(row));
@@ -347,7 +313,7 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
   }
   __syncthreads();
   // one warp per query row: lane l owns dims 4l .. 4l+3 (lanes beyond hd/4 hold zeros)
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, w = wtid() >> 5;
   const bool on = lane < q4;
   for (int t = w; consumer && t < T; t += kThreads / 32) {
     const float4 q = on ? *reinterpret_cast<const float4 *>(qq + t * ks + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -381,99 +347,122 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
 }  // namespace
 
 template <int MT>
-__global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a, const int S) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kAll, 1) gemv_kernel(const __grid_constant__ GemvArgs a, const int S) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int NR = 32 * MT;                 // B rows: hi rows then lo rows
+  constexpr int BCH = NR * 128;               // bytes of one 64-column B chunk
+  constexpr uint32_t IDESC = umma_idesc(128, NR, true);
   const int tile = blockIdx.x;
   const int m0 = tile * kTile;
   const int split = blockIdx.y;
   const int k_begin = split * a.Kc;
   const int nchunks = a.Kc / kChunk;
-  const int lda = a_stride(a.Kp);
+  const int cpp = a.Kp / kChunk;              // chunks per staged piece
+  const int npieces = (nchunks + cpp - 1) / cpp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t ring = base;
   Smem s;
-  s.ring = smem_u32(smem);
-  const uint32_t a_bytes = (uint32_t)(16 * MT) * lda * 2;
-  s.ahi = s.ring + S * kStageBytes;
-  s.alo = s.ahi + a_bytes;
-  s.cs = s.alo + a_bytes;
-  s.cs_ptr = reinterpret_cast<float *>(smem + S * kStageBytes + 2 * a_bytes);
+  s.bbuf[0] = ring + S * kStageBytes;
+  s.bbuf[1] = s.bbuf[0] + cpp * BCH;
+  s.cs_ptr = reinterpret_cast<float *>(gbase + S * kStageBytes + 2 * cpp * BCH);
   s.stat_mu = s.cs_ptr + 16 * MT * kCsStride;
   s.stat_rs = s.stat_mu + kMaxT;
   const uint32_t bars = smem_u32(s.stat_rs + kMaxT);
   auto full = [&](int i) { return bars + 8 * i; };
   auto empty = [&](int i) { return bars + 8 * (S + i); };
+  const uint32_t bfull0 = bars + 8 * (2 * S), bempty0 = bfull0 + 16, accfull = bfull0 + 32;
+  const uint32_t tslot = accfull + 8;
   const uint8_t *wsrc = a.Wt + ((size_t)tile * (a.K / kChunk) + k_begin / kChunk) * kStageBytes;
 
-  if (threadIdx.x == kThreads) {
+  if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full(i), 1);
-      mbar_init(empty(i), kThreads / 32);
+      mbar_init(empty(i), 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bfull0 + 8 * i, 1);
+      mbar_init(bempty0 + 8 * i, 1);
+    }
+    mbar_init(accfull, 1);
     mbar_fence_init();
     // weights do not depend on earlier kernels: start streaming them now
     for (int c = 0; c < S && c < nchunks; ++c) {
       mbar_expect_tx(full(c), kStageBytes);
-      bulk_g2s(s.ring + c * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(c));
+      bulk_g2s(ring + c * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(c));
     }
   }
+  if (warp == 1) tmem_alloc<NR>(tslot);
   pdl_trigger();
+  tc_fence_before();
   __syncthreads();
-
-  float acc[MT][2][kNC][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int c = 0; c < kNC; ++c)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][j][c][e] = 0.f;
-
+  tc_fence_after();
+  const uint32_t tmem = lds32(tslot);
   pdl_wait();
   const int T = a.T_const > 0 ? a.T_const : a.sp->T;
-  if (warp == kThreads / 32) {
-    // producer: refill each stage once its 8 consumer warps have released it
+
+  if (warp == 0) {
+    // weights: refill a stage once the MMAs that read it have completed
     if (lane == 0) {
       for (int c = S; c < nchunks; ++c) {
         const int st = c % S;
         if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
         mbar_expect_tx(full(st), kStageBytes);
-        bulk_g2s(s.ring + st * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(st));
+        bulk_g2s(ring + st * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(st));
       }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int st = c % S, piece = c / cpp, pb = piece & 1;
+        if (c % cpp == 0 && !mbar_wait_bounded(bfull0 + 8 * pb, (piece >> 1) & 1, a.err)) ok = false;
+        if (ok && !mbar_wait_bounded(full(st), (c / S) & 1, a.err)) ok = false;
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(ring + st * kStageBytes);
+        const uint64_t bd = umma_desc_sw128(s.bbuf[pb] + (c % cpp) * BCH);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk) umma_ss(tmem, ad + 2 * kk, bd + 2 * kk, IDESC, (c | kk) ? 1u : 0u);
+        umma_commit(empty(st));
+        if (c % cpp == cpp - 1 || c == nchunks - 1) umma_commit(bempty0 + 8 * pb);
+      }
+      umma_commit(accfull);
     }
   } else {
+    // workers: stage the activation pieces, then read the accumulator
     load_row_stats(a, T, s.stat_mu, s.stat_rs);
-    named_sync(1, kThreads);
-    const int cpp = a.Kp / kChunk;  // chunks per A piece
-    bool ok = true;
-    for (int c = 0; c < nchunks; ++c) {
-      if (c % cpp == 0) {
-        if (c) named_sync(1, kThreads);
-        const int kp = min(a.Kp, a.Kc - c * kChunk);
-        stage_a<MT>(a, s, T, m0, k_begin + c * kChunk, kp);
-        named_sync(1, kThreads);
-      }
-      const int st = c % S;
-      if (ok && !mbar_wait_bounded(full(st), (c / S) & 1, a.err)) ok = false;
-      if (ok) compute_chunk<MT>(s.ring + st * kStageBytes, s, lda, (c % cpp) * kChunk, acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty(st));
+    named_sync(1, kWorkers);
+    for (int p = 0; p < npieces; ++p) {
+      const int pb = p & 1;
+      if (p >= 2) mbar_wait_bounded(bempty0 + 8 * pb, ((p - 2) >> 1) & 1, a.err);
+      const int kp = min(a.Kp, a.Kc - p * a.Kp);
+      stage_a<MT>(a, s, s.bbuf[pb], T, m0, k_begin + p * a.Kp, kp);
+      fence_proxy_async();
+      named_sync(1, kWorkers);
+      if (wtid() == 0) mbar_arrive(bfull0 + 8 * pb);
     }
-    // partial tile -> shared memory
-    const int g = lane >> 2, q = lane & 3;
+    mbar_wait_bounded(accfull, 0, a.err);
+    tc_fence_after();
+    // TMEM lane = weight row; columns: hi rows then lo rows of the activations
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
+    if (MT == 1) {
+      float v[32];
+      tmem_ld32(taddr, v);   // columns 0..15 hi, 16..31 lo
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+      for (int t = 0; t < 16; ++t) s.cs_ptr[t * kCsStride + row] = v[t] + v[16 + t];
+    } else {
+      float hi[32], lo[32];
+      tmem_ld32(taddr, hi);        // columns 0..31 hi
+      tmem_ld32(taddr + 32, lo);   // columns 32..63 lo
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int col = 16 * warp + 8 * j + 2 * q;
-        const int t0 = 16 * mt + g;
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = (acc[mt][j][0][e] + acc[mt][j][2][e]) + (acc[mt][j][1][e] + acc[mt][j][3][e]);
-        *reinterpret_cast<float2 *>(s.cs_ptr + t0 * kCsStride + col) = make_float2(v[0], v[1]);
-        *reinterpret_cast<float2 *>(s.cs_ptr + (t0 + 8) * kCsStride + col) = make_float2(v[2], v[3]);
-      }
+      for (int t = 0; t < 32; ++t) s.cs_ptr[t * kCsStride + row] = hi[t] + lo[t];
+    }
+    tc_fence_before();
   }
   __syncthreads();
 
@@ -482,8 +471,9 @@ __global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __gri
   const int rank = ks > 1 ? (int)cluster.block_rank() : 0;
   if (ks > 1) cluster.sync();
 
-  if (warp < kThreads / 32) {
-    for (int t = rank + ks * warp; t < T; t += ks * (kThreads / 32)) {
+  if (warp >= 2) {
+    const int ew = warp - 2;
+    for (int t = rank + ks * ew; t < T; t += ks * (kWorkers / 32)) {
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       float4 part[8];
 #pragma unroll
@@ -524,23 +514,29 @@ __global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __gri
     for (int i = 0; i < heads_in_tile; ++i) {
       if (s_last[i] >= 0) {
         __threadfence();
-        self_attention_head(a, s_last[i], T, reinterpret_cast<float *>(smem));
+        self_attention_head(a, s_last[i], T, reinterpret_cast<float *>(gbase));
       }
     }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_free<NR>(tmem);
   }
 }
 
 static int gemv_stages(const GemvArgs &a, int mt) {
+  (void)mt;
   const int nchunks = a.Kc / kChunk;
-  const int cap = mt == 1 ? 4 : 3;  // two CTAs per SM
-  return nchunks < cap ? nchunks : cap;
+  return nchunks < 4 ? nchunks : 4;
 }
 
 size_t gemv_smem_bytes(const GemvArgs &a, int mt) {
   const int S = gemv_stages(a, mt);
-  const size_t a_bytes = (size_t)(16 * mt) * a_stride(a.Kp) * 2;
-  size_t bytes = (size_t)S * kStageBytes + 2 * a_bytes + (size_t)(16 * mt) * kCsStride * 4 + 2 * kMaxT * 4 + 16 * S;
-  const size_t attn = a.self_D > 0 ? (size_t)3 * kMaxT * (a.hd + 4) * 4 : 0;
+  const int cpp = a.Kp / kChunk;
+  size_t bytes = 1024 + (size_t)S * kStageBytes + 2 * (size_t)cpp * (32 * mt * 128) +
+                 (size_t)(16 * mt) * kCsStride * 4 + 2 * kMaxT * 4 + 16 * S + 64;
+  const size_t attn = 1024 + (size_t)3 * kMaxT * (a.hd + 4) * 4;
   return bytes > attn ? bytes : attn;
 }
 

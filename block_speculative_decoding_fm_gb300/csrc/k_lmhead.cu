@@ -5,13 +5,21 @@
 // separate argmaxRows pass (flashmap_drafter.js ``draft``; the table is Q8_0 in
 // the GGUF block format the MTP loader on ternary_bonsai_2_mtp.js repacks into
 // an int8 plane and a scale plane).  Here one persistent kernel streams the
-// table once: each CTA keeps Y (split into hi + lo 16-bit halves) resident in
-// shared memory, a producer warp streams 128-row x 64-column table chunks with
-// 1-D bulk TMA copies into an mbarrier ring, consumer warps run the
-// products on the tensor cores (Q8_0: int8 -> f16 exactly, per-32 block
-// partial sums scaled by the block's f16 scale; bf16: directly), and keeps a
-// running (value, index) best per row in registers.  The logits never reach
-// memory; pass two is the last CTA reducing the per-CTA bests.
+// table once and the logits never reach memory:
+//   * Y is split into hi + lo 16-bit halves and kept resident in shared memory
+//     as the B operand (N = 32: per group of 8 slots, 8 hi rows then 8 lo rows)
+//     in the tensor cores' 128-byte-swizzle K-major layout;
+//   * a producer warp streams 128-row x 64-column table chunks with 1-D bulk
+//     TMA copies into an mbarrier ring;
+//   * bf16 table: the chunk is already a swizzled K-major tile; one thread
+//     issues tcgen05.mma (M = 128 table rows) into a TMEM accumulator per tile;
+//   * Q8_0 table: converter warps turn each row's int8 block into f16 (exact)
+//     and store it into TMEM, which tcgen05.mma reads as the A operand; every
+//     32-column block has its own accumulator so its f16 scale is applied to
+//     the block's partial sums, in f32, by the same warps (one thread per table
+//     row and group of 8 slots), four chunks in flight;
+//   * each thread keeps a running (value, index) best per slot; pass two is
+//     the last CTA reducing the per-CTA bests.
 #include "dev_common.cuh"
 #include "fm_internal.h"
 
@@ -19,74 +27,68 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 256;        // consumer warps 0..7
-constexpr int kAll = kThreads + 32;  // + the producer warp
 constexpr int kChunk = 64;
-constexpr int kBfStage = kTile * kChunk * 2;
+constexpr int kBfStage = kTile * kChunk * 2;  // 16 KB bf16 chunk
+constexpr int kYChunk = 32 * 128;             // one 64-column chunk of the resident Y (32 rows x 128 B)
+constexpr int kNSlot = 4;                     // Q8: chunks in flight between conversion and epilogue
+constexpr int kLook = kNSlot - 1;             // Q8: conversion runs this many chunks ahead
+constexpr int kQ8Workers = 256;               // Q8: warps 2..9
+constexpr int kBfWorkers = 128;               // bf16: warps 2..5
+constexpr int kBase = 64;                     // warp 0: producer, warp 1: TMEM owner + MMA issuer
 
-__host__ __device__ constexpr int lm_stage_bytes(bool q8) { return q8 ? kQ8Chunk : kBfStage; }
+// B row of slot t (hi half; the lo half is 8 rows further)
+__device__ __forceinline__ int yrow(int t) { return (t >> 3) * 16 + (t & 7); }
 
-}  // namespace
+// tcgen05.mma with A in tensor memory (lane = A row, 32-bit columns hold K pairs)
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&f)[16]) {
+  uint32_t v[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+}
 
+// Y (f32 [T][ldy]) -> resident B operand: hi and lo halves (f16 for the Q8
+// table, bf16 for the bf16 table), slots >= T zero.
 template <bool Q8>
-__global__ void __launch_bounds__(kAll, 1) lmhead_kernel(const __grid_constant__ LmArgs a, const int S) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int SB = lm_stage_bytes(Q8);
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = lane >> 2, q = lane & 3;
-  const int H = a.H;
-  const int lda = H + 32;  // 16-bit elements per A row (64-byte pad)
-  const uint32_t ring = smem_u32(smem);
-  const uint32_t ahi = ring + S * SB, alo = ahi + 16 * lda * 2;
-  const uint32_t bars = alo + 16 * lda * 2;
-  auto full = [&](int i) { return bars + 8 * i; };
-  auto empty = [&](int i) { return bars + 8 * (S + i); };
-
-  const int n_tiles = (a.V + kTile - 1) / kTile;
-  const int kcs = H / kChunk;
-  const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int total = my_tiles * kcs;
-  const uint8_t *table = Q8 ? a.q8 : a.wb;
-  auto src_of = [&](int c) {
-    const int tile = blockIdx.x + (c / kcs) * gridDim.x;
-    return table + ((size_t)tile * kcs + (c % kcs)) * SB;
-  };
-
-  if (threadIdx.x == kThreads) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(full(i), 1);
-      mbar_init(empty(i), kThreads / 32);
+__device__ void stage_y(const LmArgs &a, uint32_t ybuf, int T, int tid, int nthreads) {
+  const int q4 = a.H >> 2;
+  constexpr int kBatch = 8;
+  for (int i0 = tid; i0 < 16 * q4; i0 += nthreads * kBatch) {
+    float4 y[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int i = i0 + b * nthreads;
+      const int t = i / q4, k = (i - t * q4) * 4;
+      y[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < 16 * q4 && t < T) y[b] = __ldcg(reinterpret_cast<const float4 *>(a.Y + (size_t)t * a.ldy + k));
     }
-    mbar_fence_init();
-    // the table does not depend on earlier kernels
-    for (int c = 0; c < S && c < total; ++c) {
-      mbar_expect_tx(full(c), SB);
-      bulk_g2s(ring + c * SB, src_of(c), SB, full(c));
-    }
-  }
-  pdl_trigger();
-  __syncthreads();
-  pdl_wait();
-  const int T = a.T_const > 0 ? a.T_const : a.sp->T;
-
-  float bv[2] = {-INFINITY, -INFINITY};  // running best for rows g and g + 8
-  int bi[2] = {0x7fffffff, 0x7fffffff};
-  if (w == kThreads / 32) {
-    if (lane == 0) {
-      for (int c = S; c < total; ++c) {
-        const int st = c % S;
-        if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
-        mbar_expect_tx(full(st), SB);
-        bulk_g2s(ring + st * SB, src_of(c), SB, full(st));
-      }
-    }
-  } else {
-    // Y -> 16-bit hi / lo, rows >= T zero
-    for (int i = threadIdx.x; i < 16 * (H >> 2); i += kThreads) {
-      const int t = i / (H >> 2), k = (i - t * (H >> 2)) * 4;
-      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < T) y = __ldcg(reinterpret_cast<const float4 *>(a.Y + (size_t)t * a.ldy + k));
-      const float v[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int i = i0 + b * nthreads;
+      if (i >= 16 * q4) break;
+      const int t = i / q4, k = (i - t * q4) * 4;
+      const float v[4] = {y[b].x, y[b].y, y[b].z, y[b].w};
       uint32_t hw[2], lw[2];
       if (Q8) {
         __half h[4], l[4];
@@ -101,148 +103,44 @@ __global__ void __launch_bounds__(kAll, 1) lmhead_kernel(const __grid_constant__
         hw[0] = pack_bf16(h[0], h[1]); hw[1] = pack_bf16(h[2], h[3]);
         lw[0] = pack_bf16(l[0], l[1]); lw[1] = pack_bf16(l[2], l[3]);
       }
-      const uint32_t off = (uint32_t)(t * lda + k) * 2;
-      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(ahi + off), "r"(hw[0]), "r"(hw[1]));
-      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(alo + off), "r"(lw[0]), "r"(lw[1]));
+      const uint32_t cb = ybuf + (uint32_t)(k >> 6) * kYChunk;
+      const int r = yrow(t);
+      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cb + sw128(r, k & 63)), "r"(hw[0]), "r"(hw[1]));
+      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cb + sw128(r + 8, k & 63)), "r"(lw[0]), "r"(lw[1]));
     }
-    named_sync(1, kThreads);
-
-    float acc[2][4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    // per-thread shared-memory offsets that do not change from chunk to chunk
-    uint32_t woff[2][2], soff[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int r = 16 * w + 8 * j + g;
-      if (Q8) {
-        woff[j][0] = q8_slot(r, 8 * q);        // block 0: columns 8q .. 8q+7
-        woff[j][1] = q8_slot(r, 32 + 8 * q);   // block 1
-      } else {
-        woff[j][0] = r * 128 + ((q ^ ((r & 1) << 2)) << 4);
-        woff[j][1] = r * 128 + (((4 + q) ^ ((r & 1) << 2)) << 4);
-      }
-      soff[j] = kTile * kChunk + (16 * w + 8 * j + 2 * q) * 2;
-    }
-    bool ok = true;
-    int tile = blockIdx.x, kc = 0;
-    for (int c = 0; c < total; ++c) {
-      const int st = c % S;
-      if (ok && !mbar_wait_bounded(full(st), (c / S) & 1, a.err)) ok = false;
-      const uint32_t buf = ring + st * SB;
-      if (ok) {
-        if (Q8) {
-#pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const uint32_t ar0 = (uint32_t)(g * lda + kc * kChunk + 32 * b + 8 * q) * 2;
-            const uint32_t ar1 = ar0 + 8 * lda * 2;
-            const uint4 h0 = lds128(ahi + ar0), h1 = lds128(ahi + ar1);
-            const uint4 l0 = lds128(alo + ar0), l1 = lds128(alo + ar1);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const uint2 raw = lds64(buf + woff[j][b]);
-              uint32_t wq[4];
-              i8x4_to_f16x4(raw.x, wq[0], wq[1]);
-              i8x4_to_f16x4(raw.y, wq[2], wq[3]);
-              // four independent products (k16 step x hi / lo), summed after
-              float p[4][4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) p[u][0] = p[u][1] = p[u][2] = p[u][3] = 0.f;
-              mma_f16(p[0], word(h0, 0), word(h1, 0), word(h0, 1), word(h1, 1), wq[0], wq[1]);
-              mma_f16(p[1], word(h0, 2), word(h1, 2), word(h0, 3), word(h1, 3), wq[2], wq[3]);
-              mma_f16(p[2], word(l0, 0), word(l1, 0), word(l0, 1), word(l1, 1), wq[0], wq[1]);
-              mma_f16(p[3], word(l0, 2), word(l1, 2), word(l0, 3), word(l1, 3), wq[2], wq[3]);
-              const uint32_t sw = lds32(buf + soff[j] + b * 256);
-              const __half2 d2 = *reinterpret_cast<const __half2 *>(&sw);
-              const float d0 = __low2float(d2), d1 = __high2float(d2);
-              acc[j][0] += d0 * ((p[0][0] + p[1][0]) + (p[2][0] + p[3][0]));
-              acc[j][1] += d1 * ((p[0][1] + p[1][1]) + (p[2][1] + p[3][1]));
-              acc[j][2] += d0 * ((p[0][2] + p[1][2]) + (p[2][2] + p[3][2]));
-              acc[j][3] += d1 * ((p[0][3] + p[1][3]) + (p[2][3] + p[3][3]));
-            }
-          }
-        } else {
-          uint4 blo[2], bhi[2];
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            blo[j] = lds128(buf + woff[j][0]);
-            bhi[j] = lds128(buf + woff[j][1]);
-          }
-          const uint32_t r0 = (uint32_t)(g * lda + kc * kChunk + 8 * q) * 2, r1 = r0 + 8 * lda * 2;
-          const uint4 h0 = lds128(ahi + r0), h1 = lds128(ahi + r1), h2 = lds128(ahi + r0 + 64),
-                      h3 = lds128(ahi + r1 + 64);
-          const uint4 l0 = lds128(alo + r0), l1 = lds128(alo + r1), l2 = lds128(alo + r0 + 64),
-                      l3 = lds128(alo + r1 + 64);
-          float p[2][4][4];
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) p[j][u][0] = p[j][u][1] = p[j][u][2] = p[j][u][3] = 0.f;
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const int ch = (jj & 1) * 2;
-              mma_bf16(p[j][ch], word(h0, jj), word(h1, jj), word(h2, jj), word(h3, jj), word(blo[j], jj),
-                       word(bhi[j], jj));
-              mma_bf16(p[j][ch + 1], word(l0, jj), word(l1, jj), word(l2, jj), word(l3, jj), word(blo[j], jj),
-                       word(bhi[j], jj));
-            }
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[j][e] += (p[j][0][e] + p[j][2][e]) + (p[j][1][e] + p[j][3][e]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty(st));
-      if (kc == kcs - 1) {
-        // tile finished: fold into the running best, optionally store the logits
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int v = tile * kTile + 16 * w + 8 * j + 2 * q + (e & 1);
-            const int row = g + 8 * (e >> 1);
-            if (v < a.V && row < T) {
-              if (a.logits) a.logits[(size_t)row * a.V + v] = acc[j][e];
-              if (better(acc[j][e], v, bv[e >> 1], bi[e >> 1])) {
-                bv[e >> 1] = acc[j][e];
-                bi[e >> 1] = v;
-              }
-            }
-            acc[j][e] = 0.f;
-          }
-        kc = 0;
-        tile += gridDim.x;
-      } else {
-        ++kc;
-      }
-    }
-    // per-warp best: across the 4 lanes of a row
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int o = 1; o < 4; o <<= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv[h], o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi[h], o);
-        if (better(ov, oi, bv[h], bi[h])) { bv[h] = ov; bi[h] = oi; }
-      }
   }
-  __shared__ float s_v[8][16];
-  __shared__ int s_i[8][16];
+}
+
+// Per-CTA best per slot from the per-thread bests (each worker thread owns one
+// table row per tile and NB slots starting at t0), then the cross-CTA pass.
+template <int NB>
+__device__ void finish_argmax(const LmArgs &a, int T, bool worker, int t0, float (&bv)[NB], int (&bi)[NB]) {
+  __shared__ float s_v[4][16];
+  __shared__ int s_i[4][16];
   __shared__ int s_last;
-  if (w < kThreads / 32 && q == 0) {
-    s_v[w][g] = bv[0]; s_i[w][g] = bi[0];
-    s_v[w][g + 8] = bv[1]; s_i[w][g + 8] = bi[1];
+  const int lane = threadIdx.x & 31, quad = (threadIdx.x >> 5) & 3;
+  if (worker) {
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv[j], o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi[j], o);
+        if (better(ov, oi, bv[j], bi[j])) { bv[j] = ov; bi[j] = oi; }
+      }
+      if (lane == 0) {
+        s_v[quad][t0 + j] = bv[j];
+        s_i[quad][t0 + j] = bi[j];
+      }
+    }
   }
   __syncthreads();
   if (threadIdx.x < 16) {
     const int t = threadIdx.x;
     float v = s_v[0][t];
     int i = s_i[0][t];
-    for (int ww = 1; ww < 8; ++ww)
-      if (better(s_v[ww][t], s_i[ww][t], v, i)) { v = s_v[ww][t]; i = s_i[ww][t]; }
+    for (int qd = 1; qd < 4; ++qd)
+      if (better(s_v[qd][t], s_i[qd][t], v, i)) { v = s_v[qd][t]; i = s_i[qd][t]; }
     __stcg(a.part + blockIdx.x * kMaxT + t, make_float2(v, __int_as_float(i)));
   }
   __threadfence();
@@ -269,6 +167,300 @@ __global__ void __launch_bounds__(kAll, 1) lmhead_kernel(const __grid_constant__
   }
 }
 
+__device__ __forceinline__ int my_tile_count(int n_tiles) {
+  return (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- Q8_0 table
+// TMEM columns: A slots [32 j, 32 j + 32), D slots 128 + 64 j + 32 blk.
+__global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int SB = kQ8Chunk;
+  constexpr uint32_t IDESC = umma_idesc(128, 32, false);
+  const int H = a.H, kcs = H / kChunk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ybuf = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t ring = ybuf + kcs * kYChunk;
+  const uint32_t bars = ring + S * SB;
+  auto full = [&](int i) { return bars + 8 * i; };
+  auto empty = [&](int i) { return bars + 8 * (S + i); };
+  auto afull = [&](int j) { return bars + 8 * (2 * S + j); };
+  auto dfull = [&](int j) { return bars + 8 * (2 * S + kNSlot + j); };
+  auto dempty = [&](int j) { return bars + 8 * (2 * S + 2 * kNSlot + j); };
+  const uint32_t tslot = bars + 8 * (2 * S + 3 * kNSlot);
+
+  const int n_tiles = (a.V + kTile - 1) / kTile;
+  const int total = my_tile_count(n_tiles) * kcs;
+  auto src_of = [&](int c) {
+    const int tile = blockIdx.x + (c / kcs) * gridDim.x;
+    return a.q8 + ((size_t)tile * kcs + (c % kcs)) * SB;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), kQ8Workers / 32);
+    }
+    for (int j = 0; j < kNSlot; ++j) {
+      mbar_init(afull(j), kQ8Workers / 32);
+      mbar_init(dfull(j), 1);
+      mbar_init(dempty(j), kQ8Workers / 32);
+    }
+    mbar_fence_init();
+    // the table does not depend on earlier kernels
+    for (int c = 0; c < S && c < total; ++c) {
+      mbar_expect_tx(full(c), SB);
+      bulk_g2s(ring + c * SB, src_of(c), SB, full(c));
+    }
+  }
+  if (warp == 1) tmem_alloc<512>(tslot);
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = lds32(tslot);
+  pdl_wait();
+  const int T = a.T_const > 0 ? a.T_const : a.sp->T;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int c = S; c < total; ++c) {
+        const int st = c % S;
+        if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
+        mbar_expect_tx(full(st), SB);
+        bulk_g2s(ring + st * SB, src_of(c), SB, full(st));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int c = 0; c < total; ++c) {
+        const int j = c % kNSlot;
+        if (!mbar_wait_bounded(afull(j), (c / kNSlot) & 1, a.err)) break;
+        if (c >= kNSlot && !mbar_wait_bounded(dempty(j), (c / kNSlot - 1) & 1, a.err)) break;
+        tc_fence_after();
+        const uint64_t bd = umma_desc_sw128(ybuf + (c % kcs) * kYChunk);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            umma_ts(tmem + 128 + 64 * j + 32 * blk, tmem + 32 * j + 16 * blk + 8 * kk, bd + 2 * (2 * blk + kk), IDESC,
+                    kk);
+        umma_commit(dfull(j));
+      }
+    }
+  }
+
+  // converter / epilogue threads: row r of each tile, slot group G (8 slots)
+  const int e = (int)threadIdx.x - kBase;
+  const int quad = warp & 3;
+  const int r = 32 * quad + lane;
+  const int G = (warp - 2) >> 2;   // warps 2..5: block 0 / slots 0..7; warps 6..9: block 1 / slots 8..15
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16);
+  float bv[8], acc[8];
+  int bi[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; acc[i] = 0.f; }
+  if (warp >= 2) {
+    stage_y<true>(a, ybuf, T, e, kQ8Workers);
+    fence_proxy_async();
+    named_sync(1, kQ8Workers);
+    uint32_t sc[kNSlot];   // the two block scales (f16x2) of each chunk in flight, by slot
+    bool ok = true;
+    for (int base = 0; base < total + kLook; base += kNSlot) {
+#pragma unroll
+      for (int u = 0; u < kNSlot; ++u) {
+        const int c = base + u;
+        if (c < total && ok) {
+          // convert: block G of row r -> f16 into A slot u (= c % kNSlot)
+          const int st = c % S;
+          if (!mbar_wait_bounded(full(st), (c / S) & 1, a.err)) ok = false;
+          const uint32_t buf = ring + st * SB;
+          const uint32_t x = ((r >> 1) & 3);
+          const uint4 q0 = lds128(buf + r * 64 + (((2 * G) ^ x) << 4));
+          const uint4 q1 = lds128(buf + r * 64 + (((2 * G + 1) ^ x) << 4));
+          // the f16 scales of row r for blocks 0 and 1 (two rows share each 32-bit word)
+          const uint32_t w0 = lds32(buf + kTile * 64 + (r & ~1) * 2);
+          const uint32_t w1 = lds32(buf + kTile * 64 + 256 + (r & ~1) * 2);
+          sc[u] = (r & 1) ? (w0 >> 16) | (w1 & 0xffff0000u) : (w0 & 0xffffu) | (w1 << 16);
+          uint32_t w[16];
+          i8x4_to_f16x4(q0.x, w[0], w[1]);
+          i8x4_to_f16x4(q0.y, w[2], w[3]);
+          i8x4_to_f16x4(q0.z, w[4], w[5]);
+          i8x4_to_f16x4(q0.w, w[6], w[7]);
+          i8x4_to_f16x4(q1.x, w[8], w[9]);
+          i8x4_to_f16x4(q1.y, w[10], w[11]);
+          i8x4_to_f16x4(q1.z, w[12], w[13]);
+          i8x4_to_f16x4(q1.w, w[14], w[15]);
+          tmem_st16(lane_base + 32 * u + 16 * G, w);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(empty(st));
+            mbar_arrive(afull(u));
+          }
+        }
+        const int ce = c - kLook;
+        const int ue = (u + 1) % kNSlot;   // = ce % kNSlot
+        if (ce >= 0 && ce < total && ok) {
+          if (!mbar_wait_bounded(dfull(ue), (ce / kNSlot) & 1, a.err)) ok = false;
+          tc_fence_after();
+          float d0[16], d1[16];
+          tmem_ld16(lane_base + 128 + 64 * ue + 16 * G, d0);
+          tmem_ld16(lane_base + 128 + 64 * ue + 32 + 16 * G, d1);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dempty(ue));
+          const uint32_t scw = sc[ue];
+          const __half2 sh = *reinterpret_cast<const __half2 *>(&scw);
+          const float f0 = __low2float(sh), f1 = __high2float(sh);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += f0 * (d0[i] + d0[8 + i]) + f1 * (d1[i] + d1[8 + i]);
+          if (ce % kcs == kcs - 1) {
+            const int v = (blockIdx.x + (ce / kcs) * gridDim.x) * kTile + r;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int t = 8 * G + i;
+              if (v < a.V && t < T) {
+                if (a.logits) a.logits[(size_t)t * a.V + v] = acc[i];
+                if (better(acc[i], v, bv[i], bi[i])) { bv[i] = acc[i]; bi[i] = v; }
+              }
+              acc[i] = 0.f;
+            }
+          }
+        }
+      }
+    }
+  }
+  // rows are split over quadrants; slot group G's bests live in warps of that group
+  finish_argmax<8>(a, T, warp >= 2, 8 * G, bv, bi);
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_free<512>(tmem);
+  }
+}
+
+// ---------------------------------------------------------------- bf16 table
+// TMEM columns: per-tile accumulator, double buffered at 0 and 32.
+__global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(const __grid_constant__ LmArgs a, const int S) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int SB = kBfStage;
+  constexpr uint32_t IDESC = umma_idesc(128, 32, true);
+  const int H = a.H, kcs = H / kChunk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ybuf = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t ring = ybuf + kcs * kYChunk;
+  const uint32_t bars = ring + S * SB;
+  auto full = [&](int i) { return bars + 8 * i; };
+  auto empty = [&](int i) { return bars + 8 * (S + i); };
+  auto dfull = [&](int j) { return bars + 8 * (2 * S + j); };
+  auto dempty = [&](int j) { return bars + 8 * (2 * S + 2 + j); };
+  const uint32_t yfull = bars + 8 * (2 * S + 4);
+  const uint32_t tslot = yfull + 8;
+
+  const int n_tiles = (a.V + kTile - 1) / kTile;
+  const int tiles = my_tile_count(n_tiles);
+  const int total = tiles * kcs;
+  auto src_of = [&](int c) {
+    const int tile = blockIdx.x + (c / kcs) * gridDim.x;
+    return a.wb + ((size_t)tile * kcs + (c % kcs)) * SB;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(dfull(j), 1);
+      mbar_init(dempty(j), kBfWorkers / 32);
+    }
+    mbar_init(yfull, 1);
+    mbar_fence_init();
+    for (int c = 0; c < S && c < total; ++c) {
+      mbar_expect_tx(full(c), SB);
+      bulk_g2s(ring + c * SB, src_of(c), SB, full(c));
+    }
+  }
+  if (warp == 1) tmem_alloc<64>(tslot);
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = lds32(tslot);
+  pdl_wait();
+  const int T = a.T_const > 0 ? a.T_const : a.sp->T;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int c = S; c < total; ++c) {
+        const int st = c % S;
+        if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
+        mbar_expect_tx(full(st), SB);
+        bulk_g2s(ring + st * SB, src_of(c), SB, full(st));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
+      for (int c = 0; c < total; ++c) {
+        const int st = c % S, ti = c / kcs, kc = c % kcs, db = ti & 1;
+        if (kc == 0 && ti >= 2 && !mbar_wait_bounded(dempty(db), ((ti >> 1) - 1) & 1, a.err)) break;
+        if (!mbar_wait_bounded(full(st), (c / S) & 1, a.err)) break;
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(ring + st * SB);
+        const uint64_t bd = umma_desc_sw128(ybuf + kc * kYChunk);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk)
+          umma_ss(tmem + 32 * db, ad + 2 * kk, bd + 2 * kk, IDESC, (kc | kk) ? 1u : 0u);
+        umma_commit(empty(st));
+        if (kc == kcs - 1) umma_commit(dfull(db));
+      }
+    }
+  }
+
+  const int quad = warp & 3;
+  const int r = 32 * quad + lane;
+  float bv[16];
+  int bi[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; }
+  if (warp >= 2) {
+    stage_y<false>(a, ybuf, T, (int)threadIdx.x - kBase, kBfWorkers);
+    fence_proxy_async();
+    named_sync(1, kBfWorkers);
+    if (threadIdx.x == kBase) mbar_arrive(yfull);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16);
+    for (int ti = 0; ti < tiles; ++ti) {
+      const int db = ti & 1;
+      if (!mbar_wait_bounded(dfull(db), (ti >> 1) & 1, a.err)) break;
+      tc_fence_after();
+      float d0[16], d1[16];
+      tmem_ld16(lane_base + 32 * db, d0);        // slots 0..7 hi, lo
+      tmem_ld16(lane_base + 32 * db + 16, d1);   // slots 8..15 hi, lo
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty(db));
+      const int v = (blockIdx.x + ti * gridDim.x) * kTile + r;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float val = t < 8 ? d0[t] + d0[8 + t] : d1[t - 8] + d1[t];
+        if (v < a.V && t < T) {
+          if (a.logits) a.logits[(size_t)t * a.V + v] = val;
+          if (better(val, v, bv[t], bi[t])) { bv[t] = val; bi[t] = v; }
+        }
+      }
+    }
+  }
+  finish_argmax<16>(a, T, warp >= 2, 0, bv, bi);
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_free<64>(tmem);
+  }
+}
+
 int lmhead_grid(const LmArgs &a, int n_sm) {
   const int n_tiles = (a.V + kTile - 1) / kTile;
   return n_tiles < n_sm ? n_tiles : n_sm;
@@ -276,16 +468,17 @@ int lmhead_grid(const LmArgs &a, int n_sm) {
 
 cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) {
   const bool q8 = a.q8 != nullptr;
-  const size_t a_bytes = 2 * 16 * (size_t)(a.H + 32) * 2;
-  const size_t budget = 227 * 1024 - a_bytes - 1024;
-  const size_t sb = lm_stage_bytes(q8);
-  int S = (int)(budget / (sb + 16));
-  if (S > 16) S = 16;
-  if (S < 2) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)S * sb + a_bytes + 16 * S;
+  const size_t ybytes = (size_t)(a.H / kChunk) * kYChunk;
+  const size_t sb = q8 ? kQ8Chunk : kBfStage;
+  const size_t fixed = 1024 + ybytes + 8 * (3 * kNSlot + 8) + 16;
+  const size_t budget = 227 * 1024 - 2048;   // leaves room for the static shared arrays
+  if (fixed + 2 * (sb + 16) > budget) return cudaErrorInvalidValue;
+  int S = (int)((budget - fixed) / (sb + 16));
+  if (S > 12) S = 12;
+  const size_t smem = fixed + (size_t)S * (sb + 16);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kAll, 1, 1);
+  cfg.blockDim = dim3(kBase + (q8 ? kQ8Workers : kBfWorkers), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -295,13 +488,13 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) 
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
   if (q8) {
-    e = cudaFuncSetAttribute(lmhead_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(lmhead_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, lmhead_kernel<true>, a, S);
+    return cudaLaunchKernelEx(&cfg, lmhead_q8_kernel, a, S);
   }
-  e = cudaFuncSetAttribute(lmhead_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(lmhead_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, lmhead_kernel<false>, a, S);
+  return cudaLaunchKernelEx(&cfg, lmhead_bf16_kernel, a, S);
 }
 
 }  // namespace fm

@@ -129,8 +129,8 @@ __global__ void accept_kernel(int n, int block, const int32_t *draft, const int3
 }
 
 // One 16-byte unit (8 bf16) per thread: row r, unit u of chunk kc of tile
-// -> byte ((tile * nck + kc) * 16384) + r * 128 + ((u ^ ((r & 1) << 2)) << 4),
-// the order the GEMV kernel reads its shared-memory stages in.
+// -> byte ((tile * nck + kc) * 16384) + sw128(r, 8u): the tensor cores'
+// 128-byte-swizzle K-major layout, so a bulk copy lands a ready operand tile.
 __global__ void tile_weights_kernel(const uint4 *src, int M, int K, uint8_t *dst) {
   const int nck = K / 64;
   const long long id = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -142,7 +142,7 @@ __global__ void tile_weights_kernel(const uint4 *src, int M, int K, uint8_t *dst
   const int m = tile * 128 + r;
   uint4 v = make_uint4(0u, 0u, 0u, 0u);
   if (m < M) v = src[((size_t)m * K + (size_t)kc * 64 + u * 8) / 8];
-  *reinterpret_cast<uint4 *>(dst + (size_t)tk * 16384 + r * 128 + ((u ^ ((r & 1) << 2)) << 4)) = v;
+  *reinterpret_cast<uint4 *>(dst + (size_t)tk * 16384 + sw128(r, 8 * u)) = v;
 }
 
 __global__ void fill_kernel(float *p, size_t n, float v) {
