@@ -28,7 +28,7 @@ FM_DEBUG_KEEP_HIDDEN = 1
 FM_DEBUG_PROFILE = 2
 
 EXPORTS = ["fm_create", "fm_context_append", "fm_context_append_batched", "fm_draft", "fm_accept",
-           "fm_accept_batched", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
+           "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
            "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy"]
 
 
@@ -76,6 +76,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fm_draft": (I32, [P, I32, P, P, P, P, P]),
         "fm_accept": (I32, [P, P, I32, P, P]),
         "fm_accept_batched": (I32, [P, I32, P, P, P, P, P, P]),
+        "fm_lm_head_argmax_noalloc": (I32, [P, P, I32, P, P]),
         "fm_debug_copy": (I32, [P, I32, I32, I32, I64, P, I64, P]),
         "fm_set_debug": (I32, [P, I32]),
         "fm_get_length": (I32, [P, I32, ctypes.POINTER(I32)]),
@@ -195,6 +196,16 @@ def fm_accept_batched(h, draft, target, k, n_accepted, bonus, stream=None) -> No
     lib = load_library()
     _check(lib.fm_accept_batched(h, draft.shape[0], _ptr(draft), _ptr(target), _ptr(k), _ptr(n_accepted),
                                  _ptr(bonus), _stream(stream)), h)
+
+
+def fm_lm_head_argmax_noalloc(h, y, tokens, stream=None) -> None:
+    """The fused lm_head + argmax on caller rows, for callers that must not
+    allocate device memory while they run (the library keeps its scratch in
+    static device memory).  y: a CUDA float32 tensor [n_rows, target_dim]
+    (n_rows <= 16); tokens: a CUDA int32 tensor [n_rows] that receives the
+    argmax over the token table.  The first call on a device does a one-time
+    set-up, so make it before any stream capture; overlapping calls race."""
+    _check(load_library().fm_lm_head_argmax_noalloc(h, _ptr(y), y.shape[0], _ptr(tokens), _stream(stream)), h)
 
 
 def fm_debug_copy(h, what: int, seq: int, index: int, out: np.ndarray, offset: int = 0, stream=None) -> np.ndarray:

@@ -1412,6 +1412,39 @@ fm_status fm_accept_batched(fm_handle *h, int32_t n_seqs, const int32_t *draft, 
   return FM_OK;
 }
 
+// The fused lm_head + argmax on caller rows, with its cross-CTA scratch in the
+// library's static device memory instead of the handle's buffers.
+fm_status fm_lm_head_argmax_noalloc(fm_handle *h, const float *y_dev, int32_t n_rows, int32_t *tokens_dev,
+                                     void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  if (!y_dev || !tokens_dev || n_rows < 1 || n_rows > 16)
+    return fail(h, FM_ERR_INVALID_ARG, "bad lm_head arguments (n_rows must be in 1..16)");
+  const fm_config &c = h->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LmArgs a;
+  memset(&a, 0, sizeof a);
+  if (c.lm_format == FM_LM_Q8_0)
+    a.q8 = h->tq8;
+  else
+    a.wb = h->tb;
+  a.err = h->dev_err;
+  a.V = c.vocab;
+  a.H = c.target_dim;
+  a.T_const = n_rows;
+  a.Y = y_dev;
+  a.ldy = c.target_dim;
+  a.tokens = tokens_dev;
+  const int grid = lmhead_grid(a, h->n_sm);
+  if (grid > lmhead_static_max_grid())
+    return fail(h, FM_ERR_UNSUPPORTED, "lm_head grid of %d CTAs exceeds the static scratch (at most %d)", grid,
+                lmhead_static_max_grid());
+  CK(lmhead_static_scratch(grid, &a.part, &a.ticket, s));
+  CK(launch_lmhead(a, grid, s, false));
+  ++h->last_launches;
+  return FM_OK;
+}
+
 fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, int64_t offset, void *dst,
                         int64_t nbytes, void *stream) {
   if (!h) return FM_ERR_INVALID_ARG;

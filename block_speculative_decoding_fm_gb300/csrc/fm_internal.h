@@ -156,6 +156,11 @@ size_t gemv_smem_bytes(const GemvArgs &a, int mt);
 cudaError_t launch_attn(const AttnArgs &a, int L_now, cudaStream_t s, bool pdl);
 cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t s, bool pdl);
 int lmhead_grid(const LmArgs &a, int n_sm);
+// The static scratch of the lm_head entry point that allocates nothing: the
+// largest grid it holds, and its ticket / partial-best pointers on the current
+// device (the first call per device resolves the address and zeroes the ticket).
+int lmhead_static_max_grid();
+cudaError_t lmhead_static_scratch(int grid, float2 **part, int32_t **ticket, cudaStream_t st);
 
 // set-up and small kernels
 cudaError_t launch_q8_repack(const uint8_t *raw, int32_t V, int32_t H, uint8_t *dst, cudaStream_t s);

@@ -20,6 +20,8 @@
 //     row and group of 8 slots), four chunks in flight;
 //   * each thread keeps a running (value, index) best per slot; pass two is
 //     the last CTA reducing the per-CTA bests.
+#include <mutex>
+
 #include "dev_common.cuh"
 #include "fm_internal.h"
 
@@ -459,6 +461,43 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
     tc_fence_after();
     tmem_free<64>(tmem);
   }
+}
+
+// Scratch of the lm_head entry point that allocates nothing: the completion
+// ticket (first 256 bytes; it must read zero before a launch, and the last CTA
+// of every launch puts it back to zero) followed by the per-CTA partial bests
+// (grid x kMaxT float2).  Static device memory of this library: every device
+// that loads it holds one copy until the process exits, shared by all calls.
+constexpr size_t kStaticLmScratchBytes = 64 * 1024;
+static __device__ __align__(256) unsigned char g_lm_scratch[kStaticLmScratchBytes];
+
+int lmhead_static_max_grid() { return (int)((kStaticLmScratchBytes - 256) / (kMaxT * sizeof(float2))); }
+
+cudaError_t lmhead_static_scratch(int grid, float2 **part, int32_t **ticket, cudaStream_t st) {
+  if (grid < 1 || grid > lmhead_static_max_grid()) return cudaErrorInvalidValue;
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static unsigned char *addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned char *p = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    p = addr[dev];
+    if (!p) {
+      // first call on this device (current): the symbol's device address, then a zero ticket
+      e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_lm_scratch);
+      if (e != cudaSuccess) return e;
+      e = cudaMemsetAsync(p, 0, 256, st);
+      if (e != cudaSuccess) return e;
+      addr[dev] = p;
+    }
+  }
+  *ticket = reinterpret_cast<int32_t *>(p);
+  *part = reinterpret_cast<float2 *>(p + 256);
+  return cudaSuccess;
 }
 
 int lmhead_grid(const LmArgs &a, int n_sm) {

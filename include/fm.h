@@ -187,6 +187,31 @@ FM_API fm_status fm_accept(const int32_t *draft_host, const int32_t *target_host
 FM_API fm_status fm_accept_batched(fm_handle *h, int32_t n_seqs, const int32_t *draft_dev, const int32_t *target_dev,
                             const int32_t *k_dev, int32_t *n_accepted_dev, int32_t *bonus_dev, void *stream);
 
+/*
+ * fm_lm_head_argmax_noalloc -- fm_draft's fused lm_head + per-row argmax on
+ * rows the caller supplies: tokens[t] = argmax_v sum_k y[t][k] E[v][k]
+ * (ties -> lowest v) over the handle's token table E.  The paper has no
+ * counterpart to this entry point.  It is for callers that may not allocate
+ * device memory while they run -- a serving loop whose memory is all handed
+ * out up front by its own pool, or code running where cudaMalloc would stall
+ * the device or could fail under memory pressure.  It allocates nothing: the
+ * cross-CTA partial bests and the completion ticket live in a fixed 64 KB
+ * block of static device memory inside the library, which every GPU that
+ * loads the library keeps until the process exits.  That block holds at
+ * most 255 CTAs of partials; larger grids are rejected with
+ * FM_ERR_UNSUPPORTED.  The first call on a device looks up the block's
+ * address and zeroes the ticket on the stream, so make that first call
+ * before any stream capture.  Every call shares the block: calls that
+ * overlap on the GPU (other streams, other handles on the same device) race
+ * and must be serialised by the caller.
+ * y_dev: device f32 [n_rows][target_dim], row-major.  tokens_dev: device
+ * int32 [n_rows], written in stream order.  Both stay owned by the caller.
+ * Errors: FM_ERR_INVALID_ARG (null pointer, n_rows outside 1..16),
+ *   FM_ERR_UNSUPPORTED (grid beyond the static block), FM_ERR_CUDA.
+ */
+FM_API fm_status fm_lm_head_argmax_noalloc(fm_handle *h, const float *y_dev, int32_t n_rows, int32_t *tokens_dev,
+                                    void *stream);
+
 /* fm_debug_copy selectors ([FM] readOut / peek: look at working buffers) */
 #define FM_DEBUG_HIDDEN 0   /* index = layer: the block's hidden rows after that layer [block][dim] f32 (last draft) */
 #define FM_DEBUG_HEAD_OUT 1 /* the head output Y [block][target_dim] f32 (last draft of seq) */
