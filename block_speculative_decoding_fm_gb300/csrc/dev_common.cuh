@@ -142,6 +142,8 @@ __host__ __device__ __forceinline__ uint32_t sw128(int r, int k) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 3) ^ r) & 7) << 4) + (k & 7) * 2);
 }
 __host__ __device__ __forceinline__ uint32_t w_slot(int r, int k) { return sw128(r, k); }
+// lm_head operand row of slot t's hi half (groups of 8 slots: 8 hi rows, then their 8 lo rows)
+__host__ __device__ __forceinline__ int lm_yrow(int t) { return (t >> 3) * 16 + (t & 7); }
 
 // ---- tcgen05 (5th-generation tensor cores, TMEM accumulators) --------------
 // shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row atoms 1024 bytes apart
@@ -255,6 +257,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+// warm L2 with a global range (16-byte aligned, size a multiple of 16); no completion to wait for
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");

@@ -71,6 +71,7 @@ struct fm_handle {
 
   // ---- work buffers ----
   float *X = nullptr, *qkv = nullptr, *qc = nullptr, *attn = nullptr, *u = nullptr, *Y = nullptr;
+  uint8_t *ylm = nullptr;  // the head output as the lm_head operand (hi/lo halves, swizzled)
   float *ctx = nullptr, *actx = nullptr, *uni = nullptr, *hid = nullptr, *dbg_logits = nullptr;
   float2 *st_x = nullptr, *st_h0 = nullptr, *st_c = nullptr, *st_a = nullptr, *st_u = nullptr, *st_init = nullptr;
   float *part_o = nullptr;
@@ -363,7 +364,7 @@ fm_status run_attn(fm_handle *h, const float *Q, int ldq, const Seg2 &kv, int T,
 }
 
 fm_status run_lmhead(fm_handle *h, const float *Y, int T, const StepParams *sp, int32_t *tokens, float *logits,
-                     cudaStream_t s) {
+                     cudaStream_t s, const uint8_t *ylm = nullptr) {
   const fm_config &c = h->cfg;
   LmArgs a;
   memset(&a, 0, sizeof a);
@@ -378,6 +379,7 @@ fm_status run_lmhead(fm_handle *h, const float *Y, int T, const StepParams *sp, 
   a.sp = sp;
   a.Y = Y;
   a.ldy = c.target_dim;
+  a.ylm = ylm;
   a.part = h->lm_part;
   a.ticket = h->tickets + 2 * c.n_heads;
   a.tokens = tokens;
@@ -601,8 +603,10 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
   hd.bias = h->b_head;
   hd.Y = h->Y;
   hd.ldy = Ht;
+  hd.ylm = h->ylm;
+  hd.ylm_f16 = c.lm_format == FM_LM_Q8_0;
   TRY(run_gemv(h, hd, s, "gemv.head"));
-  return run_lmhead(h, h->Y, B, sp, nullptr, nullptr, s);
+  return run_lmhead(h, h->Y, B, sp, nullptr, nullptr, s, h->ylm);
 }
 
 // ---------------------------------------------------------------- DFlash
@@ -737,8 +741,10 @@ fm_status dflash_draft_launch(fm_handle *h, int seq, int pos, const StepParams *
   op.emode = E_STORE;
   op.Y = h->Y;
   op.ldy = H;
+  op.ylm = h->ylm;
+  op.ylm_f16 = c.lm_format == FM_LM_Q8_0;
   TRY(run_gemv(h, op, s, "gemv.out_proj", G));
-  return run_lmhead(h, h->Y, G, sp, nullptr, nullptr, s);
+  return run_lmhead(h, h->Y, G, sp, nullptr, nullptr, s, h->ylm);
 }
 
 // ---------------------------------------------------------------- dense prefill
@@ -969,6 +975,9 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   TRY(dalloc(h, &h->attn, (size_t)kMaxT * D));
   TRY(dalloc(h, &h->u, (size_t)kMaxT * (F > wmax ? F : wmax)));
   TRY(dalloc(h, &h->Y, (size_t)kMaxT * Ht));
+  // the head's output also split into the lm_head operand; rows of unused slots stay zero
+  TRY(dalloc(h, &h->ylm, (size_t)(Ht / 64) * kLmYChunk));
+  CK(cudaMemsetAsync(h->ylm, 0, (size_t)(Ht / 64) * kLmYChunk, s));
   TRY(dalloc(h, &h->ctx, (size_t)kMaxT * D));
   TRY(dalloc(h, &h->actx, (size_t)kMaxT * D));
   TRY(dalloc(h, &h->hid, (size_t)c.n_layers * kMaxT * D));
@@ -1470,7 +1479,7 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
       fm_status st;
       const StepParams *sp = next_params(h, p, s, &st);
       if (!sp) return st;
-      TRY(run_lmhead(h, h->Y, c.block, sp, h->tok_tmp, h->dbg_logits, s));
+      TRY(run_lmhead(h, h->Y, c.block, sp, h->tok_tmp, h->dbg_logits, s, h->ylm));
       src = h->dbg_logits;
       size = (int64_t)c.block * c.vocab * 4;
       break;

@@ -94,6 +94,8 @@ struct GemvArgs {
   const __nv_bfloat16 *bias;  // [M] or null
   float *Y;
   int32_t ldy;
+  uint8_t *ylm;               // E_STORE: also write Y as the lm_head operand (kLmYChunk layout), or null
+  int32_t ylm_f16;            // 1: f16 hi/lo halves (Q8_0 table), 0: bf16
   float2 *out_st;             // [M / 128][kMaxT] (sum, sumsq) of the stored rows, or null
   const __nv_bfloat16 *st_w;  // if set, out_st holds (sum v^2, sum (v st_w)^2) instead
   const float *gate;          // E_RESID gate [M] (null = 1)
@@ -135,6 +137,10 @@ struct AttnArgs {
 // block: 128 rows x 64 int8 (pre-swizzled, q8_slot) then the two 32-column
 // blocks' f16 scales [2][128].  bf16 table: the GEMV tile layout.
 constexpr int kQ8Chunk = kTile * 64 + 2 * kTile * 2;
+// lm_head operand rows of Y: per 64 columns one 32-row x 128-byte block in the
+// 128-byte-swizzle K-major layout; slot t has its hi half in row lm_yrow(t) and
+// its lo half 8 rows further (f16 halves for the Q8_0 table, bf16 for bf16).
+constexpr int kLmYChunk = 32 * 128;
 struct LmArgs {
   const uint8_t *q8;         // Q8_0 table (layout above) or null
   const uint8_t *wb;         // bf16 table (GEMV tile layout) or null
@@ -144,6 +150,7 @@ struct LmArgs {
   const StepParams *sp;
   const float *Y;            // [T][H]
   int32_t ldy;
+  const uint8_t *ylm;        // Y already split into the resident operand layout (kLmYChunk per 64 columns), or null
   float2 *part;              // [gridDim.x][kMaxT] (value, index-as-float bits)
   int32_t *ticket;           // [1]
   int32_t *tokens;           // [T]; null: sp->tokens

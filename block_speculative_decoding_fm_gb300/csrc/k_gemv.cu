@@ -213,6 +213,27 @@ __device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], i
       }
       if (live)
         __stcg(reinterpret_cast<float4 *>(a.Y + (size_t)t * a.ldy + mrow), make_float4(v[0], v[1], v[2], v[3]));
+      if (a.ylm && live) {
+        // the same rows split into the lm_head's resident operand (hi row, lo row 8 further)
+        uint32_t hw[2], lw[2];
+        if (a.ylm_f16) {
+          __half hh[4], ll[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_f16(v[e], hh[e], ll[e]);
+          hw[0] = pack_f16(hh[0], hh[1]); hw[1] = pack_f16(hh[2], hh[3]);
+          lw[0] = pack_f16(ll[0], ll[1]); lw[1] = pack_f16(ll[2], ll[3]);
+        } else {
+          __nv_bfloat16 hh[4], ll[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_bf16(v[e], hh[e], ll[e]);
+          hw[0] = pack_bf16(hh[0], hh[1]); hw[1] = pack_bf16(hh[2], hh[3]);
+          lw[0] = pack_bf16(ll[0], ll[1]); lw[1] = pack_bf16(ll[2], ll[3]);
+        }
+        uint8_t *cb = a.ylm + (size_t)(mrow >> 6) * kLmYChunk;
+        const int r = lm_yrow(t);
+        *reinterpret_cast<uint2 *>(cb + sw128(r, mrow & 63)) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint2 *>(cb + sw128(r + 8, mrow & 63)) = make_uint2(lw[0], lw[1]);
+      }
       if (a.out_st) {
         float s1 = 0.f, s2 = 0.f;
         if (live) {
@@ -393,6 +414,8 @@ __global__ void __launch_bounds__(kAll, 1) gemv_kernel(const __grid_constant__ G
       mbar_expect_tx(full(c), kStageBytes);
       bulk_g2s(ring + c * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(c));
     }
+    // the rest of this CTA's slice goes to L2 now, so the ring refills hit L2
+    for (int c = S; c < nchunks; ++c) bulk_prefetch_l2(wsrc + (size_t)c * kStageBytes, kStageBytes);
   }
   if (warp == 1) tmem_alloc<NR>(tslot);
   pdl_trigger();

@@ -31,15 +31,14 @@ namespace {
 
 constexpr int kChunk = 64;
 constexpr int kBfStage = kTile * kChunk * 2;  // 16 KB bf16 chunk
-constexpr int kYChunk = 32 * 128;             // one 64-column chunk of the resident Y (32 rows x 128 B)
+constexpr int kYChunk = kLmYChunk;            // one 64-column chunk of the resident Y (32 rows x 128 B)
 constexpr int kNSlot = 4;                     // Q8: chunks in flight between conversion and epilogue
 constexpr int kLook = kNSlot - 1;             // Q8: conversion runs this many chunks ahead
 constexpr int kQ8Workers = 256;               // Q8: warps 2..9
 constexpr int kBfWorkers = 128;               // bf16: warps 2..5
 constexpr int kBase = 64;                     // warp 0: producer, warp 1: TMEM owner + MMA issuer
+constexpr int kL2Ahead = 16;                  // chunks warmed in L2 ahead of the shared-memory ring
 
-// B row of slot t (hi half; the lo half is 8 rows further)
-__device__ __forceinline__ int yrow(int t) { return (t >> 3) * 16 + (t & 7); }
 
 // tcgen05.mma with A in tensor memory (lane = A row, 32-bit columns hold K pairs)
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -106,7 +105,7 @@ __device__ void stage_y(const LmArgs &a, uint32_t ybuf, int T, int tid, int nthr
         lw[0] = pack_bf16(l[0], l[1]); lw[1] = pack_bf16(l[2], l[3]);
       }
       const uint32_t cb = ybuf + (uint32_t)(k >> 6) * kYChunk;
-      const int r = yrow(t);
+      const int r = lm_yrow(t);
       asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cb + sw128(r, k & 63)), "r"(hw[0]), "r"(hw[1]));
       asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cb + sw128(r + 8, k & 63)), "r"(lw[0]), "r"(lw[1]));
     }
@@ -169,6 +168,14 @@ __device__ void finish_argmax(const LmArgs &a, int T, bool worker, int t0, float
   }
 }
 
+// The producer's copy of a pre-split Y (kLmYChunk per 64 columns) into the resident operand.
+__device__ __forceinline__ void load_ylm(const LmArgs &a, uint32_t ybuf, uint32_t yfull) {
+  const uint32_t bytes = (uint32_t)(a.H / kChunk) * kYChunk;
+  mbar_expect_tx(yfull, bytes);
+  for (uint32_t off = 0; off < bytes; off += 16384)
+    bulk_g2s(ybuf + off, a.ylm + off, bytes - off < 16384 ? bytes - off : 16384, yfull);
+}
+
 __device__ __forceinline__ int my_tile_count(int n_tiles) {
   return (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 }
@@ -191,7 +198,8 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   auto afull = [&](int j) { return bars + 8 * (2 * S + j); };
   auto dfull = [&](int j) { return bars + 8 * (2 * S + kNSlot + j); };
   auto dempty = [&](int j) { return bars + 8 * (2 * S + 2 * kNSlot + j); };
-  const uint32_t tslot = bars + 8 * (2 * S + 3 * kNSlot);
+  const uint32_t yfull = bars + 8 * (2 * S + 3 * kNSlot);
+  const uint32_t tslot = yfull + 8;
 
   const int n_tiles = (a.V + kTile - 1) / kTile;
   const int total = my_tile_count(n_tiles) * kcs;
@@ -210,12 +218,15 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
       mbar_init(dfull(j), 1);
       mbar_init(dempty(j), kQ8Workers / 32);
     }
+    mbar_init(yfull, 1);
     mbar_fence_init();
     // the table does not depend on earlier kernels
     for (int c = 0; c < S && c < total; ++c) {
       mbar_expect_tx(full(c), SB);
       bulk_g2s(ring + c * SB, src_of(c), SB, full(c));
     }
+    // a bulk copy takes microseconds to land: keep more of the stream in flight through L2
+    for (int c = S; c < S + kL2Ahead && c < total; ++c) bulk_prefetch_l2(src_of(c), SB);
   }
   if (warp == 1) tmem_alloc<512>(tslot);
   pdl_trigger();
@@ -228,15 +239,17 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
 
   if (warp == 0) {
     if (lane == 0) {
+      if (a.ylm) load_ylm(a, ybuf, yfull);
       for (int c = S; c < total; ++c) {
         const int st = c % S;
         if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
         mbar_expect_tx(full(st), SB);
         bulk_g2s(ring + st * SB, src_of(c), SB, full(st));
+        if (c + kL2Ahead < total) bulk_prefetch_l2(src_of(c + kL2Ahead), SB);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
       for (int c = 0; c < total; ++c) {
         const int j = c % kNSlot;
         if (!mbar_wait_bounded(afull(j), (c / kNSlot) & 1, a.err)) break;
@@ -265,9 +278,12 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
 #pragma unroll
   for (int i = 0; i < 8; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; acc[i] = 0.f; }
   if (warp >= 2) {
-    stage_y<true>(a, ybuf, T, e, kQ8Workers);
-    fence_proxy_async();
-    named_sync(1, kQ8Workers);
+    if (!a.ylm) {
+      stage_y<true>(a, ybuf, T, e, kQ8Workers);
+      fence_proxy_async();
+      named_sync(1, kQ8Workers);
+      if (e == 0) mbar_arrive(yfull);
+    }
     uint32_t sc[kNSlot];   // the two block scales (f16x2) of each chunk in flight, by slot
     bool ok = true;
     for (int base = 0; base < total + kLook; base += kNSlot) {
@@ -385,6 +401,8 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
       mbar_expect_tx(full(c), SB);
       bulk_g2s(ring + c * SB, src_of(c), SB, full(c));
     }
+    // a bulk copy takes microseconds to land: keep more of the stream in flight through L2
+    for (int c = S; c < S + kL2Ahead && c < total; ++c) bulk_prefetch_l2(src_of(c), SB);
   }
   if (warp == 1) tmem_alloc<64>(tslot);
   pdl_trigger();
@@ -397,11 +415,13 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
 
   if (warp == 0) {
     if (lane == 0) {
+      if (a.ylm) load_ylm(a, ybuf, yfull);
       for (int c = S; c < total; ++c) {
         const int st = c % S;
         if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
         mbar_expect_tx(full(st), SB);
         bulk_g2s(ring + st * SB, src_of(c), SB, full(st));
+        if (c + kL2Ahead < total) bulk_prefetch_l2(src_of(c + kL2Ahead), SB);
       }
     }
   } else if (warp == 1) {
@@ -429,10 +449,12 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
 #pragma unroll
   for (int i = 0; i < 16; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; }
   if (warp >= 2) {
-    stage_y<false>(a, ybuf, T, (int)threadIdx.x - kBase, kBfWorkers);
-    fence_proxy_async();
-    named_sync(1, kBfWorkers);
-    if (threadIdx.x == kBase) mbar_arrive(yfull);
+    if (!a.ylm) {
+      stage_y<false>(a, ybuf, T, (int)threadIdx.x - kBase, kBfWorkers);
+      fence_proxy_async();
+      named_sync(1, kBfWorkers);
+      if (threadIdx.x == kBase) mbar_arrive(yfull);
+    }
     const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16);
     for (int ti = 0; ti < tiles; ++ti) {
       const int db = ti & 1;
