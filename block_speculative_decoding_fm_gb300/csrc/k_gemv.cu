@@ -33,7 +33,7 @@ namespace fm {
 
 namespace {
 
-constexpr int kWorkers = 128;          // warps 2..5: stage activations, read TMEM, epilogue
+constexpr int kWorkers = 256;          // warps 2..9: stage activations, read TMEM, epilogue
 constexpr int kAll = 64 + kWorkers;    // warp 0 streams weights, warp 1 owns TMEM and issues MMAs
 constexpr int kThreads = kWorkers;     // threads that share the epilogue loops
 constexpr int kWorkerBase = 64;        // first worker thread
@@ -90,90 +90,81 @@ __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
 // after another (each chunk 32MT rows x 128 bytes, 128-byte swizzle).
 template <int MT>
 __device__ void stage_a(const GemvArgs &a, const Smem &s, uint32_t dst, int T, int m0, int k0, int kp) {
-  const int rows = 16 * MT;
-  const int quads = kp >> 2;
-  constexpr int kThreads = kWorkers;
+  constexpr int rows = 16 * MT;
+  constexpr int tpr = kWorkers / rows;        // threads per activation row (16 or 8)
+  constexpr int kMaxQ = 256 / 4 / tpr;        // quads per thread for a 256-column piece
+  const int tid = wtid();
+  const int t = tid / tpr, q0 = tid % tpr;    // constant divisors
+  const int nq = (kp >> 2) / tpr;             // kp is a multiple of 64
   const float *X = a.x_from_sp ? a.sp->feats : a.X;
   const __nv_bfloat16 *nw = a.nw;
   const __nv_bfloat16 *nw2 = a.nw2;
   if (a.amode == A_RMS2 && a.nw_rows > 0) nw2 += (size_t)(m0 / a.nw_rows) * a.K;
-  // each thread handles up to kBatch quads; all of its loads are issued before
-  // any of them is used so the L2 round trips overlap
-  constexpr int kBatch = 8;
-  for (int i0 = wtid(); i0 < rows * quads; i0 += kThreads * kBatch) {
-    float4 xv[kBatch];
+  const bool second = a.split > 0 && t >= a.split;
+  const bool load = t < T && a.amode != A_ROW_Q8 && a.amode != A_ROW_BF16;
+  const float *xr = second ? a.X2 + (size_t)(t - a.split) * a.ldx : X + (size_t)t * a.ldx;
+  // every load of this thread is in flight before the first one is used
+  float4 xv[kMaxQ];
 #pragma unroll
-    for (int bi = 0; bi < kBatch; ++bi) {
-      const int i = i0 + bi * kThreads;
-      xv[bi] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < rows * quads) {
-        const int t = i / quads, k = k0 + (i - t * quads) * 4;
-        if (t < T && a.amode != A_ROW_Q8 && a.amode != A_ROW_BF16) {
-          const bool second = a.split > 0 && t >= a.split;
-          const float *xr = second ? a.X2 + (size_t)(t - a.split) * a.ldx : X + (size_t)t * a.ldx;
-          xv[bi] = __ldcg(reinterpret_cast<const float4 *>(xr + k));
-        }
-      }
-    }
+  for (int j = 0; j < kMaxQ; ++j) {
+    xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < nq && load) xv[j] = __ldcg(reinterpret_cast<const float4 *>(xr + k0 + 4 * (q0 + tpr * j)));
+  }
+  float mu = 0.f, rs = 1.f;
+  if (t < T) { mu = s.stat_mu[t]; rs = s.stat_rs[t]; }
+  const __nv_bfloat16 *wv = second ? a.nw_alt : nw;
 #pragma unroll
-    for (int bi = 0; bi < kBatch; ++bi) {
-      const int i = i0 + bi * kThreads;
-      if (i >= rows * quads) break;
-      const int t = i / quads, kq = (i - t * quads) * 4;
-      const int k = k0 + kq;
-      float v[4] = {xv[bi].x, xv[bi].y, xv[bi].z, xv[bi].w};
-      if (t < T) {
-        if (a.amode == A_ROW_Q8 || a.amode == A_ROW_BF16) {
-          v[0] = v[1] = v[2] = v[3] = 0.f;
-          if (t == 0) {
-            const int r = a.sp->anchor;
-            const size_t chunk = (size_t)(r >> 7) * (a.K / 64) + (k >> 6);
-            const int rr = r & 127, kk = k & 63;
-            if (a.amode == A_ROW_Q8) {
-              const uint8_t *base = a.tq8 + chunk * kQ8Chunk;
-              const char4 q = *reinterpret_cast<const char4 *>(base + q8_slot(rr, kk));
-              const float d = __half2float(
-                  *reinterpret_cast<const __half *>(base + kTile * 64 + (kk >> 5) * 256 + rr * 2));
-              v[0] = d * q.x; v[1] = d * q.y; v[2] = d * q.z; v[3] = d * q.w;
-            } else {
-              const uint8_t *base = a.tb + chunk * 16384;
-              const uint2 u = *reinterpret_cast<const uint2 *>(base + w_slot(rr, kk));
-              const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-              const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-              v[0] = __low2float(p0); v[1] = __high2float(p0); v[2] = __low2float(p1); v[3] = __high2float(p1);
-            }
+  for (int j = 0; j < kMaxQ; ++j) {
+    if (j >= nq) break;
+    const int kq = 4 * (q0 + tpr * j);   // column inside the piece
+    const int k = k0 + kq;
+    float v[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+    if (t < T) {
+      if (a.amode == A_ROW_Q8 || a.amode == A_ROW_BF16) {
+        v[0] = v[1] = v[2] = v[3] = 0.f;
+        if (t == 0) {
+          const int r = a.sp->anchor;
+          const size_t chunk = (size_t)(r >> 7) * (a.K / 64) + (k >> 6);
+          const int rr = r & 127, kk = k & 63;
+          if (a.amode == A_ROW_Q8) {
+            const uint8_t *base = a.tq8 + chunk * kQ8Chunk;
+            const char4 qv = *reinterpret_cast<const char4 *>(base + q8_slot(rr, kk));
+            const float d = __half2float(
+                *reinterpret_cast<const __half *>(base + kTile * 64 + (kk >> 5) * 256 + rr * 2));
+            v[0] = d * qv.x; v[1] = d * qv.y; v[2] = d * qv.z; v[3] = d * qv.w;
+          } else {
+            const uint8_t *base = a.tb + chunk * 16384;
+            const uint2 u = *reinterpret_cast<const uint2 *>(base + w_slot(rr, kk));
+            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+            v[0] = __low2float(p0); v[1] = __high2float(p0); v[2] = __low2float(p1); v[3] = __high2float(p1);
           }
-        } else if (a.amode == A_RMS) {
-          const bool second = a.split > 0 && t >= a.split;
-          const float r = s.stat_rs[t];
-          const __nv_bfloat16 *wv = second ? a.nw_alt : nw;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[e] = v[e] * r * __bfloat162float(wv[k + e]);
-        } else if (a.amode == A_RMS2) {
-          const float r1 = s.stat_mu[t], r2 = s.stat_rs[t];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            v[e] = (v[e] * r1 * __bfloat162float(nw[k + e])) * r2 * __bfloat162float(nw2[k + e]);
-        } else if (a.amode == A_LNMOD) {
-          const float mu = s.stat_mu[t], r = s.stat_rs[t];
-          const float4 sc = *reinterpret_cast<const float4 *>(a.sc + k);
-          const float4 sh = *reinterpret_cast<const float4 *>(a.sh + k);
-          v[0] = (v[0] - mu) * r * (1.f + sc.x) + sh.x;
-          v[1] = (v[1] - mu) * r * (1.f + sc.y) + sh.y;
-          v[2] = (v[2] - mu) * r * (1.f + sc.z) + sh.z;
-          v[3] = (v[3] - mu) * r * (1.f + sc.w) + sh.w;
         }
-      }
-      __nv_bfloat16 h[4], l[4];
+      } else if (a.amode == A_RMS) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
-      const uint32_t cbase = dst + (uint32_t)(kq >> 6) * (32 * MT * 128);
-      const int kk = kq & 63;
-      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(t, kk)), "r"(pack_bf16(h[0], h[1])),
-                   "r"(pack_bf16(h[2], h[3])));
-      asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(rows + t, kk)), "r"(pack_bf16(l[0], l[1])),
-                   "r"(pack_bf16(l[2], l[3])));
+        for (int e = 0; e < 4; ++e) v[e] = v[e] * rs * __bfloat162float(wv[k + e]);
+      } else if (a.amode == A_RMS2) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          v[e] = (v[e] * mu * __bfloat162float(nw[k + e])) * rs * __bfloat162float(nw2[k + e]);
+      } else if (a.amode == A_LNMOD) {
+        const float4 sc = *reinterpret_cast<const float4 *>(a.sc + k);
+        const float4 sh = *reinterpret_cast<const float4 *>(a.sh + k);
+        v[0] = (v[0] - mu) * rs * (1.f + sc.x) + sh.x;
+        v[1] = (v[1] - mu) * rs * (1.f + sc.y) + sh.y;
+        v[2] = (v[2] - mu) * rs * (1.f + sc.z) + sh.z;
+        v[3] = (v[3] - mu) * rs * (1.f + sc.w) + sh.w;
+      }
     }
+    __nv_bfloat16 h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
+    const uint32_t cbase = dst + (uint32_t)(kq >> 6) * (32 * MT * 128);
+    const int kk = kq & 63;
+    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(t, kk)), "r"(pack_bf16(h[0], h[1])),
+                 "r"(pack_bf16(h[2], h[3])));
+    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(rows + t, kk)), "r"(pack_bf16(l[0], l[1])),
+                 "r"(pack_bf16(l[2], l[3])));
   }
 }
 
@@ -368,7 +359,7 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
 }  // namespace
 
 template <int MT>
-__global__ void __launch_bounds__(kAll, 1) gemv_kernel(const __grid_constant__ GemvArgs a, const int S) {
+__global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int NR = 32 * MT;                 // B rows: hi rows then lo rows
   constexpr int BCH = NR * 128;               // bytes of one 64-column B chunk
@@ -385,10 +376,14 @@ __global__ void __launch_bounds__(kAll, 1) gemv_kernel(const __grid_constant__ G
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
   const uint32_t ring = base;
+  // a ring stage holds U consecutive chunks moved by one bulk copy (the copy engine
+  // takes a roughly fixed time per copy, so larger copies stream faster)
+  const int UB = U * kStageBytes;
+  const int units = nchunks / U;
   Smem s;
-  s.bbuf[0] = ring + S * kStageBytes;
+  s.bbuf[0] = ring + S * UB;
   s.bbuf[1] = s.bbuf[0] + cpp * BCH;
-  s.cs_ptr = reinterpret_cast<float *>(gbase + S * kStageBytes + 2 * cpp * BCH);
+  s.cs_ptr = reinterpret_cast<float *>(gbase + S * UB + 2 * cpp * BCH);
   s.stat_mu = s.cs_ptr + 16 * MT * kCsStride;
   s.stat_rs = s.stat_mu + kMaxT;
   const uint32_t bars = smem_u32(s.stat_rs + kMaxT);
@@ -410,12 +405,10 @@ __global__ void __launch_bounds__(kAll, 1) gemv_kernel(const __grid_constant__ G
     mbar_init(accfull, 1);
     mbar_fence_init();
     // weights do not depend on earlier kernels: start streaming them now
-    for (int c = 0; c < S && c < nchunks; ++c) {
-      mbar_expect_tx(full(c), kStageBytes);
-      bulk_g2s(ring + c * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(c));
+    for (int j = 0; j < S && j < units; ++j) {
+      mbar_expect_tx(full(j), UB);
+      bulk_g2s(ring + j * UB, wsrc + (size_t)j * UB, UB, full(j));
     }
-    // the rest of this CTA's slice goes to L2 now, so the ring refills hit L2
-    for (int c = S; c < nchunks; ++c) bulk_prefetch_l2(wsrc + (size_t)c * kStageBytes, kStageBytes);
   }
   if (warp == 1) tmem_alloc<NR>(tslot);
   pdl_trigger();
@@ -429,27 +422,27 @@ __global__ void __launch_bounds__(kAll, 1) gemv_kernel(const __grid_constant__ G
   if (warp == 0) {
     // weights: refill a stage once the MMAs that read it have completed
     if (lane == 0) {
-      for (int c = S; c < nchunks; ++c) {
-        const int st = c % S;
-        if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
-        mbar_expect_tx(full(st), kStageBytes);
-        bulk_g2s(ring + st * kStageBytes, wsrc + (size_t)c * kStageBytes, kStageBytes, full(st));
+      for (int j = S; j < units; ++j) {
+        const int st = j % S;
+        if (!mbar_wait_bounded(empty(st), (j / S - 1) & 1, a.err)) break;
+        mbar_expect_tx(full(st), UB);
+        bulk_g2s(ring + st * UB, wsrc + (size_t)j * UB, UB, full(st));
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c % S, piece = c / cpp, pb = piece & 1;
+        const int j = c / U, st = j % S, piece = c / cpp, pb = piece & 1;
         if (c % cpp == 0 && !mbar_wait_bounded(bfull0 + 8 * pb, (piece >> 1) & 1, a.err)) ok = false;
-        if (ok && !mbar_wait_bounded(full(st), (c / S) & 1, a.err)) ok = false;
+        if (ok && !mbar_wait_bounded(full(st), (j / S) & 1, a.err)) ok = false;
         if (!ok) break;
         tc_fence_after();
-        const uint64_t ad = umma_desc_sw128(ring + st * kStageBytes);
+        const uint64_t ad = umma_desc_sw128(ring + st * UB + (c % U) * kStageBytes);
         const uint64_t bd = umma_desc_sw128(s.bbuf[pb] + (c % cpp) * BCH);
 #pragma unroll
         for (int kk = 0; kk < kChunk / 16; ++kk) umma_ss(tmem, ad + 2 * kk, bd + 2 * kk, IDESC, (c | kk) ? 1u : 0u);
-        umma_commit(empty(st));
+        if (c % U == U - 1) umma_commit(empty(st));
         if (c % cpp == cpp - 1 || c == nchunks - 1) umma_commit(bempty0 + 8 * pb);
       }
       umma_commit(accfull);
@@ -469,6 +462,8 @@ __global__ void __launch_bounds__(kAll, 1) gemv_kernel(const __grid_constant__ G
     }
     mbar_wait_bounded(accfull, 0, a.err);
     tc_fence_after();
+  }
+  if (warp >= 2 && warp < 6) {
     // TMEM lane = weight row; columns: hi rows then lo rows of the activations
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
@@ -548,10 +543,14 @@ __global__ void __launch_bounds__(kAll, 1) gemv_kernel(const __grid_constant__ G
   }
 }
 
+// ring chunks (16 KB each), and chunks per bulk copy
 static int gemv_stages(const GemvArgs &a, int mt) {
   (void)mt;
   const int nchunks = a.Kc / kChunk;
   return nchunks < 4 ? nchunks : 4;
+}
+static int gemv_unit(const GemvArgs &a, int mt) {
+  return (a.Kc / kChunk) % 2 == 0 && gemv_stages(a, mt) % 2 == 0 ? 2 : 1;
 }
 
 size_t gemv_smem_bytes(const GemvArgs &a, int mt) {
@@ -566,7 +565,8 @@ size_t gemv_smem_bytes(const GemvArgs &a, int mt) {
 cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t st, bool pdl) {
   const int mt = (a.T_const > 0 && a.T_const <= 16) ? 1 : 2;
   const size_t smem = gemv_smem_bytes(a, mt);
-  const int S = gemv_stages(a, mt);
+  const int U = gemv_unit(a, mt);
+  const int S = gemv_stages(a, mt) / U;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_tiles, a.ksplit, 1);
   cfg.blockDim = dim3(kAll, 1, 1);
@@ -590,11 +590,11 @@ cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t st, bool pd
   if (mt == 1) {
     e = cudaFuncSetAttribute(gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<1>, a, S);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<1>, a, S, U);
   }
   e = cudaFuncSetAttribute(gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<2>, a, S);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<2>, a, S, U);
 }
 
 }  // namespace fm

@@ -37,7 +37,6 @@ constexpr int kLook = kNSlot - 1;             // Q8: conversion runs this many c
 constexpr int kQ8Workers = 256;               // Q8: warps 2..9
 constexpr int kBfWorkers = 128;               // bf16: warps 2..5
 constexpr int kBase = 64;                     // warp 0: producer, warp 1: TMEM owner + MMA issuer
-constexpr int kL2Ahead = 16;                  // chunks warmed in L2 ahead of the shared-memory ring
 
 
 // tcgen05.mma with A in tensor memory (lane = A row, 32-bit columns hold K pairs)
@@ -184,7 +183,7 @@ __device__ __forceinline__ int my_tile_count(int n_tiles) {
 
 // ---------------------------------------------------------------- Q8_0 table
 // TMEM columns: A slots [32 j, 32 j + 32), D slots 128 + 64 j + 32 blk.
-__global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S) {
+__global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kQ8Chunk;
   constexpr uint32_t IDESC = umma_idesc(128, 32, false);
@@ -192,7 +191,10 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ybuf = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t ring = ybuf + kcs * kYChunk;
-  const uint32_t bars = ring + S * SB;
+  // a ring stage holds U consecutive chunks of one tile, moved by one bulk copy: the
+  // copy engine takes a roughly fixed time per copy, so fewer, larger copies stream faster
+  const int UB = U * SB;
+  const uint32_t bars = ring + S * UB;
   auto full = [&](int i) { return bars + 8 * i; };
   auto empty = [&](int i) { return bars + 8 * (S + i); };
   auto afull = [&](int j) { return bars + 8 * (2 * S + j); };
@@ -221,12 +223,10 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
     mbar_init(yfull, 1);
     mbar_fence_init();
     // the table does not depend on earlier kernels
-    for (int c = 0; c < S && c < total; ++c) {
-      mbar_expect_tx(full(c), SB);
-      bulk_g2s(ring + c * SB, src_of(c), SB, full(c));
+    for (int j = 0; j < S && j * U < total; ++j) {
+      mbar_expect_tx(full(j), UB);
+      bulk_g2s(ring + j * UB, src_of(j * U), UB, full(j));
     }
-    // a bulk copy takes microseconds to land: keep more of the stream in flight through L2
-    for (int c = S; c < S + kL2Ahead && c < total; ++c) bulk_prefetch_l2(src_of(c), SB);
   }
   if (warp == 1) tmem_alloc<512>(tslot);
   pdl_trigger();
@@ -240,12 +240,11 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   if (warp == 0) {
     if (lane == 0) {
       if (a.ylm) load_ylm(a, ybuf, yfull);
-      for (int c = S; c < total; ++c) {
-        const int st = c % S;
-        if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
-        mbar_expect_tx(full(st), SB);
-        bulk_g2s(ring + st * SB, src_of(c), SB, full(st));
-        if (c + kL2Ahead < total) bulk_prefetch_l2(src_of(c + kL2Ahead), SB);
+      for (int j = S; j * U < total; ++j) {
+        const int st = j % S;
+        if (!mbar_wait_bounded(empty(st), (j / S - 1) & 1, a.err)) break;
+        mbar_expect_tx(full(st), UB);
+        bulk_g2s(ring + st * UB, src_of(j * U), UB, full(st));
       }
     }
   } else if (warp == 1) {
@@ -292,9 +291,9 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
         const int c = base + u;
         if (c < total && ok) {
           // convert: block G of row r -> f16 into A slot u (= c % kNSlot)
-          const int st = c % S;
-          if (!mbar_wait_bounded(full(st), (c / S) & 1, a.err)) ok = false;
-          const uint32_t buf = ring + st * SB;
+          const int j = c / U, st = j % S;
+          if (!mbar_wait_bounded(full(st), (j / S) & 1, a.err)) ok = false;
+          const uint32_t buf = ring + st * UB + (c % U) * SB;
           const uint32_t x = ((r >> 1) & 3);
           const uint4 q0 = lds128(buf + r * 64 + (((2 * G) ^ x) << 4));
           const uint4 q1 = lds128(buf + r * 64 + (((2 * G + 1) ^ x) << 4));
@@ -315,7 +314,7 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(empty(st));
+            if (c % U == U - 1) mbar_arrive(empty(st));
             mbar_arrive(afull(u));
           }
         }
@@ -362,7 +361,7 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
 
 // ---------------------------------------------------------------- bf16 table
 // TMEM columns: per-tile accumulator, double buffered at 0 and 32.
-__global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(const __grid_constant__ LmArgs a, const int S) {
+__global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kBfStage;
   constexpr uint32_t IDESC = umma_idesc(128, 32, true);
@@ -370,7 +369,10 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ybuf = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t ring = ybuf + kcs * kYChunk;
-  const uint32_t bars = ring + S * SB;
+  // a ring stage holds U consecutive chunks of one tile, moved by one bulk copy: the
+  // copy engine takes a roughly fixed time per copy, so fewer, larger copies stream faster
+  const int UB = U * SB;
+  const uint32_t bars = ring + S * UB;
   auto full = [&](int i) { return bars + 8 * i; };
   auto empty = [&](int i) { return bars + 8 * (S + i); };
   auto dfull = [&](int j) { return bars + 8 * (2 * S + j); };
@@ -397,12 +399,10 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
     }
     mbar_init(yfull, 1);
     mbar_fence_init();
-    for (int c = 0; c < S && c < total; ++c) {
-      mbar_expect_tx(full(c), SB);
-      bulk_g2s(ring + c * SB, src_of(c), SB, full(c));
+    for (int j = 0; j < S && j * U < total; ++j) {
+      mbar_expect_tx(full(j), UB);
+      bulk_g2s(ring + j * UB, src_of(j * U), UB, full(j));
     }
-    // a bulk copy takes microseconds to land: keep more of the stream in flight through L2
-    for (int c = S; c < S + kL2Ahead && c < total; ++c) bulk_prefetch_l2(src_of(c), SB);
   }
   if (warp == 1) tmem_alloc<64>(tslot);
   pdl_trigger();
@@ -416,27 +416,26 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
   if (warp == 0) {
     if (lane == 0) {
       if (a.ylm) load_ylm(a, ybuf, yfull);
-      for (int c = S; c < total; ++c) {
-        const int st = c % S;
-        if (!mbar_wait_bounded(empty(st), (c / S - 1) & 1, a.err)) break;
-        mbar_expect_tx(full(st), SB);
-        bulk_g2s(ring + st * SB, src_of(c), SB, full(st));
-        if (c + kL2Ahead < total) bulk_prefetch_l2(src_of(c + kL2Ahead), SB);
+      for (int j = S; j * U < total; ++j) {
+        const int st = j % S;
+        if (!mbar_wait_bounded(empty(st), (j / S - 1) & 1, a.err)) break;
+        mbar_expect_tx(full(st), UB);
+        bulk_g2s(ring + st * UB, src_of(j * U), UB, full(st));
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
       for (int c = 0; c < total; ++c) {
-        const int st = c % S, ti = c / kcs, kc = c % kcs, db = ti & 1;
+        const int st = (c / U) % S, ti = c / kcs, kc = c % kcs, db = ti & 1;
         if (kc == 0 && ti >= 2 && !mbar_wait_bounded(dempty(db), ((ti >> 1) - 1) & 1, a.err)) break;
-        if (!mbar_wait_bounded(full(st), (c / S) & 1, a.err)) break;
+        if (!mbar_wait_bounded(full(st), (c / U / S) & 1, a.err)) break;
         tc_fence_after();
-        const uint64_t ad = umma_desc_sw128(ring + st * SB);
+        const uint64_t ad = umma_desc_sw128(ring + st * UB + (c % U) * SB);
         const uint64_t bd = umma_desc_sw128(ybuf + kc * kYChunk);
 #pragma unroll
         for (int kk = 0; kk < kChunk / 16; ++kk)
           umma_ss(tmem + 32 * db, ad + 2 * kk, bd + 2 * kk, IDESC, (kc | kk) ? 1u : 0u);
-        umma_commit(empty(st));
+        if (c % U == U - 1) umma_commit(empty(st));
         if (kc == kcs - 1) umma_commit(dfull(db));
       }
     }
@@ -530,9 +529,15 @@ int lmhead_grid(const LmArgs &a, int n_sm) {
 cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) {
   const bool q8 = a.q8 != nullptr;
   const size_t ybytes = (size_t)(a.H / kChunk) * kYChunk;
-  const size_t sb = q8 ? kQ8Chunk : kBfStage;
   const size_t fixed = 1024 + ybytes + 8 * (3 * kNSlot + 8) + 16;
   const size_t budget = 227 * 1024 - 2048;   // leaves room for the static shared arrays
+  // two chunks per bulk copy when a tile's chunk count is even and three such stages fit
+  int U = (a.H / kChunk) % 2 == 0 ? 2 : 1;
+  size_t sb = (size_t)U * (q8 ? kQ8Chunk : kBfStage);
+  if (U == 2 && fixed + 3 * (sb + 16) > budget) {
+    U = 1;
+    sb /= 2;
+  }
   if (fixed + 2 * (sb + 16) > budget) return cudaErrorInvalidValue;
   int S = (int)((budget - fixed) / (sb + 16));
   if (S > 12) S = 12;
@@ -551,11 +556,11 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) 
   if (q8) {
     e = cudaFuncSetAttribute(lmhead_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, lmhead_q8_kernel, a, S);
+    return cudaLaunchKernelEx(&cfg, lmhead_q8_kernel, a, S, U);
   }
   e = cudaFuncSetAttribute(lmhead_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, lmhead_bf16_kernel, a, S);
+  return cudaLaunchKernelEx(&cfg, lmhead_bf16_kernel, a, S, U);
 }
 
 }  // namespace fm
