@@ -32,8 +32,6 @@ namespace {
 constexpr int kChunk = 64;
 constexpr int kBfStage = kTile * kChunk * 2;  // 16 KB bf16 chunk
 constexpr int kYChunk = kLmYChunk;            // one 64-column chunk of the resident Y (32 rows x 128 B)
-constexpr int kNSlot = 4;                     // Q8: chunks in flight between conversion and epilogue
-constexpr int kLook = kNSlot - 1;             // Q8: conversion runs this many chunks ahead
 constexpr int kQ8Workers = 256;               // Q8: warps 2..9
 constexpr int kBfWorkers = 128;               // bf16: warps 2..5
 constexpr int kBase = 64;                     // warp 0: producer, warp 1: TMEM owner + MMA issuer
@@ -56,6 +54,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
+// 16 columns of this thread's lane; the caller waits with tmem_ld_wait() before using them
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&f)[16]) {
   uint32_t v[16];
   asm volatile(
@@ -182,10 +189,16 @@ __device__ __forceinline__ int my_tile_count(int n_tiles) {
 }  // namespace
 
 // ---------------------------------------------------------------- Q8_0 table
-// TMEM columns: A slots [32 j, 32 j + 32), D slots 128 + 64 j + 32 blk.
+// Roles: warp 0 streams the table, warp 1 owns TMEM and issues the MMAs, warps
+// 2..5 convert (one thread per table row), warps 6..9 apply the block scales
+// and keep the running best (one thread per table row, all 16 slots).
+// TMEM columns: A slots [32 i, 32 i + 32) for i < kNA; D slots 128 + 64 j + 32 blk
+// for j < kND (per 32-column block of the chunk: 32 columns, per group of 8
+// slots 8 hi then 8 lo).
 __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kQ8Chunk;
+  constexpr int kNA = 4, kND = 6;
   constexpr uint32_t IDESC = umma_idesc(128, 32, false);
   const int H = a.H, kcs = H / kChunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,10 +210,11 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   const uint32_t bars = ring + S * UB;
   auto full = [&](int i) { return bars + 8 * i; };
   auto empty = [&](int i) { return bars + 8 * (S + i); };
-  auto afull = [&](int j) { return bars + 8 * (2 * S + j); };
-  auto dfull = [&](int j) { return bars + 8 * (2 * S + kNSlot + j); };
-  auto dempty = [&](int j) { return bars + 8 * (2 * S + 2 * kNSlot + j); };
-  const uint32_t yfull = bars + 8 * (2 * S + 3 * kNSlot);
+  auto afull = [&](int i) { return bars + 8 * (2 * S + i); };
+  auto aempty = [&](int i) { return bars + 8 * (2 * S + kNA + i); };
+  auto dfull = [&](int j) { return bars + 8 * (2 * S + 2 * kNA + j); };
+  auto dempty = [&](int j) { return bars + 8 * (2 * S + 2 * kNA + kND + j); };
+  const uint32_t yfull = bars + 8 * (2 * S + 2 * kNA + 2 * kND);
   const uint32_t tslot = yfull + 8;
 
   const int n_tiles = (a.V + kTile - 1) / kTile;
@@ -213,12 +227,15 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full(i), 1);
-      mbar_init(empty(i), kQ8Workers / 32);
+      mbar_init(empty(i), 4);
     }
-    for (int j = 0; j < kNSlot; ++j) {
-      mbar_init(afull(j), kQ8Workers / 32);
+    for (int i = 0; i < kNA; ++i) {
+      mbar_init(afull(i), 4);
+      mbar_init(aempty(i), 1);
+    }
+    for (int j = 0; j < kND; ++j) {
       mbar_init(dfull(j), 1);
-      mbar_init(dempty(j), kQ8Workers / 32);
+      mbar_init(dempty(j), 4);
     }
     mbar_init(yfull, 1);
     mbar_fence_init();
@@ -237,6 +254,21 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   pdl_wait();
   const int T = a.T_const > 0 ? a.T_const : a.sp->T;
 
+  if (!a.ylm && warp >= 2) {
+    stage_y<true>(a, ybuf, T, (int)threadIdx.x - kBase, kQ8Workers);
+    fence_proxy_async();
+    named_sync(1, kQ8Workers);
+    if (threadIdx.x == kBase) mbar_arrive(yfull);
+  }
+
+  const int quad = warp & 3;
+  const int r = 32 * quad + lane;
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16);
+  float bv[16];
+  int bi[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; }
+
   if (warp == 0) {
     if (lane == 0) {
       if (a.ylm) load_ylm(a, ybuf, yfull);
@@ -250,108 +282,114 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   } else if (warp == 1) {
     if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
       for (int c = 0; c < total; ++c) {
-        const int j = c % kNSlot;
-        if (!mbar_wait_bounded(afull(j), (c / kNSlot) & 1, a.err)) break;
-        if (c >= kNSlot && !mbar_wait_bounded(dempty(j), (c / kNSlot - 1) & 1, a.err)) break;
+        const int i = c % kNA, j = c % kND;
+        if (!mbar_wait_bounded(afull(i), (c / kNA) & 1, a.err)) break;
+        if (c >= kND && !mbar_wait_bounded(dempty(j), (c / kND - 1) & 1, a.err)) break;
         tc_fence_after();
         const uint64_t bd = umma_desc_sw128(ybuf + (c % kcs) * kYChunk);
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
-            umma_ts(tmem + 128 + 64 * j + 32 * blk, tmem + 32 * j + 16 * blk + 8 * kk, bd + 2 * (2 * blk + kk), IDESC,
+            umma_ts(tmem + 128 + 64 * j + 32 * blk, tmem + 32 * i + 16 * blk + 8 * kk, bd + 2 * (2 * blk + kk), IDESC,
                     kk);
+        umma_commit(aempty(i));
         umma_commit(dfull(j));
       }
     }
-  }
-
-  // converter / epilogue threads: row r of each tile, slot group G (8 slots)
-  const int e = (int)threadIdx.x - kBase;
-  const int quad = warp & 3;
-  const int r = 32 * quad + lane;
-  const int G = (warp - 2) >> 2;   // warps 2..5: block 0 / slots 0..7; warps 6..9: block 1 / slots 8..15
-  const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16);
-  float bv[8], acc[8];
-  int bi[8];
+  } else if (warp < 6) {
+    // converters: row r of chunk c -> f16 pairs in A slot c % kNA
+    const uint32_t x = (uint32_t)((r >> 1) & 3);
+    for (int c = 0; c < total; ++c) {
+      const int jj = c / U, st = jj % S, i = c % kNA;
+      if (!mbar_wait_bounded(full(st), (jj / S) & 1, a.err)) break;
+      if (c >= kNA && !mbar_wait_bounded(aempty(i), (c / kNA - 1) & 1, a.err)) break;
+      tc_fence_after();
+      const uint32_t buf = ring + st * UB + (c % U) * SB + r * 64;
+      uint4 q[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; acc[i] = 0.f; }
-  if (warp >= 2) {
-    if (!a.ylm) {
-      stage_y<true>(a, ybuf, T, e, kQ8Workers);
-      fence_proxy_async();
-      named_sync(1, kQ8Workers);
-      if (e == 0) mbar_arrive(yfull);
-    }
-    uint32_t sc[kNSlot];   // the two block scales (f16x2) of each chunk in flight, by slot
-    bool ok = true;
-    for (int base = 0; base < total + kLook; base += kNSlot) {
+      for (int pc = 0; pc < 4; ++pc) q[pc] = lds128(buf + ((pc ^ x) << 4));
 #pragma unroll
-      for (int u = 0; u < kNSlot; ++u) {
-        const int c = base + u;
-        if (c < total && ok) {
-          // convert: block G of row r -> f16 into A slot u (= c % kNSlot)
-          const int j = c / U, st = j % S;
-          if (!mbar_wait_bounded(full(st), (j / S) & 1, a.err)) ok = false;
-          const uint32_t buf = ring + st * UB + (c % U) * SB;
-          const uint32_t x = ((r >> 1) & 3);
-          const uint4 q0 = lds128(buf + r * 64 + (((2 * G) ^ x) << 4));
-          const uint4 q1 = lds128(buf + r * 64 + (((2 * G + 1) ^ x) << 4));
-          // the f16 scales of row r for blocks 0 and 1 (two rows share each 32-bit word)
-          const uint32_t w0 = lds32(buf + kTile * 64 + (r & ~1) * 2);
-          const uint32_t w1 = lds32(buf + kTile * 64 + 256 + (r & ~1) * 2);
-          sc[u] = (r & 1) ? (w0 >> 16) | (w1 & 0xffff0000u) : (w0 & 0xffffu) | (w1 << 16);
-          uint32_t w[16];
-          i8x4_to_f16x4(q0.x, w[0], w[1]);
-          i8x4_to_f16x4(q0.y, w[2], w[3]);
-          i8x4_to_f16x4(q0.z, w[4], w[5]);
-          i8x4_to_f16x4(q0.w, w[6], w[7]);
-          i8x4_to_f16x4(q1.x, w[8], w[9]);
-          i8x4_to_f16x4(q1.y, w[10], w[11]);
-          i8x4_to_f16x4(q1.z, w[12], w[13]);
-          i8x4_to_f16x4(q1.w, w[14], w[15]);
-          tmem_st16(lane_base + 32 * u + 16 * G, w);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if (c % U == U - 1) mbar_arrive(empty(st));
-            mbar_arrive(afull(u));
-          }
+      for (int h = 0; h < 2; ++h) {   // block h: pieces 2h, 2h + 1
+        uint32_t w[16];
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          const uint4 v = q[2 * h + pp];
+          i8x4_to_f16x4(v.x, w[8 * pp + 0], w[8 * pp + 1]);
+          i8x4_to_f16x4(v.y, w[8 * pp + 2], w[8 * pp + 3]);
+          i8x4_to_f16x4(v.z, w[8 * pp + 4], w[8 * pp + 5]);
+          i8x4_to_f16x4(v.w, w[8 * pp + 6], w[8 * pp + 7]);
         }
-        const int ce = c - kLook;
-        const int ue = (u + 1) % kNSlot;   // = ce % kNSlot
-        if (ce >= 0 && ce < total && ok) {
-          if (!mbar_wait_bounded(dfull(ue), (ce / kNSlot) & 1, a.err)) ok = false;
-          tc_fence_after();
-          float d0[16], d1[16];
-          tmem_ld16(lane_base + 128 + 64 * ue + 16 * G, d0);
-          tmem_ld16(lane_base + 128 + 64 * ue + 32 + 16 * G, d1);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(dempty(ue));
-          const uint32_t scw = sc[ue];
-          const __half2 sh = *reinterpret_cast<const __half2 *>(&scw);
-          const float f0 = __low2float(sh), f1 = __high2float(sh);
+        tmem_st16(lane_base + 32 * i + 16 * h, w);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(afull(i));
+        if (c % U == U - 1) mbar_arrive(empty(st));
+      }
+    }
+  } else {
+    // epilogue: scale each block's partial sums, accumulate the row's logits, keep the best
+    float acc[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] += f0 * (d0[i] + d0[8 + i]) + f1 * (d1[i] + d1[8 + i]);
-          if (ce % kcs == kcs - 1) {
-            const int v = (blockIdx.x + (ce / kcs) * gridDim.x) * kTile + r;
+    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+    // the row's two f16 block scales of chunk c, read from the table (L2) kND chunks ahead
+    auto scale_of = [&](int c) -> uint32_t {
+      if (c >= total) return 0u;
+      const uint8_t *sp = src_of(c) + kTile * 64;
+      const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(sp + (r & ~1) * 2));
+      const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t *>(sp + 256 + (r & ~1) * 2));
+      return (r & 1) ? (w0 >> 16) | (w1 & 0xffff0000u) : (w0 & 0xffffu) | (w1 << 16);
+    };
+    uint32_t sc[kND];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int t = 8 * G + i;
-              if (v < a.V && t < T) {
-                if (a.logits) a.logits[(size_t)t * a.V + v] = acc[i];
-                if (better(acc[i], v, bv[i], bi[i])) { bv[i] = acc[i]; bi[i] = v; }
-              }
-              acc[i] = 0.f;
+    for (int u = 0; u < kND; ++u) sc[u] = scale_of(u);
+    bool ok = true;
+    for (int base = 0; base < total && ok; base += kND) {
+#pragma unroll
+      for (int u = 0; u < kND; ++u) {
+        const int c = base + u;
+        if (c >= total || !ok) break;
+        if (!mbar_wait_bounded(dfull(u), (c / kND) & 1, a.err)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t dr[4][16];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_async(lane_base + 128 + 64 * u + 16 * q4, dr[q4]);
+        tmem_ld_wait();
+        float d[4][16];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) d[q4][e] = __uint_as_float(dr[q4][e]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dempty(u));
+        const uint32_t scw = sc[u];
+        sc[u] = scale_of(c + kND);
+        const __half2 sh = *reinterpret_cast<const __half2 *>(&scw);
+        const float f0 = __low2float(sh), f1 = __high2float(sh);
+        // d[0]: block 0 slots 0..7 (hi, lo), d[1]: block 0 slots 8..15, d[2], d[3]: block 1
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          acc[t] += f0 * (d[0][t] + d[0][8 + t]) + f1 * (d[2][t] + d[2][8 + t]);
+          acc[8 + t] += f0 * (d[1][t] + d[1][8 + t]) + f1 * (d[3][t] + d[3][8 + t]);
+        }
+        if (c % kcs == kcs - 1) {
+          const int v = (blockIdx.x + (c / kcs) * gridDim.x) * kTile + r;
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            if (v < a.V && t < T) {
+              if (a.logits) a.logits[(size_t)t * a.V + v] = acc[t];
+              if (better(acc[t], v, bv[t], bi[t])) { bv[t] = acc[t]; bi[t] = v; }
             }
+            acc[t] = 0.f;
           }
         }
       }
     }
   }
-  // rows are split over quadrants; slot group G's bests live in warps of that group
-  finish_argmax<8>(a, T, warp >= 2, 8 * G, bv, bi);
+  finish_argmax<16>(a, T, warp >= 6, 0, bv, bi);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -529,7 +567,7 @@ int lmhead_grid(const LmArgs &a, int n_sm) {
 cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) {
   const bool q8 = a.q8 != nullptr;
   const size_t ybytes = (size_t)(a.H / kChunk) * kYChunk;
-  const size_t fixed = 1024 + ybytes + 8 * (3 * kNSlot + 8) + 16;
+  const size_t fixed = 1024 + ybytes + 8 * (2 * 4 + 2 * 6 + 2) + 16;
   const size_t budget = 227 * 1024 - 2048;   // leaves room for the static shared arrays
   // two chunks per bulk copy when a tile's chunk count is even and three such stages fit
   int U = (a.H / kChunk) % 2 == 0 ? 2 : 1;
