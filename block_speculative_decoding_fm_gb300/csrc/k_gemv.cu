@@ -422,28 +422,32 @@ __global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __gri
   if (warp == 0) {
     // weights: refill a stage once the MMAs that read it have completed
     if (lane == 0) {
+      int st = 0;
+      uint32_t par = 0;
       for (int j = S; j < units; ++j) {
-        const int st = j % S;
-        if (!mbar_wait_bounded(empty(st), (j / S - 1) & 1, a.err)) break;
+        if (!mbar_wait_bounded(empty(st), par, a.err)) break;
         mbar_expect_tx(full(st), UB);
         bulk_g2s(ring + st * UB, wsrc + (size_t)j * UB, UB, full(st));
+        if (++st == S) { st = 0; par ^= 1; }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = true;
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int j = c / U, st = j % S, piece = c / cpp, pb = piece & 1;
-        if (c % cpp == 0 && !mbar_wait_bounded(bfull0 + 8 * pb, (piece >> 1) & 1, a.err)) ok = false;
-        if (ok && !mbar_wait_bounded(full(st), (j / S) & 1, a.err)) ok = false;
-        if (!ok) break;
+      // counters instead of divisions: this thread's per-chunk work is a serial chain
+      int st = 0, uo = 0, pc = 0, pb = 0;
+      uint32_t fpar = 0, ppar = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        if (pc == 0 && !mbar_wait_bounded(bfull0 + 8 * pb, ppar, a.err)) break;
+        if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) break;
         tc_fence_after();
-        const uint64_t ad = umma_desc_sw128(ring + st * UB + (c % U) * kStageBytes);
-        const uint64_t bd = umma_desc_sw128(s.bbuf[pb] + (c % cpp) * BCH);
+        const uint64_t ad = umma_desc_sw128(ring + st * UB + uo * kStageBytes);
+        const uint64_t bd = umma_desc_sw128(s.bbuf[pb] + pc * BCH);
 #pragma unroll
         for (int kk = 0; kk < kChunk / 16; ++kk) umma_ss(tmem, ad + 2 * kk, bd + 2 * kk, IDESC, (c | kk) ? 1u : 0u);
-        if (c % U == U - 1) umma_commit(empty(st));
-        if (c % cpp == cpp - 1 || c == nchunks - 1) umma_commit(bempty0 + 8 * pb);
+        if (uo == U - 1) umma_commit(empty(st));
+        if (pc == cpp - 1 || c == nchunks - 1) umma_commit(bempty0 + 8 * pb);
+        if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
+        if (++pc == cpp) { pc = 0; pb ^= 1; if (pb == 0) ppar ^= 1; }
       }
       umma_commit(accfull);
     }

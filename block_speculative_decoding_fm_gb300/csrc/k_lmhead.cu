@@ -32,7 +32,6 @@ namespace {
 constexpr int kChunk = 64;
 constexpr int kBfStage = kTile * kChunk * 2;  // 16 KB bf16 chunk
 constexpr int kYChunk = kLmYChunk;            // one 64-column chunk of the resident Y (32 rows x 128 B)
-constexpr int kQ8Workers = 256;               // Q8: warps 2..9
 constexpr int kBfWorkers = 128;               // bf16: warps 2..5
 constexpr int kBase = 64;                     // warp 0: producer, warp 1: TMEM owner + MMA issuer
 
@@ -190,12 +189,16 @@ __device__ __forceinline__ int my_tile_count(int n_tiles) {
 
 // ---------------------------------------------------------------- Q8_0 table
 // Roles: warp 0 streams the table, warp 1 owns TMEM and issues the MMAs, warps
-// 2..5 convert (one thread per table row), warps 6..9 apply the block scales
-// and keep the running best (one thread per table row, all 16 slots).
+// 2..9 convert (one thread per table row and 32-column block), warps 10..17
+// apply the block scales and keep the running best (one thread per table row
+// and group of 8 slots).
 // TMEM columns: A slots [32 i, 32 i + 32) for i < kNA; D slots 128 + 64 j + 32 blk
 // for j < kND (per 32-column block of the chunk: 32 columns, per group of 8
 // slots 8 hi then 8 lo).
-__global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
+constexpr int kQ8Conv = 8, kQ8Epi = 8;   // warps
+constexpr int kQ8Threads = kBase + 32 * (kQ8Conv + kQ8Epi);
+
+__global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kQ8Chunk;
   constexpr int kNA = 4, kND = 6;
@@ -218,31 +221,35 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   const uint32_t tslot = yfull + 8;
 
   const int n_tiles = (a.V + kTile - 1) / kTile;
-  const int total = my_tile_count(n_tiles) * kcs;
-  auto src_of = [&](int c) {
-    const int tile = blockIdx.x + (c / kcs) * gridDim.x;
-    return a.q8 + ((size_t)tile * kcs + (c % kcs)) * SB;
-  };
+  const int tiles = my_tile_count(n_tiles);
+  const int total = tiles * kcs;
+  const int units = total / U;
+  const size_t tile_stride = (size_t)gridDim.x * kcs * SB;   // bytes between this CTA's tiles
+  const uint8_t *first = a.q8 + (size_t)blockIdx.x * kcs * SB;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full(i), 1);
-      mbar_init(empty(i), 4);
+      mbar_init(empty(i), kQ8Conv);
     }
     for (int i = 0; i < kNA; ++i) {
-      mbar_init(afull(i), 4);
+      mbar_init(afull(i), kQ8Conv);
       mbar_init(aempty(i), 1);
     }
     for (int j = 0; j < kND; ++j) {
       mbar_init(dfull(j), 1);
-      mbar_init(dempty(j), 4);
+      mbar_init(dempty(j), kQ8Epi);
     }
     mbar_init(yfull, 1);
     mbar_fence_init();
-    // the table does not depend on earlier kernels
-    for (int j = 0; j < S && j * U < total; ++j) {
+    // the table does not depend on earlier kernels; a CTA's units walk its tiles in order
+    const uint8_t *src = first;
+    int kc = 0;
+    for (int j = 0; j < S && j < units; ++j) {
       mbar_expect_tx(full(j), UB);
-      bulk_g2s(ring + j * UB, src_of(j * U), UB, full(j));
+      bulk_g2s(ring + j * UB, src + (size_t)kc * SB, UB, full(j));
+      kc += U;
+      if (kc == kcs) { kc = 0; src += tile_stride; }
     }
   }
   if (warp == 1) tmem_alloc<512>(tslot);
@@ -255,38 +262,51 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
   const int T = a.T_const > 0 ? a.T_const : a.sp->T;
 
   if (!a.ylm && warp >= 2) {
-    stage_y<true>(a, ybuf, T, (int)threadIdx.x - kBase, kQ8Workers);
+    stage_y<true>(a, ybuf, T, (int)threadIdx.x - kBase, kQ8Threads - kBase);
     fence_proxy_async();
-    named_sync(1, kQ8Workers);
+    named_sync(1, kQ8Threads - kBase);
     if (threadIdx.x == kBase) mbar_arrive(yfull);
   }
 
   const int quad = warp & 3;
   const int r = 32 * quad + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16);
-  float bv[16];
-  int bi[16];
+  float bv[8];
+  int bi[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; }
+  for (int i = 0; i < 8; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; }
+  int group = 0;   // epilogue: slot group
 
   if (warp == 0) {
     if (lane == 0) {
       if (a.ylm) load_ylm(a, ybuf, yfull);
-      for (int j = S; j * U < total; ++j) {
-        const int st = j % S;
-        if (!mbar_wait_bounded(empty(st), (j / S - 1) & 1, a.err)) break;
+      // unit j reuses stage j % S once the converters released unit j - S
+      const uint8_t *src = first;
+      int kc = 0;
+      for (int j = 0; j < S && j < units; ++j) {
+        kc += U;
+        if (kc == kcs) { kc = 0; src += tile_stride; }
+      }
+      int st = 0;
+      uint32_t par = 0;
+      for (int j = S; j < units; ++j) {
+        if (!mbar_wait_bounded(empty(st), par, a.err)) break;
         mbar_expect_tx(full(st), UB);
-        bulk_g2s(ring + st * UB, src_of(j * U), UB, full(st));
+        bulk_g2s(ring + st * UB, src + (size_t)kc * SB, UB, full(st));
+        kc += U;
+        if (kc == kcs) { kc = 0; src += tile_stride; }
+        if (++st == S) { st = 0; par ^= 1; }
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
+      int i = 0, j = 0, kc = 0;
+      uint32_t apar = 0, dpar = 0;
       for (int c = 0; c < total; ++c) {
-        const int i = c % kNA, j = c % kND;
-        if (!mbar_wait_bounded(afull(i), (c / kNA) & 1, a.err)) break;
-        if (c >= kND && !mbar_wait_bounded(dempty(j), (c / kND - 1) & 1, a.err)) break;
+        if (!mbar_wait_bounded(afull(i), apar, a.err)) break;
+        if (c >= kND && !mbar_wait_bounded(dempty(j), dpar ^ 1, a.err)) break;
         tc_fence_after();
-        const uint64_t bd = umma_desc_sw128(ybuf + (c % kcs) * kYChunk);
+        const uint64_t bd = umma_desc_sw128(ybuf + kc * kYChunk);
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
@@ -295,101 +315,113 @@ __global__ void __launch_bounds__(kBase + kQ8Workers, 1) lmhead_q8_kernel(const 
                     kk);
         umma_commit(aempty(i));
         umma_commit(dfull(j));
+        if (++i == kNA) { i = 0; apar ^= 1; }
+        if (++j == kND) { j = 0; dpar ^= 1; }
+        if (++kc == kcs) kc = 0;
       }
     }
-  } else if (warp < 6) {
-    // converters: row r of chunk c -> f16 pairs in A slot c % kNA
+  } else if (warp < 2 + kQ8Conv) {
+    // converters: block b of row r of chunk c -> f16 pairs in A slot c % kNA
+    const int b = (warp - 2) >> 2;
     const uint32_t x = (uint32_t)((r >> 1) & 3);
+    const uint32_t o0 = (uint32_t)r * 64 + (((2 * b) ^ x) << 4), o1 = (uint32_t)r * 64 + (((2 * b + 1) ^ x) << 4);
+    int st = 0, uo = 0, i = 0;
+    uint32_t fpar = 0, apar = 0;
     for (int c = 0; c < total; ++c) {
-      const int jj = c / U, st = jj % S, i = c % kNA;
-      if (!mbar_wait_bounded(full(st), (jj / S) & 1, a.err)) break;
-      if (c >= kNA && !mbar_wait_bounded(aempty(i), (c / kNA - 1) & 1, a.err)) break;
+      if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) break;
+      if (c >= kNA && !mbar_wait_bounded(aempty(i), apar ^ 1, a.err)) break;
       tc_fence_after();
-      const uint32_t buf = ring + st * UB + (c % U) * SB + r * 64;
-      uint4 q[4];
-#pragma unroll
-      for (int pc = 0; pc < 4; ++pc) q[pc] = lds128(buf + ((pc ^ x) << 4));
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {   // block h: pieces 2h, 2h + 1
-        uint32_t w[16];
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-          const uint4 v = q[2 * h + pp];
-          i8x4_to_f16x4(v.x, w[8 * pp + 0], w[8 * pp + 1]);
-          i8x4_to_f16x4(v.y, w[8 * pp + 2], w[8 * pp + 3]);
-          i8x4_to_f16x4(v.z, w[8 * pp + 4], w[8 * pp + 5]);
-          i8x4_to_f16x4(v.w, w[8 * pp + 6], w[8 * pp + 7]);
-        }
-        tmem_st16(lane_base + 32 * i + 16 * h, w);
-      }
+      const uint32_t buf = ring + st * UB + uo * SB;
+      const uint4 v0 = lds128(buf + o0), v1 = lds128(buf + o1);
+      uint32_t w[16];
+      i8x4_to_f16x4(v0.x, w[0], w[1]);
+      i8x4_to_f16x4(v0.y, w[2], w[3]);
+      i8x4_to_f16x4(v0.z, w[4], w[5]);
+      i8x4_to_f16x4(v0.w, w[6], w[7]);
+      i8x4_to_f16x4(v1.x, w[8], w[9]);
+      i8x4_to_f16x4(v1.y, w[10], w[11]);
+      i8x4_to_f16x4(v1.z, w[12], w[13]);
+      i8x4_to_f16x4(v1.w, w[14], w[15]);
+      tmem_st16(lane_base + 32 * i + 16 * b, w);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(afull(i));
-        if (c % U == U - 1) mbar_arrive(empty(st));
+        if (uo == U - 1) mbar_arrive(empty(st));
       }
+      if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
+      if (++i == kNA) { i = 0; apar ^= 1; }
     }
   } else {
-    // epilogue: scale each block's partial sums, accumulate the row's logits, keep the best
-    float acc[16];
+    // epilogue: slot group g of row r: scale each block's partial sums, accumulate, keep the best
+    group = (warp - 2 - kQ8Conv) >> 2;
+    const int g = group;
+    float acc[8];
 #pragma unroll
-    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
-    // the row's two f16 block scales of chunk c, read from the table (L2) kND chunks ahead
-    auto scale_of = [&](int c) -> uint32_t {
-      if (c >= total) return 0u;
-      const uint8_t *sp = src_of(c) + kTile * 64;
-      const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(sp + (r & ~1) * 2));
-      const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t *>(sp + 256 + (r & ~1) * 2));
+    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+    // the row's two f16 block scales of a chunk, read from the table (L2) kND chunks ahead
+    const uint32_t soff = (uint32_t)kTile * 64 + (uint32_t)(r & ~1) * 2;
+    auto scale_at = [&](const uint8_t *chunk) -> uint32_t {
+      const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(chunk + soff));
+      const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t *>(chunk + soff + 256));
       return (r & 1) ? (w0 >> 16) | (w1 & 0xffff0000u) : (w0 & 0xffffu) | (w1 << 16);
     };
+    // lookahead cursor: chunk c + kND
+    const uint8_t *la_tile = first;
+    int la_kc = 0, la_c = 0;
     uint32_t sc[kND];
 #pragma unroll
-    for (int u = 0; u < kND; ++u) sc[u] = scale_of(u);
+    for (int u = 0; u < kND; ++u) {
+      sc[u] = la_c < total ? scale_at(la_tile + (size_t)la_kc * SB) : 0u;
+      ++la_c;
+      if (++la_kc == kcs) { la_kc = 0; la_tile += tile_stride; }
+    }
+    int kc = 0, tile = blockIdx.x;
+    uint32_t dpar = 0;
     bool ok = true;
     for (int base = 0; base < total && ok; base += kND) {
 #pragma unroll
       for (int u = 0; u < kND; ++u) {
         const int c = base + u;
-        if (c >= total || !ok) break;
-        if (!mbar_wait_bounded(dfull(u), (c / kND) & 1, a.err)) { ok = false; break; }
+        if (c >= total) break;
+        if (!mbar_wait_bounded(dfull(u), dpar, a.err)) { ok = false; break; }
         tc_fence_after();
-        uint32_t dr[4][16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_async(lane_base + 128 + 64 * u + 16 * q4, dr[q4]);
+        uint32_t d0[16], d1[16];
+        tmem_ld16_async(lane_base + 128 + 64 * u + 16 * g, d0);        // block 0: group g hi, lo
+        tmem_ld16_async(lane_base + 128 + 64 * u + 32 + 16 * g, d1);   // block 1
         tmem_ld_wait();
-        float d[4][16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) d[q4][e] = __uint_as_float(dr[q4][e]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dempty(u));
         const uint32_t scw = sc[u];
-        sc[u] = scale_of(c + kND);
+        sc[u] = la_c < total ? scale_at(la_tile + (size_t)la_kc * SB) : 0u;
+        ++la_c;
+        if (++la_kc == kcs) { la_kc = 0; la_tile += tile_stride; }
         const __half2 sh = *reinterpret_cast<const __half2 *>(&scw);
         const float f0 = __low2float(sh), f1 = __high2float(sh);
-        // d[0]: block 0 slots 0..7 (hi, lo), d[1]: block 0 slots 8..15, d[2], d[3]: block 1
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          acc[t] += f0 * (d[0][t] + d[0][8 + t]) + f1 * (d[2][t] + d[2][8 + t]);
-          acc[8 + t] += f0 * (d[1][t] + d[1][8 + t]) + f1 * (d[3][t] + d[3][8 + t]);
-        }
-        if (c % kcs == kcs - 1) {
-          const int v = (blockIdx.x + (c / kcs) * gridDim.x) * kTile + r;
+        for (int t = 0; t < 8; ++t)
+          acc[t] += f0 * (__uint_as_float(d0[t]) + __uint_as_float(d0[8 + t])) +
+                    f1 * (__uint_as_float(d1[t]) + __uint_as_float(d1[8 + t]));
+        if (++kc == kcs) {
+          kc = 0;
+          const int v = tile * kTile + r;
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            if (v < a.V && t < T) {
-              if (a.logits) a.logits[(size_t)t * a.V + v] = acc[t];
+          for (int t = 0; t < 8; ++t) {
+            const int slot = 8 * g + t;
+            if (v < a.V && slot < T) {
+              if (a.logits) a.logits[(size_t)slot * a.V + v] = acc[t];
               if (better(acc[t], v, bv[t], bi[t])) { bv[t] = acc[t]; bi[t] = v; }
             }
             acc[t] = 0.f;
           }
+          tile += gridDim.x;
         }
       }
+      dpar ^= 1;
     }
   }
-  finish_argmax<16>(a, T, warp >= 6, 0, bv, bi);
+  finish_argmax<8>(a, T, warp >= 2 + kQ8Conv, 8 * group, bv, bi);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -582,7 +614,7 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) 
   const size_t smem = fixed + (size_t)S * (sb + 16);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kBase + (q8 ? kQ8Workers : kBfWorkers), 1, 1);
+  cfg.blockDim = dim3(q8 ? kQ8Threads : kBase + kBfWorkers, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
