@@ -57,6 +57,30 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# kernel tag (as fm_profile_read names it) -> the source file that defines it
+KERNEL_SOURCES = {"lm_head": "k_lmhead.cu", "attn": "k_attn.cu", "gemv": "k_gemv.cu"}
+
+
+def ncu_traffic(tag):
+    """DRAM bytes (read + write) per launch of the kernel behind `tag`, from the
+    committed ncu summary profiles/ncu_dram_traffic.txt, or None when there is
+    no capture or the kernel's source has changed since it was taken (each
+    line records the digest of the source file the capture ran)."""
+    import hashlib
+    src = KERNEL_SOURCES.get(tag.split(".")[0])
+    path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
+    if src is None or not os.path.exists(path):
+        return None
+    with open(os.path.join(ROOT, "block_speculative_decoding_fm_gb300", "csrc", src), "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == tag and parts[3] == digest:
+                return float(parts[1])
+    return None
+
+
 class Clocks:
     """nvidia-smi samples every 200 ms while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -330,7 +354,7 @@ def run_ours(args):
         kernels = {k: {"launches": v[0] // 20, "ms_per_step": v[1] / 20,
                        "gbs": (v[2] / v[0]) / ((v[1] / v[0]) / 1000) / 1e9} for k, v in sorted(prof.items())}
         roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": None, "peak_source": f"{peak_src} burst copy",
+                    "frac": achieved / hbm, "traffic": ncu_traffic(name), "peak_source": f"{peak_src} burst copy",
                     "bytes_per_launch": tb / nl, "ms_per_launch": per_launch_ms}
 
     extra = {}
@@ -353,7 +377,9 @@ def run_ours(args):
     if rank == 0:
         line = {"metric": METRIC, "value": steps_s, "unit": "steps/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, f32 activations", "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "dtype_note": "bf16 / Q8_0 weights on bf16/f16 tensor cores with split (hi + lo) activations, "
+                              "f32 accumulate", "data": "synthetic",
                 "config": {"workload": "flashmap4b_step: append 17 rows at 1024 + 16-slot draft at 1041 (L=1042), "
                                        "Q8_0 vocab 151936", "global_batch": 16 * ws, "seq_len": 1042,
                            "parallelism": "replicas" if ws > 1 else "single", "l2": "inputs > L2 (1.35 GB/step)"},

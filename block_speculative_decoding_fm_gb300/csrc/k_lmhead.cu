@@ -192,25 +192,38 @@ __device__ __forceinline__ int my_tile_count(int n_tiles) {
 // 2..9 convert (one thread per table row and 32-column block), warps 10..17
 // apply the block scales and keep the running best (one thread per table row
 // and group of 8 slots).
-// TMEM columns: A slots [32 i, 32 i + 32) for i < kNA; D slots 128 + 64 j + 32 blk
-// for j < kND (per 32-column block of the chunk: 32 columns, per group of 8
-// slots 8 hi then 8 lo).
+// Work moves in pairs of chunks ("super-chunks"): every wait and commit covers
+// two chunks, since a single-thread mbarrier wait or tcgen05.commit costs about
+// as much as one of the small MMAs.
+// TMEM columns: A slots [64 i, 64 i + 64) for i < kNA (chunk h of the pair at
+// +32 h); D slots 128 + 128 j + 64 h + 32 blk for j < kND (per 32-column block
+// of chunk h: 32 columns, per group of 8 slots 8 hi then 8 lo).
+// Y operand: kStreamY (Y pre-split in global memory): each ring stage carries
+// the Y chunks its table chunks need, so the ring can be deep; otherwise Y is
+// split here and stays resident, and the ring gets what shared memory is left.
 constexpr int kQ8Conv = 8, kQ8Epi = 8;   // warps
 constexpr int kQ8Threads = kBase + 32 * (kQ8Conv + kQ8Epi);
 
+// bytes of one ring stage: (streamed Y chunks, then) U table chunks, 1024-aligned
+__host__ __device__ constexpr int q8_stage_bytes(bool stream_y, int U) {
+  return ((stream_y ? U * kYChunk : 0) + U * kQ8Chunk + 1023) / 1024 * 1024;
+}
+
+template <bool kStreamY>
 __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kQ8Chunk;
-  constexpr int kNA = 4, kND = 6;
+  constexpr int kNA = 2, kND = 3, kG = 2;
   constexpr uint32_t IDESC = umma_idesc(128, 32, false);
   const int H = a.H, kcs = H / kChunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ybuf = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t ring = ybuf + kcs * kYChunk;
+  const uint32_t ring = kStreamY ? ybuf : ybuf + kcs * kYChunk;
   // a ring stage holds U consecutive chunks of one tile, moved by one bulk copy: the
   // copy engine takes a roughly fixed time per copy, so fewer, larger copies stream faster
-  const int UB = U * SB;
-  const uint32_t bars = ring + S * UB;
+  const int SS = q8_stage_bytes(kStreamY, U);          // stage stride
+  const int TOFF = kStreamY ? U * kYChunk : 0;         // table offset inside a stage
+  const uint32_t bars = ring + S * SS;
   auto full = [&](int i) { return bars + 8 * i; };
   auto empty = [&](int i) { return bars + 8 * (S + i); };
   auto afull = [&](int i) { return bars + 8 * (2 * S + i); };
@@ -224,13 +237,16 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
   const int tiles = my_tile_count(n_tiles);
   const int total = tiles * kcs;
   const int units = total / U;
+  const int nsc = (total + kG - 1) / kG;   // super-chunks (the last may hold one chunk)
   const size_t tile_stride = (size_t)gridDim.x * kcs * SB;   // bytes between this CTA's tiles
   const uint8_t *first = a.q8 + (size_t)blockIdx.x * kcs * SB;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full(i), 1);
-      mbar_init(empty(i), kQ8Conv);
+      // the stage is free once the converters and the epilogue (block scales) are done
+      // with it, and, for streamed Y, the MMAs that read its Y
+      mbar_init(empty(i), kQ8Conv + kQ8Epi + (kStreamY ? 1 : 0));
     }
     for (int i = 0; i < kNA; ++i) {
       mbar_init(afull(i), kQ8Conv);
@@ -246,8 +262,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
     const uint8_t *src = first;
     int kc = 0;
     for (int j = 0; j < S && j < units; ++j) {
-      mbar_expect_tx(full(j), UB);
-      bulk_g2s(ring + j * UB, src + (size_t)kc * SB, UB, full(j));
+      // streamed Y: one expect for the stage's table and Y bytes; Y is copied after griddepcontrol.wait
+      mbar_expect_tx(full(j), U * SB + (kStreamY ? U * kYChunk : 0));
+      bulk_g2s(ring + j * SS + TOFF, src + (size_t)kc * SB, U * SB, full(j));
       kc += U;
       if (kc == kcs) { kc = 0; src += tile_stride; }
     }
@@ -261,7 +278,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
   pdl_wait();
   const int T = a.T_const > 0 ? a.T_const : a.sp->T;
 
-  if (!a.ylm && warp >= 2) {
+  if (!kStreamY && warp >= 2) {
     stage_y<true>(a, ybuf, T, (int)threadIdx.x - kBase, kQ8Threads - kBase);
     fence_proxy_async();
     named_sync(1, kQ8Threads - kBase);
@@ -279,8 +296,17 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
 
   if (warp == 0) {
     if (lane == 0) {
-      if (a.ylm) load_ylm(a, ybuf, yfull);
-      // unit j reuses stage j % S once the converters released unit j - S
+      if (kStreamY) {
+        // the Y chunks of the first stages (Y is this call's data: after griddepcontrol.wait)
+        int kc = 0;
+        for (int j = 0; j < S && j < units; ++j) {
+          bulk_g2s(ring + j * SS, a.ylm + (size_t)kc * kYChunk, U * kYChunk, full(j));
+          kc += U;
+          if (kc == kcs) kc = 0;
+        }
+        mbar_arrive(yfull);
+      }
+      // unit j reuses stage j % S once unit j - S is released
       const uint8_t *src = first;
       int kc = 0;
       for (int j = 0; j < S && j < units; ++j) {
@@ -291,8 +317,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
       uint32_t par = 0;
       for (int j = S; j < units; ++j) {
         if (!mbar_wait_bounded(empty(st), par, a.err)) break;
-        mbar_expect_tx(full(st), UB);
-        bulk_g2s(ring + st * UB, src + (size_t)kc * SB, UB, full(st));
+        mbar_expect_tx(full(st), U * SB + (kStreamY ? U * kYChunk : 0));
+        bulk_g2s(ring + st * SS + TOFF, src + (size_t)kc * SB, U * SB, full(st));
+        if (kStreamY) bulk_g2s(ring + st * SS, a.ylm + (size_t)kc * kYChunk, U * kYChunk, full(st));
         kc += U;
         if (kc == kcs) { kc = 0; src += tile_stride; }
         if (++st == S) { st = 0; par ^= 1; }
@@ -300,24 +327,30 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
     }
   } else if (warp == 1) {
     if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
-      int i = 0, j = 0, kc = 0;
+      int i = 0, j = 0, kc = 0, st = 0, uo = 0;
       uint32_t apar = 0, dpar = 0;
-      for (int c = 0; c < total; ++c) {
+      for (int sc = 0; sc < nsc; ++sc) {
+        const int n = min(kG, total - kG * sc);
         if (!mbar_wait_bounded(afull(i), apar, a.err)) break;
-        if (c >= kND && !mbar_wait_bounded(dempty(j), dpar ^ 1, a.err)) break;
+        if (sc >= kND && !mbar_wait_bounded(dempty(j), dpar ^ 1, a.err)) break;
         tc_fence_after();
-        const uint64_t bd = umma_desc_sw128(ybuf + kc * kYChunk);
+        for (int h = 0; h < n; ++h) {
+          // (streamed Y: the converters' afull for this chunk implies its stage has landed)
+          const uint64_t bd = umma_desc_sw128(kStreamY ? ring + st * SS + uo * kYChunk : ybuf + kc * kYChunk);
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk)
+          for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            umma_ts(tmem + 128 + 64 * j + 32 * blk, tmem + 32 * i + 16 * blk + 8 * kk, bd + 2 * (2 * blk + kk), IDESC,
-                    kk);
+            for (int kk = 0; kk < 2; ++kk)
+              umma_ts(tmem + 128 + 128 * j + 64 * h + 32 * blk, tmem + 64 * i + 32 * h + 16 * blk + 8 * kk,
+                      bd + 2 * (2 * blk + kk), IDESC, kk);
+          if (kStreamY && uo == U - 1) umma_commit(empty(st));
+          if (++kc == kcs) kc = 0;
+          if (++uo == U) { uo = 0; if (++st == S) st = 0; }
+        }
         umma_commit(aempty(i));
         umma_commit(dfull(j));
         if (++i == kNA) { i = 0; apar ^= 1; }
         if (++j == kND) { j = 0; dpar ^= 1; }
-        if (++kc == kcs) kc = 0;
       }
     }
   } else if (warp < 2 + kQ8Conv) {
@@ -327,29 +360,34 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
     const uint32_t o0 = (uint32_t)r * 64 + (((2 * b) ^ x) << 4), o1 = (uint32_t)r * 64 + (((2 * b + 1) ^ x) << 4);
     int st = 0, uo = 0, i = 0;
     uint32_t fpar = 0, apar = 0;
-    for (int c = 0; c < total; ++c) {
-      if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) break;
-      if (c >= kNA && !mbar_wait_bounded(aempty(i), apar ^ 1, a.err)) break;
+    bool ok = true;
+    for (int sc = 0; sc < nsc && ok; ++sc) {
+      const int n = min(kG, total - kG * sc);
+      if (sc >= kNA && !mbar_wait_bounded(aempty(i), apar ^ 1, a.err)) break;
       tc_fence_after();
-      const uint32_t buf = ring + st * UB + uo * SB;
-      const uint4 v0 = lds128(buf + o0), v1 = lds128(buf + o1);
-      uint32_t w[16];
-      i8x4_to_f16x4(v0.x, w[0], w[1]);
-      i8x4_to_f16x4(v0.y, w[2], w[3]);
-      i8x4_to_f16x4(v0.z, w[4], w[5]);
-      i8x4_to_f16x4(v0.w, w[6], w[7]);
-      i8x4_to_f16x4(v1.x, w[8], w[9]);
-      i8x4_to_f16x4(v1.y, w[10], w[11]);
-      i8x4_to_f16x4(v1.z, w[12], w[13]);
-      i8x4_to_f16x4(v1.w, w[14], w[15]);
-      tmem_st16(lane_base + 32 * i + 16 * b, w);
+      for (int h = 0; h < n; ++h) {
+        if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) { ok = false; break; }
+        const uint32_t buf = ring + st * SS + TOFF + uo * SB;
+        const uint4 v0 = lds128(buf + o0), v1 = lds128(buf + o1);
+        uint32_t w[16];
+        i8x4_to_f16x4(v0.x, w[0], w[1]);
+        i8x4_to_f16x4(v0.y, w[2], w[3]);
+        i8x4_to_f16x4(v0.z, w[4], w[5]);
+        i8x4_to_f16x4(v0.w, w[6], w[7]);
+        i8x4_to_f16x4(v1.x, w[8], w[9]);
+        i8x4_to_f16x4(v1.y, w[10], w[11]);
+        i8x4_to_f16x4(v1.z, w[12], w[13]);
+        i8x4_to_f16x4(v1.w, w[14], w[15]);
+        tmem_st16(lane_base + 64 * i + 32 * h + 16 * b, w);
+        if (uo == U - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(st));
+        }
+        if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(afull(i));
-        if (uo == U - 1) mbar_arrive(empty(st));
-      }
-      if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
+      if (lane == 0) mbar_arrive(afull(i));
       if (++i == kNA) { i = 0; apar ^= 1; }
     }
   } else {
@@ -359,63 +397,62 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
     float acc[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) acc[t] = 0.f;
-    // the row's two f16 block scales of a chunk, read from the table (L2) kND chunks ahead
+    // the row's f16 block scales sit in the chunk's scale plane (two rows per 32-bit word)
     const uint32_t soff = (uint32_t)kTile * 64 + (uint32_t)(r & ~1) * 2;
-    auto scale_at = [&](const uint8_t *chunk) -> uint32_t {
-      const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(chunk + soff));
-      const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t *>(chunk + soff + 256));
-      return (r & 1) ? (w0 >> 16) | (w1 & 0xffff0000u) : (w0 & 0xffffu) | (w1 << 16);
-    };
-    // lookahead cursor: chunk c + kND
-    const uint8_t *la_tile = first;
-    int la_kc = 0, la_c = 0;
-    uint32_t sc[kND];
-#pragma unroll
-    for (int u = 0; u < kND; ++u) {
-      sc[u] = la_c < total ? scale_at(la_tile + (size_t)la_kc * SB) : 0u;
-      ++la_c;
-      if (++la_kc == kcs) { la_kc = 0; la_tile += tile_stride; }
-    }
-    int kc = 0, tile = blockIdx.x;
-    uint32_t dpar = 0;
+    const int sh = (r & 1) * 16;
+    int kc = 0, tile = blockIdx.x, st = 0, uo = 0;
+    uint32_t dpar = 0, fpar = 0;
     bool ok = true;
-    for (int base = 0; base < total && ok; base += kND) {
+    for (int base = 0; base < nsc && ok; base += kND) {
 #pragma unroll
       for (int u = 0; u < kND; ++u) {
-        const int c = base + u;
-        if (c >= total) break;
+        const int sc = base + u;
+        if (sc >= nsc) break;
+        const int n = min(kG, total - kG * sc);
         if (!mbar_wait_bounded(dfull(u), dpar, a.err)) { ok = false; break; }
         tc_fence_after();
-        uint32_t d0[16], d1[16];
-        tmem_ld16_async(lane_base + 128 + 64 * u + 16 * g, d0);        // block 0: group g hi, lo
-        tmem_ld16_async(lane_base + 128 + 64 * u + 32 + 16 * g, d1);   // block 1
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dempty(u));
-        const uint32_t scw = sc[u];
-        sc[u] = la_c < total ? scale_at(la_tile + (size_t)la_kc * SB) : 0u;
-        ++la_c;
-        if (++la_kc == kcs) { la_kc = 0; la_tile += tile_stride; }
-        const __half2 sh = *reinterpret_cast<const __half2 *>(&scw);
-        const float f0 = __low2float(sh), f1 = __high2float(sh);
+        // one chunk of the pair at a time (registers), one wait and one release for both
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-          acc[t] += f0 * (__uint_as_float(d0[t]) + __uint_as_float(d0[8 + t])) +
-                    f1 * (__uint_as_float(d1[t]) + __uint_as_float(d1[8 + t]));
-        if (++kc == kcs) {
-          kc = 0;
-          const int v = tile * kTile + r;
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const int slot = 8 * g + t;
-            if (v < a.V && slot < T) {
-              if (a.logits) a.logits[(size_t)slot * a.V + v] = acc[t];
-              if (better(acc[t], v, bv[t], bi[t])) { bv[t] = acc[t]; bi[t] = v; }
-            }
-            acc[t] = 0.f;
+        for (int h = 0; h < kG; ++h) {
+          if (h >= n) break;
+          uint32_t d0[16], d1[16];
+          tmem_ld16_async(lane_base + 128 + 128 * u + 64 * h + 16 * g, d0);        // block 0: group g hi, lo
+          tmem_ld16_async(lane_base + 128 + 128 * u + 64 * h + 32 + 16 * g, d1);   // block 1
+          // the row's block scales, from the stage that holds the chunk (released after use)
+          if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) ok = false;
+          const uint32_t sa = ring + st * SS + TOFF + uo * SB + soff;
+          const uint32_t w0 = lds32(sa), w1 = lds32(sa + 256);
+          tmem_ld_wait();
+          const float f0 = __half2float(__ushort_as_half((unsigned short)(w0 >> sh)));
+          const float f1 = __half2float(__ushort_as_half((unsigned short)(w1 >> sh)));
+          if (h == n - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty(u));
           }
-          tile += gridDim.x;
+          if (uo == U - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(st));
+          }
+          if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            acc[t] += f0 * (__uint_as_float(d0[t]) + __uint_as_float(d0[8 + t])) +
+                      f1 * (__uint_as_float(d1[t]) + __uint_as_float(d1[8 + t]));
+          if (++kc == kcs) {
+            kc = 0;
+            const int v = tile * kTile + r;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int slot = 8 * g + t;
+              if (v < a.V && slot < T) {
+                if (a.logits) a.logits[(size_t)slot * a.V + v] = acc[t];
+                if (better(acc[t], v, bv[t], bi[t])) { bv[t] = acc[t]; bi[t] = v; }
+              }
+              acc[t] = 0.f;
+            }
+            tile += gridDim.x;
+          }
         }
       }
       dpar ^= 1;
@@ -598,20 +635,35 @@ int lmhead_grid(const LmArgs &a, int n_sm) {
 
 cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) {
   const bool q8 = a.q8 != nullptr;
-  const size_t ybytes = (size_t)(a.H / kChunk) * kYChunk;
-  const size_t fixed = 1024 + ybytes + 8 * (2 * 4 + 2 * 6 + 2) + 16;
+  const int kcs = a.H / kChunk;
+  const size_t bars = 8 * (2 * 4 + 2 * 6 + 2) + 16;
   const size_t budget = 227 * 1024 - 2048;   // leaves room for the static shared arrays
-  // two chunks per bulk copy when a tile's chunk count is even and three such stages fit
-  int U = (a.H / kChunk) % 2 == 0 ? 2 : 1;
-  size_t sb = (size_t)U * (q8 ? kQ8Chunk : kBfStage);
-  if (U == 2 && fixed + 3 * (sb + 16) > budget) {
-    U = 1;
-    sb /= 2;
+  int U, S;
+  size_t smem;
+  const bool stream = q8 && a.ylm != nullptr;
+  if (stream) {
+    // four chunks (and their Y) per stage when the tile's chunk count allows
+    U = kcs % 4 == 0 ? 4 : kcs % 2 == 0 ? 2 : 1;
+    const size_t ss = (size_t)q8_stage_bytes(true, U);
+    S = (int)((budget - 1024 - bars) / (ss + 16));
+    if (S > 8) S = 8;
+    if (S < 2) return cudaErrorInvalidValue;
+    smem = 1024 + bars + (size_t)S * (ss + 16);
+  } else {
+    const size_t ybytes = (size_t)kcs * kYChunk;
+    const size_t fixed = 1024 + ybytes + bars;
+    // two chunks per bulk copy when a tile's chunk count is even and three such stages fit
+    U = kcs % 2 == 0 ? 2 : 1;
+    size_t sb = q8 ? (size_t)q8_stage_bytes(false, U) : (size_t)U * kBfStage;
+    if (U == 2 && fixed + 3 * (sb + 16) > budget) {
+      U = 1;
+      sb = q8 ? (size_t)q8_stage_bytes(false, 1) : (size_t)kBfStage;
+    }
+    if (fixed + 2 * (sb + 16) > budget) return cudaErrorInvalidValue;
+    S = (int)((budget - fixed) / (sb + 16));
+    if (S > 12) S = 12;
+    smem = fixed + (size_t)S * (sb + 16);
   }
-  if (fixed + 2 * (sb + 16) > budget) return cudaErrorInvalidValue;
-  int S = (int)((budget - fixed) / (sb + 16));
-  if (S > 12) S = 12;
-  const size_t smem = fixed + (size_t)S * (sb + 16);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(q8 ? kQ8Threads : kBase + kBfWorkers, 1, 1);
@@ -622,15 +674,13 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e;
-  if (q8) {
-    e = cudaFuncSetAttribute(lmhead_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto go = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, lmhead_q8_kernel, a, S, U);
-  }
-  e = cudaFuncSetAttribute(lmhead_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, lmhead_bf16_kernel, a, S, U);
+    return cudaLaunchKernelEx(&cfg, kern, a, S, U);
+  };
+  if (q8) return stream ? go(lmhead_q8_kernel<true>) : go(lmhead_q8_kernel<false>);
+  return go(lmhead_bf16_kernel);
 }
 
 }  // namespace fm
