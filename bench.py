@@ -65,14 +65,18 @@ def ncu_traffic(tag):
     """DRAM bytes (read + write) per launch of the kernel behind `tag`, from the
     committed ncu summary profiles/ncu_dram_traffic.txt, or None when there is
     no capture or the kernel's source has changed since it was taken (each
-    line records the digest of the source file the capture ran)."""
+    line records the digest of the kernel's source file and the two headers
+    it includes, as built for the capture)."""
     import hashlib
     src = KERNEL_SOURCES.get(tag.split(".")[0])
     path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
     if src is None or not os.path.exists(path):
         return None
-    with open(os.path.join(ROOT, "block_speculative_decoding_fm_gb300", "csrc", src), "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in (src, "dev_common.cuh", "fm_internal.h"):   # the kernel and the headers it is built from
+        with open(os.path.join(ROOT, "block_speculative_decoding_fm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()[:16]
     with open(path) as f:
         for line in f:
             parts = line.split()
