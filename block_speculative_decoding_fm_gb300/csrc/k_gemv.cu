@@ -175,14 +175,38 @@ __device__ __forceinline__ int row_pos(const GemvArgs &a, int t) {
 }
 
 // Epilogue for one (token t, 128-row tile): lane holds rows 4 * lane .. + 3.
-__device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], int tile) {
+// The global operands of an epilogue unit (bias, residual row, gate), loaded
+// ahead of time so their L2 latency overlaps the cluster barrier.
+struct EpiIn {
+  float4 r, g;
+  float b[4];
+};
+__device__ __forceinline__ void epilogue_load(const GemvArgs &a, int t, int m0, EpiIn &in) {
+  const int mrow = m0 + 4 * (threadIdx.x & 31);
+  const bool live = mrow < a.M;
+  in.r = make_float4(0.f, 0.f, 0.f, 0.f);
+  in.g = make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) in.b[e] = 0.f;
+  if (!live) return;
+  if (a.bias) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(a.bias + mrow);
+    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+    in.b[0] = __low2float(p0); in.b[1] = __high2float(p0); in.b[2] = __low2float(p1); in.b[3] = __high2float(p1);
+  }
+  if (a.emode == E_RESID) {
+    in.r = __ldcg(reinterpret_cast<const float4 *>(a.R + (size_t)t * a.ldr + mrow));
+    if (a.gate) in.g = *reinterpret_cast<const float4 *>(a.gate + mrow);
+  }
+}
+
+__device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], int tile, const EpiIn &in) {
   const int lane = threadIdx.x & 31;
   const int mrow = m0 + 4 * lane;
   const bool live = mrow < a.M;  // M is a multiple of 4
-  if (a.bias && live) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) v[e] += __bfloat162float(a.bias[mrow + e]);
-  }
+  for (int e = 0; e < 4; ++e) v[e] += in.b[e];
   switch (a.emode) {
     case E_STORE:
     case E_GELU:
@@ -191,16 +215,10 @@ __device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], i
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = gelu_erf(v[e]);
       } else if (a.emode == E_RESID && live) {
-        const float4 r = __ldcg(reinterpret_cast<const float4 *>(a.R + (size_t)t * a.ldr + mrow));
-        float gt[4] = {1.f, 1.f, 1.f, 1.f};
-        if (a.gate) {
-          const float4 gg = *reinterpret_cast<const float4 *>(a.gate + mrow);
-          gt[0] = gg.x; gt[1] = gg.y; gt[2] = gg.z; gt[3] = gg.w;
-        }
-        v[0] = r.x + gt[0] * v[0];
-        v[1] = r.y + gt[1] * v[1];
-        v[2] = r.z + gt[2] * v[2];
-        v[3] = r.w + gt[3] * v[3];
+        v[0] = in.r.x + in.g.x * v[0];
+        v[1] = in.r.y + in.g.y * v[1];
+        v[2] = in.r.z + in.g.z * v[2];
+        v[3] = in.r.w + in.g.w * v[3];
       }
       if (live)
         __stcg(reinterpret_cast<float4 *>(a.Y + (size_t)t * a.ldy + mrow), make_float4(v[0], v[1], v[2], v[3]));
@@ -491,12 +509,20 @@ __global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __gri
   cg::cluster_group cluster = cg::this_cluster();
   const int ks = a.ksplit;
   const int rank = ks > 1 ? (int)cluster.block_rank() : 0;
-  if (ks > 1) cluster.sync();
+  // the partial tiles are published; the first unit's epilogue operands load meanwhile
+  if (ks > 1) cluster_arrive_release();
+  const int ew = warp - 2;
+  const int t0 = rank + ks * ew;             // this warp's first (token, tile) unit
+  constexpr int kMaxUnits = kMaxT / (kWorkers / 32);
+  EpiIn pre;
+  if (warp >= 2 && t0 < T) epilogue_load(a, t0, m0, pre);
+  if (ks > 1) cluster_wait_acquire();
 
+  // sum the partial tiles of this warp's units in rank order (deterministic)
+  float vs[kMaxUnits][4];
+  int nu = 0;
   if (warp >= 2) {
-    const int ew = warp - 2;
-    for (int t = rank + ks * ew; t < T; t += ks * (kWorkers / 32)) {
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int t = t0; t < T; t += ks * (kWorkers / 32), ++nu) {
       float4 part[8];
 #pragma unroll
       for (int r = 0; r < 8; ++r) {  // all partial rows requested before any is summed (ks <= 8)
@@ -506,14 +532,30 @@ __global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __gri
           part[r] = *reinterpret_cast<const float4 *>(src + t * kCsStride + 4 * lane);
         }
       }
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         v[0] += part[r].x; v[1] += part[r].y; v[2] += part[r].z; v[3] += part[r].w;
       }
-      epilogue_unit(a, t, m0, v, tile);
+#pragma unroll
+      for (int u = 0; u < kMaxUnits; ++u)
+        if (u == nu) { vs[u][0] = v[0]; vs[u][1] = v[1]; vs[u][2] = v[2]; vs[u][3] = v[3]; }
     }
   }
-  if (ks > 1) cluster.sync();
+  // done reading the peers' tiles: they may leave once everyone has arrived
+  if (ks > 1) cluster_arrive_release();
+  if (warp >= 2) {
+#pragma unroll
+    for (int u = 0; u < kMaxUnits; ++u) {
+      if (u >= nu) break;
+      const int t = t0 + u * ks * (kWorkers / 32);
+      EpiIn in;
+      if (u == 0) in = pre;
+      else epilogue_load(a, t, m0, in);
+      float v[4] = {vs[u][0], vs[u][1], vs[u][2], vs[u][3]};
+      epilogue_unit(a, t, m0, v, tile, in);
+    }
+  }
 
   // self-attention tail: the last CTA to finish a head's q, k and v computes it
   if (a.self_D > 0) {
@@ -540,6 +582,8 @@ __global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __gri
       }
     }
   }
+  // no CTA leaves (or reuses its tile buffer) before every peer has read it
+  if (ks > 1) cluster_wait_acquire();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
