@@ -10,8 +10,9 @@ flush is needed between steps.
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle (the only
 reference implementation of this path) on the same workload.
-``--workload`` selects another timed unit: prefill (32768-row context
-injection), dflash (draft/accept cycles), tiny.
+``--workload`` selects another configuration's timed unit: prefill (32768-row
+context injection, then a draft over 32769 keys), dflash (draft / append
+cycles), batched (32 sequences), tiny.
 """
 from __future__ import annotations
 
@@ -38,7 +39,7 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="flashmap4b", choices=["flashmap4b", "prefill", "dflash", "tiny"])
+    p.add_argument("--workload", default="flashmap4b", choices=["flashmap4b", "prefill", "dflash", "tiny", "batched"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill rows/s figure")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
@@ -232,6 +233,189 @@ class PrefillStep:
         self.launches += self.fm.fm_last_launch_count(self.h)
 
 
+class TinyStep:
+    """Config 1: the tiny drafter, 64 context rows; one timed unit = draft at 64 + device acceptance."""
+    name = "tiny_step"
+
+    def __init__(self, torch):
+        import block_speculative_decoding_fm_gb300 as fm
+        import fm_synth as S
+        self.fm, self.torch = fm, torch
+        self.cfg = S.tiny_config(max_ctx=128)
+        w = S.gen_weights(self.cfg, 1001)
+        self.h = fm.fm_create(self.cfg, fm.weight_items(w), S.gen_modulation(self.cfg, 1001))
+        fm.fm_context_append(self.h, 0, torch.from_numpy(S.gen_features(S.streams(1001)["features"], 64,
+                                                                       self.cfg.feat_dim)).cuda(), 64, 0)
+        self.anchor = S.gen_anchor(S.streams(1001)["tokens"], self.cfg.vocab)
+        self.tokens = torch.zeros((1, 16), dtype=torch.int32, device="cuda")
+        self.target = torch.zeros((1, 17), dtype=torch.int32, device="cuda")
+        self.k = torch.full((1,), 16, dtype=torch.int32, device="cuda")
+        self.acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.bonus = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.launches = 0
+
+    def step(self):
+        fm = self.fm
+        fm.fm_draft(self.h, [0], [self.anchor], [64], self.tokens)
+        self.launches += fm.fm_last_launch_count(self.h)
+        fm.fm_accept_batched(self.h, self.tokens, self.target, self.k, self.acc, self.bonus)
+        self.launches += 1
+
+
+class DFlashCycles:
+    """Config 4: the DFlash drafter, 4096 context rows, then draft -> accept -> append acc + 1 rows at the
+    anchor position, with seeded acceptance counts in [0, 5]; one timed unit = one cycle."""
+    name = "dflash_cycle"
+
+    def __init__(self, torch, cycles):
+        import block_speculative_decoding_fm_gb300 as fm
+        import fm_synth as S
+        self.fm, self.torch = fm, torch
+        self.cfg = S.dflash_config(max_ctx=4096 + 6 * cycles + 64)
+        c = self.cfg
+        w = S.gen_weights(self.cfg, 1004)
+        self.h = fm.fm_create(self.cfg, fm.weight_items(w), S.gen_modulation(self.cfg, 1004))
+        g = torch.Generator(device="cuda")
+        g.manual_seed(1004)
+        ctx = torch.randn((4096, c.feat_dim), generator=g, device="cuda")
+        fm.fm_context_append(self.h, 0, ctx, 4096, 0)
+        del ctx
+        self.pool = torch.randn((6 * cycles + 6, c.feat_dim), generator=g, device="cuda")
+        rng = np.random.default_rng(1004)
+        self.acc = rng.integers(0, c.block + 1, size=cycles + 8)
+        self.anchors = rng.integers(0, c.vocab, size=cycles + 8)
+        self.tokens = torch.zeros((1, c.block), dtype=torch.int32, device="cuda")
+        self.pos, self.i, self.used, self.launches = 4096, 0, 0, 0
+        table = c.vocab * c.target_dim * 2
+        others = sum(t.data.nbytes for n, t in w.items()) - table
+        self.bytes_fixed = table + others
+
+    def bytes_at(self, pos):
+        c = self.cfg
+        return self.bytes_fixed + c.n_layers * 2 * pos * c.dim * 2
+
+    def step(self):
+        fm = self.fm
+        fm.fm_draft(self.h, [0], [int(self.anchors[self.i])], [self.pos], self.tokens)
+        self.launches += fm.fm_last_launch_count(self.h)
+        n = int(self.acc[self.i]) + 1
+        fm.fm_context_append(self.h, 0, self.pool[self.used:self.used + n], n, self.pos)
+        self.launches += fm.fm_last_launch_count(self.h)
+        self.pos += n
+        self.used += n
+        self.i += 1
+
+
+class BatchedStep:
+    """Config 5: 32 sequences, contexts U[512, 8192] (prefilled untimed), each appends acc_i + 1 rows
+    (acc_i ~ U{0..16}) then all 32 draft 16 slots; every step re-appends at the same positions."""
+    name = "batched_32_step"
+
+    def __init__(self, torch, n_seqs=32):
+        import block_speculative_decoding_fm_gb300 as fm
+        import fm_synth as S
+        self.fm, self.torch = fm, torch
+        self.cfg = S.flashmap_4b_config(max_ctx=8192 + 17 + 64, max_seqs=n_seqs)
+        c = self.cfg
+        w = S.gen_weights(self.cfg, 1005)
+        self.h = fm.fm_create(self.cfg, fm.weight_items(w), S.gen_modulation(self.cfg, 1005))
+        rng = S.streams(1005)["workload"]
+        self.L = [int(x) for x in S.batched_lengths(rng, n_seqs)]
+        self.n = [int(x) + 1 for x in rng.integers(0, 17, size=n_seqs)]
+        self.anchors = [int(x) for x in rng.integers(0, c.vocab, size=n_seqs)]
+        g = torch.Generator(device="cuda")
+        g.manual_seed(1005)
+        for i, L in enumerate(self.L):
+            f = torch.randn((L, c.feat_dim), generator=g, device="cuda")
+            fm.fm_context_append(self.h, i, f, L, 0)
+            del f
+        self.feats = torch.randn((sum(self.n), c.feat_dim), generator=g, device="cuda")
+        self.ids = list(range(n_seqs))
+        self.pos = [L + n for L, n in zip(self.L, self.n)]
+        self.tokens = torch.zeros((n_seqs, 16), dtype=torch.int32, device="cuda")
+        self.launches = 0
+        D, F, Ht, Ll = c.dim, c.ff_dim, c.target_dim, c.n_layers
+        weights = (D * c.feat_dim + D * Ht * 2 + Ll * (4 * D * D + 4 * D * D + 2 * F * D) + Ht * D) * 2
+        table = c.vocab * (Ht + Ht // 16)
+        kv = sum((p + 1) * Ll * 2 * D * 2 for p in self.pos)
+        self.bytes_per_step = weights + table + kv + sum(self.n) * c.feat_dim * 4
+
+    def step(self):
+        fm = self.fm
+        fm.fm_context_append_batched(self.h, self.ids, self.feats, self.n, self.L)
+        self.launches += fm.fm_last_launch_count(self.h)
+        fm.fm_draft(self.h, self.ids, self.anchors, self.pos, self.tokens)
+        self.launches += fm.fm_last_launch_count(self.h)
+
+
+def run_workload(args):
+    """The other configs' timed units (one JSON line each, same keys as the default line)."""
+    import torch
+    torch.cuda.set_device(0)
+    from block_speculative_decoding_fm_gb300 import build
+    build.build()
+    import block_speculative_decoding_fm_gb300 as fm
+    hbm, bf16, _, peak_src = peaks()
+    extra, unit, value, ms, launches = {}, "steps/s", None, None, 0
+    with Clocks(0) as clk:
+        if args.workload == "tiny":
+            w = TinyStep(torch)
+            for _ in range(max(3, args.warmup)):
+                w.step()
+            w.launches = 0
+            ms = time_steps(torch, w.step, args.steps)
+            value, launches = args.steps / (ms / 1000), w.launches
+            cfgd = {"workload": "tiny: D 256, 2 layers, 64 context rows, draft at 64 + device acceptance"}
+        elif args.workload == "dflash":
+            w = DFlashCycles(torch, args.steps + args.warmup + 3)
+            for _ in range(max(3, args.warmup)):
+                w.step()
+            w.launches = 0
+            p0 = w.pos
+            ms = time_steps(torch, w.step, args.steps)
+            value, unit, launches = args.steps / (ms / 1000), "cycles/s", w.launches
+            gb = (w.bytes_at(p0) + w.bytes_at(w.pos)) / 2 * args.steps / 1e9
+            extra["achieved_hbm_gbs"] = gb / (ms / 1000)
+            extra["bytes_per_cycle"] = (w.bytes_at(p0) + w.bytes_at(w.pos)) / 2
+            cfgd = {"workload": f"dflash: D 1024, 5 layers, gamma 5, bf16 vocab 262144, context {p0}..{w.pos} "
+                                "(draft -> append acc+1 rows, acc seeded in [0,5])"}
+        elif args.workload == "batched":
+            w = BatchedStep(torch)
+            for _ in range(max(3, args.warmup)):
+                w.step()
+            w.launches = 0
+            ms = time_steps(torch, w.step, args.steps)
+            value, launches = args.steps / (ms / 1000), w.launches
+            extra["tokens_drafted_per_s"] = value * 32 * 16
+            extra["achieved_hbm_gbs"] = w.bytes_per_step * value / 1e9
+            extra["bytes_per_step"] = w.bytes_per_step
+            cfgd = {"workload": "batched: 32 FlashMap-4B sequences, contexts U[512,8192], append acc_i+1 rows "
+                                "(acc_i in 0..16) + 32 x 16-slot draft", "global_batch": 512}
+        else:   # prefill
+            w = PrefillStep(torch)
+            w.step()
+            torch.cuda.synchronize()
+            w.launches = 0
+            ms = time_steps(torch, w.step, max(2, args.steps // 50))
+            n = max(2, args.steps // 50)
+            value, unit, launches = w.rows * n / (ms / 1000), "rows/s", w.launches
+            extra["prefill_tflops"] = w.flops * n / (ms / 1000) / 1e12
+            extra["tensor_frac_of_measured_bf16"] = extra["prefill_tflops"] / bf16
+            # then the 16-slot draft over the 32768-row context (L = 32769)
+            tok = torch.zeros((1, 16), dtype=torch.int32, device="cuda")
+            fm.fm_draft(w.h, [0], [123], [w.rows], tok)
+            dms = time_steps(torch, lambda: fm.fm_draft(w.h, [0], [123], [w.rows], tok), 10) / 10
+            extra["draft_after_prefill_ms"] = dms
+            ms = ms * args.steps / n   # reported per the requested steps below
+            cfgd = {"workload": "prefill: fm_context_append of 32768 rows x 12800 (FlashMap-4B), then a draft at "
+                                "L=32769"}
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfgd, "gpu_launches": launches,
+            "clocks": clk.summary(), "cpu_baseline": None, **extra}
+    print(json.dumps(line), flush=True)
+
+
 def time_steps(torch, fn, k):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -399,6 +583,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "flashmap4b":
+        run_workload(args)
     else:
         run_ours(args)
 

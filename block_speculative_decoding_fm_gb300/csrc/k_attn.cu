@@ -74,17 +74,21 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   per = (per + 15) & ~15;
   const int kbeg = min(L, split * per), kend = min(L, kbeg + per);
   const int nst = (kend - kbeg + kKeys - 1) / kKeys;
-  // rows below `stable` are not written by this call's kernels: fetch them now
-  const int pre = nst > 0 ? max(0, min(kKeys, a.sp->stable - kbeg)) : 0;
-  if (pre > 0) issue_kv<HD>(a, head, kb0, vb0, kbeg, kend, 0, pre);
-  cp_async_commit();
+  // rows below `stable` are not written by this call's kernels: the first NS - 1
+  // stages' stable rows are requested before griddepcontrol.wait, the rest after it
+  const int stable = a.sp->stable;
+  int pre[NS];
+#pragma unroll
+  for (int st = 0; st < NS - 1; ++st) {
+    pre[st] = st < nst ? max(0, min(kKeys, stable - (kbeg + st * kKeys))) : 0;
+    if (pre[st] > 0) issue_kv<HD>(a, head, kbuf(st), vbuf(st), kbeg + st * kKeys, kend, 0, pre[st]);
+  }
   pdl_wait();
   const int T = a.T_const > 0 ? a.T_const : a.sp->T;
-  if (nst > 0 && pre < kKeys) issue_kv<HD>(a, head, kb0, vb0, kbeg, kend, pre, kKeys);
-  cp_async_commit();
-  for (int st = 1; st < NS - 1; ++st) {
-    if (st < nst) issue_kv<HD>(a, head, kbuf(st), vbuf(st), kbeg + st * kKeys, kend);
-    cp_async_commit();
+#pragma unroll
+  for (int st = 0; st < NS - 1; ++st) {
+    if (st < nst && pre[st] < kKeys) issue_kv<HD>(a, head, kbuf(st), vbuf(st), kbeg + st * kKeys, kend, pre[st], kKeys);
+    cp_async_commit();   // one group per stage, as the main loop expects
   }
 
   // queries -> f16 hi / lo (rows >= T are zero)
@@ -313,6 +317,10 @@ cudaError_t launch_attn(const AttnArgs &a, int L_now, cudaStream_t st, bool pdl)
   auto go = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    if (a.splits > 8) {   // clusters of up to 16 CTAs are an opt-in on this GPU
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     return cudaLaunchKernelEx(&cfg, kern, a);
   };
   if (HD == 128) return NS == 4 ? go(attn_kernel<128, 4>) : go(attn_kernel<128, 2>);
