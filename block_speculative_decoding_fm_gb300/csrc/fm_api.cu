@@ -91,8 +91,24 @@ struct fm_handle {
   int32_t *dev_err = nullptr;     // raised by a device-side bounded wait that gave up
   std::vector<void *> to_free;    // row-major staging copies released at the end of fm_create
 
-  // ---- deferred K/V projection of the last short append ----
-  int pend_seq = -1, pend_start = 0, pend_n = 0;
+  // ---- per-sequence lanes ----
+  // Each sequence has its own work buffers (and, with several sequences, its own
+  // stream), so the chains of different sequences can run at the same time; the
+  // fields X .. tickets above point at the lane whose chain is being built.
+  struct Lane {
+    float *X = nullptr, *qkv = nullptr, *qc = nullptr, *attn = nullptr, *u = nullptr, *Y = nullptr;
+    float *ctx = nullptr, *actx = nullptr;
+    uint8_t *ylm = nullptr;
+    float2 *st_x = nullptr, *st_c = nullptr, *st_a = nullptr, *st_u = nullptr, *lm_part = nullptr;
+    int32_t *tickets = nullptr;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t done = nullptr;
+    // a short append whose K/V projection waits for this sequence's next draft
+    bool pending = false;
+    int pend_start = 0, pend_n = 0;
+  };
+  std::vector<Lane> lanes;
+  cudaEvent_t fork_ev = nullptr;
 
   // ---- captured chains ----
   struct GraphEntry {
@@ -125,6 +141,15 @@ struct fm_handle {
 namespace {
 
 thread_local std::string g_create_error;  // reason of the last failed fm_create on this thread
+
+// point the handle's work-buffer fields at sequence seq's lane
+void use_lane(fm_handle *h, int seq) {
+  const fm_handle::Lane &L = h->lanes[seq];
+  h->X = L.X; h->qkv = L.qkv; h->qc = L.qc; h->attn = L.attn; h->u = L.u; h->Y = L.Y;
+  h->ctx = L.ctx; h->actx = L.actx; h->ylm = L.ylm;
+  h->st_x = L.st_x; h->st_c = L.st_c; h->st_a = L.st_a; h->st_u = L.st_u; h->lm_part = L.lm_part;
+  h->tickets = L.tickets;
+}
 
 fm_status fail(fm_handle *h, fm_status s, const char *fmt, ...) {
   if (h) {
@@ -890,13 +915,15 @@ uint64_t chain_key(int kind, int seq, int T, int splits, int debug) {
 
 // Project the K/V rows of a deferred append (when no draft of that sequence
 // follows it directly).
-fm_status flush_pending(fm_handle *h, cudaStream_t s) {
-  if (h->pend_seq < 0) return FM_OK;
-  const int seq = h->pend_seq, n = h->pend_n;
+fm_status flush_pending(fm_handle *h, int seq, cudaStream_t s) {
+  fm_handle::Lane &L = h->lanes[seq];
+  if (!L.pending) return FM_OK;
+  use_lane(h, seq);
+  const int n = L.pend_n;
   StepParams p{};
   p.T = n;
-  p.start = h->pend_start;
-  h->pend_seq = -1;
+  p.start = L.pend_start;
+  L.pending = false;
   return run_chain(h, chain_key(4, seq, n, 0, 0), p, s, [&](const StepParams *sp, cudaStream_t st) {
     return run_gemv(h, flashmap_kv_args(h, seq, sp, 0, 0), st, "gemv.kv_append", n);
   });
@@ -904,18 +931,19 @@ fm_status flush_pending(fm_handle *h, cudaStream_t s) {
 
 fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s) {
   const fm_config &c = h->cfg;
+  fm_handle::Lane &lane = h->lanes[seq];
   int n_pend = 0;
-  if (h->pend_seq >= 0) {
-    if (h->pend_seq == seq && h->pend_start + h->pend_n == pos && c.variant == FM_VARIANT_FLASHMAP &&
-        h->pend_n + 1 <= kMaxT) {
-      n_pend = h->pend_n;
+  if (lane.pending) {
+    if (lane.pend_start + lane.pend_n == pos && c.variant == FM_VARIANT_FLASHMAP && lane.pend_n + 1 <= kMaxT) {
+      n_pend = lane.pend_n;
     } else {
-      TRY(flush_pending(h, s));
+      TRY(flush_pending(h, seq, s));
     }
   }
+  use_lane(h, seq);
   StepParams p{};
-  p.start = n_pend ? h->pend_start : 0;
-  if (n_pend) h->pend_seq = -1;
+  p.start = n_pend ? lane.pend_start : 0;
+  if (n_pend) lane.pending = false;
   // cache rows no kernel of this draft writes: below the pending rows / the anchor / the block
   p.stable = n_pend ? p.start : pos;
   p.T = c.block;
@@ -971,33 +999,46 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   TRY(dalloc(h, &h->rope, (size_t)h->rope_pos * c.head_dim / 2));
   CK(launch_rope_table(h->rope, h->rope_pos, c.head_dim, c.rope_theta, s));
   const int wmax = 3 * D > F ? (3 * D > Ht ? 3 * D : Ht) : (F > Ht ? F : Ht);
-  TRY(dalloc(h, &h->X, (size_t)kMaxT * D));
-  TRY(dalloc(h, &h->qkv, (size_t)kMaxT * 3 * D));
-  TRY(dalloc(h, &h->qc, (size_t)kMaxT * D));
-  TRY(dalloc(h, &h->attn, (size_t)kMaxT * D));
-  TRY(dalloc(h, &h->u, (size_t)kMaxT * (F > wmax ? F : wmax)));
-  TRY(dalloc(h, &h->Y, (size_t)kMaxT * Ht));
-  // the head's output also split into the lm_head operand; rows of unused slots stay zero
-  TRY(dalloc(h, &h->ylm, (size_t)(Ht / 64) * kLmYChunk));
-  CK(cudaMemsetAsync(h->ylm, 0, (size_t)(Ht / 64) * kLmYChunk, s));
-  TRY(dalloc(h, &h->ctx, (size_t)kMaxT * D));
-  TRY(dalloc(h, &h->actx, (size_t)kMaxT * D));
-  TRY(dalloc(h, &h->hid, (size_t)c.n_layers * kMaxT * D));
-  CK(cudaMemsetAsync(h->X, 0, (size_t)kMaxT * D * 4, s));
-  CK(cudaMemsetAsync(h->hid, 0, (size_t)c.n_layers * kMaxT * D * 4, s));
   const int tiles_max = (wmax + kTile - 1) / kTile + 64;
-  float2 **sts[] = {&h->st_x, &h->st_h0, &h->st_c, &h->st_a, &h->st_u, &h->st_init};
+  h->lanes.resize(c.max_seqs);
+  for (int i = 0; i < c.max_seqs; ++i) {
+    fm_handle::Lane &L = h->lanes[i];
+    TRY(dalloc(h, &L.X, (size_t)kMaxT * D));
+    TRY(dalloc(h, &L.qkv, (size_t)kMaxT * 3 * D));
+    TRY(dalloc(h, &L.qc, (size_t)kMaxT * D));
+    TRY(dalloc(h, &L.attn, (size_t)kMaxT * D));
+    TRY(dalloc(h, &L.u, (size_t)kMaxT * (F > wmax ? F : wmax)));
+    TRY(dalloc(h, &L.Y, (size_t)kMaxT * Ht));
+    // the head's output also split into the lm_head operand; rows of unused slots stay zero
+    TRY(dalloc(h, &L.ylm, (size_t)(Ht / 64) * kLmYChunk));
+    CK(cudaMemsetAsync(L.ylm, 0, (size_t)(Ht / 64) * kLmYChunk, s));
+    TRY(dalloc(h, &L.ctx, (size_t)kMaxT * D));
+    TRY(dalloc(h, &L.actx, (size_t)kMaxT * D));
+    CK(cudaMemsetAsync(L.X, 0, (size_t)kMaxT * D * 4, s));
+    float2 **sts[] = {&L.st_x, &L.st_c, &L.st_a, &L.st_u};
+    for (float2 **p : sts) {
+      TRY(dalloc(h, p, (size_t)tiles_max * kMaxT));
+      CK(cudaMemsetAsync(*p, 0, (size_t)tiles_max * kMaxT * sizeof(float2), s));
+    }
+    TRY(dalloc(h, &L.lm_part, (size_t)h->n_sm * kMaxT));
+    TRY(dalloc(h, &L.tickets, (size_t)2 * c.n_heads + 8));
+    CK(cudaMemsetAsync(L.tickets, 0, ((size_t)2 * c.n_heads + 8) * 4, s));
+    if (c.max_seqs > 1) {
+      CK(cudaStreamCreateWithFlags(&L.stream, cudaStreamNonBlocking));
+      CK(cudaEventCreateWithFlags(&L.done, cudaEventDisableTiming));
+    }
+  }
+  if (c.max_seqs > 1) CK(cudaEventCreateWithFlags(&h->fork_ev, cudaEventDisableTiming));
+  use_lane(h, 0);
+  TRY(dalloc(h, &h->hid, (size_t)c.n_layers * kMaxT * D));
+  CK(cudaMemsetAsync(h->hid, 0, (size_t)c.n_layers * kMaxT * D * 4, s));
+  float2 **sts[] = {&h->st_h0, &h->st_init};
   for (float2 **p : sts) {
     TRY(dalloc(h, p, (size_t)tiles_max * kMaxT));
     CK(cudaMemsetAsync(*p, 0, (size_t)tiles_max * kMaxT * sizeof(float2), s));
   }
   h->max_splits = 2 * h->n_sm / c.n_heads;
   if (h->max_splits < 1) h->max_splits = 1;
-  TRY(dalloc(h, &h->part_o, (size_t)c.n_heads * h->max_splits * kMaxT * c.head_dim));
-  TRY(dalloc(h, &h->part_ml, (size_t)c.n_heads * h->max_splits * kMaxT));
-  TRY(dalloc(h, &h->lm_part, (size_t)h->n_sm * kMaxT));
-  TRY(dalloc(h, &h->tickets, (size_t)2 * c.n_heads + 8));
-  CK(cudaMemsetAsync(h->tickets, 0, ((size_t)2 * c.n_heads + 8) * 4, s));
   TRY(dalloc(h, &h->tok_tmp, (size_t)kMaxT));
   TRY(dalloc(h, &h->dev_err, 4));
   CK(cudaMemsetAsync(h->dev_err, 0, 4, s));
@@ -1261,7 +1302,8 @@ fm_status append_checks(fm_handle *h, int32_t seq, const float *feats, int32_t n
 
 fm_status append_one(fm_handle *h, int32_t seq, const float *feats, int32_t n, int32_t start, cudaStream_t s) {
   const int FW = h->cfg.n_taps * h->cfg.target_dim;
-  TRY(flush_pending(h, s));
+  TRY(flush_pending(h, seq, s));
+  use_lane(h, seq);
   if (h->cfg.variant == FM_VARIANT_FLASHMAP && n > 0 && n < kMaxT && h->use_defer) {
     // fc now; the K/V projection joins the next draft of this sequence
     StepParams p{};
@@ -1271,9 +1313,10 @@ fm_status append_one(fm_handle *h, int32_t seq, const float *feats, int32_t n, i
     TRY(run_chain(h, chain_key(3, seq, n, 0, 0), p, s, [&](const StepParams *sp, cudaStream_t st) {
       return flashmap_fc_rows(h, sp, n, st);
     }));
-    h->pend_seq = seq;
-    h->pend_start = start;
-    h->pend_n = n;
+    fm_handle::Lane &L = h->lanes[seq];
+    L.pending = true;
+    L.pend_start = start;
+    L.pend_n = n;
     h->length[seq] = start + n;
     return FM_OK;
   }
@@ -1299,6 +1342,34 @@ fm_status append_one(fm_handle *h, int32_t seq, const float *feats, int32_t n, i
 }
 
 }  // namespace
+
+// Run body(i, stream) for the n sequences ids[0..n): one sequence on the caller's
+// stream as is; several on their lanes' streams, forked from and joined back into
+// the caller's stream, so independent sequences' chains overlap on the GPU.
+template <typename F>
+fm_status run_lanes(fm_handle *h, int n, const int32_t *ids, cudaStream_t s, F body) {
+  if (n == 1 || h->lanes.size() < 2) {
+    for (int i = 0; i < n; ++i) TRY(body(i, s));
+    return FM_OK;
+  }
+  CK(cudaEventRecord(h->fork_ev, s));
+  fm_status st = FM_OK;
+  int started = 0;
+  for (int i = 0; i < n && st == FM_OK; ++i, ++started) {
+    fm_handle::Lane &L = h->lanes[ids[i]];
+    if (cudaStreamWaitEvent(L.stream, h->fork_ev, 0) != cudaSuccess) {
+      st = fail(h, FM_ERR_CUDA, "stream wait failed");
+      break;
+    }
+    st = body(i, L.stream);
+  }
+  for (int i = 0; i < started; ++i) {
+    fm_handle::Lane &L = h->lanes[ids[i]];
+    if (cudaEventRecord(L.done, L.stream) != cudaSuccess || cudaStreamWaitEvent(s, L.done, 0) != cudaSuccess)
+      if (st == FM_OK) st = fail(h, FM_ERR_CUDA, "stream join failed");
+  }
+  return st;
+}
 
 extern "C" {
 
@@ -1368,17 +1439,28 @@ fm_status fm_context_append_batched(fm_handle *h, int32_t n_seqs, const int32_t 
     off += (size_t)n_rows[i] * h->cfg.n_taps * h->cfg.target_dim;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::vector<size_t> offs(n_seqs);
   off = 0;
-  int total = 0;
   for (int i = 0; i < n_seqs; ++i) {
-    const int launches = h->last_launches;
-    TRY(append_one(h, seq_ids[i], feats + off, n_rows[i], start[i], s));
-    total = h->last_launches;
-    (void)launches;
+    offs[i] = off;
     off += (size_t)n_rows[i] * h->cfg.n_taps * h->cfg.target_dim;
   }
-  h->last_launches = total;
-  return FM_OK;
+  // dense appends share the prefill scratch: they run first, one after the other, on the caller's stream
+  std::vector<int32_t> rest;
+  std::vector<int> rest_i;
+  for (int i = 0; i < n_seqs; ++i) {
+    if (n_rows[i] >= kPrefillMin) {
+      TRY(append_one(h, seq_ids[i], feats + offs[i], n_rows[i], start[i], s));
+    } else {
+      rest.push_back(seq_ids[i]);
+      rest_i.push_back(i);
+    }
+  }
+  if (rest.empty()) return FM_OK;
+  return run_lanes(h, (int)rest.size(), rest.data(), s, [&](int j, cudaStream_t ls) {
+    const int i = rest_i[j];
+    return append_one(h, seq_ids[i], feats + offs[i], n_rows[i], start[i], ls);
+  });
 }
 
 fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const int32_t *anchors, const int32_t *pos,
@@ -1400,10 +1482,9 @@ fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const i
       return fail(h, FM_ERR_CONTEXT_FULL, "context full at pos %d", pos[i]);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  for (int i = 0; i < n_seqs; ++i) {
-    TRY(draft_one(h, seq_ids[i], anchors[i], pos[i], tokens + (size_t)i * h->cfg.block, s));
-  }
-  return FM_OK;
+  return run_lanes(h, n_seqs, seq_ids, s, [&](int i, cudaStream_t ls) {
+    return draft_one(h, seq_ids[i], anchors[i], pos[i], tokens + (size_t)i * h->cfg.block, ls);
+  });
 }
 
 fm_status fm_accept(const int32_t *draft, const int32_t *target, int32_t k, int32_t *n_accepted, int32_t *bonus) {
@@ -1471,10 +1552,14 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
       size = (int64_t)c.block * c.dim * 4;
       break;
     case FM_DEBUG_HEAD_OUT:
+      TRY(check_seq(h, seq));
+      use_lane(h, seq);
       src = h->Y;
       size = (int64_t)c.block * c.target_dim * 4;
       break;
     case FM_DEBUG_LOGITS: {
+      TRY(check_seq(h, seq));
+      use_lane(h, seq);
       if (!h->dbg_logits) TRY(dalloc(h, &h->dbg_logits, (size_t)kMaxT * c.vocab));
       StepParams p{};
       p.T = c.block;
@@ -1489,7 +1574,7 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
     case FM_DEBUG_CACHE_K:
     case FM_DEBUG_CACHE_V: {
       TRY(check_seq(h, seq));
-      TRY(flush_pending(h, s));
+      TRY(flush_pending(h, seq, s));
       if (index < 0 || index >= c.n_layers) return fail(h, FM_ERR_INVALID_ARG, "layer %d", index);
       Seg2 kv = h->kv(seq, index);
       src = what == FM_DEBUG_CACHE_K ? kv.k : kv.v;
@@ -1597,6 +1682,11 @@ void fm_destroy(fm_handle *h) {
   for (auto &kv : h->graphs)
     if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
   if (h->cap) cudaStreamDestroy(h->cap);
+  for (fm_handle::Lane &L : h->lanes) {
+    if (L.stream) cudaStreamDestroy(L.stream);
+    if (L.done) cudaEventDestroy(L.done);
+  }
+  if (h->fork_ev) cudaEventDestroy(h->fork_ev);
   delete h;
 }
 
