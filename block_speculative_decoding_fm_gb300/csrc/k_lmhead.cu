@@ -202,7 +202,11 @@ __device__ __forceinline__ int my_tile_count(int n_tiles) {
 // the Y chunks its table chunks need, so the ring can be deep; otherwise Y is
 // split here and stays resident, and the ring gets what shared memory is left.
 constexpr int kQ8Conv = 8, kQ8Epi = 8;   // warps
-constexpr int kQ8Threads = kBase + 32 * (kQ8Conv + kQ8Epi);
+// a second MMA-issuing warp: one thread issuing small MMAs is latency-bound (a
+// second issuer nearly doubles an SM's rate at N = 32), so with NI = 2 the chunk
+// pairs alternate between warp 1 and this warp
+constexpr int kQ8Issuer2 = 2 + kQ8Conv + kQ8Epi;
+constexpr int kQ8Threads = kBase + 32 * (kQ8Conv + kQ8Epi + 1);
 
 // bytes of one ring stage: (streamed Y chunks, then) U table chunks, 1024-aligned
 __host__ __device__ constexpr int q8_stage_bytes(bool stream_y, int U) {
@@ -210,7 +214,7 @@ __host__ __device__ constexpr int q8_stage_bytes(bool stream_y, int U) {
 }
 
 template <bool kStreamY>
-__global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
+__global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U, const int NI) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kQ8Chunk;
   constexpr int kNA = 2, kND = 3, kG = 2;
@@ -246,7 +250,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
       mbar_init(full(i), 1);
       // the stage is free once the converters and the epilogue (block scales) are done
       // with it, and, for streamed Y, the MMAs that read its Y
-      mbar_init(empty(i), kQ8Conv + kQ8Epi + (kStreamY ? 1 : 0));
+      // (with two issuers each stage's unit spans one pair of each, and both commit)
+      mbar_init(empty(i), kQ8Conv + kQ8Epi + (kStreamY ? NI : 0));
     }
     for (int i = 0; i < kNA; ++i) {
       mbar_init(afull(i), kQ8Conv);
@@ -325,32 +330,41 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
         if (++st == S) { st = 0; par ^= 1; }
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
-      int i = 0, j = 0, kc = 0, st = 0, uo = 0;
-      uint32_t apar = 0, dpar = 0;
+  } else if (warp == 1 || warp == kQ8Issuer2) {
+    const int me = warp == 1 ? 0 : 1;
+    if (lane == 0 && me < NI && mbar_wait_bounded(yfull, 0, a.err)) {
+      // every issuer walks all pairs (to keep the stage / chunk counters) and issues its own
+      int kc = 0, st = 0, uo = 0;
       for (int sc = 0; sc < nsc; ++sc) {
         const int n = min(kG, total - kG * sc);
-        if (!mbar_wait_bounded(afull(i), apar, a.err)) break;
-        if (sc >= kND && !mbar_wait_bounded(dempty(j), dpar ^ 1, a.err)) break;
-        tc_fence_after();
+        if (sc % NI == me) {
+          const int i = sc % kNA, j = sc % kND;
+          if (!mbar_wait_bounded(afull(i), (uint32_t)(sc / kNA) & 1, a.err)) break;
+          if (sc >= kND && !mbar_wait_bounded(dempty(j), (uint32_t)(sc / kND - 1) & 1, a.err)) break;
+          tc_fence_after();
+          int kc2 = kc, st2 = st, uo2 = uo;
+          for (int h = 0; h < n; ++h) {
+            // (streamed Y: the converters' afull for this chunk implies its stage has landed)
+            const uint64_t bd =
+                umma_desc_sw128(kStreamY ? ring + st2 * SS + uo2 * kYChunk : ybuf + kc2 * kYChunk);
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk)
+                umma_ts(tmem + 128 + 128 * j + 64 * h + 32 * blk, tmem + 64 * i + 32 * h + 16 * blk + 8 * kk,
+                        bd + 2 * (2 * blk + kk), IDESC, kk);
+            // one issuer: release the stage after its last chunk; two: each releases after its pair
+            if (kStreamY && ((NI == 1 && uo2 == U - 1) || (NI == 2 && h == n - 1))) umma_commit(empty(st2));
+            if (++kc2 == kcs) kc2 = 0;
+            if (++uo2 == U) { uo2 = 0; if (++st2 == S) st2 = 0; }
+          }
+          umma_commit(aempty(i));
+          umma_commit(dfull(j));
+        }
         for (int h = 0; h < n; ++h) {
-          // (streamed Y: the converters' afull for this chunk implies its stage has landed)
-          const uint64_t bd = umma_desc_sw128(kStreamY ? ring + st * SS + uo * kYChunk : ybuf + kc * kYChunk);
-#pragma unroll
-          for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-              umma_ts(tmem + 128 + 128 * j + 64 * h + 32 * blk, tmem + 64 * i + 32 * h + 16 * blk + 8 * kk,
-                      bd + 2 * (2 * blk + kk), IDESC, kk);
-          if (kStreamY && uo == U - 1) umma_commit(empty(st));
           if (++kc == kcs) kc = 0;
           if (++uo == U) { uo = 0; if (++st == S) st = 0; }
         }
-        umma_commit(aempty(i));
-        umma_commit(dfull(j));
-        if (++i == kNA) { i = 0; apar ^= 1; }
-        if (++j == kND) { j = 0; dpar ^= 1; }
       }
     }
   } else if (warp < 2 + kQ8Conv) {
@@ -458,7 +472,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
       dpar ^= 1;
     }
   }
-  finish_argmax<8>(a, T, warp >= 2 + kQ8Conv, 8 * group, bv, bi);
+  finish_argmax<8>(a, T, warp >= 2 + kQ8Conv && warp < kQ8Issuer2, 8 * group, bv, bi);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -467,7 +481,14 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
 }
 
 // ---------------------------------------------------------------- bf16 table
-// TMEM columns: per-tile accumulator, double buffered at 0 and 32.
+// TMEM columns: per-tile accumulator, double buffered at 0 and 32.  Y either
+// streams with the table (each stage: U Y chunks, then U table chunks) or stays
+// resident, as in the Q8_0 kernel.
+__host__ __device__ constexpr int bf_stage_bytes(bool stream_y, int U) {
+  return (stream_y ? U * kYChunk : 0) + U * kBfStage;   // multiples of 1024
+}
+
+template <bool kStreamY>
 __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kBfStage;
@@ -475,11 +496,12 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
   const int H = a.H, kcs = H / kChunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ybuf = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t ring = ybuf + kcs * kYChunk;
+  const uint32_t ring = kStreamY ? ybuf : ybuf + kcs * kYChunk;
   // a ring stage holds U consecutive chunks of one tile, moved by one bulk copy: the
   // copy engine takes a roughly fixed time per copy, so fewer, larger copies stream faster
-  const int UB = U * SB;
-  const uint32_t bars = ring + S * UB;
+  const int SS = bf_stage_bytes(kStreamY, U);
+  const int TOFF = kStreamY ? U * kYChunk : 0;
+  const uint32_t bars = ring + S * SS;
   auto full = [&](int i) { return bars + 8 * i; };
   auto empty = [&](int i) { return bars + 8 * (S + i); };
   auto dfull = [&](int j) { return bars + 8 * (2 * S + j); };
@@ -507,8 +529,9 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
     mbar_init(yfull, 1);
     mbar_fence_init();
     for (int j = 0; j < S && j * U < total; ++j) {
-      mbar_expect_tx(full(j), UB);
-      bulk_g2s(ring + j * UB, src_of(j * U), UB, full(j));
+      // streamed Y: one expect for the stage's table and Y bytes; Y is copied after griddepcontrol.wait
+      mbar_expect_tx(full(j), U * SB + (kStreamY ? U * kYChunk : 0));
+      bulk_g2s(ring + j * SS + TOFF, src_of(j * U), U * SB, full(j));
     }
   }
   if (warp == 1) tmem_alloc<64>(tslot);
@@ -522,28 +545,42 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
 
   if (warp == 0) {
     if (lane == 0) {
-      if (a.ylm) load_ylm(a, ybuf, yfull);
+      if (kStreamY) {
+        for (int j = 0; j < S && j * U < total; ++j)
+          bulk_g2s(ring + j * SS, a.ylm + (size_t)((j * U) % kcs) * kYChunk, U * kYChunk, full(j));
+        mbar_arrive(yfull);
+      } else if (a.ylm) {
+        load_ylm(a, ybuf, yfull);
+      }
+      int st = 0;
+      uint32_t par = 0;
       for (int j = S; j * U < total; ++j) {
-        const int st = j % S;
-        if (!mbar_wait_bounded(empty(st), (j / S - 1) & 1, a.err)) break;
-        mbar_expect_tx(full(st), UB);
-        bulk_g2s(ring + st * UB, src_of(j * U), UB, full(st));
+        if (!mbar_wait_bounded(empty(st), par, a.err)) break;
+        mbar_expect_tx(full(st), U * SB + (kStreamY ? U * kYChunk : 0));
+        bulk_g2s(ring + st * SS + TOFF, src_of(j * U), U * SB, full(st));
+        if (kStreamY) bulk_g2s(ring + st * SS, a.ylm + (size_t)((j * U) % kcs) * kYChunk, U * kYChunk, full(st));
+        if (++st == S) { st = 0; par ^= 1; }
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
+      // counters instead of divisions: this thread's per-chunk work is a serial chain
+      int st = 0, uo = 0, kc = 0, ti = 0;
+      uint32_t fpar = 0;
       for (int c = 0; c < total; ++c) {
-        const int st = (c / U) % S, ti = c / kcs, kc = c % kcs, db = ti & 1;
+        const int db = ti & 1;
         if (kc == 0 && ti >= 2 && !mbar_wait_bounded(dempty(db), ((ti >> 1) - 1) & 1, a.err)) break;
-        if (!mbar_wait_bounded(full(st), (c / U / S) & 1, a.err)) break;
+        if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) break;
         tc_fence_after();
-        const uint64_t ad = umma_desc_sw128(ring + st * UB + (c % U) * SB);
-        const uint64_t bd = umma_desc_sw128(ybuf + kc * kYChunk);
+        const uint64_t ad = umma_desc_sw128(ring + st * SS + TOFF + uo * SB);
+        const uint64_t bd = umma_desc_sw128(kStreamY ? ring + st * SS + uo * kYChunk : ybuf + kc * kYChunk);
 #pragma unroll
         for (int kk = 0; kk < kChunk / 16; ++kk)
           umma_ss(tmem + 32 * db, ad + 2 * kk, bd + 2 * kk, IDESC, (kc | kk) ? 1u : 0u);
-        if (c % U == U - 1) umma_commit(empty(st));
+        if (uo == U - 1) umma_commit(empty(st));
         if (kc == kcs - 1) umma_commit(dfull(db));
+        if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
+        if (++kc == kcs) { kc = 0; ++ti; }
       }
     }
   }
@@ -555,7 +592,7 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
 #pragma unroll
   for (int i = 0; i < 16; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; }
   if (warp >= 2) {
-    if (!a.ylm) {
+    if (!kStreamY && !a.ylm) {
       stage_y<false>(a, ybuf, T, (int)threadIdx.x - kBase, kBfWorkers);
       fence_proxy_async();
       named_sync(1, kBfWorkers);
@@ -640,11 +677,11 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) 
   const size_t budget = 227 * 1024 - 2048;   // leaves room for the static shared arrays
   int U, S;
   size_t smem;
-  const bool stream = q8 && a.ylm != nullptr;
+  const bool stream = a.ylm != nullptr;
   if (stream) {
-    // four chunks (and their Y) per stage when the tile's chunk count allows
-    U = kcs % 4 == 0 ? 4 : kcs % 2 == 0 ? 2 : 1;
-    const size_t ss = (size_t)q8_stage_bytes(true, U);
+    // several chunks (and their Y) per stage when the tile's chunk count allows
+    U = q8 ? (kcs % 4 == 0 ? 4 : kcs % 2 == 0 ? 2 : 1) : (kcs % 2 == 0 ? 2 : 1);
+    const size_t ss = q8 ? (size_t)q8_stage_bytes(true, U) : (size_t)bf_stage_bytes(true, U);
     S = (int)((budget - 1024 - bars) / (ss + 16));
     if (S > 8) S = 8;
     if (S < 2) return cudaErrorInvalidValue;
@@ -679,8 +716,15 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) 
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, kern, a, S, U);
   };
-  if (q8) return stream ? go(lmhead_q8_kernel<true>) : go(lmhead_q8_kernel<false>);
-  return go(lmhead_bf16_kernel);
+  // two MMA issuers when Y streams in 4-chunk units (each unit = one pair per issuer)
+  const int NI = q8 && stream && U == 4 ? 2 : 1;
+  auto goq = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, kern, a, S, U, NI);
+  };
+  if (q8) return stream ? goq(lmhead_q8_kernel<true>) : goq(lmhead_q8_kernel<false>);
+  return stream ? go(lmhead_bf16_kernel<true>) : go(lmhead_bf16_kernel<false>);
 }
 
 }  // namespace fm
