@@ -337,7 +337,9 @@ GemvArgs gemv_base(const fm_handle *h, const __nv_bfloat16 *W, int M, int K, int
   while (ks < 8 && K % (64 * ks * 2) == 0 && tiles * ks * 2 <= 2 * h->n_sm) ks *= 2;
   a.ksplit = ks;
   a.Kc = K / ks;
-  a.Kp = a.Kc < 256 ? a.Kc : 256;
+  // activation pieces: 256 columns; 128 for 17..32 rows, which keeps two CTAs per SM
+  const int kp = (T_const > 0 && T_const <= 16) ? 256 : 128;
+  a.Kp = a.Kc < kp ? a.Kc : kp;
   a.hd = h->cfg.head_dim;
   a.max_ctx = h->cfg.max_ctx;
   a.rope = h->rope;

@@ -377,7 +377,7 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
 }  // namespace
 
 template <int MT>
-__global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __grid_constant__ GemvArgs a, const int S, const int U) {
+__global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ GemvArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int NR = 32 * MT;                 // B rows: hi rows then lo rows
   constexpr int BCH = NR * 128;               // bytes of one 64-column B chunk
@@ -593,9 +593,9 @@ __global__ void __launch_bounds__(kAll, MT == 1 ? 2 : 1) gemv_kernel(const __gri
 
 // ring chunks (16 KB each), and chunks per bulk copy
 static int gemv_stages(const GemvArgs &a, int mt) {
-  (void)mt;
   const int nchunks = a.Kc / kChunk;
-  return nchunks < 4 ? nchunks : 4;
+  const int most = mt == 1 ? 4 : 3;   // 17..32 rows: a shorter ring keeps two CTAs per SM
+  return nchunks < most ? nchunks : most;
 }
 static int gemv_unit(const GemvArgs &a, int mt) {
   return (a.Kc / kChunk) % 2 == 0 && gemv_stages(a, mt) % 2 == 0 ? 2 : 1;
