@@ -73,17 +73,6 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 // kind::f16 instruction descriptor: D f32, A/B f16, both K-major, M 128, N 256
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
-          d_tmem),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
-}
-
 #define FM_TLD32(taddr, v)                                                                                          \
   asm volatile(                                                                                                     \
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19," \
@@ -242,26 +231,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (uint32_t j = it > ST ? it - ST : 0; j < it; ++j) mbar_wait(full(j % ST), (j / ST) & 1, a.err, false);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      uint32_t it = 0, tc = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-        const int b = tc & 1;
-        if (!mbar_wait(tempty(b), ((tc >> 1) & 1) ^ 1, a.err)) break;
+    // the whole warp runs the issue loop (warp-uniform state); one elected lane
+    // issues each MMA and commit, and every wait's verdict is made warp-uniform
+    uint32_t it = 0, tc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+      const int b = tc & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(tempty(b), ((tc >> 1) & 1) ^ 1, a.err))) break;
+      tc_fence_after();
+      const uint32_t d = tmem + b * BN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % ST;
+        if (!__all_sync(0xffffffffu, mbar_wait(full(s), (it / ST) & 1, a.err))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + b * BN;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % ST;
-          if (!mbar_wait(full(s), (it / ST) & 1, a.err)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sa = base + s * STAGE, sb = sa + A_BYTES;
-          const uint64_t ad = sdesc(sa), bd = sdesc(sb);
+        const uint32_t sa = base + s * STAGE, sb = sa + A_BYTES;
+        const uint64_t ad = sdesc(sa), bd = sdesc(sb);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) mma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, (kb | kk) ? 1u : 0u);
-          mma_commit(empty(s));
-        }
-        if (ok) mma_commit(tfull(b));
+        for (int kk = 0; kk < BK / 16; ++kk) umma_ss_elect(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (kb | kk) ? 1u : 0u);
+        umma_commit_elect(empty(s));
       }
+      if (ok) umma_commit_elect(tfull(b));
     }
   } else {
     const int quad = warp & 3;  // TMEM lanes 32 * quad .. + 31 belong to this warp

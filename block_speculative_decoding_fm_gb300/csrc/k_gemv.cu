@@ -450,25 +450,24 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // counters instead of divisions: this thread's per-chunk work is a serial chain
-      int st = 0, uo = 0, pc = 0, pb = 0;
-      uint32_t fpar = 0, ppar = 0;
-      for (int c = 0; c < nchunks; ++c) {
-        if (pc == 0 && !mbar_wait_bounded(bfull0 + 8 * pb, ppar, a.err)) break;
-        if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) break;
-        tc_fence_after();
-        const uint64_t ad = umma_desc_sw128(ring + st * UB + uo * kStageBytes);
-        const uint64_t bd = umma_desc_sw128(s.bbuf[pb] + pc * BCH);
+    // the whole warp runs the issue loop (warp-uniform counters and descriptors);
+    // one elected lane issues each MMA and commit.  Counters, not divisions.
+    int st = 0, uo = 0, pc = 0, pb = 0;
+    uint32_t fpar = 0, ppar = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      if (pc == 0 && !mbar_wait_warp(bfull0 + 8 * pb, ppar, a.err)) break;
+      if (uo == 0 && !mbar_wait_warp(full(st), fpar, a.err)) break;
+      tc_fence_after();
+      const uint64_t ad = umma_desc_sw128(ring + st * UB + uo * kStageBytes);
+      const uint64_t bd = umma_desc_sw128(s.bbuf[pb] + pc * BCH);
 #pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk) umma_ss(tmem, ad + 2 * kk, bd + 2 * kk, IDESC, (c | kk) ? 1u : 0u);
-        if (uo == U - 1) umma_commit(empty(st));
-        if (pc == cpp - 1 || c == nchunks - 1) umma_commit(bempty0 + 8 * pb);
-        if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
-        if (++pc == cpp) { pc = 0; pb ^= 1; if (pb == 0) ppar ^= 1; }
-      }
-      umma_commit(accfull);
+      for (int kk = 0; kk < kChunk / 16; ++kk) umma_ss_elect(tmem, ad + 2 * kk, bd + 2 * kk, IDESC, (c | kk) ? 1u : 0u);
+      if (uo == U - 1) umma_commit_elect(empty(st));
+      if (pc == cpp - 1 || c == nchunks - 1) umma_commit_elect(bempty0 + 8 * pb);
+      if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
+      if (++pc == cpp) { pc = 0; pb ^= 1; if (pb == 0) ppar ^= 1; }
     }
+    umma_commit_elect(accfull);
   } else {
     // workers: stage the activation pieces, then read the accumulator
     load_row_stats(a, T, s.stat_mu, s.stat_rs);

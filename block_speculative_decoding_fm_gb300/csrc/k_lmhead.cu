@@ -22,6 +22,8 @@
 //     the last CTA reducing the per-CTA bests.
 #include <mutex>
 
+#include <type_traits>
+
 #include "dev_common.cuh"
 #include "fm_internal.h"
 
@@ -36,22 +38,23 @@ constexpr int kBfWorkers = 128;               // bf16: warps 2..5
 constexpr int kBase = 64;                     // warp 0: producer, warp 1: TMEM owner + MMA issuer
 
 
-// tcgen05.mma with A in tensor memory (lane = A row, 32-bit columns hold K pairs)
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+// tcgen05.mma with A in tensor memory (lane = A row, 32-bit columns hold K pairs),
+// issued by one elected lane of a warp that runs the issue loop together
+__device__ __forceinline__ void umma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
-          d_tmem),
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16], bool wait = true) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
           taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
       "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+  if (wait) asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 // 16 columns of this thread's lane; the caller waits with tmem_ld_wait() before using them
 __device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&v)[16]) {
@@ -188,23 +191,27 @@ __device__ __forceinline__ int my_tile_count(int n_tiles) {
 }  // namespace
 
 // ---------------------------------------------------------------- Q8_0 table
-// Roles: warp 0 streams the table, warp 1 owns TMEM and issues the MMAs, warps
-// 2..9 convert (one thread per table row and 32-column block), warps 10..17
-// apply the block scales and keep the running best (one thread per table row
-// and group of 8 slots).
-// Work moves in pairs of chunks ("super-chunks"): every wait and commit covers
-// two chunks, since a single-thread mbarrier wait or tcgen05.commit costs about
-// as much as one of the small MMAs.
-// TMEM columns: A slots [64 i, 64 i + 64) for i < kNA (chunk h of the pair at
-// +32 h); D slots 128 + 128 j + 64 h + 32 blk for j < kND (per 32-column block
-// of chunk h: 32 columns, per group of 8 slots 8 hi then 8 lo).
+// The block scale is folded into the A operand: for table row r and 32-column
+// block b, the converters form w = q * d (int8 times the f16 block scale, exact
+// in f32) as two f16 halves, hi = rn(q d) and lo = rn(q d - hi) (one f16
+// multiply and one fused multiply-add; lo holds the exact residual, which has
+// at most 9 significant bits), and write both to TMEM.  The MMAs then run the
+// whole K extent of a tile into one f32 accumulator (A = hi, then A = lo, each
+// against the Y hi/lo rows), so the epilogue touches each tile once.
+// Roles: warp 0 streams the table, warp 1 owns TMEM and issues MMAs, warps
+// 2..17 convert (two sets of 8: set h takes chunk h of each pair; in a set,
+// one thread per table row and 32-column block), warps 18..21 read each
+// finished tile and keep the per-row running best, warp 22 is the second MMA
+// issuer (pairs alternate between the issuers, each with its own accumulator).
+// Work moves in pairs of chunks (G = 2; G = 1 when a tile's chunk count is odd).
+// TMEM columns: A slot i < kNA (= 3, so the converters can run two pairs ahead
+// of the MMAs) at 128 i, chunk h of the pair at + 64 h, hi at + 0 and lo at
+// + 32 (16 columns per 32-column block); accumulators at 384 + 64 me + 32 db
+// (issuer me, tile parity db), per group of 8 slots 8 hi then 8 lo columns.
 // Y operand: kStreamY (Y pre-split in global memory): each ring stage carries
 // the Y chunks its table chunks need, so the ring can be deep; otherwise Y is
 // split here and stays resident, and the ring gets what shared memory is left.
-constexpr int kQ8Conv = 8, kQ8Epi = 8;   // warps
-// a second MMA-issuing warp: one thread issuing small MMAs is latency-bound (a
-// second issuer nearly doubles an SM's rate at N = 32), so with NI = 2 the chunk
-// pairs alternate between warp 1 and this warp
+constexpr int kQ8Conv = 16, kQ8Epi = 4;   // warps
 constexpr int kQ8Issuer2 = 2 + kQ8Conv + kQ8Epi;
 constexpr int kQ8Threads = kBase + 32 * (kQ8Conv + kQ8Epi + 1);
 
@@ -213,11 +220,25 @@ __host__ __device__ constexpr int q8_stage_bytes(bool stream_y, int U) {
   return ((stream_y ? U * kYChunk : 0) + U * kQ8Chunk + 1023) / 1024 * 1024;
 }
 
+// position of a chunk in the ring: stage, offset inside the stage's unit, phase parity
+struct RingPos {
+  int st = 0, uo = 0;
+  uint32_t par = 0;
+  __device__ __forceinline__ void step(int n, int U, int S) {
+    uo += n;
+    while (uo >= U) {
+      uo -= U;
+      if (++st == S) { st = 0; par ^= 1; }
+    }
+  }
+};
+
 template <bool kStreamY>
-__global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U, const int NI) {
+__global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U, const int NI, const int G) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kQ8Chunk;
-  constexpr int kNA = 2, kND = 3, kG = 2;
+  constexpr int kNA = 3;
+  constexpr int kD = 128 * kNA;   // first accumulator column
   constexpr uint32_t IDESC = umma_idesc(128, 32, false);
   const int H = a.H, kcs = H / kChunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -233,32 +254,31 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
   auto afull = [&](int i) { return bars + 8 * (2 * S + i); };
   auto aempty = [&](int i) { return bars + 8 * (2 * S + kNA + i); };
   auto dfull = [&](int j) { return bars + 8 * (2 * S + 2 * kNA + j); };
-  auto dempty = [&](int j) { return bars + 8 * (2 * S + 2 * kNA + kND + j); };
-  const uint32_t yfull = bars + 8 * (2 * S + 2 * kNA + 2 * kND);
+  auto dempty = [&](int j) { return bars + 8 * (2 * S + 2 * kNA + 2 + j); };
+  const uint32_t yfull = bars + 8 * (2 * S + 2 * kNA + 4);
   const uint32_t tslot = yfull + 8;
 
   const int n_tiles = (a.V + kTile - 1) / kTile;
   const int tiles = my_tile_count(n_tiles);
   const int total = tiles * kcs;
   const int units = total / U;
-  const int nsc = (total + kG - 1) / kG;   // super-chunks (the last may hold one chunk)
+  const int npairs = total / G;                        // G divides kcs
   const size_t tile_stride = (size_t)gridDim.x * kcs * SB;   // bytes between this CTA's tiles
   const uint8_t *first = a.q8 + (size_t)blockIdx.x * kcs * SB;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full(i), 1);
-      // the stage is free once the converters and the epilogue (block scales) are done
-      // with it, and, for streamed Y, the MMAs that read its Y
-      // (with two issuers each stage's unit spans one pair of each, and both commit)
-      mbar_init(empty(i), kQ8Conv + kQ8Epi + (kStreamY ? NI : 0));
+      // free once the converters that read its table chunks (one set per chunk, both
+      // sets when a unit spans a pair) and, for streamed Y, the issuers' MMAs are done
+      mbar_init(empty(i), (U == 1 ? kQ8Conv / 2 : kQ8Conv) + (kStreamY ? NI : 0));
     }
     for (int i = 0; i < kNA; ++i) {
-      mbar_init(afull(i), kQ8Conv);
+      mbar_init(afull(i), (kQ8Conv / 2) * G);
       mbar_init(aempty(i), 1);
     }
-    for (int j = 0; j < kND; ++j) {
-      mbar_init(dfull(j), 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(dfull(j), NI);
       mbar_init(dempty(j), kQ8Epi);
     }
     mbar_init(yfull, 1);
@@ -290,14 +310,64 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
     if (threadIdx.x == kBase) mbar_arrive(yfull);
   }
 
-  const int quad = warp & 3;
+  const int quad = warp & 3;   // TMEM lanes 32 quad .. + 31 belong to this warp
   const int r = 32 * quad + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(32 * quad) << 16);
-  float bv[8];
-  int bi[8];
+  float bv[16];
+  int bi[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; }
-  int group = 0;   // epilogue: slot group
+  for (int i = 0; i < 16; ++i) { bv[i] = -INFINITY; bi[i] = 0x7fffffff; }
+
+  // the MMA issuers: one code path per issuer, so that every value the MMAs take
+  // (TMEM and shared-memory addresses) derives from compile-time constants and
+  // warp-uniform counters
+  auto issue = [&](auto me_c) {
+    constexpr int me = decltype(me_c)::value;
+    // the whole warp runs the issue loop (warp-uniform state); one elected lane issues.
+    // Issuer me takes pairs me, me + NI, ...: a tile's pairs alternate between the
+    // issuers (the launcher makes their count even).  Counters only: a division or
+    // modulo by a runtime value in this loop slowed the MMA stream threefold.
+    if (me < NI && mbar_wait_warp(yfull, 0, a.err)) {
+      const int stride = G * NI;            // chunks from one of this issuer's pairs to the next
+      int kc = G * me, tl = 0;              // the pair's first chunk in its tile; the tile
+      int i = me, q = 0;                    // A slot (pair % kNA) and pair / kNA
+      RingPos y;                            // ring position of the pair's first chunk
+      y.step(G * me, U, S);
+      for (int sc = me; sc < npairs; sc += NI) {
+        const int db = tl & 1;
+        const uint32_t d = tmem + kD + 64 * me + 32 * db;
+        const bool first_in_tile = kc == G * me;
+        if (first_in_tile && tl >= 2 && !mbar_wait_warp(dempty(db), ((tl >> 1) - 1) & 1, a.err)) break;
+        if (!mbar_wait_warp(afull(i), (uint32_t)q & 1, a.err)) break;
+        tc_fence_after();
+        RingPos y2 = y;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h < G) {
+            // (streamed Y: the converters' afull for this chunk implies its stage has landed)
+            const uint64_t bd = umma_desc_sw128(kStreamY ? ring + y2.st * SS + y2.uo * kYChunk
+                                                          : ybuf + (kc + h) * kYChunk);
+            const uint32_t ah = tmem + 128 * i + 64 * h;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              umma_ts_elect(d, ah + 8 * kk, bd + 2 * kk, IDESC, (first_in_tile && h == 0 && kk == 0) ? 0u : 1u);
+              umma_ts_elect(d, ah + 32 + 8 * kk, bd + 2 * kk, IDESC, 1u);
+            }
+            // one issuer: release the stage after its last chunk; two: each releases after its pair
+            if (kStreamY && ((NI == 1 && y2.uo == U - 1) || (NI == 2 && h == G - 1))) umma_commit_elect(empty(y2.st));
+            y2.step(1, U, S);
+          }
+        }
+        umma_commit_elect(aempty(i));
+        if (kc + stride >= kcs) umma_commit_elect(dfull(db));   // this issuer's last pair of the tile
+        y.step(stride, U, S);
+        kc += stride;
+        if (kc >= kcs) { kc -= kcs; ++tl; }
+        i += NI;
+        if (i >= kNA) { i -= kNA; ++q; }
+      }
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -330,59 +400,35 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
         if (++st == S) { st = 0; par ^= 1; }
       }
     }
-  } else if (warp == 1 || warp == kQ8Issuer2) {
-    const int me = warp == 1 ? 0 : 1;
-    if (lane == 0 && me < NI && mbar_wait_bounded(yfull, 0, a.err)) {
-      // every issuer walks all pairs (to keep the stage / chunk counters) and issues its own
-      int kc = 0, st = 0, uo = 0;
-      for (int sc = 0; sc < nsc; ++sc) {
-        const int n = min(kG, total - kG * sc);
-        if (sc % NI == me) {
-          const int i = sc % kNA, j = sc % kND;
-          if (!mbar_wait_bounded(afull(i), (uint32_t)(sc / kNA) & 1, a.err)) break;
-          if (sc >= kND && !mbar_wait_bounded(dempty(j), (uint32_t)(sc / kND - 1) & 1, a.err)) break;
-          tc_fence_after();
-          int kc2 = kc, st2 = st, uo2 = uo;
-          for (int h = 0; h < n; ++h) {
-            // (streamed Y: the converters' afull for this chunk implies its stage has landed)
-            const uint64_t bd =
-                umma_desc_sw128(kStreamY ? ring + st2 * SS + uo2 * kYChunk : ybuf + kc2 * kYChunk);
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk)
-                umma_ts(tmem + 128 + 128 * j + 64 * h + 32 * blk, tmem + 64 * i + 32 * h + 16 * blk + 8 * kk,
-                        bd + 2 * (2 * blk + kk), IDESC, kk);
-            // one issuer: release the stage after its last chunk; two: each releases after its pair
-            if (kStreamY && ((NI == 1 && uo2 == U - 1) || (NI == 2 && h == n - 1))) umma_commit(empty(st2));
-            if (++kc2 == kcs) kc2 = 0;
-            if (++uo2 == U) { uo2 = 0; if (++st2 == S) st2 = 0; }
-          }
-          umma_commit(aempty(i));
-          umma_commit(dfull(j));
-        }
-        for (int h = 0; h < n; ++h) {
-          if (++kc == kcs) kc = 0;
-          if (++uo == U) { uo = 0; if (++st == S) st = 0; }
-        }
-      }
-    }
+  } else if (warp == 1) {
+    issue(std::integral_constant<int, 0>());
+  } else if (warp == kQ8Issuer2) {
+    issue(std::integral_constant<int, 1>());
   } else if (warp < 2 + kQ8Conv) {
-    // converters: block b of row r of chunk c -> f16 pairs in A slot c % kNA
-    const int b = (warp - 2) >> 2;
-    const uint32_t x = (uint32_t)((r >> 1) & 3);
-    const uint32_t o0 = (uint32_t)r * 64 + (((2 * b) ^ x) << 4), o1 = (uint32_t)r * 64 + (((2 * b + 1) ^ x) << 4);
-    int st = 0, uo = 0, i = 0;
-    uint32_t fpar = 0, apar = 0;
-    bool ok = true;
-    for (int sc = 0; sc < nsc && ok; ++sc) {
-      const int n = min(kG, total - kG * sc);
-      if (sc >= kNA && !mbar_wait_bounded(aempty(i), apar ^ 1, a.err)) break;
-      tc_fence_after();
-      for (int h = 0; h < n; ++h) {
-        if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) { ok = false; break; }
-        const uint32_t buf = ring + st * SS + TOFF + uo * SB;
+    // converters: set h takes chunk h of each pair; thread = (row r, block b) of the chunk
+    const int h = (warp - 2) >> 3;
+    const int b = ((warp - 2) >> 2) & 1;
+    if (h < G) {
+      const uint32_t x = (uint32_t)((r >> 1) & 3);
+      const uint32_t o0 = (uint32_t)r * 64 + (((2 * b) ^ x) << 4), o1 = (uint32_t)r * 64 + (((2 * b + 1) ^ x) << 4);
+      // the row's f16 block scale (two rows per 32-bit word in the chunk's scale plane)
+      const uint32_t soff = (uint32_t)kTile * 64 + (uint32_t)b * 256 + (uint32_t)(r & ~1) * 2;
+      const int sh = (r & 1) * 16;
+      RingPos c;
+      c.step(h, U, S);
+      int i = 0;
+      uint32_t apar = 0;
+      for (int sc = 0; sc < npairs; ++sc) {
+        if (sc >= kNA && !mbar_wait_bounded(aempty(i), apar ^ 1, a.err)) break;
+        // first chunk of this set in the stage's unit: wait for the stage
+        if (c.uo < G && !mbar_wait_bounded(full(c.st), c.par, a.err)) break;
+        tc_fence_after();
+        const uint32_t buf = ring + c.st * SS + TOFF + c.uo * SB;
         const uint4 v0 = lds128(buf + o0), v1 = lds128(buf + o1);
+        const uint32_t sw = lds32(buf + soff);
+        const uint32_t dd = (sw >> sh) & 0xffffu;
+        const uint32_t dpair = dd | (dd << 16);
+        const __half2 d2 = *reinterpret_cast<const __half2 *>(&dpair);
         uint32_t w[16];
         i8x4_to_f16x4(v0.x, w[0], w[1]);
         i8x4_to_f16x4(v0.y, w[2], w[3]);
@@ -392,87 +438,61 @@ __global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_c
         i8x4_to_f16x4(v1.y, w[10], w[11]);
         i8x4_to_f16x4(v1.z, w[12], w[13]);
         i8x4_to_f16x4(v1.w, w[14], w[15]);
-        tmem_st16(lane_base + 64 * i + 32 * h + 16 * b, w);
-        if (uo == U - 1) {
+        // last chunk of this set in the unit: the stage may be refilled after these loads
+        if (c.uo + G >= U) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(empty(st));
+          if (lane == 0) mbar_arrive(empty(c.st));
         }
-        if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const __half2 q = *reinterpret_cast<const __half2 *>(&w[j]);
+          const __half2 ph = __hmul2(q, d2);
+          const __half2 pl = __hfma2(q, d2, __hneg2(ph));
+          hi[j] = *reinterpret_cast<const uint32_t *>(&ph);
+          lo[j] = *reinterpret_cast<const uint32_t *>(&pl);
+        }
+        const uint32_t ta = lane_base + 128 * i + 64 * h + 16 * b;
+        tmem_st16(ta, hi, false);
+        tmem_st16(ta + 32, lo);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afull(i));
+        if (++i == kNA) { i = 0; apar ^= 1; }
+        c.step(G, U, S);
+      }
+    }
+  } else if (warp < 2 + kQ8Conv + kQ8Epi) {
+    // epilogue: one finished tile at a time; row r, all 16 slots (8 hi then 8 lo columns per group)
+    int tile = blockIdx.x;
+    for (int tl = 0; tl < tiles; ++tl, tile += gridDim.x) {
+      const int db = tl & 1;
+      if (!mbar_wait_bounded(dfull(db), (tl >> 1) & 1, a.err)) break;
+      tc_fence_after();
+      const int v = tile * kTile + r;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        uint32_t d0[16], d1[16];
+        tmem_ld16_async(lane_base + kD + 32 * db + 16 * g, d0);
+        if (NI == 2) tmem_ld16_async(lane_base + kD + 64 + 32 * db + 16 * g, d1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          float l = __uint_as_float(d0[t]) + __uint_as_float(d0[8 + t]);
+          if (NI == 2) l += __uint_as_float(d1[t]) + __uint_as_float(d1[8 + t]);
+          const int slot = 8 * g + t;
+          if (v < a.V && slot < T) {
+            if (a.logits) a.logits[(size_t)slot * a.V + v] = l;
+            if (better(l, v, bv[slot], bi[slot])) { bv[slot] = l; bi[slot] = v; }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(afull(i));
-      if (++i == kNA) { i = 0; apar ^= 1; }
-    }
-  } else {
-    // epilogue: slot group g of row r: scale each block's partial sums, accumulate, keep the best
-    group = (warp - 2 - kQ8Conv) >> 2;
-    const int g = group;
-    float acc[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
-    // the row's f16 block scales sit in the chunk's scale plane (two rows per 32-bit word)
-    const uint32_t soff = (uint32_t)kTile * 64 + (uint32_t)(r & ~1) * 2;
-    const int sh = (r & 1) * 16;
-    int kc = 0, tile = blockIdx.x, st = 0, uo = 0;
-    uint32_t dpar = 0, fpar = 0;
-    bool ok = true;
-    for (int base = 0; base < nsc && ok; base += kND) {
-#pragma unroll
-      for (int u = 0; u < kND; ++u) {
-        const int sc = base + u;
-        if (sc >= nsc) break;
-        const int n = min(kG, total - kG * sc);
-        if (!mbar_wait_bounded(dfull(u), dpar, a.err)) { ok = false; break; }
-        tc_fence_after();
-        // one chunk of the pair at a time (registers), one wait and one release for both
-#pragma unroll
-        for (int h = 0; h < kG; ++h) {
-          if (h >= n) break;
-          uint32_t d0[16], d1[16];
-          tmem_ld16_async(lane_base + 128 + 128 * u + 64 * h + 16 * g, d0);        // block 0: group g hi, lo
-          tmem_ld16_async(lane_base + 128 + 128 * u + 64 * h + 32 + 16 * g, d1);   // block 1
-          // the row's block scales, from the stage that holds the chunk (released after use)
-          if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) ok = false;
-          const uint32_t sa = ring + st * SS + TOFF + uo * SB + soff;
-          const uint32_t w0 = lds32(sa), w1 = lds32(sa + 256);
-          tmem_ld_wait();
-          const float f0 = __half2float(__ushort_as_half((unsigned short)(w0 >> sh)));
-          const float f1 = __half2float(__ushort_as_half((unsigned short)(w1 >> sh)));
-          if (h == n - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dempty(u));
-          }
-          if (uo == U - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty(st));
-          }
-          if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
-#pragma unroll
-          for (int t = 0; t < 8; ++t)
-            acc[t] += f0 * (__uint_as_float(d0[t]) + __uint_as_float(d0[8 + t])) +
-                      f1 * (__uint_as_float(d1[t]) + __uint_as_float(d1[8 + t]));
-          if (++kc == kcs) {
-            kc = 0;
-            const int v = tile * kTile + r;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int slot = 8 * g + t;
-              if (v < a.V && slot < T) {
-                if (a.logits) a.logits[(size_t)slot * a.V + v] = acc[t];
-                if (better(acc[t], v, bv[t], bi[t])) { bv[t] = acc[t]; bi[t] = v; }
-              }
-              acc[t] = 0.f;
-            }
-            tile += gridDim.x;
-          }
-        }
-      }
-      dpar ^= 1;
+      if (lane == 0) mbar_arrive(dempty(db));
     }
   }
-  finish_argmax<8>(a, T, warp >= 2 + kQ8Conv && warp < kQ8Issuer2, 8 * group, bv, bi);
+  finish_argmax<16>(a, T, warp >= 2 + kQ8Conv && warp < kQ8Issuer2, 0, bv, bi);
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -563,22 +583,23 @@ __global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(cons
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && mbar_wait_bounded(yfull, 0, a.err)) {
-      // counters instead of divisions: this thread's per-chunk work is a serial chain
+    // the whole warp runs the issue loop (warp-uniform state); one elected lane issues
+    if (mbar_wait_warp(yfull, 0, a.err)) {
+      // counters instead of divisions
       int st = 0, uo = 0, kc = 0, ti = 0;
       uint32_t fpar = 0;
       for (int c = 0; c < total; ++c) {
         const int db = ti & 1;
-        if (kc == 0 && ti >= 2 && !mbar_wait_bounded(dempty(db), ((ti >> 1) - 1) & 1, a.err)) break;
-        if (uo == 0 && !mbar_wait_bounded(full(st), fpar, a.err)) break;
+        if (kc == 0 && ti >= 2 && !mbar_wait_warp(dempty(db), ((ti >> 1) - 1) & 1, a.err)) break;
+        if (uo == 0 && !mbar_wait_warp(full(st), fpar, a.err)) break;
         tc_fence_after();
         const uint64_t ad = umma_desc_sw128(ring + st * SS + TOFF + uo * SB);
         const uint64_t bd = umma_desc_sw128(kStreamY ? ring + st * SS + uo * kYChunk : ybuf + kc * kYChunk);
 #pragma unroll
         for (int kk = 0; kk < kChunk / 16; ++kk)
-          umma_ss(tmem + 32 * db, ad + 2 * kk, bd + 2 * kk, IDESC, (kc | kk) ? 1u : 0u);
-        if (uo == U - 1) umma_commit(empty(st));
-        if (kc == kcs - 1) umma_commit(dfull(db));
+          umma_ss_elect(tmem + 32 * db, ad + 2 * kk, bd + 2 * kk, IDESC, (kc | kk) ? 1u : 0u);
+        if (uo == U - 1) umma_commit_elect(empty(st));
+        if (kc == kcs - 1) umma_commit_elect(dfull(db));
         if (++uo == U) { uo = 0; if (++st == S) { st = 0; fpar ^= 1; } }
         if (++kc == kcs) { kc = 0; ++ti; }
       }
@@ -716,12 +737,15 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) 
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, kern, a, S, U);
   };
-  // two MMA issuers when Y streams in 4-chunk units (each unit = one pair per issuer)
-  const int NI = q8 && stream && U == 4 ? 2 : 1;
+  // Q8_0: chunks move in pairs when a tile's chunk count is even; two MMA issuers when
+  // Y streams in 4-chunk units (each unit = one pair per issuer) and a tile's pairs
+  // split evenly between them
+  const int G = kcs % 2 == 0 ? 2 : 1;
+  const int NI = q8 && stream && U == 4 && (kcs / G) % 2 == 0 ? 2 : 1;
   auto goq = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, kern, a, S, U, NI);
+    return cudaLaunchKernelEx(&cfg, kern, a, S, U, NI, G);
   };
   if (q8) return stream ? goq(lmhead_q8_kernel<true>) : goq(lmhead_q8_kernel<false>);
   return stream ? go(lmhead_bf16_kernel<true>) : go(lmhead_bf16_kernel<false>);

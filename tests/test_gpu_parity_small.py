@@ -72,6 +72,18 @@ def test_tiny_flashmap_one_step(lm):
     p.close()
 
 
+@pytest.mark.parametrize("target_dim", [384, 512])
+def test_tiny_flashmap_q8_chunk_pairs(target_dim):
+    """Q8_0 lm_head widths whose 64-column chunk count per tile is 6 (pairs, one
+    MMA issuer) and 8 (pairs alternating between two issuers)."""
+    cfg = S.tiny_config(max_ctx=96).replace(lm_format=S.LM_Q8_0, target_dim=target_dim)
+    p = Pair(cfg, 1005)
+    p.append(0, S.gen_features(S.streams(1005)["features"], 40, cfg.feat_dim), 0)
+    got, ref = p.draft(0, 123, 40)
+    check_draft(p, got, ref)
+    p.close()
+
+
 def test_tiny_flashmap_ragged_appends_and_rewind():
     cfg = S.tiny_config(max_ctx=160)
     p = Pair(cfg, 1002)
