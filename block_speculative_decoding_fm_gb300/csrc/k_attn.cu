@@ -178,13 +178,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
         p[e] = mm == -INFINITY ? 0.f : exp2f(s[j][e] - mm);
         rsum[e >> 1] += p[e];
       }
-      __half h[4], l[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) split_f16(p[e], h[e], l[e]);
-      ph[2 * j] = pack_f16(h[0], h[1]);      // row g
-      ph[2 * j + 1] = pack_f16(h[2], h[3]);  // row g + 8
-      pl[2 * j] = pack_f16(l[0], l[1]);
-      pl[2 * j + 1] = pack_f16(l[2], l[3]);
+      split2_f16(p[0], p[1], ph[2 * j], pl[2 * j]);          // row g
+      split2_f16(p[2], p[3], ph[2 * j + 1], pl[2 * j + 1]);  // row g + 8
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -288,7 +283,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
 #pragma unroll
     for (int e = 0; e < PL; ++e) dst[e] = acc[e] * inv;
   }
-  cluster.sync();
+  // no CTA leaves while a peer may still read its partials (the reads above are consumed)
+  cluster_arrive_relaxed();
+  cluster_wait_acquire();
 }
 
 cudaError_t launch_attn(const AttnArgs &a, int L_now, cudaStream_t st, bool pdl) {

@@ -156,15 +156,13 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, uint32_t dst, int T, i
         v[3] = (v[3] - mu) * rs * (1.f + sc.w) + sh.w;
       }
     }
-    __nv_bfloat16 h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
+    uint32_t h01, l01, h23, l23;
+    split2_bf16(v[0], v[1], h01, l01);
+    split2_bf16(v[2], v[3], h23, l23);
     const uint32_t cbase = dst + (uint32_t)(kq >> 6) * (32 * MT * 128);
     const int kk = kq & 63;
-    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(t, kk)), "r"(pack_bf16(h[0], h[1])),
-                 "r"(pack_bf16(h[2], h[3])));
-    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(rows + t, kk)), "r"(pack_bf16(l[0], l[1])),
-                 "r"(pack_bf16(l[2], l[3])));
+    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(t, kk)), "r"(h01), "r"(h23));
+    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(rows + t, kk)), "r"(l01), "r"(l23));
   }
 }
 
@@ -226,17 +224,11 @@ __device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], i
         // the same rows split into the lm_head's resident operand (hi row, lo row 8 further)
         uint32_t hw[2], lw[2];
         if (a.ylm_f16) {
-          __half hh[4], ll[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split_f16(v[e], hh[e], ll[e]);
-          hw[0] = pack_f16(hh[0], hh[1]); hw[1] = pack_f16(hh[2], hh[3]);
-          lw[0] = pack_f16(ll[0], ll[1]); lw[1] = pack_f16(ll[2], ll[3]);
+          split2_f16(v[0], v[1], hw[0], lw[0]);
+          split2_f16(v[2], v[3], hw[1], lw[1]);
         } else {
-          __nv_bfloat16 hh[4], ll[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split_bf16(v[e], hh[e], ll[e]);
-          hw[0] = pack_bf16(hh[0], hh[1]); hw[1] = pack_bf16(hh[2], hh[3]);
-          lw[0] = pack_bf16(ll[0], ll[1]); lw[1] = pack_bf16(ll[2], ll[3]);
+          split2_bf16(v[0], v[1], hw[0], lw[0]);
+          split2_bf16(v[2], v[3], hw[1], lw[1]);
         }
         uint8_t *cb = a.ylm + (size_t)(mrow >> 6) * kLmYChunk;
         const int r = lm_yrow(t);
@@ -541,8 +533,8 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
         if (u == nu) { vs[u][0] = v[0]; vs[u][1] = v[1]; vs[u][2] = v[2]; vs[u][3] = v[3]; }
     }
   }
-  // done reading the peers' tiles: they may leave once everyone has arrived
-  if (ks > 1) cluster_arrive_release();
+  // done reading the peers' tiles (the values are summed): they may leave once everyone has arrived
+  if (ks > 1) cluster_arrive_relaxed();
   if (warp >= 2) {
 #pragma unroll
     for (int u = 0; u < kMaxUnits; ++u) {

@@ -100,17 +100,11 @@ __device__ void stage_y(const LmArgs &a, uint32_t ybuf, int T, int tid, int nthr
       const float v[4] = {y[b].x, y[b].y, y[b].z, y[b].w};
       uint32_t hw[2], lw[2];
       if (Q8) {
-        __half h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) split_f16(v[e], h[e], l[e]);
-        hw[0] = pack_f16(h[0], h[1]); hw[1] = pack_f16(h[2], h[3]);
-        lw[0] = pack_f16(l[0], l[1]); lw[1] = pack_f16(l[2], l[3]);
+        split2_f16(v[0], v[1], hw[0], lw[0]);
+        split2_f16(v[2], v[3], hw[1], lw[1]);
       } else {
-        __nv_bfloat16 h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
-        hw[0] = pack_bf16(h[0], h[1]); hw[1] = pack_bf16(h[2], h[3]);
-        lw[0] = pack_bf16(l[0], l[1]); lw[1] = pack_bf16(l[2], l[3]);
+        split2_bf16(v[0], v[1], hw[0], lw[0]);
+        split2_bf16(v[2], v[3], hw[1], lw[1]);
       }
       const uint32_t cb = ybuf + (uint32_t)(k >> 6) * kYChunk;
       const int r = lm_yrow(t);
