@@ -44,7 +44,7 @@ constexpr int kCsStride = kTile + 8;             // f32 partial tile row stride
 
 
 struct Smem {
-  uint32_t bbuf[2];             // staged activation pieces (128-byte swizzle), double buffered
+  uint32_t bbuf0, bbuf_stride;  // staged activation pieces (128-byte swizzle), double buffered
   float *cs_ptr;
   float *stat_mu, *stat_rs;     // [kMaxT]
 };
@@ -84,41 +84,68 @@ __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
   }
 }
 
-// Stage A[t][k0 .. k0 + kp) for all 16 * MT rows as bf16 hi / lo.
-// Stage activation columns k0 .. k0 + kp as the MMA's B operand: rows 0 .. 16MT-1
-// hold the bf16 hi parts, rows 16MT .. 32MT-1 the lo parts, one 64-column chunk
-// after another (each chunk 32MT rows x 128 bytes, 128-byte swizzle).
+// Staging of activation columns k0 .. k0 + kp as the MMA's B operand: rows
+// 0 .. 16MT-1 hold the bf16 hi parts, rows 16MT .. 32MT-1 the lo parts, one
+// 64-column chunk after another (each chunk 32MT rows x 128 bytes, 128-byte
+// swizzle).  Two phases, so that a piece's global loads (activations and norm
+// weights) are in flight while the row statistics are formed: stage_load
+// issues them into registers, stage_store transforms and stores.
 template <int MT>
-__device__ void stage_a(const GemvArgs &a, const Smem &s, uint32_t dst, int T, int m0, int k0, int kp) {
-  constexpr int rows = 16 * MT;
-  constexpr int tpr = kWorkers / rows;        // threads per activation row (16 or 8)
-  constexpr int kMaxQ = 256 / 4 / tpr;        // quads per thread for a 256-column piece
+struct StageRegs {
+  static constexpr int rows = 16 * MT;
+  static constexpr int tpr = kWorkers / rows;   // threads per activation row (16 or 8)
+  static constexpr int kMaxQ = 256 / 4 / tpr;   // quads per thread for a 256-column piece
+  float4 xv[kMaxQ];
+  uint2 wv[kMaxQ];                              // 4 bf16 norm weights per quad (A_RMS, A_RMS2 first)
+  uint2 wv2[kMaxQ];                             // A_RMS2 second weights
+};
+
+template <int MT>
+__device__ __forceinline__ void stage_load(const GemvArgs &a, int T, int m0, int k0, int kp, StageRegs<MT> &g) {
+  using R = StageRegs<MT>;
   const int tid = wtid();
-  const int t = tid / tpr, q0 = tid % tpr;    // constant divisors
-  const int nq = (kp >> 2) / tpr;             // kp is a multiple of 64
+  const int t = tid / R::tpr, q0 = tid % R::tpr;   // constant divisors
+  const int nq = (kp >> 2) / R::tpr;               // kp is a multiple of 64
   const float *X = a.x_from_sp ? a.sp->feats : a.X;
-  const __nv_bfloat16 *nw = a.nw;
-  const __nv_bfloat16 *nw2 = a.nw2;
-  if (a.amode == A_RMS2 && a.nw_rows > 0) nw2 += (size_t)(m0 / a.nw_rows) * a.K;
   const bool second = a.split > 0 && t >= a.split;
   const bool load = t < T && a.amode != A_ROW_Q8 && a.amode != A_ROW_BF16;
   const float *xr = second ? a.X2 + (size_t)(t - a.split) * a.ldx : X + (size_t)t * a.ldx;
-  // every load of this thread is in flight before the first one is used
-  float4 xv[kMaxQ];
+  const __nv_bfloat16 *wv = (a.amode == A_RMS && second) ? a.nw_alt : a.nw;
+  const __nv_bfloat16 *nw2 = a.nw2;
+  if (a.amode == A_RMS2 && a.nw_rows > 0) nw2 += (size_t)(m0 / a.nw_rows) * a.K;
+  const bool wload = t < T && (a.amode == A_RMS || a.amode == A_RMS2);
 #pragma unroll
-  for (int j = 0; j < kMaxQ; ++j) {
-    xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (j < nq && load) xv[j] = __ldcg(reinterpret_cast<const float4 *>(xr + k0 + 4 * (q0 + tpr * j)));
+  for (int j = 0; j < R::kMaxQ; ++j) {
+    g.xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    g.wv[j] = make_uint2(0u, 0u);
+    g.wv2[j] = make_uint2(0u, 0u);
+    const int k = k0 + 4 * (q0 + R::tpr * j);
+    if (j < nq && load) g.xv[j] = __ldcg(reinterpret_cast<const float4 *>(xr + k));
+    if (j < nq && wload) {
+      g.wv[j] = *reinterpret_cast<const uint2 *>(wv + k);
+      if (a.amode == A_RMS2) g.wv2[j] = *reinterpret_cast<const uint2 *>(nw2 + k);
+    }
   }
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int MT>
+__device__ __forceinline__ void stage_store(const GemvArgs &a, const Smem &s, uint32_t dst, int T, int k0, int kp,
+                                            const StageRegs<MT> &g) {
+  using R = StageRegs<MT>;
+  const int tid = wtid();
+  const int t = tid / R::tpr, q0 = tid % R::tpr;
+  const int nq = (kp >> 2) / R::tpr;
   float mu = 0.f, rs = 1.f;
   if (t < T) { mu = s.stat_mu[t]; rs = s.stat_rs[t]; }
-  const __nv_bfloat16 *wv = second ? a.nw_alt : nw;
 #pragma unroll
-  for (int j = 0; j < kMaxQ; ++j) {
+  for (int j = 0; j < R::kMaxQ; ++j) {
     if (j >= nq) break;
-    const int kq = 4 * (q0 + tpr * j);   // column inside the piece
+    const int kq = 4 * (q0 + R::tpr * j);   // column inside the piece
     const int k = k0 + kq;
-    float v[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+    float v[4] = {g.xv[j].x, g.xv[j].y, g.xv[j].z, g.xv[j].w};
     if (t < T) {
       if (a.amode == A_ROW_Q8 || a.amode == A_ROW_BF16) {
         v[0] = v[1] = v[2] = v[3] = 0.f;
@@ -135,18 +162,18 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, uint32_t dst, int T, i
           } else {
             const uint8_t *base = a.tb + chunk * 16384;
             const uint2 u = *reinterpret_cast<const uint2 *>(base + w_slot(rr, kk));
-            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-            v[0] = __low2float(p0); v[1] = __high2float(p0); v[2] = __low2float(p1); v[3] = __high2float(p1);
+            v[0] = bf_lo(u.x); v[1] = bf_hi(u.x); v[2] = bf_lo(u.y); v[3] = bf_hi(u.y);
           }
         }
       } else if (a.amode == A_RMS) {
+        const float w[4] = {bf_lo(g.wv[j].x), bf_hi(g.wv[j].x), bf_lo(g.wv[j].y), bf_hi(g.wv[j].y)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = v[e] * rs * __bfloat162float(wv[k + e]);
+        for (int e = 0; e < 4; ++e) v[e] = v[e] * rs * w[e];
       } else if (a.amode == A_RMS2) {
+        const float w[4] = {bf_lo(g.wv[j].x), bf_hi(g.wv[j].x), bf_lo(g.wv[j].y), bf_hi(g.wv[j].y)};
+        const float w2[4] = {bf_lo(g.wv2[j].x), bf_hi(g.wv2[j].x), bf_lo(g.wv2[j].y), bf_hi(g.wv2[j].y)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          v[e] = (v[e] * mu * __bfloat162float(nw[k + e])) * rs * __bfloat162float(nw2[k + e]);
+        for (int e = 0; e < 4; ++e) v[e] = (v[e] * mu * w[e]) * rs * w2[e];
       } else if (a.amode == A_LNMOD) {
         const float4 sc = *reinterpret_cast<const float4 *>(a.sc + k);
         const float4 sh = *reinterpret_cast<const float4 *>(a.sh + k);
@@ -162,7 +189,7 @@ __device__ void stage_a(const GemvArgs &a, const Smem &s, uint32_t dst, int T, i
     const uint32_t cbase = dst + (uint32_t)(kq >> 6) * (32 * MT * 128);
     const int kk = kq & 63;
     asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(t, kk)), "r"(h01), "r"(h23));
-    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(rows + t, kk)), "r"(l01), "r"(l23));
+    asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(cbase + sw128(R::rows + t, kk)), "r"(l01), "r"(l23));
   }
 }
 
@@ -391,8 +418,8 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
   const int UB = U * kStageBytes;
   const int units = nchunks / U;
   Smem s;
-  s.bbuf[0] = ring + S * UB;
-  s.bbuf[1] = s.bbuf[0] + cpp * BCH;
+  s.bbuf0 = ring + S * UB;
+  s.bbuf_stride = cpp * BCH;
   s.cs_ptr = reinterpret_cast<float *>(gbase + S * UB + 2 * cpp * BCH);
   s.stat_mu = s.cs_ptr + 16 * MT * kCsStride;
   s.stat_rs = s.stat_mu + kMaxT;
@@ -451,7 +478,7 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
       if (uo == 0 && !mbar_wait_warp(full(st), fpar, a.err)) break;
       tc_fence_after();
       const uint64_t ad = umma_desc_sw128(ring + st * UB + uo * kStageBytes);
-      const uint64_t bd = umma_desc_sw128(s.bbuf[pb] + pc * BCH);
+      const uint64_t bd = umma_desc_sw128(s.bbuf0 + pb * s.bbuf_stride + pc * BCH);
 #pragma unroll
       for (int kk = 0; kk < kChunk / 16; ++kk) umma_ss_elect(tmem, ad + 2 * kk, bd + 2 * kk, IDESC, (c | kk) ? 1u : 0u);
       if (uo == U - 1) umma_commit_elect(empty(st));
@@ -462,13 +489,18 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
     umma_commit_elect(accfull);
   } else {
     // workers: stage the activation pieces, then read the accumulator
-    load_row_stats(a, T, s.stat_mu, s.stat_rs);
-    named_sync(1, kWorkers);
     for (int p = 0; p < npieces; ++p) {
       const int pb = p & 1;
       if (p >= 2) mbar_wait_bounded(bempty0 + 8 * pb, ((p - 2) >> 1) & 1, a.err);
       const int kp = min(a.Kp, a.Kc - p * a.Kp);
-      stage_a<MT>(a, s, s.bbuf[pb], T, m0, k_begin + p * a.Kp, kp);
+      StageRegs<MT> g;
+      stage_load<MT>(a, T, m0, k_begin + p * a.Kp, kp, g);
+      if (p == 0) {
+        // the row statistics while the first piece's loads are in flight
+        load_row_stats(a, T, s.stat_mu, s.stat_rs);
+        named_sync(1, kWorkers);
+      }
+      stage_store<MT>(a, s, s.bbuf0 + pb * s.bbuf_stride, T, k_begin + p * a.Kp, kp, g);
       fence_proxy_async();
       named_sync(1, kWorkers);
       if (wtid() == 0) mbar_arrive(bfull0 + 8 * pb);
