@@ -361,27 +361,32 @@ __device__ void self_attention_head(const GemvArgs &a, int head, int T, float *s
     *reinterpret_cast<float4 *>(vv + t * ks + d) = v;
   }
   __syncthreads();
-  // one warp per query row: lane l owns dims 4l .. 4l+3 (lanes beyond hd/4 hold zeros)
+  // one warp per query row.  Scores: lane j < T forms q_t . k_j over the head's dims
+  // (no cross-lane sums); softmax over the lanes; output: lane l owns dims 4l .. 4l+3
+  // and gathers p_j from lane j.
   const int lane = threadIdx.x & 31, w = wtid() >> 5;
   const bool on = lane < q4;
   for (int t = w; consumer && t < T; t += kThreads / 32) {
-    const float4 q = on ? *reinterpret_cast<const float4 *>(qq + t * ks + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float sc[kMaxT];
-    float mx = -INFINITY;
-    for (int j = 0; j < T; ++j) {
-      const float4 k = on ? *reinterpret_cast<const float4 *>(kk + j * ks + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float s = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w) * a.attn_scale;
-      sc[j] = s;
-      mx = fmaxf(mx, s);
+    const float *qrow = qq + t * ks;
+    const float *krow = kk + (lane < T ? lane : 0) * ks;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    for (int d = 0; d < hd; d += 4) {
+      const float4 q = *reinterpret_cast<const float4 *>(qrow + d);
+      const float4 k = *reinterpret_cast<const float4 *>(krow + d);
+      s0 += q.x * k.x; s1 += q.y * k.y; s2 += q.z * k.z; s3 += q.w * k.w;
     }
-    float den = 0.f;
+    const float sc = lane < T ? ((s0 + s1) + (s2 + s3)) * a.attn_scale : -INFINITY;
+    float mx = sc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float p = lane < T ? __expf(sc - mx) : 0.f;
+    const float den = warp_sum(p);
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < T; ++j) {
-      const float p = __expf(sc[j] - mx);
-      den += p;
+      const float pj = __shfl_sync(0xffffffffu, p, j);
       if (on) {
         const float4 v = *reinterpret_cast<const float4 *>(vv + j * ks + 4 * lane);
-        o.x += p * v.x; o.y += p * v.y; o.z += p * v.z; o.w += p * v.w;
+        o.x += pj * v.x; o.y += pj * v.y; o.z += pj * v.z; o.w += pj * v.w;
       }
     }
     if (on) {
