@@ -94,10 +94,13 @@ template <int MT>
 struct StageRegs {
   static constexpr int rows = 16 * MT;
   static constexpr int tpr = kWorkers / rows;   // threads per activation row (16 or 8)
-  static constexpr int kMaxQ = 256 / 4 / tpr;   // quads per thread for a 256-column piece
+  static constexpr int kMaxKp = MT == 1 ? 256 : 128;   // piece width (17..32 rows: 128, see the launcher)
+  static constexpr int kMaxQ = kMaxKp / 4 / tpr;       // quads per thread for a full piece
   float4 xv[kMaxQ];
-  uint2 wv[kMaxQ];                              // 4 bf16 norm weights per quad (A_RMS, A_RMS2 first)
-  uint2 wv2[kMaxQ];                             // A_RMS2 second weights
+  // per-column operands of the transform, loaded with the activations:
+  // A_RMS: p0.xy = 4 bf16 norm weights; A_RMS2: p0.xy, p0.zw = both weight quads;
+  // A_LNMOD: p0 = scale, p1 = shift
+  float4 p0[kMaxQ], p1[kMaxQ];
 };
 
 template <int MT>
@@ -114,16 +117,23 @@ __device__ __forceinline__ void stage_load(const GemvArgs &a, int T, int m0, int
   const __nv_bfloat16 *nw2 = a.nw2;
   if (a.amode == A_RMS2 && a.nw_rows > 0) nw2 += (size_t)(m0 / a.nw_rows) * a.K;
   const bool wload = t < T && (a.amode == A_RMS || a.amode == A_RMS2);
+  const bool mload = t < T && a.amode == A_LNMOD;
 #pragma unroll
   for (int j = 0; j < R::kMaxQ; ++j) {
     g.xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    g.wv[j] = make_uint2(0u, 0u);
-    g.wv2[j] = make_uint2(0u, 0u);
+    g.p0[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    g.p1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     const int k = k0 + 4 * (q0 + R::tpr * j);
     if (j < nq && load) g.xv[j] = __ldcg(reinterpret_cast<const float4 *>(xr + k));
     if (j < nq && wload) {
-      g.wv[j] = *reinterpret_cast<const uint2 *>(wv + k);
-      if (a.amode == A_RMS2) g.wv2[j] = *reinterpret_cast<const uint2 *>(nw2 + k);
+      const uint2 w = *reinterpret_cast<const uint2 *>(wv + k);
+      uint2 w2 = make_uint2(0u, 0u);
+      if (a.amode == A_RMS2) w2 = *reinterpret_cast<const uint2 *>(nw2 + k);
+      g.p0[j] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w2.x), __uint_as_float(w2.y));
+    }
+    if (j < nq && mload) {
+      g.p0[j] = *reinterpret_cast<const float4 *>(a.sc + k);
+      g.p1[j] = *reinterpret_cast<const float4 *>(a.sh + k);
     }
   }
 }
@@ -166,17 +176,20 @@ __device__ __forceinline__ void stage_store(const GemvArgs &a, const Smem &s, ui
           }
         }
       } else if (a.amode == A_RMS) {
-        const float w[4] = {bf_lo(g.wv[j].x), bf_hi(g.wv[j].x), bf_lo(g.wv[j].y), bf_hi(g.wv[j].y)};
+        const uint32_t w01 = __float_as_uint(g.p0[j].x), w23 = __float_as_uint(g.p0[j].y);
+        const float w[4] = {bf_lo(w01), bf_hi(w01), bf_lo(w23), bf_hi(w23)};
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = v[e] * rs * w[e];
       } else if (a.amode == A_RMS2) {
-        const float w[4] = {bf_lo(g.wv[j].x), bf_hi(g.wv[j].x), bf_lo(g.wv[j].y), bf_hi(g.wv[j].y)};
-        const float w2[4] = {bf_lo(g.wv2[j].x), bf_hi(g.wv2[j].x), bf_lo(g.wv2[j].y), bf_hi(g.wv2[j].y)};
+        const uint32_t w01 = __float_as_uint(g.p0[j].x), w23 = __float_as_uint(g.p0[j].y);
+        const uint32_t u01 = __float_as_uint(g.p0[j].z), u23 = __float_as_uint(g.p0[j].w);
+        const float w[4] = {bf_lo(w01), bf_hi(w01), bf_lo(w23), bf_hi(w23)};
+        const float w2[4] = {bf_lo(u01), bf_hi(u01), bf_lo(u23), bf_hi(u23)};
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = (v[e] * mu * w[e]) * rs * w2[e];
       } else if (a.amode == A_LNMOD) {
-        const float4 sc = *reinterpret_cast<const float4 *>(a.sc + k);
-        const float4 sh = *reinterpret_cast<const float4 *>(a.sh + k);
+        const float4 sc = g.p0[j];
+        const float4 sh = g.p1[j];
         v[0] = (v[0] - mu) * rs * (1.f + sc.x) + sh.x;
         v[1] = (v[1] - mu) * rs * (1.f + sc.y) + sh.y;
         v[2] = (v[2] - mu) * rs * (1.f + sc.z) + sh.z;
@@ -205,6 +218,8 @@ __device__ __forceinline__ int row_pos(const GemvArgs &a, int t) {
 struct EpiIn {
   float4 r, g;
   float b[4];
+  uint2 nw;          // E_SEGS: the four per-head norm weights of this lane's rows (bf16)
+  float2 cs0, cs1;   // E_SEGS: the rotation (cos, sin) of the two pairs, at the row's position
 };
 __device__ __forceinline__ void epilogue_load(const GemvArgs &a, int t, int m0, EpiIn &in) {
   const int mrow = m0 + 4 * (threadIdx.x & 31);
@@ -213,7 +228,22 @@ __device__ __forceinline__ void epilogue_load(const GemvArgs &a, int t, int m0, 
   in.g = make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
   for (int e = 0; e < 4; ++e) in.b[e] = 0.f;
+  in.nw = make_uint2(0u, 0u);
+  in.cs0 = in.cs1 = make_float2(1.f, 0.f);
   if (!live) return;
+  if (a.emode == E_SEGS) {
+    const int seg = m0 / a.seg_rows;
+    const SegDesc &sd = a.segs[seg];
+    const int d0 = (mrow - seg * a.seg_rows) % a.hd;
+    if (sd.norm_w) {
+      in.nw = *reinterpret_cast<const uint2 *>(sd.norm_w + d0);
+      if (sd.rope) {
+        const int p = row_pos(a, t);
+        in.cs0 = a.rope[(size_t)p * (a.hd >> 1) + (d0 >> 1)];
+        in.cs1 = a.rope[(size_t)p * (a.hd >> 1) + (d0 >> 1) + 1];
+      }
+    }
+  }
   if (a.bias) {
     const uint2 u = *reinterpret_cast<const uint2 *>(a.bias + mrow);
     const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
@@ -310,13 +340,12 @@ __device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], i
         float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
         ss = group_sum(ss, lanes_per_head);
         const float r = rsqrtf(ss / (float)hd + a.qk_eps);
-        const int d0 = mseg % hd;
+        const float w[4] = {__uint_as_float(in.nw.x << 16), __uint_as_float(in.nw.x & 0xffff0000u),
+                            __uint_as_float(in.nw.y << 16), __uint_as_float(in.nw.y & 0xffff0000u)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = v[e] * r * __bfloat162float(sd.norm_w[d0 + e]);
+        for (int e = 0; e < 4; ++e) v[e] = v[e] * r * w[e];
         if (sd.rope) {
-          const int p = row_pos(a, t);
-          const float2 cs0 = a.rope[(size_t)p * (hd >> 1) + (d0 >> 1)];
-          const float2 cs1 = a.rope[(size_t)p * (hd >> 1) + (d0 >> 1) + 1];
+          const float2 cs0 = in.cs0, cs1 = in.cs1;
           const float x0 = v[0], x1 = v[1], x2 = v[2], x3 = v[3];
           v[0] = x0 * cs0.x - x1 * cs0.y;
           v[1] = x1 * cs0.x + x0 * cs0.y;
@@ -640,6 +669,7 @@ size_t gemv_smem_bytes(const GemvArgs &a, int mt) {
 
 cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t st, bool pdl) {
   const int mt = (a.T_const > 0 && a.T_const <= 16) ? 1 : 2;
+  if (a.Kp > (mt == 1 ? 256 : 128) || a.Kp % kChunk != 0) return cudaErrorInvalidValue;   // the staging registers hold one piece
   const size_t smem = gemv_smem_bytes(a, mt);
   const int U = gemv_unit(a, mt);
   const int S = gemv_stages(a, mt) / U;
