@@ -49,7 +49,11 @@ struct Smem {
   float *stat_mu, *stat_rs;     // [kMaxT]
 };
 
-// Row statistics of the input rows (sum over the producer's tiles, in double).
+// Row statistics of the input rows: the producer's per-tile partial sums added
+// up, in f32.  (FP64 runs at a small fraction of the f32 rate on this GPU: the
+// same arithmetic in double, one warp deep, cost about a microsecond on the
+// critical path of every normalised GEMV.  The partials are f32 already; the
+// sum of at most a few dozen of them loses ~1e-6 relative.)
 __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
   const int t = wtid();
   if (t < kMaxT) {
@@ -58,25 +62,31 @@ __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
       const bool second = a.split > 0 && t >= a.split;
       const int ts = a.st_bcast ? 0 : (second ? t - a.split : t);
       const float2 *stp = second ? a.st2 : a.st;
-      double s1 = 0.0, s2 = 0.0;
-      for (int i = 0; i < a.st_tiles; ++i) {
-        const float2 v = __ldcg(stp + i * kMaxT + ts);
-        s1 += v.x;
-        s2 += v.y;
+      float s1a = 0.f, s2a = 0.f, s1b = 0.f, s2b = 0.f;   // two chains: independent loads, shorter adds
+      int i = 0;
+      for (; i + 1 < a.st_tiles; i += 2) {
+        const float2 v0 = __ldcg(stp + i * kMaxT + ts);
+        const float2 v1 = __ldcg(stp + (i + 1) * kMaxT + ts);
+        s1a += v0.x; s2a += v0.y;
+        s1b += v1.x; s2b += v1.y;
       }
+      if (i < a.st_tiles) {
+        const float2 v0 = __ldcg(stp + i * kMaxT + ts);
+        s1a += v0.x; s2a += v0.y;
+      }
+      const float s1 = s1a + s1b, s2 = s2a + s2b;
       if (a.amode == A_RMS) {
-        r = (float)(1.0 / sqrt(s2 * a.inv_n + (double)a.eps));
+        r = rsqrtf(s2 * a.inv_n + a.eps);
       } else if (a.amode == A_RMS2) {
-        const double r1 = 1.0 / sqrt(s1 * a.inv_n + (double)a.eps);
-        const double r2 = 1.0 / sqrt(r1 * r1 * s2 * a.inv_n + (double)a.eps);
-        m = (float)r1;   // A_RMS2 keeps r1 in the mean slot
-        r = (float)r2;
+        const float r1 = rsqrtf(s1 * a.inv_n + a.eps);
+        const float r2 = rsqrtf(r1 * r1 * s2 * a.inv_n + a.eps);
+        m = r1;   // A_RMS2 keeps r1 in the mean slot
+        r = r2;
       } else {
-        const double mean = s1 * a.inv_n;
-        double var = s2 * a.inv_n - mean * mean;
-        if (var < 0.0) var = 0.0;
-        m = (float)mean;
-        r = (float)(1.0 / sqrt(var + (double)a.eps));
+        const float mean = s1 * a.inv_n;
+        const float var = fmaxf(s2 * a.inv_n - mean * mean, 0.f);
+        m = mean;
+        r = rsqrtf(var + a.eps);
       }
     }
     mu[t] = m;
