@@ -91,14 +91,27 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     cp_async_commit();   // one group per stage, as the main loop expects
   }
 
-  // queries -> f16 hi / lo (rows >= T are zero)
-  for (int i = threadIdx.x; i < 16 * HD; i += kThreads) {
-    const int t = i / HD, d = i - t * HD;
-    float x = t < T ? __ldcg(a.Q + (size_t)t * a.ldq + head * HD + d) : 0.f;
-    __half h, l;
-    split_f16(x, h, l);
-    reinterpret_cast<__half *>(smem + (qhi - sbase))[t * QS + d] = h;
-    reinterpret_cast<__half *>(smem + (qlo - sbase))[t * QS + d] = l;
+  // queries -> f16 hi / lo (rows >= T are zero): every load in flight before the first is used
+  {
+    constexpr int Q4 = 16 * HD / 4 / kThreads;   // float4 per thread
+    float4 xq[Q4];
+#pragma unroll
+    for (int j = 0; j < Q4; ++j) {
+      const int i = threadIdx.x + j * kThreads;
+      const int t = i / (HD / 4), d = 4 * (i - t * (HD / 4));
+      xq[j] = t < T ? __ldcg(reinterpret_cast<const float4 *>(a.Q + (size_t)t * a.ldq + head * HD + d))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < Q4; ++j) {
+      const int i = threadIdx.x + j * kThreads;
+      const int t = i / (HD / 4), d = 4 * (i - t * (HD / 4));
+      uint2 hv, lv;
+      split2_f16(xq[j].x, xq[j].y, hv.x, lv.x);
+      split2_f16(xq[j].z, xq[j].w, hv.y, lv.y);
+      *reinterpret_cast<uint2 *>(smem + (qhi - sbase) + (size_t)(t * QS + d) * 2) = hv;
+      *reinterpret_cast<uint2 *>(smem + (qlo - sbase) + (size_t)(t * QS + d) * 2) = lv;
+    }
   }
 
   float o[NT][4];
