@@ -275,21 +275,50 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   const int rank = (int)cluster.block_rank();
   const int ns = a.splits;
   constexpr int PL = HD / 32;  // values per lane
+  constexpr int kBatch = 8;   // up to this many ranks: every remote load in flight before any is used
   for (int t = rank + ns * w; t < T; t += ns * (kThreads / 32)) {
     float M = -INFINITY;
-    for (int r = 0; r < ns; ++r) M = fmaxf(M, cluster.map_shared_rank(cml, r)[t * 2]);
     float lsum = 0.f;
     float acc[PL];
 #pragma unroll
     for (int e = 0; e < PL; ++e) acc[e] = 0.f;
-    for (int r = 0; r < ns; ++r) {
-      const float *rml = cluster.map_shared_rank(cml, r);
-      const float mr = rml[t * 2];
-      const float f = mr == -INFINITY ? 0.f : exp2f(mr - M);
-      lsum += f * rml[t * 2 + 1];
-      const float *ro = cluster.map_shared_rank(co, r) + t * HD + PL * lane;
+    if (ns <= kBatch) {
+      float mr[kBatch], lr[kBatch], ov[kBatch][PL];
 #pragma unroll
-      for (int e = 0; e < PL; ++e) acc[e] += f * ro[e];
+      for (int r = 0; r < kBatch; ++r) {
+        mr[r] = -INFINITY;
+        lr[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) ov[r][e] = 0.f;
+        if (r < ns) {
+          const float *rml = cluster.map_shared_rank(cml, r);
+          const float *ro = cluster.map_shared_rank(co, r) + t * HD + PL * lane;
+          mr[r] = rml[t * 2];
+          lr[r] = rml[t * 2 + 1];
+#pragma unroll
+          for (int e = 0; e < PL; ++e) ov[r][e] = ro[e];
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) M = fmaxf(M, mr[r]);
+#pragma unroll
+      for (int r = 0; r < kBatch; ++r) {   // rank order
+        const float f = mr[r] == -INFINITY ? 0.f : exp2f(mr[r] - M);
+        lsum += f * lr[r];
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[e] += f * ov[r][e];
+      }
+    } else {
+      for (int r = 0; r < ns; ++r) M = fmaxf(M, cluster.map_shared_rank(cml, r)[t * 2]);
+      for (int r = 0; r < ns; ++r) {
+        const float *rml = cluster.map_shared_rank(cml, r);
+        const float mr = rml[t * 2];
+        const float f = mr == -INFINITY ? 0.f : exp2f(mr - M);
+        lsum += f * rml[t * 2 + 1];
+        const float *ro = cluster.map_shared_rank(co, r) + t * HD + PL * lane;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[e] += f * ro[e];
+      }
     }
     const float inv = 1.f / lsum;
     float *dst = a.out + (size_t)t * a.ldo + head * HD + PL * lane;

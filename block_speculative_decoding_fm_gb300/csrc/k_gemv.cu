@@ -612,15 +612,17 @@ __global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ G
   // done reading the peers' tiles (the values are summed): they may leave once everyone has arrived
   if (ks > 1) cluster_arrive_relaxed();
   if (warp >= 2) {
+    // the next unit's operands load while this unit's epilogue runs
+    EpiIn cur = pre;
 #pragma unroll
     for (int u = 0; u < kMaxUnits; ++u) {
       if (u >= nu) break;
       const int t = t0 + u * ks * (kWorkers / 32);
-      EpiIn in;
-      if (u == 0) in = pre;
-      else epilogue_load(a, t, m0, in);
+      EpiIn nxt;
+      if (u + 1 < nu) epilogue_load(a, t + ks * (kWorkers / 32), m0, nxt);
       float v[4] = {vs[u][0], vs[u][1], vs[u][2], vs[u][3]};
-      epilogue_unit(a, t, m0, v, tile, in);
+      epilogue_unit(a, t, m0, v, tile, cur);
+      cur = nxt;
     }
   }
 
