@@ -41,6 +41,7 @@ __device__ __forceinline__ int wtid() { return (int)threadIdx.x - kWorkerBase; }
 constexpr int kChunk = 64;                       // k per pipeline stage
 constexpr int kStageBytes = kTile * kChunk * 2;  // 16 KB of bf16 weights
 constexpr int kCsStride = kTile + 8;             // f32 partial tile row stride
+static_assert(kWorkers == 8 * kMaxT, "row statistics: eight worker threads per row");
 
 
 struct Smem {
@@ -50,31 +51,44 @@ struct Smem {
 };
 
 // Row statistics of the input rows: the producer's per-tile partial sums added
-// up, in f32.  (FP64 runs at a small fraction of the f32 rate on this GPU: the
+// up, in f32, by all worker threads.  (FP64 runs at a small fraction of the f32 rate on this GPU: the
 // same arithmetic in double, one warp deep, cost about a microsecond on the
 // critical path of every normalised GEMV.  The partials are f32 already; the
 // sum of at most a few dozen of them loses ~1e-6 relative.)
 __device__ void load_row_stats(const GemvArgs &a, int T, float *mu, float *rs) {
-  const int t = wtid();
-  if (t < kMaxT) {
+  // eight threads per row (kWorkers = 8 * kMaxT): thread j takes tiles j, j + 8, ...,
+  // all its loads in flight at once; the row's eight partial sums meet by shuffles
+  const int tid = wtid();
+  const int t = tid >> 3, j = tid & 7;
+  const bool active =
+      t < T && (a.amode == A_RMS || a.amode == A_LNMOD || a.amode == A_RMS2);
+  float s1 = 0.f, s2 = 0.f;
+  if (active) {
+    const bool second = a.split > 0 && t >= a.split;
+    const int ts = a.st_bcast ? 0 : (second ? t - a.split : t);
+    const float2 *stp = second ? a.st2 : a.st;
+    const int n = a.st_tiles;
+    float2 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = j + 8 * u;
+      v[u] = i < n ? __ldcg(stp + i * kMaxT + ts) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) { s1 += v[u].x; s2 += v[u].y; }
+    for (int i = j + 32; i < n; i += 8) {
+      const float2 w = __ldcg(stp + i * kMaxT + ts);
+      s1 += w.x; s2 += w.y;
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+  }
+  if (j == 0 && t < kMaxT) {
     float m = 0.f, r = 1.f;
-    if (t < T && (a.amode == A_RMS || a.amode == A_LNMOD || a.amode == A_RMS2)) {
-      const bool second = a.split > 0 && t >= a.split;
-      const int ts = a.st_bcast ? 0 : (second ? t - a.split : t);
-      const float2 *stp = second ? a.st2 : a.st;
-      float s1a = 0.f, s2a = 0.f, s1b = 0.f, s2b = 0.f;   // two chains: independent loads, shorter adds
-      int i = 0;
-      for (; i + 1 < a.st_tiles; i += 2) {
-        const float2 v0 = __ldcg(stp + i * kMaxT + ts);
-        const float2 v1 = __ldcg(stp + (i + 1) * kMaxT + ts);
-        s1a += v0.x; s2a += v0.y;
-        s1b += v1.x; s2b += v1.y;
-      }
-      if (i < a.st_tiles) {
-        const float2 v0 = __ldcg(stp + i * kMaxT + ts);
-        s1a += v0.x; s2a += v0.y;
-      }
-      const float s1 = s1a + s1b, s2 = s2a + s2b;
+    if (active) {
       if (a.amode == A_RMS) {
         r = rsqrtf(s2 * a.inv_n + a.eps);
       } else if (a.amode == A_RMS2) {
