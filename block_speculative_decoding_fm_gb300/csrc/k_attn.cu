@@ -333,9 +333,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
 cudaError_t launch_attn(const AttnArgs &a, int L_now, cudaStream_t st, bool pdl) {
   const int HD = a.hd;
   const size_t tile = (size_t)kKeys * HD * 2;
-  // deeper ring when each CTA streams many key tiles
+  // deeper ring when each CTA streams several key tiles (NS - 1 of them are requested
+  // before griddepcontrol.wait); three stages (~106 KB) still start beside a GEMV CTA
   const int per_cta = (L_now + a.splits - 1) / a.splits;
-  const int NS = per_cta > 4 * kKeys ? 4 : 2;
+  const int NS = per_cta > 4 * kKeys ? 4 : per_cta > kKeys ? 3 : 2;
   size_t smem = 2 * NS * tile + 2 * 16 * (HD + 32) * 2;
   const size_t merge = (size_t)4 * 16 * HD * 4 + 4 * 16 * 2 * 4 + (size_t)16 * HD * 4 + 16 * 2 * 4;
   if (merge > smem) smem = merge;
@@ -362,8 +363,8 @@ cudaError_t launch_attn(const AttnArgs &a, int L_now, cudaStream_t st, bool pdl)
     }
     return cudaLaunchKernelEx(&cfg, kern, a);
   };
-  if (HD == 128) return NS == 4 ? go(attn_kernel<128, 4>) : go(attn_kernel<128, 2>);
-  return NS == 4 ? go(attn_kernel<64, 4>) : go(attn_kernel<64, 2>);
+  if (HD == 128) return NS == 4 ? go(attn_kernel<128, 4>) : NS == 3 ? go(attn_kernel<128, 3>) : go(attn_kernel<128, 2>);
+  return NS == 4 ? go(attn_kernel<64, 4>) : NS == 3 ? go(attn_kernel<64, 3>) : go(attn_kernel<64, 2>);
 }
 
 }  // namespace fm
