@@ -156,17 +156,39 @@ __device__ void finish_argmax(const LmArgs &a, int T, bool worker, int t0, float
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (threadIdx.x < T) {
-    const int t = threadIdx.x;
+  // the last CTA: one warp per slot, the lanes take the CTAs' bests 32 apart with all
+  // their loads in flight, then a shuffle reduction (ties -> lowest index, any order)
+  const int wq = threadIdx.x >> 5, nwq = blockDim.x >> 5;
+  constexpr int kPer = 8;   // per lane in flight: grids up to 256 CTAs in one round
+  for (int t = wq; t < T; t += nwq) {
     float v = -INFINITY;
     int i = 0x7fffffff;
-    for (int b = 0; b < (int)gridDim.x; ++b) {
-      const float2 p = __ldcg(a.part + b * kMaxT + t);
-      const int pi = __float_as_int(p.y);
-      if (better(p.x, pi, v, i)) { v = p.x; i = pi; }
+    float2 p[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int b = lane + 32 * j;
+      p[j] = b < (int)gridDim.x ? __ldcg(a.part + b * kMaxT + t) : make_float2(-INFINITY, __int_as_float(0x7fffffff));
     }
-    int32_t *out = a.tokens ? a.tokens : a.sp->tokens;
-    out[t] = i == 0x7fffffff ? -1 : i;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int pi = __float_as_int(p[j].y);
+      if (better(p[j].x, pi, v, i)) { v = p[j].x; i = pi; }
+    }
+    for (int b = lane + 32 * kPer; b < (int)gridDim.x; b += 32) {
+      const float2 q = __ldcg(a.part + b * kMaxT + t);
+      const int qi = __float_as_int(q.y);
+      if (better(q.x, qi, v, i)) { v = q.x; i = qi; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+      if (better(ov, oi, v, i)) { v = ov; i = oi; }
+    }
+    if (lane == 0) {
+      int32_t *out = a.tokens ? a.tokens : a.sp->tokens;
+      out[t] = i == 0x7fffffff ? -1 : i;
+    }
   }
 }
 
