@@ -9,7 +9,8 @@
 //               A tiles and 256 x 64 B tiles (128-byte swizzle) into a 4-stage
 //               shared-memory ring guarded by mbarriers;
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 f32 accumulators) and
-//               one thread issues tcgen05.mma (kind::f16, M 128, N 256, K 16);
+//               runs the issue loop warp-wide, an elected lane issuing
+//               tcgen05.mma (kind::f16, M 128, N 256, K 16);
 //               tcgen05.commit frees ring stages and publishes accumulators;
 //   warps 2..5  read an accumulator with tcgen05.ld (one row per thread) while
 //               the next tile accumulates into the other buffer, and run the

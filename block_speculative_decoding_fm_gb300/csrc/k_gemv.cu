@@ -12,10 +12,11 @@
 //   * the activations are transformed on the way in (RMSNorm, adaLN LayerNorm
 //     modulate, a table row) and split into bf16 hi + lo, so the bf16 tensor
 //     cores see f32-accurate operands: A*W = hi*W + lo*W, f32 accumulate;
-//   * the contraction runs on the 5th-generation tensor cores: one thread
-//     issues tcgen05.mma (M = 128 weight rows, N = the hi rows then the lo rows
-//     of the activations, K = 16) from shared-memory operands in the 128-byte
-//     swizzle layout into a TMEM accumulator; worker warps read it back with
+//   * the contraction runs on the 5th-generation tensor cores: the MMA warp
+//     runs the issue loop warp-wide and an elected lane issues tcgen05.mma
+//     (M = 128 weight rows, N = the hi rows then the lo rows of the
+//     activations, K = 16) from shared-memory operands in the 128-byte swizzle
+//     layout into a TMEM accumulator; worker warps read it back with
 //     tcgen05.ld;
 //   * split-K across a thread-block cluster; the partial tiles are summed
 //     through distributed shared memory in a fixed order (deterministic);

@@ -6,22 +6,22 @@
 // the GGUF block format the MTP loader on ternary_bonsai_2_mtp.js repacks into
 // an int8 plane and a scale plane).  Here one persistent kernel streams the
 // table once and the logits never reach memory:
-//   * Y is split into hi + lo 16-bit halves and kept resident in shared memory
-//     as the B operand (N = 32: per group of 8 slots, 8 hi rows then 8 lo rows)
-//     in the tensor cores' 128-byte-swizzle K-major layout;
+//   * Y is split into hi + lo 16-bit halves (by the head GEMV's epilogue, or
+//     here) as the B operand (N = 32: per group of 8 slots, 8 hi rows then 8 lo
+//     rows) in the tensor cores' 128-byte-swizzle K-major layout, streamed with
+//     the table or kept resident in shared memory;
 //   * a producer warp streams 128-row x 64-column table chunks with 1-D bulk
 //     TMA copies into an mbarrier ring;
-//   * bf16 table: the chunk is already a swizzled K-major tile; one thread
-//     issues tcgen05.mma (M = 128 table rows) into a TMEM accumulator per tile;
-//   * Q8_0 table: converter warps turn each row's int8 block into f16 (exact)
-//     and store it into TMEM, which tcgen05.mma reads as the A operand; every
-//     32-column block has its own accumulator so its f16 scale is applied to
-//     the block's partial sums, in f32, by the same warps (one thread per table
-//     row and group of 8 slots), four chunks in flight;
-//   * each thread keeps a running (value, index) best per slot; pass two is
-//     the last CTA reducing the per-CTA bests.
+//   * bf16 table: the chunk is already a swizzled K-major tile; the MMA warp
+//     (an elected lane issuing) runs tcgen05.mma (M = 128 table rows) into a
+//     TMEM accumulator per tile;
+//   * Q8_0 table: converter warps form each weight times its block scale as an
+//     f16 value plus its exact f16 residual and store both into TMEM, which
+//     tcgen05.mma reads as the A operand, so each tile's whole K accumulates
+//     into one f32 accumulator per issuing warp;
+//   * each tile's rows keep a running (value, index) best per slot; pass two is
+//     the last CTA reducing the per-CTA bests (one warp per slot).
 #include <mutex>
-
 #include <type_traits>
 
 #include "dev_common.cuh"
