@@ -28,7 +28,7 @@ FM_DEBUG_KEEP_HIDDEN = 1
 FM_DEBUG_PROFILE = 2
 
 EXPORTS = ["fm_create", "fm_context_append", "fm_context_append_batched", "fm_draft", "fm_accept",
-           "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
+           "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_synchronize", "fm_selftest_wait_timeout", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
            "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy"]
 
 
@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fm_accept": (I32, [P, P, I32, P, P]),
         "fm_accept_batched": (I32, [P, I32, P, P, P, P, P, P]),
         "fm_lm_head_argmax_noalloc": (I32, [P, P, I32, P, P]),
+        "fm_synchronize": (I32, [P, P]),
+        "fm_selftest_wait_timeout": (I32, [P, I32, P]),
         "fm_debug_copy": (I32, [P, I32, I32, I32, I64, P, I64, P]),
         "fm_set_debug": (I32, [P, I32]),
         "fm_get_length": (I32, [P, I32, ctypes.POINTER(I32)]),
@@ -156,6 +158,7 @@ def fm_create(cfg, weights: Iterable[Tuple[str, object, int]], modulation=None, 
     c = make_config(cfg)
     h = ctypes.c_void_p()
     _check(lib.fm_create(ctypes.byref(c), arr, len(items), _ptr(mod), _stream(stream), ctypes.byref(h)))
+    h._fm_target_dim = int(cfg.target_dim)
     return h
 
 
@@ -205,7 +208,33 @@ def fm_lm_head_argmax_noalloc(h, y, tokens, stream=None) -> None:
     (n_rows <= 16); tokens: a CUDA int32 tensor [n_rows] that receives the
     argmax over the token table.  The first call on a device does a one-time
     set-up, so make it before any stream capture; overlapping calls race."""
+    import torch
+    if not (isinstance(y, torch.Tensor) and isinstance(tokens, torch.Tensor)):
+        raise ValueError("y and tokens must be torch tensors")
+    if not (y.is_cuda and tokens.is_cuda):
+        raise ValueError("y and tokens must be CUDA tensors")
+    if y.dtype != torch.float32 or tokens.dtype != torch.int32:
+        raise ValueError("y must be float32 and tokens int32")
+    if y.dim() != 2 or not y.is_contiguous() or not tokens.is_contiguous():
+        raise ValueError("y must be a contiguous [n_rows, target_dim] tensor and tokens contiguous")
+    width = getattr(h, "_fm_target_dim", None)
+    if width is not None and y.shape[1] != width:
+        raise ValueError(f"y has {y.shape[1]} columns, the drafter's target_dim is {width}")
+    if tokens.numel() < y.shape[0]:
+        raise ValueError("tokens holds fewer entries than y has rows")
     _check(load_library().fm_lm_head_argmax_noalloc(h, _ptr(y), y.shape[0], _ptr(tokens), _stream(stream)), h)
+
+
+def fm_synchronize(h, stream=None) -> None:
+    """Wait for the stream; raise FmError(FM_ERR_TIMEOUT) if a device-side
+    bounded wait gave up since the last check."""
+    _check(load_library().fm_synchronize(h, _stream(stream)), h)
+
+
+def fm_selftest_wait_timeout(h, budget_us: int, stream=None) -> None:
+    """Launch a wait that cannot complete, bounded by budget_us (the failure
+    path of the bounded waits); the next fm_synchronize reports it."""
+    _check(load_library().fm_selftest_wait_timeout(h, budget_us, _stream(stream)), h)
 
 
 def fm_debug_copy(h, what: int, seq: int, index: int, out: np.ndarray, offset: int = 0, stream=None) -> np.ndarray:

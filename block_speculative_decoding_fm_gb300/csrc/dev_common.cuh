@@ -246,7 +246,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // clock budget runs out, or when another thread already raised *err.  The
 // error word lives in global memory, so it is polled only every few thousand
 // cycles: a load per spin would delay noticing the phase by an L2 round trip.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int32_t *err) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int32_t *err,
+                                                  long long budget = kWaitBudgetCycles) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   long long next = t0 + 8192;
@@ -254,7 +255,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     const long long t = clock64();
     if (t > next) {
       if (*reinterpret_cast<volatile int32_t *>(err)) return false;
-      if (t - t0 > kWaitBudgetCycles) {
+      if (t - t0 > budget) {
         atomicExch(err, 1);
         return false;
       }

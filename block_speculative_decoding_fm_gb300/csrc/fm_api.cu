@@ -1514,6 +1514,14 @@ fm_status fm_lm_head_argmax_noalloc(fm_handle *h, const float *y_dev, int32_t n_
   h->last_launches = 0;
   if (!y_dev || !tokens_dev || n_rows < 1 || n_rows > 16)
     return fail(h, FM_ERR_INVALID_ARG, "bad lm_head arguments (n_rows must be in 1..16)");
+  // the kernel reads the rows as float4 and writes the tokens as int32
+  if (reinterpret_cast<uintptr_t>(y_dev) & 15) return fail(h, FM_ERR_INVALID_ARG, "y_dev is not 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(tokens_dev) & 3) return fail(h, FM_ERR_INVALID_ARG, "tokens_dev is not 4-byte aligned");
+  // the table and the static scratch are those of the current device: it must be the handle's
+  int cur = -1;
+  CK(cudaGetDevice(&cur));
+  if (cur != h->dev)
+    return fail(h, FM_ERR_INVALID_ARG, "the current device (%d) is not the handle's device (%d)", cur, h->dev);
   const fm_config &c = h->cfg;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LmArgs a;
@@ -1536,6 +1544,33 @@ fm_status fm_lm_head_argmax_noalloc(fm_handle *h, const float *y_dev, int32_t n_
   CK(lmhead_static_scratch(grid, &a.part, &a.ticket, s));
   CK(launch_lmhead(a, grid, s, false));
   ++h->last_launches;
+  return FM_OK;
+}
+
+fm_status fm_synchronize(fm_handle *h, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t flag = 0;
+  CK(cudaMemcpyAsync(&flag, h->dev_err, 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  if (flag) {
+    CK(cudaMemsetAsync(h->dev_err, 0, 4, s));
+    CK(cudaStreamSynchronize(s));
+    return fail(h, FM_ERR_TIMEOUT, "a device-side bounded wait gave up; the outputs of the calls since the last check "
+                                   "are undefined");
+  }
+  return FM_OK;
+}
+
+fm_status fm_selftest_wait_timeout(fm_handle *h, int32_t budget_us, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  if (budget_us < 1 || budget_us > 1000000) return fail(h, FM_ERR_INVALID_ARG, "budget_us outside [1, 1000000]");
+  int khz = 0;
+  CK(cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, h->dev));
+  if (khz <= 0) khz = 2000000;
+  const long long cycles = (long long)budget_us * (khz / 1000);
+  CK(launch_wait_selftest(h->dev_err, cycles, static_cast<cudaStream_t>(stream)));
+  h->last_launches = 1;
   return FM_OK;
 }
 

@@ -72,7 +72,7 @@ struct GemvArgs {
   const float *X;          // input rows X[t * ldx + k] (ldx 0 = one row broadcast)
   int32_t ldx;
   int32_t x_from_sp;       // X = sp->feats
-  const float2 *st;        // input row stats: st[i * kMaxT + t] = (sum, sumsq), i < st_tiles
+  const float2 *st;        // input row stats: st[i * kMaxT + t] = (mean, M2) of tile i (128 columns), i < st_tiles
   int32_t st_tiles;
   int32_t st_bcast;        // stats of row 0 serve every row
   const __nv_bfloat16 *nw; // RMS weight (A_RMS, first weight of A_RMS2)
@@ -96,7 +96,7 @@ struct GemvArgs {
   int32_t ldy;
   uint8_t *ylm;               // E_STORE: also write Y as the lm_head operand (kLmYChunk layout), or null
   int32_t ylm_f16;            // 1: f16 hi/lo halves (Q8_0 table), 0: bf16
-  float2 *out_st;             // [M / 128][kMaxT] (sum, sumsq) of the stored rows, or null
+  float2 *out_st;             // [M / 128][kMaxT] per-tile (mean, M2) of the stored rows, or null
   const __nv_bfloat16 *st_w;  // if set, out_st holds (sum v^2, sum (v st_w)^2) instead
   const float *gate;          // E_RESID gate [M] (null = 1)
   const float *R;             // E_RESID residual source R[t * ldr + m]
@@ -182,6 +182,7 @@ cudaError_t launch_block_consts(const __nv_bfloat16 *mask_emb, const __nv_bfloat
 cudaError_t launch_row_stats(const float *x, int32_t rows, int32_t d, float2 *st, cudaStream_t s);
 cudaError_t launch_accept(int32_t n, int32_t block, const int32_t *draft, const int32_t *target,
                           const int32_t *k, int32_t *acc, int32_t *bonus, cudaStream_t s);
+cudaError_t launch_wait_selftest(int32_t *err, long long budget_cycles, cudaStream_t s);
 cudaError_t launch_fill_f32(float *p, size_t n, float v, cudaStream_t s);
 // [M][K] bf16 row-major -> GEMV tile layout (zero rows past M)
 cudaError_t launch_tile_weights(const __nv_bfloat16 *src, int32_t M, int32_t K, uint8_t *dst, cudaStream_t s);

@@ -100,19 +100,38 @@ __global__ void block_consts_kernel(const __nv_bfloat16 *mask_emb, const __nv_bf
   out[i] = j == 0 ? 0.f : __bfloat162float(mask_emb[(size_t)(j - 1) * d + k]) + __bfloat162float(block_pos[i]);
 }
 
-// (sum, sumsq) of each row over each 128-column tile: st[tile * kMaxT + row]
+// (mean, M2) of each row over each 128-column tile, two-pass (M2 = the sum of
+// squared deviations from the tile mean): st[tile * kMaxT + row].  Consumers
+// combine the tiles with the pairwise update of Chan, Golub and LeVeque.
 __global__ void row_stats_kernel(const float *x, int rows, int d, float2 *st) {
   const int tile = blockIdx.x, row = blockIdx.y;
   const int lane = threadIdx.x;
-  float s1 = 0.f, s2 = 0.f;
-  for (int c = tile * kTile + lane; c < min(d, (tile + 1) * kTile); c += 32) {
-    const float v = x[(size_t)row * d + c];
-    s1 += v;
-    s2 += v * v;
+  const int c0 = tile * kTile, c1 = min(d, (tile + 1) * kTile);
+  float s = 0.f;
+  for (int c = c0 + lane; c < c1; c += 32) s += x[(size_t)row * d + c];
+  const float mean = warp_sum(s) / (float)(c1 - c0);
+  float q = 0.f;
+  for (int c = c0 + lane; c < c1; c += 32) {
+    const float e = x[(size_t)row * d + c] - mean;
+    q += e * e;
   }
-  s1 = warp_sum(s1);
-  s2 = warp_sum(s2);
-  if (lane == 0 && row < rows) st[tile * kMaxT + row] = make_float2(s1, s2);
+  q = warp_sum(q);
+  if (lane == 0 && row < rows) st[tile * kMaxT + row] = make_float2(mean, q);
+}
+
+// The failure path of the bounded waits: one thread waits on an mbarrier phase
+// that nothing completes, with a short budget; the wait gives up, raises the
+// error word and the kernel returns (nothing hangs, nothing faults).
+__global__ void wait_selftest_kernel(int32_t *err, long long budget_cycles) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(b, 0, err, budget_cycles);
+  __syncthreads();
 }
 
 __global__ void accept_kernel(int n, int block, const int32_t *draft, const int32_t *target, const int32_t *k,
@@ -230,6 +249,11 @@ cudaError_t launch_tile_weights(const __nv_bfloat16 *src, int32_t M, int32_t K, 
 cudaError_t launch_fill_f32(float *p, size_t n, float v, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   fill_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, n, v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int32_t *err, long long budget_cycles, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(err, budget_cycles);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,8 @@
  *     and returns an fm_status; nothing aborts and no C++ exception crosses the
  *     ABI.  On failure fm_last_error(h) holds a one-line reason.
  *   - All device work is ordered on the given stream; no call synchronises the
- *     host except fm_debug_copy (it copies to host memory) and fm_create.
+ *     host except fm_debug_copy (it copies to host memory), fm_synchronize and
+ *     fm_create.
  *   - A handle is not thread-safe: one host thread at a time per handle.
  */
 #ifndef FM_H_
@@ -144,7 +145,9 @@ FM_API fm_status fm_context_append(fm_handle *h, int32_t seq, const float *feats
 
 /*
  * fm_context_append_batched -- fm_context_append for several sequences in one
- * pass (the rows of all sequences share each weight read).  feats_dev holds
+ * call.  Dense appends (>= 128 rows) run one after another through the
+ * tensor-core prefill; shorter appends run per sequence on that sequence's
+ * own stream, concurrently (each reads the weights itself).  feats_dev holds
  * the rows of seq_ids[0], then seq_ids[1], ...; n_rows_host[i] and
  * start_host[i] are per sequence (host arrays of n_seqs).  Same checks per
  * sequence; nothing is launched if any check fails.  Sequence ids must be
@@ -204,13 +207,39 @@ FM_API fm_status fm_accept_batched(fm_handle *h, int32_t n_seqs, const int32_t *
  * before any stream capture.  Every call shares the block: calls that
  * overlap on the GPU (other streams, other handles on the same device) race
  * and must be serialised by the caller.
- * y_dev: device f32 [n_rows][target_dim], row-major.  tokens_dev: device
- * int32 [n_rows], written in stream order.  Both stay owned by the caller.
- * Errors: FM_ERR_INVALID_ARG (null pointer, n_rows outside 1..16),
- *   FM_ERR_UNSUPPORTED (grid beyond the static block), FM_ERR_CUDA.
+ * y_dev: device f32 [n_rows][target_dim], row-major, 16-byte aligned.
+ * tokens_dev: device int32 [n_rows], 4-byte aligned, written in stream
+ * order.  Both stay owned by the caller.  The handle's device must be the
+ * current device.
+ * Errors: FM_ERR_INVALID_ARG (null or misaligned pointer, n_rows outside
+ *   1..16, the current device is not the handle's), FM_ERR_UNSUPPORTED (grid
+ *   beyond the static block), FM_ERR_CUDA.  A device-side bounded wait that
+ *   gives up inside the kernel is reported late: the call has already
+ *   returned FM_OK, tokens_dev is then undefined, and the next
+ *   fm_synchronize (or fm_debug_copy) on the handle returns FM_ERR_TIMEOUT.
  */
 FM_API fm_status fm_lm_head_argmax_noalloc(fm_handle *h, const float *y_dev, int32_t n_rows, int32_t *tokens_dev,
                                     void *stream);
+
+/*
+ * fm_synchronize -- wait for the work on stream, then report whether a
+ * device-side bounded wait gave up in any call since the last check (a wait
+ * that exceeds its clock budget raises an error word on the device and its
+ * kernel returns instead of hanging).  Clears the word.
+ * Errors: FM_ERR_TIMEOUT (a wait gave up: the outputs of those calls are
+ *   undefined; the handle stays usable), FM_ERR_CUDA, FM_ERR_INVALID_ARG.
+ */
+FM_API fm_status fm_synchronize(fm_handle *h, void *stream);
+
+/*
+ * fm_selftest_wait_timeout -- exercise the failure path of the bounded waits:
+ * launches one CTA whose mbarrier wait can never complete, with a budget of
+ * budget_us microseconds (1 .. 1e6); the wait gives up, raises the handle's
+ * device error word and the kernel returns.  A following fm_synchronize
+ * returns FM_ERR_TIMEOUT.  Nothing hangs and nothing faults.
+ * Errors: FM_ERR_INVALID_ARG (budget out of range), FM_ERR_CUDA.
+ */
+FM_API fm_status fm_selftest_wait_timeout(fm_handle *h, int32_t budget_us, void *stream);
 
 /* fm_debug_copy selectors ([FM] readOut / peek: look at working buffers) */
 #define FM_DEBUG_HIDDEN 0   /* index = layer: the block's hidden rows after that layer [block][dim] f32 (last draft) */

@@ -7,7 +7,7 @@ retained per-layer context K/V), ``#buildBlock``, ``#layer`` (Eq 3),
 ``#backbone``, ``#baseLogits`` and the greedy branch of ``forwardRows``.
 Weights are [in, out] as the page stores them (y = x @ W).
 
-Readings (listed in DESIGN.md):
+Readings taken where the page leaves a step open:
   * eps is the target's RMSNorm eps; the page takes it from the target config;
     1e-6 here.
   * the anchor embedding is a plain row of the tied token table E (no scale);

@@ -6,7 +6,7 @@ header comment (the math of the drafter), ``init`` (h0), ``extendContext``
 (context injection) and ``draft`` (the 16-slot block, head, lm_head, argmax).
 The tied token table E [V, Ht] is the target's table (bf16 or Q8_0).
 
-Readings taken where the page leaves a step open (listed in the design doc):
+Readings taken where the page leaves a step open:
   * anchor_proj, x_embed, mlp.fc1/fc2 and head carry biases; fc, every q/k/v/o
     projection and the context k/v projections have none (the page's ``gemm``
     adds a bias only when the checkpoint has one, and passes ``false`` for the
