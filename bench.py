@@ -396,8 +396,8 @@ def run_workload(args):
             w.step()
             torch.cuda.synchronize()
             w.launches = 0
-            ms = time_steps(torch, w.step, max(2, args.steps // 50))
-            n = max(2, args.steps // 50)
+            n = max(10, args.steps // 20)
+            ms = time_steps(torch, w.step, n)
             value, unit, launches = w.rows * n / (ms / 1000), "rows/s", w.launches
             extra["prefill_tflops"] = w.flops * n / (ms / 1000) / 1e12
             extra["tensor_frac_of_measured_bf16"] = extra["prefill_tflops"] / bf16
@@ -441,11 +441,31 @@ def cpu_baseline(w, budget_s=15.0):
 
 
 def blas_threads():
+    """Threads of the BLAS numpy uses: threadpoolctl when installed, else the
+    OpenBLAS library numpy loaded, asked directly through its C API."""
     try:
         from threadpoolctl import threadpool_info
         return max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
     except Exception:
-        return None
+        pass
+    try:
+        import ctypes
+        np.dot(np.ones((2, 2)), np.ones((2, 2)))   # the BLAS is loaded by now
+        libs = set()
+        with open("/proc/self/maps") as f:
+            for line in f:
+                path = line.split()[-1]
+                if "openblas" in path.lower() and ".so" in path:
+                    libs.add(path)
+        for path in sorted(libs):
+            lib = ctypes.CDLL(path)
+            for fn in ("openblas_get_num_threads64_", "openblas_get_num_threads", "scipy_openblas_get_num_threads64_",
+                       "scipy_openblas_get_num_threads"):
+                if hasattr(lib, fn):
+                    return int(getattr(lib, fn)())
+    except Exception:
+        pass
+    return None
 
 
 # ----------------------------------------------------------------- arms
@@ -550,8 +570,9 @@ def run_ours(args):
         pf = PrefillStep(torch)
         pf.step()
         torch.cuda.synchronize()
-        pms = time_steps(torch, pf.step, 2) / 2
+        pms = time_steps(torch, pf.step, 10) / 10
         extra["prefill_rows_per_s"] = pf.rows / (pms / 1000)
+        extra["prefill_reps"] = 10
         extra["prefill_tflops"] = pf.flops / (pms / 1000) / 1e12
         fm.fm_destroy(pf.h)
 

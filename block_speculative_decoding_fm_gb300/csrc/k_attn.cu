@@ -51,7 +51,7 @@ __device__ __forceinline__ void issue_kv(const AttnArgs &a, int head, uint32_t k
 }  // namespace
 
 template <int HD, int NS>
-__global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kThreads) fm_attn_decode_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NT = HD / 8;        // n8 tiles of the output
   constexpr int QS = HD + 32;       // f16 row stride of the query tile (64-byte pad)
@@ -363,8 +363,8 @@ cudaError_t launch_attn(const AttnArgs &a, int L_now, cudaStream_t st, bool pdl)
     }
     return cudaLaunchKernelEx(&cfg, kern, a);
   };
-  if (HD == 128) return NS == 4 ? go(attn_kernel<128, 4>) : NS == 3 ? go(attn_kernel<128, 3>) : go(attn_kernel<128, 2>);
-  return NS == 4 ? go(attn_kernel<64, 4>) : NS == 3 ? go(attn_kernel<64, 3>) : go(attn_kernel<64, 2>);
+  if (HD == 128) return NS == 4 ? go(fm_attn_decode_kernel<128, 4>) : NS == 3 ? go(fm_attn_decode_kernel<128, 3>) : go(fm_attn_decode_kernel<128, 2>);
+  return NS == 4 ? go(fm_attn_decode_kernel<64, 4>) : NS == 3 ? go(fm_attn_decode_kernel<64, 3>) : go(fm_attn_decode_kernel<64, 2>);
 }
 
 }  // namespace fm

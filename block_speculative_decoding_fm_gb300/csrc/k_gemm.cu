@@ -175,7 +175,7 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t bars = base + ST * STAGE;
@@ -332,7 +332,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, int n_sm, cudaStream_t s) {
   const int n_tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
   const int grid = n_tiles < n_sm ? n_tiles : n_sm;
   const size_t smem = tc_gemm_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(fm_prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
@@ -344,7 +344,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, int n_sm, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, a);
+  return cudaLaunchKernelEx(&cfg, fm_prefill_gemm_kernel, a);
 }
 
 cudaError_t launch_f32_to_f16(const float *in, __half *out, size_t n, int n_sm, cudaStream_t s) {

@@ -42,7 +42,7 @@ struct Smem {
 }  // namespace
 
 template <int MT>
-__global__ void __launch_bounds__(kAll, 2) gemv_kernel(const __grid_constant__ GemvArgs a, const int S, const int U) {
+__global__ void __launch_bounds__(kAll, 2) fm_linear_kernel(const __grid_constant__ GemvArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int NR = 32 * MT;                 // B rows: hi rows then lo rows
   constexpr int BCH = NR * 128;               // bytes of one 64-column B chunk
@@ -308,13 +308,13 @@ cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t st, bool pd
   cfg.numAttrs = na;
   cudaError_t e;
   if (mt == 1) {
-    e = cudaFuncSetAttribute(gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(fm_linear_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<1>, a, S, U);
+    return cudaLaunchKernelEx(&cfg, fm_linear_kernel<1>, a, S, U);
   }
-  e = cudaFuncSetAttribute(gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(fm_linear_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<2>, a, S, U);
+  return cudaLaunchKernelEx(&cfg, fm_linear_kernel<2>, a, S, U);
 }
 
 }  // namespace fm

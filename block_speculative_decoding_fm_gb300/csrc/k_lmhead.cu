@@ -250,7 +250,7 @@ struct RingPos {
 };
 
 template <bool kStreamY>
-__global__ void __launch_bounds__(kQ8Threads, 1) lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U, const int NI, const int G) {
+__global__ void __launch_bounds__(kQ8Threads, 1) fm_lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U, const int NI, const int G) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kQ8Chunk;
   constexpr int kNA = 3;
@@ -525,7 +525,7 @@ __host__ __device__ constexpr int bf_stage_bytes(bool stream_y, int U) {
 }
 
 template <bool kStreamY>
-__global__ void __launch_bounds__(kBase + kBfWorkers, 1) lmhead_bf16_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
+__global__ void __launch_bounds__(kBase + kBfWorkers, 1) fm_lmhead_bf16_kernel(const __grid_constant__ LmArgs a, const int S, const int U) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kBfStage;
   constexpr uint32_t IDESC = umma_idesc(128, 32, true);
@@ -763,8 +763,8 @@ cudaError_t launch_lmhead(const LmArgs &a, int grid, cudaStream_t st, bool pdl) 
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, kern, a, S, U, NI, G);
   };
-  if (q8) return stream ? goq(lmhead_q8_kernel<true>) : goq(lmhead_q8_kernel<false>);
-  return stream ? go(lmhead_bf16_kernel<true>) : go(lmhead_bf16_kernel<false>);
+  if (q8) return stream ? goq(fm_lmhead_q8_kernel<true>) : goq(fm_lmhead_q8_kernel<false>);
+  return stream ? go(fm_lmhead_bf16_kernel<true>) : go(fm_lmhead_bf16_kernel<false>);
 }
 
 }  // namespace fm

@@ -32,12 +32,17 @@ def tokens_match(got, want, logits) -> bool:
 class Pair:
     """The CUDA drafter (through the C ABI) and the oracle on one workload."""
 
-    def __init__(self, cfg: S.DrafterConfig, seed: int, oracle_max_ctx: int | None = None, keep_hidden=True):
+    def __init__(self, cfg: S.DrafterConfig, seed: int, oracle_max_ctx: int | None = None, keep_hidden=True,
+                 edit=None):
+        """edit: optional callable that changes the generated weights (name ->
+        fm_synth.Tensor) in place before both sides are built."""
         import torch
         self.torch = torch
         self.cfg = cfg
         self.seed = seed
         self.w = S.gen_weights(cfg, seed)
+        if edit is not None:
+            edit(self.w)
         raw = {n: t.data for n, t in self.w.items()}
         if cfg.variant == S.VARIANT_FLASHMAP:
             self.mod = S.gen_modulation(cfg, seed)
@@ -74,13 +79,13 @@ class Pair:
         out = np.empty((self.cfg.block, self.cfg.dim), np.float32)
         return fm.fm_debug_copy(self.h, fm.FM_DEBUG_HIDDEN, 0, layer, out)
 
-    def head_out(self):
+    def head_out(self, seq=0):
         out = np.empty((self.cfg.block, self.cfg.target_dim), np.float32)
-        return fm.fm_debug_copy(self.h, fm.FM_DEBUG_HEAD_OUT, 0, 0, out)
+        return fm.fm_debug_copy(self.h, fm.FM_DEBUG_HEAD_OUT, seq, 0, out)
 
-    def logits(self):
+    def logits(self, seq=0):
         out = np.empty((self.cfg.block, self.cfg.vocab), np.float32)
-        return fm.fm_debug_copy(self.h, fm.FM_DEBUG_LOGITS, 0, 0, out)
+        return fm.fm_debug_copy(self.h, fm.FM_DEBUG_LOGITS, seq, 0, out)
 
     def cache(self, seq, layer, which="k"):
         c = self.cfg

@@ -252,3 +252,107 @@ def test_tiny_flashmap_batched_sequences():
         assert tokens_match(got[s], ref.tokens, ref.logits), (s, got[s], ref.tokens)
         assert fm.fm_get_length(p.h, s) == pos[s]
     p.close()
+
+
+def test_tiny_flashmap_large_dc_offset():
+    """A residual stream far from zero mean: x_embed's bias set to 1000 makes
+    h0 ~ 1000 + O(0.4), so every LayerNorm sees |mean| / std ~ 2500.  The
+    variance must come from deviations about the mean (the page's two-pass
+    lnMod); a variance formed as E[x^2] - mean^2 in f32 loses every digit of it
+    (mean^2 ~ 1e6, f32 spacing ~0.06, variance ~0.15) and fails the bars."""
+    def offset(w):
+        t = w["x_embed.bias"]
+        t.data = S.f32_to_bf16_bits(np.full(t.shape, 1000.0, np.float32))
+    cfg = S.tiny_config(max_ctx=96)
+    p = Pair(cfg, 1011, edit=offset)
+    assert abs(float(p.oracle.h0.mean())) > 900.0 and float(p.oracle.h0.std()) < 1.0
+    p.append(0, S.gen_features(S.streams(1011)["features"], 40, cfg.feat_dim), 0)
+    got, ref = p.draft(0, 321, 40)
+    check_draft(p, got, ref)
+    p.close()
+
+
+@pytest.mark.parametrize("lm", [S.LM_BF16, S.LM_Q8_0])
+def test_argmax_ties_go_to_the_lowest_index(lm):
+    """Every odd table row is a copy of the even row before it, so each slot's
+    best logit is tied between rows 2j and 2j + 1: the fused two-pass argmax
+    must return the even (lower) index, as numpy's first-occurrence argmax
+    does; identical rows give bit-identical logits on the device."""
+    def pairs(w):
+        t = w["token_embd.weight"]
+        t.data = t.data.copy()
+        t.data[1::2] = t.data[0::2]
+    cfg = S.tiny_config(max_ctx=96).replace(lm_format=lm)
+    p = Pair(cfg, 1012, edit=pairs)
+    p.append(0, S.gen_features(S.streams(1012)["features"], 40, cfg.feat_dim), 0)
+    got, ref = p.draft(0, 200, 40)
+    lg = p.logits()
+    assert np.array_equal(lg[:, 0::2], lg[:, 1::2])          # the ties are exact on the device
+    assert np.all(got % 2 == 0), got
+    assert np.array_equal(got, np.argmax(lg, axis=-1))
+    # against the oracle where the winning pair is clear of every other row
+    best = ref.tokens
+    rest = ref.logits.copy()
+    rows = np.arange(cfg.block)
+    rest[rows, best] = -np.inf
+    rest[rows, best + 1] = -np.inf
+    clear = ref.logits[rows, best] - rest.max(axis=1) >= 1e-3
+    assert np.all(best % 2 == 0)
+    assert np.array_equal(got[clear], best[clear]), (got, best)
+    assert rel_l2(lg, ref.logits) < REL_L2
+    p.close()
+
+
+def test_allocation_failure_is_reported_and_released():
+    """FM_FAULT_INJECT=alloc:N makes the N-th device allocation of fm_create
+    fail (a host-side fault, nothing on the GPU faults): fm_create returns
+    FM_ERR_OOM with a reason, frees what it had allocated, and a later
+    fm_create on the same device works."""
+    import os
+    import torch
+    import block_speculative_decoding_fm_gb300 as fm
+    cfg = S.tiny_config(max_ctx=96)
+    w = S.gen_weights(cfg, 1013)
+    mod = S.gen_modulation(cfg, 1013)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    try:
+        for n in (1, 7, 40):
+            os.environ["FM_FAULT_INJECT"] = f"alloc:{n}"
+            with pytest.raises(fm.FmError) as e:
+                fm.fm_create(cfg, fm.weight_items(w), mod)
+            assert e.value.status == fm.FM_ERR_OOM
+            assert f"allocation {n}" in str(e.value)
+    finally:
+        os.environ.pop("FM_FAULT_INJECT", None)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] >= free0 - (16 << 20)   # nothing of the failed handles is kept
+    h = fm.fm_create(cfg, fm.weight_items(w), mod)
+    tok = torch.zeros((1, cfg.block), dtype=torch.int32, device="cuda")
+    fm.fm_draft(h, [0], [9], [0], tok)
+    fm.fm_synchronize(h)
+    fm.fm_destroy(h)
+
+
+def test_bounded_wait_gives_up_and_is_reported():
+    """A device wait that can never complete (an mbarrier phase nothing
+    completes) gives up after its budget, raises the handle's error word and
+    returns: fm_synchronize reports FM_ERR_TIMEOUT once, and the handle keeps
+    drafting correctly afterwards."""
+    import time
+    import block_speculative_decoding_fm_gb300 as fm
+    cfg = S.tiny_config(max_ctx=96)
+    p = Pair(cfg, 1014)
+    p.append(0, S.gen_features(S.streams(1014)["features"], 30, cfg.feat_dim), 0)
+    fm.fm_synchronize(p.h)
+    t0 = time.perf_counter()
+    fm.fm_selftest_wait_timeout(p.h, 20000)          # 20 ms budget
+    with pytest.raises(fm.FmError) as e:
+        fm.fm_synchronize(p.h)
+    assert e.value.status == fm.FM_ERR_TIMEOUT
+    assert time.perf_counter() - t0 < 10.0
+    fm.fm_synchronize(p.h)                           # reported once, then cleared
+    got, ref = p.draft(0, 77, 30)
+    check_draft(p, got, ref)
+    fm.fm_synchronize(p.h)
+    p.close()
