@@ -265,3 +265,28 @@ def targets_with_flip(drafts: np.ndarray, k: int, flip: int, vocab: int,
 def batched_lengths(rng: np.random.Generator, n_seqs: int = 32, lo: int = 512, hi: int = 8192):
     """Per-sequence context lengths, uniform in [lo, hi]."""
     return rng.integers(lo, hi + 1, size=n_seqs).astype(np.int64)
+
+
+# ---------------------------------------------------------------- time conditioning
+
+def time_cond_specs(cfg: DrafterConfig, time_dim: int = 256, cond_dim: int = 256):
+    """(name, shape) of the FlashMap time-conditioning linears: the sinusoid's
+    two MLPs (time_embed for s, jump_embed for t) and one adaLN linear per
+    norm, in table order."""
+    s = []
+    for p in ("time_embed", "jump_embed"):
+        s += [(f"{p}.linear_1.weight", (cond_dim, time_dim)), (f"{p}.linear_1.bias", (cond_dim,)),
+              (f"{p}.linear_2.weight", (cond_dim, cond_dim)), (f"{p}.linear_2.bias", (cond_dim,))]
+    names = [f"layers.{l}.{n}.linear" for l in range(cfg.n_layers)
+             for n in ("self_attn_adaln", "cross_attn_adaln", "mlp_adaln")] + ["final_adaln.linear"]
+    for n in names:
+        s += [(n + ".weight", (3 * cfg.dim, cond_dim)), (n + ".bias", (3 * cfg.dim,))]
+    return s
+
+
+def gen_time_cond_weights(cfg: DrafterConfig, seed: int, time_dim: int = 256, cond_dim: int = 256,
+                          std: float = 0.02) -> Dict[str, Tensor]:
+    """bf16(N(0, std)) time-conditioning weights and biases (seeded stream of their own)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7])))
+    return {n: Tensor(n, shape, DT_BF16, f32_to_bf16_bits(_normal(rng, shape, std)))
+            for n, shape in time_cond_specs(cfg, time_dim, cond_dim)}

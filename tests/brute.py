@@ -289,3 +289,37 @@ class BruteDFlash:
         Y = [vecmat(o, W["out_proj"]) for o in out]
         logits = [[sum(e[i] * y[i] for i in range(len(y))) for e in self.E] for y in Y]
         return [argmax(r) for r in logits], logits, Y, hidden
+
+
+def time_conditioning(weights, n_layers: int, time_dim: int, time_scale: float, s: float, t: float):
+    """flashmap_drafter.js ``timeConditioning`` by explicit loops: for each of
+    s (time_embed) and t (jump_embed) a [cos | sin] embedding of width time_dim
+    (frequencies exp(-ln(10000) i / half)), linear_1, x / (1 + exp(-x)),
+    linear_2; cond = SiLU(sum); then every adaLN linear of cond, (self, cross,
+    mlp) per layer and the final one."""
+    def lin(name, x):
+        W = mat(weights[name + ".weight"])
+        b = vec(weights[name + ".bias"]) if name + ".bias" in weights else None
+        return matvec(W, x, b)
+
+    def sig_lu(v):
+        return [x / (1.0 + math.exp(-x)) for x in v]
+
+    def embed(prefix, time):
+        half_ = time_dim // 2
+        e = [0.0] * time_dim
+        for i in range(half_):
+            a = time * time_scale * math.exp(-math.log(10000.0) * i / half_)
+            e[i] = math.cos(a)
+            e[half_ + i] = math.sin(a)
+        return lin(prefix + ".linear_2", sig_lu(lin(prefix + ".linear_1", e)))
+
+    ts = embed("time_embed", s)
+    tj = embed("jump_embed", t)
+    cond = sig_lu([a + b for a, b in zip(ts, tj)])
+    out = []
+    for l in range(n_layers):
+        for n in ("self_attn_adaln", "cross_attn_adaln", "mlp_adaln"):
+            out.extend(lin(f"layers.{l}.{n}.linear", cond))
+    out.extend(lin("final_adaln.linear", cond))
+    return out
