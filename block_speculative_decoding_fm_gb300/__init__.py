@@ -23,11 +23,13 @@ FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_OOM, FM_ERR_CONTEXT_FULL, 
 FM_VARIANT_FLASHMAP, FM_VARIANT_DFLASH = 0, 1
 FM_LM_BF16, FM_LM_Q8_0 = 0, 1
 FM_DTYPE_BF16, FM_DTYPE_Q8_0, FM_DTYPE_F32 = 0, 1, 2
-FM_DEBUG_HIDDEN, FM_DEBUG_HEAD_OUT, FM_DEBUG_LOGITS, FM_DEBUG_CACHE_K, FM_DEBUG_CACHE_V, FM_DEBUG_H0 = range(6)
+FM_DEBUG_HIDDEN, FM_DEBUG_HEAD_OUT, FM_DEBUG_LOGITS, FM_DEBUG_CACHE_K, FM_DEBUG_CACHE_V, FM_DEBUG_H0, \
+    FM_DEBUG_STEP_TRACE = range(7)
 FM_DEBUG_KEEP_HIDDEN = 1
 FM_DEBUG_PROFILE = 2
+FM_DEBUG_TRACE = 4
 
-EXPORTS = ["fm_create", "fm_context_append", "fm_context_append_batched", "fm_draft", "fm_accept",
+EXPORTS = ["fm_create", "fm_time_conditioning", "fm_context_append", "fm_context_append_batched", "fm_draft", "fm_accept",
            "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_synchronize", "fm_selftest_wait_timeout", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
            "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy"]
 
@@ -71,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     sig = {
         "fm_create": (I32, [ctypes.POINTER(FmConfig), ctypes.POINTER(FmTensor), I32, P, P, ctypes.POINTER(P)]),
+        "fm_time_conditioning": (I32, [ctypes.POINTER(FmConfig), ctypes.POINTER(FmTensor), I32, I32, I32,
+                                       ctypes.c_float, ctypes.c_float, ctypes.c_float, P, P]),
         "fm_context_append": (I32, [P, I32, P, I32, I32, P]),
         "fm_context_append_batched": (I32, [P, I32, P, P, P, P, P]),
         "fm_draft": (I32, [P, I32, P, P, P, P, P]),
@@ -132,10 +136,7 @@ def make_config(cfg) -> FmConfig:
                     cfg.rope_theta, cfg.ln_eps, cfg.rms_eps, cfg.qk_eps)
 
 
-def fm_create(cfg, weights: Iterable[Tuple[str, object, int]], modulation=None, stream=None) -> ctypes.c_void_p:
-    """weights: (name, array, FM_DTYPE_*) triples; arrays are host numpy
-    arrays or CUDA tensors (their raw bytes are passed)."""
-    lib = load_library()
+def _tensor_array(weights):
     items = list(weights)
     keep = []
     arr = (FmTensor * max(1, len(items)))()
@@ -151,9 +152,30 @@ def fm_create(cfg, weights: Iterable[Tuple[str, object, int]], modulation=None, 
         bname = name.encode()
         keep.append(bname)
         arr[i] = FmTensor(bname, _ptr(data), nbytes, dtype, on_dev)
+    return arr, len(items), keep
+
+
+def fm_time_conditioning(cfg, weights: Iterable[Tuple[str, object, int]], time_dim: int, cond_dim: int,
+                         time_scale: float, s: float, t: float, table, stream=None) -> None:
+    """The adaLN table of the jump s -> t into ``table`` (a CUDA float32
+    tensor of (3 n_layers + 1) * 3 * dim values)."""
+    lib = load_library()
+    arr, n, keep = _tensor_array(weights)
+    c = make_config(cfg)
+    _check(lib.fm_time_conditioning(ctypes.byref(c), arr, n, time_dim, cond_dim, time_scale, s, t, _ptr(table),
+                                    _stream(stream)))
+
+
+def fm_create(cfg, weights: Iterable[Tuple[str, object, int]], modulation=None, stream=None) -> ctypes.c_void_p:
+    """weights: (name, array, FM_DTYPE_*) triples; arrays are host numpy
+    arrays or CUDA tensors (their raw bytes are passed).  modulation: a host
+    array or a CUDA float32 tensor."""
+    lib = load_library()
+    arr, n_items, keep = _tensor_array(weights)
+    items = range(n_items)
     mod = None
     if modulation is not None:
-        mod = np.ascontiguousarray(modulation, dtype=np.float32)
+        mod = modulation if hasattr(modulation, "data_ptr") else np.ascontiguousarray(modulation, dtype=np.float32)
         keep.append(mod)
     c = make_config(cfg)
     h = ctypes.c_void_p()

@@ -264,6 +264,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
   return true;
 }
+// Bounded wait that does not give up early when the error word is raised: for
+// winding down (copies in flight must land and MMAs complete before a CTA
+// frees its resources and exits).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity))
+    if (clock64() - t0 > kWaitBudgetCycles) return false;
+  return true;
+}
 // Warp-wide bounded wait: every lane polls, and the verdict is made uniform so
 // that a timeout seen by one lane ends the whole warp's loop together.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int32_t *err) {

@@ -9,7 +9,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <string>
+#include <tuple>
 #include <unordered_map>
 #include <vector>
 
@@ -89,6 +91,19 @@ struct fm_handle {
   CUtensorMap tm_wfc{}, tm_wkv{}, tm_c{};
 
   int32_t *dev_err = nullptr;     // raised by a device-side bounded wait that gave up
+
+  // ---- the persistent draft step ----
+  bool use_step = true;
+  int step_attrs = 3;                 // launch attributes the device accepted (cooperative | PDL)
+  uint32_t *step_bar = nullptr;       // grid barrier words
+  int32_t *step_tickets = nullptr;    // tile / head tickets (self-resetting)
+  float *step_part = nullptr;         // partial tiles [n_sm][kStepMaxSeg][kMaxT][kTile]
+  float *step_apart = nullptr;        // attention partials [n_sm][kMaxT * hd + 2 kMaxT]
+  // device programs by (sequence, key splits, debug, parameter slot): the jobs
+  // carry the address of the parameter slot their chain reads
+  std::map<std::tuple<int, int, int, const void *>, StepPhase *> step_progs;
+  uint64_t *step_trace = nullptr;     // FM_DEBUG_TRACE: per phase and CTA, globaltimer stamps
+  int step_trace_phases = 0;
   std::vector<void *> to_free;    // row-major staging copies released at the end of fm_create
 
   // ---- per-sequence lanes ----
@@ -478,10 +493,20 @@ fm_status flashmap_append_rows(fm_handle *h, int seq, const StepParams *sp, int 
   return run_gemv(h, flashmap_kv_args(h, seq, sp, 0, 0), s, "gemv.kv_append", T);
 }
 
-fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams *sp, int n_pend, cudaStream_t s) {
+// The products of one FlashMap draft, in order: the anchor slot (anchor_proj,
+// then the K/V of the pending rows and the anchor row), per layer the self
+// q/k/v (+ the block attention tail), o, cross q, cross o, fc1 and fc2, then
+// the head.  Shared by the launch-per-product chain and the persistent step.
+struct FlashMapPlan {
+  GemvArgs anchor, kv;
+  std::vector<GemvArgs> qkv, o, cq, co, f1, f2;
+  GemvArgs head;
+};
+
+FlashMapPlan flashmap_plan(fm_handle *h, int seq, const StepParams *sp, int n_pend) {
   const fm_config &c = h->cfg;
   const int D = c.dim, B = c.block, Ht = c.target_dim, F = c.ff_dim, L = c.n_layers;
-
+  FlashMapPlan pl;
   // the anchor's context slot at pos: anchor_proj(E[anchor]) -> anchor_norm -> k / v of every layer
   GemvArgs a = gemv_base(h, h->w_ap, D, Ht, 1, sp);
   a.amode = c.lm_format == FM_LM_Q8_0 ? A_ROW_Q8 : A_ROW_BF16;
@@ -492,11 +517,9 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
   a.Y = h->actx;
   a.ldy = D;
   a.out_st = h->st_a;
-  TRY(run_gemv(h, a, s, "gemv.anchor_proj", 1));
-
+  pl.anchor = a;
   // the pending appended rows (deferred) and the anchor row share one pass over the cross K/V weights
-  GemvArgs kvp = flashmap_kv_args(h, seq, sp, n_pend + 1, n_pend);
-  TRY(run_gemv(h, kvp, s, n_pend ? "gemv.kv_fused" : "gemv.kv_anchor", n_pend + 1));
+  pl.kv = flashmap_kv_args(h, seq, sp, n_pend + 1, n_pend);
 
   const float attn_scale = (float)(1.0 / std::sqrt((double)c.head_dim));
   for (int l = 0; l < L; ++l) {
@@ -530,7 +553,7 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
     q.attn_out = h->attn;
     q.self_D = D;
     q.attn_scale = attn_scale;
-    TRY(run_gemv(h, q, s, "gemv.qkv_self"));
+    pl.qkv.push_back(q);
 
     GemvArgs o = gemv_base(h, h->w_so[l], D, D, B, sp);
     o.amode = A_PLAIN;
@@ -543,7 +566,7 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
     o.Y = h->X;
     o.ldy = D;
     o.out_st = h->st_x;
-    TRY(run_gemv(h, o, s, "gemv.o_self"));
+    pl.o.push_back(o);
 
     // cross-attention over cache rows 0 .. pos
     GemvArgs cq = gemv_base(h, h->w_cq[l], D, D, B, sp);
@@ -564,9 +587,7 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
     cq.segs[0] = {SEG_F32, 0, 1, 0, h->w_cqn[l], nullptr};
     cq.pos_src = 0;
     cq.pos_add = 1;
-    TRY(run_gemv(h, cq, s, "gemv.q_cross"));
-
-    TRY(run_attn(h, h->qc, D, h->kv(seq, l), B, 1, 0, pos + 1, sp, h->attn, s));
+    pl.cq.push_back(cq);
 
     GemvArgs co = gemv_base(h, h->w_co[l], D, D, B, sp);
     co.amode = A_PLAIN;
@@ -579,7 +600,7 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
     co.Y = h->X;
     co.ldy = D;
     co.out_st = h->st_x;
-    TRY(run_gemv(h, co, s, "gemv.o_cross"));
+    pl.co.push_back(co);
 
     // MLP: adaLN -> fc1 + bias -> exact GELU -> fc2 + bias -> gated residual
     GemvArgs f1 = gemv_base(h, h->w_f1[l], F, D, B, sp);
@@ -596,7 +617,7 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
     f1.bias = h->b_f1[l];
     f1.Y = h->u;
     f1.ldy = F;
-    TRY(run_gemv(h, f1, s, "gemv.fc1"));
+    pl.f1.push_back(f1);
 
     GemvArgs f2 = gemv_base(h, h->w_f2[l], D, F, B, sp);
     f2.amode = A_PLAIN;
@@ -610,13 +631,9 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
     f2.Y = h->X;
     f2.ldy = D;
     f2.out_st = h->st_x;
-    TRY(run_gemv(h, f2, s, "gemv.fc2"));
-
-    if (h->debug & FM_DEBUG_KEEP_HIDDEN) {
-      CK(cudaMemcpyAsync(h->hid + (size_t)l * kMaxT * D, h->X, (size_t)B * D * 4, cudaMemcpyDeviceToDevice, s));
-    }
+    pl.f2.push_back(f2);
   }
-  // final adaLN -> head -> lm_head + argmax
+  // final adaLN -> head (its output also split into the lm_head operand)
   const float *m_fin = h->mod + (size_t)(3 * L) * 3 * D;
   GemvArgs hd = gemv_base(h, h->w_head, Ht, D, B, sp);
   hd.amode = A_LNMOD;
@@ -634,7 +651,174 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
   hd.ldy = Ht;
   hd.ylm = h->ylm;
   hd.ylm_f16 = c.lm_format == FM_LM_Q8_0;
-  TRY(run_gemv(h, hd, s, "gemv.head"));
+  pl.head = hd;
+  return pl;
+}
+
+// Cross-attention key ranges per head in the persistent step: enough CTAs per
+// head to fill the GPU, at least 64 keys each.
+int step_splits(const fm_handle *h, int L) {
+  int sp = h->n_sm / h->cfg.n_heads;
+  const int need = (L + 63) / 64;
+  if (sp > need) sp = need;
+  return sp < 1 ? 1 : sp;
+}
+
+// The persistent program of one FlashMap draft (layers + head): one linear
+// phase per product, one attention phase per layer.  Returns false when the
+// schedule does not fit the kernel's limits (the caller then runs the chain).
+bool flashmap_step_program(fm_handle *h, int seq, const FlashMapPlan &pl, int nsp, std::vector<StepPhase> &ph) {
+  const fm_config &c = h->cfg;
+  const int D = c.dim, L = c.n_layers, G = h->n_sm;
+  if (c.block > 16 || c.n_heads * nsp > G || c.n_heads > kStepHeadTickets) return false;
+  auto linear = [&](const GemvArgs &g, int self_tail) {
+    StepPhase P;
+    memset(&P, 0, sizeof P);
+    P.kind = PH_LINEAR;
+    P.njobs = 1;
+    P.prefetch = -1;
+    StepJob &J = P.jobs[0];
+    J.g = g;
+    J.cpt = g.K / 64;
+    J.nchunks = ((g.M + kTile - 1) / kTile) * J.cpt;
+    J.chunk0 = 0;
+    J.tile0 = 0;
+    J.self_tail = self_tail;
+    P.nchunks = J.nchunks;
+    P.ntiles = (g.M + kTile - 1) / kTile;
+    ph.push_back(P);
+  };
+  const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  for (int l = 0; l < L; ++l) {
+    linear(pl.qkv[l], 1);
+    linear(pl.o[l], 0);
+    linear(pl.cq[l], 0);
+    ph.back().prefetch = (int)ph.size();   // the attention phase that follows
+    StepPhase A;
+    memset(&A, 0, sizeof A);
+    A.kind = PH_ATTN;
+    A.prefetch = -1;
+    Seg2 kv = h->kv(seq, l);
+    A.at.Q = h->qc;
+    A.at.ldq = D;
+    A.at.max_ctx = c.max_ctx;
+    A.at.n_heads = c.n_heads;
+    A.at.hd = c.head_dim;
+    A.at.Kc = kv.k;
+    A.at.Vc = kv.v;
+    A.at.nsp = nsp;
+    A.at.L_src = 1;
+    A.at.L_add = 0;
+    A.at.prefetched = 1;
+    A.at.scale_log2 = scale_log2;
+    A.at.out = h->attn;
+    A.at.ldo = D;
+    ph.push_back(A);
+    linear(pl.co[l], 0);
+    linear(pl.f1[l], 0);
+    GemvArgs f2 = pl.f2[l];
+    if (h->debug & FM_DEBUG_KEEP_HIDDEN) {
+      f2.Y2 = h->hid + (size_t)l * kMaxT * D;
+      f2.ldy2 = D;
+    }
+    linear(f2, 0);
+  }
+  linear(pl.head, 0);
+  // the kernel's limits: segments per CTA, tickets, and the K of every job
+  for (const StepPhase &P : ph) {
+    if (P.kind != PH_LINEAR) continue;
+    if (P.ntiles > kStepTileTickets) return false;
+    for (int j = 0; j < P.njobs; ++j)
+      if (P.jobs[j].g.K % 64 || P.jobs[j].cpt < 1) return false;
+    for (int b = 0; b < G; ++b) {
+      const int lo = step_lo(b, P.nchunks, G), hi = step_lo(b + 1, P.nchunks, G);
+      int n = 0;
+      for (int cc = lo; cc < hi;) {
+        const int j = step_job(P, cc);
+        const StepJob &J = P.jobs[j];
+        const int tile = (cc - J.chunk0) / J.cpt;
+        cc = std::min(hi, J.chunk0 + (tile + 1) * J.cpt);
+        ++n;
+      }
+      if (n > kStepMaxSeg) return false;
+    }
+    // every chunk is owned once: the owner of chunk c has c inside its range
+    for (int cc = 0; cc < P.nchunks; ++cc) {
+      const int o = step_owner(cc, P.nchunks, G);
+      if (o < 0 || o >= G || step_lo(o, P.nchunks, G) > cc || step_lo(o + 1, P.nchunks, G) <= cc) return false;
+    }
+  }
+  return true;
+}
+
+fm_status run_step(fm_handle *h, int seq, int nsp, const std::vector<StepPhase> &prog, const StepParams *sp, int T,
+                   double bytes, cudaStream_t s) {
+  const auto key = std::make_tuple(seq, nsp, h->debug & FM_DEBUG_KEEP_HIDDEN, (const void *)sp);
+  auto it = h->step_progs.find(key);
+  if (it == h->step_progs.end()) {
+    StepPhase *d = nullptr;
+    TRY(dalloc(h, &d, prog.size()));
+    CK(cudaMemcpy(d, prog.data(), prog.size() * sizeof(StepPhase), cudaMemcpyHostToDevice));
+    it = h->step_progs.emplace(key, d).first;
+  }
+  StepArgs a;
+  memset(&a, 0, sizeof a);
+  a.ph = it->second;
+  a.n_phases = (int)prog.size();
+  a.T = T;
+  a.sp = sp;
+  a.bar = h->step_bar;
+  a.tickets = h->step_tickets;
+  a.part = h->step_part;
+  a.apart = h->step_apart;
+  a.err = h->dev_err;
+  if (h->debug & FM_DEBUG_TRACE) {
+    if (!h->step_trace || h->step_trace_phases < (int)prog.size()) {
+      TRY(dalloc(h, &h->step_trace, (size_t)prog.size() * h->n_sm * kStepTraceSlots));
+      h->step_trace_phases = (int)prog.size();
+    }
+    CK(cudaMemsetAsync(h->step_trace, 0, (size_t)prog.size() * h->n_sm * kStepTraceSlots * 8, s));
+    a.trace = h->step_trace;
+  }
+  ProfScope ps(h, s, "draft_step", bytes);
+  CK(launch_step(a, h->n_sm, s, h->step_attrs));
+  ++h->last_launches;
+  return FM_OK;
+}
+
+fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams *sp, int n_pend, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int D = c.dim, B = c.block, L = c.n_layers, Ht = c.target_dim, F = c.ff_dim;
+  const FlashMapPlan pl = flashmap_plan(h, seq, sp, n_pend);
+  TRY(run_gemv(h, pl.anchor, s, "gemv.anchor_proj", 1));
+  TRY(run_gemv(h, pl.kv, s, n_pend ? "gemv.kv_fused" : "gemv.kv_anchor", n_pend + 1));
+
+  if (h->use_step) {
+    const int nsp = step_splits(h, pos + 1);
+    std::vector<StepPhase> prog;
+    if (flashmap_step_program(h, seq, pl, nsp, prog)) {
+      // algorithmic bytes: every weight of the layers and the head once, the keys and values read once
+      // (q/k/v 3 D^2, o, cross q, cross o D^2 each, fc1 and fc2 F D per layer; the head Ht D; bf16)
+      const double bytes = 2.0 * ((double)L * (6.0 * D * D + 2.0 * F * D) + (double)Ht * D) +
+                           (double)L * (pos + 1) * D * 2 * 2;
+      TRY(run_step(h, seq, nsp, prog, sp, B, bytes, s));
+      return run_lmhead(h, h->Y, B, sp, nullptr, nullptr, s, h->ylm);
+    }
+  }
+
+  for (int l = 0; l < L; ++l) {
+    TRY(run_gemv(h, pl.qkv[l], s, "gemv.qkv_self"));
+    TRY(run_gemv(h, pl.o[l], s, "gemv.o_self"));
+    TRY(run_gemv(h, pl.cq[l], s, "gemv.q_cross"));
+    TRY(run_attn(h, h->qc, D, h->kv(seq, l), B, 1, 0, pos + 1, sp, h->attn, s));
+    TRY(run_gemv(h, pl.co[l], s, "gemv.o_cross"));
+    TRY(run_gemv(h, pl.f1[l], s, "gemv.fc1"));
+    TRY(run_gemv(h, pl.f2[l], s, "gemv.fc2"));
+    if (h->debug & FM_DEBUG_KEEP_HIDDEN) {
+      CK(cudaMemcpyAsync(h->hid + (size_t)l * kMaxT * D, h->X, (size_t)B * D * 4, cudaMemcpyDeviceToDevice, s));
+    }
+  }
+  TRY(run_gemv(h, pl.head, s, "gemv.head"));
   return run_lmhead(h, h->Y, B, sp, nullptr, nullptr, s, h->ylm);
 }
 
@@ -877,7 +1061,7 @@ fm_status flashmap_prefill(fm_handle *h, int seq, const float *feats, int n, int
 // and replay the graph.  With FM_DEBUG_PROFILE the chain is launched directly.
 template <typename Enqueue>
 fm_status run_chain(fm_handle *h, uint64_t key, const StepParams &p, cudaStream_t s, Enqueue &&enqueue) {
-  if (h->use_graphs && !(h->debug & FM_DEBUG_PROFILE)) {
+  if (h->use_graphs && !(h->debug & (FM_DEBUG_PROFILE | FM_DEBUG_TRACE))) {
     auto it = h->graphs.find(key);
     if (it == h->graphs.end()) {
       fm_handle::GraphEntry g;
@@ -960,7 +1144,8 @@ fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens,
     p.L = pos;  // context rows 0 .. pos-1; the block's own keys go to rows pos .. pos+block-1
     L_now = pos + c.block;
   }
-  const uint64_t key = chain_key(1, seq, c.block + 64 * n_pend, attn_splits(h, L_now), h->debug);
+  const int splits = h->use_step && c.variant == FM_VARIANT_FLASHMAP ? step_splits(h, L_now) : attn_splits(h, L_now);
+  const uint64_t key = chain_key(1, seq, c.block + 64 * n_pend, splits, h->debug);
   return run_chain(h, key, p, s, [&](const StepParams *sp, cudaStream_t st) {
     return c.variant == FM_VARIANT_FLASHMAP ? flashmap_draft_launch(h, seq, pos, sp, n_pend, st)
                                             : dflash_draft_launch(h, seq, pos, sp, st);
@@ -1044,6 +1229,12 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   TRY(dalloc(h, &h->tok_tmp, (size_t)kMaxT));
   TRY(dalloc(h, &h->dev_err, 4));
   CK(cudaMemsetAsync(h->dev_err, 0, 4, s));
+  TRY(dalloc(h, &h->step_bar, 64));
+  CK(cudaMemsetAsync(h->step_bar, 0, 64 * 4, s));
+  TRY(dalloc(h, &h->step_tickets, (size_t)kStepTileTickets + 2 * kStepHeadTickets));
+  CK(cudaMemsetAsync(h->step_tickets, 0, ((size_t)kStepTileTickets + 2 * kStepHeadTickets) * 4, s));
+  TRY(dalloc(h, &h->step_part, (size_t)h->n_sm * kStepMaxSeg * kMaxT * kTile));
+  TRY(dalloc(h, &h->step_apart, (size_t)h->n_sm * step_apart_floats(c.head_dim)));
   TRY(dalloc(h, &h->sp_dev, kParamSlots));
   CK(cudaMallocHost(&h->sp_host, sizeof(StepParams) * kParamSlots));
   memset(h->sp_host, 0, sizeof(StepParams) * kParamSlots);
@@ -1055,6 +1246,28 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   h->use_defer = !(df && df[0] == '1');
   const char *pf = getenv("FM_NO_TC_PREFILL");
   h->use_prefill = !(pf && pf[0] == '1');
+  // the persistent draft step needs one co-resident CTA per SM; an empty program
+  // finds the launch attributes the device takes (outside any stream capture)
+  const char *ps = getenv("FM_PERSISTENT");
+  h->use_step = (ps && ps[0] == '1') && c.variant == FM_VARIANT_FLASHMAP && step_max_grid() >= 1;
+  if (h->use_step) {
+    StepArgs a;
+    memset(&a, 0, sizeof a);
+    a.bar = h->step_bar;
+    a.tickets = h->step_tickets;
+    a.part = h->step_part;
+    a.apart = h->step_apart;
+    a.err = h->dev_err;
+    h->step_attrs = -1;
+    for (int attrs : {3, 1}) {
+      if (launch_step(a, h->n_sm, s, attrs) == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess) {
+        h->step_attrs = attrs;
+        break;
+      }
+      cudaGetLastError();
+    }
+    if (h->step_attrs < 0) h->use_step = false;
+  }
   return FM_OK;
 }
 
@@ -1484,6 +1697,12 @@ fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const i
       return fail(h, FM_ERR_CONTEXT_FULL, "context full at pos %d", pos[i]);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (h->use_step) {
+    // the persistent step holds every SM: sequences draft one after another on the caller's stream
+    for (int i = 0; i < n_seqs; ++i)
+      TRY(draft_one(h, seq_ids[i], anchors[i], pos[i], tokens + (size_t)i * h->cfg.block, s));
+    return FM_OK;
+  }
   return run_lanes(h, n_seqs, seq_ids, s, [&](int i, cudaStream_t ls) {
     return draft_one(h, seq_ids[i], anchors[i], pos[i], tokens + (size_t)i * h->cfg.block, ls);
   });
@@ -1545,6 +1764,79 @@ fm_status fm_lm_head_argmax_noalloc(fm_handle *h, const float *y_dev, int32_t n_
   CK(launch_lmhead(a, grid, s, false));
   ++h->last_launches;
   return FM_OK;
+}
+
+fm_status fm_time_conditioning(const fm_config *cfg, const fm_tensor *weights, int32_t n_weights, int32_t time_dim,
+                               int32_t cond_dim, float time_scale, float s_time, float t_time, float *table_dev,
+                               void *stream) {
+  fm_handle tmp;   // holds the temporary buffers and the error text
+  fm_handle *h = &tmp;
+  auto done = [&](fm_status st) {
+    for (void *p : tmp.allocs) cudaFree(p);
+    tmp.allocs.clear();
+    if (st != FM_OK) g_create_error = tmp.err;
+    return st;
+  };
+  if (!cfg || (!weights && n_weights > 0) || n_weights < 0 || !table_dev) return FM_ERR_INVALID_ARG;
+  tmp.cfg = *cfg;
+  if (cfg->variant != FM_VARIANT_FLASHMAP) return done(fail(h, FM_ERR_INVALID_ARG, "time conditioning is FlashMap's"));
+  if (cfg->dim < 1 || cfg->n_layers < 1 || time_dim < 2 || time_dim % 2 || cond_dim < 1)
+    return done(fail(h, FM_ERR_INVALID_ARG, "bad dims (time_dim must be even, all dims positive)"));
+  if (reinterpret_cast<uintptr_t>(table_dev) & 3) return done(fail(h, FM_ERR_INVALID_ARG, "table_dev not 4-byte aligned"));
+  TensorSet ts;
+  for (int i = 0; i < n_weights; ++i) {
+    if (!weights[i].name) return done(fail(h, FM_ERR_INVALID_ARG, "unnamed tensor"));
+    ts.by_name[weights[i].name] = &weights[i];
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int L = cfg->n_layers, D3 = 3 * cfg->dim, nb = 3 * L + 1;
+  struct Lin {
+    __nv_bfloat16 *w = nullptr, *b = nullptr;
+  };
+  auto load = [&](const std::string &name, int M, int N, Lin &out) -> fm_status {
+    TRY(dalloc(h, &out.w, (size_t)M * N));
+    TRY(put_bf16(h, ts, name + ".weight", out.w, (int64_t)M * N, s));
+    TRY(dalloc(h, &out.b, M));
+    return put_bf16(h, ts, name + ".bias", out.b, M, s, true);
+  };
+  Lin te1, te2, je1, je2;
+  fm_status st;
+  if ((st = load("time_embed.linear_1", cond_dim, time_dim, te1)) != FM_OK ||
+      (st = load("time_embed.linear_2", cond_dim, cond_dim, te2)) != FM_OK ||
+      (st = load("jump_embed.linear_1", cond_dim, time_dim, je1)) != FM_OK ||
+      (st = load("jump_embed.linear_2", cond_dim, cond_dim, je2)) != FM_OK)
+    return done(st);
+  std::vector<Lin> ada(nb);
+  for (int n = 0; n < nb; ++n) {
+    const std::string name = n < 3 * L ? "layers." + std::to_string(n / 3) + "." +
+                                             (n % 3 == 0 ? "self_attn_adaln" : n % 3 == 1 ? "cross_attn_adaln" : "mlp_adaln") +
+                                             ".linear"
+                                       : "final_adaln.linear";
+    if ((st = load(name, D3, cond_dim, ada[n])) != FM_OK) return done(st);
+  }
+  float *e = nullptr, *hid = nullptr, *tsv = nullptr, *tjv = nullptr;
+  if ((st = dalloc(h, &e, time_dim)) != FM_OK || (st = dalloc(h, &hid, cond_dim)) != FM_OK ||
+      (st = dalloc(h, &tsv, cond_dim)) != FM_OK || (st = dalloc(h, &tjv, cond_dim)) != FM_OK)
+    return done(st);
+  auto run = [&]() -> cudaError_t {
+    cudaError_t r;
+    // ts = linear_2(SiLU(linear_1(embed(s)))), tj likewise for t
+    if ((r = launch_time_embed(e, time_dim, time_scale, s_time, s)) != cudaSuccess) return r;
+    if ((r = launch_setup_linear(te1.w, te1.b, e, nullptr, cond_dim, time_dim, 0, hid, s)) != cudaSuccess) return r;
+    if ((r = launch_setup_linear(te2.w, te2.b, hid, nullptr, cond_dim, cond_dim, 1, tsv, s)) != cudaSuccess) return r;
+    if ((r = launch_time_embed(e, time_dim, time_scale, t_time, s)) != cudaSuccess) return r;
+    if ((r = launch_setup_linear(je1.w, je1.b, e, nullptr, cond_dim, time_dim, 0, hid, s)) != cudaSuccess) return r;
+    if ((r = launch_setup_linear(je2.w, je2.b, hid, nullptr, cond_dim, cond_dim, 1, tjv, s)) != cudaSuccess) return r;
+    // every adaLN block from cond = SiLU(ts + tj)
+    for (int n = 0; n < nb; ++n)
+      if ((r = launch_setup_linear(ada[n].w, ada[n].b, tsv, tjv, D3, cond_dim, 2, table_dev + (size_t)n * D3, s)) !=
+          cudaSuccess)
+        return r;
+    return cudaStreamSynchronize(s);
+  };
+  const cudaError_t r = run();
+  if (r != cudaSuccess) return done(fail(h, FM_ERR_CUDA, "time conditioning: %s", cudaGetErrorString(r)));
+  return done(FM_OK);
 }
 
 fm_status fm_synchronize(fm_handle *h, void *stream) {
@@ -1618,6 +1910,11 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
       size = (int64_t)h->cache_plane * 2;
       break;
     }
+    case FM_DEBUG_STEP_TRACE:
+      if (!h->step_trace) return fail(h, FM_ERR_INVALID_ARG, "no trace recorded (set FM_DEBUG_TRACE before a draft)");
+      src = h->step_trace;
+      size = (int64_t)h->step_trace_phases * h->n_sm * kStepTraceSlots * 8;
+      break;
     case FM_DEBUG_H0:
       if (!h->h0) return fail(h, FM_ERR_INVALID_ARG, "no h0 for this variant");
       src = h->h0;
@@ -1701,7 +1998,7 @@ const char *fm_status_str(fm_status s) {
   return "unknown status";
 }
 
-// With a null handle: the reason the last fm_create on this thread failed.
+// With a null handle: the reason the last failed fm_create or fm_time_conditioning on this thread.
 const char *fm_last_error(const fm_handle *h) { return h ? h->err.c_str() : g_create_error.c_str(); }
 
 void fm_destroy(fm_handle *h) {

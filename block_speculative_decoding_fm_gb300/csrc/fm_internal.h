@@ -108,6 +108,8 @@ struct GemvArgs {
   const float2 *rope;         // [positions][hd / 2] (cos, sin)
   float qk_eps;
   SegDesc segs[kMaxSegs];
+  float *Y2;                  // E_RESID: a second copy of the stored rows (debug), or null
+  int32_t ldy2;
   // self-attention handoff: after the q/k/v segments of a head are stored, the
   // last CTA to finish one computes that head's attention over the T rows.
   int32_t *tickets;           // [n_heads] zero-initialised, self-resetting
@@ -157,6 +159,93 @@ struct LmArgs {
   float *logits;             // optional [T][V] store (debug), null in the hot path
 };
 
+// --- the persistent draft step (k_step.cu) -----------------------------------
+// One launch runs a program of phases separated by grid-wide barriers.  A
+// linear phase concatenates the 64-column weight chunks of its jobs (tile-major,
+// so a run of chunks is one contiguous byte range of a job's tiled weights);
+// CTA b of G owns chunks [b*NC/G, (b+1)*NC/G).  The part of one 128-row tile a
+// CTA owns is a segment; its partial sums go to global memory and the last
+// contributor of the tile (a ticket) adds them in CTA order and runs the
+// epilogue.  An attention phase splits every head's keys over CTAs.
+constexpr int kStepMaxJobs = 2;
+constexpr int kStepMaxSeg = 3;         // segments one CTA may own in a phase
+constexpr int kStepTileTickets = 1024; // tickets of tile reductions; then per-head tickets
+constexpr int kStepHeadTickets = 256;
+enum StepKind : int32_t { PH_LINEAR = 0, PH_ATTN = 1 };
+
+struct StepJob {
+  GemvArgs g;
+  int32_t chunk0;      // first chunk of the job in the phase's chunk sequence
+  int32_t nchunks;     // tiles * cpt
+  int32_t cpt;         // chunks per tile (K / 64)
+  int32_t tile0;       // first tile of the job in the phase's tile sequence
+  int32_t self_tail;   // 1: the last of each head's q, k, v tile epilogues runs the block attention of that head
+  int32_t pad[3];
+};
+
+struct StepAttn {
+  const float *Q;      // [T][ldq] f32 queries (head h at column h * hd)
+  int32_t ldq;
+  int32_t max_ctx, n_heads, hd;
+  const __half *Kc, *Vc;   // head-major caches [n_heads][max_ctx][hd]
+  int32_t nsp;         // CTAs (key ranges) per head
+  int32_t L_src;       // 0: sp->L, 1: sp->pos + 1
+  int32_t L_add;
+  int32_t prefetched;  // 1: an earlier phase requested the stable rows of the first two key stages
+  float scale_log2;    // log2(e) / sqrt(hd)
+  int32_t ldo;
+  float *out;          // [T][ldo]
+};
+
+struct StepPhase {
+  int32_t kind;        // StepKind
+  int32_t njobs;
+  int32_t nchunks;     // linear: chunks of all jobs
+  int32_t ntiles;      // linear: tiles of all jobs
+  int32_t prefetch;    // >= 0: phase index of an attention phase whose stable key rows this phase requests early
+  int32_t pad[3];
+  StepJob jobs[kStepMaxJobs];
+  StepAttn at;
+};
+
+struct StepArgs {
+  const StepPhase *ph;
+  int32_t n_phases;
+  int32_t T;
+  const StepParams *sp;
+  uint32_t *bar;       // [0]: arrivals, [32]: generation (separate cache lines)
+  int32_t *tickets;    // [kStepTileTickets + 2 * kStepHeadTickets], zero-initialised, self-resetting
+  float *part;         // [gridDim][kStepMaxSeg][kMaxT][kTile] partial tiles
+  float *apart;        // attention partials per CTA: [kMaxT][hd] unnormalised rows, then [kMaxT] (max, sum)
+  int32_t *err;
+  uint64_t *trace;     // null, or [n_phases][gridDim][kStepTraceSlots] globaltimer stamps (ns)
+};
+// trace slots per (phase, CTA): 0 workers start the phase (barrier passed),
+// 1 staging done, 2 epilogues done (arrive), 3 the producer issued the phase's
+// last copy, 4 the MMA warp committed the phase's last segment, 5 row stats loaded
+constexpr int kStepTraceSlots = 8;
+
+// chunk ownership: CTA b of G owns chunks [step_lo(b), step_lo(b + 1)) of nc
+__host__ __device__ __forceinline__ int step_lo(int b, int nc, int G) { return (int)(((long long)b * nc) / G); }
+// the CTA that owns chunk c (nc > c >= 0)
+__host__ __device__ __forceinline__ int step_owner(int c, int nc, int G) {
+  return (int)(((long long)(c + 1) * G - 1) / nc);
+}
+// job of chunk c in a phase
+__host__ __device__ __forceinline__ int step_job(const StepPhase &P, int c) {
+  return (P.njobs > 1 && c >= P.jobs[1].chunk0) ? 1 : 0;
+}
+// phase-wide tile of chunk c
+__host__ __device__ __forceinline__ int step_tile(const StepPhase &P, int c) {
+  const StepJob &J = P.jobs[step_job(P, c)];
+  return J.tile0 + (c - J.chunk0) / J.cpt;
+}
+
+size_t step_smem_bytes();
+size_t step_apart_floats(int hd);
+cudaError_t launch_step(const StepArgs &a, int grid, cudaStream_t s, int attrs);
+int step_max_grid();   // CTAs of the step kernel one SM holds (must be >= 1)
+
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t s, bool pdl);
 size_t gemv_smem_bytes(const GemvArgs &a, int mt);
@@ -183,6 +272,9 @@ cudaError_t launch_row_stats(const float *x, int32_t rows, int32_t d, float2 *st
 cudaError_t launch_accept(int32_t n, int32_t block, const int32_t *draft, const int32_t *target,
                           const int32_t *k, int32_t *acc, int32_t *bonus, cudaStream_t s);
 cudaError_t launch_wait_selftest(int32_t *err, long long budget_cycles, cudaStream_t s);
+cudaError_t launch_time_embed(float *e, int32_t time_dim, double time_scale, double time, cudaStream_t s);
+cudaError_t launch_setup_linear(const __nv_bfloat16 *W, const __nv_bfloat16 *b, const float *x, const float *x2,
+                                int32_t M, int32_t N, int32_t act, float *y, cudaStream_t s);
 cudaError_t launch_fill_f32(float *p, size_t n, float v, cudaStream_t s);
 // [M][K] bf16 row-major -> GEMV tile layout (zero rows past M)
 cudaError_t launch_tile_weights(const __nv_bfloat16 *src, int32_t M, int32_t K, uint8_t *dst, cudaStream_t s);

@@ -119,6 +119,35 @@ __global__ void row_stats_kernel(const float *x, int rows, int d, float2 *st) {
   if (lane == 0 && row < rows) st[tile * kMaxT + row] = make_float2(mean, q);
 }
 
+// ---- time conditioning (flashmap_drafter.js, ``timeConditioning``): set-up only ----
+// [cos a_i | sin a_i], a_i = time * time_scale * exp(-ln(10000) i / half), in double
+__global__ void time_embed_kernel(float *e, int time_dim, double time_scale, double time) {
+  const int half = time_dim / 2;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    const double a = time * time_scale * exp(-log(10000.0) * (double)i / (double)half);
+    e[i] = (float)cos(a);
+    e[half + i] = (float)sin(a);
+  }
+}
+__device__ __forceinline__ float silu(float v) { return v / (1.f + expf(-v)); }
+// y[m] = sum_k W[m][k] x'[k] + b[m] (bf16 W [M][N], optional bias), one warp per
+// row; x' = x (act 0), SiLU(x) (act 1) or SiLU(x + x2) (act 2)
+__global__ void setup_linear_kernel(const __nv_bfloat16 *W, const __nv_bfloat16 *b, const float *x, const float *x2,
+                                    int M, int N, int act, float *y) {
+  const int m = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (m >= M) return;
+  float acc = 0.f;
+  for (int k = lane; k < N; k += 32) {
+    float v = x[k];
+    if (act == 1) v = silu(v);
+    if (act == 2) v = silu(v + x2[k]);
+    acc = fmaf(__bfloat162float(W[(size_t)m * N + k]), v, acc);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) y[m] = acc + (b ? __bfloat162float(b[m]) : 0.f);
+}
+
 // The failure path of the bounded waits: one thread waits on an mbarrier phase
 // that nothing completes, with a short budget; the wait gives up, raises the
 // error word and the kernel returns (nothing hangs, nothing faults).
@@ -254,6 +283,17 @@ cudaError_t launch_fill_f32(float *p, size_t n, float v, cudaStream_t s) {
 
 cudaError_t launch_wait_selftest(int32_t *err, long long budget_cycles, cudaStream_t s) {
   wait_selftest_kernel<<<1, 32, 0, s>>>(err, budget_cycles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_time_embed(float *e, int32_t time_dim, double time_scale, double time, cudaStream_t s) {
+  time_embed_kernel<<<1, 256, 0, s>>>(e, time_dim, time_scale, time);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_setup_linear(const __nv_bfloat16 *W, const __nv_bfloat16 *b, const float *x, const float *x2,
+                                int32_t M, int32_t N, int32_t act, float *y, cudaStream_t s) {
+  setup_linear_kernel<<<(M + 7) / 8, 256, 0, s>>>(W, b, x, x2, M, N, act, y);
   return cudaGetLastError();
 }
 

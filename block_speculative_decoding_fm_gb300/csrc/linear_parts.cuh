@@ -323,6 +323,8 @@ __device__ void epilogue_unit(const GemvArgs &a, int t, int m0, float (&v)[4], i
       }
       if (live)
         __stcg(reinterpret_cast<float4 *>(a.Y + (size_t)t * a.ldy + mrow), make_float4(v[0], v[1], v[2], v[3]));
+      if (a.Y2 && live)
+        __stcg(reinterpret_cast<float4 *>(a.Y2 + (size_t)t * a.ldy2 + mrow), make_float4(v[0], v[1], v[2], v[3]));
       if (a.ylm && live) {
         // the same rows split into the lm_head's resident operand (hi row, lo row 8 further)
         uint32_t hw[2], lw[2];

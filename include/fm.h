@@ -113,7 +113,8 @@ typedef struct fm_handle fm_handle;
  * ([FM] FlashMapDrafter.load / upload / init; [DF] DflashDrafter.load).
  *   modulation_host: [FM] the adaLN table [(3*n_layers+1) * 3 * dim] f32 in
  *     blocks [scale dim | shift dim | gate dim] for (self, cross, mlp) of every
- *     layer and the final norm ([FM] timeConditioning output); NULL for [DF].
+ *     layer and the final norm ([FM] timeConditioning output, e.g. from
+ *     fm_time_conditioning); host or device memory; NULL for [DF].
  *   On success *out owns: the repacked weights, per-sequence caches of max_ctx
  *   rows, work buffers, and the constant start row h0 = x_embed(state_norm(
  *   mean row of E)) ([FM] init).  Synchronises the stream before returning.
@@ -123,6 +124,33 @@ typedef struct fm_handle fm_handle;
  */
 FM_API fm_status fm_create(const fm_config *cfg, const fm_tensor *weights, int32_t n_weights,
                     const float *modulation_host, void *stream, fm_handle **out);
+
+/*
+ * fm_time_conditioning -- the adaLN table fm_create takes for [FM], computed
+ * from the checkpoint's time-conditioning linears for the jump s -> t of the
+ * flow map ([FM] timeConditioning; the page drafts with s = 0, t = 1):
+ *   e(x) = [cos a_i | sin a_i], a_i = x * time_scale * exp(-ln(10000) i / half),
+ *   half = time_dim / 2 ([FM] CFG.timeDim, CFG.timeScale);
+ *   ts = time_embed.linear_2(SiLU(time_embed.linear_1(e(s)))), tj likewise with
+ *   jump_embed and e(t); cond = SiLU(ts + tj), SiLU(x) = x / (1 + exp(-x));
+ *   block n of the table = adaLN linear n of cond, n over
+ *   layers.{l}.{self_attn_adaln,cross_attn_adaln,mlp_adaln}.linear then
+ *   final_adaln.linear, each [scale dim | shift dim | gate dim].
+ * weights: bf16 tensors (host or device) time_embed.linear_{1,2}.{weight,bias},
+ *   jump_embed.linear_{1,2}.{weight,bias} (linear_1 [cond_dim][time_dim],
+ *   linear_2 [cond_dim][cond_dim]) and every adaLN linear .weight
+ *   [3 dim][cond_dim] / .bias [3 dim]; a missing bias is read as zero.  Other
+ *   tensors in the list are ignored, so the full checkpoint list may be passed.
+ * table_dev: device f32 [(3 n_layers + 1) * 3 * dim], caller-owned; pass it to
+ *   fm_create as the modulation table (device memory is accepted there).
+ * Set-up: allocates temporary device buffers and synchronises the stream.
+ * Errors: FM_ERR_INVALID_ARG (null or misaligned pointer, odd time_dim,
+ *   missing / mis-sized tensor, not [FM]), FM_ERR_OOM, FM_ERR_CUDA; the reason
+ *   is in fm_last_error(NULL).
+ */
+FM_API fm_status fm_time_conditioning(const fm_config *cfg, const fm_tensor *weights, int32_t n_weights,
+                                      int32_t time_dim, int32_t cond_dim, float time_scale, float s, float t,
+                                      float *table_dev, void *stream);
 
 /*
  * fm_context_append -- context injection ([FM] extendContext; [DF] Eq 2 and
@@ -248,6 +276,9 @@ FM_API fm_status fm_selftest_wait_timeout(fm_handle *h, int32_t budget_us, void 
 #define FM_DEBUG_CACHE_K 3  /* index = layer: cache K of seq, [n_heads][max_ctx][head_dim] as f16 bits */
 #define FM_DEBUG_CACHE_V 4  /* index = layer: cache V, same layout */
 #define FM_DEBUG_H0 5       /* [FM] the constant start row h0 [dim] f32 */
+#define FM_DEBUG_STEP_TRACE 6 /* [FM] persistent step trace of the last traced draft: u64 [phases][SMs][8]
+                                 globaltimer ns: 0 phase start, 1 staged, 2 done, 3 last copy issued,
+                                 4 last MMA committed, 5 row statistics read; 0 = no event */
 
 /*
  * fm_debug_copy -- copy nbytes of the selected buffer, starting at byte
@@ -260,6 +291,7 @@ FM_API fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t 
 /* fm_set_debug flags */
 #define FM_DEBUG_KEEP_HIDDEN 1 /* keep every layer's block hidden rows for FM_DEBUG_HIDDEN (adds copies) */
 #define FM_DEBUG_PROFILE 2     /* bracket every kernel launch with CUDA events (serialises the chain) */
+#define FM_DEBUG_TRACE 4       /* record per-phase timestamps of the persistent draft step (FM_DEBUG_STEP_TRACE) */
 
 /* Debug switches for later calls (0 = the plain hot path).  Errors: FM_ERR_INVALID_ARG. */
 FM_API fm_status fm_set_debug(fm_handle *h, int32_t flags);
@@ -287,7 +319,8 @@ FM_API fm_status fm_memory_bytes(const fm_handle *h, int64_t *bytes);
 FM_API fm_status fm_last_launch_count(const fm_handle *h, int32_t *count);
 
 FM_API const char *fm_status_str(fm_status s);
-FM_API const char *fm_last_error(const fm_handle *h);   /* never NULL; "" when no error; NULL h: the last failed fm_create on this thread */
+FM_API const char *fm_last_error(const fm_handle *h);   /* never NULL; "" when no error; NULL h: the last failed
+                                                            fm_create / fm_time_conditioning on this thread */
 
 /* Free everything the handle owns.  NULL is ignored. */
 FM_API void fm_destroy(fm_handle *h);

@@ -356,3 +356,44 @@ def test_bounded_wait_gives_up_and_is_reported():
     check_draft(p, got, ref)
     fm.fm_synchronize(p.h)
     p.close()
+
+
+def test_time_conditioning_table_and_draft():
+    """fm_time_conditioning builds the adaLN table of the jump 0 -> 1 from the
+    time-conditioning linears on the device; the table matches the oracle's,
+    and a drafter created from it drafts what the oracle drafts from the
+    oracle's own table."""
+    import torch
+    import block_speculative_decoding_fm_gb300 as fm
+    from oracle import FlashMap
+    from oracle.timecond import time_conditioning
+    cfg = S.tiny_config(max_ctx=96)
+    w = S.gen_weights(cfg, 1016)
+    tw = S.gen_time_cond_weights(cfg, 1016, time_dim=256, cond_dim=256)
+    table = torch.full(((3 * cfg.n_layers + 1) * 3 * cfg.dim,), float("nan"), device="cuda")
+    # the whole checkpoint list: the entry point picks the tensors it needs
+    fm.fm_time_conditioning(cfg, fm.weight_items({**w, **tw}), 256, 256, 1000.0, 0.0, 1.0, table)
+    want = time_conditioning({n: t.data for n, t in tw.items()}, cfg.n_layers, cfg.dim, 256, 1000.0, 0.0, 1.0)
+    got = table.cpu().numpy()
+    assert np.isfinite(got).all()
+    assert rel_l2(got, want) < 1e-5, rel_l2(got, want)
+    h = fm.fm_create(cfg, fm.weight_items(w), table)
+    o = FlashMap(cfg, {n: t.data for n, t in w.items()}, want, False)
+    st = o.new_state()
+    feats = S.gen_features(S.streams(1016)["features"], 30, cfg.feat_dim)
+    fm.fm_context_append(h, 0, torch.from_numpy(feats).cuda(), 30, 0)
+    o.context_append(st, feats, 0)
+    tok = torch.zeros((1, cfg.block), dtype=torch.int32, device="cuda")
+    fm.fm_draft(h, [0], [55], [30], tok)
+    torch.cuda.synchronize()
+    ref = o.draft(st, 55, 30)
+    y = np.empty((cfg.block, cfg.target_dim), np.float32)
+    fm.fm_debug_copy(h, fm.FM_DEBUG_HEAD_OUT, 0, 0, y)
+    assert rel_l2(y, ref.head_out) < REL_L2
+    assert tokens_match(tok.cpu().numpy()[0], ref.tokens, ref.logits)
+    fm.fm_destroy(h)
+    # a missing linear is reported, nothing is written
+    with pytest.raises(fm.FmError) as e:
+        fm.fm_time_conditioning(cfg, fm.weight_items({k: v for k, v in tw.items() if "final_adaln" not in k}),
+                                256, 256, 1000.0, 0.0, 1.0, table)
+    assert e.value.status == fm.FM_ERR_INVALID_ARG
