@@ -95,10 +95,8 @@ struct fm_handle {
   // ---- the persistent draft step ----
   bool use_step = true;
   int step_attrs = 3;                 // launch attributes the device accepted (cooperative | PDL)
+  int step_clusters = 0;              // co-resident clusters of the step kernel
   uint32_t *step_bar = nullptr;       // grid barrier words
-  int32_t *step_tickets = nullptr;    // tile / head tickets (self-resetting)
-  float *step_part = nullptr;         // partial tiles [n_sm][kStepMaxSeg][kMaxT][kTile]
-  float *step_apart = nullptr;        // attention partials [n_sm][kMaxT * hd + 2 kMaxT]
   // device programs by (sequence, key splits, debug, parameter slot): the jobs
   // carry the address of the parameter slot their chain reads
   std::map<std::tuple<int, int, int, const void *>, StepPhase *> step_progs;
@@ -655,65 +653,55 @@ FlashMapPlan flashmap_plan(fm_handle *h, int seq, const StepParams *sp, int n_pe
   return pl;
 }
 
-// Cross-attention key ranges per head in the persistent step: enough CTAs per
-// head to fill the GPU, at least 64 keys each.
-int step_splits(const fm_handle *h, int L) {
-  int sp = h->n_sm / h->cfg.n_heads;
-  const int need = (L + 63) / 64;
-  if (sp > need) sp = need;
-  return sp < 1 ? 1 : sp;
-}
-
-// The persistent program of one FlashMap draft (layers + head): one linear
-// phase per product, one attention phase per layer.  Returns false when the
-// schedule does not fit the kernel's limits (the caller then runs the chain).
-bool flashmap_step_program(fm_handle *h, int seq, const FlashMapPlan &pl, int nsp, std::vector<StepPhase> &ph) {
+// The persistent program of one FlashMap draft (layers + head): per layer the
+// q/k/v product, o with the block self-attention as its prologue, cross-q with
+// the cross-attention as its tail, cross-o, fc1 and fc2; then the head.
+// Returns false when the shapes do not fit the kernel's limits (the caller
+// then runs the launch-per-product chain).
+bool flashmap_step_program(fm_handle *h, int seq, const FlashMapPlan &pl, std::vector<StepPhase> &ph) {
   const fm_config &c = h->cfg;
-  const int D = c.dim, L = c.n_layers, G = h->n_sm;
-  if (c.block > 16 || c.n_heads * nsp > G || c.n_heads > kStepHeadTickets) return false;
-  auto linear = [&](const GemvArgs &g, int self_tail) {
+  const int D = c.dim, L = c.n_layers, hd = c.head_dim, ncl = h->step_clusters;
+  if (ncl < 1 || c.block > 16) return false;
+  int rot = 0;
+  auto linear = [&](const GemvArgs &g, int map_mod) {
     StepPhase P;
     memset(&P, 0, sizeof P);
-    P.kind = PH_LINEAR;
-    P.njobs = 1;
-    P.prefetch = -1;
-    StepJob &J = P.jobs[0];
-    J.g = g;
-    J.cpt = g.K / 64;
-    J.nchunks = ((g.M + kTile - 1) / kTile) * J.cpt;
-    J.chunk0 = 0;
-    J.tile0 = 0;
-    J.self_tail = self_tail;
-    P.nchunks = J.nchunks;
+    P.g = g;
+    P.cpt = g.K / 64;
     P.ntiles = (g.M + kTile - 1) / kTile;
+    P.map_mod = map_mod > 0 ? map_mod : P.ntiles;
+    P.rot = rot % ncl;
+    rot += P.ntiles;   // the clusters that got an extra tile move on from phase to phase
+    P.prologue = SP_NONE;
+    P.tail = ST_NONE;
     ph.push_back(P);
+    return &ph.back();
   };
-  const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  const float scale = (float)(1.0 / std::sqrt((double)hd));
   for (int l = 0; l < L; ++l) {
-    linear(pl.qkv[l], 1);
-    linear(pl.o[l], 0);
-    linear(pl.cq[l], 0);
-    ph.back().prefetch = (int)ph.size();   // the attention phase that follows
-    StepPhase A;
-    memset(&A, 0, sizeof A);
-    A.kind = PH_ATTN;
-    A.prefetch = -1;
+    linear(pl.qkv[l], 0);
+    StepPhase *o = linear(pl.o[l], 0);
+    o->prologue = SP_SELF_ATTN;
+    o->at.hd = hd;
+    o->at.scale = scale;
+    o->at.D = D;
+    o->at.qkv = h->qkv;
+    StepPhase *q = linear(pl.cq[l], 0);
+    q->tail = ST_CROSS_ATTN;
     Seg2 kv = h->kv(seq, l);
-    A.at.Q = h->qc;
-    A.at.ldq = D;
-    A.at.max_ctx = c.max_ctx;
-    A.at.n_heads = c.n_heads;
-    A.at.hd = c.head_dim;
-    A.at.Kc = kv.k;
-    A.at.Vc = kv.v;
-    A.at.nsp = nsp;
-    A.at.L_src = 1;
-    A.at.L_add = 0;
-    A.at.prefetched = 1;
-    A.at.scale_log2 = scale_log2;
-    A.at.out = h->attn;
-    A.at.ldo = D;
-    ph.push_back(A);
+    q->at.max_ctx = c.max_ctx;
+    q->at.n_heads = c.n_heads;
+    q->at.hd = hd;
+    q->at.L_src = 1;
+    q->at.L_add = 0;
+    q->at.scale = scale;
+    q->at.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+    q->at.Kc = kv.k;
+    q->at.Vc = kv.v;
+    q->at.Q = h->qc;
+    q->at.ldq = D;
+    q->at.out = h->attn;
+    q->at.ldo = D;
     linear(pl.co[l], 0);
     linear(pl.f1[l], 0);
     GemvArgs f2 = pl.f2[l];
@@ -724,36 +712,37 @@ bool flashmap_step_program(fm_handle *h, int seq, const FlashMapPlan &pl, int ns
     linear(f2, 0);
   }
   linear(pl.head, 0);
-  // the kernel's limits: segments per CTA, tickets, and the K of every job
-  for (const StepPhase &P : ph) {
-    if (P.kind != PH_LINEAR) continue;
-    if (P.ntiles > kStepTileTickets) return false;
-    for (int j = 0; j < P.njobs; ++j)
-      if (P.jobs[j].g.K % 64 || P.jobs[j].cpt < 1) return false;
-    for (int b = 0; b < G; ++b) {
-      const int lo = step_lo(b, P.nchunks, G), hi = step_lo(b + 1, P.nchunks, G);
-      int n = 0;
-      for (int cc = lo; cc < hi;) {
-        const int j = step_job(P, cc);
-        const StepJob &J = P.jobs[j];
-        const int tile = (cc - J.chunk0) / J.cpt;
-        cc = std::min(hi, J.chunk0 + (tile + 1) * J.cpt);
-        ++n;
-      }
-      if (n > kStepMaxSeg) return false;
+  // the kernel's limits
+  for (size_t i = 0; i < ph.size(); ++i) {
+    const StepPhase &P = ph[i];
+    if (P.g.K % 64 || P.cpt < 1) return false;
+    std::vector<int> per(ncl, 0);
+    for (int t = 0; t < P.ntiles; ++t) ++per[step_cluster_of(P, t, ncl)];
+    const int most = *std::max_element(per.begin(), per.end());
+    if (most > kStepMaxTiles) return false;
+    // the rank's K slice fits one staged piece when it is formed in shared memory
+    int slice = 0;
+    for (int r = 0; r < kStepCS; ++r) slice = std::max(slice, (step_klo(r + 1, P.cpt) - step_klo(r, P.cpt)) * 64);
+    if (P.prologue == SP_SELF_ATTN) {
+      if (slice > 256 || D % hd) return false;
+      const int heads = slice / hd + 1;
+      if ((size_t)heads * 3 * 16 * (hd + 4) * 4 > 52 * 1024) return false;
     }
-    // every chunk is owned once: the owner of chunk c has c inside its range
-    for (int cc = 0; cc < P.nchunks; ++cc) {
-      const int o = step_owner(cc, P.nchunks, G);
-      if (o < 0 || o >= G || step_lo(o, P.nchunks, G) > cc || step_lo(o + 1, P.nchunks, G) <= cc) return false;
+    // the cross-attention tail requests its first key stage in the partial area
+    // behind the previous phase's two tiles
+    if (P.tail == ST_CROSS_ATTN) {
+      if (most > 2 || i == 0 || hd % 16) return false;
+      std::vector<int> prev(ncl, 0);
+      for (int t = 0; t < ph[i - 1].ntiles; ++t) ++prev[step_cluster_of(ph[i - 1], t, ncl)];
+      if (*std::max_element(prev.begin(), prev.end()) > 2) return false;
     }
   }
   return true;
 }
 
-fm_status run_step(fm_handle *h, int seq, int nsp, const std::vector<StepPhase> &prog, const StepParams *sp, int T,
+fm_status run_step(fm_handle *h, int seq, const std::vector<StepPhase> &prog, const StepParams *sp, int T,
                    double bytes, cudaStream_t s) {
-  const auto key = std::make_tuple(seq, nsp, h->debug & FM_DEBUG_KEEP_HIDDEN, (const void *)sp);
+  const auto key = std::make_tuple(seq, 0, h->debug & FM_DEBUG_KEEP_HIDDEN, (const void *)sp);
   auto it = h->step_progs.find(key);
   if (it == h->step_progs.end()) {
     StepPhase *d = nullptr;
@@ -766,22 +755,21 @@ fm_status run_step(fm_handle *h, int seq, int nsp, const std::vector<StepPhase> 
   a.ph = it->second;
   a.n_phases = (int)prog.size();
   a.T = T;
+  a.n_clusters = h->step_clusters;
   a.sp = sp;
   a.bar = h->step_bar;
-  a.tickets = h->step_tickets;
-  a.part = h->step_part;
-  a.apart = h->step_apart;
   a.err = h->dev_err;
+  const int G = h->step_clusters * kStepCS;
   if (h->debug & FM_DEBUG_TRACE) {
     if (!h->step_trace || h->step_trace_phases < (int)prog.size()) {
-      TRY(dalloc(h, &h->step_trace, (size_t)prog.size() * h->n_sm * kStepTraceSlots));
+      TRY(dalloc(h, &h->step_trace, (size_t)prog.size() * G * kStepTraceSlots));
       h->step_trace_phases = (int)prog.size();
     }
-    CK(cudaMemsetAsync(h->step_trace, 0, (size_t)prog.size() * h->n_sm * kStepTraceSlots * 8, s));
+    CK(cudaMemsetAsync(h->step_trace, 0, (size_t)prog.size() * G * kStepTraceSlots * 8, s));
     a.trace = h->step_trace;
   }
   ProfScope ps(h, s, "draft_step", bytes);
-  CK(launch_step(a, h->n_sm, s, h->step_attrs));
+  CK(launch_step(a, h->step_clusters, s, h->step_attrs));
   ++h->last_launches;
   return FM_OK;
 }
@@ -794,14 +782,13 @@ fm_status flashmap_draft_launch(fm_handle *h, int seq, int pos, const StepParams
   TRY(run_gemv(h, pl.kv, s, n_pend ? "gemv.kv_fused" : "gemv.kv_anchor", n_pend + 1));
 
   if (h->use_step) {
-    const int nsp = step_splits(h, pos + 1);
     std::vector<StepPhase> prog;
-    if (flashmap_step_program(h, seq, pl, nsp, prog)) {
+    if (flashmap_step_program(h, seq, pl, prog)) {
       // algorithmic bytes: every weight of the layers and the head once, the keys and values read once
       // (q/k/v 3 D^2, o, cross q, cross o D^2 each, fc1 and fc2 F D per layer; the head Ht D; bf16)
       const double bytes = 2.0 * ((double)L * (6.0 * D * D + 2.0 * F * D) + (double)Ht * D) +
                            (double)L * (pos + 1) * D * 2 * 2;
-      TRY(run_step(h, seq, nsp, prog, sp, B, bytes, s));
+      TRY(run_step(h, seq, prog, sp, B, bytes, s));
       return run_lmhead(h, h->Y, B, sp, nullptr, nullptr, s, h->ylm);
     }
   }
@@ -1144,8 +1131,7 @@ fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens,
     p.L = pos;  // context rows 0 .. pos-1; the block's own keys go to rows pos .. pos+block-1
     L_now = pos + c.block;
   }
-  const int splits = h->use_step && c.variant == FM_VARIANT_FLASHMAP ? step_splits(h, L_now) : attn_splits(h, L_now);
-  const uint64_t key = chain_key(1, seq, c.block + 64 * n_pend, splits, h->debug);
+  const uint64_t key = chain_key(1, seq, c.block + 64 * n_pend, attn_splits(h, L_now), h->debug);
   return run_chain(h, key, p, s, [&](const StepParams *sp, cudaStream_t st) {
     return c.variant == FM_VARIANT_FLASHMAP ? flashmap_draft_launch(h, seq, pos, sp, n_pend, st)
                                             : dflash_draft_launch(h, seq, pos, sp, st);
@@ -1231,10 +1217,6 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   CK(cudaMemsetAsync(h->dev_err, 0, 4, s));
   TRY(dalloc(h, &h->step_bar, 64));
   CK(cudaMemsetAsync(h->step_bar, 0, 64 * 4, s));
-  TRY(dalloc(h, &h->step_tickets, (size_t)kStepTileTickets + 2 * kStepHeadTickets));
-  CK(cudaMemsetAsync(h->step_tickets, 0, ((size_t)kStepTileTickets + 2 * kStepHeadTickets) * 4, s));
-  TRY(dalloc(h, &h->step_part, (size_t)h->n_sm * kStepMaxSeg * kMaxT * kTile));
-  TRY(dalloc(h, &h->step_apart, (size_t)h->n_sm * step_apart_floats(c.head_dim)));
   TRY(dalloc(h, &h->sp_dev, kParamSlots));
   CK(cudaMallocHost(&h->sp_host, sizeof(StepParams) * kParamSlots));
   memset(h->sp_host, 0, sizeof(StepParams) * kParamSlots);
@@ -1249,18 +1231,17 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   // the persistent draft step needs one co-resident CTA per SM; an empty program
   // finds the launch attributes the device takes (outside any stream capture)
   const char *ps = getenv("FM_PERSISTENT");
-  h->use_step = (ps && ps[0] == '1') && c.variant == FM_VARIANT_FLASHMAP && step_max_grid() >= 1;
+  h->step_clusters = c.variant == FM_VARIANT_FLASHMAP ? step_max_clusters() : 0;
+  h->use_step = (ps && ps[0] == '1') && h->step_clusters >= 1;
   if (h->use_step) {
     StepArgs a;
     memset(&a, 0, sizeof a);
+    a.n_clusters = h->step_clusters;
     a.bar = h->step_bar;
-    a.tickets = h->step_tickets;
-    a.part = h->step_part;
-    a.apart = h->step_apart;
     a.err = h->dev_err;
     h->step_attrs = -1;
-    for (int attrs : {3, 1}) {
-      if (launch_step(a, h->n_sm, s, attrs) == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess) {
+    for (int attrs : {3, 1, 2, 0}) {
+      if (launch_step(a, h->step_clusters, s, attrs) == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess) {
         h->step_attrs = attrs;
         break;
       }
@@ -1913,7 +1894,7 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
     case FM_DEBUG_STEP_TRACE:
       if (!h->step_trace) return fail(h, FM_ERR_INVALID_ARG, "no trace recorded (set FM_DEBUG_TRACE before a draft)");
       src = h->step_trace;
-      size = (int64_t)h->step_trace_phases * h->n_sm * kStepTraceSlots * 8;
+      size = (int64_t)h->step_trace_phases * h->step_clusters * kStepCS * kStepTraceSlots * 8;
       break;
     case FM_DEBUG_H0:
       if (!h->h0) return fail(h, FM_ERR_INVALID_ARG, "no h0 for this variant");

@@ -160,51 +160,43 @@ struct LmArgs {
 };
 
 // --- the persistent draft step (k_step.cu) -----------------------------------
-// One launch runs a program of phases separated by grid-wide barriers.  A
-// linear phase concatenates the 64-column weight chunks of its jobs (tile-major,
-// so a run of chunks is one contiguous byte range of a job's tiled weights);
-// CTA b of G owns chunks [b*NC/G, (b+1)*NC/G).  The part of one 128-row tile a
-// CTA owns is a segment; its partial sums go to global memory and the last
-// contributor of the tile (a ticket) adds them in CTA order and runs the
-// epilogue.  An attention phase splits every head's keys over CTAs.
-constexpr int kStepMaxJobs = 2;
-constexpr int kStepMaxSeg = 3;         // segments one CTA may own in a phase
-constexpr int kStepTileTickets = 1024; // tickets of tile reductions; then per-head tickets
-constexpr int kStepHeadTickets = 256;
-enum StepKind : int32_t { PH_LINEAR = 0, PH_ATTN = 1 };
-
-struct StepJob {
-  GemvArgs g;
-  int32_t chunk0;      // first chunk of the job in the phase's chunk sequence
-  int32_t nchunks;     // tiles * cpt
-  int32_t cpt;         // chunks per tile (K / 64)
-  int32_t tile0;       // first tile of the job in the phase's tile sequence
-  int32_t self_tail;   // 1: the last of each head's q, k, v tile epilogues runs the block attention of that head
-  int32_t pad[3];
-};
+// One launch runs a program of phases separated by grid-wide barriers, on
+// clusters of kStepCS CTAs (one CTA per SM).  In a linear phase the 128-row
+// weight tiles are dealt to clusters: tile i goes to cluster
+// ((i % map_mod) + rot) % n_clusters.  Rank r of a cluster takes the same K
+// slice [r cpt / kStepCS, (r + 1) cpt / kStepCS) of every tile its cluster
+// owns, so it stages that slice of the activations once; the partial tiles
+// meet through distributed shared memory and rank r finishes rows r and
+// r + kStepCS of every tile (the fused epilogue).
+constexpr int kStepCS = 8;          // CTAs per cluster
+constexpr int kStepMaxTiles = 6;    // tiles one cluster may own in a phase
+enum StepPrologue : int32_t { SP_NONE = 0, SP_SELF_ATTN = 1 };
+enum StepTail : int32_t { ST_NONE = 0, ST_CROSS_ATTN = 1 };
 
 struct StepAttn {
-  const float *Q;      // [T][ldq] f32 queries (head h at column h * hd)
-  int32_t ldq;
   int32_t max_ctx, n_heads, hd;
-  const __half *Kc, *Vc;   // head-major caches [n_heads][max_ctx][hd]
-  int32_t nsp;         // CTAs (key ranges) per head
-  int32_t L_src;       // 0: sp->L, 1: sp->pos + 1
+  int32_t L_src;              // cross keys: 0: sp->L, 1: sp->pos + 1 (plus L_add)
   int32_t L_add;
-  int32_t prefetched;  // 1: an earlier phase requested the stable rows of the first two key stages
-  float scale_log2;    // log2(e) / sqrt(hd)
+  float scale;                // 1 / sqrt(hd)
+  float scale_log2;           // log2(e) / sqrt(hd)
   int32_t ldo;
-  float *out;          // [T][ldo]
+  const __half *Kc, *Vc;      // cross: head-major caches [n_heads][max_ctx][hd]
+  const float *Q;             // cross: queries [T][ldq] (head h at column h * hd)
+  int32_t ldq;
+  int32_t D;                  // self: width of each of q / k / v
+  const float *qkv;           // self: [T][3 D] rows (q, k, v)
+  float *out;                 // cross: attention rows [T][ldo]
 };
 
 struct StepPhase {
-  int32_t kind;        // StepKind
-  int32_t njobs;
-  int32_t nchunks;     // linear: chunks of all jobs
-  int32_t ntiles;      // linear: tiles of all jobs
-  int32_t prefetch;    // >= 0: phase index of an attention phase whose stable key rows this phase requests early
-  int32_t pad[3];
-  StepJob jobs[kStepMaxJobs];
+  GemvArgs g;
+  int32_t cpt;        // chunks per tile (K / 64)
+  int32_t ntiles;
+  int32_t map_mod;    // tile i -> cluster ((i % map_mod) + rot) % n_clusters
+  int32_t rot;
+  int32_t prologue;   // StepPrologue: SP_SELF_ATTN forms the activations as the block self-attention of q/k/v
+  int32_t tail;       // StepTail: ST_CROSS_ATTN attends the cluster's heads over the cache after the epilogue
+  int32_t pad[2];
   StepAttn at;
 };
 
@@ -212,39 +204,29 @@ struct StepArgs {
   const StepPhase *ph;
   int32_t n_phases;
   int32_t T;
+  int32_t n_clusters;
   const StepParams *sp;
   uint32_t *bar;       // [0]: arrivals, [32]: generation (separate cache lines)
-  int32_t *tickets;    // [kStepTileTickets + 2 * kStepHeadTickets], zero-initialised, self-resetting
-  float *part;         // [gridDim][kStepMaxSeg][kMaxT][kTile] partial tiles
-  float *apart;        // attention partials per CTA: [kMaxT][hd] unnormalised rows, then [kMaxT] (max, sum)
   int32_t *err;
   uint64_t *trace;     // null, or [n_phases][gridDim][kStepTraceSlots] globaltimer stamps (ns)
 };
 // trace slots per (phase, CTA): 0 workers start the phase (barrier passed),
-// 1 staging done, 2 epilogues done (arrive), 3 the producer issued the phase's
-// last copy, 4 the MMA warp committed the phase's last segment, 5 row stats loaded
+// 1 staging done, 2 phase done (arrive), 3 the producer issued the phase's last
+// copy, 4 the MMA warp committed the phase's last tile, 5 partials published,
+// 6 epilogues done
 constexpr int kStepTraceSlots = 8;
 
-// chunk ownership: CTA b of G owns chunks [step_lo(b), step_lo(b + 1)) of nc
-__host__ __device__ __forceinline__ int step_lo(int b, int nc, int G) { return (int)(((long long)b * nc) / G); }
-// the CTA that owns chunk c (nc > c >= 0)
-__host__ __device__ __forceinline__ int step_owner(int c, int nc, int G) {
-  return (int)(((long long)(c + 1) * G - 1) / nc);
+// the cluster that owns tile i of a phase
+__host__ __device__ __forceinline__ int step_cluster_of(const StepPhase &P, int i, int ncl) {
+  return ((i % P.map_mod) + P.rot) % ncl;
 }
-// job of chunk c in a phase
-__host__ __device__ __forceinline__ int step_job(const StepPhase &P, int c) {
-  return (P.njobs > 1 && c >= P.jobs[1].chunk0) ? 1 : 0;
-}
-// phase-wide tile of chunk c
-__host__ __device__ __forceinline__ int step_tile(const StepPhase &P, int c) {
-  const StepJob &J = P.jobs[step_job(P, c)];
-  return J.tile0 + (c - J.chunk0) / J.cpt;
-}
+// chunk range of rank r in every tile: [step_klo(r), step_klo(r + 1))
+__host__ __device__ __forceinline__ int step_klo(int r, int cpt) { return r * cpt / kStepCS; }
 
 size_t step_smem_bytes();
-size_t step_apart_floats(int hd);
-cudaError_t launch_step(const StepArgs &a, int grid, cudaStream_t s, int attrs);
-int step_max_grid();   // CTAs of the step kernel one SM holds (must be >= 1)
+// attrs: bit 0 = cooperative launch, bit 1 = programmatic stream serialisation
+cudaError_t launch_step(const StepArgs &a, int clusters, cudaStream_t s, int attrs);
+int step_max_clusters();   // clusters of the step kernel the device holds at once
 
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t s, bool pdl);

@@ -2,37 +2,37 @@
 //
 // The pages run the draft as a list of dispatches, one GEMM / attention / norm
 // kernel after another, each reading its weights once (flashmap_drafter.js,
-// ``draft``).  A launch per product leaves every SM idle between products while
-// the chain of row statistics -> staging -> MMA -> reduction -> epilogue of
-// each small product runs; on sm_103a that latency, not HBM, bounded the step.
-// Here one CTA per SM runs the whole program of phases (the q/k/v, o, cross-q,
-// cross-attention, o, fc1, fc2 products of every layer and the head):
-//   * warp 0 streams this CTA's share of every phase's weights, in program
+// ``draft``).  With a launch per product every SM idles while each small
+// product's chain of row statistics -> staging -> MMA -> reduction ->
+// epilogue runs, and on this GPU a dependent round trip through L2 costs well
+// over a microsecond, so latency, not HBM, bounded the step.  Here clusters of
+// 8 CTAs (one CTA per SM) run the whole program of phases -- per layer the
+// q/k/v, o (with the block self-attention as its prologue), cross-q (with the
+// cross-attention as its tail), cross-o, fc1 and fc2 products -- and the head:
+//   * warp 0 streams the CTA's share of every phase's weights, in program
 //     order, with 32 KB bulk copies into a shared-memory ring; weights do not
-//     depend on activations, so the stream runs ahead across phase boundaries,
-//     limited only by the ring;
+//     depend on activations, so the stream runs ahead across phase boundaries;
 //   * warp 1 issues tcgen05.mma (M = 128 weight rows, N = 16 hi + 16 lo
-//     activation rows, K = 16) into one of four TMEM accumulators per segment;
-//   * warps 2..9 wait for the phase's grid barrier, stage the activations
-//     (RMSNorm / adaLN LayerNorm-modulate prologues, bf16 hi + lo split) as the
-//     MMA's B operand, read the accumulators, and publish partial tiles;
-//   * a linear phase's chunks are dealt to CTAs in equal contiguous ranges
-//     (stream-K), so every SM streams the same number of bytes; the last CTA to
-//     finish a tile (a ticket) adds the tile's partials in CTA order
-//     (deterministic) and runs the fused epilogue (bias, GELU, gated residual,
-//     per-head RMSNorm + RoPE, row statistics, the head's lm_head operand);
-//   * the block self-attention of a head runs after the last of its q, k and v
-//     tiles is finished (a head ticket);
-//   * cross-attention is a phase of its own: every head's keys are split over
-//     CTAs (flash-decoding), f16 mma.sync on swizzled cp.async stages, an
-//     online softmax per warp, a merge of the warps in shared memory and of the
-//     CTAs by the last one to finish (a head ticket);
+//     activation rows, K = 16) into one TMEM accumulator per owned tile;
+//   * the 128-row tiles of a phase are dealt to clusters; every rank of a
+//     cluster owns the same K slice of each of its cluster's tiles, so warps
+//     2..9 stage that slice of the activations (RMSNorm / adaLN
+//     LayerNorm-modulate prologues, bf16 hi + lo split) once per phase;
+//   * the partial tiles meet through distributed shared memory: a worker-only
+//     cluster barrier (remote mbarrier arrivals, release / acquire at cluster
+//     scope) publishes them, and rank r adds rows r and r + 8 of every tile in
+//     rank order (deterministic) and runs the fused epilogue (bias, GELU, gated
+//     residual + row moments, per-head RMSNorm + RoPE, the lm_head operand);
+//   * the block self-attention of a head is the prologue of the o product:
+//     each rank attends the heads its K slice covers;
+//   * the cross-attention is the tail of the cross-q product: each cluster
+//     owns its heads' q tiles, splits the keys over its 8 CTAs (f16 mma.sync
+//     on swizzled cp.async stages, online softmax, warps merged in shared
+//     memory) and merges the ranks through distributed shared memory;
 //   * phases are separated by a grid-wide barrier (an arrival counter and a
-//     generation word); every wait is bounded: a wait that exceeds its budget
-//     raises the error word and the kernel winds down (waits for its own copies
-//     in flight and its MMAs, frees its TMEM) instead of hanging.
-// The grid is one CTA per SM (the shared-memory footprint admits no second),
-// launched cooperatively so that all CTAs are resident together.
+//     generation word); every wait is bounded: one that exceeds its budget
+//     raises the error word and the kernel winds down (its copies in flight
+//     land and its MMAs complete before it frees TMEM and exits).
 #include <cooperative_groups.h>
 
 #include "linear_parts.cuh"
@@ -41,32 +41,37 @@ namespace fm {
 
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kRing = 4;                          // ring stages
 constexpr int kUnit = 2 * kStageBytes;            // 32 KB: two 16 KB chunks per bulk copy
 constexpr int kPieceCols = 256;                   // activation columns per staged B piece
 constexpr int kCpp = kPieceCols / kChunk;         // chunks per piece
 constexpr int kBch = 32 * 128;                    // bytes of one 64-column B chunk (32 rows)
 constexpr int kPieceBytes = kCpp * kBch;          // 16 KB
-constexpr int kScratch = 64 * 1024;
-constexpr int kNAcc = 4;                          // TMEM accumulators of 32 columns
-constexpr int kTmemCols = 128;
+constexpr int kRows = 16;                         // block rows a phase carries
+constexpr int kPartTile = kRows * kTile * 4;      // one partial tile, f32 [16][128]
+constexpr int kNAcc = kStepMaxTiles;              // one TMEM accumulator (32 columns) per owned tile
+constexpr int kTmemCols = 256;
 constexpr uint32_t kIdesc = umma_idesc(128, 32, true);
 constexpr int kKeys = 64;                         // keys per attention stage
 
 // shared-memory layout (offsets from the 1024-aligned base)
 constexpr int kOffRing = 0;
-constexpr int kOffPiece = kOffRing + kRing * kUnit;
-constexpr int kOffScratch = kOffPiece + 2 * kPieceBytes;
-constexpr int kOffMisc = kOffScratch + kScratch;
-// misc: stats [2 jobs][2][kMaxT] f32, flags, barriers, TMEM slot
-constexpr int kOffStats = kOffMisc;
-constexpr int kOffFlags = kOffStats + 2 * 2 * kMaxT * 4;
+constexpr int kOffB = kOffRing + kRing * kUnit;                  // 2 B pieces (or a key stage)
+constexpr int kOffPart = kOffB + 2 * kPieceBytes;                // partial tiles / q, k, v / key stage
+constexpr int kPartArea = 52 * 1024;
+constexpr int kOffQ = kOffPart + kPartArea;                      // f16 hi / lo query tiles [16][hd]
+constexpr int kOffMisc = kOffQ + 8 * 1024;
+constexpr int kOffStats = kOffMisc;                              // mu, rs [kMaxT]
+constexpr int kOffFlags = kOffStats + 2 * kMaxT * 4;
 constexpr int kOffBars = kOffFlags + 64;
-constexpr int kNBars = 2 * kRing + 2 + 2 + 2 * kNAcc + 1;
+constexpr int kNBars = 2 * kRing + 2 + 2 + kNAcc + 1 + 2;
 constexpr int kOffTslot = kOffBars + 8 * kNBars;
 constexpr int kSmemUsed = kOffTslot + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory beyond the per-CTA limit");
+static_assert(kStepMaxTiles * kPartTile <= kPartArea, "partial tiles beyond their area");
 
 struct Bars {
   uint32_t base;
@@ -75,8 +80,11 @@ struct Bars {
   __device__ uint32_t bfull(int i) const { return base + 8 * (2 * kRing + i); }
   __device__ uint32_t bempty(int i) const { return base + 8 * (2 * kRing + 2 + i); }
   __device__ uint32_t accfull(int i) const { return base + 8 * (2 * kRing + 4 + i); }
-  __device__ uint32_t accempty(int i) const { return base + 8 * (2 * kRing + 4 + kNAcc + i); }
-  __device__ uint32_t drain() const { return base + 8 * (2 * kRing + 4 + 2 * kNAcc); }
+  __device__ uint32_t drain() const { return base + 8 * (2 * kRing + 4 + kNAcc); }
+  // two cluster barriers used alternately: a rank arrives on a barrier again only
+  // after every rank has finished its arrivals of the sync before (it passed the
+  // sync in between), so no arrival can land in a phase that is still open
+  __device__ uint32_t cluster(int i) const { return base + 8 * (2 * kRing + 5 + kNAcc + i); }
 };
 
 __device__ __forceinline__ uint64_t gtimer() {
@@ -94,8 +102,8 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-// All of this CTA's earlier writes are made visible, then the CTA counts itself
-// in; the last of G resets the counter and advances the generation.
+// This CTA's earlier writes are made visible, then it counts itself in; the
+// last of G resets the counter and advances the generation.
 __device__ __forceinline__ void grid_arrive(uint32_t *bar, int G) {
   __threadfence();
   const uint32_t old = atomicAdd(bar, 1u);
@@ -105,7 +113,7 @@ __device__ __forceinline__ void grid_arrive(uint32_t *bar, int G) {
     atomicAdd(bar + 32, 1u);
   }
 }
-// Wait until the generation has advanced `k` times past g0; bounded.
+// Wait until the generation has advanced k times past g0; bounded.
 __device__ __forceinline__ bool grid_wait(const uint32_t *bar, uint32_t g0, uint32_t k, int32_t *err) {
   if (ld_acquire(bar + 32) - g0 >= k) return true;
   const long long t0 = clock64();
@@ -124,85 +132,62 @@ __device__ __forceinline__ bool grid_wait(const uint32_t *bar, uint32_t g0, uint
   return true;
 }
 
-// ---- schedule walkers ------------------------------------------------------------
-// A CTA's segments in a linear phase: maximal runs of its chunks inside one tile.
-struct Seg {
-  int job, tile, gt;   // job, tile in the job, tile in the phase
-  int c0, c1;          // chunks [c0, c1) in the phase's sequence
-  int k0;              // first chunk column inside the tile (kc)
-};
-__device__ __forceinline__ int phase_segments(const StepPhase &P, int lo, int hi, Seg (&s)[kStepMaxSeg]) {
-  int n = 0;
-  int c = lo;
-  while (c < hi && n < kStepMaxSeg) {
-    const int j = step_job(P, c);
-    const StepJob &J = P.jobs[j];
-    const int lc = c - J.chunk0;
-    const int tile = lc / J.cpt;
-    const int end = min(hi, J.chunk0 + (tile + 1) * J.cpt);
-    s[n].job = j;
-    s[n].tile = tile;
-    s[n].gt = J.tile0 + tile;
-    s[n].c0 = c;
-    s[n].c1 = end;
-    s[n].k0 = lc - tile * J.cpt;
-    ++n;
-    c = end;
-  }
-  return n;
-}
-
-// ---- block self-attention of one head by a group of 4 warps ------------------------
-// O = softmax(q k^T * scale) v over the T rows of the block (no mask), from the
-// q / k / v rows the head's epilogues stored; one warp per query row.
-__device__ void group_self_attention(const GemvArgs &a, int head, int T, float *sm, int bar_id, int gtid) {
-  const int hd = a.hd, D = a.self_D;
-  const int ks = hd + 4;
-  // three [16][hd + 4] f32 tiles: 25 KB at hd 128, inside the group's 32 KB half of the scratch
-  float *qq = sm, *kk = sm + 16 * ks, *vv = sm + 2 * 16 * ks;
-  const int q4 = hd / 4;
-  for (int i = gtid; i < T * q4; i += 128) {
-    const int t = i / q4, d = 4 * (i - t * q4);
-    const float *row = a.Y + (size_t)t * a.ldy + head * hd + d;
-    *reinterpret_cast<float4 *>(qq + t * ks + d) = __ldcg(reinterpret_cast<const float4 *>(row));
-    *reinterpret_cast<float4 *>(kk + t * ks + d) = __ldcg(reinterpret_cast<const float4 *>(row + D));
-    *reinterpret_cast<float4 *>(vv + t * ks + d) = __ldcg(reinterpret_cast<const float4 *>(row + 2 * D));
-  }
-  named_sync(bar_id, 128);
-  const int lane = threadIdx.x & 31, w = gtid >> 5;
-  const bool on = lane < q4;
-  for (int t = w; t < T; t += 4) {
-    const float *qrow = qq + t * ks;
-    const float *krow = kk + (lane < T ? lane : 0) * ks;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    for (int d = 0; d < hd; d += 4) {
-      const float4 q = *reinterpret_cast<const float4 *>(qrow + d);
-      const float4 k = *reinterpret_cast<const float4 *>(krow + d);
-      s0 += q.x * k.x; s1 += q.y * k.y; s2 += q.z * k.z; s3 += q.w * k.w;
+// ---- cluster barrier among the worker warps ---------------------------------------
+// The producer and MMA warps run ahead on their own, so the hardware cluster
+// barrier (which counts every thread) cannot be used inside the phase loop.
+// Instead one worker thread per CTA arrives, with release semantics at cluster
+// scope, on an mbarrier of every CTA of the cluster (the CTA's named barrier
+// before it orders all its workers' writes), and waits for its own barrier's 8
+// arrivals with acquire semantics.
+__device__ __forceinline__ bool cl_sync(const Bars &bars, uint32_t &n, int tid, int32_t *err, volatile int *flag) {
+  const uint32_t bar = bars.cluster(n & 1), parity = (n >> 1) & 1;
+  ++n;
+  named_sync(1, kWorkers);
+  if (tid == 0) {
+#pragma unroll
+    for (int r = 0; r < kStepCS; ++r) {
+      uint32_t remote;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(bar), "r"(r));
+      asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote) : "memory");
     }
-    const float sc = lane < T ? ((s0 + s1) + (s2 + s3)) * a.attn_scale : -INFINITY;
-    const float mx = warp_max(sc);
-    const float p = lane < T ? __expf(sc - mx) : 0.f;
-    const float den = warp_sum(p);
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < T; ++j) {
-      const float pj = __shfl_sync(0xffffffffu, p, j);
-      if (on) {
-        const float4 v = *reinterpret_cast<const float4 *>(vv + j * ks + 4 * lane);
-        o.x += pj * v.x; o.y += pj * v.y; o.z += pj * v.z; o.w += pj * v.w;
+    bool ok = true;
+    const long long t0 = clock64();
+    for (;;) {
+      uint32_t done;
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+          " selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(bar), "r"(parity), "r"(100000u)
+          : "memory");
+      if (done) break;
+      if (clock64() - t0 > kWaitBudgetCycles || *reinterpret_cast<volatile int32_t *>(err)) {
+        atomicExch(err, 1);
+        ok = false;
+        break;
       }
     }
-    if (on) {
-      const float inv = 1.f / den;
-      *reinterpret_cast<float4 *>(a.attn_out + (size_t)t * D + head * hd + 4 * lane) =
-          make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-    }
+    *flag = ok ? 1 : 0;
   }
-  named_sync(bar_id, 128);
+  named_sync(1, kWorkers);
+  return *flag != 0;
 }
 
-// ---- cross-attention helpers --------------------------------------------------------
-// m16n8k8 f16 MMA, f32 accumulate
+// ---- a phase's work of this CTA -------------------------------------------------------
+struct Own {
+  int tiles[kStepMaxTiles];
+  int n;        // tiles of this cluster
+  int kc0, kc1; // this rank's chunk range in every tile
+};
+__device__ __forceinline__ void phase_own(const StepPhase &P, int c, int r, int ncl, Own &o) {
+  o.n = 0;
+  for (int i = 0; i < P.ntiles && o.n < kStepMaxTiles; ++i)
+    if (step_cluster_of(P, i, ncl) == c) o.tiles[o.n++] = i;
+  o.kc0 = step_klo(r, P.cpt);
+  o.kc1 = step_klo(r + 1, P.cpt);
+}
+
+// ---- attention helpers --------------------------------------------------------------
 __device__ __forceinline__ void mma_f16_k8(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
   asm volatile(
       "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
@@ -214,45 +199,39 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-// byte offset of 16-byte unit u of row r in a stage tile of 256-byte rows (hd 128)
-// or 128-byte rows (hd 64): units permuted by r % 8, so eight rows reading the
-// same unit hit eight distinct bank groups
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// byte offset of 16-byte unit u of row r in a tile of (hd * 2)-byte rows, the
+// units permuted by r % 8 so that eight rows reading one unit hit eight bank groups
 __device__ __forceinline__ uint32_t kv_slot(int r, int u, int hd) {
   return (uint32_t)(r * hd * 2 + ((u ^ (r & 7)) << 4));
 }
-// key range of one attention item
-struct AttnItem {
-  int head, split, kbeg, kend, nst, L;
-};
-__device__ __forceinline__ AttnItem attn_item(const StepAttn &A, const StepParams *sp, int b) {
-  AttnItem it;
-  it.head = b / A.nsp;
-  it.split = b - it.head * A.nsp;
-  it.L = (A.L_src == 0 ? sp->L : sp->pos + 1) + A.L_add;
-  int per = (it.L + A.nsp - 1) / A.nsp;
-  per = (per + 15) & ~15;
-  it.kbeg = min(it.L, it.split * per);
-  it.kend = min(it.L, it.kbeg + per);
-  it.nst = (it.kend - it.kbeg + kKeys - 1) / kKeys;
-  return it;
-}
-// request rows [rlo, rhi) of key stage st (64 keys) into K / V buffers (rows past
-// kend read as zero); 256 worker threads
-__device__ __forceinline__ void attn_issue(const StepAttn &A, const AttnItem &it, int st, uint32_t kb, uint32_t vb,
-                                           int rlo, int rhi, int tid) {
+// request rows [rlo, rhi) of the 64-key stage starting at key k0 (rows at or past
+// kend read as zero) into K / V tiles; 256 worker threads
+__device__ __forceinline__ void kv_issue(const StepAttn &A, int head, int k0, int kend, uint32_t kb, uint32_t vb,
+                                         int rlo, int rhi, int tid) {
   const int hd = A.hd;
   const int U = hd / 8;
-  const __half *kh = A.Kc + (size_t)it.head * A.max_ctx * hd;
-  const __half *vh = A.Vc + (size_t)it.head * A.max_ctx * hd;
-  const int k0 = it.kbeg + st * kKeys;
+  const __half *kh = A.Kc + (size_t)head * A.max_ctx * hd;
+  const __half *vh = A.Vc + (size_t)head * A.max_ctx * hd;
   for (int i = tid + rlo * U; i < rhi * U; i += kWorkers) {
-    const int r = i / U, u = i - r * U;
-    const int key = k0 + r;
-    const bool ok = key < it.kend;
+    const int rr = i / U, u = i - rr * U;
+    const int key = k0 + rr;
+    const bool ok = key < kend;
     const size_t off = (size_t)(ok ? key : 0) * hd + u * 8;
-    cp_async16(kb + kv_slot(r, u, hd), kh + off, ok ? 16u : 0u);
-    cp_async16(vb + kv_slot(r, u, hd), vh + off, ok ? 16u : 0u);
+    cp_async16(kb + kv_slot(rr, u, hd), kh + off, ok ? 16u : 0u);
+    cp_async16(vb + kv_slot(rr, u, hd), vh + off, ok ? 16u : 0u);
   }
+}
+// keys of rank r of a head: [kbeg, kend)
+__device__ __forceinline__ void rank_keys(int L, int r, int &kbeg, int &kend) {
+  int per = (L + kStepCS - 1) / kStepCS;
+  per = (per + 15) & ~15;
+  kbeg = min(L, r * per);
+  kend = min(L, kbeg + per);
 }
 
 }  // namespace
@@ -262,115 +241,104 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x, b = blockIdx.x;
+  const int G = gridDim.x;
+  const int c = blockIdx.x / kStepCS;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int r = (int)cluster.block_rank();
+  const int ncl = a.n_clusters;
   const int T = a.T;
-  const uint32_t ring = base + kOffRing, piece0 = base + kOffPiece, scratch = base + kOffScratch;
-  float *stats = reinterpret_cast<float *>(gbase + kOffStats);      // [2][2][kMaxT]: mu, rs per job
+  const uint32_t ring = base + kOffRing, bbuf = base + kOffB, part = base + kOffPart, qbuf = base + kOffQ;
+  float *partf = reinterpret_cast<float *>(gbase + kOffPart);
+  float *stats = reinterpret_cast<float *>(gbase + kOffStats);
   volatile int *flags = reinterpret_cast<volatile int *>(gbase + kOffFlags);
   const Bars bars{base + kOffBars};
   const uint32_t tslot = base + kOffTslot;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNBars; ++i) mbar_init(bars.base + 8 * i, 1);
+    for (int i = 0; i < kNBars - 2; ++i) mbar_init(bars.base + 8 * i, 1);
+    mbar_init(bars.cluster(0), kStepCS);
+    mbar_init(bars.cluster(1), kStepCS);
     mbar_fence_init();
   }
   if (warp == 1) tmem_alloc<kTmemCols>(tslot);
   tc_fence_before();
-  __syncthreads();
+  // every CTA's barriers are initialised before any peer arrives on them
+  cluster.sync();
   tc_fence_after();
   const uint32_t tmem = lds32(tslot);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- weight stream
     if (lane == 0) {
-      int u = 0;                 // units issued
+      int u = 0;
       int last_round[kRing];
       for (int i = 0; i < kRing; ++i) last_round[i] = -1;
-      bool waited = false;       // griddepcontrol.wait done (the first kRing units go before it)
       bool ok = true;
       for (int p = 0; p < a.n_phases && ok; ++p) {
         const StepPhase &P = a.ph[p];
-        if (P.kind != PH_LINEAR) continue;
-        const int lo = step_lo(b, P.nchunks, G), hi = step_lo(b + 1, P.nchunks, G);
-        for (int j = 0; j < P.njobs && ok; ++j) {
-          const StepJob &J = P.jobs[j];
-          const int c0 = max(lo, J.chunk0), c1 = min(hi, J.chunk0 + J.nchunks);
-          for (int c = c0; c < c1; c += 2) {
-            const int st = u % kRing, r = u / kRing;
-            if (r >= 1) {
-              if (!waited) { pdl_wait(); waited = true; }
-              if (!mbar_wait_bounded(bars.empty(st), (r - 1) & 1, a.err)) { ok = false; break; }
-            }
-            const int nch = min(2, c1 - c);
+        Own o;
+        phase_own(P, c, r, ncl, o);
+        for (int ti = 0; ti < o.n && ok; ++ti) {
+          const uint8_t *src = P.g.Wt + ((size_t)o.tiles[ti] * P.cpt + o.kc0) * kStageBytes;
+          for (int kc = o.kc0; kc < o.kc1; kc += 2) {
+            const int st = u % kRing, rd = u / kRing;
+            if (rd >= 1 && !mbar_wait_bounded(bars.empty(st), (rd - 1) & 1, a.err)) { ok = false; break; }
+            const int nch = min(2, o.kc1 - kc);
             mbar_expect_tx(bars.full(st), nch * kStageBytes);
-            bulk_g2s(ring + st * kUnit, J.g.Wt + (size_t)(c - J.chunk0) * kStageBytes, nch * kStageBytes,
-                     bars.full(st));
-            last_round[st] = r;
+            bulk_g2s(ring + st * kUnit, src + (size_t)(kc - o.kc0) * kStageBytes, nch * kStageBytes, bars.full(st));
+            last_round[st] = rd;
             ++u;
           }
         }
         stamp(a, p, 3);
       }
-      if (!waited) pdl_wait();
       // wind down: every copy this CTA issued has landed before the CTA may exit
       for (int st = 0; st < kRing; ++st)
         if (last_round[st] >= 0) mbar_wait_drain(bars.full(st), last_round[st] & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issue
-    pdl_wait();
-    int u = 0, sc = 0, pc = 0;   // units, segments, B pieces consumed
+    int u = 0, pc = 0;   // units consumed, B pieces consumed (counter shared with the workers)
     bool ok = true;
     for (int p = 0; p < a.n_phases && ok; ++p) {
       const StepPhase &P = a.ph[p];
-      if (P.kind != PH_LINEAR) continue;
-      const int lo = step_lo(b, P.nchunks, G), hi = step_lo(b + 1, P.nchunks, G);
-      Seg segs[kStepMaxSeg];
-      const int ns = phase_segments(P, lo, hi, segs);
-      int si = -1, i_in_seg = 0, acc = 0;
-      for (int j = 0; j < P.njobs && ok; ++j) {
-        const StepJob &J = P.jobs[j];
-        const int c0 = max(lo, J.chunk0), c1 = min(hi, J.chunk0 + J.nchunks);
-        for (int c = c0; c < c1 && ok; c += 2) {
-          const int st = u % kRing, r = u / kRing;
-          if (!mbar_wait_warp(bars.full(st), r & 1, a.err)) { ok = false; break; }
+      Own o;
+      phase_own(P, c, r, ncl, o);
+      const int nch = o.kc1 - o.kc0;
+      if (o.n == 0 || nch == 0) continue;
+      const int npc = (nch + kCpp - 1) / kCpp;
+      const bool resident = npc <= 2;
+      const int pc0 = pc;
+      for (int ti = 0; ti < o.n && ok; ++ti) {
+        const uint32_t d = tmem + ti * 32;
+        for (int j = 0; j < nch && ok; j += 2) {
+          const int st = u % kRing, rd = u / kRing;
+          if (!mbar_wait_warp(bars.full(st), rd & 1, a.err)) { ok = false; break; }
           tc_fence_after();
-          const int nch = min(2, c1 - c);
-          for (int x = 0; x < nch; ++x) {
-            const int cc = c + x;
-            if (si < 0 || cc >= segs[si].c1) {
-              // a new segment: the previous one's accumulator is complete
-              if (si >= 0) { umma_commit_elect(bars.accfull(acc)); ++sc; }
-              ++si;
-              if (si >= ns) { ok = false; break; }   // cannot happen: the host checked the schedule
-              acc = sc % kNAcc;
-              if (sc >= kNAcc && !mbar_wait_warp(bars.accempty(acc), ((sc / kNAcc) - 1) & 1, a.err)) { ok = false; break; }
-              tc_fence_after();
-              i_in_seg = 0;
-            }
-            const int pb = pc & 1;
-            if (i_in_seg % kCpp == 0) {
-              if (!mbar_wait_warp(bars.bfull(pb), (pc >> 1) & 1, a.err)) { ok = false; break; }
+          const int nu = min(2, nch - j);
+          for (int x = 0; x < nu; ++x) {
+            const int jj = j + x;
+            const int q = resident ? pc0 + jj / kCpp : pc0 + ti * npc + jj / kCpp;
+            const int pb = q & 1;
+            if (jj % kCpp == 0 && (!resident || ti == 0)) {
+              if (!mbar_wait_warp(bars.bfull(pb), (q >> 1) & 1, a.err)) { ok = false; break; }
               tc_fence_after();
             }
             const uint64_t ad = umma_desc_sw128(ring + st * kUnit + x * kStageBytes);
-            const uint64_t bd = umma_desc_sw128(piece0 + pb * kPieceBytes + (i_in_seg % kCpp) * kBch);
-            const uint32_t d = tmem + acc * 32;
+            const uint64_t bd = umma_desc_sw128(bbuf + pb * kPieceBytes + (jj % kCpp) * kBch);
 #pragma unroll
             for (int kk = 0; kk < kChunk / 16; ++kk)
-              umma_ss_elect(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (i_in_seg | kk) ? 1u : 0u);
-            if (i_in_seg % kCpp == kCpp - 1 || cc + 1 == segs[si].c1) {
+              umma_ss_elect(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (jj | kk) ? 1u : 0u);
+            if ((jj % kCpp == kCpp - 1 || jj == nch - 1) && (!resident || ti == o.n - 1))
               umma_commit_elect(bars.bempty(pb));
-              ++pc;
-            }
-            ++i_in_seg;
           }
           if (!ok) break;
           umma_commit_elect(bars.empty(st));
           ++u;
         }
+        if (ok) umma_commit_elect(bars.accfull(ti));
       }
-      if (ok && si >= 0) { umma_commit_elect(bars.accfull(acc)); ++sc; }
+      pc = pc0 + (resident ? npc : npc * o.n);
       if (lane == 0) stamp(a, p, 4);
     }
     // wind down: every MMA issued has completed before TMEM is freed
@@ -380,51 +348,98 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
   } else {
     // ---------------------------------------------------------------- workers
     const int tid = wtid();
-    const int grp = (warp - 2) >> 2;            // two groups of four warps
-    const int gtid = tid & 127;
+    const int w = warp - 2;
     pdl_wait();
-    uint32_t g0 = 0;
     if (tid == 0) flags[0] = (int)ld_acquire(a.bar + 32);
     named_sync(1, kWorkers);
-    g0 = (uint32_t)flags[0];
-    int pc = 0, sc = 0;                          // B pieces staged, segments read
-    bool ok = true;
-    for (int p = 0; p < a.n_phases && ok; ++p) {
+    const uint32_t g0 = (uint32_t)flags[0];
+    uint32_t clpar = 0;
+    int pc = 0;
+    int acc_use[kNAcc];   // completions of each accumulator so far (its barrier's parity)
+    for (int i = 0; i < kNAcc; ++i) acc_use[i] = 0;
+    for (int p = 0; p < a.n_phases; ++p) {
       const StepPhase &P = a.ph[p];
-      // an earlier request of a later attention phase's stable key rows
-      if (P.prefetch >= 0) {
-        const StepAttn &A = a.ph[P.prefetch].at;
-        if (b < A.n_heads * A.nsp) {
-          const AttnItem it = attn_item(A, a.sp, b);
-          const int stable = a.sp->stable;
-          for (int st = 0; st < 2; ++st) {
-            const int pre = st < it.nst ? max(0, min(kKeys, stable - (it.kbeg + st * kKeys))) : 0;
-            if (pre > 0)
-              attn_issue(A, it, st, scratch + st * 2 * kKeys * A.hd * 2, scratch + (st * 2 + 1) * kKeys * A.hd * 2, 0,
-                         pre, tid);
-            cp_async_commit();
-          }
-        }
+      const GemvArgs &g = P.g;
+      Own o;
+      phase_own(P, c, r, ncl, o);
+      const int nch = o.kc1 - o.kc0;
+      // cross-attention tail: this rank's first key stage of its cluster's first
+      // head (rows below `stable` are not written by this call) is requested early
+      int kbeg = 0, kend = 0, pre = 0;
+      const uint32_t stageA = part + 16 * 1024, stageB = bbuf;
+      const uint32_t tileb = (uint32_t)kKeys * P.at.hd * 2;
+      if (P.tail == ST_CROSS_ATTN && o.n > 0) {
+        const int L = (P.at.L_src == 0 ? a.sp->L : a.sp->pos + 1) + P.at.L_add;
+        rank_keys(L, r, kbeg, kend);
+        const int stable = a.sp->stable;
+        pre = kend > kbeg ? max(0, min(kKeys, stable - kbeg)) : 0;
+        const int head0 = o.tiles[0] * kTile / P.at.hd;
+        if (pre > 0) kv_issue(P.at, head0, kbeg, kend, stageA, stageA + tileb, 0, pre, tid);
+        cp_async_commit();
       }
-      // the previous phase is complete everywhere
       if (p > 0) {
         if (tid == 0) flags[1] = grid_wait(a.bar, g0, (uint32_t)p, a.err) ? 1 : 0;
         named_sync(1, kWorkers);
-        if (!flags[1]) { ok = false; break; }
+        if (!flags[1]) break;
       }
       if (tid == 0) stamp(a, p, 0);
-      if (P.kind == PH_LINEAR) {
-        const int lo = step_lo(b, P.nchunks, G), hi = step_lo(b + 1, P.nchunks, G);
-        Seg segs[kStepMaxSeg];
-        const int ns = phase_segments(P, lo, hi, segs);
-        // stage every piece of every segment (the MMA warp consumes them in order)
-        int last_job = -1;
-        for (int s = 0; s < ns; ++s) {
-          const GemvArgs &g = P.jobs[segs[s].job].g;
-          const int kb = segs[s].k0 * kChunk;                     // first column of the segment
-          const int ncol = (segs[s].c1 - segs[s].c0) * kChunk;
-          const int m0 = segs[s].tile * kTile;
-          float *mu = stats + segs[s].job * 2 * kMaxT, *rs = mu + kMaxT;
+      if (o.n > 0 && nch > 0) {
+        const int npc = (nch + kCpp - 1) / kCpp;
+        const bool resident = npc <= 2;
+        const int kb = o.kc0 * kChunk, ncol = nch * kChunk;
+        float *mu = stats, *rs = stats + kMaxT;
+        // -------------------------------------------- prologue: the block self-attention of this rank's heads
+        const float *osm = nullptr;     // activations from shared memory (f32 [16][ncol]) instead of global
+        if (P.prologue == SP_SELF_ATTN) {
+          const StepAttn &A = P.at;
+          const int hd = A.hd, D = A.D;
+          const int h0 = kb / hd, h1 = (kb + ncol - 1) / hd;
+          const int nh = h1 - h0 + 1;
+          // q, k, v rows of the heads into the partial area: [head][q|k|v][16][hd + 4]
+          const int ks = hd + 4;
+          float *qkv = partf;
+          const int q4 = hd / 4;
+          for (int i = tid; i < nh * 3 * kRows * q4; i += kWorkers) {
+            const int d4 = i % q4, rest = i / q4;
+            const int t = rest % kRows, m = (rest / kRows) % 3, hh = rest / (3 * kRows);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < T)
+              v = __ldcg(reinterpret_cast<const float4 *>(A.qkv + (size_t)t * 3 * D + m * D + (h0 + hh) * hd + 4 * d4));
+            *reinterpret_cast<float4 *>(qkv + ((hh * 3 + m) * kRows + t) * ks + 4 * d4) = v;
+          }
+          named_sync(1, kWorkers);
+          // one warp per (head, query row); lane j < T holds the score of key j
+          float *ob = reinterpret_cast<float *>(gbase + kOffB + kPieceBytes);   // f32 [16][ncol]
+          for (int u = w; u < nh * T; u += 8) {
+            const int hh = u / T, t = u - hh * T;
+            const float *qr = qkv + ((hh * 3 + 0) * kRows + t) * ks;
+            const float *kr = qkv + ((hh * 3 + 1) * kRows + (lane < T ? lane : 0)) * ks;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            for (int d = 0; d < hd; d += 4) {
+              const float4 qv = *reinterpret_cast<const float4 *>(qr + d);
+              const float4 kv = *reinterpret_cast<const float4 *>(kr + d);
+              s0 += qv.x * kv.x; s1 += qv.y * kv.y; s2 += qv.z * kv.z; s3 += qv.w * kv.w;
+            }
+            const float sc = lane < T ? ((s0 + s1) + (s2 + s3)) * A.scale : -INFINITY;
+            const float mx = warp_max(sc);
+            const float pr = lane < T ? __expf(sc - mx) : 0.f;
+            const float inv = 1.f / warp_sum(pr);
+            const float *vb = qkv + ((hh * 3 + 2) * kRows) * ks;
+            for (int d = lane; d < hd; d += 32) {
+              const int col = (h0 + hh) * hd + d - kb;
+              float acc = 0.f;
+              for (int j = 0; j < T; ++j) acc += __shfl_sync(0xffffffffu, pr, j) * vb[j * ks + d];
+              if (col >= 0 && col < ncol) ob[t * ncol + col] = acc * inv;
+            }
+          }
+          named_sync(1, kWorkers);
+          osm = ob;
+        }
+        // -------------------------------------------- stage this rank's K slice of the activations
+        const int passes = resident ? 1 : o.n;
+        bool stats_done = false;
+        for (int ps = 0; ps < passes; ++ps) {
+          const int m0 = o.tiles[resident ? 0 : ps] * kTile;
           for (int x = 0; x < ncol; x += kPieceCols) {
             const int pb = pc & 1;
             // (a wait that gives up raises the error word; the workers still take every
@@ -432,15 +447,27 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
             if (pc >= 2) mbar_wait_bounded(bars.bempty(pb), ((pc >> 1) - 1) & 1, a.err);
             const int kp = min(kPieceCols, ncol - x);
             StageRegs<1> rg;
-            stage_load<1>(g, T, m0, kb + x, kp, rg);
-            if (segs[s].job != last_job) {
-              // this job's row statistics while the first piece's loads are in flight
+            if (osm) {
+              using R = StageRegs<1>;
+              const int t = tid / R::tpr, q0 = tid % R::tpr;
+              const int nq = (kp >> 2) / R::tpr;
+#pragma unroll
+              for (int j = 0; j < R::kMaxQ; ++j) {
+                rg.xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                rg.p0[j] = rg.p1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < nq && t < T)
+                  rg.xv[j] = *reinterpret_cast<const float4 *>(osm + t * ncol + x + 4 * (q0 + R::tpr * j));
+              }
+            } else {
+              stage_load<1>(g, T, m0, kb + x, kp, rg);
+            }
+            if (!stats_done) {
+              // the row statistics while the first piece's loads are in flight
               load_row_stats(g, T, mu, rs, tid);
               named_sync(1, kWorkers);
-              last_job = segs[s].job;
-              if (tid == 0) stamp(a, p, 5);
+              stats_done = true;
             }
-            stage_store<1>(g, mu, rs, piece0 + pb * kPieceBytes, T, kb + x, kp, rg);
+            stage_store<1>(g, mu, rs, bbuf + pb * kPieceBytes, T, kb + x, kp, rg);
             fence_proxy_async();
             named_sync(1, kWorkers);
             if (tid == 0) mbar_arrive(bars.bfull(pb));
@@ -448,151 +475,107 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
           }
         }
         if (tid == 0) stamp(a, p, 1);
-        // read the accumulators (segment s by group s & 1), publish, reduce
-        for (int s = grp; s < ns; s += 2) {
-          const StepJob &J = P.jobs[segs[s].job];
-          const GemvArgs &g = J.g;
-          const int my_sc = sc + s;
-          const int acc = my_sc % kNAcc;
-          mbar_wait_bounded(bars.accfull(acc), (my_sc / kNAcc) & 1, a.err);
+        // -------------------------------------------- accumulators -> partial tiles in shared memory
+        for (int ti = w >> 2; ti < o.n; ti += 2) {
+          mbar_wait_bounded(bars.accfull(ti), acc_use[ti] & 1, a.err);
           tc_fence_after();
           const int quad = warp & 3;
           float v[32];
-          tmem_ld32(tmem + acc * 32 + ((uint32_t)(quad * 32) << 16), v);   // columns 0..15 hi, 16..31 lo
+          tmem_ld32(tmem + ti * 32 + ((uint32_t)(quad * 32) << 16), v);   // columns 0..15 hi, 16..31 lo
           tc_fence_before();
-          named_sync(2 + grp, 128);
-          if (gtid == 0) mbar_arrive(bars.accempty(acc));
-          float *mine = a.part + ((size_t)b * kStepMaxSeg + s) * kMaxT * kTile;
+          float *pt = partf + ti * (kPartTile / 4);
           const int row = quad * 32 + lane;
 #pragma unroll
-          for (int t = 0; t < 16; ++t)
-            if (t < T) __stcg(mine + t * kTile + row, v[t] + v[16 + t]);
-          __threadfence();
-          named_sync(2 + grp, 128);
-          // contributors of this tile: with at least as many chunks as CTAs every CTA
-          // owns a non-empty range and they are the owners of the tile's first to
-          // last chunk; with fewer, each chunk is one CTA's whole range
-          const int tc0 = J.chunk0 + segs[s].tile * J.cpt;
-          const bool dense = P.nchunks >= G;
-          const int blo = step_owner(tc0, P.nchunks, G);
-          const int ncontrib = dense ? step_owner(tc0 + J.cpt - 1, P.nchunks, G) - blo + 1 : J.cpt;
-          if (gtid == 0) {
-            int *tk = a.tickets + segs[s].gt;
-            const int old = atomicAdd(tk, 1);
-            const bool last = old == ncontrib - 1;
-            if (last) atomicExch(tk, 0);
-            flags[4 + grp] = last ? 1 : 0;
-          }
-          named_sync(2 + grp, 128);
-          if (!flags[4 + grp]) continue;
-          __threadfence();
-          // the last contributor: partials in CTA order, then the fused epilogue
-          const int m0 = segs[s].tile * kTile;
-          const int gw = gtid >> 5;
-          for (int t = gw; t < T; t += 4) {
-            EpiIn in;
-            epilogue_load(g, t, m0, in);
-            float vv[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int i0 = 0; i0 < ncontrib; i0 += 8) {
-              float4 pr[8];
-#pragma unroll
-              for (int x = 0; x < 8; ++x) {
-                pr[x] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i0 + x < ncontrib) {
-                  const int bb = dense ? blo + i0 + x : step_owner(tc0 + i0 + x, P.nchunks, G);
-                  // the segment index of this tile in CTA bb's list
-                  const int si = segs[s].gt - step_tile(P, step_lo(bb, P.nchunks, G));
-                  pr[x] = __ldcg(reinterpret_cast<const float4 *>(
-                      a.part + (((size_t)bb * kStepMaxSeg + si) * kMaxT + t) * kTile + 4 * lane));
-                }
-              }
-#pragma unroll
-              for (int x = 0; x < 8; ++x) {
-                vv[0] += pr[x].x; vv[1] += pr[x].y; vv[2] += pr[x].z; vv[3] += pr[x].w;
-              }
-            }
-            epilogue_unit(g, t, m0, vv, segs[s].tile, in);
-          }
-          if (J.self_tail) {
-            // the block attention of each head of this tile once its q, k and v tiles are all stored
-            __threadfence();
-            named_sync(2 + grp, 128);
-            const int heads = kTile / g.hd;
-            if (gtid == 0) {
-              const int mseg = m0 % g.self_D;
-              for (int i = 0; i < heads; ++i) {
-                const int h = mseg / g.hd + i;
-                int *tk = a.tickets + kStepTileTickets + h;
-                const int old = atomicAdd(tk, 1);
-                const bool last = old == 2;
-                if (last) atomicExch(tk, 0);
-                flags[8 + 2 * grp + i] = last ? h : -1;
-              }
-            }
-            named_sync(2 + grp, 128);
-            for (int i = 0; i < heads; ++i) {
-              const int h = flags[8 + 2 * grp + i];
-              if (h >= 0) {
-                __threadfence();
-                group_self_attention(g, h, T, reinterpret_cast<float *>(gbase + kOffScratch + grp * (kScratch / 2)),
-                                     2 + grp, gtid);
-              }
-            }
-          }
+          for (int t = 0; t < kRows; ++t) pt[t * kTile + row] = v[t] + v[16 + t];
         }
-        sc += ns;
-      } else {
-        // ------------------------------------------------------------ cross-attention
+        for (int ti = 0; ti < o.n; ++ti) ++acc_use[ti];
+      } else if (o.n > 0) {
+        // a rank without chunks in this phase (a short K) contributes zero tiles
+        for (int i = tid; i < o.n * kPartTile / 16; i += kWorkers)
+          reinterpret_cast<float4 *>(partf)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      // -------------------------------------------------- publish the partials to the cluster
+      if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) break;
+      if (tid == 0) stamp(a, p, 5);
+      // -------------------------------------------------- rank r finishes rows r, r + 8 of every tile
+      if (o.n > 0) {
+        const int nrows = T > kStepCS ? 2 : 1;
+        for (int uu = w; uu < o.n * nrows; uu += 8) {
+          const int ti = uu / nrows, t = r + kStepCS * (uu - ti * nrows);
+          if (t >= T) continue;
+          const int tile = o.tiles[ti];
+          const int m0 = tile * kTile;
+          EpiIn in;
+          epilogue_load(g, t, m0, in);
+          float4 pv[kStepCS];
+#pragma unroll
+          for (int q = 0; q < kStepCS; ++q) {
+            const float *src = cluster.map_shared_rank(partf, q) + ti * (kPartTile / 4) + t * kTile + 4 * lane;
+            pv[q] = *reinterpret_cast<const float4 *>(src);
+          }
+          float vv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int q = 0; q < kStepCS; ++q) {   // rank order
+            vv[0] += pv[q].x; vv[1] += pv[q].y; vv[2] += pv[q].z; vv[3] += pv[q].w;
+          }
+          epilogue_unit(g, t, m0, vv, tile, in);
+        }
+      }
+      if (tid == 0) stamp(a, p, 6);
+      // -------------------------------------------------- tail: cross-attention of the cluster's heads
+      if (P.tail == ST_CROSS_ATTN && o.n > 0) {
         const StepAttn &A = P.at;
         const int hd = A.hd;
-        const bool active = b < A.n_heads * A.nsp;
-        AttnItem it;
-        if (active) it = attn_item(A, a.sp, b);
-        const uint32_t tileb = kKeys * hd * 2;
-        auto kbuf = [&](int i) { return scratch + 2 * i * tileb; };
-        auto vbuf = [&](int i) { return scratch + (2 * i + 1) * tileb; };
-        if (active) {
-          // the rest of the first two stages (all of them if nothing was requested early)
-          const int stable = A.prefetched ? a.sp->stable : 0;
-          for (int st = 0; st < 2; ++st) {
-            if (st < it.nst) {
-              const int pre = max(0, min(kKeys, stable - (it.kbeg + st * kKeys)));
-              if (pre < kKeys) attn_issue(A, it, st, kbuf(st), vbuf(st), pre, kKeys, tid);
-            }
+        // every rank's q rows are stored (global) and every rank is done reading the partials
+        if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) break;
+        const int heads_per_tile = kTile / hd;
+        bool ok = true;
+        for (int hi = 0; hi < o.n * heads_per_tile && ok; ++hi) {
+          const int head = o.tiles[hi / heads_per_tile] * heads_per_tile + hi % heads_per_tile;
+          if (head >= A.n_heads) continue;
+          if (hi > 0) {
+            // the previous head's partial slot is read by the peers before it is reused
+            if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) { ok = false; break; }
+            pre = 0;
             cp_async_commit();
           }
-          // queries -> f16 hi / lo tiles in the (idle) B piece area: [16 rows][hd], units permuted by row
-          const uint32_t qhi = piece0, qlo = piece0 + 16 * hd * 2;
+          const int nst = (kend - kbeg + kKeys - 1) / kKeys;
+          // the rest of the first key stage, and the second (buffer B: the MMAs are done)
+          if (nst > 0 && pre < kKeys) kv_issue(A, head, kbeg, kend, stageA, stageA + tileb, pre, kKeys, tid);
+          cp_async_commit();
+          if (nst > 1) kv_issue(A, head, kbeg + kKeys, kend, stageB, stageB + tileb, 0, kKeys, tid);
+          cp_async_commit();
+          // queries -> f16 hi / lo tiles [16][hd], units permuted by row
+          const uint32_t qhi = qbuf, qlo = qbuf + kRows * hd * 2;
           const int q4 = hd / 4;
-          for (int i = tid; i < 16 * q4; i += kWorkers) {
+          for (int i = tid; i < kRows * q4; i += kWorkers) {
             const int t = i / q4, d = 4 * (i - t * q4);
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < T) x = __ldcg(reinterpret_cast<const float4 *>(A.Q + (size_t)t * A.ldq + it.head * hd + d));
+            float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < T) xq = __ldcg(reinterpret_cast<const float4 *>(A.Q + (size_t)t * A.ldq + head * hd + d));
             uint32_t h01, l01, h23, l23;
-            split2_f16(x.x, x.y, h01, l01);
-            split2_f16(x.z, x.w, h23, l23);
+            split2_f16(xq.x, xq.y, h01, l01);
+            split2_f16(xq.z, xq.w, h23, l23);
             const uint32_t off = kv_slot(t, d >> 3, hd) + (d & 7) * 2;
             asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qhi + off), "r"(h01), "r"(h23));
             asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qlo + off), "r"(l01), "r"(l23));
           }
           // per warp: keys 8w .. 8w + 7 of each stage; thread rows g and g + 8
-          const int w = warp - 2, gq = lane >> 2, q = lane & 3;
+          const int gq = lane >> 2, qq = lane & 3;
           const int NT = hd / 8;
-          float o[16][4];
+          float oacc[16][4];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+          for (int i = 0; i < 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
           float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
           const int mi = lane >> 3, ri = lane & 7;
-          for (int st = 0; st < it.nst; ++st) {
+          for (int st = 0; st < nst; ++st) {
             cp_async_wait<1>();
             named_sync(1, kWorkers);
-            const uint32_t kb = kbuf(st & 1), vb = vbuf(st & 1);
-            const int key = 8 * w + ri;     // this lane's row address for ldmatrix
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-            float s4b[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t kbuf = (st & 1) ? stageB : stageA, vbuf = kbuf + tileb;
+            const int key = 8 * w + ri;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f}, s4b[4] = {0.f, 0.f, 0.f, 0.f};
             for (int ks = 0; ks < hd / 16; ks += 2) {
               uint32_t b0, b1, b2, b3;
-              ldsm_x4(kb + kv_slot(key, 2 * ks + mi, hd), b0, b1, b2, b3);
+              ldsm_x4(kbuf + kv_slot(key, 2 * ks + mi, hd), b0, b1, b2, b3);
 #pragma unroll
               for (int h2 = 0; h2 < 2; ++h2) {
                 const int kq = ks + h2;
@@ -605,14 +588,11 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
                 mma_f16(s4b, c0, c1, c2, c3, bb0, bb1);
               }
             }
-            // scores (log2 domain), masked past kend; rows g (s[0], s[1]) and g + 8 (s[2], s[3])
-            const int kabs = it.kbeg + st * kKeys + 8 * w + 2 * q;
+            // scores in the log2 domain, masked past kend; rows g (s[0], s[1]) and g + 8 (s[2], s[3])
+            const int kabs = kbeg + st * kKeys + 8 * w + 2 * qq;
             float s[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int kk = kabs + (e & 1);
-              s[e] = kk < it.kend ? (s4[e] + s4b[e]) * A.scale_log2 : -INFINITY;
-            }
+            for (int e = 0; e < 4; ++e) s[e] = kabs + (e & 1) < kend ? (s4[e] + s4b[e]) * A.scale_log2 : -INFINITY;
             float alpha[2];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -623,13 +603,13 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
               alpha[h2] = mn == -INFINITY ? 1.f : exp2f(m_r[h2] - mn);
               m_r[h2] = mn;
             }
-            float pr[4];
+            float prb[4];
             float rsum[2] = {0.f, 0.f};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float mm = m_r[e >> 1];
-              pr[e] = mm == -INFINITY ? 0.f : exp2f(s[e] - mm);
-              rsum[e >> 1] += pr[e];
+              prb[e] = mm == -INFINITY ? 0.f : exp2f(s[e] - mm);
+              rsum[e >> 1] += prb[e];
             }
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -638,54 +618,53 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
               l_r[h2] = l_r[h2] * alpha[h2] + rsum[h2];
             }
             uint32_t ph0, pl0, ph1, pl1;
-            split2_f16(pr[0], pr[1], ph0, pl0);   // row g, keys 2q, 2q + 1
-            split2_f16(pr[2], pr[3], ph1, pl1);   // row g + 8
+            split2_f16(prb[0], prb[1], ph0, pl0);
+            split2_f16(prb[2], prb[3], ph1, pl1);
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt) {
               if (nt < NT) {
-                o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
-                o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
+                oacc[nt][0] *= alpha[0]; oacc[nt][1] *= alpha[0];
+                oacc[nt][2] *= alpha[1]; oacc[nt][3] *= alpha[1];
               }
             }
-            // O += P V: B = V[8 keys][8 dims] via ldmatrix.trans, four n-tiles per load
 #pragma unroll
             for (int nt = 0; nt < 16; nt += 4) {
               if (nt < NT) {
                 uint32_t v0, v1, v2, v3;
-                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                             : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
-                             : "r"(vb + kv_slot(key, nt + mi, hd)));
-                mma_f16_k8(o[nt], ph0, ph1, v0);
-                mma_f16_k8(o[nt], pl0, pl1, v0);
-                mma_f16_k8(o[nt + 1], ph0, ph1, v1);
-                mma_f16_k8(o[nt + 1], pl0, pl1, v1);
-                mma_f16_k8(o[nt + 2], ph0, ph1, v2);
-                mma_f16_k8(o[nt + 2], pl0, pl1, v2);
-                mma_f16_k8(o[nt + 3], ph0, ph1, v3);
-                mma_f16_k8(o[nt + 3], pl0, pl1, v3);
+                ldsm_x4_t(vbuf + kv_slot(key, nt + mi, hd), v0, v1, v2, v3);
+                mma_f16_k8(oacc[nt], ph0, ph1, v0);
+                mma_f16_k8(oacc[nt], pl0, pl1, v0);
+                mma_f16_k8(oacc[nt + 1], ph0, ph1, v1);
+                mma_f16_k8(oacc[nt + 1], pl0, pl1, v1);
+                mma_f16_k8(oacc[nt + 2], ph0, ph1, v2);
+                mma_f16_k8(oacc[nt + 2], pl0, pl1, v2);
+                mma_f16_k8(oacc[nt + 3], ph0, ph1, v3);
+                mma_f16_k8(oacc[nt + 3], pl0, pl1, v3);
               }
             }
             named_sync(1, kWorkers);   // every warp is done with this stage's buffers
-            if (st + 2 < it.nst) attn_issue(A, it, st + 2, kbuf(st & 1), vbuf(st & 1), 0, kKeys, tid);
+            if (st + 2 < nst)
+              kv_issue(A, head, kbeg + (st + 2) * kKeys, kend, kbuf, vbuf, 0, kKeys, tid);
             cp_async_commit();
           }
           cp_async_wait<0>();
           named_sync(1, kWorkers);
-          // merge the eight warps in three halving rounds through the scratch
-          float *mo = reinterpret_cast<float *>(gbase + kOffScratch);        // [4][16][hd]
-          float *mml = mo + 4 * 16 * hd;                                     // [4][16][2]
+          // merge the eight warps in three halving rounds (scratch: the B buffers, 32 KB,
+          // then the (max, sum) pairs past the first key stage)
+          float *mo = reinterpret_cast<float *>(gbase + kOffB);                 // [4][16][hd]
+          float *mml = reinterpret_cast<float *>(gbase + kOffPart + 16 * 1024 + 2 * tileb);
           for (int half = 4; half >= 1; half >>= 1) {
             if (w >= half && w < 2 * half) {
               const int ww = w - half;
 #pragma unroll
               for (int nt = 0; nt < 16; ++nt) {
                 if (nt < NT) {
-                  const int d = 8 * nt + 2 * q;
-                  *reinterpret_cast<float2 *>(mo + (ww * 16 + gq) * hd + d) = make_float2(o[nt][0], o[nt][1]);
-                  *reinterpret_cast<float2 *>(mo + (ww * 16 + gq + 8) * hd + d) = make_float2(o[nt][2], o[nt][3]);
+                  const int d = 8 * nt + 2 * qq;
+                  *reinterpret_cast<float2 *>(mo + (ww * 16 + gq) * hd + d) = make_float2(oacc[nt][0], oacc[nt][1]);
+                  *reinterpret_cast<float2 *>(mo + (ww * 16 + gq + 8) * hd + d) = make_float2(oacc[nt][2], oacc[nt][3]);
                 }
               }
-              if (q == 0) {
+              if (qq == 0) {
                 mml[(ww * 16 + gq) * 2] = m_r[0];
                 mml[(ww * 16 + gq) * 2 + 1] = l_r[0];
                 mml[(ww * 16 + gq + 8) * 2] = m_r[1];
@@ -706,81 +685,72 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
 #pragma unroll
                 for (int nt = 0; nt < 16; ++nt) {
                   if (nt < NT) {
-                    const float2 x = *reinterpret_cast<const float2 *>(mo + (w * 16 + row) * hd + 8 * nt + 2 * q);
-                    o[nt][2 * h2] = o[nt][2 * h2] * f1 + x.x * f2;
-                    o[nt][2 * h2 + 1] = o[nt][2 * h2 + 1] * f1 + x.y * f2;
+                    const float2 xo = *reinterpret_cast<const float2 *>(mo + (w * 16 + row) * hd + 8 * nt + 2 * qq);
+                    oacc[nt][2 * h2] = oacc[nt][2 * h2] * f1 + xo.x * f2;
+                    oacc[nt][2 * h2 + 1] = oacc[nt][2 * h2 + 1] * f1 + xo.y * f2;
                   }
                 }
               }
             }
             named_sync(1, kWorkers);
           }
-          // this CTA's partial (unnormalised rows, max, sum) to global memory
-          float *po = a.apart + (size_t)b * (kMaxT * hd + 2 * kMaxT);
-          float *pml = po + kMaxT * hd;
+          // this rank's partial (unnormalised rows, max, sum) into its partial slot
+          float *po = partf;                   // [16][hd], then [16][2]
+          float *pml = partf + kRows * hd;
           if (w == 0) {
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt) {
               if (nt < NT) {
-                const int d = 8 * nt + 2 * q;
-                __stcg(reinterpret_cast<float2 *>(po + gq * hd + d), make_float2(o[nt][0], o[nt][1]));
-                __stcg(reinterpret_cast<float2 *>(po + (gq + 8) * hd + d), make_float2(o[nt][2], o[nt][3]));
+                const int d = 8 * nt + 2 * qq;
+                *reinterpret_cast<float2 *>(po + gq * hd + d) = make_float2(oacc[nt][0], oacc[nt][1]);
+                *reinterpret_cast<float2 *>(po + (gq + 8) * hd + d) = make_float2(oacc[nt][2], oacc[nt][3]);
               }
             }
-            if (q == 0) {
-              __stcg(reinterpret_cast<float2 *>(pml + 2 * gq), make_float2(m_r[0], l_r[0]));
-              __stcg(reinterpret_cast<float2 *>(pml + 2 * (gq + 8)), make_float2(m_r[1], l_r[1]));
+            if (qq == 0) {
+              pml[2 * gq] = m_r[0];
+              pml[2 * gq + 1] = l_r[0];
+              pml[2 * (gq + 8)] = m_r[1];
+              pml[2 * (gq + 8) + 1] = l_r[1];
             }
-            __threadfence();
           }
-          named_sync(1, kWorkers);
-          if (tid == 0) {
-            int *tk = a.tickets + kStepTileTickets + kStepHeadTickets + it.head;
-            const int old = atomicAdd(tk, 1);
-            const bool last = old == A.nsp - 1;
-            if (last) atomicExch(tk, 0);
-            flags[2] = last ? 1 : 0;
-          }
-          named_sync(1, kWorkers);
-          if (flags[2]) {
-            // the last CTA of the head merges the splits in order: per row the
-            // weight of each split, exp2(m_s - M) / sum_s' exp2(m_s' - M) l_s', then
-            // the weighted sum of the unnormalised rows
-            __threadfence();
-            const int b0 = it.head * A.nsp;
-            const size_t stride = (size_t)kMaxT * hd + 2 * kMaxT;
-            float *fw = reinterpret_cast<float *>(gbase + kOffScratch);   // [16][nsp]
-            if (tid < 16) {
-              const int t = tid;
+          if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) { ok = false; break; }
+          // rank r merges rows r and r + 8 over the cluster's ranks, in rank order
+          if (w < 2) {
+            const int t = r + kStepCS * w;
+            if (t < T) {
+              float mq[kStepCS], lq[kStepCS];
               float M = -INFINITY;
-              for (int sp = 0; sp < A.nsp; ++sp)
-                M = fmaxf(M, __ldcg(a.apart + (b0 + sp) * stride + kMaxT * hd + 2 * t));
+#pragma unroll
+              for (int q = 0; q < kStepCS; ++q) {
+                const float *rm = cluster.map_shared_rank(pml, q);
+                mq[q] = rm[2 * t];
+                lq[q] = rm[2 * t + 1];
+                M = fmaxf(M, mq[q]);
+              }
               float den = 0.f;
-              for (int sp = 0; sp < A.nsp; ++sp) {
-                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.apart + (b0 + sp) * stride + kMaxT * hd + 2 * t));
-                const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-                fw[t * A.nsp + sp] = f;
-                den += f * ml.y;
+              float f[kStepCS];
+#pragma unroll
+              for (int q = 0; q < kStepCS; ++q) {
+                f[q] = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
+                den += f[q] * lq[q];
               }
               const float inv = 1.f / den;
-              for (int sp = 0; sp < A.nsp; ++sp) fw[t * A.nsp + sp] *= inv;
-            }
-            named_sync(1, kWorkers);
-            for (int i = tid; i < 16 * (hd / 4); i += kWorkers) {
-              const int t = i / (hd / 4), d = 4 * (i - t * (hd / 4));
-              if (t >= T) continue;
-              float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-              for (int sp = 0; sp < A.nsp; ++sp) {
-                const float f = fw[t * A.nsp + sp];
-                const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.apart + (b0 + sp) * stride + t * hd + d));
-                acc4.x += f * x.x; acc4.y += f * x.y; acc4.z += f * x.z; acc4.w += f * x.w;
+              for (int d = 4 * lane; d < hd; d += 128) {
+                float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < kStepCS; ++q) {
+                  const float4 xo = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(po, q) + t * hd + d);
+                  accv.x += f[q] * xo.x; accv.y += f[q] * xo.y; accv.z += f[q] * xo.z; accv.w += f[q] * xo.w;
+                }
+                *reinterpret_cast<float4 *>(A.out + (size_t)t * A.ldo + head * hd + d) =
+                    make_float4(accv.x * inv, accv.y * inv, accv.z * inv, accv.w * inv);
               }
-              *reinterpret_cast<float4 *>(A.out + (size_t)t * A.ldo + it.head * hd + d) = acc4;
             }
           }
-        } else {
-          cp_async_wait<0>();
         }
+        if (!ok) break;
+      } else if (P.tail == ST_CROSS_ATTN) {
+        cp_async_wait<0>();
       }
       // this phase is done here
       named_sync(1, kWorkers);
@@ -789,30 +759,37 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
         grid_arrive(a.bar, G);
       }
     }
+    cp_async_wait<0>();
   }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_free<kTmemCols>(tmem);
   }
+  // no CTA leaves while a peer may still read its shared memory
+  cluster.sync();
 }
 
 size_t step_smem_bytes() { return (size_t)kSmemBytes; }
-size_t step_apart_floats(int hd) { return (size_t)kMaxT * hd + 2 * kMaxT; }
 
 // attrs: bit 0 = cooperative launch (the driver co-schedules every CTA), bit 1 =
 // programmatic stream serialisation (the CTAs may start while the previous
 // kernel drains; they call griddepcontrol.wait before reading its results)
-cudaError_t launch_step(const StepArgs &a, int grid, cudaStream_t st, int attrs) {
+cudaError_t launch_step(const StepArgs &a, int clusters, cudaStream_t st, int attrs) {
   cudaError_t e = cudaFuncSetAttribute(fm_draft_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.gridDim = dim3(clusters * kStepCS, 1, 1);
   cfg.blockDim = dim3(kAll, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = kStepCS;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
   if (attrs & 1) {
     attr[na].id = cudaLaunchAttributeCooperative;
     attr[na].val.cooperative = 1;
@@ -828,11 +805,25 @@ cudaError_t launch_step(const StepArgs &a, int grid, cudaStream_t st, int attrs)
   return cudaLaunchKernelEx(&cfg, fm_draft_step_kernel, a);
 }
 
-int step_max_grid() {
-  int n = 0;
+int step_max_clusters() {
   if (cudaFuncSetAttribute(fm_draft_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fm_draft_step_kernel, kAll, kSmemBytes) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kStepCS * 64, 1, 1);
+  cfg.blockDim = dim3(kAll, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kStepCS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fm_draft_step_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   return n;
 }
 

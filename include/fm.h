@@ -276,9 +276,10 @@ FM_API fm_status fm_selftest_wait_timeout(fm_handle *h, int32_t budget_us, void 
 #define FM_DEBUG_CACHE_K 3  /* index = layer: cache K of seq, [n_heads][max_ctx][head_dim] as f16 bits */
 #define FM_DEBUG_CACHE_V 4  /* index = layer: cache V, same layout */
 #define FM_DEBUG_H0 5       /* [FM] the constant start row h0 [dim] f32 */
-#define FM_DEBUG_STEP_TRACE 6 /* [FM] persistent step trace of the last traced draft: u64 [phases][SMs][8]
-                                 globaltimer ns: 0 phase start, 1 staged, 2 done, 3 last copy issued,
-                                 4 last MMA committed, 5 row statistics read; 0 = no event */
+#define FM_DEBUG_STEP_TRACE 6 /* [FM] persistent step trace of the last traced draft: u64 [phases][CTAs][8]
+                                 (CTAs = the step's clusters x 8) globaltimer ns: 0 phase start, 1 staged,
+                                 2 done, 3 last copy issued, 4 last MMA committed, 5 partials published,
+                                 6 epilogues done; 0 = no event */
 
 /*
  * fm_debug_copy -- copy nbytes of the selected buffer, starting at byte

@@ -29,6 +29,12 @@ def tokens_match(got, want, logits) -> bool:
     return bool(np.all((got == want) | (margin < MARGIN)))
 
 
+def persistent_step_requested() -> bool:
+    """FM_PERSISTENT=1 asks fm_create for the one-launch draft step."""
+    import os
+    return os.environ.get("FM_PERSISTENT", "") == "1"
+
+
 class Pair:
     """The CUDA drafter (through the C ABI) and the oracle on one workload."""
 
@@ -70,6 +76,7 @@ class Pair:
     def draft(self, seq, anchor, pos, oracle=True):
         tok = self.torch.zeros((1, self.cfg.block), dtype=self.torch.int32, device="cuda")
         fm.fm_draft(self.h, [seq], [anchor], [pos], tok)
+        self.last_launches = fm.fm_last_launch_count(self.h)
         self.torch.cuda.synchronize()
         got = tok.cpu().numpy()[0]
         ref = self.oracle.draft(self.state(seq), anchor, pos) if oracle else None

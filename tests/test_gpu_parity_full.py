@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import fm_synth as S
-from gpu_common import REL_L2, Pair, rel_l2, tokens_match
+from gpu_common import REL_L2, Pair, persistent_step_requested, rel_l2, tokens_match
 
 pytestmark = pytest.mark.gpu
 
@@ -30,6 +30,8 @@ def test_flashmap_4b_step():
     p.append(0, f17, 1024)
     anchor = S.gen_anchor(S.streams(1002)["tokens"], cfg.vocab)
     got, ref = p.draft(0, anchor, 1041)
+    if persistent_step_requested():
+        assert p.last_launches <= 6, p.last_launches      # anchor, K/V, the step, the lm_head
     for l in range(cfg.n_layers):
         assert rel_l2(p.hidden(l), ref.hidden[l]) < REL_L2, l
     assert rel_l2(p.head_out(), ref.head_out) < REL_L2

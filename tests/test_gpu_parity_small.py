@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import fm_synth as S
-from gpu_common import REL_L2, Pair, rel_l2, tokens_match
+from gpu_common import REL_L2, Pair, persistent_step_requested, rel_l2, tokens_match
 
 pytestmark = pytest.mark.gpu
 
@@ -67,6 +67,8 @@ def test_tiny_flashmap_one_step(lm):
     check_cache(p, 0, 64)
     anchor = S.gen_anchor(S.streams(1001)["tokens"], cfg.vocab)
     got, ref = p.draft(0, anchor, 64)
+    if persistent_step_requested():
+        assert p.last_launches <= 6, p.last_launches      # anchor, K/V, the step, the lm_head
     check_draft(p, got, ref)
     check_cache(p, 0, 65)
     p.close()
