@@ -348,6 +348,38 @@ class BatchedStep:
         self.launches += fm.fm_last_launch_count(self.h)
 
 
+def kernel_profile(fm, h, step, n):
+    """Per-kernel device time over n steps (FM_DEBUG_PROFILE brackets every
+    launch with CUDA events on its stream): {name: (launches, ms, bytes)}."""
+    fm.fm_set_debug(h, fm.FM_DEBUG_PROFILE)
+    for _ in range(n):
+        step()
+    prof = fm.fm_profile_read(h)
+    fm.fm_set_debug(h, 0)
+    return prof
+
+
+def hbm_roofline(prof, hbm, peak_src, steps):
+    """The kernel with the largest device time per step against the HBM copy peak."""
+    name, (nl, tms, tb) = max(prof.items(), key=lambda kv: kv[1][1])
+    achieved = (tb / nl) / ((tms / nl) / 1000) / 1e9
+    return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": ncu_traffic(name), "peak_source": f"{peak_src} burst copy", "bytes_per_launch": tb / nl,
+            "ms_per_launch": tms / nl}, \
+        {k: {"launches": v[0] / steps, "ms_per_step": v[1] / steps} for k, v in sorted(prof.items())}
+
+
+def oracle_sample(fn, budget_s=15.0, most=20):
+    """Run fn() until the budget or `most` repetitions; (repetitions, seconds)."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= most:
+            break
+    return n, time.perf_counter() - t0
+
+
 def run_workload(args):
     """The other configs' timed units (one JSON line each, same keys as the default line)."""
     import torch
@@ -355,8 +387,11 @@ def run_workload(args):
     from block_speculative_decoding_fm_gb300 import build
     build.build()
     import block_speculative_decoding_fm_gb300 as fm
+    import fm_synth as S
     hbm, bf16, _, peak_src = peaks()
+    cores = len(os.sched_getaffinity(0))
     extra, unit, value, ms, launches = {}, "steps/s", None, None, 0
+    roofline, kernels, cpu, e2e = None, None, None, None
     with Clocks(0) as clk:
         if args.workload == "tiny":
             w = TinyStep(torch)
@@ -367,7 +402,7 @@ def run_workload(args):
             value, launches = args.steps / (ms / 1000), w.launches
             cfgd = {"workload": "tiny: D 256, 2 layers, 64 context rows, draft at 64 + device acceptance"}
         elif args.workload == "dflash":
-            w = DFlashCycles(torch, args.steps + args.warmup + 3)
+            w = DFlashCycles(torch, args.steps + args.warmup + 3 + 8)
             for _ in range(max(3, args.warmup)):
                 w.step()
             w.launches = 0
@@ -401,6 +436,7 @@ def run_workload(args):
             value, unit, launches = w.rows * n / (ms / 1000), "rows/s", w.launches
             extra["prefill_tflops"] = w.flops * n / (ms / 1000) / 1e12
             extra["tensor_frac_of_measured_bf16"] = extra["prefill_tflops"] / bf16
+            extra["prefill_reps"] = n
             # then the 16-slot draft over the 32768-row context (L = 32769)
             tok = torch.zeros((1, 16), dtype=torch.int32, device="cuda")
             fm.fm_draft(w.h, [0], [123], [w.rows], tok)
@@ -409,10 +445,72 @@ def run_workload(args):
             ms = ms * args.steps / n   # reported per the requested steps below
             cfgd = {"workload": "prefill: fm_context_append of 32768 rows x 12800 (FlashMap-4B), then a draft at "
                                 "L=32769"}
+    # per-kernel device times (a separate pass) and the roofline of the dominant kernel
+    if args.workload == "prefill":
+        prof = kernel_profile(fm, w.h, w.step, 3)
+        gemm = [(k, v) for k, v in prof.items() if k.startswith("prefill.gemm")]
+        flops = sum(v[2] for _, v in gemm)
+        gms = sum(v[1] for _, v in gemm)
+        achieved = flops / (gms / 1000) / 1e12
+        roofline = {"bound": "tensor", "kernel": "prefill.gemm_fc + prefill.gemm_kv (tcgen05, f16 operands)",
+                    "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16, "traffic": None,
+                    "peak_source": f"{peak_src} bf16 burst (f16 has the same nominal tensor rate)",
+                    "flops_per_launch": flops / max(1, sum(v[0] for _, v in gemm)),
+                    "ms_per_launch": gms / max(1, sum(v[0] for _, v in gemm))}
+        kernels = {k: {"launches": v[0] / 3, "ms_per_step": v[1] / 3} for k, v in sorted(prof.items())}
+    elif args.workload != "tiny":
+        steps = 5 if args.workload == "batched" else 20
+        roofline, kernels = hbm_roofline(kernel_profile(fm, w.h, w.step, steps), hbm, peak_src, steps)
+    # the oracle on a bounded sample of the same workload, on the host cores
+    if not args.no_cpu_baseline:
+        from oracle import DFlash, FlashMap
+        if args.workload == "prefill":
+            c = w.cfg
+            o = FlashMap(c, {n_: t.data for n_, t in S.gen_weights(c, 1003).items()}, S.gen_modulation(c, 1003), True)
+            st = o.new_state(1024)
+            rows = S.gen_features(S.streams(1003)["features"], 256, c.feat_dim)
+            k, dt = oracle_sample(lambda: o.context_append(st, rows, 0), 15.0, 10)
+            cpu = {"value": 256 * k / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{k} appends of 256 of the 32768 rows in {dt:.1f} s", "blas_threads": blas_threads()}
+        elif args.workload == "dflash":
+            c = S.dflash_config(max_ctx=4096 + 64)
+            o = DFlash(c, {n_: t.data for n_, t in S.gen_weights(c, 1004).items()})
+            st = o.new_state()
+            fr = S.streams(1004)["features"]
+            o.context_append(st, S.gen_features(fr, 4096, c.feat_dim), 0)
+            row = S.gen_features(fr, 1, c.feat_dim)
+
+            def cycle():   # draft at the context length, then append one row at the anchor position
+                pos = st.length
+                o.draft(st, 7, pos)
+                o.context_append(st, row, pos)
+            k, dt = oracle_sample(cycle, 15.0, 10)
+            cpu = {"value": k / dt, "unit": "cycles/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{k} draft + 1-row append cycles at context 4096 in {dt:.1f} s",
+                   "blas_threads": blas_threads()}
+        elif args.workload == "batched":
+            c = S.flashmap_4b_config(max_ctx=4096 + 64)
+            o = FlashMap(c, {n_: t.data for n_, t in S.gen_weights(c, 1005).items()}, S.gen_modulation(c, 1005), True)
+            st = o.new_state()
+            fr = S.streams(1005)["features"]
+            o.context_append(st, S.gen_features(fr, 4352, c.feat_dim)[:4080], 0)
+            rows = S.gen_features(fr, 9, c.feat_dim)
+            k, dt = oracle_sample(lambda: (o.context_append(st, rows, 4080), o.draft(st, 7, 4089)), 15.0, 10)
+            cpu = {"value": k / dt / 32, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{k} single-sequence append (9 rows) + draft at the mean context 4089 in {dt:.1f} s, "
+                             "scaled to 32 sequences", "blas_threads": blas_threads()}
+        else:
+            c = S.tiny_config(max_ctx=128)
+            o = FlashMap(c, {n_: t.data for n_, t in S.gen_weights(c, 1001).items()}, S.gen_modulation(c, 1001), False)
+            st = o.new_state()
+            o.context_append(st, S.gen_features(S.streams(1001)["features"], 64, c.feat_dim), 0)
+            k, dt = oracle_sample(lambda: o.draft(st, 7, 64), 10.0, 200)
+            cpu = {"value": k / dt, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{k} drafts in {dt:.1f} s", "blas_threads": blas_threads()}
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfgd, "gpu_launches": launches,
-            "clocks": clk.summary(), "cpu_baseline": None, **extra}
+            "roofline": roofline, "kernels": kernels, "clocks": clk.summary(), "cpu_baseline": cpu, **extra}
     print(json.dumps(line), flush=True)
 
 

@@ -720,13 +720,17 @@ bool flashmap_step_program(fm_handle *h, int seq, const FlashMapPlan &pl, std::v
     for (int t = 0; t < P.ntiles; ++t) ++per[step_cluster_of(P, t, ncl)];
     const int most = *std::max_element(per.begin(), per.end());
     if (most > kStepMaxTiles) return false;
-    // the rank's K slice fits one staged piece when it is formed in shared memory
-    int slice = 0;
-    for (int r = 0; r < kStepCS; ++r) slice = std::max(slice, (step_klo(r + 1, P.cpt) - step_klo(r, P.cpt)) * 64);
+    // the rank's K slice fits one staged piece when it is formed in shared memory,
+    // and the q, k, v rows of the heads it covers fit the partial area
     if (P.prologue == SP_SELF_ATTN) {
-      if (slice > 256 || D % hd) return false;
-      const int heads = slice / hd + 1;
-      if ((size_t)heads * 3 * 16 * (hd + 4) * 4 > 52 * 1024) return false;
+      if (D % hd) return false;
+      for (int r = 0; r < kStepCS; ++r) {
+        const int kb = step_klo(r, P.cpt) * 64, ncol = (step_klo(r + 1, P.cpt) - step_klo(r, P.cpt)) * 64;
+        if (ncol == 0) continue;
+        if (ncol > 256) return false;
+        const int heads = (kb + ncol - 1) / hd - kb / hd + 1;
+        if ((size_t)heads * 3 * 16 * (hd + 4) * 4 > 52 * 1024) return false;
+      }
     }
     // the cross-attention tail requests its first key stage in the partial area
     // behind the previous phase's two tiles
@@ -1828,6 +1832,8 @@ fm_status fm_synchronize(fm_handle *h, void *stream) {
   CK(cudaStreamSynchronize(s));
   if (flag) {
     CK(cudaMemsetAsync(h->dev_err, 0, 4, s));
+    // a draft step that wound down early left its grid barrier's arrival count off
+    if (h->step_bar) CK(cudaMemsetAsync(h->step_bar, 0, 64 * 4, s));
     CK(cudaStreamSynchronize(s));
     return fail(h, FM_ERR_TIMEOUT, "a device-side bounded wait gave up; the outputs of the calls since the last check "
                                    "are undefined");

@@ -97,28 +97,26 @@ __device__ __forceinline__ void stamp(const StepArgs &a, int p, int slot) {
 }
 
 // ---- grid barrier ------------------------------------------------------------
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+// A monotonic 64-bit arrival counter: after each phase every CTA adds one with
+// release semantics (no returned value, no separate fence); the phase is
+// complete everywhere when the counter has grown by G past the phase's base.
+// Every launch adds exactly n_phases * G, so at a launch's start the counter,
+// rounded down to a multiple of G, is the launch's base (no CTA of this
+// launch can have completed a phase before this CTA arrives).
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-// This CTA's earlier writes are made visible, then it counts itself in; the
-// last of G resets the counter and advances the generation.
-__device__ __forceinline__ void grid_arrive(uint32_t *bar, int G) {
-  __threadfence();
-  const uint32_t old = atomicAdd(bar, 1u);
-  if (old == (uint32_t)(G - 1)) {
-    atomicExch(bar, 0u);
-    __threadfence();
-    atomicAdd(bar + 32, 1u);
-  }
+__device__ __forceinline__ void grid_arrive(unsigned long long *ctr) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], 1;\n" ::"l"(ctr) : "memory");
 }
-// Wait until the generation has advanced k times past g0; bounded.
-__device__ __forceinline__ bool grid_wait(const uint32_t *bar, uint32_t g0, uint32_t k, int32_t *err) {
-  if (ld_acquire(bar + 32) - g0 >= k) return true;
+// Wait until the counter reaches target; bounded.
+__device__ __forceinline__ bool grid_wait(const unsigned long long *ctr, unsigned long long target, int32_t *err) {
+  if (ld_acquire64(ctr) >= target) return true;
   const long long t0 = clock64();
   long long next = t0 + 4096;
-  while (ld_acquire(bar + 32) - g0 < k) {
+  while (ld_acquire64(ctr) < target) {
     const long long t = clock64();
     if (t > next) {
       if (*reinterpret_cast<volatile int32_t *>(err)) return false;
@@ -132,6 +130,11 @@ __device__ __forceinline__ bool grid_wait(const uint32_t *bar, uint32_t g0, uint
   return true;
 }
 
+// the L2 prefetch of a byte range (no shared memory, no completion to wait for)
+__device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---- cluster barrier among the worker warps ---------------------------------------
 // The producer and MMA warps run ahead on their own, so the hardware cluster
 // barrier (which counts every thread) cannot be used inside the phase loop.
@@ -143,28 +146,34 @@ __device__ __forceinline__ bool cl_sync(const Bars &bars, uint32_t &n, int tid, 
   const uint32_t bar = bars.cluster(n & 1), parity = (n >> 1) & 1;
   ++n;
   named_sync(1, kWorkers);
+  if (tid < kStepCS) {
+    // eight lanes of one warp arrive on the eight ranks' barriers at once; a release
+    // after the named barrier covers every worker's earlier writes
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(bar), "r"(tid));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote) : "memory");
+  }
   if (tid == 0) {
-#pragma unroll
-    for (int r = 0; r < kStepCS; ++r) {
-      uint32_t remote;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(bar), "r"(r));
-      asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote) : "memory");
-    }
     bool ok = true;
     const long long t0 = clock64();
+    long long next = t0 + 4096;
     for (;;) {
       uint32_t done;
       asm volatile(
-          "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+          "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
           " selp.u32 %0, 1, 0, p;\n}\n"
           : "=r"(done)
-          : "r"(bar), "r"(parity), "r"(100000u)
+          : "r"(bar), "r"(parity)
           : "memory");
       if (done) break;
-      if (clock64() - t0 > kWaitBudgetCycles || *reinterpret_cast<volatile int32_t *>(err)) {
-        atomicExch(err, 1);
-        ok = false;
-        break;
+      const long long t = clock64();
+      if (t > next) {
+        if (t - t0 > kWaitBudgetCycles || *reinterpret_cast<volatile int32_t *>(err)) {
+          atomicExch(err, 1);
+          ok = false;
+          break;
+        }
+        next = t + 4096;
       }
     }
     *flag = ok ? 1 : 0;
@@ -174,15 +183,20 @@ __device__ __forceinline__ bool cl_sync(const Bars &bars, uint32_t &n, int tid, 
 }
 
 // ---- a phase's work of this CTA -------------------------------------------------------
+// The tiles of cluster c in a phase (tile i -> cluster (i + rot) % n_clusters):
+// c0, c0 + ncl, c0 + 2 ncl, ... (computed, not stored: local arrays cost an L2
+// round trip here, where shared memory leaves little L1).
 struct Own {
-  int tiles[kStepMaxTiles];
-  int n;        // tiles of this cluster
+  int c0, n;    // first tile and number of tiles of this cluster
+  int ncl;
   int kc0, kc1; // this rank's chunk range in every tile
+  __device__ __forceinline__ int tile(int ti) const { return c0 + ti * ncl; }
 };
 __device__ __forceinline__ void phase_own(const StepPhase &P, int c, int r, int ncl, Own &o) {
-  o.n = 0;
-  for (int i = 0; i < P.ntiles && o.n < kStepMaxTiles; ++i)
-    if (step_cluster_of(P, i, ncl) == c) o.tiles[o.n++] = i;
+  o.ncl = ncl;
+  o.c0 = ((c - P.rot) % ncl + ncl) % ncl;
+  o.n = o.c0 < P.ntiles ? (P.ntiles - o.c0 + ncl - 1) / ncl : 0;
+  if (o.n > kStepMaxTiles) o.n = kStepMaxTiles;   // the host checked the schedule
   o.kc0 = step_klo(r, P.cpt);
   o.kc1 = step_klo(r + 1, P.cpt);
 }
@@ -234,6 +248,258 @@ __device__ __forceinline__ void rank_keys(int L, int r, int &kbeg, int &kend) {
   kend = min(L, kbeg + per);
 }
 
+// The cross-attention tail of a cross-q phase for the cluster's heads (its own
+// function: its registers are not held across the rest of the phase loop).
+__device__ __noinline__ bool cross_tail(const StepArgs &a, const StepPhase &P, const Own &o, int r, int T, int tid,
+                                        const Bars &bars, uint32_t &clpar, volatile int *flags, uint8_t *gbase,
+                                        uint32_t base, int kbeg, int kend, int pre) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, w = warp - 2;
+  float *partf = reinterpret_cast<float *>(gbase + kOffPart);
+  const uint32_t bbuf = base + kOffB, part = base + kOffPart, qbuf = base + kOffQ;
+  const uint32_t stageA = part + 16 * 1024, stageB = bbuf;
+  const uint32_t tileb = (uint32_t)kKeys * P.at.hd * 2;
+  (void)stageB;
+  const StepAttn &A = P.at;
+  const int hd = A.hd;
+  // every rank's q rows are stored (global) and every rank is done reading the partials
+  if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) return false;
+  const int heads_per_tile = kTile / hd;
+  bool ok = true;
+  for (int hi = 0; hi < o.n * heads_per_tile && ok; ++hi) {
+    const int head = o.tile(hi / heads_per_tile) * heads_per_tile + hi % heads_per_tile;
+    if (head >= A.n_heads) continue;
+    if (hi > 0) {
+      // the previous head's partial slot is read by the peers before it is reused
+      if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) { ok = false; break; }
+      pre = 0;
+      cp_async_commit();
+    }
+    const int nst = (kend - kbeg + kKeys - 1) / kKeys;
+    // the rest of the first key stage, and the second (buffer B: the MMAs are done)
+    if (nst > 0 && pre < kKeys) kv_issue(A, head, kbeg, kend, stageA, stageA + tileb, pre, kKeys, tid);
+    cp_async_commit();
+    if (nst > 1) kv_issue(A, head, kbeg + kKeys, kend, stageB, stageB + tileb, 0, kKeys, tid);
+    cp_async_commit();
+    // queries -> f16 hi / lo tiles [16][hd], units permuted by row
+    const uint32_t qhi = qbuf, qlo = qbuf + kRows * hd * 2;
+    const int q4 = hd / 4;
+    {
+      float4 xq[2];   // 16 rows x hd / 4 quads over 256 threads: two each, both in flight
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int i = tid + x * kWorkers;
+        const int t = i / q4, d = 4 * (i - t * q4);
+        xq[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < kRows * q4 && t < T)
+          xq[x] = __ldcg(reinterpret_cast<const float4 *>(A.Q + (size_t)t * A.ldq + head * hd + d));
+      }
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int i = tid + x * kWorkers;
+        if (i >= kRows * q4) continue;
+        const int t = i / q4, d = 4 * (i - t * q4);
+        uint32_t h01, l01, h23, l23;
+        split2_f16(xq[x].x, xq[x].y, h01, l01);
+        split2_f16(xq[x].z, xq[x].w, h23, l23);
+        const uint32_t off = kv_slot(t, d >> 3, hd) + (d & 7) * 2;
+        asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qhi + off), "r"(h01), "r"(h23));
+        asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qlo + off), "r"(l01), "r"(l23));
+      }
+    }
+    // per warp: keys 8w .. 8w + 7 of each stage; thread rows g and g + 8
+    const int gq = lane >> 2, qq = lane & 3;
+    const int NT = hd / 8;
+    float oacc[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+    const int mi = lane >> 3, ri = lane & 7;
+    for (int st = 0; st < nst; ++st) {
+      cp_async_wait<1>();
+      named_sync(1, kWorkers);
+      const uint32_t kbuf = (st & 1) ? stageB : stageA, vbuf = kbuf + tileb;
+      const int key = 8 * w + ri;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f}, s4b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int ks = 0; ks < hd / 16; ks += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbuf + kv_slot(key, 2 * ks + mi, hd), b0, b1, b2, b3);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int kq = ks + h2;
+          const int arow = ri + 8 * (mi & 1), aunit = 2 * kq + (mi >> 1);
+          uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+          ldsm_x4(qhi + kv_slot(arow, aunit, hd), a0, a1, a2, a3);
+          ldsm_x4(qlo + kv_slot(arow, aunit, hd), c0, c1, c2, c3);
+          const uint32_t bb0 = h2 ? b2 : b0, bb1 = h2 ? b3 : b1;
+          mma_f16(s4, a0, a1, a2, a3, bb0, bb1);
+          mma_f16(s4b, c0, c1, c2, c3, bb0, bb1);
+        }
+      }
+      // scores in the log2 domain, masked past kend; rows g (s[0], s[1]) and g + 8 (s[2], s[3])
+      const int kabs = kbeg + st * kKeys + 8 * w + 2 * qq;
+      float s[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[e] = kabs + (e & 1) < kend ? (s4[e] + s4b[e]) * A.scale_log2 : -INFINITY;
+      float alpha[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float mx = fmaxf(s[2 * h2], s[2 * h2 + 1]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m_r[h2], mx);
+        alpha[h2] = mn == -INFINITY ? 1.f : exp2f(m_r[h2] - mn);
+        m_r[h2] = mn;
+      }
+      float prb[4];
+      float rsum[2] = {0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float mm = m_r[e >> 1];
+        prb[e] = mm == -INFINITY ? 0.f : exp2f(s[e] - mm);
+        rsum[e >> 1] += prb[e];
+      }
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        rsum[h2] += __shfl_xor_sync(0xffffffffu, rsum[h2], 1);
+        rsum[h2] += __shfl_xor_sync(0xffffffffu, rsum[h2], 2);
+        l_r[h2] = l_r[h2] * alpha[h2] + rsum[h2];
+      }
+      uint32_t ph0, pl0, ph1, pl1;
+      split2_f16(prb[0], prb[1], ph0, pl0);
+      split2_f16(prb[2], prb[3], ph1, pl1);
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        if (nt < NT) {
+          oacc[nt][0] *= alpha[0]; oacc[nt][1] *= alpha[0];
+          oacc[nt][2] *= alpha[1]; oacc[nt][3] *= alpha[1];
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 16; nt += 4) {
+        if (nt < NT) {
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_t(vbuf + kv_slot(key, nt + mi, hd), v0, v1, v2, v3);
+          mma_f16_k8(oacc[nt], ph0, ph1, v0);
+          mma_f16_k8(oacc[nt], pl0, pl1, v0);
+          mma_f16_k8(oacc[nt + 1], ph0, ph1, v1);
+          mma_f16_k8(oacc[nt + 1], pl0, pl1, v1);
+          mma_f16_k8(oacc[nt + 2], ph0, ph1, v2);
+          mma_f16_k8(oacc[nt + 2], pl0, pl1, v2);
+          mma_f16_k8(oacc[nt + 3], ph0, ph1, v3);
+          mma_f16_k8(oacc[nt + 3], pl0, pl1, v3);
+        }
+      }
+      named_sync(1, kWorkers);   // every warp is done with this stage's buffers
+      if (st + 2 < nst)
+        kv_issue(A, head, kbeg + (st + 2) * kKeys, kend, kbuf, vbuf, 0, kKeys, tid);
+      cp_async_commit();
+    }
+    cp_async_wait<0>();
+    named_sync(1, kWorkers);
+    // merge the eight warps in three halving rounds (scratch: the B buffers, 32 KB,
+    // then the (max, sum) pairs past the first key stage)
+    float *mo = reinterpret_cast<float *>(gbase + kOffB);                 // [4][16][hd]
+    float *mml = reinterpret_cast<float *>(gbase + kOffPart + 16 * 1024 + 2 * tileb);
+    for (int half = 4; half >= 1; half >>= 1) {
+      if (w >= half && w < 2 * half) {
+        const int ww = w - half;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          if (nt < NT) {
+            const int d = 8 * nt + 2 * qq;
+            *reinterpret_cast<float2 *>(mo + (ww * 16 + gq) * hd + d) = make_float2(oacc[nt][0], oacc[nt][1]);
+            *reinterpret_cast<float2 *>(mo + (ww * 16 + gq + 8) * hd + d) = make_float2(oacc[nt][2], oacc[nt][3]);
+          }
+        }
+        if (qq == 0) {
+          mml[(ww * 16 + gq) * 2] = m_r[0];
+          mml[(ww * 16 + gq) * 2 + 1] = l_r[0];
+          mml[(ww * 16 + gq + 8) * 2] = m_r[1];
+          mml[(ww * 16 + gq + 8) * 2 + 1] = l_r[1];
+        }
+      }
+      named_sync(1, kWorkers);
+      if (w < half) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int row = gq + 8 * h2;
+          const float m2 = mml[(w * 16 + row) * 2], l2 = mml[(w * 16 + row) * 2 + 1];
+          const float M = fmaxf(m_r[h2], m2);
+          const float f1 = m_r[h2] == -INFINITY ? 0.f : exp2f(m_r[h2] - M);
+          const float f2 = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
+          l_r[h2] = l_r[h2] * f1 + l2 * f2;
+          m_r[h2] = M;
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt) {
+            if (nt < NT) {
+              const float2 xo = *reinterpret_cast<const float2 *>(mo + (w * 16 + row) * hd + 8 * nt + 2 * qq);
+              oacc[nt][2 * h2] = oacc[nt][2 * h2] * f1 + xo.x * f2;
+              oacc[nt][2 * h2 + 1] = oacc[nt][2 * h2 + 1] * f1 + xo.y * f2;
+            }
+          }
+        }
+      }
+      named_sync(1, kWorkers);
+    }
+    // this rank's partial (unnormalised rows, max, sum) into its partial slot
+    float *po = partf;                   // [16][hd], then [16][2]
+    float *pml = partf + kRows * hd;
+    if (w == 0) {
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        if (nt < NT) {
+          const int d = 8 * nt + 2 * qq;
+          *reinterpret_cast<float2 *>(po + gq * hd + d) = make_float2(oacc[nt][0], oacc[nt][1]);
+          *reinterpret_cast<float2 *>(po + (gq + 8) * hd + d) = make_float2(oacc[nt][2], oacc[nt][3]);
+        }
+      }
+      if (qq == 0) {
+        pml[2 * gq] = m_r[0];
+        pml[2 * gq + 1] = l_r[0];
+        pml[2 * (gq + 8)] = m_r[1];
+        pml[2 * (gq + 8) + 1] = l_r[1];
+      }
+    }
+    if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) { ok = false; break; }
+    // rank r merges rows r and r + 8 over the cluster's ranks, in rank order
+    if (w < 2) {
+      const int t = r + kStepCS * w;
+      if (t < T) {
+        float mq[kStepCS], lq[kStepCS];
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kStepCS; ++q) {
+          const float *rm = cluster.map_shared_rank(pml, q);
+          mq[q] = rm[2 * t];
+          lq[q] = rm[2 * t + 1];
+          M = fmaxf(M, mq[q]);
+        }
+        float den = 0.f;
+        float f[kStepCS];
+#pragma unroll
+        for (int q = 0; q < kStepCS; ++q) {
+          f[q] = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
+          den += f[q] * lq[q];
+        }
+        const float inv = 1.f / den;
+        for (int d = 4 * lane; d < hd; d += 128) {
+          float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < kStepCS; ++q) {
+            const float4 xo = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(po, q) + t * hd + d);
+            accv.x += f[q] * xo.x; accv.y += f[q] * xo.y; accv.z += f[q] * xo.z; accv.w += f[q] * xo.w;
+          }
+          *reinterpret_cast<float4 *>(A.out + (size_t)t * A.ldo + head * hd + d) =
+              make_float4(accv.x * inv, accv.y * inv, accv.z * inv, accv.w * inv);
+        }
+      }
+    }
+  }
+  return ok;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_constant__ StepArgs a) {
@@ -271,30 +537,52 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
     // ---------------------------------------------------------------- weight stream
     if (lane == 0) {
       int u = 0;
-      int last_round[kRing];
-      for (int i = 0; i < kRing; ++i) last_round[i] = -1;
       bool ok = true;
       for (int p = 0; p < a.n_phases && ok; ++p) {
         const StepPhase &P = a.ph[p];
         Own o;
         phase_own(P, c, r, ncl, o);
+        // this CTA's weight slices (and cross-attention key rows) two phases ahead into L2:
+        // HBM idles while a phase waits on its chain, so the next big phases stream from L2
+        for (int pp = (p == 0 ? 0 : p + 2); pp <= p + 2 && pp < a.n_phases; ++pp) {
+          const StepPhase &Q = a.ph[pp];
+          Own oq;
+          phase_own(Q, c, r, ncl, oq);
+          if (oq.kc1 > oq.kc0)
+            for (int ti = 0; ti < oq.n; ++ti)
+              l2_prefetch(Q.g.Wt + ((size_t)oq.tile(ti) * Q.cpt + oq.kc0) * kStageBytes,
+                          (uint32_t)(oq.kc1 - oq.kc0) * kStageBytes);
+          if (Q.tail == ST_CROSS_ATTN && oq.n > 0) {
+            const StepAttn &A = Q.at;
+            const int L = (A.L_src == 0 ? a.sp->L : a.sp->pos + 1) + A.L_add;
+            int kb0, ke0;
+            rank_keys(L, r, kb0, ke0);
+            const int top = min(ke0, a.sp->stable);   // rows later phases do not write
+            if (top > kb0)
+              for (int hi = 0; hi < oq.n * (kTile / A.hd); ++hi) {
+                const int head = oq.tile(hi / (kTile / A.hd)) * (kTile / A.hd) + hi % (kTile / A.hd);
+                if (head >= A.n_heads) continue;
+                const size_t off = ((size_t)head * A.max_ctx + kb0) * A.hd;
+                l2_prefetch(A.Kc + off, (uint32_t)(top - kb0) * A.hd * 2);
+                l2_prefetch(A.Vc + off, (uint32_t)(top - kb0) * A.hd * 2);
+              }
+          }
+        }
         for (int ti = 0; ti < o.n && ok; ++ti) {
-          const uint8_t *src = P.g.Wt + ((size_t)o.tiles[ti] * P.cpt + o.kc0) * kStageBytes;
+          const uint8_t *src = P.g.Wt + ((size_t)o.tile(ti) * P.cpt + o.kc0) * kStageBytes;
           for (int kc = o.kc0; kc < o.kc1; kc += 2) {
             const int st = u % kRing, rd = u / kRing;
             if (rd >= 1 && !mbar_wait_bounded(bars.empty(st), (rd - 1) & 1, a.err)) { ok = false; break; }
             const int nch = min(2, o.kc1 - kc);
             mbar_expect_tx(bars.full(st), nch * kStageBytes);
             bulk_g2s(ring + st * kUnit, src + (size_t)(kc - o.kc0) * kStageBytes, nch * kStageBytes, bars.full(st));
-            last_round[st] = rd;
             ++u;
           }
         }
         stamp(a, p, 3);
       }
-      // wind down: every copy this CTA issued has landed before the CTA may exit
-      for (int st = 0; st < kRing; ++st)
-        if (last_round[st] >= 0) mbar_wait_drain(bars.full(st), last_round[st] & 1);
+      // wind down: every copy this CTA issued (the last kRing units) has landed before the CTA may exit
+      for (int v = u > kRing ? u - kRing : 0; v < u; ++v) mbar_wait_drain(bars.full(v % kRing), (v / kRing) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issue
@@ -350,13 +638,11 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
     const int tid = wtid();
     const int w = warp - 2;
     pdl_wait();
-    if (tid == 0) flags[0] = (int)ld_acquire(a.bar + 32);
-    named_sync(1, kWorkers);
-    const uint32_t g0 = (uint32_t)flags[0];
+    unsigned long long *ctr = reinterpret_cast<unsigned long long *>(a.bar);
+    const unsigned long long base0 = ld_acquire64(ctr) / (unsigned long long)G * (unsigned long long)G;
     uint32_t clpar = 0;
     int pc = 0;
-    int acc_use[kNAcc];   // completions of each accumulator so far (its barrier's parity)
-    for (int i = 0; i < kNAcc; ++i) acc_use[i] = 0;
+    uint32_t acc_par = 0;   // bit ti: parity of accumulator ti's next completion
     for (int p = 0; p < a.n_phases; ++p) {
       const StepPhase &P = a.ph[p];
       const GemvArgs &g = P.g;
@@ -373,12 +659,12 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
         rank_keys(L, r, kbeg, kend);
         const int stable = a.sp->stable;
         pre = kend > kbeg ? max(0, min(kKeys, stable - kbeg)) : 0;
-        const int head0 = o.tiles[0] * kTile / P.at.hd;
+        const int head0 = o.tile(0) * kTile / P.at.hd;
         if (pre > 0) kv_issue(P.at, head0, kbeg, kend, stageA, stageA + tileb, 0, pre, tid);
         cp_async_commit();
       }
       if (p > 0) {
-        if (tid == 0) flags[1] = grid_wait(a.bar, g0, (uint32_t)p, a.err) ? 1 : 0;
+        if (tid == 0) flags[1] = grid_wait(ctr, base0 + (unsigned long long)p * G, a.err) ? 1 : 0;
         named_sync(1, kWorkers);
         if (!flags[1]) break;
       }
@@ -399,15 +685,34 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
           const int ks = hd + 4;
           float *qkv = partf;
           const int q4 = hd / 4;
-          for (int i = tid; i < nh * 3 * kRows * q4; i += kWorkers) {
-            const int d4 = i % q4, rest = i / q4;
-            const int t = rest % kRows, m = (rest / kRows) % 3, hh = rest / (3 * kRows);
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < T)
-              v = __ldcg(reinterpret_cast<const float4 *>(A.qkv + (size_t)t * 3 * D + m * D + (h0 + hh) * hd + 4 * d4));
-            *reinterpret_cast<float4 *>(qkv + ((hh * 3 + m) * kRows + t) * ks + 4 * d4) = v;
+          // every load in flight before any is stored (one round trip, not one per element)
+          const int total = nh * 3 * kRows * q4;
+          for (int i0 = tid; i0 < total; i0 += kWorkers * 6) {
+            float4 v[6];
+#pragma unroll
+            for (int x = 0; x < 6; ++x) {
+              const int i = i0 + x * kWorkers;
+              v[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (i < total) {
+                const int d4 = i % q4, rest = i / q4;
+                const int t = rest % kRows, m = (rest / kRows) % 3, hh = rest / (3 * kRows);
+                if (t < T)
+                  v[x] = __ldcg(
+                      reinterpret_cast<const float4 *>(A.qkv + (size_t)t * 3 * D + m * D + (h0 + hh) * hd + 4 * d4));
+              }
+            }
+#pragma unroll
+            for (int x = 0; x < 6; ++x) {
+              const int i = i0 + x * kWorkers;
+              if (i < total) {
+                const int d4 = i % q4, rest = i / q4;
+                const int t = rest % kRows, m = (rest / kRows) % 3, hh = rest / (3 * kRows);
+                *reinterpret_cast<float4 *>(qkv + ((hh * 3 + m) * kRows + t) * ks + 4 * d4) = v[x];
+              }
+            }
           }
           named_sync(1, kWorkers);
+          if (tid == 0) stamp(a, p, 7);
           // one warp per (head, query row); lane j < T holds the score of key j
           float *ob = reinterpret_cast<float *>(gbase + kOffB + kPieceBytes);   // f32 [16][ncol]
           for (int u = w; u < nh * T; u += 8) {
@@ -424,13 +729,20 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
             const float mx = warp_max(sc);
             const float pr = lane < T ? __expf(sc - mx) : 0.f;
             const float inv = 1.f / warp_sum(pr);
+            // output: lane l owns dims 4l .. 4l + 3 of the head
             const float *vb = qkv + ((hh * 3 + 2) * kRows) * ks;
-            for (int d = lane; d < hd; d += 32) {
-              const int col = (h0 + hh) * hd + d - kb;
-              float acc = 0.f;
-              for (int j = 0; j < T; ++j) acc += __shfl_sync(0xffffffffu, pr, j) * vb[j * ks + d];
-              if (col >= 0 && col < ncol) ob[t * ncol + col] = acc * inv;
+            const bool on = 4 * lane < hd;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < T; ++j) {
+              const float pj = __shfl_sync(0xffffffffu, pr, j);
+              if (on) {
+                const float4 v = *reinterpret_cast<const float4 *>(vb + j * ks + 4 * lane);
+                acc.x += pj * v.x; acc.y += pj * v.y; acc.z += pj * v.z; acc.w += pj * v.w;
+              }
             }
+            const int col = (h0 + hh) * hd + 4 * lane - kb;
+            if (on && col >= 0 && col < ncol)
+              *reinterpret_cast<float4 *>(ob + t * ncol + col) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
           }
           named_sync(1, kWorkers);
           osm = ob;
@@ -439,7 +751,7 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
         const int passes = resident ? 1 : o.n;
         bool stats_done = false;
         for (int ps = 0; ps < passes; ++ps) {
-          const int m0 = o.tiles[resident ? 0 : ps] * kTile;
+          const int m0 = o.tile(resident ? 0 : ps) * kTile;
           for (int x = 0; x < ncol; x += kPieceCols) {
             const int pb = pc & 1;
             // (a wait that gives up raises the error word; the workers still take every
@@ -477,7 +789,7 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
         if (tid == 0) stamp(a, p, 1);
         // -------------------------------------------- accumulators -> partial tiles in shared memory
         for (int ti = w >> 2; ti < o.n; ti += 2) {
-          mbar_wait_bounded(bars.accfull(ti), acc_use[ti] & 1, a.err);
+          mbar_wait_bounded(bars.accfull(ti), (acc_par >> ti) & 1, a.err);
           tc_fence_after();
           const int quad = warp & 3;
           float v[32];
@@ -488,25 +800,35 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
 #pragma unroll
           for (int t = 0; t < kRows; ++t) pt[t * kTile + row] = v[t] + v[16 + t];
         }
-        for (int ti = 0; ti < o.n; ++ti) ++acc_use[ti];
+        acc_par ^= (1u << o.n) - 1u;
       } else if (o.n > 0) {
         // a rank without chunks in this phase (a short K) contributes zero tiles
         for (int i = tid; i < o.n * kPartTile / 16; i += kWorkers)
           reinterpret_cast<float4 *>(partf)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      // the epilogue operands of this rank's units (bias, residual, gate, norm
+      // weights, rotations) load while the partials are published
+      const int nrows = T > kStepCS ? 2 : 1;
+      EpiIn epre;   // the first unit of this warp (most phases give a warp at most one)
+      if (o.n > 0 && w < o.n * nrows) {
+        const int ti = w / nrows, t = r + kStepCS * (w - ti * nrows);
+        if (t < T) epilogue_load(g, t, o.tile(ti) * kTile, epre);
       }
       // -------------------------------------------------- publish the partials to the cluster
       if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) break;
       if (tid == 0) stamp(a, p, 5);
       // -------------------------------------------------- rank r finishes rows r, r + 8 of every tile
       if (o.n > 0) {
-        const int nrows = T > kStepCS ? 2 : 1;
         for (int uu = w; uu < o.n * nrows; uu += 8) {
           const int ti = uu / nrows, t = r + kStepCS * (uu - ti * nrows);
           if (t >= T) continue;
-          const int tile = o.tiles[ti];
+          const int tile = o.tile(ti);
           const int m0 = tile * kTile;
           EpiIn in;
-          epilogue_load(g, t, m0, in);
+          if (uu == w)
+            in = epre;
+          else
+            epilogue_load(g, t, m0, in);
           float4 pv[kStepCS];
 #pragma unroll
           for (int q = 0; q < kStepCS; ++q) {
@@ -524,231 +846,7 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
       if (tid == 0) stamp(a, p, 6);
       // -------------------------------------------------- tail: cross-attention of the cluster's heads
       if (P.tail == ST_CROSS_ATTN && o.n > 0) {
-        const StepAttn &A = P.at;
-        const int hd = A.hd;
-        // every rank's q rows are stored (global) and every rank is done reading the partials
-        if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) break;
-        const int heads_per_tile = kTile / hd;
-        bool ok = true;
-        for (int hi = 0; hi < o.n * heads_per_tile && ok; ++hi) {
-          const int head = o.tiles[hi / heads_per_tile] * heads_per_tile + hi % heads_per_tile;
-          if (head >= A.n_heads) continue;
-          if (hi > 0) {
-            // the previous head's partial slot is read by the peers before it is reused
-            if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) { ok = false; break; }
-            pre = 0;
-            cp_async_commit();
-          }
-          const int nst = (kend - kbeg + kKeys - 1) / kKeys;
-          // the rest of the first key stage, and the second (buffer B: the MMAs are done)
-          if (nst > 0 && pre < kKeys) kv_issue(A, head, kbeg, kend, stageA, stageA + tileb, pre, kKeys, tid);
-          cp_async_commit();
-          if (nst > 1) kv_issue(A, head, kbeg + kKeys, kend, stageB, stageB + tileb, 0, kKeys, tid);
-          cp_async_commit();
-          // queries -> f16 hi / lo tiles [16][hd], units permuted by row
-          const uint32_t qhi = qbuf, qlo = qbuf + kRows * hd * 2;
-          const int q4 = hd / 4;
-          for (int i = tid; i < kRows * q4; i += kWorkers) {
-            const int t = i / q4, d = 4 * (i - t * q4);
-            float4 xq = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < T) xq = __ldcg(reinterpret_cast<const float4 *>(A.Q + (size_t)t * A.ldq + head * hd + d));
-            uint32_t h01, l01, h23, l23;
-            split2_f16(xq.x, xq.y, h01, l01);
-            split2_f16(xq.z, xq.w, h23, l23);
-            const uint32_t off = kv_slot(t, d >> 3, hd) + (d & 7) * 2;
-            asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qhi + off), "r"(h01), "r"(h23));
-            asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qlo + off), "r"(l01), "r"(l23));
-          }
-          // per warp: keys 8w .. 8w + 7 of each stage; thread rows g and g + 8
-          const int gq = lane >> 2, qq = lane & 3;
-          const int NT = hd / 8;
-          float oacc[16][4];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-          float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-          const int mi = lane >> 3, ri = lane & 7;
-          for (int st = 0; st < nst; ++st) {
-            cp_async_wait<1>();
-            named_sync(1, kWorkers);
-            const uint32_t kbuf = (st & 1) ? stageB : stageA, vbuf = kbuf + tileb;
-            const int key = 8 * w + ri;
-            float s4[4] = {0.f, 0.f, 0.f, 0.f}, s4b[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int ks = 0; ks < hd / 16; ks += 2) {
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(kbuf + kv_slot(key, 2 * ks + mi, hd), b0, b1, b2, b3);
-#pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int kq = ks + h2;
-                const int arow = ri + 8 * (mi & 1), aunit = 2 * kq + (mi >> 1);
-                uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-                ldsm_x4(qhi + kv_slot(arow, aunit, hd), a0, a1, a2, a3);
-                ldsm_x4(qlo + kv_slot(arow, aunit, hd), c0, c1, c2, c3);
-                const uint32_t bb0 = h2 ? b2 : b0, bb1 = h2 ? b3 : b1;
-                mma_f16(s4, a0, a1, a2, a3, bb0, bb1);
-                mma_f16(s4b, c0, c1, c2, c3, bb0, bb1);
-              }
-            }
-            // scores in the log2 domain, masked past kend; rows g (s[0], s[1]) and g + 8 (s[2], s[3])
-            const int kabs = kbeg + st * kKeys + 8 * w + 2 * qq;
-            float s[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[e] = kabs + (e & 1) < kend ? (s4[e] + s4b[e]) * A.scale_log2 : -INFINITY;
-            float alpha[2];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              float mx = fmaxf(s[2 * h2], s[2 * h2 + 1]);
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-              const float mn = fmaxf(m_r[h2], mx);
-              alpha[h2] = mn == -INFINITY ? 1.f : exp2f(m_r[h2] - mn);
-              m_r[h2] = mn;
-            }
-            float prb[4];
-            float rsum[2] = {0.f, 0.f};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float mm = m_r[e >> 1];
-              prb[e] = mm == -INFINITY ? 0.f : exp2f(s[e] - mm);
-              rsum[e >> 1] += prb[e];
-            }
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              rsum[h2] += __shfl_xor_sync(0xffffffffu, rsum[h2], 1);
-              rsum[h2] += __shfl_xor_sync(0xffffffffu, rsum[h2], 2);
-              l_r[h2] = l_r[h2] * alpha[h2] + rsum[h2];
-            }
-            uint32_t ph0, pl0, ph1, pl1;
-            split2_f16(prb[0], prb[1], ph0, pl0);
-            split2_f16(prb[2], prb[3], ph1, pl1);
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-              if (nt < NT) {
-                oacc[nt][0] *= alpha[0]; oacc[nt][1] *= alpha[0];
-                oacc[nt][2] *= alpha[1]; oacc[nt][3] *= alpha[1];
-              }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 16; nt += 4) {
-              if (nt < NT) {
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(vbuf + kv_slot(key, nt + mi, hd), v0, v1, v2, v3);
-                mma_f16_k8(oacc[nt], ph0, ph1, v0);
-                mma_f16_k8(oacc[nt], pl0, pl1, v0);
-                mma_f16_k8(oacc[nt + 1], ph0, ph1, v1);
-                mma_f16_k8(oacc[nt + 1], pl0, pl1, v1);
-                mma_f16_k8(oacc[nt + 2], ph0, ph1, v2);
-                mma_f16_k8(oacc[nt + 2], pl0, pl1, v2);
-                mma_f16_k8(oacc[nt + 3], ph0, ph1, v3);
-                mma_f16_k8(oacc[nt + 3], pl0, pl1, v3);
-              }
-            }
-            named_sync(1, kWorkers);   // every warp is done with this stage's buffers
-            if (st + 2 < nst)
-              kv_issue(A, head, kbeg + (st + 2) * kKeys, kend, kbuf, vbuf, 0, kKeys, tid);
-            cp_async_commit();
-          }
-          cp_async_wait<0>();
-          named_sync(1, kWorkers);
-          // merge the eight warps in three halving rounds (scratch: the B buffers, 32 KB,
-          // then the (max, sum) pairs past the first key stage)
-          float *mo = reinterpret_cast<float *>(gbase + kOffB);                 // [4][16][hd]
-          float *mml = reinterpret_cast<float *>(gbase + kOffPart + 16 * 1024 + 2 * tileb);
-          for (int half = 4; half >= 1; half >>= 1) {
-            if (w >= half && w < 2 * half) {
-              const int ww = w - half;
-#pragma unroll
-              for (int nt = 0; nt < 16; ++nt) {
-                if (nt < NT) {
-                  const int d = 8 * nt + 2 * qq;
-                  *reinterpret_cast<float2 *>(mo + (ww * 16 + gq) * hd + d) = make_float2(oacc[nt][0], oacc[nt][1]);
-                  *reinterpret_cast<float2 *>(mo + (ww * 16 + gq + 8) * hd + d) = make_float2(oacc[nt][2], oacc[nt][3]);
-                }
-              }
-              if (qq == 0) {
-                mml[(ww * 16 + gq) * 2] = m_r[0];
-                mml[(ww * 16 + gq) * 2 + 1] = l_r[0];
-                mml[(ww * 16 + gq + 8) * 2] = m_r[1];
-                mml[(ww * 16 + gq + 8) * 2 + 1] = l_r[1];
-              }
-            }
-            named_sync(1, kWorkers);
-            if (w < half) {
-#pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int row = gq + 8 * h2;
-                const float m2 = mml[(w * 16 + row) * 2], l2 = mml[(w * 16 + row) * 2 + 1];
-                const float M = fmaxf(m_r[h2], m2);
-                const float f1 = m_r[h2] == -INFINITY ? 0.f : exp2f(m_r[h2] - M);
-                const float f2 = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
-                l_r[h2] = l_r[h2] * f1 + l2 * f2;
-                m_r[h2] = M;
-#pragma unroll
-                for (int nt = 0; nt < 16; ++nt) {
-                  if (nt < NT) {
-                    const float2 xo = *reinterpret_cast<const float2 *>(mo + (w * 16 + row) * hd + 8 * nt + 2 * qq);
-                    oacc[nt][2 * h2] = oacc[nt][2 * h2] * f1 + xo.x * f2;
-                    oacc[nt][2 * h2 + 1] = oacc[nt][2 * h2 + 1] * f1 + xo.y * f2;
-                  }
-                }
-              }
-            }
-            named_sync(1, kWorkers);
-          }
-          // this rank's partial (unnormalised rows, max, sum) into its partial slot
-          float *po = partf;                   // [16][hd], then [16][2]
-          float *pml = partf + kRows * hd;
-          if (w == 0) {
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-              if (nt < NT) {
-                const int d = 8 * nt + 2 * qq;
-                *reinterpret_cast<float2 *>(po + gq * hd + d) = make_float2(oacc[nt][0], oacc[nt][1]);
-                *reinterpret_cast<float2 *>(po + (gq + 8) * hd + d) = make_float2(oacc[nt][2], oacc[nt][3]);
-              }
-            }
-            if (qq == 0) {
-              pml[2 * gq] = m_r[0];
-              pml[2 * gq + 1] = l_r[0];
-              pml[2 * (gq + 8)] = m_r[1];
-              pml[2 * (gq + 8) + 1] = l_r[1];
-            }
-          }
-          if (!cl_sync(bars, clpar, tid, a.err, flags + 2)) { ok = false; break; }
-          // rank r merges rows r and r + 8 over the cluster's ranks, in rank order
-          if (w < 2) {
-            const int t = r + kStepCS * w;
-            if (t < T) {
-              float mq[kStepCS], lq[kStepCS];
-              float M = -INFINITY;
-#pragma unroll
-              for (int q = 0; q < kStepCS; ++q) {
-                const float *rm = cluster.map_shared_rank(pml, q);
-                mq[q] = rm[2 * t];
-                lq[q] = rm[2 * t + 1];
-                M = fmaxf(M, mq[q]);
-              }
-              float den = 0.f;
-              float f[kStepCS];
-#pragma unroll
-              for (int q = 0; q < kStepCS; ++q) {
-                f[q] = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
-                den += f[q] * lq[q];
-              }
-              const float inv = 1.f / den;
-              for (int d = 4 * lane; d < hd; d += 128) {
-                float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int q = 0; q < kStepCS; ++q) {
-                  const float4 xo = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(po, q) + t * hd + d);
-                  accv.x += f[q] * xo.x; accv.y += f[q] * xo.y; accv.z += f[q] * xo.z; accv.w += f[q] * xo.w;
-                }
-                *reinterpret_cast<float4 *>(A.out + (size_t)t * A.ldo + head * hd + d) =
-                    make_float4(accv.x * inv, accv.y * inv, accv.z * inv, accv.w * inv);
-              }
-            }
-          }
-        }
-        if (!ok) break;
+        if (!cross_tail(a, P, o, r, T, tid, bars, clpar, flags, gbase, base, kbeg, kend, pre)) break;
       } else if (P.tail == ST_CROSS_ATTN) {
         cp_async_wait<0>();
       }
@@ -756,7 +854,7 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
       named_sync(1, kWorkers);
       if (tid == 0) {
         stamp(a, p, 2);
-        grid_arrive(a.bar, G);
+        grid_arrive(ctr);
       }
     }
     cp_async_wait<0>();
