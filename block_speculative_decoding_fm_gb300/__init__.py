@@ -31,7 +31,8 @@ FM_DEBUG_TRACE = 4
 
 EXPORTS = ["fm_create", "fm_time_conditioning", "fm_context_append", "fm_context_append_batched", "fm_draft", "fm_accept",
            "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_synchronize", "fm_selftest_wait_timeout", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
-           "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy"]
+           "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy",
+           "fm_policy_init", "fm_policy_next", "fm_policy_after_round", "fm_policy_after_plain"]
 
 
 class FmConfig(ctypes.Structure):
@@ -51,6 +52,16 @@ class FmTensor(ctypes.Structure):
 class FmKernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int32), ("ms", ctypes.c_float),
                 ("bytes", ctypes.c_double)]
+
+
+class FmVerifyPolicy(ctypes.Structure):
+    _fields_ = [("block", ctypes.c_int32), ("verify", ctypes.c_int32), ("fallback", ctypes.c_int32),
+                ("probe_every", ctypes.c_int32), ("ema", ctypes.c_double), ("ema_tokens", ctypes.c_double),
+                ("round_ms", ctypes.c_double), ("step_ms", ctypes.c_double), ("plain_left", ctypes.c_int32),
+                ("rounds", ctypes.c_int32), ("catch_up", ctypes.c_int32), ("pad", ctypes.c_int32)]
+
+
+FM_ACT_ROUND, FM_ACT_PLAIN, FM_ACT_PLAIN_LIMIT = 0, 1, 2
 
 
 class FmError(RuntimeError):
@@ -92,6 +103,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fm_status_str": (ctypes.c_char_p, [I32]),
         "fm_last_error": (ctypes.c_char_p, [P]),
         "fm_destroy": (None, [P]),
+        "fm_policy_init": (I32, [ctypes.POINTER(FmVerifyPolicy), I32, I32, I32, I32]),
+        "fm_policy_next": (I32, [ctypes.POINTER(FmVerifyPolicy), I32, I32, ctypes.POINTER(I32), ctypes.POINTER(I32)]),
+        "fm_policy_after_round": (I32, [ctypes.POINTER(FmVerifyPolicy), I32, ctypes.c_double]),
+        "fm_policy_after_plain": (I32, [ctypes.POINTER(FmVerifyPolicy), ctypes.c_double, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -304,3 +319,24 @@ def fm_destroy(h) -> None:
 def weight_items(tensors: Dict[str, object]):
     """(name, array, dtype) triples from name -> object with .data / .dtype."""
     return [(n, t.data, t.dtype) for n, t in tensors.items()]
+
+
+def fm_policy_init(block: int, verify: int = 0, fallback: bool = True, probe_every: int = 16) -> FmVerifyPolicy:
+    p = FmVerifyPolicy()
+    _check(load_library().fm_policy_init(ctypes.byref(p), block, verify, 1 if fallback else 0, probe_every))
+    return p
+
+
+def fm_policy_next(p: FmVerifyPolicy, position: int, max_ctx: int) -> Tuple[int, int]:
+    """(action, k): FM_ACT_ROUND with the verify length, or a plain step."""
+    a, k = ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().fm_policy_next(ctypes.byref(p), position, max_ctx, ctypes.byref(a), ctypes.byref(k)))
+    return a.value, k.value
+
+
+def fm_policy_after_round(p: FmVerifyPolicy, accepted: int, ms: float) -> None:
+    _check(load_library().fm_policy_after_round(ctypes.byref(p), accepted, ms))
+
+
+def fm_policy_after_plain(p: FmVerifyPolicy, ms: float, rows_handed: bool) -> None:
+    _check(load_library().fm_policy_after_plain(ctypes.byref(p), ms, 1 if rows_handed else 0))

@@ -269,6 +269,48 @@ FM_API fm_status fm_synchronize(fm_handle *h, void *stream);
  */
 FM_API fm_status fm_selftest_wait_timeout(fm_handle *h, int32_t budget_us, void *stream);
 
+/*
+ * The verify-length and fallback policy of the speculative loop ([FM]
+ * specGenerate): a caller-owned record and four host functions, no device
+ * work.  Per step of the loop fm_policy_next says whether to run a draft round
+ * verifying k drafts (FM_ACT_ROUND), a step of a plain-decoding stretch
+ * (FM_ACT_PLAIN: report it with fm_policy_after_plain), or a plain step at the
+ * drafter's context limit (FM_ACT_PLAIN_LIMIT: position + 2 block + 2 >
+ * max_ctx; no statistics).  After a round, fm_policy_after_round takes the
+ * accepted count and the round's time.
+ *   k: adaptive (verify = 0): block when the acceptance average >= 5, else 7;
+ *      fixed: min(block, verify).
+ *   averages: acceptance 0.6 / 0.4 (starts at 4), tokens per round
+ *      0.75 / 0.25 of accepted + 1 (starts at 5), round time 0.6 / 0.4 (the
+ *      first round after a stretch whose rows were handed to the drafter is left
+ *      out), plain-step time 0.7 / 0.3 (starts at 30 ms).
+ *   fallback: from the fourth round on, when tokens per round x plain-step time
+ *      < 0.85 x round time, a plain stretch of probe_every steps starts (then
+ *      one round probes again).
+ * Errors: FM_ERR_INVALID_ARG (null pointer, block < 1, verify < 0,
+ *   probe_every < 1, accepted < 0, a plain report outside a stretch).
+ */
+typedef struct fm_verify_policy {
+  int32_t block, verify, fallback, probe_every;
+  double ema;          /* acceptance average */
+  double ema_tokens;   /* tokens-per-round average */
+  double round_ms;     /* round-time average, < 0 until the first round */
+  double step_ms;      /* plain-step time average */
+  int32_t plain_left;  /* steps left in the current plain stretch */
+  int32_t rounds;      /* rounds so far */
+  int32_t catch_up;    /* the next round's time is left out of the average */
+  int32_t pad;
+} fm_verify_policy;
+#define FM_ACT_ROUND 0
+#define FM_ACT_PLAIN 1
+#define FM_ACT_PLAIN_LIMIT 2
+FM_API fm_status fm_policy_init(fm_verify_policy *p, int32_t block, int32_t verify, int32_t fallback,
+                                int32_t probe_every);
+FM_API fm_status fm_policy_next(const fm_verify_policy *p, int32_t position, int32_t max_ctx, int32_t *action,
+                                int32_t *k);
+FM_API fm_status fm_policy_after_round(fm_verify_policy *p, int32_t accepted, double ms);
+FM_API fm_status fm_policy_after_plain(fm_verify_policy *p, double ms, int32_t rows_handed);
+
 /* fm_debug_copy selectors ([FM] readOut / peek: look at working buffers) */
 #define FM_DEBUG_HIDDEN 0   /* index = layer: the block's hidden rows after that layer [block][dim] f32 (last draft) */
 #define FM_DEBUG_HEAD_OUT 1 /* the head output Y [block][target_dim] f32 (last draft of seq) */

@@ -96,3 +96,49 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.fm_debug_copy(None, 0, 0, 0, 0, None, 0, None) == fm.FM_ERR_INVALID_ARG
     lib.fm_destroy(None)
     assert lib.fm_last_error(None) is not None
+
+
+def test_verify_policy_matches_the_oracle_step_for_step(lib):
+    """fm_policy_* (the library's host policy) against oracle.policy on seeded
+    random loops: the same actions, verify lengths and state, bit for bit."""
+    from oracle.policy import PLAIN, PLAIN_LIMIT, ROUND, VerifyPolicy
+    rng = np.random.default_rng(21)
+    for trial in range(40):
+        block = int(rng.choice([5, 8, 16]))
+        verify = int(rng.choice([0, 0, 3, 40]))
+        fallback = bool(rng.integers(0, 2))
+        probe = int(rng.integers(1, 20))
+        c = fm.fm_policy_init(block, verify, fallback, probe)
+        o = VerifyPolicy(block, verify, fallback, probe)
+        max_ctx = 4096
+        for step in range(300):
+            pos = int(rng.integers(0, max_ctx)) if rng.random() < 0.1 else int(rng.integers(0, max_ctx // 2))
+            act_c, k_c = fm.fm_policy_next(c, pos, max_ctx)
+            act_o, k_o = o.next_action(pos, max_ctx)
+            assert (act_c, k_c) == (act_o, k_o), (trial, step)
+            if act_o == ROUND:
+                acc = int(rng.integers(0, k_o + 1)) if rng.random() < 0.5 else int(rng.integers(0, 2))
+                ms = float(rng.uniform(5, 200))
+                fm.fm_policy_after_round(c, acc, ms)
+                o.after_round(acc, ms)
+            elif act_o == PLAIN:
+                ms = float(rng.uniform(5, 60))
+                handed = o.plain_left == 1 or rng.random() < 0.1
+                fm.fm_policy_after_plain(c, ms, handed)
+                o.after_plain(ms, handed)
+            else:
+                assert act_o == PLAIN_LIMIT
+            assert (c.ema, c.ema_tokens, c.step_ms, c.plain_left, c.rounds, bool(c.catch_up)) == \
+                (o.ema, o.ema_tokens, o.step_ms, o.plain_left, o.rounds, o.catch_up), (trial, step)
+            assert (c.round_ms < 0) == (o.round_ms is None)
+            if o.round_ms is not None:
+                assert c.round_ms == o.round_ms
+
+
+def test_verify_policy_rejects_bad_arguments(lib):
+    p = fm.FmVerifyPolicy()
+    assert lib.fm_policy_init(ctypes.byref(p), 0, 0, 1, 16) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_policy_init(ctypes.byref(p), 16, -1, 1, 16) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_policy_init(ctypes.byref(p), 16, 0, 1, 16) == fm.FM_OK
+    assert lib.fm_policy_after_plain(ctypes.byref(p), 10.0, 0) == fm.FM_ERR_INVALID_ARG   # no stretch running
+    assert lib.fm_policy_after_round(ctypes.byref(p), -1, 10.0) == fm.FM_ERR_INVALID_ARG
