@@ -290,3 +290,23 @@ def gen_time_cond_weights(cfg: DrafterConfig, seed: int, time_dim: int = 256, co
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7])))
     return {n: Tensor(n, shape, DT_BF16, f32_to_bf16_bits(_normal(rng, shape, std)))
             for n, shape in time_cond_specs(cfg, time_dim, cond_dim)}
+
+
+# ---------------------------------------------------------------- DFlash sequential head
+
+def gen_seq_head_weights(cfg: DrafterConfig, seed: int, variant: str = "markov", rank: int = 256,
+                         w1_std: float = 1.0, w2_std: float = 0.05) -> Dict[str, Tensor]:
+    """The sequential logit head (markov.w1 [V, r], markov.w2 [r, V]; with
+    variant "rnn" also rnn.wH [r, r], rnn.bH [r], rnn.wO [r, V]) and the
+    confidence head (conf.w [d + r, 1], conf.b [1]), bf16.  The bias e1 . w2
+    is scaled to the size of the base logits so that it moves some argmaxes."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 11])))
+    V, d = cfg.vocab, cfg.dim
+    spec = [("markov.w1", (V, rank), w1_std), ("markov.w2", (rank, V), w2_std),
+            ("conf.w", (d + rank, 1), 0.02), ("conf.b", (1,), 0.1)]
+    if variant == "rnn":
+        spec += [("rnn.wH", (rank, rank), 0.05), ("rnn.bH", (rank,), 0.05), ("rnn.wO", (rank, V), 0.1)]
+    out = {}
+    for n, shape, std in spec:
+        out[n] = Tensor(n, shape, DT_BF16, f32_to_bf16_bits(_normal(rng, shape, std)))
+    return out

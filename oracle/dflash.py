@@ -27,6 +27,14 @@ from .common import attention, bf16_to_f64, gelu_tanh, rms_norm
 
 
 @dataclass
+class SequentialResult:
+    tokens: np.ndarray            # [gamma] greedy tokens with the sequential bias
+    scores: np.ndarray            # [gamma, V] base logits + bias
+    conf: np.ndarray              # [gamma] predicted acceptance (empty without a confidence head)
+    length: int                   # positions kept after confidence pruning (gamma without pruning)
+
+
+@dataclass
 class DFlashState:
     k: List[np.ndarray]      # per layer [max_ctx, d]
     v: List[np.ndarray]
@@ -116,3 +124,50 @@ class DFlash:
         Y = out @ self.w["out_proj"]
         logits = Y @ self.E.T
         return DFlashResult(np.argmax(logits, axis=-1).astype(np.int64), logits, Y, hidden)
+
+    def sequential_head(self, res: DFlashResult, anchor: int, thresholds=None, min_conf=None) -> SequentialResult:
+        """The sequential logit head and confidence pruning of the greedy draft
+        (``forwardRows``: ``#markov`` / ``#rnn`` per position, ``#confidence``,
+        Alg 1 pruning).  For position k, with prev the anchor (k = 0) or the token
+        of position k - 1:
+          e1 = markov.w1[prev];
+          Markov: bias = e1 markov.w2;  RNN: s = tanh(s rnn.wH + e1 + rnn.bH)
+          (s starts at 0), bias = s rnn.wO;
+          token_k = argmax(base logits_k + bias);
+          conf_k = sigmoid([block_k, e1] conf.w + conf.b), block = the
+          out_norm'd backbone rows.
+        Pruning: the threshold of position k is thresholds[k] when given, else
+        min_conf; the block ends at the first k >= 1 whose conf_k is below it
+        (position 0 is always kept), and no later position is drafted."""
+        c = self.cfg
+        w = self.w
+        rnn = "rnn.wH" in w
+        has_conf = "conf.w" in w
+        block = rms_norm(res.hidden[-1], w["out_norm"], c.rms_eps)
+        r = w["markov.w1"].shape[1]
+        state = np.zeros(r)
+        prev = int(anchor)
+        tokens, scores, conf = [], [], []
+        length = None
+        for k in range(c.block):
+            e1 = w["markov.w1"][prev]
+            if rnn:
+                state = np.tanh(state @ w["rnn.wH"] + e1 + w["rnn.bH"])
+                bias = state @ w["rnn.wO"]
+            else:
+                bias = e1 @ w["markov.w2"]
+            sc = res.logits[k] + bias
+            tok = int(np.argmax(sc))
+            tokens.append(tok)
+            scores.append(sc)
+            prev = tok
+            if has_conf:
+                z = float(np.concatenate([block[k], e1]) @ w["conf.w"][:, 0] + w["conf.b"][0])
+                conf.append(1.0 / (1.0 + np.exp(-z)))
+                thr = thresholds[k] if thresholds is not None else min_conf
+                if k > 0 and thr is not None and conf[-1] < thr:
+                    length = k
+                    break
+        if length is None:
+            length = len(tokens)
+        return SequentialResult(np.array(tokens, np.int64), np.stack(scores), np.array(conf), length)

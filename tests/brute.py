@@ -323,3 +323,47 @@ def time_conditioning(weights, n_layers: int, time_dim: int, time_scale: float, 
             out.extend(lin(f"layers.{l}.{n}.linear", cond))
     out.extend(lin("final_adaln.linear", cond))
     return out
+
+
+def dflash_sequential(weights, base_logits, block_rows, anchor: int, rms_eps: float, thresholds=None, min_conf=None):
+    """The greedy sequential head by loops (module-dflash.ts ``forwardRows``):
+    base_logits [gamma][V] and block_rows [gamma][d] (the backbone rows before
+    out_norm) as lists; returns (tokens, conf, length)."""
+    w1 = mat(weights["markov.w1"])
+    rnn = "rnn.wH" in weights
+    if rnn:
+        wH, bH, wO = mat(weights["rnn.wH"]), vec(weights["rnn.bH"]), mat(weights["rnn.wO"])
+    else:
+        w2 = mat(weights["markov.w2"])
+    onw = vec(weights["out_norm"])
+    cw = [row[0] for row in mat(weights["conf.w"])] if "conf.w" in weights else None
+    cb = vec(weights["conf.b"])[0] if "conf.b" in weights else 0.0
+    r = len(w1[0])
+    V = len(base_logits[0])
+    s = [0.0] * r
+    prev = anchor
+    tokens, conf = [], []
+    for k in range(len(base_logits)):
+        e1 = w1[prev]
+        if rnn:
+            s = [math.tanh(sum(s[i] * wH[i][j] for i in range(r)) + e1[j] + bH[j]) for j in range(r)]
+            bias = [sum(s[i] * wO[i][v] for i in range(r)) for v in range(V)]
+        else:
+            bias = [sum(e1[i] * w2[i][v] for i in range(r)) for v in range(V)]
+        sc = [base_logits[k][v] + bias[v] for v in range(V)]
+        best = 0
+        for v in range(1, V):
+            if sc[v] > sc[best]:
+                best = v
+        tokens.append(best)
+        prev = best
+        if cw is not None:
+            row = block_rows[k]
+            ms = sum(x * x for x in row) / len(row)
+            h = [row[i] * onw[i] / math.sqrt(ms + rms_eps) for i in range(len(row))]
+            z = sum(a * b for a, b in zip(h + list(e1), cw)) + cb
+            conf.append(1.0 / (1.0 + math.exp(-z)))
+            thr = thresholds[k] if thresholds is not None else min_conf
+            if k > 0 and thr is not None and conf[-1] < thr:
+                return tokens, conf, k
+    return tokens, conf, len(tokens)
