@@ -13,8 +13,9 @@ Readings taken where the page leaves a step open:
   * the anchor embedding is a plain row of the tied token table E (no scale);
     the bf16 cast of the hidden before the target's lm_head is not modelled.
   * the retained context K/V is kept exact (the page keeps it as an f32 array).
-  * the sequential (markov / rnn) logit bias is zero: markov.w2 starts at zero,
-    so the parallel draft is the base logits' argmax.
+  * ``draft`` is the parallel draft, the base logits' argmax (what the page
+    drafts while markov.w2 is still at its zero init); ``sequential_head``
+    adds the sequential bias, the confidence and the pruning on top of it.
 """
 from __future__ import annotations
 
@@ -136,9 +137,11 @@ class DFlash:
           token_k = argmax(base logits_k + bias);
           conf_k = sigmoid([block_k, e1] conf.w + conf.b), block = the
           out_norm'd backbone rows.
-        Pruning: the threshold of position k is thresholds[k] when given, else
-        min_conf; the block ends at the first k >= 1 whose conf_k is below it
-        (position 0 is always kept), and no later position is drafted."""
+        Pruning: the threshold of position k is thresholds[k] when the list has
+        one there (not None, not NaN), else min_conf (the page's
+        ``thresholds?.[step] ?? minConf``); the block ends at the first k >= 1
+        whose conf_k is below it (position 0 is always kept), and no later
+        position is drafted."""
         c = self.cfg
         w = self.w
         rnn = "rnn.wH" in w
@@ -164,7 +167,9 @@ class DFlash:
             if has_conf:
                 z = float(np.concatenate([block[k], e1]) @ w["conf.w"][:, 0] + w["conf.b"][0])
                 conf.append(1.0 / (1.0 + np.exp(-z)))
-                thr = thresholds[k] if thresholds is not None else min_conf
+                thr = thresholds[k] if thresholds is not None and k < len(thresholds) else None
+                if thr is None or thr != thr:      # no threshold of its own (None or NaN): min_conf
+                    thr = min_conf
                 if k > 0 and thr is not None and conf[-1] < thr:
                     length = k
                     break

@@ -363,7 +363,11 @@ def dflash_sequential(weights, base_logits, block_rows, anchor: int, rms_eps: fl
             h = [row[i] * onw[i] / math.sqrt(ms + rms_eps) for i in range(len(row))]
             z = sum(a * b for a, b in zip(h + list(e1), cw)) + cb
             conf.append(1.0 / (1.0 + math.exp(-z)))
-            thr = thresholds[k] if thresholds is not None else min_conf
+            thr = None
+            if thresholds is not None and k < len(thresholds) and thresholds[k] is not None and thresholds[k] == thresholds[k]:
+                thr = thresholds[k]
+            if thr is None:
+                thr = min_conf
             if k > 0 and thr is not None and conf[-1] < thr:
                 return tokens, conf, k
     return tokens, conf, len(tokens)

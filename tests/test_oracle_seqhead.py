@@ -88,3 +88,9 @@ def test_constant_confidence_and_the_pruning_rule():
     assert o.sequential_head(res, 3, thresholds=[1.0, 0.4, 0.6]).length == 2
     # a given per-position threshold wins over min_conf
     assert o.sequential_head(res, 3, thresholds=[0.0, 0.0, 0.0], min_conf=0.9).length == 3
+    # a position the list leaves open (None or NaN) takes min_conf, as the
+    # page's per-position lookup falls back to the uniform override
+    assert o.sequential_head(res, 3, thresholds=[0.0, None, 0.0], min_conf=0.9).length == 1
+    assert o.sequential_head(res, 3, thresholds=[0.0, 0.0, float("nan")], min_conf=0.9).length == 2
+    assert o.sequential_head(res, 3, thresholds=[0.0, 0.0], min_conf=0.9).length == 2
+    assert o.sequential_head(res, 3, thresholds=[0.0, None, None]).length == 3
