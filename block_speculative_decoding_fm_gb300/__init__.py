@@ -29,7 +29,8 @@ FM_DEBUG_KEEP_HIDDEN = 1
 FM_DEBUG_PROFILE = 2
 FM_DEBUG_TRACE = 4
 
-EXPORTS = ["fm_create", "fm_time_conditioning", "fm_context_append", "fm_context_append_batched", "fm_draft", "fm_accept",
+EXPORTS = ["fm_create", "fm_time_conditioning", "fm_context_append", "fm_context_append_batched", "fm_draft",
+           "fm_draft_pruned", "fm_accept",
            "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_synchronize", "fm_selftest_wait_timeout", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
            "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy",
            "fm_policy_init", "fm_policy_next", "fm_policy_after_round", "fm_policy_after_plain"]
@@ -89,6 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fm_context_append": (I32, [P, I32, P, I32, I32, P]),
         "fm_context_append_batched": (I32, [P, I32, P, P, P, P, P]),
         "fm_draft": (I32, [P, I32, P, P, P, P, P]),
+        "fm_draft_pruned": (I32, [P, I32, I32, I32, P, ctypes.c_float, P, P, P, P]),
         "fm_accept": (I32, [P, P, I32, P, P]),
         "fm_accept_batched": (I32, [P, I32, P, P, P, P, P, P]),
         "fm_lm_head_argmax_noalloc": (I32, [P, P, I32, P, P]),
@@ -221,6 +223,20 @@ def fm_draft(h, seq_ids: Sequence[int], anchors: Sequence[int], pos: Sequence[in
     an = np.ascontiguousarray(anchors, np.int32)
     ps = np.ascontiguousarray(pos, np.int32)
     _check(lib.fm_draft(h, len(ids), _ptr(ids), _ptr(an), _ptr(ps), _ptr(tokens), _stream(stream)), h)
+
+
+def fm_draft_pruned(h, seq: int, anchor: int, pos: int, tokens, conf=None, length=None, thresholds=None,
+                    min_conf: Optional[float] = None, stream=None) -> None:
+    """The DFlash draft through the sequential head with confidence pruning.
+    tokens: a CUDA int32 tensor [block]; conf: a CUDA float32 tensor [block] or
+    None; length: a CUDA int32 tensor [1] or None.  thresholds: per-position
+    thresholds (a sequence of block floats, NaN for none) or None, in which
+    case min_conf (None: no pruning) applies to every position."""
+    lib = load_library()
+    thr = None if thresholds is None else np.ascontiguousarray(thresholds, np.float32)
+    mc = float("nan") if min_conf is None else float(min_conf)
+    _check(lib.fm_draft_pruned(h, seq, anchor, pos, _ptr(thr), mc, _ptr(tokens), _ptr(conf), _ptr(length),
+                               _stream(stream)), h)
 
 
 def fm_accept(draft: Sequence[int], target: Sequence[int], k: int) -> Tuple[int, int]:

@@ -82,6 +82,13 @@ struct fm_handle {
   int32_t *tickets = nullptr;  // [0, H): self, [H, 2H): cross, [2H]: lm head
   int32_t *tok_tmp = nullptr;
 
+  // ---- DFlash sequential logit head and confidence head (optional tensors) ----
+  __nv_bfloat16 *seq_w1 = nullptr;   // markov.w1 [V][r]
+  __nv_bfloat16 *seq_W = nullptr;    // markov.w2, or rnn.wO with the RNN head [r][V]
+  __nv_bfloat16 *seq_wH = nullptr, *seq_bH = nullptr;  // RNN head only: [r][r], [r]
+  __nv_bfloat16 *conf_w = nullptr, *conf_b = nullptr;  // [d + r], [1], or null
+  int seq_rank = 0;                   // r; 0: no sequential head (each slot's argmax is its token)
+
   // ---- dense prefill (tcgen05) ----
   __half *w_fc16 = nullptr, *w_kv16 = nullptr;  // f16 copies of fc and the stacked cross K/V
   __half *pf_a = nullptr, *pf_c = nullptr;       // scratch: f16 feature rows, f16 weighted fc output
@@ -114,6 +121,11 @@ struct fm_handle {
     uint8_t *ylm = nullptr;
     float2 *st_x = nullptr, *st_c = nullptr, *st_a = nullptr, *st_u = nullptr, *lm_part = nullptr;
     int32_t *tickets = nullptr;
+    // sequential head: base logits [block][V], RNN states [2][r], per-CTA bests,
+    // flags {decided, length, ticket, -, scratch tokens [kMaxT]}
+    float *seq_base = nullptr, *seq_state = nullptr;
+    float2 *seq_part = nullptr;
+    int32_t *seq_flags = nullptr;
     cudaStream_t stream = nullptr;
     cudaEvent_t done = nullptr;
     // a short append whose K/V projection waits for this sequence's next draft
@@ -852,6 +864,61 @@ fm_status dflash_append_rows(fm_handle *h, int seq, const StepParams *sp, cudaSt
   return run_gemv(h, b, s, "gemv.kv_append", 32);
 }
 
+// The sequential head after the parallel block: the lm_head stores the block's
+// base logits, then position k = 0 .. block-1 in turn adds its bias (Markov:
+// markov.w1[prev] markov.w2; RNN: the recurrent state through rnn.wO) and takes
+// the argmax, which is position k + 1's prev; the confidence head and the
+// pruning decision ride on the same launch.  Positions after a pruned one see
+// the decided flag and return at once.
+fm_status dflash_seq_head(fm_handle *h, int seq, const StepParams *sp, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int G = c.block, V = c.vocab, r = h->seq_rank;
+  fm_handle::Lane &ln = h->lanes[seq];
+  TRY(run_lmhead(h, h->Y, G, sp, ln.seq_flags + 4, ln.seq_base, s, h->ylm));
+  CK(launch_seq_init(ln.seq_flags, G, s));
+  ++h->last_launches;
+  SeqArgs q{};
+  q.base = ln.seq_base;
+  q.V = V;
+  q.r = r;
+  q.d = c.dim;
+  q.w1 = h->seq_w1;
+  q.W = h->seq_W;
+  q.sp = sp;
+  q.part = ln.seq_part;
+  q.ticket = ln.seq_flags + 2;
+  q.flags = ln.seq_flags;
+  q.conf_w = h->conf_w;
+  q.conf_b = h->conf_b;
+  q.X = h->X;
+  q.out_norm = h->out_norm;
+  q.eps = c.rms_eps;
+  q.T = G;
+  for (int k = 0; k < G; ++k) {
+    if (h->seq_wH) {
+      RnnArgs ra{};
+      ra.w1 = h->seq_w1;
+      ra.wH = h->seq_wH;
+      ra.bH = h->seq_bH;
+      ra.s_in = ln.seq_state + (size_t)((k + 1) & 1) * r;
+      ra.s_out = ln.seq_state + (size_t)(k & 1) * r;
+      ra.r = r;
+      ra.k = k;
+      ra.sp = sp;
+      ra.flags = ln.seq_flags;
+      ProfScope ps(h, s, "seq.rnn", (double)r * r * 2 + (double)r * 2 * 2);
+      CK(launch_rnn_step(ra, s));
+      ++h->last_launches;
+      q.state = ra.s_out;
+    }
+    q.k = k;
+    ProfScope ps(h, s, "seq.bias_argmax", (double)r * V * 2 + (double)V * 4);
+    CK(launch_seq_bias_argmax(q, s));
+    ++h->last_launches;
+  }
+  return FM_OK;
+}
+
 fm_status dflash_draft_launch(fm_handle *h, int seq, int pos, const StepParams *sp, cudaStream_t s) {
   const fm_config &c = h->cfg;
   const int d = c.dim, G = c.block, H = c.target_dim, F = c.ff_dim, L = c.n_layers;
@@ -948,7 +1015,8 @@ fm_status dflash_draft_launch(fm_handle *h, int seq, int pos, const StepParams *
   op.ylm = h->ylm;
   op.ylm_f16 = c.lm_format == FM_LM_Q8_0;
   TRY(run_gemv(h, op, s, "gemv.out_proj", G));
-  return run_lmhead(h, h->Y, G, sp, nullptr, nullptr, s, h->ylm);
+  if (!h->seq_rank) return run_lmhead(h, h->Y, G, sp, nullptr, nullptr, s, h->ylm);
+  return dflash_seq_head(h, seq, sp, s);
 }
 
 // ---------------------------------------------------------------- dense prefill
@@ -1013,6 +1081,10 @@ fm_status flashmap_prefill(fm_handle *h, int seq, const float *feats, int n, int
     k.N = L * 2 * D;
     k.K = D;
     k.epi = TC_EPI_KV;
+    // the stacked K/V weights (L * 2 * D rows) outweigh the rows' A panel: the
+    // CTAs in flight walk the row blocks of a 16 MB A panel under one B tile
+    k.group_m = (int)((16u << 20) / ((size_t)128 * D * 2));
+    if (k.group_m < 1) k.group_m = 1;
     k.err = h->pf_err;
     k.in_st = h->pf_st;
     k.in_st_n = D / 256;
@@ -1106,7 +1178,10 @@ fm_status flush_pending(fm_handle *h, int seq, cudaStream_t s) {
   });
 }
 
-fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s) {
+// conf, length, thr: the sequential head's confidence outputs and pruning
+// thresholds (thr[k] NaN: none), all optional
+fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens, cudaStream_t s,
+                    float *conf = nullptr, int32_t *length = nullptr, const float *thr = nullptr) {
   const fm_config &c = h->cfg;
   fm_handle::Lane &lane = h->lanes[seq];
   int n_pend = 0;
@@ -1127,6 +1202,9 @@ fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens,
   p.pos = pos;
   p.anchor = anchor;
   p.tokens = tokens;
+  p.conf = conf;
+  p.length = length;
+  for (int k = 0; k < 16; ++k) p.thr[k] = thr && k < c.block ? thr[k] : NAN;
   int L_now;
   if (c.variant == FM_VARIANT_FLASHMAP) {
     p.L = pos + 1;
@@ -1404,6 +1482,51 @@ fm_status create_flashmap(fm_handle *h, const TensorSet &ts, const float *modula
   return FM_OK;
 }
 
+// The sequential logit head is present when the weights hold markov.w1 [V][r]
+// (bf16, r <= 512): the Markov head with markov.w2 [r][V], or the RNN head when
+// rnn.wH [r][r], rnn.bH [r] and rnn.wO [r][V] are there too; conf.w [d + r] and
+// conf.b [1] add the confidence head.
+fm_status create_seq_head(fm_handle *h, const TensorSet &ts, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  const int V = c.vocab, G = c.block;
+  auto it = ts.by_name.find("markov.w1");
+  if (it == ts.by_name.end()) return FM_OK;
+  const fm_tensor *t = it->second;
+  if (t->dtype != FM_DTYPE_BF16 || t->nbytes <= 0 || t->nbytes % ((int64_t)2 * V))
+    return fail(h, FM_ERR_INVALID_ARG, "markov.w1: expected bf16 [%d][r]", V);
+  const int r = (int)(t->nbytes / ((int64_t)2 * V));
+  if (r > 512) return fail(h, FM_ERR_UNSUPPORTED, "sequential head rank %d > 512", r);
+  if (V % 8) return fail(h, FM_ERR_UNSUPPORTED, "sequential head needs vocab %% 8 == 0 (vocab %d)", V);
+  h->seq_rank = r;
+  const size_t rv = (size_t)r * V;
+  TRY(dalloc(h, &h->seq_w1, rv));
+  TRY(put_bf16(h, ts, "markov.w1", h->seq_w1, (int64_t)rv, s));
+  TRY(dalloc(h, &h->seq_W, rv));
+  if (ts.by_name.count("rnn.wH")) {
+    TRY(dalloc(h, &h->seq_wH, (size_t)r * r));
+    TRY(put_bf16(h, ts, "rnn.wH", h->seq_wH, (int64_t)r * r, s));
+    TRY(dalloc(h, &h->seq_bH, (size_t)r));
+    TRY(put_bf16(h, ts, "rnn.bH", h->seq_bH, r, s));
+    TRY(put_bf16(h, ts, "rnn.wO", h->seq_W, (int64_t)rv, s));
+  } else {
+    TRY(put_bf16(h, ts, "markov.w2", h->seq_W, (int64_t)rv, s));
+  }
+  if (ts.by_name.count("conf.w")) {
+    TRY(dalloc(h, &h->conf_w, (size_t)c.dim + r));
+    TRY(put_bf16(h, ts, "conf.w", h->conf_w, (int64_t)c.dim + r, s));
+    TRY(dalloc(h, &h->conf_b, 1));
+    TRY(put_bf16(h, ts, "conf.b", h->conf_b, 1, s));
+  }
+  for (fm_handle::Lane &L : h->lanes) {
+    TRY(dalloc(h, &L.seq_base, (size_t)G * V));
+    TRY(dalloc(h, &L.seq_state, (size_t)2 * r));
+    TRY(dalloc(h, &L.seq_part, (size_t)seq_grid(V)));
+    TRY(dalloc(h, &L.seq_flags, (size_t)4 + kMaxT));
+    CK(cudaMemsetAsync(L.seq_flags, 0, ((size_t)4 + kMaxT) * 4, s));
+  }
+  return FM_OK;
+}
+
 fm_status create_dflash(fm_handle *h, const TensorSet &ts, cudaStream_t s) {
   const fm_config &c = h->cfg;
   const int d = c.dim, H = c.target_dim, F = c.ff_dim, L = c.n_layers, G = c.block;
@@ -1464,6 +1587,7 @@ fm_status create_dflash(fm_handle *h, const TensorSet &ts, cudaStream_t s) {
   TRY(dalloc(h, &h->w_out, (size_t)H * d));
   TRY(put_bf16_t(h, ts, "out_proj", d, H, h->w_out, d, tmp, s));
   TRY(create_common(h, s));
+  TRY(create_seq_head(h, ts, s));
   TRY(dalloc(h, &h->hinit, (size_t)kMaxT * d));
   CK(cudaMemsetAsync(h->hinit, 0, (size_t)kMaxT * d * 4, s));
   CK(launch_block_consts(mask_emb, h->block_pos, G, d, h->hinit, h->st_init, s));
@@ -1691,6 +1815,30 @@ fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const i
   return run_lanes(h, n_seqs, seq_ids, s, [&](int i, cudaStream_t ls) {
     return draft_one(h, seq_ids[i], anchors[i], pos[i], tokens + (size_t)i * h->cfg.block, ls);
   });
+}
+
+fm_status fm_draft_pruned(fm_handle *h, int32_t seq, int32_t anchor, int32_t pos, const float *thresholds,
+                          float min_conf, int32_t *tokens, float *conf, int32_t *length, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  const fm_config &c = h->cfg;
+  if (!h->seq_rank) return fail(h, FM_ERR_UNSUPPORTED, "the weights hold no sequential head (markov.w1)");
+  if (!tokens) return fail(h, FM_ERR_INVALID_ARG, "null tokens");
+  TRY(check_seq(h, seq));
+  if (anchor < 0 || anchor >= c.vocab) return fail(h, FM_ERR_INVALID_ARG, "anchor %d outside [0, %d)", anchor, c.vocab);
+  if (pos != h->length[seq]) return fail(h, FM_ERR_STATE, "pos %d != length %d", pos, h->length[seq]);
+  if ((int64_t)pos + c.block + 1 > c.max_ctx) return fail(h, FM_ERR_CONTEXT_FULL, "context full at pos %d", pos);
+  float thr[16];
+  bool any = false;
+  for (int k = 0; k < 16; ++k) {
+    // a position without a threshold of its own (NaN) takes min_conf
+    thr[k] = k >= c.block ? NAN : thresholds && thresholds[k] == thresholds[k] ? thresholds[k] : min_conf;
+    any = any || thr[k] == thr[k];
+  }
+  if (!h->conf_w && (any || conf))
+    return fail(h, FM_ERR_UNSUPPORTED, "the weights hold no confidence head (conf.w, conf.b)");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return draft_one(h, seq, anchor, pos, tokens, s, conf, length, thr);
 }
 
 fm_status fm_accept(const int32_t *draft, const int32_t *target, int32_t k, int32_t *n_accepted, int32_t *bonus) {

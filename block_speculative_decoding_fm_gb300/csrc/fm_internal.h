@@ -25,7 +25,41 @@ struct StepParams {
   int32_t pad1, pad2;
   const float *feats;  // append: feature rows [T][feat_dim]
   int32_t *tokens;     // draft: where the argmax tokens go [T]
+  float *conf;         // sequential head: the confidence of each position [T], or null
+  int32_t *length;     // sequential head: positions kept after pruning [1], or null
+  float thr[16];       // sequential head: pruning threshold of each position (NaN: none)
 };
+
+// --- the DFlash sequential logit head and confidence (k_seqhead.cu) ---------
+struct SeqArgs {
+  const float *base;           // [T][V] base logits of the block
+  int32_t V, r, k, d;          // vocab, rank, position, draft width
+  const __nv_bfloat16 *w1;     // markov.w1 [V][r]
+  const __nv_bfloat16 *W;      // markov.w2 or rnn.wO [r][V]
+  const float *state;          // RNN: s_k [r]; null: Markov (e1 = w1[prev])
+  const StepParams *sp;        // anchor (position 0's prev), tokens, conf, length, thr
+  float2 *part;                // [gridDim] per-CTA bests
+  int32_t *ticket;             // [1]
+  int32_t *flags;              // [0]: decided (pruning ended the block), [1]: length so far
+  // confidence
+  const __nv_bfloat16 *conf_w, *conf_b;   // [d + r], [1] (null: no confidence head)
+  const float *X;              // backbone rows before out_norm [T][d]
+  const __nv_bfloat16 *out_norm;
+  float eps;
+  int32_t T;                   // positions in the block
+};
+struct RnnArgs {
+  const __nv_bfloat16 *w1, *wH, *bH;   // [V][r], [r][r], [r]
+  const float *s_in;           // s_{k-1} [r]
+  float *s_out;                // s_k [r]
+  int32_t r, k;
+  const StepParams *sp;
+  const int32_t *flags;
+};
+cudaError_t launch_seq_bias_argmax(const SeqArgs &a, cudaStream_t s);
+int seq_grid(int V);
+cudaError_t launch_rnn_step(const RnnArgs &a, cudaStream_t s);
+cudaError_t launch_seq_init(int32_t *flags, int32_t T, cudaStream_t s);
 
 // --- skinny GEMV: Y[t][m] = sum_k A[t][k] W[m][k] for t < T <= 32 ----------
 enum AMode : int32_t {

@@ -201,6 +201,37 @@ FM_API fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids_h
                    const int32_t *pos_host, int32_t *tokens_dev, void *stream);
 
 /*
+ * fm_draft_pruned -- [DF] the greedy draft of one sequence through the
+ * sequential logit head, with the confidence head and confidence pruning
+ * (module-dflash.ts: ``#markov`` (Eq 5), ``#rnn`` (Eq 6), ``#confidence`` and
+ * the pruning of Alg 1 in ``forwardRows``).  Needs weights that hold
+ * markov.w1 [V][r] (r <= 512, vocab % 8 == 0) and markov.w2 [r][V], or the RNN
+ * head (rnn.wH [r][r], rnn.bH [r], rnn.wO [r][V]); conf.w [dim + r] and
+ * conf.b [1] for conf_dev and any threshold.  With such weights fm_draft also
+ * drafts through the sequential head (no pruning).
+ * Position k (prev = anchor for k = 0, else token k - 1; e1 = markov.w1[prev]):
+ *   Markov bias = e1 markov.w2; RNN s_k = tanh(s_{k-1} rnn.wH + e1 + rnn.bH),
+ *   s_{-1} = 0, bias = s_k rnn.wO;  token_k = argmax(base logits_k + bias),
+ *   ties to the lower index;  conf_k = sigmoid([out_norm(row k), e1] conf.w
+ *   + conf.b).
+ * Pruning: the threshold of position k is thresholds_host[k] (host float
+ * [block], or NULL) unless that is NaN, else min_conf (NaN: none), as the
+ * page's per-position lookup falls back to its uniform override.  The block ends at the
+ * first k >= 1 with conf_k below its threshold (length = k).  Entries
+ * 0 .. min(length, block - 1) of tokens_dev and conf_dev are written (the
+ * cut position's own, whose confidence decided the cut, included); later
+ * positions are not drafted and their entries are left as they were.
+ * tokens_dev: device int32 [block]; conf_dev: device float [block] or NULL;
+ * length_dev: device int32 [1] or NULL, the positions kept (block without
+ * pruning).  All written in stream order.  Same argument checks as fm_draft;
+ * FM_ERR_UNSUPPORTED without a sequential head, or without a confidence head
+ * when conf_dev or a threshold is given.
+ */
+FM_API fm_status fm_draft_pruned(fm_handle *h, int32_t seq, int32_t anchor, int32_t pos,
+                                 const float *thresholds_host, float min_conf, int32_t *tokens_dev,
+                                 float *conf_dev, int32_t *length_dev, void *stream);
+
+/*
  * fm_accept -- greedy acceptance ([FM] specGenerate verify step; [MTP] the
  * same rule): n_accepted = the longest prefix i < k with draft[i] == target[i];
  * bonus = target[n_accepted].  draft_host has k entries, target_host k + 1.
