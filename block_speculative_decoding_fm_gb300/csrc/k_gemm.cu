@@ -173,6 +173,15 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
   }
 }
 
+// tile -> (row block, column block) in the grouped order of TcGemmArgs::group_m
+__device__ __forceinline__ void tile_coords(int tile, int n_mb, int n_nb, int gm_full, int &mb, int &nb) {
+  const int per_group = gm_full * n_nb;
+  const int g = tile / per_group, local = tile - g * per_group;
+  const int gm = min(gm_full, n_mb - g * gm_full);
+  mb = g * gm_full + local % gm;
+  nb = local / gm;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
@@ -210,7 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
   pdl_wait();
 
   const int n_nb = a.N / BN;
-  const int n_tiles = ((a.M + BM - 1) / BM) * n_nb;
+  const int n_mb = (a.M + BM - 1) / BM;
+  const int n_tiles = n_mb * n_nb;
+  const int gm = a.group_m > 0 ? a.group_m : 1;
   const int nk = a.K / BK;
 
   if (warp == 0) {
@@ -218,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int mb = tile / n_nb, nb = tile - mb * n_nb;
+        int mb, nb;
+        tile_coords(tile, n_mb, n_nb, gm, mb, nb);
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % ST;
           if (!mbar_wait(empty(s), ((it / ST) & 1) ^ 1, a.err)) { ok = false; break; }
@@ -261,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
       const int b = tc & 1;
       if (!mbar_wait(tfull(b), (tc >> 1) & 1, a.err)) break;
       tc_fence_after();
-      const int mb = tile / n_nb, nb = tile - mb * n_nb;
+      int mb, nb;
+      tile_coords(tile, n_mb, n_nb, gm, mb, nb);
       const uint32_t taddr = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
       if (a.epi == TC_EPI_FC)
         epilogue_fc(a, taddr, mb * BM + rl, nb * BN, nb);

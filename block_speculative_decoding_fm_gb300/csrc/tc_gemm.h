@@ -18,6 +18,10 @@ struct TcGemmArgs {
   CUtensorMap tma_b;  // B [N][K] f16, box 64 x 256
   int32_t M, N, K;
   int32_t epi;
+  // tile order: groups of group_m consecutive 128-row blocks; inside a group
+  // the row block runs fastest, so the CTAs in flight share B tiles while the
+  // group's A panel stays in L2 (1: the column block runs fastest)
+  int32_t group_m;
   int32_t *err;       // set to 1 when a bounded wait gives up
   // FC
   const __nv_bfloat16 *colw;
