@@ -39,11 +39,13 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="flashmap4b", choices=["flashmap4b", "prefill", "dflash", "tiny", "batched"])
+    p.add_argument("--workload", default="flashmap4b", choices=["flashmap4b", "prefill", "dflash", "dflash_seq", "tiny", "batched"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill rows/s figure")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     p.add_argument("--no-kprof", action="store_true", help="skip the per-kernel timing pass")
+    p.add_argument("--prefill-rows", type=int, default=32768, help="rows of the prefill workload (a smaller case "
+                   "for profiling captures)")
     return p.parse_args()
 
 
@@ -59,25 +61,34 @@ def peaks():
 
 
 # kernel tag (as fm_profile_read names it) -> the source file that defines it
-KERNEL_SOURCES = {"lm_head": "k_lmhead.cu", "attn": "k_attn.cu", "gemv": "k_gemv.cu"}
+KERNEL_SOURCES = {"lm_head": ("k_lmhead.cu",), "attn": ("k_attn.cu",), "gemv": ("k_gemv.cu", "linear_parts.cuh"),
+                  "seq": ("k_seqhead.cu",), "draft_step": ("k_step.cu", "linear_parts.cuh"),
+                  "prefill": ("k_gemm.cu", "tc_gemm.h")}
+
+
+def source_digest(tag):
+    """Digest of the sources the kernel behind `tag` is built from: its own
+    files and the two headers every kernel includes."""
+    import hashlib
+    src = KERNEL_SOURCES.get(tag.split(".")[0])
+    if src is None:
+        return None
+    h = hashlib.sha256()
+    for name in (*src, "dev_common.cuh", "fm_internal.h"):
+        with open(os.path.join(ROOT, "block_speculative_decoding_fm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(tag):
     """DRAM bytes (read + write) per launch of the kernel behind `tag`, from the
     committed ncu summary profiles/ncu_dram_traffic.txt, or None when there is
-    no capture or the kernel's source has changed since it was taken (each
-    line records the digest of the kernel's source file and the two headers
-    it includes, as built for the capture)."""
-    import hashlib
-    src = KERNEL_SOURCES.get(tag.split(".")[0])
+    no capture or the kernel's sources have changed since it was taken (each
+    line records source_digest() of the build the capture ran)."""
+    digest = source_digest(tag)
     path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
-    if src is None or not os.path.exists(path):
+    if digest is None or not os.path.exists(path):
         return None
-    h = hashlib.sha256()
-    for name in (src, "dev_common.cuh", "fm_internal.h"):   # the kernel and the headers it is built from
-        with open(os.path.join(ROOT, "block_speculative_decoding_fm_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    digest = h.hexdigest()[:16]
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -264,16 +275,23 @@ class TinyStep:
 
 class DFlashCycles:
     """Config 4: the DFlash drafter, 4096 context rows, then draft -> accept -> append acc + 1 rows at the
-    anchor position, with seeded acceptance counts in [0, 5]; one timed unit = one cycle."""
+    anchor position, with seeded acceptance counts in [0, 5]; one timed unit = one cycle.  seq_head: the
+    drafter also carries the Markov sequential head (rank 256) and the confidence head, and drafts through
+    fm_draft_pruned with a uniform min_conf."""
     name = "dflash_cycle"
 
-    def __init__(self, torch, cycles):
+    def __init__(self, torch, cycles, seq_head=False):
         import block_speculative_decoding_fm_gb300 as fm
         import fm_synth as S
         self.fm, self.torch = fm, torch
         self.cfg = S.dflash_config(max_ctx=4096 + 6 * cycles + 64)
         c = self.cfg
         w = S.gen_weights(self.cfg, 1004)
+        self.seq_head = seq_head
+        if seq_head:
+            w.update(S.gen_seq_head_weights(self.cfg, 1004, "markov", rank=256))
+            self.conf = torch.zeros((c.block,), dtype=torch.float32, device="cuda")
+            self.length = torch.zeros((1,), dtype=torch.int32, device="cuda")
         self.h = fm.fm_create(self.cfg, fm.weight_items(w), S.gen_modulation(self.cfg, 1004))
         g = torch.Generator(device="cuda")
         g.manual_seed(1004)
@@ -287,8 +305,12 @@ class DFlashCycles:
         self.tokens = torch.zeros((1, c.block), dtype=torch.int32, device="cuda")
         self.pos, self.i, self.used, self.launches = 4096, 0, 0, 0
         table = c.vocab * c.target_dim * 2
-        others = sum(t.data.nbytes for n, t in w.items()) - table
+        seq = ("markov.", "rnn.", "conf.")
+        others = sum(t.data.nbytes for n, t in w.items() if not n.startswith(seq)) - table
         self.bytes_fixed = table + others
+        if seq_head:
+            # per position: markov.w2 streamed once, the base logits row read; the lm_head stores the rows
+            self.bytes_fixed += c.block * (256 * c.vocab * 2 + c.vocab * 4) + c.block * c.vocab * 4
 
     def bytes_at(self, pos):
         c = self.cfg
@@ -296,7 +318,11 @@ class DFlashCycles:
 
     def step(self):
         fm = self.fm
-        fm.fm_draft(self.h, [0], [int(self.anchors[self.i])], [self.pos], self.tokens)
+        if self.seq_head:
+            fm.fm_draft_pruned(self.h, 0, int(self.anchors[self.i]), self.pos, self.tokens[0], self.conf,
+                               self.length, min_conf=0.5)
+        else:
+            fm.fm_draft(self.h, [0], [int(self.anchors[self.i])], [self.pos], self.tokens)
         self.launches += fm.fm_last_launch_count(self.h)
         n = int(self.acc[self.i]) + 1
         fm.fm_context_append(self.h, 0, self.pool[self.used:self.used + n], n, self.pos)
@@ -401,8 +427,9 @@ def run_workload(args):
             ms = time_steps(torch, w.step, args.steps)
             value, launches = args.steps / (ms / 1000), w.launches
             cfgd = {"workload": "tiny: D 256, 2 layers, 64 context rows, draft at 64 + device acceptance"}
-        elif args.workload == "dflash":
-            w = DFlashCycles(torch, args.steps + args.warmup + 3 + 8)
+        elif args.workload in ("dflash", "dflash_seq"):
+            # cycles for the warm-up, the timed steps and the per-kernel pass below
+            w = DFlashCycles(torch, args.steps + max(3, args.warmup) + 20 + 8, seq_head=args.workload == "dflash_seq")
             for _ in range(max(3, args.warmup)):
                 w.step()
             w.launches = 0
@@ -414,6 +441,8 @@ def run_workload(args):
             extra["bytes_per_cycle"] = (w.bytes_at(p0) + w.bytes_at(w.pos)) / 2
             cfgd = {"workload": f"dflash: D 1024, 5 layers, gamma 5, bf16 vocab 262144, context {p0}..{w.pos} "
                                 "(draft -> append acc+1 rows, acc seeded in [0,5])"}
+            if w.seq_head:
+                cfgd["workload"] += "; Markov sequential head rank 256 + confidence pruning at min_conf 0.5"
         elif args.workload == "batched":
             w = BatchedStep(torch)
             for _ in range(max(3, args.warmup)):
@@ -427,7 +456,7 @@ def run_workload(args):
             cfgd = {"workload": "batched: 32 FlashMap-4B sequences, contexts U[512,8192], append acc_i+1 rows "
                                 "(acc_i in 0..16) + 32 x 16-slot draft", "global_batch": 512}
         else:   # prefill
-            w = PrefillStep(torch)
+            w = PrefillStep(torch, rows=args.prefill_rows)
             w.step()
             torch.cuda.synchronize()
             w.launches = 0
@@ -441,10 +470,11 @@ def run_workload(args):
             tok = torch.zeros((1, 16), dtype=torch.int32, device="cuda")
             fm.fm_draft(w.h, [0], [123], [w.rows], tok)
             dms = time_steps(torch, lambda: fm.fm_draft(w.h, [0], [123], [w.rows], tok), 10) / 10
+            torch.cuda.synchronize()
             extra["draft_after_prefill_ms"] = dms
             ms = ms * args.steps / n   # reported per the requested steps below
-            cfgd = {"workload": "prefill: fm_context_append of 32768 rows x 12800 (FlashMap-4B), then a draft at "
-                                "L=32769"}
+            cfgd = {"workload": f"prefill: fm_context_append of {w.rows} rows x 12800 (FlashMap-4B), then a draft at "
+                                f"L={w.rows + 1}"}
     # per-kernel device times (a separate pass) and the roofline of the dominant kernel
     if args.workload == "prefill":
         prof = kernel_profile(fm, w.h, w.step, 3)
@@ -472,9 +502,13 @@ def run_workload(args):
             k, dt = oracle_sample(lambda: o.context_append(st, rows, 0), 15.0, 10)
             cpu = {"value": 256 * k / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
                    "sample": f"{k} appends of 256 of the 32768 rows in {dt:.1f} s", "blas_threads": blas_threads()}
-        elif args.workload == "dflash":
+        elif args.workload in ("dflash", "dflash_seq"):
             c = S.dflash_config(max_ctx=4096 + 64)
-            o = DFlash(c, {n_: t.data for n_, t in S.gen_weights(c, 1004).items()})
+            wd = S.gen_weights(c, 1004)
+            if args.workload == "dflash_seq":
+                wd.update(S.gen_seq_head_weights(c, 1004, "markov", rank=256))
+            o = DFlash(c, {n_: t.data for n_, t in wd.items()})
+            del wd
             st = o.new_state()
             fr = S.streams(1004)["features"]
             o.context_append(st, S.gen_features(fr, 4096, c.feat_dim), 0)
@@ -482,7 +516,9 @@ def run_workload(args):
 
             def cycle():   # draft at the context length, then append one row at the anchor position
                 pos = st.length
-                o.draft(st, 7, pos)
+                res = o.draft(st, 7, pos)
+                if args.workload == "dflash_seq":
+                    o.sequential_head(res, 7, min_conf=0.5)
                 o.context_append(st, row, pos)
             k, dt = oracle_sample(cycle, 15.0, 10)
             cpu = {"value": k / dt, "unit": "cycles/s", "cores": cores, "kind": "oracle",
