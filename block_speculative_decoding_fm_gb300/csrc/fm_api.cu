@@ -80,6 +80,9 @@ struct fm_handle {
   float2 *part_ml = nullptr, *lm_part = nullptr;
   int max_splits = 1;
   int32_t *tickets = nullptr;  // [0, H): self, [H, 2H): cross, [2H]: lm head
+  float *xo = nullptr;         // cross-attention range partials of the current lane
+  float2 *xml = nullptr;
+  int32_t *xtickets = nullptr;
   int32_t *tok_tmp = nullptr;
 
   // ---- DFlash sequential logit head and confidence head (optional tensors) ----
@@ -126,6 +129,10 @@ struct fm_handle {
     float *seq_base = nullptr, *seq_state = nullptr;
     float2 *seq_part = nullptr;
     int32_t *seq_flags = nullptr;
+    // tensor-core cross-attention: per-range partials and per-head tickets
+    float *xo = nullptr;
+    float2 *xml = nullptr;
+    int32_t *xtickets = nullptr;
     cudaStream_t stream = nullptr;
     cudaEvent_t done = nullptr;
     // a short append whose K/V projection waits for this sequence's next draft
@@ -174,6 +181,7 @@ void use_lane(fm_handle *h, int seq) {
   h->ctx = L.ctx; h->actx = L.actx; h->ylm = L.ylm;
   h->st_x = L.st_x; h->st_c = L.st_c; h->st_a = L.st_a; h->st_u = L.st_u; h->lm_part = L.lm_part;
   h->tickets = L.tickets;
+  h->xo = L.xo; h->xml = L.xml; h->xtickets = L.xtickets;
 }
 
 fm_status fail(fm_handle *h, fm_status s, const char *fmt, ...) {
@@ -383,17 +391,52 @@ fm_status run_gemv(fm_handle *h, const GemvArgs &a, cudaStream_t s, const char *
 }
 
 int attn_splits(const fm_handle *h, int L) {
+  int sp = (L + 127) / 128;
+  if (h->cfg.head_dim == 128) {
+    // tensor-core kernel: up to one 128-key tile per CTA, all CTAs in one wave (one per SM)
+    int cap = h->n_sm / h->cfg.n_heads;
+    if (cap > kMaxXSplits) cap = kMaxXSplits;
+    if (sp > cap) sp = cap;
+    return sp < 1 ? 1 : sp;
+  }
   // one thread-block cluster per head, 128+ keys per CTA, at most 8 CTAs (16-CTA clusters
   // were measured slower: their scheduling and merge cost more than the shorter key loop saves)
-  int sp = (L + 127) / 128;
   if (sp > 8) sp = 8;
-  (void)h;
   return sp < 1 ? 1 : sp;
 }
 
 fm_status run_attn(fm_handle *h, const float *Q, int ldq, const Seg2 &kv, int T, int L_src, int L_add, int L_now,
                    const StepParams *sp, float *out, cudaStream_t s) {
   const fm_config &c = h->cfg;
+  if (c.head_dim == 128) {
+    XAttnArgs x;
+    memset(&x, 0, sizeof x);
+    if (!make_cache_map(&x.tm_k, kv.k, c.n_heads, c.max_ctx) || !make_cache_map(&x.tm_v, kv.v, c.n_heads, c.max_ctx))
+      return fail(h, FM_ERR_CUDA, "cache tensor map encoding failed");
+    x.Q = Q;
+    x.ldq = ldq;
+    x.max_ctx = c.max_ctx;
+    x.n_heads = c.n_heads;
+    x.splits = attn_splits(h, L_now);
+    x.T_const = T;
+    x.L_src = L_src;
+    x.L_add = L_add;
+    x.sp = sp;
+    x.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
+    x.out = out;
+    x.ldo = c.dim;
+    x.part_o = h->xo;
+    x.part_ml = h->xml;
+    x.tickets = h->xtickets;
+    x.err = h->dev_err;
+    // ranges of one tile: a one-stage ring and a cluster merge (at most 16 ranges);
+    // longer ranges: a three-stage ring and the ticket merge
+    const bool short_ranges = x.splits == (L_now + 127) / 128 && x.splits <= 16;
+    ProfScope ps(h, s, "attn.cross", (double)L_now * c.dim * 2 * 2 + 2.0 * T * c.dim * 4);
+    CK(launch_xattn(x, short_ranges ? 1 : 3, short_ranges, s, true));
+    ++h->last_launches;
+    return FM_OK;
+  }
   AttnArgs a;
   memset(&a, 0, sizeof a);
   a.Q = Q;
@@ -1278,6 +1321,12 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
     TRY(dalloc(h, &L.lm_part, (size_t)h->n_sm * kMaxT));
     TRY(dalloc(h, &L.tickets, (size_t)2 * c.n_heads + 8));
     CK(cudaMemsetAsync(L.tickets, 0, ((size_t)2 * c.n_heads + 8) * 4, s));
+    if (c.head_dim == 128) {
+      TRY(dalloc(h, &L.xo, (size_t)c.n_heads * kMaxXSplits * 16 * 128));
+      TRY(dalloc(h, &L.xml, (size_t)c.n_heads * kMaxXSplits * 16));
+      TRY(dalloc(h, &L.xtickets, (size_t)c.n_heads));
+      CK(cudaMemsetAsync(L.xtickets, 0, (size_t)c.n_heads * 4, s));
+    }
     if (c.max_seqs > 1) {
       CK(cudaStreamCreateWithFlags(&L.stream, cudaStreamNonBlocking));
       CK(cudaEventCreateWithFlags(&L.done, cudaEventDisableTiming));

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -167,6 +168,30 @@ struct AttnArgs {
   float *out;              // [T][ldo]
   int32_t ldo;
 };
+
+// --- tensor-core attention over the cache, head dim 128 (k_xattn.cu) --------
+constexpr int kMaxXSplits = 32;   // key ranges per head
+struct XAttnArgs {
+  CUtensorMap tm_k, tm_v;  // the K / V planes as [n_heads * max_ctx][128] f16, 128 x 64 boxes
+  const float *Q;          // [T][ldq] f32 queries (head h at column h * 128)
+  int32_t ldq;
+  int32_t max_ctx, n_heads;
+  int32_t splits;          // key ranges (CTAs) per head, <= kMaxXSplits
+  int32_t T_const;
+  int32_t L_src;           // 0: sp->L, 1: sp->pos + 1
+  int32_t L_add;
+  const StepParams *sp;
+  float scale_log2;        // log2(e) / sqrt(128)
+  float *out;              // [T][ldo]
+  int32_t ldo;
+  float *part_o;           // [n_heads][splits][16][128] unnormalised partial outputs
+  float2 *part_ml;         // [n_heads][splits][16] (reference m, row sum l)
+  int32_t *tickets;        // [n_heads], zero between launches
+  int32_t *err;
+};
+cudaError_t launch_xattn(const XAttnArgs &a, int stages, bool cluster, cudaStream_t st, bool pdl);
+size_t xattn_smem_bytes(int stages);
+bool make_cache_map(CUtensorMap *map, const __half *plane, int n_heads, int max_ctx);
 
 // --- lm_head GEMV fused with the per-row argmax -----------------------------
 // Q8_0 table layout: per (128-row tile, 64-column chunk) one contiguous 8704-byte

@@ -870,7 +870,7 @@ __global__ void __launch_bounds__(kAll, 1) fm_draft_step_kernel(const __grid_con
 
 size_t step_smem_bytes() { return (size_t)kSmemBytes; }
 
-// attrs: bit 0 = cooperative launch (the driver co-schedules every CTA), bit 1 =
+// attrs: bit 0 = cooperative launch (every CTA is guaranteed co-resident), bit 1 =
 // programmatic stream serialisation (the CTAs may start while the previous
 // kernel drains; they call griddepcontrol.wait before reading its results)
 cudaError_t launch_step(const StepArgs &a, int clusters, cudaStream_t st, int attrs) {

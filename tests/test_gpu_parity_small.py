@@ -174,6 +174,29 @@ def test_small_dflash_steps():
     p.close()
 
 
+def test_small_dflash_long_context_sharp_scores():
+    """Attention with head dim 128 over 32,768 context rows, with the query and
+    key projections scaled up so that scores spread over tens of log2 units:
+    each key range holds eight 128-key tiles, and later tiles often beat the
+    first tile's maximum by more than 2^8, which moves the range's softmax
+    reference and rescales its accumulator.  Hidden states, head output and
+    logits against the oracle."""
+    cfg = small_dflash(max_ctx=32768 + 16)
+
+    def sharpen(w):
+        for l in range(cfg.n_layers):
+            for n in ("q", "k"):
+                t = w[f"bb.{l}.{n}"]
+                t.data = S.f32_to_bf16_bits(S.bf16_bits_to_f32(t.data) * 16.0)
+    p = Pair(cfg, 1009, edit=sharpen)
+    fr = S.streams(1009)["features"]
+    for start in range(0, 32768, 4096):
+        p.append(0, S.gen_features(fr, 4096, cfg.feat_dim), start)
+    got, ref = p.draft(0, 21, 32768)
+    check_draft(p, got, ref)
+    p.close()
+
+
 def test_small_dflash_empty_context():
     cfg = small_dflash()
     p = Pair(cfg, 1007)
