@@ -310,3 +310,78 @@ def gen_seq_head_weights(cfg: DrafterConfig, seed: int, variant: str = "markov",
     for n, shape, std in spec:
         out[n] = Tensor(n, shape, DT_BF16, f32_to_bf16_bits(_normal(rng, shape, std)))
     return out
+
+
+# --- the MTP draft head (ternary_bonsai_2_mtp.js, ``MCFG`` / ``MTP_HEAD``) --
+
+@dataclasses.dataclass(frozen=True)
+class MtpConfig:
+    hidden: int = 5120
+    inter: int = 17408
+    n_heads: int = 24
+    n_kv_heads: int = 4
+    head_dim: int = 256
+    rot_dims: int = 64
+    theta: float = 1e7
+    eps: float = 1e-6
+    vocab: int = 248320
+    kv_cap: int = 4096 + 64
+    max_rows: int = 8
+
+    def replace(self, **kw) -> "MtpConfig":
+        return dataclasses.replace(self, **kw)
+
+
+def mtp_config(kv_cap: int = 4096 + 64) -> MtpConfig:
+    """The page's MTP head: H 5120, I 17408, 24 q heads and 4 KV heads of 256,
+    NEOX RoPE on 64 dims with theta 1e7, eps 1e-6, vocab 248320, M <= 8 rows."""
+    return MtpConfig(kv_cap=kv_cap)
+
+
+def mtp_micro_config(kv_cap: int = 96) -> MtpConfig:
+    """A small MTP head of the same structure (the oracle runs it in seconds)."""
+    return MtpConfig(hidden=256, inter=512, n_heads=4, n_kv_heads=2, head_dim=64, rot_dims=32, theta=1e4,
+                     vocab=4096, kv_cap=kv_cap)
+
+
+def mtp_tensor_specs(cfg: MtpConfig) -> List[Tuple[str, Tuple[int, ...], str]]:
+    """(name, [N, K] or [n], kind): "q" a Q8_0 matrix (y = W x, W [N][K]), "n" an
+    f32 norm weight, "e" the bf16 embedding table, "l" the Q8_0 lm_head."""
+    H, I, nh, nkv, hd = cfg.hidden, cfg.inter, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+    return [("eh_proj", (H, 2 * H), "q"), ("attn_q", (nh * 2 * hd, H), "q"), ("attn_k", (nkv * hd, H), "q"),
+            ("attn_v", (nkv * hd, H), "q"), ("attn_output", (H, nh * hd), "q"), ("ffn_gate", (I, H), "q"),
+            ("ffn_up", (I, H), "q"), ("ffn_down", (H, I), "q"),
+            ("enorm", (H,), "n"), ("hnorm", (H,), "n"), ("attn_norm", (H,), "n"), ("attn_q_norm", (hd,), "n"),
+            ("attn_k_norm", (hd,), "n"), ("post_attention_norm", (H,), "n"), ("shared_head_norm", (H,), "n"),
+            ("token_embd", (cfg.vocab, H), "e"), ("lm_head", (cfg.vocab, H), "l")]
+
+
+def gen_mtp_weights(cfg: MtpConfig, seed: int) -> Dict[str, Tensor]:
+    """Matrices N(0, 0.02) quantised to Q8_0, norms f32 1 + N(0, 0.02), the
+    embedding table bf16(N(0, 1)) (embedding rows of unit scale, as a trunk's
+    are), the lm_head N(0, 0.02) quantised to Q8_0.  Large tensors are drawn
+    and quantised in row blocks."""
+    rng = streams(seed)["weights"]
+    out: Dict[str, Tensor] = {}
+    for name, shape, kind in mtp_tensor_specs(cfg):
+        if kind == "n":
+            out[name] = Tensor(name, shape, DT_F32, _normal(rng, shape, 0.02, 1.0))
+        elif kind == "e":
+            bits = np.empty(shape, dtype=np.uint16)
+            for r0 in range(0, shape[0], 16384):
+                r1 = min(shape[0], r0 + 16384)
+                bits[r0:r1] = f32_to_bf16_bits(_normal(rng, (r1 - r0, shape[1]), 1.0))
+            out[name] = Tensor(name, shape, DT_BF16, bits)
+        else:
+            rows, cols = shape
+            raw = np.empty((rows, cols // 32 * 34), dtype=np.uint8)
+            for r0 in range(0, rows, 4096):
+                r1 = min(rows, r0 + 4096)
+                raw[r0:r1] = quantize_q8_0(_normal(rng, (r1 - r0, cols), 0.02))
+            out[name] = Tensor(name, shape, DT_Q8_0, raw)
+    return out
+
+
+def gen_mtp_hidden(rng: np.random.Generator, n: int, hidden: int) -> np.ndarray:
+    """Rows standing in for the trunk's output-normed hidden states: f32 N(0, 1)."""
+    return rng.standard_normal((n, hidden), dtype=np.float32)

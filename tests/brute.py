@@ -371,3 +371,77 @@ def dflash_sequential(weights, base_logits, block_rows, anchor: int, rms_eps: fl
             if k > 0 and thr is not None and conf[-1] < thr:
                 return tokens, conf, k
     return tokens, conf, len(tokens)
+
+
+def mtp_forward(weights, cfg, tokens, hn_rows, pos0: int, kv_lo: int, kcache, vcache):
+    """The MTP head's forward over len(tokens) rows by loops (ternary_bonsai_2_mtp.js,
+    ``MTPHead.forward`` and its WGSL kernels); kcache / vcache are lists of rows
+    (None where unwritten), updated in place.  Returns the shared_head_norm rows."""
+    H, hd, nh, nkv, rot, eps = cfg.hidden, cfg.head_dim, cfg.n_heads, cfg.n_kv_heads, cfg.rot_dims, cfg.eps
+    Wm = {n: [q8_row(r, k) for r in weights[n]] for n, k in (
+        ("eh_proj", 2 * H), ("attn_q", H), ("attn_k", H), ("attn_v", H), ("attn_output", nh * hd),
+        ("ffn_gate", H), ("ffn_up", H), ("ffn_down", cfg.inter))}
+    nw = {n: [float(v) for v in weights[n]] for n in ("enorm", "hnorm", "attn_norm", "attn_q_norm", "attn_k_norm",
+                                                    "post_attention_norm", "shared_head_norm")}
+
+    def rope(y, pos):
+        y = list(y)
+        half_ = rot // 2
+        for i in range(half_):
+            ang = pos * theta_pow(i)
+            c, s = math.cos(ang), math.sin(ang)
+            a0, a1 = y[i], y[i + half_]
+            y[i] = a0 * c - a1 * s
+            y[i + half_] = a1 * c + a0 * s
+        return y
+
+    def theta_pow(i):
+        return cfg.theta ** (-2.0 * i / rot)
+
+    rows = []
+    for m, tok in enumerate(tokens):
+        e = [bf(b) for b in weights["token_embd"][tok]]
+        xc = rmsn(e, nw["enorm"], eps) + rmsn([float(v) for v in hn_rows[m]], nw["hnorm"], eps)
+        x = matvec(Wm["eh_proj"], xc)
+        a = rmsn(x, nw["attn_norm"], eps)
+        qf = matvec(Wm["attn_q"], a)
+        kt = matvec(Wm["attn_k"], a)
+        vt = matvec(Wm["attn_v"], a)
+        pos = pos0 + m
+        krow, vrow = [], []
+        for g in range(nkv):
+            krow += rope(rmsn(kt[g * hd:(g + 1) * hd], nw["attn_k_norm"], eps), pos)
+        kcache[pos] = krow
+        vcache[pos] = list(vt)
+        rows.append((x, qf, pos))
+    outs = []
+    for x, qf, pos in rows:
+        gated = []
+        for h in range(nh):
+            q = rope(rmsn(qf[h * 2 * hd:h * 2 * hd + hd], nw["attn_q_norm"], eps), pos)
+            g = h // (nh // nkv)
+            sc = []
+            for j in range(kv_lo, pos + 1):
+                s = 0.0
+                for d in range(hd):
+                    s += q[d] * kcache[j][g * hd + d]
+                sc.append(s / math.sqrt(hd))
+            mx = max(sc)
+            es = [math.exp(s - mx) for s in sc]
+            tot = sum(es)
+            for d in range(hd):
+                acc = 0.0
+                for jj, j in enumerate(range(kv_lo, pos + 1)):
+                    acc += es[jj] * vcache[j][g * hd + d]
+                gate = qf[h * 2 * hd + hd + d]
+                gated.append(acc / tot / (1.0 + math.exp(-gate)))
+        o = matvec(Wm["attn_output"], gated)
+        x = [x[i] + o[i] for i in range(H)]
+        a = rmsn(x, nw["post_attention_norm"], eps)
+        gt = matvec(Wm["ffn_gate"], a)
+        up = matvec(Wm["ffn_up"], a)
+        f = [gt[i] / (1.0 + math.exp(-gt[i])) * up[i] for i in range(len(gt))]
+        dn = matvec(Wm["ffn_down"], f)
+        x = [x[i] + dn[i] for i in range(H)]
+        outs.append(rmsn(x, nw["shared_head_norm"], eps))
+    return outs
