@@ -390,19 +390,30 @@ fm_status run_gemv(fm_handle *h, const GemvArgs &a, cudaStream_t s, const char *
   return FM_OK;
 }
 
+// Key ranges per head for the cross-attention over L keys, and how they merge.
+// Head dim 128 (tensor-core kernel): up to four 128-key tiles per range, at most
+// 16 ranges merged in a cluster (one-stage ring: two CTAs fit on an SM); longer
+// contexts: one range per SM, three-stage rings, merged by the last range (ticket).
+// Head dim 64: one cluster of at most 8 CTAs per head (16-CTA clusters were
+// measured slower there: their scheduling and merge cost more than the shorter
+// key loop saves).
+struct AttnPlan {
+  int splits;
+  bool cluster;
+};
+AttnPlan attn_plan(const fm_handle *h, int L) {
+  const int nt = (L + 127) / 128;
+  if (h->cfg.head_dim != 128) return {nt < 1 ? 1 : nt > 8 ? 8 : nt, true};
+  if (nt <= 4 * 16) return {nt < 1 ? 1 : nt > 16 ? 16 : nt, true};
+  int cap = h->n_sm / h->cfg.n_heads;
+  if (cap > kMaxXSplits) cap = kMaxXSplits;
+  if (cap < 1) cap = 1;
+  return {nt > cap ? cap : nt, false};
+}
+// the plan as one number (part of a captured chain's key)
 int attn_splits(const fm_handle *h, int L) {
-  int sp = (L + 127) / 128;
-  if (h->cfg.head_dim == 128) {
-    // tensor-core kernel: up to one 128-key tile per CTA, all CTAs in one wave (one per SM)
-    int cap = h->n_sm / h->cfg.n_heads;
-    if (cap > kMaxXSplits) cap = kMaxXSplits;
-    if (sp > cap) sp = cap;
-    return sp < 1 ? 1 : sp;
-  }
-  // one thread-block cluster per head, 128+ keys per CTA, at most 8 CTAs (16-CTA clusters
-  // were measured slower: their scheduling and merge cost more than the shorter key loop saves)
-  if (sp > 8) sp = 8;
-  return sp < 1 ? 1 : sp;
+  const AttnPlan p = attn_plan(h, L);
+  return p.splits + (p.cluster ? 0 : 64);
 }
 
 fm_status run_attn(fm_handle *h, const float *Q, int ldq, const Seg2 &kv, int T, int L_src, int L_add, int L_now,
@@ -417,7 +428,8 @@ fm_status run_attn(fm_handle *h, const float *Q, int ldq, const Seg2 &kv, int T,
     x.ldq = ldq;
     x.max_ctx = c.max_ctx;
     x.n_heads = c.n_heads;
-    x.splits = attn_splits(h, L_now);
+    const AttnPlan plan = attn_plan(h, L_now);
+    x.splits = plan.splits;
     x.T_const = T;
     x.L_src = L_src;
     x.L_add = L_add;
@@ -429,11 +441,8 @@ fm_status run_attn(fm_handle *h, const float *Q, int ldq, const Seg2 &kv, int T,
     x.part_ml = h->xml;
     x.tickets = h->xtickets;
     x.err = h->dev_err;
-    // ranges of one tile: a one-stage ring and a cluster merge (at most 16 ranges);
-    // longer ranges: a three-stage ring and the ticket merge
-    const bool short_ranges = x.splits == (L_now + 127) / 128 && x.splits <= 16;
     ProfScope ps(h, s, "attn.cross", (double)L_now * c.dim * 2 * 2 + 2.0 * T * c.dim * 4);
-    CK(launch_xattn(x, short_ranges ? 1 : 3, short_ranges, s, true));
+    CK(launch_xattn(x, plan.cluster ? 1 : 3, plan.cluster, s, true));
     ++h->last_launches;
     return FM_OK;
   }
@@ -446,7 +455,7 @@ fm_status run_attn(fm_handle *h, const float *Q, int ldq, const Seg2 &kv, int T,
   a.max_ctx = c.max_ctx;
   a.n_heads = c.n_heads;
   a.hd = c.head_dim;
-  a.splits = attn_splits(h, L_now);
+  a.splits = attn_plan(h, L_now).splits;
   a.T_const = T;
   a.L_src = L_src;
   a.L_add = L_add;
