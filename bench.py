@@ -39,7 +39,7 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="flashmap4b", choices=["flashmap4b", "prefill", "dflash", "dflash_seq", "tiny", "batched"])
+    p.add_argument("--workload", default="flashmap4b", choices=["flashmap4b", "prefill", "dflash", "dflash_seq", "tiny", "batched", "mtp"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill rows/s figure")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
@@ -332,6 +332,45 @@ class DFlashCycles:
         self.i += 1
 
 
+class MtpCycle:
+    """The MTP draft head at the page's MCFG shape (Q8_0 layer, vocab 248,320): a draft of depth 3 from two
+    pending rows (a 2-row pass, then two chained single-row passes on the device's own drafts) over a
+    1,024-row head cache; one timed unit = one draft.  The pending rows re-write the same cache rows every
+    step."""
+    name = "mtp_draft"
+
+    def __init__(self, torch, depth=3, history=1024):
+        import block_speculative_decoding_fm_gb300 as fm
+        import fm_synth as S
+        self.fm, self.torch, self.depth = fm, torch, depth
+        self.cfg = c = S.mtp_config(kv_cap=history + 64)
+        self.w = S.gen_mtp_weights(c, 1206)
+        self.h = fm.fm_mtp_create(c, fm.weight_items(self.w))
+        g = torch.Generator(device="cuda")
+        g.manual_seed(1206)
+        for p0 in range(0, history, 8):
+            toks = torch.randint(0, c.vocab, (8,), generator=g, device="cuda", dtype=torch.int32)
+            fm.fm_mtp_forward(self.h, toks, torch.randn((8, c.hidden), generator=g, device="cuda"), p0, 0)
+        self.pos = history
+        self.toks = torch.randint(0, c.vocab, (2,), generator=g, device="cuda", dtype=torch.int32)
+        self.hn = torch.randn((2, c.hidden), generator=g, device="cuda")
+        self.drafts = torch.zeros((depth,), dtype=torch.int32, device="cuda")
+        self.launches = 0
+        q8 = lambda n, k: n * k // 32 * 34
+        H, I, nh, nkv, hd = c.hidden, c.inter, c.n_heads, c.n_kv_heads, c.head_dim
+        layer = (q8(H, 2 * H) + q8(nh * 2 * hd + 2 * nkv * hd, H) + q8(H, nh * hd) + q8(2 * I, H) + q8(H, I)
+                 + 7 * H * 4 + 2 * hd * 4)
+        lm = q8(c.vocab, H)
+        cache = (history + 2) * 2 * nkv * hd * 4
+        # per pass: the layer's weights, the lm_head table and the head cache rows it attends over (read once)
+        self.bytes_per_step = depth * (layer + lm + cache)
+
+    def step(self):
+        fm = self.fm
+        fm.fm_mtp_draft(self.h, self.toks, self.hn, self.pos, 0, self.depth, self.drafts)
+        self.launches += fm.fm_mtp_last_launch_count(self.h)
+
+
 class BatchedStep:
     """Config 5: 32 sequences, contexts U[512, 8192] (prefilled untimed), each appends acc_i + 1 rows
     (acc_i ~ U{0..16}) then all 32 draft 16 slots; every step re-appends at the same positions."""
@@ -443,6 +482,18 @@ def run_workload(args):
                                 "(draft -> append acc+1 rows, acc seeded in [0,5])"}
             if w.seq_head:
                 cfgd["workload"] += "; Markov sequential head rank 256 + confidence pruning at min_conf 0.5"
+        elif args.workload == "mtp":
+            w = MtpCycle(torch)
+            for _ in range(max(3, args.warmup)):
+                w.step()
+            w.launches = 0
+            ms = time_steps(torch, w.step, args.steps)
+            value, unit, launches = args.steps / (ms / 1000), "drafts/s", w.launches
+            extra["achieved_hbm_gbs"] = w.bytes_per_step * value / 1e9
+            extra["bytes_per_step"] = w.bytes_per_step
+            extra["tokens_drafted_per_s"] = value * w.depth
+            cfgd = {"workload": "mtp: MTP head H 5120, I 17408, 24/4 heads x 256, Q8_0, vocab 248320; depth-3 draft "
+                                "from 2 pending rows over a 1024-row head cache"}
         elif args.workload == "batched":
             w = BatchedStep(torch)
             for _ in range(max(3, args.warmup)):
@@ -488,6 +539,13 @@ def run_workload(args):
                     "flops_per_launch": flops / max(1, sum(v[0] for _, v in gemm)),
                     "ms_per_launch": gms / max(1, sum(v[0] for _, v in gemm))}
         kernels = {k: {"launches": v[0] / 3, "ms_per_step": v[1] / 3} for k, v in sorted(prof.items())}
+    elif args.workload == "mtp":
+        # the head's launches are not profiled one by one: the roofline of the whole draft
+        achieved = extra["achieved_hbm_gbs"]
+        roofline = {"bound": "hbm", "kernel": "mtp_draft (every launch of the draft)", "achieved": achieved,
+                    "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                    "peak_source": f"{peak_src} burst copy", "bytes_per_launch": w.bytes_per_step,
+                    "ms_per_launch": ms / args.steps}
     elif args.workload != "tiny":
         steps = 5 if args.workload == "batched" else 20
         roofline, kernels = hbm_roofline(kernel_profile(fm, w.h, w.step, steps), hbm, peak_src, steps)
@@ -524,6 +582,18 @@ def run_workload(args):
             cpu = {"value": k / dt, "unit": "cycles/s", "cores": cores, "kind": "oracle",
                    "sample": f"{k} draft + 1-row append cycles at context 4096 in {dt:.1f} s",
                    "blas_threads": blas_threads()}
+        elif args.workload == "mtp":
+            from oracle.mtp import MtpHead
+            c = w.cfg
+            o = MtpHead(c, {n_: t.data for n_, t in w.w.items()})
+            st = o.new_state()
+            rng = S.streams(1206)["features"]
+            o.forward(st, o.embed(list(range(8))), S.gen_mtp_hidden(rng, 8, c.hidden).astype(np.float64), 0, 0)
+            hn = S.gen_mtp_hidden(rng, 2, c.hidden).astype(np.float64)
+            k, dt = oracle_sample(lambda: o.draft(st, [5, 6], hn, 8, 0, 3), 20.0, 3)
+            cpu = {"value": k / dt, "unit": "drafts/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{k} depth-3 drafts over an 8-row head cache in {dt:.1f} s (fp64, lm_head dequantised "
+                             "by row blocks)", "blas_threads": blas_threads()}
         elif args.workload == "batched":
             c = S.flashmap_4b_config(max_ctx=4096 + 64)
             o = FlashMap(c, {n_: t.data for n_, t in S.gen_weights(c, 1005).items()}, S.gen_modulation(c, 1005), True)

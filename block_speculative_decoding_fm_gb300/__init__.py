@@ -33,7 +33,9 @@ EXPORTS = ["fm_create", "fm_time_conditioning", "fm_context_append", "fm_context
            "fm_draft_pruned", "fm_accept",
            "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_synchronize", "fm_selftest_wait_timeout", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
            "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy",
-           "fm_policy_init", "fm_policy_next", "fm_policy_after_round", "fm_policy_after_plain"]
+           "fm_policy_init", "fm_policy_next", "fm_policy_after_round", "fm_policy_after_plain",
+           "fm_mtp_create", "fm_mtp_forward", "fm_mtp_draft", "fm_mtp_cache", "fm_mtp_last_launch_count",
+           "fm_mtp_last_error", "fm_mtp_destroy"]
 
 
 class FmConfig(ctypes.Structure):
@@ -63,6 +65,13 @@ class FmVerifyPolicy(ctypes.Structure):
 
 
 FM_ACT_ROUND, FM_ACT_PLAIN, FM_ACT_PLAIN_LIMIT = 0, 1, 2
+
+
+class FmMtpConfig(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("rot_dims", ctypes.c_int32),
+                ("theta", ctypes.c_float), ("eps", ctypes.c_float), ("vocab", ctypes.c_int32),
+                ("kv_cap", ctypes.c_int32), ("max_rows", ctypes.c_int32)]
 
 
 class FmError(RuntimeError):
@@ -109,6 +118,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fm_policy_next": (I32, [ctypes.POINTER(FmVerifyPolicy), I32, I32, ctypes.POINTER(I32), ctypes.POINTER(I32)]),
         "fm_policy_after_round": (I32, [ctypes.POINTER(FmVerifyPolicy), I32, ctypes.c_double]),
         "fm_policy_after_plain": (I32, [ctypes.POINTER(FmVerifyPolicy), ctypes.c_double, I32]),
+        "fm_mtp_create": (I32, [ctypes.POINTER(FmMtpConfig), ctypes.POINTER(FmTensor), I32, P, ctypes.POINTER(P)]),
+        "fm_mtp_forward": (I32, [P, I32, P, P, I32, I32, P, P, P]),
+        "fm_mtp_draft": (I32, [P, I32, P, P, I32, I32, I32, P, P]),
+        "fm_mtp_cache": (I32, [P, I32, I32, P, P]),
+        "fm_mtp_last_launch_count": (I32, [P, ctypes.POINTER(I32)]),
+        "fm_mtp_last_error": (ctypes.c_char_p, [P]),
+        "fm_mtp_destroy": (None, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -335,6 +351,55 @@ def fm_destroy(h) -> None:
 def weight_items(tensors: Dict[str, object]):
     """(name, array, dtype) triples from name -> object with .data / .dtype."""
     return [(n, t.data, t.dtype) for n, t in tensors.items()]
+
+
+def _mtp_check(status: int, m=None):
+    if status != FM_OK:
+        lib = load_library()
+        raise FmError(status, f"{lib.fm_status_str(status).decode()}: {lib.fm_mtp_last_error(m).decode()}")
+
+
+def fm_mtp_create(cfg, weights: Iterable[Tuple[str, object, int]], stream=None) -> ctypes.c_void_p:
+    """The MTP draft head.  cfg: any object with the fm_mtp_config fields;
+    weights: (name, array, FM_DTYPE_*) triples (host arrays or CUDA tensors)."""
+    lib = load_library()
+    arr, n_items, keep = _tensor_array(weights)
+    c = FmMtpConfig(cfg.hidden, cfg.inter, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.rot_dims, cfg.theta, cfg.eps,
+                    cfg.vocab, cfg.kv_cap, cfg.max_rows)
+    m = ctypes.c_void_p()
+    _mtp_check(lib.fm_mtp_create(ctypes.byref(c), arr, n_items, _stream(stream), ctypes.byref(m)))
+    return m
+
+
+def fm_mtp_forward(m, tokens, hn, pos0: int, kv_lo: int, hout=None, drafts=None, stream=None) -> None:
+    """One pass over len(tokens) rows.  tokens: CUDA int32 [M]; hn: CUDA float32
+    [M, H]; hout: CUDA float32 [M, H] or None; drafts: CUDA int32 [M] or None."""
+    _mtp_check(load_library().fm_mtp_forward(m, int(tokens.shape[0]), _ptr(tokens), _ptr(hn), pos0, kv_lo, _ptr(hout),
+                                             _ptr(drafts), _stream(stream)), m)
+
+
+def fm_mtp_draft(m, tokens, hn, pos0: int, kv_lo: int, depth: int, drafts, stream=None) -> None:
+    """A pass over the pending rows then depth - 1 chained single-row passes;
+    drafts: CUDA int32 [depth]."""
+    _mtp_check(load_library().fm_mtp_draft(m, int(tokens.shape[0]), _ptr(tokens), _ptr(hn), pos0, kv_lo, depth,
+                                           _ptr(drafts), _stream(stream)), m)
+
+
+def fm_mtp_cache(m, which: int, rows: int, out: np.ndarray, stream=None) -> np.ndarray:
+    """Copy K (0) or V (1) cache rows [0, rows) into a host float32 array."""
+    _mtp_check(load_library().fm_mtp_cache(m, which, rows, _ptr(out), _stream(stream)), m)
+    return out
+
+
+def fm_mtp_last_launch_count(m) -> int:
+    n = ctypes.c_int32()
+    _mtp_check(load_library().fm_mtp_last_launch_count(m, ctypes.byref(n)), m)
+    return n.value
+
+
+def fm_mtp_destroy(m) -> None:
+    if m is not None:
+        load_library().fm_mtp_destroy(m)
 
 
 def fm_policy_init(block: int, verify: int = 0, fallback: bool = True, probe_every: int = 16) -> FmVerifyPolicy:

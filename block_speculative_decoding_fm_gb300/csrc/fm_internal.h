@@ -215,7 +215,12 @@ struct LmArgs {
   float2 *part;              // [gridDim.x][kMaxT] (value, index-as-float bits)
   int32_t *ticket;           // [1]
   int32_t *tokens;           // [T]; null: sp->tokens
-  float *logits;             // optional [T][V] store (debug), null in the hot path
+  float *logits;             // optional [T][V] store (debug, or the output of a Q8_0 linear layer)
+  // Q8_0 with a pre-split Y only: a linear layer split along K into slices of H columns,
+  // the table's tiles in slice order (y_slice_tiles tiles each) and Y holding every
+  // slice's chunks in turn; the row v of tile t is slice t / y_slice_tiles's partial
+  // sum (0: no split)
+  int32_t y_slice_tiles;
 };
 
 // --- the persistent draft step (k_step.cu) -----------------------------------

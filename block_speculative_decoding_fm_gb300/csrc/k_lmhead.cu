@@ -387,22 +387,28 @@ __global__ void __launch_bounds__(kQ8Threads, 1) fm_lmhead_q8_kernel(const __gri
 
   if (warp == 0) {
     if (lane == 0) {
+      // split K (y_slice_tiles > 0): the rows of tile t hold K slice t / y_slice_tiles,
+      // whose Y chunks follow the earlier slices' in the operand
+      auto ychunk = [&](int tile, int c) {
+        const int sl = a.y_slice_tiles > 0 ? tile / a.y_slice_tiles : 0;
+        return a.ylm + ((size_t)sl * kcs + c) * kYChunk;
+      };
       if (kStreamY) {
         // the Y chunks of the first stages (Y is this call's data: after griddepcontrol.wait)
-        int kc = 0;
+        int kc = 0, tile = blockIdx.x;
         for (int j = 0; j < S && j < units; ++j) {
-          bulk_g2s(ring + j * SS, a.ylm + (size_t)kc * kYChunk, U * kYChunk, full(j));
+          bulk_g2s(ring + j * SS, ychunk(tile, kc), U * kYChunk, full(j));
           kc += U;
-          if (kc == kcs) kc = 0;
+          if (kc == kcs) { kc = 0; tile += gridDim.x; }
         }
         mbar_arrive(yfull);
       }
       // unit j reuses stage j % S once unit j - S is released
       const uint8_t *src = first;
-      int kc = 0;
+      int kc = 0, tile = blockIdx.x;
       for (int j = 0; j < S && j < units; ++j) {
         kc += U;
-        if (kc == kcs) { kc = 0; src += tile_stride; }
+        if (kc == kcs) { kc = 0; src += tile_stride; tile += gridDim.x; }
       }
       int st = 0;
       uint32_t par = 0;
@@ -410,9 +416,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1) fm_lmhead_q8_kernel(const __gri
         if (!mbar_wait_bounded(empty(st), par, a.err)) break;
         mbar_expect_tx(full(st), U * SB + (kStreamY ? U * kYChunk : 0));
         bulk_g2s(ring + st * SS + TOFF, src + (size_t)kc * SB, U * SB, full(st));
-        if (kStreamY) bulk_g2s(ring + st * SS, a.ylm + (size_t)kc * kYChunk, U * kYChunk, full(st));
+        if (kStreamY) bulk_g2s(ring + st * SS, ychunk(tile, kc), U * kYChunk, full(st));
         kc += U;
-        if (kc == kcs) { kc = 0; src += tile_stride; }
+        if (kc == kcs) { kc = 0; src += tile_stride; tile += gridDim.x; }
         if (++st == S) { st = 0; par ^= 1; }
       }
     }

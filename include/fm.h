@@ -399,6 +399,93 @@ FM_API const char *fm_last_error(const fm_handle *h);   /* never NULL; "" when n
 /* Free everything the handle owns.  NULL is ignored. */
 FM_API void fm_destroy(fm_handle *h);
 
+/* ------------------------------------------------------------------------
+ * The MTP draft head ([MTP] ternary_bonsai_2_mtp.js: the header's graph,
+ * MCFG, MTPHead.forward and its kernels, MTPRunner's draft loop): one
+ * Qwen-style decoder layer with Q8_0 weights, chained in depth.  A second
+ * drafter, with its own handle.
+ *
+ * One pass over M <= max_rows rows (tokens x at positions pos0 .. pos0+M-1,
+ * each with h, the normed hidden of its previous position):
+ *   Xc = [rms(E[x]; enorm) | rms(h; hnorm)];  X = eh_proj Xc
+ *   A = rms(X; attn_norm);  [q | gate] per q head = attn_q A;  k, v = attn_k A, attn_v A
+ *   per head RMSNorm over head_dim (attn_q_norm / attn_k_norm), NEOX RoPE on the
+ *   first rot_dims (pairs i, i + rot_dims/2, angle pos * theta^(-2i/rot_dims));
+ *   k, v rows stored in the head's own f32 cache at their positions
+ *   O = softmax(q k^T / sqrt(head_dim)) v over cache rows kv_lo .. pos (KV head
+ *   h / (n_heads / n_kv_heads)), times sigmoid(gate)
+ *   X += attn_output O;  X += ffn_down(silu(ffn_gate A') * ffn_up A'), A' = rms(X; post_attention_norm)
+ *   h' = rms(X; shared_head_norm);  draft = argmax(lm_head h'), ties to the lower index
+ * ------------------------------------------------------------------------ */
+typedef struct fm_mtp_config {
+  int32_t hidden;      /* H (MCFG.H 5120); a multiple of 128 */
+  int32_t inter;       /* I (17408); a multiple of 128 */
+  int32_t n_heads;     /* q heads (24) */
+  int32_t n_kv_heads;  /* KV heads (4); divides n_heads */
+  int32_t head_dim;    /* 256; a multiple of 32, <= 256 */
+  int32_t rot_dims;    /* NEOX-rotated dims per head (64); even, <= head_dim */
+  float theta;         /* RoPE base (1e7) */
+  float eps;           /* RMSNorm eps (1e-6) */
+  int32_t vocab;       /* lm_head rows (248320) */
+  int32_t kv_cap;      /* cache rows (positions) the head keeps */
+  int32_t max_rows;    /* M per pass, <= 8 (MCFG.MAXM) */
+} fm_mtp_config;
+
+typedef struct fm_mtp fm_mtp;
+
+/*
+ * fm_mtp_create -- load the head.  weights (host or device, copied):
+ *   Q8_0 (GGUF rows [N][K/32 * 34]): eh_proj [H][2H], attn_q [n_heads*2*head_dim][H]
+ *     (per head the query rows, then its gate rows), attn_k / attn_v
+ *     [n_kv_heads*head_dim][H], attn_output [H][n_heads*head_dim], ffn_gate /
+ *     ffn_up [I][H], ffn_down [H][I], lm_head [vocab][H];
+ *   FM_DTYPE_F32: enorm, hnorm, attn_norm, post_attention_norm, shared_head_norm [H],
+ *     attn_q_norm, attn_k_norm [head_dim];
+ *   FM_DTYPE_BF16: token_embd [vocab][H] (the rows the drafted tokens are embedded with).
+ * Every 2-D product's N must be a multiple of 128 and its K of 64.
+ * Errors: FM_ERR_INVALID_ARG (null, missing / mis-sized tensor, wrong dtype),
+ *   FM_ERR_UNSUPPORTED (dims outside the limits above), FM_ERR_OOM, FM_ERR_CUDA.
+ *   *out is NULL on failure; the reason is in fm_mtp_last_error(NULL).
+ */
+FM_API fm_status fm_mtp_create(const fm_mtp_config *cfg, const fm_tensor *weights, int32_t n_weights, void *stream,
+                               fm_mtp **out);
+
+/*
+ * fm_mtp_forward -- MTPHead.forward: one pass over n_rows rows.  tokens_dev:
+ * device int32 [n_rows]; hn_dev: device f32 [n_rows][H] (the normed hidden of
+ * each row's previous position); writes cache rows pos0 .. pos0+n_rows-1 and,
+ * when hout_dev is not NULL, h' (device f32 [n_rows][H]).  Attention reads rows
+ * kv_lo .. pos; rows below pos0 must have been written by earlier passes.
+ * drafts_dev (device int32 [n_rows] or NULL) receives argmax(lm_head h') per row.
+ * Errors: FM_ERR_INVALID_ARG (n_rows outside [1, max_rows], null tokens / hn,
+ *   kv_lo outside [0, pos0], pos0 + n_rows > kv_cap), FM_ERR_CUDA.
+ */
+FM_API fm_status fm_mtp_forward(fm_mtp *m, int32_t n_rows, const int32_t *tokens_dev, const float *hn_dev,
+                                int32_t pos0, int32_t kv_lo, float *hout_dev, int32_t *drafts_dev, void *stream);
+
+/*
+ * fm_mtp_draft -- MTPRunner's draft: a pass over the n_rows pending rows (as
+ * fm_mtp_forward), the draft of its last row, then depth - 1 single-row passes
+ * at pos0 + n_rows, ..., each on the previous draft (embedded on the device)
+ * and the previous pass's last h'.  drafts_dev: device int32 [depth].  No host
+ * round trip between the passes.  Errors: as fm_mtp_forward, and depth outside
+ * [1, kv_cap - pos0 - n_rows + 1].
+ */
+FM_API fm_status fm_mtp_draft(fm_mtp *m, int32_t n_rows, const int32_t *tokens_dev, const float *hn_dev,
+                              int32_t pos0, int32_t kv_lo, int32_t depth, int32_t *drafts_dev, void *stream);
+
+/* Copy the head's K (which = 0) or V (which = 1) cache rows [0, rows) ([rows][n_kv_heads * head_dim] f32,
+   host or device dst) after the stream's work (synchronises it); for tests.  Also reports what the device
+   raised since the last check: FM_ERR_INVALID_ARG for a token outside [0, vocab) that reached the embedding
+   (row 0 was read instead), FM_ERR_TIMEOUT for a bounded wait that gave up.  Errors: FM_ERR_INVALID_ARG,
+   FM_ERR_CUDA. */
+FM_API fm_status fm_mtp_cache(fm_mtp *m, int32_t which, int32_t rows, float *dst, void *stream);
+
+/* Kernel launches issued by the last fm_mtp_forward / fm_mtp_draft. */
+FM_API fm_status fm_mtp_last_launch_count(const fm_mtp *m, int32_t *count);
+FM_API const char *fm_mtp_last_error(const fm_mtp *m);   /* never NULL; NULL m: the last failed fm_mtp_create */
+FM_API void fm_mtp_destroy(fm_mtp *m);
+
 #ifdef __cplusplus
 }
 #endif
