@@ -112,6 +112,7 @@ struct fm_handle {
   std::map<std::tuple<int, int, int, const void *>, StepPhase *> step_progs;
   uint64_t *step_trace = nullptr;     // FM_DEBUG_TRACE: per phase and CTA, globaltimer stamps
   int step_trace_phases = 0;
+  int xattn_cluster = 0;              // the largest cross-attention cluster all heads' fit at once
   std::vector<void *> to_free;    // row-major staging copies released at the end of fm_create
 
   // ---- per-sequence lanes ----
@@ -404,7 +405,10 @@ struct AttnPlan {
 AttnPlan attn_plan(const fm_handle *h, int L) {
   const int nt = (L + 127) / 128;
   if (h->cfg.head_dim != 128) return {nt < 1 ? 1 : nt > 8 ? 8 : nt, true};
-  if (nt <= 4 * 16) return {nt < 1 ? 1 : nt > 16 ? 16 : nt, true};
+  // the largest cluster of which every head's can run at once (measured on this GPU: 15
+  // clusters of 7..9 ranges, 23 of 6, 7 of 16), then up to four tiles per range
+  const int cl = nt < h->xattn_cluster ? nt : h->xattn_cluster;
+  if (cl >= 1 && nt <= 4 * cl) return {cl, true};
   int cap = h->n_sm / h->cfg.n_heads;
   if (cap > kMaxXSplits) cap = kMaxXSplits;
   if (cap < 1) cap = 1;
@@ -1352,6 +1356,12 @@ fm_status create_common(fm_handle *h, cudaStream_t s) {
   }
   h->max_splits = 2 * h->n_sm / c.n_heads;
   if (h->max_splits < 1) h->max_splits = 1;
+  if (c.head_dim == 128) {
+    // cross-attention clusters: the largest size (<= 16) of which all n_heads clusters are co-resident
+    h->xattn_cluster = 0;
+    for (int cs = 16; cs >= 1 && !h->xattn_cluster; --cs)
+      if (xattn_max_active_clusters(cs, c.n_heads) >= c.n_heads) h->xattn_cluster = cs;
+  }
   TRY(dalloc(h, &h->tok_tmp, (size_t)kMaxT));
   TRY(dalloc(h, &h->dev_err, 4));
   CK(cudaMemsetAsync(h->dev_err, 0, 4, s));

@@ -191,6 +191,7 @@ struct XAttnArgs {
 };
 cudaError_t launch_xattn(const XAttnArgs &a, int stages, bool cluster, cudaStream_t st, bool pdl);
 size_t xattn_smem_bytes(int stages);
+int xattn_max_active_clusters(int cluster, int n_heads);
 bool make_cache_map(CUtensorMap *map, const __half *plane, int n_heads, int max_ctx);
 
 // --- lm_head GEMV fused with the per-row argmax -----------------------------

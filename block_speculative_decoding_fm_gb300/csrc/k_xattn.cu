@@ -578,6 +578,34 @@ cudaError_t launch_xattn(const XAttnArgs &a, int stages, bool cluster, cudaStrea
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+// Clusters of `cluster` ranges that can run at once (one-stage ring, cluster merge); 0 on error.
+int xattn_max_active_clusters(int cluster, int n_heads) {
+  auto kern = fm_xattn_kernel<1, true>;
+  const size_t smem = xattn_smem_bytes(1);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      (cluster > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_heads, cluster, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = cluster;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 bool make_cache_map(CUtensorMap *map, const __half *plane, int n_heads, int max_ctx) {
   return make_tma_f16(map, plane, (uint64_t)n_heads * max_ctx, HD, kTileKeys);
 }
