@@ -422,7 +422,7 @@ typedef struct fm_mtp_config {
   int32_t inter;       /* I (17408); a multiple of 128 */
   int32_t n_heads;     /* q heads (24) */
   int32_t n_kv_heads;  /* KV heads (4); divides n_heads */
-  int32_t head_dim;    /* 256; 64, 128 or 256 */
+  int32_t head_dim;    /* 256; a multiple of 32, <= 256 */
   int32_t rot_dims;    /* NEOX-rotated dims per head (64); even, <= head_dim */
   float theta;         /* RoPE base (1e7) */
   float eps;           /* RMSNorm eps (1e-6) */
