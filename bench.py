@@ -150,14 +150,20 @@ def dist():
     return ws, rank, local
 
 
-def barrier_max(ws, value):
+def barrier_max(ws, value, device="cuda"):
+    """The largest of the ranks' values (the slowest rank's time): every rank gets it."""
     if ws == 1:
         return value
     import torch
     import torch.distributed as d
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    t = torch.tensor([value], dtype=torch.float64, device=device)
     d.all_reduce(t, op=d.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(steps, ws, ms):
+    """Units per second of the whole job: every rank ran `steps` units; ms is the slowest rank's time."""
+    return steps * ws / (ms / 1000)
 
 
 # ----------------------------------------------------------------- workloads
@@ -738,7 +744,7 @@ def run_ours(args):
         ms = time_steps(torch, w.step, args.steps)
     launches = w.launches
     ms = barrier_max(ws, ms)
-    steps_s = args.steps * ws / (ms / 1000)
+    steps_s = whole_job_rate(args.steps, ws, ms)
     hbm_gbs = w.bytes_per_step * steps_s / ws / 1e9
 
     # end to end through the C ABI with host buffers (H2D of the feature rows,
@@ -748,7 +754,7 @@ def run_ours(args):
         for _ in range(3):
             w.step_e2e()
         ms_e2e = barrier_max(ws, time_steps(torch, w.step_e2e, args.steps))
-        e2e = {"value": args.steps * ws / (ms_e2e / 1000), "unit": "steps/s", "h2d_bytes_per_step": w.e2e_h2d,
+        e2e = {"value": whole_job_rate(args.steps, ws, ms_e2e), "unit": "steps/s", "h2d_bytes_per_step": w.e2e_h2d,
                "d2h_bytes_per_step": w.e2e_d2h}
 
     # per-kernel device time (events around every launch; a separate pass)
