@@ -545,10 +545,11 @@ def run_workload(args):
                     "flops_per_launch": flops / max(1, sum(v[0] for _, v in gemm)),
                     "ms_per_launch": gms / max(1, sum(v[0] for _, v in gemm))}
         kernels = {k: {"launches": v[0] / 3, "ms_per_step": v[1] / 3} for k, v in sorted(prof.items())}
-    elif args.workload == "mtp":
-        # the head's launches are not profiled one by one: the roofline of the whole draft
+    elif args.workload in ("mtp", "batched"):
+        # mtp: the head's launches are not profiled one by one; batched: the sequences' chains run
+        # concurrently, so a launch's events also span its neighbours' work.  The roofline of the whole step.
         achieved = extra["achieved_hbm_gbs"]
-        roofline = {"bound": "hbm", "kernel": "mtp_draft (every launch of the draft)", "achieved": achieved,
+        roofline = {"bound": "hbm", "kernel": f"{w.name} (every launch of the step)", "achieved": achieved,
                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                     "peak_source": f"{peak_src} burst copy", "bytes_per_launch": w.bytes_per_step,
                     "ms_per_launch": ms / args.steps}

@@ -1,7 +1,7 @@
 """GPU parity of the MTP draft head (ternary_bonsai_2_mtp.js, ``MTPHead.forward``
 and ``MTPRunner``'s draft loop) through fm_mtp_* against the oracle: the head
-output h' of every row (relative L2 within 2e-3), the head's K/V cache rows,
-and the drafted tokens (exact unless the oracle's top-2 logit margin is below
+output h' of every row (relative L2 within 2e-3), the head's K/V cache rows
+(within 1e-3), and the drafted tokens (exact unless the oracle's top-2 logit margin is below
 1e-3; after an excused difference the chain follows another token and the
 later drafts are not compared)."""
 from __future__ import annotations
@@ -57,7 +57,9 @@ class MtpPair:
         c = self.cfg
         for which, want in ((0, self.st.k), (1, self.st.v)):
             got = self.fm.fm_mtp_cache(self.h, which, rows, np.empty((rows, c.n_kv_heads * c.head_dim), np.float32))
-            assert rel_l2(got[:rows], want[:rows]) < 1e-4, (which, rel_l2(got[:rows], want[:rows]))
+            # the K/V rows come out of Q8_0 products whose weights the tensor cores see rounded to f16
+            # (<= 2^-11 relative per weight): the same 1e-3 bound as the drafter's f16 cache rows
+            assert rel_l2(got[:rows], want[:rows]) < 1e-3, (which, rel_l2(got[:rows], want[:rows]))
 
     def close(self):
         self.fm.fm_mtp_destroy(self.h)
