@@ -113,6 +113,9 @@ struct fm_handle {
   uint64_t *step_trace = nullptr;     // FM_DEBUG_TRACE: per phase and CTA, globaltimer stamps
   int step_trace_phases = 0;
   int xattn_cluster = 0;              // the largest cross-attention cluster all heads' fit at once
+  // several sequences' chains run at once (a batched call): each product then runs unsplit, on as
+  // many CTAs as it has 128-row tiles, so that the chains fill the GPU side by side
+  bool narrow = false;
   std::vector<void *> to_free;    // row-major staging copies released at the end of fm_create
 
   // ---- per-sequence lanes ----
@@ -367,8 +370,11 @@ GemvArgs gemv_base(const fm_handle *h, const __nv_bfloat16 *W, int M, int K, int
   a.T_const = T_const;
   a.sp = sp;
   const int tiles = (M + kTile - 1) / kTile;
+  // split K over a cluster of up to 8 CTAs; unsplit when several sequences' chains run at once
+  // (measured, 32 FlashMap-4B sequences: split as a single chain 76 steps/s, to one wave of
+  // clusters 95, unsplit 109)
   int ks = 1;
-  while (ks < 8 && K % (64 * ks * 2) == 0 && tiles * ks * 2 <= 2 * h->n_sm) ks *= 2;
+  while (!h->narrow && ks < 8 && K % (64 * ks * 2) == 0 && tiles * ks * 2 <= 2 * h->n_sm) ks *= 2;
   a.ksplit = ks;
   a.Kc = K / ks;
   // activation pieces: 256 columns; 128 for 17..32 rows, which keeps two CTAs per SM
@@ -392,9 +398,10 @@ fm_status run_gemv(fm_handle *h, const GemvArgs &a, cudaStream_t s, const char *
 }
 
 // Key ranges per head for the cross-attention over L keys, and how they merge.
-// Head dim 128 (tensor-core kernel): up to four 128-key tiles per range, at most
-// 16 ranges merged in a cluster (one-stage ring: two CTAs fit on an SM); longer
-// contexts: one range per SM, three-stage rings, merged by the last range (ticket).
+// Head dim 128 (tensor-core kernel): up to four 128-key tiles per range, the
+// ranges of a head merged in a cluster (one-stage ring) no larger than lets every
+// head's cluster run at once; longer contexts: one range per SM, three-stage
+// rings, merged by the last range (ticket).
 // Head dim 64: one cluster of at most 8 CTAs per head (16-CTA clusters were
 // measured slower there: their scheduling and merge cost more than the shorter
 // key loop saves).
@@ -1180,6 +1187,7 @@ fm_status flashmap_prefill(fm_handle *h, int seq, const float *feats, int n, int
 // and replay the graph.  With FM_DEBUG_PROFILE the chain is launched directly.
 template <typename Enqueue>
 fm_status run_chain(fm_handle *h, uint64_t key, const StepParams &p, cudaStream_t s, Enqueue &&enqueue) {
+  key |= (uint64_t)(h->narrow ? 1 : 0) << 55;   // the products' launch shapes depend on it
   if (h->use_graphs && !(h->debug & (FM_DEBUG_PROFILE | FM_DEBUG_TRACE))) {
     auto it = h->graphs.find(key);
     if (it == h->graphs.end()) {
@@ -1813,8 +1821,11 @@ fm_status fm_context_append(fm_handle *h, int32_t seq, const float *feats, int32
   if (!h) return FM_ERR_INVALID_ARG;
   h->last_launches = 0;
   TRY(append_checks(h, seq, feats, n_rows, start_pos));
+  h->narrow = false;
   return append_one(h, seq, feats, n_rows, start_pos, static_cast<cudaStream_t>(stream));
 }
+
+constexpr int kNarrowSeqs = 8;   // sequences per call from which the products run unsplit
 
 fm_status fm_context_append_batched(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const float *feats,
                                     const int32_t *n_rows, const int32_t *start, void *stream) {
@@ -1849,6 +1860,7 @@ fm_status fm_context_append_batched(fm_handle *h, int32_t n_seqs, const int32_t 
     }
   }
   if (rest.empty()) return FM_OK;
+  h->narrow = (int)rest.size() >= kNarrowSeqs && h->lanes.size() > 1;
   return run_lanes(h, (int)rest.size(), rest.data(), s, [&](int j, cudaStream_t ls) {
     const int i = rest_i[j];
     return append_one(h, seq_ids[i], feats + offs[i], n_rows[i], start[i], ls);
@@ -1874,6 +1886,7 @@ fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const i
       return fail(h, FM_ERR_CONTEXT_FULL, "context full at pos %d", pos[i]);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->narrow = !h->use_step && n_seqs >= kNarrowSeqs && h->lanes.size() > 1;
   if (h->use_step) {
     // the persistent step holds every SM: sequences draft one after another on the caller's stream
     for (int i = 0; i < n_seqs; ++i)
@@ -1906,6 +1919,7 @@ fm_status fm_draft_pruned(fm_handle *h, int32_t seq, int32_t anchor, int32_t pos
   if (!h->conf_w && (any || conf))
     return fail(h, FM_ERR_UNSUPPORTED, "the weights hold no confidence head (conf.w, conf.b)");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->narrow = false;
   return draft_one(h, seq, anchor, pos, tokens, s, conf, length, thr);
 }
 

@@ -294,11 +294,13 @@ cudaError_t launch_gemv(const GemvArgs &a, int n_tiles, cudaStream_t st, bool pd
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int na = 0;
-  attr[na].id = cudaLaunchAttributeClusterDimension;
-  attr[na].val.clusterDim.x = 1;
-  attr[na].val.clusterDim.y = a.ksplit;
-  attr[na].val.clusterDim.z = 1;
-  ++na;
+  if (a.ksplit > 1) {   // (without K slices each CTA is its own cluster, and two may share an SM)
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = a.ksplit;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   if (pdl) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
