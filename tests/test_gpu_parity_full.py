@@ -197,3 +197,23 @@ def test_long_context_prefill_and_draft():
     assert rel_l2(p.head_out(), ref.head_out) < REL_L2
     assert tokens_match(got, ref.tokens, ref.logits), (got, ref.tokens)
     p.close()
+
+
+def test_flashmap_4b_step_persistent(monkeypatch):
+    """The opt-in one-launch draft step (FM_PERSISTENT=1: 8-CTA clusters, a
+    counter grid barrier between the layer phases) on the FlashMap-4B step:
+    the same parity as the launch chain, in at most six launches."""
+    monkeypatch.setenv("FM_PERSISTENT", "1")
+    cfg = S.flashmap_4b_config()
+    p = Pair(cfg, 1002)
+    fr = S.streams(1002)["features"]
+    p.append(0, S.gen_features(fr, 1024, cfg.feat_dim), 0)
+    p.append(0, S.gen_features(fr, 17, cfg.feat_dim), 1024)
+    anchor = S.gen_anchor(S.streams(1002)["tokens"], cfg.vocab)
+    got, ref = p.draft(0, anchor, 1041)
+    assert p.last_launches <= 6, p.last_launches
+    for l in range(cfg.n_layers):
+        assert rel_l2(p.hidden(l), ref.hidden[l]) < REL_L2, l
+    assert rel_l2(p.head_out(), ref.head_out) < REL_L2
+    assert tokens_match(got, ref.tokens, ref.logits), (got, ref.tokens)
+    p.close()
