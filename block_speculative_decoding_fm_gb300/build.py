@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "libfm.so")
-SOURCES = ["fm_api.cu", "k_gemv.cu", "k_step.cu", "k_attn.cu", "k_lmhead.cu", "k_setup.cu", "k_gemm.cu", "policy.cu", "k_seqhead.cu", "k_xattn.cu", "mtp.cu"]
+SOURCES = ["fm_api.cu", "k_gemv.cu", "k_step.cu", "k_attn.cu", "k_lmhead.cu", "k_setup.cu", "k_gemm.cu", "policy.cu", "k_seqhead.cu", "k_xattn.cu", "mtp.cu", "k_wide.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

@@ -208,6 +208,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&f)[32]) {
   for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&f)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]), "f"(f[8]), "f"(f[9]),
+      "f"(f[10]), "f"(f[11]), "f"(f[12]), "f"(f[13]), "f"(f[14]), "f"(f[15]), "f"(f[16]), "f"(f[17]), "f"(f[18]),
+      "f"(f[19]), "f"(f[20]), "f"(f[21]), "f"(f[22]), "f"(f[23]), "f"(f[24]), "f"(f[25]), "f"(f[26]), "f"(f[27]),
+      "f"(f[28]), "f"(f[29]), "f"(f[30]), "f"(f[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// OR of a predicate over the `n` threads that meet at named barrier `id`
+__device__ __forceinline__ bool bar_any(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // (value, index) ordering for argmax: larger value wins, ties to the lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -117,6 +118,38 @@ struct fm_handle {
   // many CTAs as it has 128-row tiles, so that the chains fill the GPU side by side
   bool narrow = false;
   std::vector<void *> to_free;    // row-major staging copies released at the end of fm_create
+
+  // ---- batched draft: the slot rows of up to kWideSeqs sequences go through the
+  // tensor-core GEMM together, so each weight is read once per pass ----
+  struct Wide {
+    bool on = false;
+    int Vn = 0;                                      // token table rows, padded to 256
+    std::vector<__half *> qkv, so, cq, co, f1, f2;   // f16 copies of the layer weights, [N][K]
+    __half *ap = nullptr, *head = nullptr, *table = nullptr;
+    std::vector<CUtensorMap> t_qkv, t_so, t_cq, t_co, t_f1, t_f2;
+    CUtensorMap t_ap{}, t_head{}, t_table{}, t_cache{};
+    // activations: X [rows][D] f32; q/k/v and cross q f32; the head output f32 and f16
+    float *X = nullptr, *qkv_out = nullptr, *qc = nullptr, *Y = nullptr, *kst = nullptr;
+    __half *a16 = nullptr, *o16 = nullptr, *u16 = nullptr, *y16 = nullptr, *anc16 = nullptr, *kin16 = nullptr;
+    CUtensorMap m_a16{}, m_o16{}, m_u16{}, m_y16{}, m_anc16{}, m_kin16{};
+    float *ws = nullptr;            // split-K partial tiles
+    int32_t *tickets = nullptr;     // split-K tile tickets
+    float2 *amax = nullptr;         // lm_head per-row, per-column-block bests
+    float *xo = nullptr;            // cross-attention range partials of every sequence
+    float2 *xml = nullptr;
+    int32_t *xtickets = nullptr;
+    int xsplits = 2;                // key ranges per (sequence, head)
+    WideParams *par = nullptr;      // device copy of the pass's values
+    WideParams *par_host = nullptr; // pinned ring
+    cudaEvent_t par_ev[kParamSlots]{};
+    int par_next = 0;
+    // batched append: per-row (sequence, position) of the rows' K/V
+    int32_t *rows = nullptr, *rows_host = nullptr;
+    int rows_cap = 0;
+    cudaEvent_t rows_ev[kParamSlots]{};
+    int rows_next = 0;
+    std::vector<int> row_of;        // per sequence: its first row in the last batched draft, or -1
+  } wide;
 
   // ---- per-sequence lanes ----
   // Each sequence has its own work buffers (and, with several sequences, its own
@@ -1248,6 +1281,7 @@ fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens,
                     float *conf = nullptr, int32_t *length = nullptr, const float *thr = nullptr) {
   const fm_config &c = h->cfg;
   fm_handle::Lane &lane = h->lanes[seq];
+  if (h->wide.on) h->wide.row_of[seq] = -1;
   int n_pend = 0;
   if (lane.pending) {
     if (lane.pend_start + lane.pend_n == pos && c.variant == FM_VARIANT_FLASHMAP && lane.pend_n + 1 <= kMaxT) {
@@ -1282,6 +1316,436 @@ fm_status draft_one(fm_handle *h, int seq, int anchor, int pos, int32_t *tokens,
     return c.variant == FM_VARIANT_FLASHMAP ? flashmap_draft_launch(h, seq, pos, sp, n_pend, st)
                                             : dflash_draft_launch(h, seq, pos, sp, st);
   });
+}
+
+// ---------------------------------------------------------------- batched draft
+
+// Several sequences drafting at once (flashmap_drafter.js ``draft`` per anchor;
+// above 17 rows the page hands its products to ``runGemm``): the block rows of
+// up to kWideSeqs sequences (16 each, 512 at most) go through every product as
+// one tensor-core GEMM, so each weight and the token table are read once per
+// pass instead of once per sequence.  Activations enter the tensor cores as
+// f16 (one rounding per product, against the skinny path's hi + lo split);
+// weights as f16 copies of the bf16 values and the Q8_0 table as f16(d * q).
+constexpr int kWideMin = 4;   // sequences per call from which drafts take the batched path
+
+bool wide_wanted(const fm_handle *h) {
+  const fm_config &c = h->cfg;
+  const char *e = getenv("FM_NO_WIDE");
+  if (e && e[0] == '1') return false;
+  const double cache_rows = (double)c.max_seqs * c.n_layers * 2 * c.n_heads * c.max_ctx;
+  return c.variant == FM_VARIANT_FLASHMAP && c.max_seqs >= 2 && c.head_dim == 128 && c.dim % 256 == 0 &&
+         c.ff_dim % 256 == 0 && c.target_dim % 256 == 0 && c.dim <= 4096 && c.max_ctx >= 128 &&
+         cache_rows < 2147483647.0;
+}
+
+// A-operand buffer: [rows][cols] f16 with rows a multiple of 128 (whole TMA boxes)
+fm_status wide_abuf(fm_handle *h, __half **p, CUtensorMap *m, int rows, int cols) {
+  const int r = (rows + 127) / 128 * 128;
+  TRY(dalloc(h, p, (size_t)r * cols));
+  if (!make_tma_f16(m, *p, r, cols, 128)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+  return FM_OK;
+}
+
+fm_status wide_weight(fm_handle *h, const __nv_bfloat16 *w, int N, int K, __half **out, CUtensorMap *m, cudaStream_t s) {
+  TRY(dalloc(h, out, (size_t)N * K));
+  CK(launch_bf16_to_f16(w, *out, (size_t)N * K, s));
+  if (!make_tma_f16(m, *out, N, K, 256)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+  return FM_OK;
+}
+
+// f16 copies of the layer weights (from the row-major bf16 staging copies,
+// before they are tiled) and the batched path's buffers
+fm_status create_wide(fm_handle *h, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  fm_handle::Wide &w = h->wide;
+  const int D = c.dim, F = c.ff_dim, Ht = c.target_dim, L = c.n_layers, H = c.n_heads;
+  const int ns = c.max_seqs < kWideSeqs ? c.max_seqs : kWideSeqs;
+  const int T = ns * c.block;
+  TRY(prefill_setup(h, s));
+  w.qkv.resize(L); w.so.resize(L); w.cq.resize(L); w.co.resize(L); w.f1.resize(L); w.f2.resize(L);
+  w.t_qkv.resize(L); w.t_so.resize(L); w.t_cq.resize(L); w.t_co.resize(L); w.t_f1.resize(L); w.t_f2.resize(L);
+  for (int l = 0; l < L; ++l) {
+    TRY(wide_weight(h, h->w_qkv[l], 3 * D, D, &w.qkv[l], &w.t_qkv[l], s));
+    TRY(wide_weight(h, h->w_so[l], D, D, &w.so[l], &w.t_so[l], s));
+    TRY(wide_weight(h, h->w_cq[l], D, D, &w.cq[l], &w.t_cq[l], s));
+    TRY(wide_weight(h, h->w_co[l], D, D, &w.co[l], &w.t_co[l], s));
+    TRY(wide_weight(h, h->w_f1[l], F, D, &w.f1[l], &w.t_f1[l], s));
+    TRY(wide_weight(h, h->w_f2[l], D, F, &w.f2[l], &w.t_f2[l], s));
+  }
+  TRY(wide_weight(h, h->w_ap, D, Ht, &w.ap, &w.t_ap, s));
+  TRY(wide_weight(h, h->w_head, Ht, D, &w.head, &w.t_head, s));
+  if (!make_tma_f16(&w.t_table, w.table, w.Vn, Ht, 256)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+  if (!make_cache_map(&w.t_cache, h->cache, c.max_seqs * L * 2 * H, c.max_ctx))
+    return fail(h, FM_ERR_CUDA, "cache tensor map encoding failed");
+  const int Tr = (T + 127) / 128 * 128;
+  TRY(dalloc(h, &w.X, (size_t)Tr * D));
+  TRY(dalloc(h, &w.qkv_out, (size_t)Tr * 3 * D));
+  TRY(dalloc(h, &w.qc, (size_t)Tr * D));
+  TRY(dalloc(h, &w.Y, (size_t)Tr * Ht));
+  TRY(dalloc(h, &w.kst, (size_t)128 * (D / 256)));
+  TRY(wide_abuf(h, &w.a16, &w.m_a16, T, D));
+  TRY(wide_abuf(h, &w.o16, &w.m_o16, T, D));
+  TRY(wide_abuf(h, &w.u16, &w.m_u16, T, F));
+  TRY(wide_abuf(h, &w.y16, &w.m_y16, T, Ht));
+  TRY(wide_abuf(h, &w.anc16, &w.m_anc16, ns, Ht));
+  TRY(wide_abuf(h, &w.kin16, &w.m_kin16, ns, D));
+  // split-K: at most one wave of (tile, slice) units holds a partial tile each
+  TRY(dalloc(h, &w.ws, (size_t)h->n_sm * 128 * 256));
+  TRY(dalloc(h, &w.tickets, (size_t)h->n_sm));
+  CK(cudaMemsetAsync(w.tickets, 0, (size_t)h->n_sm * 4, s));
+  TRY(dalloc(h, &w.amax, (size_t)T * (w.Vn / 256)));
+  TRY(dalloc(h, &w.xo, (size_t)ns * H * 8 * 16 * 128));
+  TRY(dalloc(h, &w.xml, (size_t)ns * H * 8 * 16));
+  TRY(dalloc(h, &w.xtickets, (size_t)ns * H));
+  CK(cudaMemsetAsync(w.xtickets, 0, (size_t)ns * H * 4, s));
+  const char *xs = getenv("FM_WIDE_XSPLITS");
+  if (xs && atoi(xs) >= 1 && atoi(xs) <= 8) w.xsplits = atoi(xs);
+  TRY(dalloc(h, &w.par, 1));
+  CK(cudaMallocHost(&w.par_host, sizeof(WideParams) * kParamSlots));
+  w.rows_cap = h->pf_rows;
+  TRY(dalloc(h, &w.rows, (size_t)2 * w.rows_cap));
+  CK(cudaMallocHost(&w.rows_host, sizeof(int32_t) * 2 * w.rows_cap * kParamSlots));
+  for (int i = 0; i < kParamSlots; ++i) {
+    CK(cudaEventCreateWithFlags(&w.par_ev[i], cudaEventDisableTiming));
+    CK(cudaEventCreateWithFlags(&w.rows_ev[i], cudaEventDisableTiming));
+  }
+  w.row_of.assign(c.max_seqs, -1);
+  w.on = true;
+  return FM_OK;
+}
+
+// device address of an int32 array inside the pass parameters
+#define WIDE_FIELD(h, f) \
+  reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>((h)->wide.par) + offsetof(WideParams, f))
+
+// one GEMM of the batched path: A [M][K] rows (map a) times the weight B [N][K] (map b)
+TcGemmArgs wide_gemm(const fm_handle *h, const CUtensorMap &a, const CUtensorMap &b, int M, int N, int K, int epi) {
+  TcGemmArgs g;
+  memset(&g, 0, sizeof g);
+  g.tma_a = a;
+  g.tma_b = b;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.epi = epi;
+  g.group_m = (M + 127) / 128;   // the row blocks that share a weight tile run side by side
+  g.err = h->dev_err;
+  // K slices fill the GPU when there are fewer tiles than SMs (one wave of units at most)
+  const int tiles = tc_gemm_tiles(M, N), nk = K / 64;
+  int ks = h->n_sm / tiles;
+  if (ks > 8) ks = 8;
+  if (ks > nk) ks = nk;
+  g.ksplit = ks < 1 ? 1 : ks;
+  g.ws = h->wide.ws;
+  g.tile_tickets = h->wide.tickets;
+  g.hd = h->cfg.head_dim;
+  g.max_ctx = h->cfg.max_ctx;
+  g.rope = h->rope;
+  g.qk_eps = h->cfg.qk_eps;
+  return g;
+}
+
+fm_status run_tc(fm_handle *h, const TcGemmArgs &g, cudaStream_t s, const char *tag) {
+  ProfScope ps(h, s, tag, (double)g.N * g.K * 2 + (double)g.M * g.K * 2);
+  CK(launch_tc_gemm(g, h->n_sm, s));
+  ++h->last_launches;
+  return FM_OK;
+}
+
+fm_status run_lnmod(fm_handle *h, const float *m, int T, cudaStream_t s) {
+  const int D = h->cfg.dim;
+  ProfScope ps(h, s, "wide.lnmod", (double)T * D * 6);
+  CK(launch_wide_lnmod(h->wide.X, D, T, m, m + D, h->cfg.ln_eps, h->wide.a16, s));
+  ++h->last_launches;
+  return FM_OK;
+}
+
+// The launches of one batched pass over n sequences (values from wide.par).
+fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  fm_handle::Wide &w = h->wide;
+  const int D = c.dim, B = c.block, Ht = c.target_dim, F = c.ff_dim, L = c.n_layers, H = c.n_heads;
+  const int T = n * B;
+  {
+    ProfScope ps(h, s, "wide.prep", (double)T * D * 4 + (double)n * Ht * 4);
+    CK(launch_wide_prep(h->h0, D, T, w.X, w.par, n, w.table, Ht, w.anc16, h->n_sm, s));
+    ++h->last_launches;
+  }
+  // the anchors' context slots: anchor_proj + bias (anchor_norm folded in), then every layer's K / V at pos
+  TcGemmArgs g = wide_gemm(h, w.m_anc16, w.t_ap, n, D, Ht, TC_EPI_FC);
+  g.bias = h->b_ap;
+  g.colw = h->w_an;
+  g.out16 = w.kin16;
+  g.ldo = D;
+  g.row_st = w.kst;
+  g.st_ld = D / 256;
+  TRY(run_tc(h, g, s, "wide.anchor_proj"));
+  g = wide_gemm(h, w.m_kin16, h->tm_wkv, n, L * 2 * D, D, TC_EPI_KV);
+  g.in_st = w.kst;
+  g.in_st_n = D / 256;
+  g.eps = c.rms_eps;
+  g.inv_n = 1.0f / D;
+  g.seg_cols = D;
+  g.kn_w = h->w_ckn;
+  g.cache = h->cache;
+  g.plane = h->cache_plane;
+  g.row_seq = WIDE_FIELD(h, kv_seq);
+  g.row_pos = WIDE_FIELD(h, kv_pos);
+  g.seq_stride = (size_t)L * 2 * h->cache_plane;
+  TRY(run_tc(h, g, s, "wide.kv_anchor"));
+  for (int l = 0; l < L; ++l) {
+    const float *ms = h->mod + (size_t)(3 * l + 0) * 3 * D;
+    const float *mc = h->mod + (size_t)(3 * l + 1) * 3 * D;
+    const float *mm = h->mod + (size_t)(3 * l + 2) * 3 * D;
+    // self-attention over each sequence's block
+    TRY(run_lnmod(h, ms, T, s));
+    g = wide_gemm(h, w.m_a16, w.t_qkv[l], T, 3 * D, D, TC_EPI_SEGS);
+    g.seg_cols = D;
+    g.nw0 = h->w_sqn[l];
+    g.nw1 = h->w_skn[l];
+    g.out32 = w.qkv_out;
+    g.ldo32 = 3 * D;
+    g.row_pos = WIDE_FIELD(h, row_pos);
+    TRY(run_tc(h, g, s, "wide.qkv_self"));
+    {
+      ProfScope ps(h, s, "wide.attn_self", (double)T * D * 3 * 4 + (double)T * D * 2);
+      CK(launch_wide_self_attn(w.qkv_out, D, B, n, H, w.o16, s));
+      ++h->last_launches;
+    }
+    g = wide_gemm(h, w.m_o16, w.t_so[l], T, D, D, TC_EPI_RESID);
+    g.X = w.X;
+    g.ldx = D;
+    g.gate = ms + 2 * D;
+    TRY(run_tc(h, g, s, "wide.o_self"));
+    // cross-attention over each sequence's own cache rows 0 .. pos
+    TRY(run_lnmod(h, mc, T, s));
+    g = wide_gemm(h, w.m_a16, w.t_cq[l], T, D, D, TC_EPI_SEGS);
+    g.seg_cols = D;
+    g.nw0 = h->w_cqn[l];
+    g.out32 = w.qc;
+    g.ldo32 = D;
+    g.row_pos = WIDE_FIELD(h, row_pos);
+    TRY(run_tc(h, g, s, "wide.q_cross"));
+    {
+      XAttnArgs xa;
+      memset(&xa, 0, sizeof xa);
+      xa.tm_k = w.t_cache;
+      xa.tm_v = w.t_cache;
+      xa.Q = w.qc;
+      xa.ldq = D;
+      xa.max_ctx = c.max_ctx;
+      xa.n_heads = H;
+      xa.splits = xs;
+      xa.T_const = B;
+      xa.scale_log2 = (float)(1.4426950408889634 / std::sqrt(128.0));
+      xa.out16 = w.o16;
+      xa.ldo = D;
+      xa.part_o = w.xo;
+      xa.part_ml = w.xml;
+      xa.tickets = w.xtickets;
+      xa.err = h->dev_err;
+      xa.bz_call = WIDE_FIELD(h, z_call);
+      xa.bz_seq = WIDE_FIELD(h, z_seq);
+      xa.bz_L = WIDE_FIELD(h, z_L);
+      xa.n_z = n;
+      xa.layer = l;
+      xa.n_layers = L;
+      ProfScope ps(h, s, "wide.attn_cross", 0.0);
+      CK(launch_xattn(xa, 3, false, s, true));
+      ++h->last_launches;
+    }
+    g = wide_gemm(h, w.m_o16, w.t_co[l], T, D, D, TC_EPI_RESID);
+    g.X = w.X;
+    g.ldx = D;
+    g.gate = mc + 2 * D;
+    TRY(run_tc(h, g, s, "wide.o_cross"));
+    // MLP
+    TRY(run_lnmod(h, mm, T, s));
+    g = wide_gemm(h, w.m_a16, w.t_f1[l], T, F, D, TC_EPI_F16);
+    g.bias = h->b_f1[l];
+    g.gelu = 1;
+    g.out16 = w.u16;
+    g.ldo = F;
+    TRY(run_tc(h, g, s, "wide.fc1"));
+    g = wide_gemm(h, w.m_u16, w.t_f2[l], T, D, F, TC_EPI_RESID);
+    g.bias = h->b_f2[l];
+    g.X = w.X;
+    g.ldx = D;
+    g.gate = mm + 2 * D;
+    TRY(run_tc(h, g, s, "wide.fc2"));
+  }
+  // final adaLN -> head -> lm_head with the per-row argmax
+  TRY(run_lnmod(h, h->mod + (size_t)(3 * L) * 3 * D, T, s));
+  g = wide_gemm(h, w.m_a16, w.t_head, T, Ht, D, TC_EPI_F16);
+  g.bias = h->b_head;
+  g.out16 = w.y16;
+  g.ldo = Ht;
+  g.out32 = w.Y;
+  g.ldo32 = Ht;
+  TRY(run_tc(h, g, s, "wide.head"));
+  g = wide_gemm(h, w.m_y16, w.t_table, T, w.Vn, Ht, TC_EPI_ARGMAX);
+  g.amax = w.amax;
+  g.amax_ld = w.Vn / 256;
+  g.n_valid = c.vocab;
+  TRY(run_tc(h, g, s, "wide.lm_head"));
+  {
+    ProfScope ps(h, s, "wide.argmax", (double)T * (w.Vn / 256) * 8);
+    CK(launch_wide_argmax(w.amax, w.Vn / 256, T, w.par, s));
+    ++h->last_launches;
+  }
+  return FM_OK;
+}
+
+// Capture a launch sequence into a CUDA graph the first time its key is seen,
+// replay it afterwards (the per-call values travel through device buffers
+// uploaded before the launch).
+template <typename Enqueue>
+fm_status run_graph(fm_handle *h, uint64_t key, cudaStream_t s, Enqueue &&enqueue) {
+  if (!h->use_graphs || (h->debug & (FM_DEBUG_PROFILE | FM_DEBUG_TRACE))) return enqueue(s);
+  auto it = h->graphs.find(key);
+  if (it == h->graphs.end()) {
+    fm_handle::GraphEntry g;
+    CK(cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeRelaxed));
+    const int before = h->last_launches;
+    fm_status st = enqueue(h->cap);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(h->cap, &graph);
+    if (st != FM_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return st;
+    }
+    CK(e);
+    e = cudaGraphInstantiate(&g.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    CK(e);
+    g.launches = h->last_launches - before;
+    h->last_launches = before;
+    it = h->graphs.emplace(key, g).first;
+  }
+  CK(cudaGraphLaunch(it->second.exec, s));
+  h->last_launches += it->second.launches;
+  return FM_OK;
+}
+
+fm_status wide_upload(fm_handle *h, const WideParams &p, cudaStream_t s) {
+  fm_handle::Wide &w = h->wide;
+  const int i = w.par_next;
+  w.par_next = (i + 1) % kParamSlots;
+  cudaEventSynchronize(w.par_ev[i]);   // the slot's previous copy has been consumed
+  w.par_host[i] = p;
+  CK(cudaMemcpyAsync(w.par, w.par_host + i, sizeof(WideParams), cudaMemcpyHostToDevice, s));
+  CK(cudaEventRecord(w.par_ev[i], s));
+  return FM_OK;
+}
+
+// Batched draft of n sequences (arguments checked by the caller), in passes of kWideSeqs.
+fm_status wide_draft(fm_handle *h, int n, const int32_t *ids, const int32_t *anchors, const int32_t *pos,
+                     int32_t *tokens, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  fm_handle::Wide &w = h->wide;
+  for (int i = 0; i < n; ++i) TRY(flush_pending(h, ids[i], s));
+  std::fill(w.row_of.begin(), w.row_of.end(), -1);
+  for (int p0 = 0; p0 < n; p0 += kWideSeqs) {
+    const int m = n - p0 < kWideSeqs ? n - p0 : kWideSeqs;
+    WideParams p;
+    memset(&p, 0, sizeof p);
+    p.n = m;
+    p.tokens = tokens + (size_t)p0 * c.block;
+    std::vector<int> order(m);
+    for (int i = 0; i < m; ++i) {
+      p.seq[i] = ids[p0 + i];
+      p.anchor[i] = anchors[p0 + i];
+      p.pos[i] = pos[p0 + i];
+      p.kv_seq[i] = ids[p0 + i];
+      p.kv_pos[i] = pos[p0 + i];
+      for (int t = 0; t < c.block; ++t) p.row_pos[i * c.block + t] = pos[p0 + i] + 1 + t;
+      order[i] = i;
+    }
+    // the cross-attention hands out its CTAs longest context first
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return p.pos[a] > p.pos[b]; });
+    for (int z = 0; z < m; ++z) {
+      p.z_call[z] = order[z];
+      p.z_seq[z] = p.seq[order[z]];
+      p.z_L[z] = p.pos[order[z]] + 1;
+    }
+    TRY(wide_upload(h, p, s));
+    const int xs = w.xsplits;
+    TRY(run_graph(h, chain_key(6, 0, m, xs, 0), s, [&](cudaStream_t st) { return wide_chain(h, m, xs, st); }));
+    if (p0 + m == n)
+      for (int i = 0; i < m; ++i) w.row_of[ids[p0 + i]] = i * c.block;
+  }
+  return FM_OK;
+}
+
+// Batched append of small row counts: every row of every sequence through one
+// fc GEMM and one K/V GEMM (per-row sequence and position), in chunks of the
+// prefill scratch.  feats: the rows of sequence i start at feats + offs[i].
+fm_status wide_append(fm_handle *h, int n, const int32_t *ids, const float *feats, const size_t *offs,
+                      const int32_t *n_rows, const int32_t *start, cudaStream_t s) {
+  const fm_config &c = h->cfg;
+  fm_handle::Wide &w = h->wide;
+  const int D = c.dim, FW = c.n_taps * c.target_dim, L = c.n_layers;
+  for (int i = 0; i < n; ++i) TRY(flush_pending(h, ids[i], s));
+  // rows in call order: (sequence index, row within it)
+  std::vector<std::pair<int, int>> rows;
+  for (int i = 0; i < n; ++i)
+    for (int r = 0; r < n_rows[i]; ++r) rows.emplace_back(i, r);
+  const int R = (int)rows.size();
+  for (int r0 = 0; r0 < R; r0 += h->pf_rows) {
+    const int Rc = R - r0 < h->pf_rows ? R - r0 : h->pf_rows;
+    // f32 -> f16 rows, one launch per run of rows adjacent in the caller's buffer
+    for (int a = 0; a < Rc;) {
+      const float *src = feats + offs[rows[r0 + a].first] + (size_t)rows[r0 + a].second * FW;
+      int b = a + 1;
+      while (b < Rc && feats + offs[rows[r0 + b].first] + (size_t)rows[r0 + b].second * FW == src + (size_t)(b - a) * FW) ++b;
+      ProfScope ps(h, s, "append.f32_to_f16", (double)(b - a) * FW * 6);
+      CK(launch_f32_to_f16(src, h->pf_a + (size_t)a * FW, (size_t)(b - a) * FW, h->n_sm, s));
+      ++h->last_launches;
+      a = b;
+    }
+    // per-row targets
+    const int slot = w.rows_next;
+    w.rows_next = (slot + 1) % kParamSlots;
+    cudaEventSynchronize(w.rows_ev[slot]);
+    int32_t *hs = w.rows_host + (size_t)slot * 2 * w.rows_cap;
+    for (int r = 0; r < Rc; ++r) {
+      const int i = rows[r0 + r].first;
+      hs[r] = ids[i];
+      hs[w.rows_cap + r] = start[i] + rows[r0 + r].second;
+    }
+    CK(cudaMemcpyAsync(w.rows, hs, (size_t)Rc * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(w.rows + w.rows_cap, hs + w.rows_cap, (size_t)Rc * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaEventRecord(w.rows_ev[slot], s));
+    // whole 128-row boxes: the maps span at least 128 rows of the scratch (rows past Rc are masked)
+    const int Rm = Rc < 128 ? 128 : Rc;
+    CUtensorMap ma;
+    if (!make_tma_f16(&ma, h->pf_a, Rm, FW, 128)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+    TcGemmArgs g = wide_gemm(h, ma, h->tm_wfc, Rc, D, FW, TC_EPI_FC);
+    g.colw = h->w_hn;
+    g.out16 = h->pf_c;
+    g.ldo = D;
+    g.row_st = h->pf_st;
+    g.st_ld = D / 256;
+    TRY(run_tc(h, g, s, "append.gemm_fc"));
+    CUtensorMap mc;
+    if (!make_tma_f16(&mc, h->pf_c, Rm, D, 128)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+    g = wide_gemm(h, mc, h->tm_wkv, Rc, L * 2 * D, D, TC_EPI_KV);
+    g.in_st = h->pf_st;
+    g.in_st_n = D / 256;
+    g.eps = c.rms_eps;
+    g.inv_n = 1.0f / D;
+    g.seg_cols = D;
+    g.kn_w = h->w_ckn;
+    g.cache = h->cache;
+    g.plane = h->cache_plane;
+    g.row_seq = w.rows;
+    g.row_pos = w.rows + w.rows_cap;
+    g.seq_stride = (size_t)L * 2 * h->cache_plane;
+    TRY(run_tc(h, g, s, "append.gemm_kv"));
+  }
+  for (int i = 0; i < n; ++i) h->length[ids[i]] = start[i] + n_rows[i];
+  return FM_OK;
 }
 
 // ---------------------------------------------------------------- create
@@ -1424,12 +1888,22 @@ fm_status create_table(fm_handle *h, const TensorSet &ts, cudaStream_t s) {
     TRY(dalloc(h, &h->tq8, q8_table_bytes(V, H)));
     CK(launch_q8_repack(raw, V, H, h->tq8, s));
     CK(launch_colmean_q8(raw, V, H, h->uni, s));
+    if (wide_wanted(h)) {
+      h->wide.Vn = (V + 255) / 256 * 256;
+      TRY(dalloc(h, &h->wide.table, (size_t)h->wide.Vn * H));
+      CK(launch_q8_to_f16(raw, V, H, h->wide.Vn, h->wide.table, s));
+    }
     dfree_later(h, raw);
   } else {
     __nv_bfloat16 *tb;
     TRY(dalloc(h, &tb, (size_t)V * H));
     TRY(put_bf16(h, ts, "token_embd.weight", tb, (int64_t)V * H, s));
     CK(launch_colmean_bf16(tb, V, H, h->uni, s));
+    if (wide_wanted(h)) {
+      h->wide.Vn = (V + 255) / 256 * 256;
+      TRY(dalloc(h, &h->wide.table, (size_t)h->wide.Vn * H));
+      CK(launch_bf16_to_f16_pad(tb, V, H, h->wide.Vn, h->wide.table, s));
+    }
     TRY(tile_weight(h, &tb, V, H, s));
     h->tb = reinterpret_cast<uint8_t *>(tb);
   }
@@ -1519,6 +1993,7 @@ fm_status create_flashmap(fm_handle *h, const TensorSet &ts, const float *modula
     CK(launch_bf16_to_f16(h->w_fc, h->w_fc16, (size_t)D * FW, s));
     CK(launch_bf16_to_f16(h->w_kvall, h->w_kv16, (size_t)L * 2 * D * D, s));
   }
+  if (wide_wanted(h)) TRY(create_wide(h, s));
   TRY(tile_weight(h, &h->w_fc, D, FW, s));
   TRY(tile_weight(h, &h->w_ap, D, Ht, s));
   TRY(tile_weight(h, &h->w_xe, D, Ht, s));
@@ -1860,6 +2335,16 @@ fm_status fm_context_append_batched(fm_handle *h, int32_t n_seqs, const int32_t 
     }
   }
   if (rest.empty()) return FM_OK;
+  if (h->wide.on && (int)rest.size() >= kWideMin && h->use_prefill) {
+    std::vector<size_t> ro(rest.size());
+    std::vector<int32_t> rn(rest.size()), rs(rest.size());
+    for (size_t j = 0; j < rest.size(); ++j) {
+      ro[j] = offs[rest_i[j]];
+      rn[j] = n_rows[rest_i[j]];
+      rs[j] = start[rest_i[j]];
+    }
+    return wide_append(h, (int)rest.size(), rest.data(), feats, ro.data(), rn.data(), rs.data(), s);
+  }
   h->narrow = (int)rest.size() >= kNarrowSeqs && h->lanes.size() > 1;
   return run_lanes(h, (int)rest.size(), rest.data(), s, [&](int j, cudaStream_t ls) {
     const int i = rest_i[j];
@@ -1886,6 +2371,7 @@ fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const i
       return fail(h, FM_ERR_CONTEXT_FULL, "context full at pos %d", pos[i]);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (h->wide.on && !h->use_step && n_seqs >= kWideMin) return wide_draft(h, n_seqs, seq_ids, anchors, pos, tokens, s);
   h->narrow = !h->use_step && n_seqs >= kNarrowSeqs && h->lanes.size() > 1;
   if (h->use_step) {
     // the persistent step holds every SM: sequences draft one after another on the caller's stream
@@ -2101,10 +2587,13 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
       TRY(check_seq(h, seq));
       use_lane(h, seq);
       src = h->Y;
+      if (h->wide.on && h->wide.row_of[seq] >= 0) src = h->wide.Y + (size_t)h->wide.row_of[seq] * c.target_dim;
       size = (int64_t)c.block * c.target_dim * 4;
       break;
     case FM_DEBUG_LOGITS: {
       TRY(check_seq(h, seq));
+      if (h->wide.on && h->wide.row_of[seq] >= 0)
+        return fail(h, FM_ERR_UNSUPPORTED, "the logits of a batched draft are not kept");
       use_lane(h, seq);
       if (!h->dbg_logits) TRY(dalloc(h, &h->dbg_logits, (size_t)kMaxT * c.vocab));
       StepParams p{};
@@ -2238,6 +2727,12 @@ void fm_destroy(fm_handle *h) {
     if (L.done) cudaEventDestroy(L.done);
   }
   if (h->fork_ev) cudaEventDestroy(h->fork_ev);
+  if (h->wide.par_host) cudaFreeHost(h->wide.par_host);
+  if (h->wide.rows_host) cudaFreeHost(h->wide.rows_host);
+  for (int i = 0; i < kParamSlots; ++i) {
+    if (h->wide.par_ev[i]) cudaEventDestroy(h->wide.par_ev[i]);
+    if (h->wide.rows_ev[i]) cudaEventDestroy(h->wide.rows_ev[i]);
+  }
   delete h;
 }
 

@@ -31,6 +31,33 @@ struct StepParams {
   float thr[16];       // sequential head: pruning threshold of each position (NaN: none)
 };
 
+// --- batched draft: many sequences' slot rows through the tensor-core GEMM ---
+constexpr int kWideSeqs = 32;                  // sequences per batched pass
+constexpr int kWideRows = kWideSeqs * 16;      // slot rows per pass
+// Device-resident per-pass values of a batched draft (uploaded before the
+// chain, so a captured chain stays fixed while positions move).
+struct WideParams {
+  int32_t n;                     // sequences in this pass
+  int32_t pad[3];
+  int32_t *tokens;               // [n][block] the drafted tokens
+  int32_t seq[kWideSeqs];        // pass slot -> sequence id
+  int32_t anchor[kWideSeqs];     // pass slot -> anchor token
+  int32_t pos[kWideSeqs];        // pass slot -> anchor position (the context length before the draft)
+  // cross-attention launch slots, longest context first: pass slot, sequence, keys
+  int32_t z_call[kWideSeqs], z_seq[kWideSeqs], z_L[kWideSeqs];
+  int32_t kv_seq[kWideSeqs];     // anchor rows' K/V: sequence and position
+  int32_t kv_pos[kWideSeqs];
+  int32_t row_pos[kWideRows];    // draft row -> RoPE position (pos + 1 + slot)
+};
+cudaError_t launch_wide_prep(const float *h0, int D, int T, float *X, const WideParams *wp, int n_max,
+                             const __half *table, int H, __half *anc, int n_sm, cudaStream_t s);
+cudaError_t launch_wide_lnmod(const float *X, int D, int T, const float *scale, const float *shift, float eps,
+                              __half *out, cudaStream_t s);
+cudaError_t launch_wide_self_attn(const float *qkv, int D, int B, int n_seqs, int n_heads, __half *out, cudaStream_t s);
+cudaError_t launch_wide_argmax(const float2 *part, int n_blocks, int T, const WideParams *wp, cudaStream_t s);
+cudaError_t launch_q8_to_f16(const uint8_t *raw, int V, int H, int Vpad, __half *out, cudaStream_t s);
+cudaError_t launch_bf16_to_f16_pad(const __nv_bfloat16 *in, int V, int H, int Vpad, __half *out, cudaStream_t s);
+
 // --- the DFlash sequential logit head and confidence (k_seqhead.cu) ---------
 struct SeqArgs {
   const float *base;           // [T][V] base logits of the block
@@ -188,6 +215,16 @@ struct XAttnArgs {
   float2 *part_ml;         // [n_heads][splits][16] (reference m, row sum l)
   int32_t *tickets;        // [n_heads], zero between launches
   int32_t *err;
+  // Several sequences in one launch (grid z; null: one sequence, the fields
+  // above): launch slot z serves the call's sequence bz_call[z] (its query rows
+  // start at bz_call[z] * T_const) over the cache of sequence bz_seq[z], keys
+  // 0 .. bz_L[z]-1.  The maps then cover the whole cache, [seqs * layers * 2 *
+  // n_heads * max_ctx][128]: K rows of (sequence, layer) from
+  // ((seq * n_layers + layer) * 2) * n_heads * max_ctx, V rows n_heads * max_ctx
+  // further.  Partials, tickets and the output are per launch slot / call row.
+  const int32_t *bz_call, *bz_seq, *bz_L;
+  int32_t n_z, layer, n_layers;
+  __half *out16;           // f16 output [rows][ldo] instead of out (null: f32 out)
 };
 cudaError_t launch_xattn(const XAttnArgs &a, int stages, bool cluster, cudaStream_t st, bool pdl);
 size_t xattn_smem_bytes(int stages);

@@ -1,8 +1,11 @@
-// k_gemm.cu -- dense context-injection prefill on the 5th-generation tensor
-// cores: D[m][n] = sum_k A[m][k] B[n][k] with A the context rows (f16) and B a
-// weight matrix (f16 copy of the bf16 weights), both K-major.
+// k_gemm.cu -- dense products on the 5th-generation tensor cores:
+// D[m][n] = sum_k A[m][k] B[n][k] with A the activation rows (f16) and B a
+// weight matrix (f16 copy of the bf16 weights, or of the token table), both
+// K-major.  Two callers: the context-injection prefill (thousands of feature
+// rows) and the batched draft, where the slot rows of many sequences share
+// each weight read.
 //
-// The page runs this as a 16 x 16 tiled WGSL GEMM (flashmap_drafter.js,
+// The page runs these products as a 16 x 16 tiled WGSL GEMM (flashmap_drafter.js,
 // ``gemmBf16`` via ``runGemm`` for more than 17 rows).  Here it is a persistent,
 // warp-specialised sm_103a kernel:
 //   warp 0      one thread issues TMA (cp.async.bulk.tensor) loads of 128 x 64
@@ -15,11 +18,20 @@
 //   warps 2..5  read an accumulator with tcgen05.ld (one row per thread) while
 //               the next tile accumulates into the other buffer, and run the
 //               fused epilogue:
-//                 FC: C' = c * hidden_norm[n] -> f16 and per-row partial sum of
-//                     squares of c (the RMSNorm that follows fc);
-//                 KV: row scale 1/rms(c), per-head RMSNorm (k_norm) and
-//                     interleaved-pair RoPE on K heads, f16 stores into the
-//                     head-major caches of every layer at the row's position.
+//                 FC:     C' = (c + bias) * norm_w[n] -> f16 and per-row partial
+//                         sum of squares (the RMSNorm that follows fc);
+//                 KV:     row scale 1/rms(c), per-head RMSNorm (k_norm) and
+//                         interleaved-pair RoPE on K heads, f16 stores into the
+//                         head-major caches of every layer at the row's
+//                         sequence and position;
+//                 F16:    bias (+ exact GELU) -> f16, the next product's operand;
+//                 RESID:  X += gate * (c + bias), the gated residual;
+//                 SEGS:   per-head RMSNorm + RoPE of q / k heads, f32 out;
+//                 ARGMAX: per row, the largest logit of the tile (lowest index
+//                         on ties), for the lm_head.
+// Split-K: a tile's K blocks can be dealt to several CTAs; each stores its
+// partial tile to a workspace and the last to finish (atomic ticket) sums the
+// partials in slice order into its TMEM accumulator and runs the epilogue.
 // Every mbarrier wait is bounded by a clock budget; on expiry the kernel sets
 // an error flag, drains, frees its TMEM and returns.
 #include <cuda.h>
@@ -110,6 +122,10 @@ __device__ void epilogue_fc(const TcGemmArgs &a, uint32_t taddr, int row, int n0
     float v[32];
     tld32(taddr + c0, v);
     if (!live) continue;
+    if (a.bias) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] += __bfloat162float(a.bias[n0 + c0 + j]);
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       ss += v[j] * v[j];
@@ -133,7 +149,8 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
     for (int i = 0; i < a.in_st_n; ++i) s += __ldcg(a.in_st + (size_t)row * a.in_st_n + i);
     rs = rsqrtf(s * a.inv_n + a.eps);
   }
-  const int p = a.start + row;
+  const int p = a.row_pos ? (live ? a.row_pos[row] : 0) : a.start + row;
+  __half *cache = a.cache + (a.row_seq && live ? (size_t)a.row_seq[row] * a.seq_stride : 0);
   for (int h0 = 0; h0 < BN; h0 += hd) {
     const int head = ((n0 % a.seg_cols) + h0) / hd;
     float r2 = 1.f;
@@ -147,7 +164,7 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
       }
       r2 = rsqrtf(ss / (float)hd + a.qk_eps);
     }
-    __half *dst = a.cache + (size_t)(layer * 2 + kind) * a.plane + ((size_t)head * a.max_ctx + p) * hd;
+    __half *dst = cache + (size_t)(layer * 2 + kind) * a.plane + ((size_t)head * a.max_ctx + p) * hd;
     const __nv_bfloat16 *kw = a.kn_w + (size_t)layer * hd;
     for (int c0 = 0; c0 < hd; c0 += 32) {
       float v[32];
@@ -171,6 +188,158 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
       for (int j = 0; j < 32; j += 8) store_h8(dst + c0 + j, v + j);
     }
   }
+}
+
+__device__ __forceinline__ void store_f4(float *dst, const float *v) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+}
+
+__device__ void epilogue_f16(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
+  const bool live = row < a.M;
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    float v[32];
+    tld32(taddr + c0, v);
+    if (!live) continue;
+    if (a.bias) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] += __bfloat162float(a.bias[n0 + c0 + j]);
+    }
+    if (a.out32) store_f4(a.out32 + (size_t)row * a.ldo32 + n0 + c0, v);
+    if (a.gelu) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+    }
+    __half *dst = a.out16 + (size_t)row * a.ldo + n0 + c0;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) store_h8(dst + j, v + j);
+  }
+}
+
+__device__ void epilogue_resid(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
+  const bool live = row < a.M;
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    float v[32];
+    tld32(taddr + c0, v);
+    if (!live) continue;
+    float *x = a.X + (size_t)row * a.ldx + n0 + c0;
+    const float *g = a.gate + n0 + c0;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      float4 xv = *reinterpret_cast<const float4 *>(x + j);
+      const float4 gv = *reinterpret_cast<const float4 *>(g + j);
+      float b[4] = {0.f, 0.f, 0.f, 0.f};
+      if (a.bias) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) b[e] = __bfloat162float(a.bias[n0 + c0 + j + e]);
+      }
+      xv.x += gv.x * (v[j] + b[0]);
+      xv.y += gv.y * (v[j + 1] + b[1]);
+      xv.z += gv.z * (v[j + 2] + b[2]);
+      xv.w += gv.w * (v[j + 3] + b[3]);
+      *reinterpret_cast<float4 *>(x + j) = xv;
+    }
+  }
+}
+
+// q / k / v rows: segment s = n / seg_cols; segments 0 and 1 take a per-head
+// RMSNorm with their weight (when given) and RoPE at the row's position
+__device__ void epilogue_segs(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
+  const bool live = row < a.M;
+  const int seg = n0 / a.seg_cols;
+  const __nv_bfloat16 *nw = seg == 0 ? a.nw0 : seg == 1 ? a.nw1 : nullptr;
+  const int hd = a.hd;
+  const int p = live ? (a.row_pos ? a.row_pos[row] : a.start + row) : 0;
+  for (int h0 = 0; h0 < BN; h0 += hd) {
+    float r2 = 1.f;
+    if (nw) {
+      float ss = 0.f;
+      for (int c0 = 0; c0 < hd; c0 += 32) {
+        float v[32];
+        tld32(taddr + h0 + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ss += v[j] * v[j];
+      }
+      r2 = rsqrtf(ss / (float)hd + a.qk_eps);
+    }
+    for (int c0 = 0; c0 < hd; c0 += 32) {
+      float v[32];
+      tld32(taddr + h0 + c0, v);
+      if (!live) continue;
+      if (nw) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * __bfloat162float(nw[c0 + j]);
+        const float2 *rp = a.rope + (size_t)p * (hd >> 1) + (c0 >> 1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 cs = rp[i];
+          const float x0 = v[2 * i], x1 = v[2 * i + 1];
+          v[2 * i] = x0 * cs.x - x1 * cs.y;
+          v[2 * i + 1] = x1 * cs.x + x0 * cs.y;
+        }
+      }
+      store_f4(a.out32 + (size_t)row * a.ldo32 + n0 + h0 + c0, v);
+    }
+  }
+}
+
+__device__ void epilogue_argmax(const TcGemmArgs &a, uint32_t taddr, int row, int n0, int nb) {
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    float v[32];
+    tld32(taddr + c0, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)   // ascending columns, strict '>': the lowest index wins a tie
+      if (n0 + c0 + j < a.n_valid && v[j] > best) {
+        best = v[j];
+        bi = n0 + c0 + j;
+      }
+  }
+  if (row < a.M) a.amax[(size_t)row * a.amax_ld + nb] = make_float2(best, __int_as_float(bi));
+}
+
+// Split-K: store this slice's partial tile; the last slice of the tile to get
+// here sums every slice's partial (slice order) back into the accumulator.
+// Returns whether this CTA runs the tile's epilogue.  All 128 epilogue threads
+// call it together.
+__device__ bool splitk_gather(const TcGemmArgs &a, uint32_t taddr, int rl, int tile, int slice, int *s_last) {
+  const int ks = a.ksplit;
+  float *mine = a.ws + (((size_t)tile * ks + slice) * BM + rl) * BN;
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    float v[32];
+    tld32(taddr + c0, v);
+    store_f4(mine + c0, v);
+  }
+  named_sync(1, 128);
+  if (threadIdx.x == 64) {
+    __threadfence();
+    const int old = atomicAdd(a.tile_tickets + tile, 1);
+    const int last = old == ks - 1;
+    if (last) atomicExch(a.tile_tickets + tile, 0);
+    *s_last = last;
+  }
+  named_sync(1, 128);
+  if (!*s_last) return false;
+  __threadfence();
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    for (int s = 0; s < ks; ++s) {
+      const float *src = a.ws + (((size_t)tile * ks + s) * BM + rl) * BN + c0;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 q = __ldcg(reinterpret_cast<const float4 *>(src + j));
+        v[j] += q.x;
+        v[j + 1] += q.y;
+        v[j + 2] += q.z;
+        v[j + 3] += q.w;
+      }
+    }
+    tmem_st32(taddr + c0, v);
+  }
+  return true;
 }
 
 // tile -> (row block, column block) in the grouped order of TcGemmArgs::group_m
@@ -223,15 +392,22 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
   const int n_tiles = n_mb * n_nb;
   const int gm = a.group_m > 0 ? a.group_m : 1;
   const int nk = a.K / BK;
+  const int ks = a.ksplit > 1 ? a.ksplit : 1;
+  const int n_units = n_tiles * ks;   // unit u: tile u / ks, K slice u % ks (slices of a tile adjacent)
+  auto kslice = [&](int slice, int &kb0, int &kb1) {
+    kb0 = slice * nk / ks;
+    kb1 = (slice + 1) * nk / ks;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        int mb, nb;
-        tile_coords(tile, n_mb, n_nb, gm, mb, nb);
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int mb, nb, kb0, kb1;
+        tile_coords(u / ks, n_mb, n_nb, gm, mb, nb);
+        kslice(u % ks, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % ST;
           if (!mbar_wait(empty(s), ((it / ST) & 1) ^ 1, a.err)) { ok = false; break; }
           const uint32_t sa = base + s * STAGE, sb = sa + A_BYTES;
@@ -248,19 +424,22 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
     // issues each MMA and commit, and every wait's verdict is made warp-uniform
     uint32_t it = 0, tc = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++tc) {
       const int b = tc & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tempty(b), ((tc >> 1) & 1) ^ 1, a.err))) break;
       tc_fence_after();
       const uint32_t d = tmem + b * BN;
-      for (int kb = 0; kb < nk; ++kb, ++it) {
+      int kb0, kb1;
+      kslice(u % ks, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
         const int s = it % ST;
         if (!__all_sync(0xffffffffu, mbar_wait(full(s), (it / ST) & 1, a.err))) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = base + s * STAGE, sb = sa + A_BYTES;
         const uint64_t ad = sdesc(sa), bd = sdesc(sb);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) umma_ss_elect(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (kb | kk) ? 1u : 0u);
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_ss_elect(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (kb > kb0 || kk) ? 1u : 0u);
         umma_commit_elect(empty(s));
       }
       if (ok) umma_commit_elect(tfull(b));
@@ -268,18 +447,29 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
   } else {
     const int quad = warp & 3;  // TMEM lanes 32 * quad .. + 31 belong to this warp
     const int rl = quad * 32 + lane;
+    __shared__ int s_last;
     uint32_t tc = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tc) {
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++tc) {
       const int b = tc & 1;
-      if (!mbar_wait(tfull(b), (tc >> 1) & 1, a.err)) break;
+      const bool ok = mbar_wait(tfull(b), (tc >> 1) & 1, a.err);
+      // with K slices the group meets at named barriers: its verdict must be one
+      if (ks > 1 ? bar_any(1, 128, !ok) : !ok) break;
       tc_fence_after();
+      const int tile = u / ks;
       int mb, nb;
       tile_coords(tile, n_mb, n_nb, gm, mb, nb);
       const uint32_t taddr = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
-      if (a.epi == TC_EPI_FC)
-        epilogue_fc(a, taddr, mb * BM + rl, nb * BN, nb);
-      else
-        epilogue_kv(a, taddr, mb * BM + rl, nb * BN);
+      const int row = mb * BM + rl;
+      if (ks == 1 || splitk_gather(a, taddr, rl, tile, u % ks, &s_last)) {
+        switch (a.epi) {
+          case TC_EPI_FC: epilogue_fc(a, taddr, row, nb * BN, nb); break;
+          case TC_EPI_KV: epilogue_kv(a, taddr, row, nb * BN); break;
+          case TC_EPI_F16: epilogue_f16(a, taddr, row, nb * BN); break;
+          case TC_EPI_RESID: epilogue_resid(a, taddr, row, nb * BN); break;
+          case TC_EPI_SEGS: epilogue_segs(a, taddr, row, nb * BN); break;
+          default: epilogue_argmax(a, taddr, row, nb * BN, nb); break;
+        }
+      }
       tc_fence_before();
       mbar_arrive(tempty(b));
     }
@@ -342,8 +532,11 @@ bool make_tma_f16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t col
 size_t tc_gemm_smem_bytes() { return (size_t)ST * STAGE + 1024 + 256; }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs &a, int n_sm, cudaStream_t s) {
-  const int n_tiles = ((a.M + BM - 1) / BM) * (a.N / BN);
-  const int grid = n_tiles < n_sm ? n_tiles : n_sm;
+  if (a.N % BN != 0 || a.K % BK != 0 || a.M < 1) return cudaErrorInvalidValue;
+  const int ks = a.ksplit > 1 ? a.ksplit : 1;
+  if (ks > a.K / BK || (ks > 1 && (!a.ws || !a.tile_tickets))) return cudaErrorInvalidValue;
+  const int n_units = ((a.M + BM - 1) / BM) * (a.N / BN) * ks;
+  const int grid = n_units < n_sm ? n_units : n_sm;
   const size_t smem = tc_gemm_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(fm_prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -26,6 +26,8 @@
 //               rescale-when-needed scheme of FlashAttention-4).
 // Each CTA stores its unnormalised O, m and row sums; the last CTA of a head
 // (atomic ticket) merges the ranges in order (deterministic) and writes O / l.
+// A batched draft runs every sequence of the call in one launch (grid z), each
+// over its own cache and context length, writing f16 rows for the next product.
 // Every mbarrier wait is bounded; on expiry the kernel raises the error word,
 // drains its copies and MMAs, frees its TMEM and returns.
 #include <cooperative_groups.h>
@@ -67,29 +69,6 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t lbo, 
   return d;
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&f)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
-      "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]), "f"(f[8]), "f"(f[9]),
-      "f"(f[10]), "f"(f[11]), "f"(f[12]), "f"(f[13]), "f"(f[14]), "f"(f[15]), "f"(f[16]), "f"(f[17]), "f"(f[18]),
-      "f"(f[19]), "f"(f[20]), "f"(f[21]), "f"(f[22]), "f"(f[23]), "f"(f[24]), "f"(f[25]), "f"(f[26]), "f"(f[27]),
-      "f"(f[28]), "f"(f[29]), "f"(f[30]), "f"(f[31])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-}
-
-// OR of a predicate over the `n` threads that meet at named barrier `id`
-__device__ __forceinline__ bool bar_any(int id, int n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 // byte offset of element (row, col) of a 32-row B operand, 64-column chunks 4 KB apart
 __device__ __forceinline__ uint32_t b_slot(int row, int col) { return (uint32_t)(col >> 6) * kQB + sw128(row, col & 63); }
 
@@ -98,7 +77,7 @@ __device__ __forceinline__ uint32_t b_slot(int row, int col) { return (uint32_t)
 // thread and 16 / PT ranges per batch, so that 16 loads are in flight at a time.
 template <int PT>
 __device__ __forceinline__ void merge_ranges(const float *ho, const float *sw, int ns, int items, int i, float *out,
-                                             int ldo, int head) {
+                                             __half *out16, int ldo, int head) {
   constexpr int RB = 16 / PT;
   float4 acc[PT];
 #pragma unroll
@@ -129,7 +108,17 @@ __device__ __forceinline__ void merge_ranges(const float *ho, const float *sw, i
 #pragma unroll
   for (int q = 0; q < PT; ++q) {
     const int itm = i + 128 * q;
-    if (itm < items) *reinterpret_cast<float4 *>(out + (size_t)(itm / 32) * ldo + head * HD + 4 * (itm % 32)) = acc[q];
+    if (itm >= items) continue;
+    const size_t o = (size_t)(itm / 32) * ldo + head * HD + 4 * (itm % 32);
+    if (out16) {
+      const __half2 h01 = __floats2half2_rn(acc[q].x, acc[q].y), h23 = __floats2half2_rn(acc[q].z, acc[q].w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t *>(&h01);
+      pk.y = *reinterpret_cast<const uint32_t *>(&h23);
+      *reinterpret_cast<uint2 *>(out16 + o) = pk;
+    } else {
+      *reinterpret_cast<float4 *>(out + o) = acc[q];
+    }
   }
 }
 
@@ -161,16 +150,24 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
   const uint32_t qfull = b2 + 64, odone = b2 + 72, tslot = b2 + 80;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x, split = blockIdx.y, ns = gridDim.y;
+  const bool batch = a.bz_call != nullptr;
+  const int z = blockIdx.z;
 
   // the per-call values were uploaded before the chain started
-  const int L = (a.L_src == 0 ? a.sp->L : a.sp->pos + 1) + a.L_add;
+  const int L = batch ? a.bz_L[z] : (a.L_src == 0 ? a.sp->L : a.sp->pos + 1) + a.L_add;
+  // this launch slot's query / output rows, partials and ticket
+  const int qrow0 = batch ? a.bz_call[z] * a.T_const : 0;
+  const size_t zslot = batch ? (size_t)z * a.n_heads + head : (size_t)head;
   // whole 128-key tiles dealt out evenly: range r takes tiles [tb, tb + ntiles)
   const int ntot = (L + kTileKeys - 1) / kTileKeys;
   const int tq = ntot / ns, trem = ntot - tq * ns;
   const int tb = split * tq + min(split, trem);
   const int ntiles = tq + (split < trem ? 1 : 0);
   const int kbeg = min(L, tb * kTileKeys), kend = min(L, (tb + ntiles) * kTileKeys);
-  const int row0 = head * a.max_ctx + kbeg;          // tensor-map row of this range's first key
+  // tensor-map rows of this range's first key (K) and the V plane's offset from it
+  const int kv_base = batch ? ((a.bz_seq[z] * a.n_layers + a.layer) * 2) * a.n_heads * a.max_ctx : 0;
+  const int row0 = kv_base + head * a.max_ctx + kbeg;
+  const int voff = batch ? a.n_heads * a.max_ctx : 0;
 
   pdl_trigger();
   if (threadIdx.x == 0) {
@@ -202,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
   if (warp == 0) {
     if (lane == 0) {
       // tiles below `stable` (rows no kernel of this call writes) go before griddepcontrol.wait
-      const int stable = a.sp->stable;
+      const int stable = batch ? 0 : a.sp->stable;
       // K runs one tile ahead of V (the MMA warp issues QK(t + 1) before P.V(t)); each ring
       // slot is refilled as soon as the MMAs that read it have completed
       auto load_k = [&](int t) -> bool {
@@ -217,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
         const int s = t % kNS;
         if (!mbar_wait_bounded(vempty(s), ((t / kNS) & 1) ^ 1, a.err)) return false;
         mbar_expect_tx(vfull(s), kKV);
-        tma_2d(vring + s * kKV, &a.tm_v, 0, row0 + t * kTileKeys, vfull(s));
-        tma_2d(vring + s * kKV + kBox, &a.tm_v, 64, row0 + t * kTileKeys, vfull(s));
+        tma_2d(vring + s * kKV, &a.tm_v, 0, row0 + voff + t * kTileKeys, vfull(s));
+        tma_2d(vring + s * kKV + kBox, &a.tm_v, 64, row0 + voff + t * kTileKeys, vfull(s));
         return true;
       };
       int nk = 0, nv = 0;
@@ -301,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
       const int n = i >> 3, d0 = (i & 7) * 16;
       float x[16];
       if (n < T) {
-        const float4 *src = reinterpret_cast<const float4 *>(a.Q + (size_t)n * a.ldq + head * HD + d0);
+        const float4 *src = reinterpret_cast<const float4 *>(a.Q + (size_t)(qrow0 + n) * a.ldq + head * HD + d0);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const float4 v = __ldcg(src + u);
@@ -432,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
           cml[n] = make_float2(ntiles ? m_ref[n] : -INFINITY, ntiles ? l : 0.f);
         }
     } else {
-      float *po = a.part_o + ((size_t)head * ns + split) * 16 * HD;
-      float2 *pml = a.part_ml + ((size_t)head * ns + split) * 16;
+      float *po = a.part_o + (zslot * ns + split) * 16 * HD;
+      float2 *pml = a.part_ml + (zslot * ns + split) * 16;
 #pragma unroll
       for (int n = 0; n < 16; ++n)
         if (n < T) po[n * HD + j] = ntiles ? o[n] + o[16 + n] : 0.f;
@@ -448,9 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
       __shared__ int last;
       if (i == 0) {
         __threadfence();
-        const int old = atomicAdd(a.tickets + head, 1);
+        const int old = atomicAdd(a.tickets + zslot, 1);
         const bool is_last = old == ns - 1;
-        if (is_last) atomicExch(a.tickets + head, 0);
+        if (is_last) atomicExch(a.tickets + zslot, 0);
         last = is_last && !*reinterpret_cast<volatile int32_t *>(a.err);   // one verdict for the group
         if (last) __threadfence();
       }
@@ -458,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
       if (last) {
         // merge the ranges in order: O[t] = sum_r w_r O_r, w_r = 2^(m_r - M) / sum_r' 2^(m_r' - M) l_r'.
         // The K ring is free: it holds the (m, l) pairs and the weights.
-        const float *ho = a.part_o + (size_t)head * ns * 16 * HD;
-        const float2 *hml = a.part_ml + (size_t)head * ns * 16;
+        const float *ho = a.part_o + zslot * ns * 16 * HD;
+        const float2 *hml = a.part_ml + zslot * ns * 16;
         float2 *sml = reinterpret_cast<float2 *>(gbase);
         float *sw = reinterpret_cast<float *>(gbase + kMaxXSplits * 16 * sizeof(float2));
         for (int idx = i; idx < ns * 16; idx += 128) sml[idx] = __ldcg(hml + idx);
@@ -480,11 +477,13 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
         named_sync(1, 128);
         // items (query n, 4 dims): T * 32 of them over the group's 128 threads
         const int items = T * (HD / 4);
+        float *out = a.out16 ? nullptr : a.out + (size_t)qrow0 * a.ldo;
+        __half *out16 = a.out16 ? a.out16 + (size_t)qrow0 * a.ldo : nullptr;
         switch ((items + 127) / 128) {
-          case 1: merge_ranges<1>(ho, sw, ns, items, i, a.out, a.ldo, head); break;
-          case 2: merge_ranges<2>(ho, sw, ns, items, i, a.out, a.ldo, head); break;
-          case 3: merge_ranges<3>(ho, sw, ns, items, i, a.out, a.ldo, head); break;
-          default: merge_ranges<4>(ho, sw, ns, items, i, a.out, a.ldo, head); break;
+          case 1: merge_ranges<1>(ho, sw, ns, items, i, out, out16, a.ldo, head); break;
+          case 2: merge_ranges<2>(ho, sw, ns, items, i, out, out16, a.ldo, head); break;
+          case 3: merge_ranges<3>(ho, sw, ns, items, i, out, out16, a.ldo, head); break;
+          default: merge_ranges<4>(ho, sw, ns, items, i, out, out16, a.ldo, head); break;
         }
       }
     }
@@ -545,6 +544,10 @@ size_t xattn_smem_bytes(int stages) { return 1024 + 2 * (size_t)stages * kKV + 2
 cudaError_t launch_xattn(const XAttnArgs &a, int stages, bool cluster, cudaStream_t st, bool pdl) {
   if (a.splits < 1 || a.splits > kMaxXSplits || (stages != 1 && stages != 3) || (cluster && a.splits > 16))
     return cudaErrorInvalidValue;
+  // several sequences per launch: ticket merge only, one query row block per sequence
+  const int nz = a.bz_call ? a.n_z : 1;
+  if (a.bz_call && (cluster || nz < 1 || !a.bz_seq || !a.bz_L || a.T_const < 1 || a.T_const > 16))
+    return cudaErrorInvalidValue;
   const size_t smem = xattn_smem_bytes(stages);
   auto kern = cluster ? (stages == 1 ? fm_xattn_kernel<1, true> : fm_xattn_kernel<3, true>)
                       : (stages == 1 ? fm_xattn_kernel<1, false> : fm_xattn_kernel<3, false>);
@@ -555,7 +558,7 @@ cudaError_t launch_xattn(const XAttnArgs &a, int stages, bool cluster, cudaStrea
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_heads, a.splits, 1);
+  cfg.gridDim = dim3(a.n_heads, a.splits, nz);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

@@ -1,4 +1,6 @@
-// tc_gemm.h -- argument block of the tcgen05 prefill GEMM (k_gemm.cu).
+// tc_gemm.h -- argument block of the tcgen05 GEMM (k_gemm.cu): the dense
+// context prefill and the products of a batched draft (many sequences' slot
+// rows sharing each weight read).
 #pragma once
 
 #include <cuda.h>
@@ -9,8 +11,12 @@
 namespace fm {
 
 enum TcEpi : int32_t {
-  TC_EPI_FC = 0,  // C' = c * colw[n] (f16) and per-row partial sum of c^2 per 256-column block
-  TC_EPI_KV = 1,  // row scale 1/rms, k_norm + RoPE on K heads, f16 stores into the head-major caches
+  TC_EPI_FC = 0,      // c = acc (+ bias); C' = c * colw[n] (f16) and per-row partial sum of c^2 per 256 columns
+  TC_EPI_KV = 1,      // row scale 1/rms, k_norm + RoPE on K heads, f16 stores into the head-major caches
+  TC_EPI_F16 = 2,     // out16 = f16(act(acc + bias)), act = identity or exact GELU; optionally out32 = acc + bias
+  TC_EPI_RESID = 3,   // X[row][n] += gate[n] * (acc + bias[n])   (gated residual, f32 in place)
+  TC_EPI_SEGS = 4,    // out32: per-head RMSNorm + interleaved-pair RoPE on segments 0 / 1, plain elsewhere
+  TC_EPI_ARGMAX = 5,  // per row, the best (value, lowest index) over the tile's columns < n_valid
 };
 
 struct TcGemmArgs {
@@ -23,6 +29,13 @@ struct TcGemmArgs {
   // group's A panel stays in L2 (1: the column block runs fastest)
   int32_t group_m;
   int32_t *err;       // set to 1 when a bounded wait gives up
+  // split-K: each output tile is computed as ksplit slices of the K blocks; a
+  // slice stores its partial tile into ws and takes a ticket, and the last
+  // slice to finish sums the partials in slice order (deterministic) and runs
+  // the epilogue.  ksplit 1: no workspace.
+  int32_t ksplit;
+  float *ws;                  // [tiles][ksplit][128][256]
+  int32_t *tile_tickets;      // [tiles], zero between launches
   // FC
   const __nv_bfloat16 *colw;
   __half *out16;
@@ -33,17 +46,38 @@ struct TcGemmArgs {
   const float *in_st; // [M][in_st_n] partial sums of squares of the fc output
   int32_t in_st_n;
   float eps, inv_n;
-  int32_t seg_cols;   // columns per K or V segment (= D)
+  int32_t seg_cols;   // columns per K or V segment (= D); SEGS: columns per segment
   int32_t hd, max_ctx, start;
   const float2 *rope;
   float qk_eps;
   const __nv_bfloat16 *kn_w;  // [layers][hd]
   __half *cache;              // [layers][2][n_heads][max_ctx][hd] of one sequence
   size_t plane;               // elements of one [n_heads][max_ctx][hd] plane
+  // per-row targets (KV, SEGS): position of row r = row_pos[r] (null: start + r);
+  // KV: cache of row r = cache + row_seq[r] * seq_stride (null: cache)
+  const int32_t *row_pos;
+  const int32_t *row_seq;
+  size_t seq_stride;
+  // F16 / RESID / FC
+  const __nv_bfloat16 *bias;  // [N] or null
+  int32_t gelu;
+  float *X;                   // RESID: [M][ldx]
+  const float *gate;          // RESID: [N]
+  int32_t ldx;
+  // SEGS (and F16's optional f32 copy)
+  float *out32;
+  int32_t ldo32;
+  const __nv_bfloat16 *nw0, *nw1;  // per-head norm weights [hd] of segments 0 and 1 (null: plain)
+  // ARGMAX
+  float2 *amax;               // [M][amax_ld]: (best value, index bits) per row and column block
+  int32_t amax_ld;
+  int32_t n_valid;            // columns < n_valid take part
 };
 
 bool make_tma_f16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 size_t tc_gemm_smem_bytes();
+// column blocks of 256 (N must be a multiple of 256), row blocks of 128
+inline int tc_gemm_tiles(int M, int N) { return ((M + 127) / 128) * (N / 256); }
 cudaError_t launch_tc_gemm(const TcGemmArgs &a, int n_sm, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float *in, __half *out, size_t n, int n_sm, cudaStream_t s);
 cudaError_t launch_bf16_to_f16(const __nv_bfloat16 *in, __half *out, size_t n, cudaStream_t s);

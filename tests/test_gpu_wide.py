@@ -1,0 +1,241 @@
+"""GPU parity of the batched draft: the 16 slot rows of every sequence in a
+call go through each product as one tensor-core GEMM (flashmap_drafter.js
+``draft`` per anchor; the page hands products above 17 rows to ``runGemm``),
+and the cross-attention serves every sequence's own cache in one launch.
+Each sequence is checked against the oracle run on its own: the head output
+within the relative-L2 bar, the tokens exactly unless the oracle's top-2
+margin is below 1e-3, the batched K/V appends through the cache rows, and the
+device acceptance bit-exactly."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import fm_synth as S
+from gpu_common import REL_L2, Pair, rel_l2, tokens_match
+from oracle.accept import accept
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_speculative_decoding_fm_gb300 import build
+    build.build()
+
+
+def mid_config(max_seqs: int, max_ctx: int = 400, lm: int = S.LM_Q8_0) -> S.DrafterConfig:
+    """FlashMap-shaped, head dim 128 (the batched path's attention), small
+    enough for the oracle: D 512, 4 heads, 2 layers, ff 1024, target dim 256,
+    2 taps, vocab 4096."""
+    return S.DrafterConfig(S.VARIANT_FLASHMAP, dim=512, n_heads=4, head_dim=128, n_layers=2, ff_dim=1024, block=16,
+                           target_dim=256, n_taps=2, vocab=4096, lm_format=lm, max_ctx=max_ctx, max_seqs=max_seqs)
+
+
+def wide_launches(cfg, passes):
+    return passes * (3 + 11 * cfg.n_layers + 4)
+
+
+def head_out(p, seq):
+    import block_speculative_decoding_fm_gb300 as fm
+    c = p.cfg
+    buf = np.empty((c.block, c.target_dim), np.float32)
+    fm.fm_debug_copy(p.h, fm.FM_DEBUG_HEAD_OUT, seq, 0, buf)
+    return buf
+
+
+def batched_draft(p, ids, anchors, pos):
+    import torch
+    import block_speculative_decoding_fm_gb300 as fm
+    tok = torch.full((len(ids), p.cfg.block), -1, dtype=torch.int32, device="cuda")
+    fm.fm_draft(p.h, ids, anchors, pos, tok)
+    torch.cuda.synchronize()
+    return tok.cpu().numpy()
+
+
+def check_seq(p, seq, got_tokens, anchor, pos):
+    """One sequence of a batched draft against the oracle's own draft of it."""
+    ref = p.oracle.draft(p.state(seq), anchor, pos)
+    y = head_out(p, seq)
+    assert rel_l2(y, ref.head_out) < REL_L2, (seq, rel_l2(y, ref.head_out))
+    assert tokens_match(got_tokens, ref.tokens, ref.logits), (seq, got_tokens, ref.tokens)
+    return ref
+
+
+def cache_rows_match(p, seq, lo, hi):
+    """Cache rows [lo, hi) of every layer against the oracle's f16 rows."""
+    st = p.state(seq)
+    for l in range(p.cfg.n_layers):
+        for which, ref in (("k", st.k[l]), ("v", st.v[l])):
+            got = p.cache(seq, l, which)[lo:hi]
+            assert rel_l2(got, ref[lo:hi]) < 1e-3, (seq, l, which, rel_l2(got, ref[lo:hi]))
+
+
+@pytest.mark.parametrize("lm", [S.LM_Q8_0, S.LM_BF16])
+def test_batched_cycles_match_oracle(lm):
+    """Six sequences with ragged contexts (1 .. 255 rows: several key tiles and
+    ragged tails), two draft / accept cycles: a batched append of acc + 1 rows
+    per sequence (0 and 16 accepted included), a batched draft, device
+    acceptance against seeded targets."""
+    import torch
+    import block_speculative_decoding_fm_gb300 as fm
+    cfg = mid_config(6, lm=lm)
+    p = Pair(cfg, 1401, keep_hidden=False)
+    fr = S.streams(1401)["features"]
+    tr = S.streams(1401)["tokens"]
+    lens = [1, 37, 128, 129, 200, 255]
+    for s, n in enumerate(lens):
+        p.append(s, S.gen_features(fr, n, cfg.feat_dim), 0)
+    ids = [3, 0, 5, 1, 4, 2]                   # call order differs from the sequence ids
+    length = list(lens)
+    acc = [0, 16, 5, 0, 9, 2]                  # accepted last cycle, per call slot
+    anchors = [int(tr.integers(0, cfg.vocab)) for _ in ids]
+    for cycle in range(2):
+        n_new = [a + 1 for a in acc]
+        rows = [S.gen_features(fr, n, cfg.feat_dim) for n in n_new]
+        fm.fm_context_append_batched(p.h, ids, torch.from_numpy(np.concatenate(rows)).cuda(), n_new,
+                                     [length[s] for s in ids])
+        for j, s in enumerate(ids):
+            p.oracle.context_append(p.state(s), rows[j], length[s])
+            length[s] += n_new[j]
+        for j, s in enumerate(ids):
+            cache_rows_match(p, s, length[s] - n_new[j], length[s])
+        pos = [length[s] for s in ids]
+        got = batched_draft(p, ids, anchors, pos)
+        # one batched pass: prep, anchor_proj, anchor K/V; per layer 11 launches; final adaLN, head,
+        # lm_head, row argmax (a per-sequence chain would launch several times as many)
+        assert fm.fm_last_launch_count(p.h) == wide_launches(cfg, 1)
+        drafts_ok, targets = [], []
+        for j, s in enumerate(ids):
+            ref = check_seq(p, s, got[j], anchors[j], pos[j])
+            drafts_ok.append(bool(np.all(got[j] == ref.tokens)))
+            # targets: the oracle's draft with one seeded flip (or none), plus a bonus token
+            t = np.append(ref.tokens, int(tr.integers(0, cfg.vocab))).astype(np.int32)
+            flip = int(tr.integers(0, cfg.block + 1))
+            if flip < cfg.block:
+                t[flip] = (t[flip] + 1) % cfg.vocab
+            targets.append(t)
+        # device acceptance against the oracle's rule
+        k = torch.full((len(ids),), cfg.block, dtype=torch.int32, device="cuda")
+        a_dev = torch.zeros((len(ids),), dtype=torch.int32, device="cuda")
+        b_dev = torch.zeros((len(ids),), dtype=torch.int32, device="cuda")
+        fm.fm_accept_batched(p.h, torch.from_numpy(got).cuda(), torch.from_numpy(np.stack(targets)).cuda(), k,
+                             a_dev, b_dev)
+        torch.cuda.synchronize()
+        a_dev, b_dev = a_dev.cpu().numpy(), b_dev.cpu().numpy()
+        for j in range(len(ids)):
+            if drafts_ok[j]:
+                assert (int(a_dev[j]), int(b_dev[j])) == accept(got[j], targets[j], cfg.block)
+        acc = [int(a) for a in a_dev]
+        anchors = [int(b) for b in b_dev]
+    p.close()
+
+
+def test_batched_draft_in_passes():
+    """34 sequences: two batched passes (32 + 2 sequences) in one call, short
+    contexts; every sequence's tokens and head output against the oracle."""
+    import block_speculative_decoding_fm_gb300 as fm
+    cfg = mid_config(34, max_ctx=160)
+    p = Pair(cfg, 1402, keep_hidden=False)
+    fr = S.streams(1402)["features"]
+    rng = S.streams(1402)["workload"]
+    lens = [int(x) for x in rng.integers(1, 60, size=34)]
+    for s, n in enumerate(lens):
+        p.append(s, S.gen_features(fr, n, cfg.feat_dim), 0)
+    ids = list(range(34))[::-1]
+    anchors = [int(x) for x in rng.integers(0, cfg.vocab, size=34)]
+    pos = [lens[s] for s in ids]
+    got = batched_draft(p, ids, anchors, pos)
+    assert fm.fm_last_launch_count(p.h) == wide_launches(cfg, 2)
+    for j, s in enumerate(ids):
+        # only the last pass keeps its head output
+        if j >= 32:
+            check_seq(p, s, got[j], anchors[j], pos[j])
+        else:
+            ref = p.oracle.draft(p.state(s), anchors[j], pos[j])
+            assert tokens_match(got[j], ref.tokens, ref.logits), (s, got[j], ref.tokens)
+    p.close()
+
+
+def test_batched_argmax_ties_go_to_the_lowest_index():
+    """Every odd table row copies the even row before it: the lm_head GEMM's
+    per-tile best and the row reduction must both keep the even index."""
+    def pairs(w):
+        t = w["token_embd.weight"]
+        t.data = t.data.copy()
+        t.data[1::2] = t.data[0::2]
+    cfg = mid_config(4, max_ctx=160)
+    p = Pair(cfg, 1403, keep_hidden=False, edit=pairs)
+    fr = S.streams(1403)["features"]
+    lens = [20, 50, 3, 90]
+    for s, n in enumerate(lens):
+        p.append(s, S.gen_features(fr, n, cfg.feat_dim), 0)
+    got = batched_draft(p, [0, 1, 2, 3], [2, 4, 6, 8], lens)
+    assert np.all(got % 2 == 0), got
+    for s in range(4):
+        check_seq(p, s, got[s], [2, 4, 6, 8][s], lens[s])
+    p.close()
+
+
+def test_batched_full_shape_sampled():
+    """The 32-sequence FlashMap-4B workload as the bench times it: contexts
+    U[512, 8192] prefilled, a batched append of acc + 1 rows (acc ~ U{0..16}),
+    a batched draft of all 32 sequences.  The oracle runs the shortest and the
+    longest sequence (their contexts built from the same seeded rows); every
+    sequence's device acceptance equals the host rule."""
+    import torch
+    import block_speculative_decoding_fm_gb300 as fm
+    n_seqs = 32
+    cfg = S.flashmap_4b_config(max_ctx=8192 + 17 + 64, max_seqs=n_seqs)
+    rng = S.streams(1404)["workload"]
+    L = [int(x) for x in S.batched_lengths(rng, n_seqs)]
+    n_new = [int(x) + 1 for x in rng.integers(0, 17, size=n_seqs)]
+    anchors = [int(x) for x in rng.integers(0, cfg.vocab, size=n_seqs)]
+    sample = sorted({int(np.argmin(L)), int(np.argmax(L))})
+    p = Pair(cfg, 1404, oracle_max_ctx=8192 + 17 + 64, keep_hidden=False)
+    fr = S.streams(1404)["features"]
+    # the sampled sequences' contexts come from the seeded host stream (the oracle needs them);
+    # the others are drawn on the device from a seeded generator
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1404)
+    ctx_rows, new_rows = {}, []
+    for s in range(n_seqs):
+        if s in sample:
+            ctx_rows[s] = S.gen_features(fr, L[s], cfg.feat_dim)
+            p.append(s, ctx_rows[s], 0, oracle=False)
+        else:
+            f = torch.randn((L[s], cfg.feat_dim), generator=g, device="cuda")
+            fm.fm_context_append(p.h, s, f, L[s], 0)
+            del f
+    for s in range(n_seqs):
+        new_rows.append(S.gen_features(fr, n_new[s], cfg.feat_dim))
+    ids = list(range(n_seqs))
+    fm.fm_context_append_batched(p.h, ids, torch.from_numpy(np.concatenate(new_rows)).cuda(), n_new, L)
+    pos = [L[s] + n_new[s] for s in ids]
+    got = batched_draft(p, ids, anchors, pos)
+    assert np.all((got >= 0) & (got < cfg.vocab))
+    for s in sample:
+        st = p.state(s)
+        p.oracle.context_append(st, ctx_rows[s], 0)
+        p.oracle.context_append(st, new_rows[s], L[s])
+        cache_rows_match(p, s, L[s], pos[s])
+        check_seq(p, s, got[s], anchors[s], pos[s])
+    # device acceptance of every sequence against the host rule (fm_accept)
+    tr = S.streams(1404)["tokens"]
+    targets = np.stack([np.append(got[s], int(tr.integers(0, cfg.vocab))) for s in ids]).astype(np.int32)
+    flips = tr.integers(0, cfg.block + 1, size=n_seqs)
+    for s in ids:
+        if flips[s] < cfg.block:
+            targets[s, flips[s]] = (targets[s, flips[s]] + 1) % cfg.vocab
+    k = torch.full((n_seqs,), cfg.block, dtype=torch.int32, device="cuda")
+    a_dev = torch.zeros((n_seqs,), dtype=torch.int32, device="cuda")
+    b_dev = torch.zeros((n_seqs,), dtype=torch.int32, device="cuda")
+    fm.fm_accept_batched(p.h, torch.from_numpy(got).cuda(), torch.from_numpy(targets).cuda(), k, a_dev, b_dev)
+    torch.cuda.synchronize()
+    for s in ids:
+        assert (int(a_dev[s]), int(b_dev[s])) == fm.fm_accept(got[s], targets[s], cfg.block)
+        assert (int(a_dev[s]), int(b_dev[s])) == accept(got[s], targets[s], cfg.block)
+    p.close()
