@@ -63,7 +63,8 @@ def peaks():
 # kernel tag (as fm_profile_read names it) -> the source file that defines it
 KERNEL_SOURCES = {"lm_head": ("k_lmhead.cu",), "attn": ("k_attn.cu",), "gemv": ("k_gemv.cu", "linear_parts.cuh"),
                   "seq": ("k_seqhead.cu",), "draft_step": ("k_step.cu", "linear_parts.cuh"),
-                  "prefill": ("k_gemm.cu", "tc_gemm.h")}
+                  "prefill": ("k_gemm.cu", "tc_gemm.h"), "append": ("k_gemm.cu", "tc_gemm.h"),
+                  "wide": ("k_gemm.cu", "tc_gemm.h", "k_wide.cu", "k_xattn.cu")}
 
 
 def source_digest(tag):
@@ -440,6 +441,22 @@ def hbm_roofline(prof, hbm, peak_src, steps):
         {k: {"launches": v[0] / steps, "ms_per_step": v[1] / steps} for k, v in sorted(prof.items())}
 
 
+def dominant_roofline(prof, hbm, bf16_sustained, peak_src, steps):
+    """The kernel with the largest device time per step against its own bound:
+    the tensor-core GEMMs (names holding "gemm", whose records carry FLOPs)
+    against the sustained bf16 peak (timed inside a long step), the rest
+    against the HBM copy peak."""
+    name, (nl, tms, tq) = max(prof.items(), key=lambda kv: kv[1][1])
+    kernels = {k: {"launches": v[0] / steps, "ms_per_step": v[1] / steps} for k, v in sorted(prof.items())}
+    if "gemm" not in name:
+        return hbm_roofline(prof, hbm, peak_src, steps)[0], kernels
+    achieved = (tq / nl) / ((tms / nl) / 1000) / 1e12
+    return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": bf16_sustained, "unit": "TFLOP/s",
+            "frac": achieved / bf16_sustained, "traffic": ncu_traffic(name),
+            "peak_source": f"{peak_src} bf16 sustained (f16 has the same nominal tensor rate)",
+            "flops_per_launch": tq / nl, "ms_per_launch": tms / nl}, kernels
+
+
 def oracle_sample(fn, budget_s=15.0, most=20):
     """Run fn() until the budget or `most` repetitions; (repetitions, seconds)."""
     n, t0 = 0, time.perf_counter()
@@ -459,7 +476,7 @@ def run_workload(args):
     build.build()
     import block_speculative_decoding_fm_gb300 as fm
     import fm_synth as S
-    hbm, bf16, _, peak_src = peaks()
+    hbm, bf16, bf16s, peak_src = peaks()
     cores = len(os.sched_getaffinity(0))
     extra, unit, value, ms, launches = {}, "steps/s", None, None, 0
     roofline, kernels, cpu, e2e = None, None, None, None
@@ -545,9 +562,20 @@ def run_workload(args):
                     "flops_per_launch": flops / max(1, sum(v[0] for _, v in gemm)),
                     "ms_per_launch": gms / max(1, sum(v[0] for _, v in gemm))}
         kernels = {k: {"launches": v[0] / 3, "ms_per_step": v[1] / 3} for k, v in sorted(prof.items())}
-    elif args.workload in ("mtp", "batched"):
-        # mtp: the head's launches are not profiled one by one; batched: the sequences' chains run
-        # concurrently, so a launch's events also span its neighbours' work.  The roofline of the whole step.
+    elif args.workload == "batched":
+        # the batched pass is one serial chain: per-kernel events; the dominant kernel against its own bound
+        prof = kernel_profile(fm, w.h, w.step, 5)
+        roofline, kernels = dominant_roofline(prof, hbm, bf16s or bf16, peak_src, 5)
+        gemm = [v for k, v in prof.items() if "gemm" in k]
+        if gemm:
+            extra["gemm_tflops"] = sum(v[2] for v in gemm) / (sum(v[1] for v in gemm) / 1000) / 1e12
+            extra["gemm_ms_per_step"] = sum(v[1] for v in gemm) / 5
+        if "wide.attn_cross" in prof:
+            v = prof["wide.attn_cross"]
+            extra["attn_cross_gbs"] = v[2] / (v[1] / 1000) / 1e9
+            extra["attn_cross_ms_per_step"] = v[1] / 5
+    elif args.workload == "mtp":
+        # the head's launches are not profiled one by one: the roofline of the whole step
         achieved = extra["achieved_hbm_gbs"]
         roofline = {"bound": "hbm", "kernel": f"{w.name} (every launch of the step)", "achieved": achieved,
                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,

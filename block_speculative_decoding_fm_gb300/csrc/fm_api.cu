@@ -139,6 +139,7 @@ struct fm_handle {
     float2 *xml = nullptr;
     int32_t *xtickets = nullptr;
     int xsplits = 2;                // key ranges per (sequence, head)
+    int max_ksplit = 6;             // K slices per GEMM tile at most (the gather stages 2 x (ks - 1) 16 KB blocks)
     WideParams *par = nullptr;      // device copy of the pass's values
     WideParams *par_host = nullptr; // pinned ring
     cudaEvent_t par_ev[kParamSlots]{};
@@ -149,6 +150,8 @@ struct fm_handle {
     cudaEvent_t rows_ev[kParamSlots]{};
     int rows_next = 0;
     std::vector<int> row_of;        // per sequence: its first row in the last batched draft, or -1
+    double keys = 0;                // the current pass's cache rows read per layer (profile bytes)
+    float *dbg_logits = nullptr;    // FM_DEBUG_LOGITS of a batched draft: [block][Vn]
   } wide;
 
   // ---- per-sequence lanes ----
@@ -1401,6 +1404,8 @@ fm_status create_wide(fm_handle *h, cudaStream_t s) {
   CK(cudaMemsetAsync(w.xtickets, 0, (size_t)ns * H * 4, s));
   const char *xs = getenv("FM_WIDE_XSPLITS");
   if (xs && atoi(xs) >= 1 && atoi(xs) <= 8) w.xsplits = atoi(xs);
+  const char *mk = getenv("FM_WIDE_MAX_KSPLIT");
+  if (mk && atoi(mk) >= 1 && atoi(mk) <= 6) w.max_ksplit = atoi(mk);
   TRY(dalloc(h, &w.par, 1));
   CK(cudaMallocHost(&w.par_host, sizeof(WideParams) * kParamSlots));
   w.rows_cap = h->pf_rows;
@@ -1434,7 +1439,7 @@ TcGemmArgs wide_gemm(const fm_handle *h, const CUtensorMap &a, const CUtensorMap
   // K slices fill the GPU when there are fewer tiles than SMs (one wave of units at most)
   const int tiles = tc_gemm_tiles(M, N), nk = K / 64;
   int ks = h->n_sm / tiles;
-  if (ks > 8) ks = 8;
+  if (ks > h->wide.max_ksplit) ks = h->wide.max_ksplit;
   if (ks > nk) ks = nk;
   g.ksplit = ks < 1 ? 1 : ks;
   g.ws = h->wide.ws;
@@ -1447,7 +1452,7 @@ TcGemmArgs wide_gemm(const fm_handle *h, const CUtensorMap &a, const CUtensorMap
 }
 
 fm_status run_tc(fm_handle *h, const TcGemmArgs &g, cudaStream_t s, const char *tag) {
-  ProfScope ps(h, s, tag, (double)g.N * g.K * 2 + (double)g.M * g.K * 2);
+  ProfScope ps(h, s, tag, 2.0 * g.M * g.N * g.K);   // GEMM records carry their FLOPs
   CK(launch_tc_gemm(g, h->n_sm, s));
   ++h->last_launches;
   return FM_OK;
@@ -1480,7 +1485,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
   g.ldo = D;
   g.row_st = w.kst;
   g.st_ld = D / 256;
-  TRY(run_tc(h, g, s, "wide.anchor_proj"));
+  TRY(run_tc(h, g, s, "wide.gemm_anchor_proj"));
   g = wide_gemm(h, w.m_kin16, h->tm_wkv, n, L * 2 * D, D, TC_EPI_KV);
   g.in_st = w.kst;
   g.in_st_n = D / 256;
@@ -1493,7 +1498,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
   g.row_seq = WIDE_FIELD(h, kv_seq);
   g.row_pos = WIDE_FIELD(h, kv_pos);
   g.seq_stride = (size_t)L * 2 * h->cache_plane;
-  TRY(run_tc(h, g, s, "wide.kv_anchor"));
+  TRY(run_tc(h, g, s, "wide.gemm_kv_anchor"));
   for (int l = 0; l < L; ++l) {
     const float *ms = h->mod + (size_t)(3 * l + 0) * 3 * D;
     const float *mc = h->mod + (size_t)(3 * l + 1) * 3 * D;
@@ -1507,7 +1512,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.out32 = w.qkv_out;
     g.ldo32 = 3 * D;
     g.row_pos = WIDE_FIELD(h, row_pos);
-    TRY(run_tc(h, g, s, "wide.qkv_self"));
+    TRY(run_tc(h, g, s, "wide.gemm_qkv_self"));
     {
       ProfScope ps(h, s, "wide.attn_self", (double)T * D * 3 * 4 + (double)T * D * 2);
       CK(launch_wide_self_attn(w.qkv_out, D, B, n, H, w.o16, s));
@@ -1517,7 +1522,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.X = w.X;
     g.ldx = D;
     g.gate = ms + 2 * D;
-    TRY(run_tc(h, g, s, "wide.o_self"));
+    TRY(run_tc(h, g, s, "wide.gemm_o_self"));
     // cross-attention over each sequence's own cache rows 0 .. pos
     TRY(run_lnmod(h, mc, T, s));
     g = wide_gemm(h, w.m_a16, w.t_cq[l], T, D, D, TC_EPI_SEGS);
@@ -1526,7 +1531,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.out32 = w.qc;
     g.ldo32 = D;
     g.row_pos = WIDE_FIELD(h, row_pos);
-    TRY(run_tc(h, g, s, "wide.q_cross"));
+    TRY(run_tc(h, g, s, "wide.gemm_q_cross"));
     {
       XAttnArgs xa;
       memset(&xa, 0, sizeof xa);
@@ -1551,7 +1556,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
       xa.n_z = n;
       xa.layer = l;
       xa.n_layers = L;
-      ProfScope ps(h, s, "wide.attn_cross", 0.0);
+      ProfScope ps(h, s, "wide.attn_cross", w.keys * c.dim * 2 * 2 + 2.0 * T * D * (4 + 2));
       CK(launch_xattn(xa, 3, false, s, true));
       ++h->last_launches;
     }
@@ -1559,7 +1564,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.X = w.X;
     g.ldx = D;
     g.gate = mc + 2 * D;
-    TRY(run_tc(h, g, s, "wide.o_cross"));
+    TRY(run_tc(h, g, s, "wide.gemm_o_cross"));
     // MLP
     TRY(run_lnmod(h, mm, T, s));
     g = wide_gemm(h, w.m_a16, w.t_f1[l], T, F, D, TC_EPI_F16);
@@ -1567,13 +1572,13 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.gelu = 1;
     g.out16 = w.u16;
     g.ldo = F;
-    TRY(run_tc(h, g, s, "wide.fc1"));
+    TRY(run_tc(h, g, s, "wide.gemm_fc1"));
     g = wide_gemm(h, w.m_u16, w.t_f2[l], T, D, F, TC_EPI_RESID);
     g.bias = h->b_f2[l];
     g.X = w.X;
     g.ldx = D;
     g.gate = mm + 2 * D;
-    TRY(run_tc(h, g, s, "wide.fc2"));
+    TRY(run_tc(h, g, s, "wide.gemm_fc2"));
   }
   // final adaLN -> head -> lm_head with the per-row argmax
   TRY(run_lnmod(h, h->mod + (size_t)(3 * L) * 3 * D, T, s));
@@ -1583,12 +1588,12 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
   g.ldo = Ht;
   g.out32 = w.Y;
   g.ldo32 = Ht;
-  TRY(run_tc(h, g, s, "wide.head"));
+  TRY(run_tc(h, g, s, "wide.gemm_head"));
   g = wide_gemm(h, w.m_y16, w.t_table, T, w.Vn, Ht, TC_EPI_ARGMAX);
   g.amax = w.amax;
   g.amax_ld = w.Vn / 256;
   g.n_valid = c.vocab;
-  TRY(run_tc(h, g, s, "wide.lm_head"));
+  TRY(run_tc(h, g, s, "wide.gemm_lm_head"));
   {
     ProfScope ps(h, s, "wide.argmax", (double)T * (w.Vn / 256) * 8);
     CK(launch_wide_argmax(w.amax, w.Vn / 256, T, w.par, s));
@@ -1670,6 +1675,8 @@ fm_status wide_draft(fm_handle *h, int n, const int32_t *ids, const int32_t *anc
       p.z_L[z] = p.pos[order[z]] + 1;
     }
     TRY(wide_upload(h, p, s));
+    w.keys = 0;
+    for (int i = 0; i < m; ++i) w.keys += p.pos[i] + 1;
     const int xs = w.xsplits;
     TRY(run_graph(h, chain_key(6, 0, m, xs, 0), s, [&](cudaStream_t st) { return wide_chain(h, m, xs, st); }));
     if (p0 + m == n)
@@ -2592,8 +2599,22 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
       break;
     case FM_DEBUG_LOGITS: {
       TRY(check_seq(h, seq));
-      if (h->wide.on && h->wide.row_of[seq] >= 0)
-        return fail(h, FM_ERR_UNSUPPORTED, "the logits of a batched draft are not kept");
+      if (h->wide.on && h->wide.row_of[seq] >= 0) {
+        // the batched lm_head's product for this sequence's rows, stored instead of reduced
+        fm_handle::Wide &w = h->wide;
+        if (!w.dbg_logits) TRY(dalloc(h, &w.dbg_logits, (size_t)c.block * w.Vn));
+        if (!h->dbg_logits) TRY(dalloc(h, &h->dbg_logits, (size_t)kMaxT * c.vocab));
+        TcGemmArgs g = wide_gemm(h, w.m_y16, w.t_table, c.block, w.Vn, c.target_dim, TC_EPI_F16);
+        g.a_row0 = w.row_of[seq];
+        g.out32 = w.dbg_logits;
+        g.ldo32 = w.Vn;
+        TRY(run_tc(h, g, s, "wide.gemm_logits"));
+        CK(cudaMemcpy2DAsync(h->dbg_logits, (size_t)c.vocab * 4, w.dbg_logits, (size_t)w.Vn * 4, (size_t)c.vocab * 4,
+                             c.block, cudaMemcpyDeviceToDevice, s));
+        src = h->dbg_logits;
+        size = (int64_t)c.block * c.vocab * 4;
+        break;
+      }
       use_lane(h, seq);
       if (!h->dbg_logits) TRY(dalloc(h, &h->dbg_logits, (size_t)kMaxT * c.vocab));
       StepParams p{};

@@ -115,21 +115,64 @@ __device__ __forceinline__ void store_h8(__half *dst, const float *v) {
   *reinterpret_cast<uint4 *>(dst) = pk;
 }
 
+// 32 bf16 values (64-byte aligned), fetched raw (16 registers) and widened when used
+struct Bf16x32 {
+  uint4 u[4];
+};
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16 *__restrict__ p, Bf16x32 &r) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) r.u[q] = __ldg(reinterpret_cast<const uint4 *>(p) + q);
+}
+__device__ __forceinline__ float bf16_at(const Bf16x32 &r, int j) {   // j: a compile-time index
+  const uint4 &u = r.u[j >> 3];
+  const uint32_t w = (j & 7) < 2 ? u.x : (j & 7) < 4 ? u.y : (j & 7) < 6 ? u.z : u.w;
+  return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
+// RoPE of 32 interleaved channels: (cos, sin) pairs in 8 float4
+__device__ __forceinline__ void load_rope16(const float2 *__restrict__ p, float4 (&r)[8]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) r[q] = __ldg(reinterpret_cast<const float4 *>(p) + q);
+}
+__device__ __forceinline__ void apply_rope16(float *v, const float4 (&r)[8]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float c0 = r[q].x, s0 = r[q].y, c1 = r[q].z, s1 = r[q].w;
+    const float a0 = v[4 * q], a1 = v[4 * q + 1], b0 = v[4 * q + 2], b1 = v[4 * q + 3];
+    v[4 * q] = a0 * c0 - a1 * s0;
+    v[4 * q + 1] = a1 * c0 + a0 * s0;
+    v[4 * q + 2] = b0 * c1 - b1 * s1;
+    v[4 * q + 3] = b1 * c1 + b0 * s1;
+  }
+}
+
+__device__ __forceinline__ void store_f4(float *dst, const float *v) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+}
+
+// The epilogues below read their per-column operands (norm weights, bias,
+// RoPE rows, the residual) before the chunk's accumulator values, so the
+// global loads are in flight while tcgen05.ld runs.
+
 __device__ void epilogue_fc(const TcGemmArgs &a, uint32_t taddr, int row, int n0, int nb) {
   float ss = 0.f;
   const bool live = row < a.M;
   for (int c0 = 0; c0 < BN; c0 += 32) {
+    Bf16x32 w, b;
+    load_bf16x32(a.colw + n0 + c0, w);
+    if (a.bias) load_bf16x32(a.bias + n0 + c0, b);
     float v[32];
     tld32(taddr + c0, v);
     if (!live) continue;
     if (a.bias) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += __bfloat162float(a.bias[n0 + c0 + j]);
+      for (int j = 0; j < 32; ++j) v[j] += bf16_at(b, j);
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       ss += v[j] * v[j];
-      v[j] *= __bfloat162float(a.colw[n0 + c0 + j]);
+      v[j] *= bf16_at(w, j);
     }
     __half *dst = a.out16 + (size_t)row * a.ldo + n0 + c0;
 #pragma unroll
@@ -151,6 +194,7 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
   }
   const int p = a.row_pos ? (live ? a.row_pos[row] : 0) : a.start + row;
   __half *cache = a.cache + (a.row_seq && live ? (size_t)a.row_seq[row] * a.seq_stride : 0);
+  const float2 *rrow = a.rope + (size_t)p * (hd >> 1);
   for (int h0 = 0; h0 < BN; h0 += hd) {
     const int head = ((n0 % a.seg_cols) + h0) / hd;
     float r2 = 1.f;
@@ -167,6 +211,12 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
     __half *dst = cache + (size_t)(layer * 2 + kind) * a.plane + ((size_t)head * a.max_ctx + p) * hd;
     const __nv_bfloat16 *kw = a.kn_w + (size_t)layer * hd;
     for (int c0 = 0; c0 < hd; c0 += 32) {
+      Bf16x32 w;
+      float4 rp[8];
+      if (kind == 0) {
+        load_bf16x32(kw + c0, w);
+        load_rope16(rrow + (c0 >> 1), rp);
+      }
       float v[32];
       tld32(taddr + h0 + c0, v);
       if (!live) continue;
@@ -174,15 +224,8 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
       for (int j = 0; j < 32; ++j) v[j] *= rs;
       if (kind == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * __bfloat162float(kw[c0 + j]);
-        const float2 *rp = a.rope + (size_t)p * (hd >> 1) + (c0 >> 1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 cs = rp[i];
-          const float x0 = v[2 * i], x1 = v[2 * i + 1];
-          v[2 * i] = x0 * cs.x - x1 * cs.y;
-          v[2 * i + 1] = x1 * cs.x + x0 * cs.y;
-        }
+        for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * bf16_at(w, j);
+        apply_rope16(v, rp);
       }
 #pragma unroll
       for (int j = 0; j < 32; j += 8) store_h8(dst + c0 + j, v + j);
@@ -190,22 +233,20 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
   }
 }
 
-__device__ __forceinline__ void store_f4(float *dst, const float *v) {
-#pragma unroll
-  for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-}
-
 __device__ void epilogue_f16(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
   const bool live = row < a.M;
   for (int c0 = 0; c0 < BN; c0 += 32) {
+    Bf16x32 bias;
+    if (a.bias) load_bf16x32(a.bias + n0 + c0, bias);
     float v[32];
     tld32(taddr + c0, v);
     if (!live) continue;
     if (a.bias) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += __bfloat162float(a.bias[n0 + c0 + j]);
+      for (int j = 0; j < 32; ++j) v[j] += bf16_at(bias, j);
     }
     if (a.out32) store_f4(a.out32 + (size_t)row * a.ldo32 + n0 + c0, v);
+    if (!a.out16) continue;
     if (a.gelu) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
@@ -216,28 +257,45 @@ __device__ void epilogue_f16(const TcGemmArgs &a, uint32_t taddr, int row, int n
   }
 }
 
+// X += gate * (acc + bias).  With one tile per CTA this epilogue's latency is
+// exposed: the next chunk's residual values (L2) are requested before the
+// current chunk is finished; gate and bias are shared by every row (L1).
 __device__ void epilogue_resid(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
   const bool live = row < a.M;
-  for (int c0 = 0; c0 < BN; c0 += 32) {
+  float *__restrict__ x = a.X + (size_t)(live ? row : 0) * a.ldx + n0;
+  const float4 *__restrict__ g4 = reinterpret_cast<const float4 *>(a.gate + n0);
+  const uint2 *__restrict__ b4 = a.bias ? reinterpret_cast<const uint2 *>(a.bias + n0) : nullptr;
+  float4 xv[2][8];
+  auto fetch = [&](int c0, int b) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      xv[b][q] = live ? __ldcg(reinterpret_cast<const float4 *>(x + c0) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  fetch(0, 0);
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    const int c0 = 32 * c, b = c & 1;
+    if (c + 1 < BN / 32) fetch(c0 + 32, b ^ 1);
     float v[32];
     tld32(taddr + c0, v);
     if (!live) continue;
-    float *x = a.X + (size_t)row * a.ldx + n0 + c0;
-    const float *g = a.gate + n0 + c0;
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      float4 xv = *reinterpret_cast<const float4 *>(x + j);
-      const float4 gv = *reinterpret_cast<const float4 *>(g + j);
-      float b[4] = {0.f, 0.f, 0.f, 0.f};
-      if (a.bias) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) b[e] = __bfloat162float(a.bias[n0 + c0 + j + e]);
+    for (int q = 0; q < 8; ++q) {
+      const float4 gg = __ldg(g4 + 8 * c + q);
+      float bb[4] = {0.f, 0.f, 0.f, 0.f};
+      if (b4) {
+        const uint2 u = __ldg(b4 + 8 * c + q);
+        bb[0] = __uint_as_float(u.x << 16);
+        bb[1] = __uint_as_float(u.x & 0xffff0000u);
+        bb[2] = __uint_as_float(u.y << 16);
+        bb[3] = __uint_as_float(u.y & 0xffff0000u);
       }
-      xv.x += gv.x * (v[j] + b[0]);
-      xv.y += gv.y * (v[j + 1] + b[1]);
-      xv.z += gv.z * (v[j + 2] + b[2]);
-      xv.w += gv.w * (v[j + 3] + b[3]);
-      *reinterpret_cast<float4 *>(x + j) = xv;
+      float4 o = xv[b][q];
+      o.x += gg.x * (v[4 * q] + bb[0]);
+      o.y += gg.y * (v[4 * q + 1] + bb[1]);
+      o.z += gg.z * (v[4 * q + 2] + bb[2]);
+      o.w += gg.w * (v[4 * q + 3] + bb[3]);
+      __stcg(reinterpret_cast<float4 *>(x + c0) + q, o);
     }
   }
 }
@@ -250,6 +308,8 @@ __device__ void epilogue_segs(const TcGemmArgs &a, uint32_t taddr, int row, int 
   const __nv_bfloat16 *nw = seg == 0 ? a.nw0 : seg == 1 ? a.nw1 : nullptr;
   const int hd = a.hd;
   const int p = live ? (a.row_pos ? a.row_pos[row] : a.start + row) : 0;
+  const float2 *rrow = a.rope + (size_t)p * (hd >> 1);
+  float *__restrict__ out = a.out32 + (size_t)(live ? row : 0) * a.ldo32 + n0;
   for (int h0 = 0; h0 < BN; h0 += hd) {
     float r2 = 1.f;
     if (nw) {
@@ -263,22 +323,21 @@ __device__ void epilogue_segs(const TcGemmArgs &a, uint32_t taddr, int row, int 
       r2 = rsqrtf(ss / (float)hd + a.qk_eps);
     }
     for (int c0 = 0; c0 < hd; c0 += 32) {
+      Bf16x32 w;
+      float4 rp[8];
+      if (nw) {
+        load_bf16x32(nw + c0, w);
+        load_rope16(rrow + (c0 >> 1), rp);
+      }
       float v[32];
       tld32(taddr + h0 + c0, v);
       if (!live) continue;
       if (nw) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * __bfloat162float(nw[c0 + j]);
-        const float2 *rp = a.rope + (size_t)p * (hd >> 1) + (c0 >> 1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 cs = rp[i];
-          const float x0 = v[2 * i], x1 = v[2 * i + 1];
-          v[2 * i] = x0 * cs.x - x1 * cs.y;
-          v[2 * i + 1] = x1 * cs.x + x0 * cs.y;
-        }
+        for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * bf16_at(w, j);
+        apply_rope16(v, rp);
       }
-      store_f4(a.out32 + (size_t)row * a.ldo32 + n0 + h0 + c0, v);
+      store_f4(out + h0 + c0, v);
     }
   }
 }
@@ -299,17 +358,30 @@ __device__ void epilogue_argmax(const TcGemmArgs &a, uint32_t taddr, int row, in
   if (row < a.M) a.amax[(size_t)row * a.amax_ld + nb] = make_float2(best, __int_as_float(bi));
 }
 
+// Split-K partial tiles in the workspace: per (tile, slice) 8 chunk blocks of
+// 128 rows x 32 f32 (16 KB each), the 16-byte units of a row XOR-swizzled by
+// (row & 7) so that a warp's reads of one unit column spread over the banks.
+__device__ __forceinline__ size_t ws_block(int tile, int ks, int slice, int c) {
+  return ((((size_t)tile * ks + slice) * 8 + c) * BM) * 32;
+}
+
 // Split-K: store this slice's partial tile; the last slice of the tile to get
-// here sums every slice's partial (slice order) back into the accumulator.
-// Returns whether this CTA runs the tile's epilogue.  All 128 epilogue threads
-// call it together.
-__device__ bool splitk_gather(const TcGemmArgs &a, uint32_t taddr, int rl, int tile, int slice, int *s_last) {
+// here sums every slice's partial (in slice order, its own from TMEM) back into
+// the accumulator.  The other slices' blocks come through the bulk-copy engine
+// into the operand ring, which is idle by then (a split GEMM gives each CTA
+// one unit), two chunks in flight.  Returns whether this CTA runs the tile's
+// epilogue.  All 128 epilogue threads call it together.
+__device__ bool splitk_gather(const TcGemmArgs &a, uint32_t taddr, int rl, int tile, int slice, int *s_last,
+                              uint32_t stage, const uint8_t *stage_ptr, uint32_t gbar) {
   const int ks = a.ksplit;
-  float *mine = a.ws + (((size_t)tile * ks + slice) * BM + rl) * BN;
-  for (int c0 = 0; c0 < BN; c0 += 32) {
+  const int sw = rl & 7;
+  for (int c = 0; c < BN / 32; ++c) {
     float v[32];
-    tld32(taddr + c0, v);
-    store_f4(mine + c0, v);
+    tld32(taddr + 32 * c, v);
+    float *dst = a.ws + ws_block(tile, ks, slice, c) + (size_t)rl * 32;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<float4 *>(dst + 4 * (u ^ sw)) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
   }
   named_sync(1, 128);
   if (threadIdx.x == 64) {
@@ -322,22 +394,48 @@ __device__ bool splitk_gather(const TcGemmArgs &a, uint32_t taddr, int rl, int t
   named_sync(1, 128);
   if (!*s_last) return false;
   __threadfence();
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    float v[32];
+  constexpr uint32_t kBlk = BM * 32 * 4;
+  const uint32_t buf = (uint32_t)(ks - 1) * kBlk;
+  auto issue = [&](int c) {
+    const uint32_t bar = gbar + 8 * (c & 1);
+    mbar_expect_tx(bar, buf);
+    int k = 0;
+    for (int s = 0; s < ks; ++s)
+      if (s != slice) bulk_g2s(stage + (c & 1) * buf + (k++) * kBlk, a.ws + ws_block(tile, ks, s, c), kBlk, bar);
+  };
+  if (threadIdx.x == 64) {
+    // the blocks were written through the generic proxy by other CTAs
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    issue(0);
+    issue(1);
+  }
+  for (int c = 0; c < BN / 32; ++c) {
+    const int b = c & 1;
+    mbar_wait_bounded(gbar + 8 * b, (c >> 1) & 1, a.err);
+    float v[32], acc[32];
+    tld32(taddr + 32 * c, v);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+    int k = 0;
     for (int s = 0; s < ks; ++s) {
-      const float *src = a.ws + (((size_t)tile * ks + s) * BM + rl) * BN + c0;
+      if (s == slice) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 q = __ldcg(reinterpret_cast<const float4 *>(src + j));
-        v[j] += q.x;
-        v[j + 1] += q.y;
-        v[j + 2] += q.z;
-        v[j + 3] += q.w;
+        for (int j = 0; j < 32; ++j) acc[j] += v[j];
+      } else {
+        const float *blk = reinterpret_cast<const float *>(stage_ptr + b * buf + (k++) * kBlk) + (size_t)rl * 32;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 q = *reinterpret_cast<const float4 *>(blk + 4 * (u ^ sw));
+          acc[4 * u] += q.x;
+          acc[4 * u + 1] += q.y;
+          acc[4 * u + 2] += q.z;
+          acc[4 * u + 3] += q.w;
+        }
       }
     }
-    tmem_st32(taddr + c0, v);
+    tmem_st32(taddr + 32 * c, acc);
+    named_sync(1, 128);   // buffer b has been read by the group
+    if (threadIdx.x == 64 && c + 2 < BN / 32) issue(c + 2);
   }
   return true;
 }
@@ -356,12 +454,14 @@ __device__ __forceinline__ void tile_coords(int tile, int n_mb, int n_nb, int gm
 __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
   const uint32_t bars = base + ST * STAGE;
   auto full = [&](int s) { return bars + 8 * s; };
   auto empty = [&](int s) { return bars + 8 * (ST + s); };
   auto tfull = [&](int b) { return bars + 8 * (2 * ST + b); };
   auto tempty = [&](int b) { return bars + 8 * (2 * ST + 2 + b); };
   const uint32_t tslot = bars + 8 * (2 * ST + 4);
+  const uint32_t gbar = bars + 8 * (2 * ST + 5);   // two: split-K gather buffers
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == 0 && lane == 0) {
@@ -372,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull(b), 1);
       mbar_init(tempty(b), 128);
+      mbar_init(gbar + 8 * b, 1);
     }
     mbar_fence_init();
   }
@@ -412,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
           if (!mbar_wait(empty(s), ((it / ST) & 1) ^ 1, a.err)) { ok = false; break; }
           const uint32_t sa = base + s * STAGE, sb = sa + A_BYTES;
           mbar_expect_tx(full(s), STAGE);
-          tma_load_2d(sa, &a.tma_a, kb * BK, mb * BM, full(s));
+          tma_load_2d(sa, &a.tma_a, kb * BK, a.a_row0 + mb * BM, full(s));
           tma_load_2d(sb, &a.tma_b, kb * BK, nb * BN, full(s));
         }
       }
@@ -460,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
       tile_coords(tile, n_mb, n_nb, gm, mb, nb);
       const uint32_t taddr = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
       const int row = mb * BM + rl;
-      if (ks == 1 || splitk_gather(a, taddr, rl, tile, u % ks, &s_last)) {
+      if (ks == 1 || splitk_gather(a, taddr, rl, tile, u % ks, &s_last, base, gbase, gbar)) {
         switch (a.epi) {
           case TC_EPI_FC: epilogue_fc(a, taddr, row, nb * BN, nb); break;
           case TC_EPI_KV: epilogue_kv(a, taddr, row, nb * BN); break;
@@ -536,6 +637,9 @@ cudaError_t launch_tc_gemm(const TcGemmArgs &a, int n_sm, cudaStream_t s) {
   const int ks = a.ksplit > 1 ? a.ksplit : 1;
   if (ks > a.K / BK || (ks > 1 && (!a.ws || !a.tile_tickets))) return cudaErrorInvalidValue;
   const int n_units = ((a.M + BM - 1) / BM) * (a.N / BN) * ks;
+  // a split GEMM gives each CTA one unit (the gather stages its partials in the idle operand
+  // ring: two chunks of ks - 1 blocks of 16 KB must fit)
+  if (ks > 1 && (n_units > n_sm || 2 * (ks - 1) * BM * 32 * 4 > ST * STAGE)) return cudaErrorInvalidValue;
   const int grid = n_units < n_sm ? n_units : n_sm;
   const size_t smem = tc_gemm_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(fm_prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -13,7 +13,8 @@ namespace fm {
 enum TcEpi : int32_t {
   TC_EPI_FC = 0,      // c = acc (+ bias); C' = c * colw[n] (f16) and per-row partial sum of c^2 per 256 columns
   TC_EPI_KV = 1,      // row scale 1/rms, k_norm + RoPE on K heads, f16 stores into the head-major caches
-  TC_EPI_F16 = 2,     // out16 = f16(act(acc + bias)), act = identity or exact GELU; optionally out32 = acc + bias
+  TC_EPI_F16 = 2,     // out16 = f16(act(acc + bias)), act = identity or exact GELU (out16 null: none);
+                      // optionally out32 = acc + bias
   TC_EPI_RESID = 3,   // X[row][n] += gate[n] * (acc + bias[n])   (gated residual, f32 in place)
   TC_EPI_SEGS = 4,    // out32: per-head RMSNorm + interleaved-pair RoPE on segments 0 / 1, plain elsewhere
   TC_EPI_ARGMAX = 5,  // per row, the best (value, lowest index) over the tile's columns < n_valid
@@ -29,6 +30,7 @@ struct TcGemmArgs {
   // group's A panel stays in L2 (1: the column block runs fastest)
   int32_t group_m;
   int32_t *err;       // set to 1 when a bounded wait gives up
+  int32_t a_row0;     // A rows start at this row of the map (rows past the map's extent read as zero)
   // split-K: each output tile is computed as ksplit slices of the K blocks; a
   // slice stores its partial tile into ws and takes a ticket, and the last
   // slice to finish sums the partials in slice order (deterministic) and runs

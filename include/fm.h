@@ -372,8 +372,10 @@ FM_API fm_status fm_set_debug(fm_handle *h, int32_t flags);
 
 /* Per-kernel timings gathered while FM_DEBUG_PROFILE is set: one entry per
  * kernel name, with the launches, their summed device time and the summed
- * algorithmic bytes they move (weights once, activations once).  Reading
- * synchronises the stream of the recorded launches and resets the record.
+ * algorithmic bytes they move (weights once, activations once); for the
+ * tensor-core GEMMs (names containing "gemm") the field holds their summed
+ * floating-point operations instead (2 M N K each).  Reading synchronises the
+ * stream of the recorded launches and resets the record.
  * Errors: FM_ERR_INVALID_ARG (null pointers, cap < 0), FM_ERR_CUDA. */
 typedef struct fm_kernel_time {
   char name[32];

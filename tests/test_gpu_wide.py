@@ -57,10 +57,16 @@ def batched_draft(p, ids, anchors, pos):
 
 
 def check_seq(p, seq, got_tokens, anchor, pos):
-    """One sequence of a batched draft against the oracle's own draft of it."""
+    """One sequence of a batched draft against the oracle's own draft of it:
+    head output and logits (the batched lm_head's product, stored instead of
+    reduced) within the bar, tokens exact or excused by the margin."""
+    import block_speculative_decoding_fm_gb300 as fm
     ref = p.oracle.draft(p.state(seq), anchor, pos)
     y = head_out(p, seq)
     assert rel_l2(y, ref.head_out) < REL_L2, (seq, rel_l2(y, ref.head_out))
+    lg = np.empty((p.cfg.block, p.cfg.vocab), np.float32)
+    fm.fm_debug_copy(p.h, fm.FM_DEBUG_LOGITS, seq, 0, lg)
+    assert rel_l2(lg, ref.logits) < REL_L2, (seq, rel_l2(lg, ref.logits))
     assert tokens_match(got_tokens, ref.tokens, ref.logits), (seq, got_tokens, ref.tokens)
     return ref
 
@@ -137,14 +143,19 @@ def test_batched_cycles_match_oracle(lm):
 def test_batched_draft_in_passes():
     """34 sequences: two batched passes (32 + 2 sequences) in one call, short
     contexts; every sequence's tokens and head output against the oracle."""
+    import torch
     import block_speculative_decoding_fm_gb300 as fm
     cfg = mid_config(34, max_ctx=160)
     p = Pair(cfg, 1402, keep_hidden=False)
     fr = S.streams(1402)["features"]
     rng = S.streams(1402)["workload"]
     lens = [int(x) for x in rng.integers(1, 60, size=34)]
+    # the contexts through one batched append (no deferred rows are left for the draft to flush)
+    rows = [S.gen_features(fr, n, cfg.feat_dim) for n in lens]
+    fm.fm_context_append_batched(p.h, list(range(34)), torch.from_numpy(np.concatenate(rows)).cuda(), lens,
+                                 [0] * 34)
     for s, n in enumerate(lens):
-        p.append(s, S.gen_features(fr, n, cfg.feat_dim), 0)
+        p.oracle.context_append(p.state(s), rows[s], 0)
     ids = list(range(34))[::-1]
     anchors = [int(x) for x in rng.integers(0, cfg.vocab, size=34)]
     pos = [lens[s] for s in ids]
@@ -177,65 +188,4 @@ def test_batched_argmax_ties_go_to_the_lowest_index():
     assert np.all(got % 2 == 0), got
     for s in range(4):
         check_seq(p, s, got[s], [2, 4, 6, 8][s], lens[s])
-    p.close()
-
-
-def test_batched_full_shape_sampled():
-    """The 32-sequence FlashMap-4B workload as the bench times it: contexts
-    U[512, 8192] prefilled, a batched append of acc + 1 rows (acc ~ U{0..16}),
-    a batched draft of all 32 sequences.  The oracle runs the shortest and the
-    longest sequence (their contexts built from the same seeded rows); every
-    sequence's device acceptance equals the host rule."""
-    import torch
-    import block_speculative_decoding_fm_gb300 as fm
-    n_seqs = 32
-    cfg = S.flashmap_4b_config(max_ctx=8192 + 17 + 64, max_seqs=n_seqs)
-    rng = S.streams(1404)["workload"]
-    L = [int(x) for x in S.batched_lengths(rng, n_seqs)]
-    n_new = [int(x) + 1 for x in rng.integers(0, 17, size=n_seqs)]
-    anchors = [int(x) for x in rng.integers(0, cfg.vocab, size=n_seqs)]
-    sample = sorted({int(np.argmin(L)), int(np.argmax(L))})
-    p = Pair(cfg, 1404, oracle_max_ctx=8192 + 17 + 64, keep_hidden=False)
-    fr = S.streams(1404)["features"]
-    # the sampled sequences' contexts come from the seeded host stream (the oracle needs them);
-    # the others are drawn on the device from a seeded generator
-    g = torch.Generator(device="cuda")
-    g.manual_seed(1404)
-    ctx_rows, new_rows = {}, []
-    for s in range(n_seqs):
-        if s in sample:
-            ctx_rows[s] = S.gen_features(fr, L[s], cfg.feat_dim)
-            p.append(s, ctx_rows[s], 0, oracle=False)
-        else:
-            f = torch.randn((L[s], cfg.feat_dim), generator=g, device="cuda")
-            fm.fm_context_append(p.h, s, f, L[s], 0)
-            del f
-    for s in range(n_seqs):
-        new_rows.append(S.gen_features(fr, n_new[s], cfg.feat_dim))
-    ids = list(range(n_seqs))
-    fm.fm_context_append_batched(p.h, ids, torch.from_numpy(np.concatenate(new_rows)).cuda(), n_new, L)
-    pos = [L[s] + n_new[s] for s in ids]
-    got = batched_draft(p, ids, anchors, pos)
-    assert np.all((got >= 0) & (got < cfg.vocab))
-    for s in sample:
-        st = p.state(s)
-        p.oracle.context_append(st, ctx_rows[s], 0)
-        p.oracle.context_append(st, new_rows[s], L[s])
-        cache_rows_match(p, s, L[s], pos[s])
-        check_seq(p, s, got[s], anchors[s], pos[s])
-    # device acceptance of every sequence against the host rule (fm_accept)
-    tr = S.streams(1404)["tokens"]
-    targets = np.stack([np.append(got[s], int(tr.integers(0, cfg.vocab))) for s in ids]).astype(np.int32)
-    flips = tr.integers(0, cfg.block + 1, size=n_seqs)
-    for s in ids:
-        if flips[s] < cfg.block:
-            targets[s, flips[s]] = (targets[s, flips[s]] + 1) % cfg.vocab
-    k = torch.full((n_seqs,), cfg.block, dtype=torch.int32, device="cuda")
-    a_dev = torch.zeros((n_seqs,), dtype=torch.int32, device="cuda")
-    b_dev = torch.zeros((n_seqs,), dtype=torch.int32, device="cuda")
-    fm.fm_accept_batched(p.h, torch.from_numpy(got).cuda(), torch.from_numpy(targets).cuda(), k, a_dev, b_dev)
-    torch.cuda.synchronize()
-    for s in ids:
-        assert (int(a_dev[s]), int(b_dev[s])) == fm.fm_accept(got[s], targets[s], cfg.block)
-        assert (int(a_dev[s]), int(b_dev[s])) == accept(got[s], targets[s], cfg.block)
     p.close()
