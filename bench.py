@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--no-kprof", action="store_true", help="skip the per-kernel timing pass")
     p.add_argument("--prefill-rows", type=int, default=32768, help="rows of the prefill workload (a smaller case "
                    "for profiling captures)")
+    p.add_argument("--batched-ctx", type=int, default=8192, help="longest context of the batched workload (a "
+                   "smaller case for profiling captures; contexts are uniform in [512, this])")
     return p.parse_args()
 
 
@@ -383,16 +385,16 @@ class BatchedStep:
     (acc_i ~ U{0..16}) then all 32 draft 16 slots; every step re-appends at the same positions."""
     name = "batched_32_step"
 
-    def __init__(self, torch, n_seqs=32):
+    def __init__(self, torch, n_seqs=32, ctx_hi=8192):
         import block_speculative_decoding_fm_gb300 as fm
         import fm_synth as S
         self.fm, self.torch = fm, torch
-        self.cfg = S.flashmap_4b_config(max_ctx=8192 + 17 + 64, max_seqs=n_seqs)
+        self.cfg = S.flashmap_4b_config(max_ctx=ctx_hi + 17 + 64, max_seqs=n_seqs)
         c = self.cfg
         w = S.gen_weights(self.cfg, 1005)
         self.h = fm.fm_create(self.cfg, fm.weight_items(w), S.gen_modulation(self.cfg, 1005))
         rng = S.streams(1005)["workload"]
-        self.L = [int(x) for x in S.batched_lengths(rng, n_seqs)]
+        self.L = [int(x) for x in S.batched_lengths(rng, n_seqs, hi=ctx_hi)]
         self.n = [int(x) + 1 for x in rng.integers(0, 17, size=n_seqs)]
         self.anchors = [int(x) for x in rng.integers(0, c.vocab, size=n_seqs)]
         g = torch.Generator(device="cuda")
@@ -518,7 +520,7 @@ def run_workload(args):
             cfgd = {"workload": "mtp: MTP head H 5120, I 17408, 24/4 heads x 256, Q8_0, vocab 248320; depth-3 draft "
                                 "from 2 pending rows over a 1024-row head cache"}
         elif args.workload == "batched":
-            w = BatchedStep(torch)
+            w = BatchedStep(torch, ctx_hi=args.batched_ctx)
             for _ in range(max(3, args.warmup)):
                 w.step()
             w.launches = 0
@@ -527,8 +529,8 @@ def run_workload(args):
             extra["tokens_drafted_per_s"] = value * 32 * 16
             extra["achieved_hbm_gbs"] = w.bytes_per_step * value / 1e9
             extra["bytes_per_step"] = w.bytes_per_step
-            cfgd = {"workload": "batched: 32 FlashMap-4B sequences, contexts U[512,8192], append acc_i+1 rows "
-                                "(acc_i in 0..16) + 32 x 16-slot draft", "global_batch": 512}
+            cfgd = {"workload": f"batched: 32 FlashMap-4B sequences, contexts U[512,{args.batched_ctx}], append "
+                                "acc_i+1 rows (acc_i in 0..16) + 32 x 16-slot draft", "global_batch": 512}
         else:   # prefill
             w = PrefillStep(torch, rows=args.prefill_rows)
             w.step()

@@ -130,16 +130,15 @@ struct fm_handle {
     CUtensorMap t_ap{}, t_head{}, t_table{}, t_cache{};
     // activations: X [rows][D] f32; q/k/v and cross q f32; the head output f32 and f16
     float *X = nullptr, *qkv_out = nullptr, *qc = nullptr, *Y = nullptr, *kst = nullptr;
+    float *br = nullptr;            // a product's gated residual branch, added by the next adaLN
     __half *a16 = nullptr, *o16 = nullptr, *u16 = nullptr, *y16 = nullptr, *anc16 = nullptr, *kin16 = nullptr;
     CUtensorMap m_a16{}, m_o16{}, m_u16{}, m_y16{}, m_anc16{}, m_kin16{};
-    float *ws = nullptr;            // split-K partial tiles
-    int32_t *tickets = nullptr;     // split-K tile tickets
     float2 *amax = nullptr;         // lm_head per-row, per-column-block bests
     float *xo = nullptr;            // cross-attention range partials of every sequence
     float2 *xml = nullptr;
     int32_t *xtickets = nullptr;
     int xsplits = 2;                // key ranges per (sequence, head)
-    int max_ksplit = 6;             // K slices per GEMM tile at most (the gather stages 2 x (ks - 1) 16 KB blocks)
+    int max_ksplit = 4;             // K slices per GEMM tile at most (1, 2 or 4)
     WideParams *par = nullptr;      // device copy of the pass's values
     WideParams *par_host = nullptr; // pinned ring
     cudaEvent_t par_ev[kParamSlots]{};
@@ -1132,7 +1131,7 @@ fm_status prefill_setup(fm_handle *h, cudaStream_t s) {
   if (!h->w_fc16) return fail(h, FM_ERR_UNSUPPORTED, "dense prefill weights were not prepared");
   TRY(dalloc(h, &h->pf_a, (size_t)rows * FW));
   TRY(dalloc(h, &h->pf_c, (size_t)rows * D));
-  TRY(dalloc(h, &h->pf_st, (size_t)rows * (D / 256)));
+  TRY(dalloc(h, &h->pf_st, (size_t)rows * (D / 256) * 4));   // up to 4 K-slice pieces per 256 columns
   TRY(dalloc(h, &h->pf_err, 4));
   CK(cudaMemsetAsync(h->pf_err, 0, 4, s));
   if (!make_tma_f16(&h->tm_wfc, h->w_fc16, D, FW, 256) || !make_tma_f16(&h->tm_wkv, h->w_kv16, (uint64_t)L * 2 * D, D, 256))
@@ -1383,20 +1382,17 @@ fm_status create_wide(fm_handle *h, cudaStream_t s) {
     return fail(h, FM_ERR_CUDA, "cache tensor map encoding failed");
   const int Tr = (T + 127) / 128 * 128;
   TRY(dalloc(h, &w.X, (size_t)Tr * D));
+  TRY(dalloc(h, &w.br, (size_t)Tr * D));
   TRY(dalloc(h, &w.qkv_out, (size_t)Tr * 3 * D));
   TRY(dalloc(h, &w.qc, (size_t)Tr * D));
   TRY(dalloc(h, &w.Y, (size_t)Tr * Ht));
-  TRY(dalloc(h, &w.kst, (size_t)128 * (D / 256)));
+  TRY(dalloc(h, &w.kst, (size_t)128 * (D / 256) * 4));   // up to 4 K-slice pieces per 256 columns
   TRY(wide_abuf(h, &w.a16, &w.m_a16, T, D));
   TRY(wide_abuf(h, &w.o16, &w.m_o16, T, D));
   TRY(wide_abuf(h, &w.u16, &w.m_u16, T, F));
   TRY(wide_abuf(h, &w.y16, &w.m_y16, T, Ht));
   TRY(wide_abuf(h, &w.anc16, &w.m_anc16, ns, Ht));
   TRY(wide_abuf(h, &w.kin16, &w.m_kin16, ns, D));
-  // split-K: at most one wave of (tile, slice) units holds a partial tile each
-  TRY(dalloc(h, &w.ws, (size_t)h->n_sm * 128 * 256));
-  TRY(dalloc(h, &w.tickets, (size_t)h->n_sm));
-  CK(cudaMemsetAsync(w.tickets, 0, (size_t)h->n_sm * 4, s));
   TRY(dalloc(h, &w.amax, (size_t)T * (w.Vn / 256)));
   TRY(dalloc(h, &w.xo, (size_t)ns * H * 8 * 16 * 128));
   TRY(dalloc(h, &w.xml, (size_t)ns * H * 8 * 16));
@@ -1405,7 +1401,7 @@ fm_status create_wide(fm_handle *h, cudaStream_t s) {
   const char *xs = getenv("FM_WIDE_XSPLITS");
   if (xs && atoi(xs) >= 1 && atoi(xs) <= 8) w.xsplits = atoi(xs);
   const char *mk = getenv("FM_WIDE_MAX_KSPLIT");
-  if (mk && atoi(mk) >= 1 && atoi(mk) <= 6) w.max_ksplit = atoi(mk);
+  if (mk && atoi(mk) >= 1 && atoi(mk) <= 4) w.max_ksplit = atoi(mk);
   TRY(dalloc(h, &w.par, 1));
   CK(cudaMallocHost(&w.par_host, sizeof(WideParams) * kParamSlots));
   w.rows_cap = h->pf_rows;
@@ -1436,14 +1432,11 @@ TcGemmArgs wide_gemm(const fm_handle *h, const CUtensorMap &a, const CUtensorMap
   g.epi = epi;
   g.group_m = (M + 127) / 128;   // the row blocks that share a weight tile run side by side
   g.err = h->dev_err;
-  // K slices fill the GPU when there are fewer tiles than SMs (one wave of units at most)
+  // K slices (clusters of 2 or 4) fill the GPU when there are fewer tiles than SMs
   const int tiles = tc_gemm_tiles(M, N), nk = K / 64;
-  int ks = h->n_sm / tiles;
-  if (ks > h->wide.max_ksplit) ks = h->wide.max_ksplit;
-  if (ks > nk) ks = nk;
-  g.ksplit = ks < 1 ? 1 : ks;
-  g.ws = h->wide.ws;
-  g.tile_tickets = h->wide.tickets;
+  int ks = 1;
+  while (ks * 2 <= h->wide.max_ksplit && tiles * ks * 2 <= h->n_sm && ks * 2 <= nk) ks *= 2;
+  g.ksplit = ks;
   g.hd = h->cfg.head_dim;
   g.max_ctx = h->cfg.max_ctx;
   g.rope = h->rope;
@@ -1458,10 +1451,11 @@ fm_status run_tc(fm_handle *h, const TcGemmArgs &g, cudaStream_t s, const char *
   return FM_OK;
 }
 
-fm_status run_lnmod(fm_handle *h, const float *m, int T, cudaStream_t s) {
+// the residual stream takes the previous product's gated branch (when `add`), then adaLN
+fm_status run_lnmod(fm_handle *h, const float *m, int T, bool add, cudaStream_t s) {
   const int D = h->cfg.dim;
-  ProfScope ps(h, s, "wide.lnmod", (double)T * D * 6);
-  CK(launch_wide_lnmod(h->wide.X, D, T, m, m + D, h->cfg.ln_eps, h->wide.a16, s));
+  ProfScope ps(h, s, "wide.lnmod", (double)T * D * (add ? 14 : 6));
+  CK(launch_wide_lnmod(h->wide.X, add ? h->wide.br : nullptr, D, T, m, m + D, h->cfg.ln_eps, h->wide.a16, s));
   ++h->last_launches;
   return FM_OK;
 }
@@ -1484,11 +1478,12 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
   g.out16 = w.kin16;
   g.ldo = D;
   g.row_st = w.kst;
-  g.st_ld = D / 256;
+  g.st_ld = D / 256 * g.ksplit;
+  const int st_n = g.st_ld;
   TRY(run_tc(h, g, s, "wide.gemm_anchor_proj"));
   g = wide_gemm(h, w.m_kin16, h->tm_wkv, n, L * 2 * D, D, TC_EPI_KV);
   g.in_st = w.kst;
-  g.in_st_n = D / 256;
+  g.in_st_n = st_n;
   g.eps = c.rms_eps;
   g.inv_n = 1.0f / D;
   g.seg_cols = D;
@@ -1503,8 +1498,8 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     const float *ms = h->mod + (size_t)(3 * l + 0) * 3 * D;
     const float *mc = h->mod + (size_t)(3 * l + 1) * 3 * D;
     const float *mm = h->mod + (size_t)(3 * l + 2) * 3 * D;
-    // self-attention over each sequence's block
-    TRY(run_lnmod(h, ms, T, s));
+    // self-attention over each sequence's block (the previous layer's MLP branch joins the stream first)
+    TRY(run_lnmod(h, ms, T, l > 0, s));
     g = wide_gemm(h, w.m_a16, w.t_qkv[l], T, 3 * D, D, TC_EPI_SEGS);
     g.seg_cols = D;
     g.nw0 = h->w_sqn[l];
@@ -1518,13 +1513,13 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
       CK(launch_wide_self_attn(w.qkv_out, D, B, n, H, w.o16, s));
       ++h->last_launches;
     }
-    g = wide_gemm(h, w.m_o16, w.t_so[l], T, D, D, TC_EPI_RESID);
-    g.X = w.X;
-    g.ldx = D;
+    g = wide_gemm(h, w.m_o16, w.t_so[l], T, D, D, TC_EPI_GATED);
+    g.out32 = w.br;
+    g.ldo32 = D;
     g.gate = ms + 2 * D;
     TRY(run_tc(h, g, s, "wide.gemm_o_self"));
     // cross-attention over each sequence's own cache rows 0 .. pos
-    TRY(run_lnmod(h, mc, T, s));
+    TRY(run_lnmod(h, mc, T, true, s));
     g = wide_gemm(h, w.m_a16, w.t_cq[l], T, D, D, TC_EPI_SEGS);
     g.seg_cols = D;
     g.nw0 = h->w_cqn[l];
@@ -1560,28 +1555,28 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
       CK(launch_xattn(xa, 3, false, s, true));
       ++h->last_launches;
     }
-    g = wide_gemm(h, w.m_o16, w.t_co[l], T, D, D, TC_EPI_RESID);
-    g.X = w.X;
-    g.ldx = D;
+    g = wide_gemm(h, w.m_o16, w.t_co[l], T, D, D, TC_EPI_GATED);
+    g.out32 = w.br;
+    g.ldo32 = D;
     g.gate = mc + 2 * D;
     TRY(run_tc(h, g, s, "wide.gemm_o_cross"));
     // MLP
-    TRY(run_lnmod(h, mm, T, s));
+    TRY(run_lnmod(h, mm, T, true, s));
     g = wide_gemm(h, w.m_a16, w.t_f1[l], T, F, D, TC_EPI_F16);
     g.bias = h->b_f1[l];
     g.gelu = 1;
     g.out16 = w.u16;
     g.ldo = F;
     TRY(run_tc(h, g, s, "wide.gemm_fc1"));
-    g = wide_gemm(h, w.m_u16, w.t_f2[l], T, D, F, TC_EPI_RESID);
+    g = wide_gemm(h, w.m_u16, w.t_f2[l], T, D, F, TC_EPI_GATED);
     g.bias = h->b_f2[l];
-    g.X = w.X;
-    g.ldx = D;
+    g.out32 = w.br;
+    g.ldo32 = D;
     g.gate = mm + 2 * D;
     TRY(run_tc(h, g, s, "wide.gemm_fc2"));
   }
-  // final adaLN -> head -> lm_head with the per-row argmax
-  TRY(run_lnmod(h, h->mod + (size_t)(3 * L) * 3 * D, T, s));
+  // the last MLP branch joins the stream; final adaLN -> head -> lm_head with the per-row argmax
+  TRY(run_lnmod(h, h->mod + (size_t)(3 * L) * 3 * D, T, true, s));
   g = wide_gemm(h, w.m_a16, w.t_head, T, Ht, D, TC_EPI_F16);
   g.bias = h->b_head;
   g.out16 = w.y16;
@@ -1733,13 +1728,14 @@ fm_status wide_append(fm_handle *h, int n, const int32_t *ids, const float *feat
     g.out16 = h->pf_c;
     g.ldo = D;
     g.row_st = h->pf_st;
-    g.st_ld = D / 256;
+    g.st_ld = D / 256 * g.ksplit;
+    const int st_n = g.st_ld;
     TRY(run_tc(h, g, s, "append.gemm_fc"));
     CUtensorMap mc;
     if (!make_tma_f16(&mc, h->pf_c, Rm, D, 128)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
     g = wide_gemm(h, mc, h->tm_wkv, Rc, L * 2 * D, D, TC_EPI_KV);
     g.in_st = h->pf_st;
-    g.in_st_n = D / 256;
+    g.in_st_n = st_n;
     g.eps = c.rms_eps;
     g.inv_n = 1.0f / D;
     g.seg_cols = D;

@@ -51,7 +51,7 @@ struct WideParams {
 };
 cudaError_t launch_wide_prep(const float *h0, int D, int T, float *X, const WideParams *wp, int n_max,
                              const __half *table, int H, __half *anc, int n_sm, cudaStream_t s);
-cudaError_t launch_wide_lnmod(const float *X, int D, int T, const float *scale, const float *shift, float eps,
+cudaError_t launch_wide_lnmod(float *X, const float *R, int D, int T, const float *scale, const float *shift, float eps,
                               __half *out, cudaStream_t s);
 cudaError_t launch_wide_self_attn(const float *qkv, int D, int B, int n_seqs, int n_heads, __half *out, cudaStream_t s);
 cudaError_t launch_wide_argmax(const float2 *part, int n_blocks, int T, const WideParams *wp, cudaStream_t s);

@@ -15,9 +15,9 @@
 //               runs the issue loop warp-wide, an elected lane issuing
 //               tcgen05.mma (kind::f16, M 128, N 256, K 16);
 //               tcgen05.commit frees ring stages and publishes accumulators;
-//   warps 2..5  read an accumulator with tcgen05.ld (one row per thread) while
-//               the next tile accumulates into the other buffer, and run the
-//               fused epilogue:
+//   warps 2..9  read an accumulator with tcgen05.ld (two threads per row, one
+//               half of the columns each) while the next tile accumulates into
+//               the other buffer, and run the fused epilogue:
 //                 FC:     C' = (c + bias) * norm_w[n] -> f16 and per-row partial
 //                         sum of squares (the RMSNorm that follows fc);
 //                 KV:     row scale 1/rms(c), per-head RMSNorm (k_norm) and
@@ -25,15 +25,17 @@
 //                         head-major caches of every layer at the row's
 //                         sequence and position;
 //                 F16:    bias (+ exact GELU) -> f16, the next product's operand;
-//                 RESID:  X += gate * (c + bias), the gated residual;
+//                 GATED:  gate * (c + bias), a gated residual branch, f32 out;
 //                 SEGS:   per-head RMSNorm + RoPE of q / k heads, f32 out;
 //                 ARGMAX: per row, the largest logit of the tile (lowest index
 //                         on ties), for the lm_head.
-// Split-K: a tile's K blocks can be dealt to several CTAs; each stores its
-// partial tile to a workspace and the last to finish (atomic ticket) sums the
-// partials in slice order into its TMEM accumulator and runs the epilogue.
+// Split-K: a tile's K blocks can be dealt to a cluster of 2 or 4 CTAs; each
+// stores its partial tile into its own shared memory, and after a cluster
+// barrier each sums its piece of the columns over every slice (distributed
+// shared memory, slice order) and runs the epilogue on that piece.
 // Every mbarrier wait is bounded by a clock budget; on expiry the kernel sets
 // an error flag, drains, frees its TMEM and returns.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,7 +49,11 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, ST = 4;
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE = A_BYTES + B_BYTES;
-constexpr int kThreads = 192;
+// Epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter, each
+// row's columns in two halves) -- the launch picks 8 when every CTA has a
+// single tile, whose epilogue is then not hidden behind a next tile's MMAs.
+__device__ __forceinline__ int n_epi() { return (int)blockDim.x - 64; }   // epilogue threads
+__device__ __forceinline__ int n_halves() { return ((int)blockDim.x - 64) >> 7; }
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s) before a wait gives up
 
 // bounded wait; honor_err = false keeps waiting (by time only) after another role gave up
@@ -104,6 +110,7 @@ __device__ __forceinline__ void tld32(uint32_t taddr, float (&f)[32]) {
   for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
 }
 
+
 __device__ __forceinline__ void store_h8(__half *dst, const float *v) {
   uint4 pk;
   __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
@@ -115,73 +122,164 @@ __device__ __forceinline__ void store_h8(__half *dst, const float *v) {
   *reinterpret_cast<uint4 *>(dst) = pk;
 }
 
-// 32 bf16 values (64-byte aligned), fetched raw (16 registers) and widened when used
-struct Bf16x32 {
-  uint4 u[4];
-};
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16 *__restrict__ p, Bf16x32 &r) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) r.u[q] = __ldg(reinterpret_cast<const uint4 *>(p) + q);
-}
-__device__ __forceinline__ float bf16_at(const Bf16x32 &r, int j) {   // j: a compile-time index
-  const uint4 &u = r.u[j >> 3];
-  const uint32_t w = (j & 7) < 2 ? u.x : (j & 7) < 4 ? u.y : (j & 7) < 6 ? u.z : u.w;
-  return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
-}
-
-// RoPE of 32 interleaved channels: (cos, sin) pairs in 8 float4
-__device__ __forceinline__ void load_rope16(const float2 *__restrict__ p, float4 (&r)[8]) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) r[q] = __ldg(reinterpret_cast<const float4 *>(p) + q);
-}
-__device__ __forceinline__ void apply_rope16(float *v, const float4 (&r)[8]) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float c0 = r[q].x, s0 = r[q].y, c1 = r[q].z, s1 = r[q].w;
-    const float a0 = v[4 * q], a1 = v[4 * q + 1], b0 = v[4 * q + 2], b1 = v[4 * q + 3];
-    v[4 * q] = a0 * c0 - a1 * s0;
-    v[4 * q + 1] = a1 * c0 + a0 * s0;
-    v[4 * q + 2] = b0 * c1 - b1 * s1;
-    v[4 * q + 3] = b1 * c1 + b0 * s1;
-  }
-}
-
-__device__ __forceinline__ void store_f4(float *dst, const float *v) {
+__device__ __forceinline__ void store_f32x32(float *dst, const float *v) {
 #pragma unroll
   for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
 }
-
-// The epilogues below read their per-column operands (norm weights, bias,
-// RoPE rows, the residual) before the chunk's accumulator values, so the
-// global loads are in flight while tcgen05.ld runs.
-
-__device__ void epilogue_fc(const TcGemmArgs &a, uint32_t taddr, int row, int n0, int nb) {
-  float ss = 0.f;
-  const bool live = row < a.M;
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    Bf16x32 w, b;
-    load_bf16x32(a.colw + n0 + c0, w);
-    if (a.bias) load_bf16x32(a.bias + n0 + c0, b);
-    float v[32];
-    tld32(taddr + c0, v);
-    if (!live) continue;
-    if (a.bias) {
+__device__ __forceinline__ void store_f16x32(__half *dst, const float *v) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += bf16_at(b, j);
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      ss += v[j] * v[j];
-      v[j] *= bf16_at(w, j);
-    }
-    __half *dst = a.out16 + (size_t)row * a.ldo + n0 + c0;
-#pragma unroll
-    for (int j = 0; j < 32; j += 8) store_h8(dst + j, v + j);
-  }
-  if (live) a.row_st[(size_t)row * a.st_ld + nb] = ss;
+  for (int j = 0; j < 32; j += 8) store_h8(dst + j, v + j);
 }
 
-__device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
+// Per-column operands of a tile (gate, bias, norm weight), staged once per tile
+// in shared memory by the epilogue threads (one round trip for all of them),
+// and the per-row values the two threads of a row exchange.
+struct EpCols {
+  float gate[BN], bias[BN], w[BN];
+  float xs[2][BM];
+  int xi[2][BM];
+};
+
+__device__ void stage_cols(const TcGemmArgs &a, EpCols *ep, int n0, int i) {
+  named_sync(1, n_epi());   // the previous tile's epilogue has finished reading
+  for (int k = i; k < BN; k += n_epi()) {
+    const int n = n0 + k;
+    float w = 1.f;
+    if (a.epi == TC_EPI_FC) {
+      w = __bfloat162float(a.colw[n]);
+    } else if (a.epi == TC_EPI_SEGS) {
+      const int seg = n / a.seg_cols;
+      const __nv_bfloat16 *nw = seg == 0 ? a.nw0 : seg == 1 ? a.nw1 : nullptr;
+      w = nw ? __bfloat162float(nw[n % a.hd]) : 1.f;
+    } else if (a.epi == TC_EPI_KV) {
+      w = __bfloat162float(a.kn_w[(size_t)((n / a.seg_cols) >> 1) * a.hd + n % a.hd]);
+    }
+    ep->gate[k] = a.gate ? a.gate[n] : 1.f;
+    ep->bias[k] = a.bias ? __bfloat162float(a.bias[n]) : 0.f;
+    ep->w[k] = w;
+  }
+  named_sync(1, n_epi());
+}
+
+// The two epilogue threads of a row (halves 0 and 1) add a per-row value, half 0's first.
+__device__ __forceinline__ float pair_sum(EpCols *ep, int rl, int h, float v) {
+  if (n_halves() == 1) return v;
+  ep->xs[h][rl] = v;
+  named_sync(1, n_epi());
+  const float s = ep->xs[0][rl] + ep->xs[1][rl];
+  named_sync(1, n_epi());
+  return s;
+}
+
+// Each epilogue gets columns [c_lo, c_hi) of the tile (all of it, or the piece a
+// K slice owns after the cluster reduction); the two threads of a row take one
+// half each (h).
+
+__device__ void epilogue_fc(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row, int n0,
+                            int st_col, int c_lo, int c_hi) {
+  float ss = 0.f;
+  const bool live = row < a.M;
+  const int w = (c_hi - c_lo) / n_halves();
+  for (int c0 = c_lo + h * w; c0 < c_lo + (h + 1) * w; c0 += 32) {
+    float v[32];
+    tld32(taddr + c0, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] += ep->bias[c0 + j];
+      ss += v[j] * v[j];
+      v[j] *= ep->w[c0 + j];
+    }
+    if (live) store_f16x32(a.out16 + (size_t)row * a.ldo + n0 + c0, v);
+  }
+  ss = pair_sum(ep, rl, h, ss);
+  if (live && h == 0) a.row_st[(size_t)row * a.st_ld + st_col] = ss;
+}
+
+// rotate the interleaved pairs of 32 channels; r: their 16 (cos, sin) pairs as 8 float4
+__device__ __forceinline__ void rope32(float *v, const float4 (&r)[8]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 cs = r[q];
+    const float a0 = v[4 * q], a1 = v[4 * q + 1], b0 = v[4 * q + 2], b1 = v[4 * q + 3];
+    v[4 * q] = a0 * cs.x - a1 * cs.y;
+    v[4 * q + 1] = a1 * cs.x + a0 * cs.y;
+    v[4 * q + 2] = b0 * cs.z - b1 * cs.w;
+    v[4 * q + 3] = b1 * cs.z + b0 * cs.w;
+  }
+}
+
+// Per-head RMSNorm (weight by channel, from the staged columns; row scale rs
+// first) and RoPE at position p of this thread's half of [c_lo, c_hi), then
+// `emit(col, v)` for each 32-column chunk.  A half narrower than a head (a
+// one-head piece) shares the head's sum of squares with the other half.  The
+// RoPE pairs of the next chunk are requested while the current one is done.
+template <typename Emit>
+__device__ __forceinline__ void norm_rope_half(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h,
+                                               float rs, bool norm, int p, int c_lo, int c_hi, Emit &&emit) {
+  const int hd = a.hd;
+  const float4 *rrow = reinterpret_cast<const float4 *>(a.rope + (size_t)p * (hd >> 1));
+  const int w = (c_hi - c_lo) / n_halves(), lo = c_lo + h * w, hi = lo + w;
+  const bool shared_head = w < hd;   // then [c_lo, c_hi) is one head
+  for (int h0 = shared_head ? c_lo : lo; h0 < (shared_head ? c_lo + 1 : hi); h0 += hd) {
+    const int b0 = shared_head ? lo : h0, b1 = shared_head ? hi : h0 + hd;   // this thread's columns of the head
+    float r2 = 1.f;
+    if (norm) {
+      float ss = 0.f;
+      for (int c0 = b0; c0 < b1; c0 += 32) {
+        float v[32];
+        tld32(taddr + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ss += (v[j] * rs) * (v[j] * rs);
+      }
+      if (shared_head) ss = pair_sum(ep, rl, h, ss);
+      r2 = rsqrtf(ss / (float)hd + a.qk_eps);
+    }
+    // chunks in pairs (this thread's columns of a head are a multiple of 64): pair members use
+    // the register buffers ra / rb, the next chunk's pairs requested one chunk ahead
+    float4 ra[8], rb[8];
+    if (norm) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ra[q] = __ldg(rrow + ((b0 - h0) >> 2) + q);
+    }
+    for (int c0 = b0; c0 < b1; c0 += 64) {
+      if (norm) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) rb[q] = __ldg(rrow + ((c0 + 32 - h0) >> 2) + q);
+      }
+      {
+        float v[32];
+        tld32(taddr + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= rs;
+        if (norm) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * ep->w[c0 + j];
+          rope32(v, ra);
+        }
+        emit(c0, v);
+      }
+      if (norm && c0 + 64 < b1) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ra[q] = __ldg(rrow + ((c0 + 64 - h0) >> 2) + q);
+      }
+      {
+        float v[32];
+        tld32(taddr + c0 + 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= rs;
+        if (norm) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * ep->w[c0 + 32 + j];
+          rope32(v, rb);
+        }
+        emit(c0 + 32, v);
+      }
+    }
+  }
+}
+
+__device__ void epilogue_kv(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row, int n0, int c_lo,
+                            int c_hi) {
   const bool live = row < a.M;
   const int seg = n0 / a.seg_cols;
   const int layer = seg >> 1, kind = seg & 1;
@@ -193,159 +291,61 @@ __device__ void epilogue_kv(const TcGemmArgs &a, uint32_t taddr, int row, int n0
     rs = rsqrtf(s * a.inv_n + a.eps);
   }
   const int p = a.row_pos ? (live ? a.row_pos[row] : 0) : a.start + row;
-  __half *cache = a.cache + (a.row_seq && live ? (size_t)a.row_seq[row] * a.seq_stride : 0);
-  const float2 *rrow = a.rope + (size_t)p * (hd >> 1);
-  for (int h0 = 0; h0 < BN; h0 += hd) {
-    const int head = ((n0 % a.seg_cols) + h0) / hd;
-    float r2 = 1.f;
-    if (kind == 0) {
-      float ss = 0.f;
-      for (int c0 = 0; c0 < hd; c0 += 32) {
-        float v[32];
-        tld32(taddr + h0 + c0, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ss += (v[j] * rs) * (v[j] * rs);
-      }
-      r2 = rsqrtf(ss / (float)hd + a.qk_eps);
-    }
-    __half *dst = cache + (size_t)(layer * 2 + kind) * a.plane + ((size_t)head * a.max_ctx + p) * hd;
-    const __nv_bfloat16 *kw = a.kn_w + (size_t)layer * hd;
-    for (int c0 = 0; c0 < hd; c0 += 32) {
-      Bf16x32 w;
-      float4 rp[8];
-      if (kind == 0) {
-        load_bf16x32(kw + c0, w);
-        load_rope16(rrow + (c0 >> 1), rp);
-      }
-      float v[32];
-      tld32(taddr + h0 + c0, v);
-      if (!live) continue;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= rs;
-      if (kind == 0) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * bf16_at(w, j);
-        apply_rope16(v, rp);
-      }
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) store_h8(dst + c0 + j, v + j);
-    }
-  }
+  __half *cache = a.cache + (a.row_seq && live ? (size_t)a.row_seq[row] * a.seq_stride : 0) +
+                  (size_t)(layer * 2 + kind) * a.plane + (size_t)p * hd;
+  const int head0 = (n0 % a.seg_cols) / hd;
+  norm_rope_half(a, ep, taddr, rl, h, rs, kind == 0, p, c_lo, c_hi, [&](int c0, const float *v) {
+    if (live) store_f16x32(cache + (size_t)(head0 + c0 / hd) * a.max_ctx * hd + c0 % hd, v);
+  });
 }
 
-__device__ void epilogue_f16(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
+// q / k / v rows: segment s = n / seg_cols; segments 0 and 1 take a per-head
+// RMSNorm with their weight (when given) and RoPE at the row's position
+__device__ void epilogue_segs(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row, int n0,
+                              int c_lo, int c_hi) {
   const bool live = row < a.M;
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    Bf16x32 bias;
-    if (a.bias) load_bf16x32(a.bias + n0 + c0, bias);
+  const int seg = n0 / a.seg_cols;
+  const bool norm = (seg == 0 && a.nw0) || (seg == 1 && a.nw1);
+  const int p = live ? (a.row_pos ? a.row_pos[row] : a.start + row) : 0;
+  float *out = a.out32 + (size_t)(live ? row : 0) * a.ldo32 + n0;
+  norm_rope_half(a, ep, taddr, rl, h, 1.f, norm, p, c_lo, c_hi, [&](int c0, const float *v) {
+    if (live) store_f32x32(out + c0, v);
+  });
+}
+
+// F16: bias (+ exact GELU) -> f16; GATED: gate * (acc + bias) -> f32 (the residual
+// stream adds it in the next kernel)
+__device__ void epilogue_f16(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int h, int row, int n0, int c_lo,
+                             int c_hi) {
+  const bool live = row < a.M;
+  const bool gated = a.epi == TC_EPI_GATED;
+  const int w = (c_hi - c_lo) / n_halves();
+  for (int c0 = c_lo + h * w; c0 < c_lo + (h + 1) * w; c0 += 32) {
     float v[32];
     tld32(taddr + c0, v);
-    if (!live) continue;
-    if (a.bias) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += bf16_at(bias, j);
+    for (int j = 0; j < 32; ++j) v[j] += ep->bias[c0 + j];
+    if (gated) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= ep->gate[c0 + j];
     }
-    if (a.out32) store_f4(a.out32 + (size_t)row * a.ldo32 + n0 + c0, v);
+    if (!live) continue;
+    if (a.out32) store_f32x32(a.out32 + (size_t)row * a.ldo32 + n0 + c0, v);
     if (!a.out16) continue;
     if (a.gelu) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
     }
-    __half *dst = a.out16 + (size_t)row * a.ldo + n0 + c0;
-#pragma unroll
-    for (int j = 0; j < 32; j += 8) store_h8(dst + j, v + j);
+    store_f16x32(a.out16 + (size_t)row * a.ldo + n0 + c0, v);
   }
 }
 
-// X += gate * (acc + bias).  With one tile per CTA this epilogue's latency is
-// exposed: the next chunk's residual values (L2) are requested before the
-// current chunk is finished; gate and bias are shared by every row (L1).
-__device__ void epilogue_resid(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
-  const bool live = row < a.M;
-  float *__restrict__ x = a.X + (size_t)(live ? row : 0) * a.ldx + n0;
-  const float4 *__restrict__ g4 = reinterpret_cast<const float4 *>(a.gate + n0);
-  const uint2 *__restrict__ b4 = a.bias ? reinterpret_cast<const uint2 *>(a.bias + n0) : nullptr;
-  float4 xv[2][8];
-  auto fetch = [&](int c0, int b) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      xv[b][q] = live ? __ldcg(reinterpret_cast<const float4 *>(x + c0) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-  };
-  fetch(0, 0);
-#pragma unroll
-  for (int c = 0; c < BN / 32; ++c) {
-    const int c0 = 32 * c, b = c & 1;
-    if (c + 1 < BN / 32) fetch(c0 + 32, b ^ 1);
-    float v[32];
-    tld32(taddr + c0, v);
-    if (!live) continue;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 gg = __ldg(g4 + 8 * c + q);
-      float bb[4] = {0.f, 0.f, 0.f, 0.f};
-      if (b4) {
-        const uint2 u = __ldg(b4 + 8 * c + q);
-        bb[0] = __uint_as_float(u.x << 16);
-        bb[1] = __uint_as_float(u.x & 0xffff0000u);
-        bb[2] = __uint_as_float(u.y << 16);
-        bb[3] = __uint_as_float(u.y & 0xffff0000u);
-      }
-      float4 o = xv[b][q];
-      o.x += gg.x * (v[4 * q] + bb[0]);
-      o.y += gg.y * (v[4 * q + 1] + bb[1]);
-      o.z += gg.z * (v[4 * q + 2] + bb[2]);
-      o.w += gg.w * (v[4 * q + 3] + bb[3]);
-      __stcg(reinterpret_cast<float4 *>(x + c0) + q, o);
-    }
-  }
-}
-
-// q / k / v rows: segment s = n / seg_cols; segments 0 and 1 take a per-head
-// RMSNorm with their weight (when given) and RoPE at the row's position
-__device__ void epilogue_segs(const TcGemmArgs &a, uint32_t taddr, int row, int n0) {
-  const bool live = row < a.M;
-  const int seg = n0 / a.seg_cols;
-  const __nv_bfloat16 *nw = seg == 0 ? a.nw0 : seg == 1 ? a.nw1 : nullptr;
-  const int hd = a.hd;
-  const int p = live ? (a.row_pos ? a.row_pos[row] : a.start + row) : 0;
-  const float2 *rrow = a.rope + (size_t)p * (hd >> 1);
-  float *__restrict__ out = a.out32 + (size_t)(live ? row : 0) * a.ldo32 + n0;
-  for (int h0 = 0; h0 < BN; h0 += hd) {
-    float r2 = 1.f;
-    if (nw) {
-      float ss = 0.f;
-      for (int c0 = 0; c0 < hd; c0 += 32) {
-        float v[32];
-        tld32(taddr + h0 + c0, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ss += v[j] * v[j];
-      }
-      r2 = rsqrtf(ss / (float)hd + a.qk_eps);
-    }
-    for (int c0 = 0; c0 < hd; c0 += 32) {
-      Bf16x32 w;
-      float4 rp[8];
-      if (nw) {
-        load_bf16x32(nw + c0, w);
-        load_rope16(rrow + (c0 >> 1), rp);
-      }
-      float v[32];
-      tld32(taddr + h0 + c0, v);
-      if (!live) continue;
-      if (nw) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = v[j] * r2 * bf16_at(w, j);
-        apply_rope16(v, rp);
-      }
-      store_f4(out + h0 + c0, v);
-    }
-  }
-}
-
-__device__ void epilogue_argmax(const TcGemmArgs &a, uint32_t taddr, int row, int n0, int nb) {
+__device__ void epilogue_argmax(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row, int n0,
+                                int nb) {
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  for (int c0 = 0; c0 < BN; c0 += 32) {
+  const int hw = BN / n_halves();
+  for (int c0 = h * hw; c0 < (h + 1) * hw; c0 += 32) {
     float v[32];
     tld32(taddr + c0, v);
 #pragma unroll
@@ -355,89 +355,109 @@ __device__ void epilogue_argmax(const TcGemmArgs &a, uint32_t taddr, int row, in
         bi = n0 + c0 + j;
       }
   }
-  if (row < a.M) a.amax[(size_t)row * a.amax_ld + nb] = make_float2(best, __int_as_float(bi));
+  if (n_halves() == 1) {
+    if (row < a.M) a.amax[(size_t)row * a.amax_ld + nb] = make_float2(best, __int_as_float(bi));
+    return;
+  }
+  ep->xs[h][rl] = best;
+  ep->xi[h][rl] = bi;
+  named_sync(1, n_epi());
+  if (h == 0 && row < a.M) {
+    // the upper half's columns come later: it wins only with a strictly larger value
+    const float b1 = ep->xs[1][rl];
+    if (b1 > best) {
+      best = b1;
+      bi = ep->xi[1][rl];
+    }
+    a.amax[(size_t)row * a.amax_ld + nb] = make_float2(best, __int_as_float(bi));
+  }
+  named_sync(1, n_epi());
 }
 
-// Split-K partial tiles in the workspace: per (tile, slice) 8 chunk blocks of
-// 128 rows x 32 f32 (16 KB each), the 16-byte units of a row XOR-swizzled by
-// (row & 7) so that a warp's reads of one unit column spread over the banks.
-__device__ __forceinline__ size_t ws_block(int tile, int ks, int slice, int c) {
-  return ((((size_t)tile * ks + slice) * 8 + c) * BM) * 32;
-}
-
-// Split-K: store this slice's partial tile; the last slice of the tile to get
-// here sums every slice's partial (in slice order, its own from TMEM) back into
-// the accumulator.  The other slices' blocks come through the bulk-copy engine
-// into the operand ring, which is idle by then (a split GEMM gives each CTA
-// one unit), two chunks in flight.  Returns whether this CTA runs the tile's
-// epilogue.  All 128 epilogue threads call it together.
-__device__ bool splitk_gather(const TcGemmArgs &a, uint32_t taddr, int rl, int tile, int slice, int *s_last,
-                              uint32_t stage, const uint8_t *stage_ptr, uint32_t gbar) {
-  const int ks = a.ksplit;
-  const int sw = rl & 7;
-  for (int c = 0; c < BN / 32; ++c) {
+// Split-K partial tile in shared memory (the operand ring, idle once the MMAs
+// are done): 8 chunk blocks of 128 rows x 32 f32, the 16-byte units of a row
+// XOR-swizzled by (row & 7) so that a warp's accesses spread over the banks.
+// Half h of the epilogue threads stores its share of the chunks.
+__device__ __forceinline__ void store_partial(uint32_t taddr, int rl, int h, float *part) {
+  const int sw = rl & 7, per = (BN / 32) / n_halves();
+  for (int c = per * h; c < per * (h + 1); ++c) {
     float v[32];
     tld32(taddr + 32 * c, v);
-    float *dst = a.ws + ws_block(tile, ks, slice, c) + (size_t)rl * 32;
+    float *dst = part + ((size_t)c * BM + rl) * 32;
 #pragma unroll
     for (int u = 0; u < 8; ++u)
       *reinterpret_cast<float4 *>(dst + 4 * (u ^ sw)) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
   }
-  named_sync(1, 128);
-  if (threadIdx.x == 64) {
-    __threadfence();
-    const int old = atomicAdd(a.tile_tickets + tile, 1);
-    const int last = old == ks - 1;
-    if (last) atomicExch(a.tile_tickets + tile, 0);
-    *s_last = last;
-  }
-  named_sync(1, 128);
-  if (!*s_last) return false;
-  __threadfence();
-  constexpr uint32_t kBlk = BM * 32 * 4;
-  const uint32_t buf = (uint32_t)(ks - 1) * kBlk;
-  auto issue = [&](int c) {
-    const uint32_t bar = gbar + 8 * (c & 1);
-    mbar_expect_tx(bar, buf);
-    int k = 0;
-    for (int s = 0; s < ks; ++s)
-      if (s != slice) bulk_g2s(stage + (c & 1) * buf + (k++) * kBlk, a.ws + ws_block(tile, ks, s, c), kBlk, bar);
-  };
-  if (threadIdx.x == 64) {
-    // the blocks were written through the generic proxy by other CTAs
-    asm volatile("fence.proxy.async.global;\n" ::: "memory");
-    issue(0);
-    issue(1);
-  }
-  for (int c = 0; c < BN / 32; ++c) {
-    const int b = c & 1;
-    mbar_wait_bounded(gbar + 8 * b, (c >> 1) & 1, a.err);
-    float v[32], acc[32];
-    tld32(taddr + 32 * c, v);
+}
+
+// This half's columns of [c_lo, c_hi) summed over the cluster's K slices in
+// slice order (deterministic), into TMEM.  Warp q reads its 32 rows of each
+// slice's chunk block (4 KB, contiguous) with 512-byte instructions from the
+// slices' shared memory (distributed shared memory serves contiguous reads far
+// better than 32 rows' scattered 16-byte pieces), sums, and turns the sums back
+// into one row per lane through its own block.
+__device__ void reduce_piece(uint32_t taddr, int rl, int h, float *part, int ks, int c_lo, int c_hi) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int q = rl >> 5, l = rl & 31, sw = rl & 7;
+  const int w = (c_hi - c_lo) / n_halves();
+  for (int c = (c_lo + h * w) / 32; c < (c_lo + (h + 1) * w) / 32; ++c) {
+    float4 acc[8];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-    int k = 0;
+    for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float *mine = part + ((size_t)c * BM + 32 * q) * 32;
     for (int s = 0; s < ks; ++s) {
-      if (s == slice) {
+      const float *src = cluster.map_shared_rank(mine, s);
+      float4 t[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] += v[j];
-      } else {
-        const float *blk = reinterpret_cast<const float *>(stage_ptr + b * buf + (k++) * kBlk) + (size_t)rl * 32;
+      for (int i = 0; i < 8; ++i) t[i] = *reinterpret_cast<const float4 *>(src + (i * 32 + l) * 4);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 q = *reinterpret_cast<const float4 *>(blk + 4 * (u ^ sw));
-          acc[4 * u] += q.x;
-          acc[4 * u + 1] += q.y;
-          acc[4 * u + 2] += q.z;
-          acc[4 * u + 3] += q.w;
-        }
+      for (int i = 0; i < 8; ++i) {
+        acc[i].x += t[i].x;
+        acc[i].y += t[i].y;
+        acc[i].z += t[i].z;
+        acc[i].w += t[i].w;
       }
     }
-    tmem_st32(taddr + 32 * c, acc);
-    named_sync(1, 128);   // buffer b has been read by the group
-    if (threadIdx.x == 64 && c + 2 < BN / 32) issue(c + 2);
+    // this block is this CTA's own piece: no peer reads it
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) *reinterpret_cast<float4 *>(mine + (i * 32 + l) * 4) = acc[i];
+    __syncwarp();
+    float v[32];
+    const float *row = mine + (size_t)l * 32;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float4 t = *reinterpret_cast<const float4 *>(row + 4 * (u ^ sw));
+      v[4 * u] = t.x;
+      v[4 * u + 1] = t.y;
+      v[4 * u + 2] = t.z;
+      v[4 * u + 3] = t.w;
+    }
+    tmem_st32(taddr + 32 * c, v);
   }
-  return true;
+}
+
+// Column pieces a split tile's epilogue is dealt in: whole heads for the
+// per-head norms, the whole tile for the argmax, else 256 / ks columns.
+__device__ __forceinline__ int epilogue_pieces(const TcGemmArgs &a, int ks) {
+  if (a.epi == TC_EPI_ARGMAX) return 1;
+  if (a.epi == TC_EPI_KV || a.epi == TC_EPI_SEGS) return ks < BN / a.hd ? ks : BN / a.hd;
+  return ks;
+}
+
+__device__ __forceinline__ void run_epilogue(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row,
+                                             int nb, int st_col, int c_lo, int c_hi) {
+  const int n0 = nb * BN;
+  if (a.epi != TC_EPI_ARGMAX) stage_cols(a, ep, n0, (int)threadIdx.x - 64);
+  switch (a.epi) {
+    case TC_EPI_FC: epilogue_fc(a, ep, taddr, rl, h, row, n0, st_col, c_lo, c_hi); break;
+    case TC_EPI_KV: epilogue_kv(a, ep, taddr, rl, h, row, n0, c_lo, c_hi); break;
+    case TC_EPI_F16:
+    case TC_EPI_GATED: epilogue_f16(a, ep, taddr, h, row, n0, c_lo, c_hi); break;
+    case TC_EPI_SEGS: epilogue_segs(a, ep, taddr, rl, h, row, n0, c_lo, c_hi); break;
+    default: epilogue_argmax(a, ep, taddr, rl, h, row, n0, nb); break;
+  }
 }
 
 // tile -> (row block, column block) in the grouped order of TcGemmArgs::group_m
@@ -451,17 +471,20 @@ __device__ __forceinline__ void tile_coords(int tile, int n_mb, int n_nb, int gm
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
+// NT: threads per CTA (192: 4 epilogue warps, 320: 8), the register budget follows
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) fm_prefill_gemm_kernel(const __grid_constant__ TcGemmArgs a) {
+  __builtin_assume(blockDim.x == NT);   // the epilogue's split into halves is known at compile time
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
+  uint8_t *gbase = smem_raw + (base - smem_u32(smem_raw));
   const uint32_t bars = base + ST * STAGE;
   auto full = [&](int s) { return bars + 8 * s; };
   auto empty = [&](int s) { return bars + 8 * (ST + s); };
   auto tfull = [&](int b) { return bars + 8 * (2 * ST + b); };
   auto tempty = [&](int b) { return bars + 8 * (2 * ST + 2 + b); };
   const uint32_t tslot = bars + 8 * (2 * ST + 4);
-  const uint32_t gbar = bars + 8 * (2 * ST + 5);   // two: split-K gather buffers
+  EpCols *ep = reinterpret_cast<EpCols *>(gbase + ST * STAGE + 256);   // the epilogue's staged columns
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == 0 && lane == 0) {
@@ -471,8 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull(b), 1);
-      mbar_init(tempty(b), 128);
-      mbar_init(gbar + 8 * b, 1);
+      mbar_init(tempty(b), n_epi());
     }
     mbar_fence_init();
   }
@@ -486,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
   const uint32_t tmem = lds32(tslot);
 
   pdl_trigger();
-  pdl_wait();
+  // the producer waits for the previous kernel itself, after requesting its first weight tiles
+  if (warp != 0) pdl_wait();
 
   const int n_nb = a.N / BN;
   const int n_mb = (a.M + BM - 1) / BM;
@@ -502,6 +525,21 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
 
   if (warp == 0) {
     if (lane == 0) {
+      // B (weights, or the token table) is never written by an earlier kernel: the first
+      // unit's first stages request their B tiles before griddepcontrol.wait, their A
+      // tiles (activations) after it
+      int pre = 0;
+      if ((int)blockIdx.x < n_units) {
+        int mb, nb, kb0, kb1;
+        tile_coords(blockIdx.x / ks, n_mb, n_nb, gm, mb, nb);
+        kslice(blockIdx.x % ks, kb0, kb1);
+        pre = kb1 - kb0 < ST ? kb1 - kb0 : ST;
+        for (int j = 0; j < pre; ++j) {
+          mbar_expect_tx(full(j), STAGE);
+          tma_load_2d(base + j * STAGE + A_BYTES, &a.tma_b, (kb0 + j) * BK, nb * BN, full(j));
+        }
+      }
+      pdl_wait();
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -510,8 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
         kslice(u % ks, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % ST;
-          if (!mbar_wait(empty(s), ((it / ST) & 1) ^ 1, a.err)) { ok = false; break; }
           const uint32_t sa = base + s * STAGE, sb = sa + A_BYTES;
+          if ((int)it < pre) {   // stage set up before the wait: only its A tile is missing
+            tma_load_2d(sa, &a.tma_a, kb * BK, a.a_row0 + mb * BM, full(s));
+            continue;
+          }
+          if (!mbar_wait(empty(s), ((it / ST) & 1) ^ 1, a.err)) { ok = false; break; }
           mbar_expect_tx(full(s), STAGE);
           tma_load_2d(sa, &a.tma_a, kb * BK, a.a_row0 + mb * BM, full(s));
           tma_load_2d(sb, &a.tma_b, kb * BK, nb * BN, full(s));
@@ -548,32 +590,49 @@ __global__ void __launch_bounds__(kThreads, 1) fm_prefill_gemm_kernel(const __gr
   } else {
     const int quad = warp & 3;  // TMEM lanes 32 * quad .. + 31 belong to this warp
     const int rl = quad * 32 + lane;
-    __shared__ int s_last;
+    const int half = (warp - 2) >> 2;   // the two warps of a lane quarter split the columns
     uint32_t tc = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++tc) {
       const int b = tc & 1;
-      const bool ok = mbar_wait(tfull(b), (tc >> 1) & 1, a.err);
-      // with K slices the group meets at named barriers: its verdict must be one
-      if (ks > 1 ? bar_any(1, 128, !ok) : !ok) break;
+      if (!mbar_wait(tfull(b), (tc >> 1) & 1, a.err)) break;
       tc_fence_after();
-      const int tile = u / ks;
-      int mb, nb;
-      tile_coords(tile, n_mb, n_nb, gm, mb, nb);
       const uint32_t taddr = tmem + b * BN + ((uint32_t)(quad * 32) << 16);
-      const int row = mb * BM + rl;
-      if (ks == 1 || splitk_gather(a, taddr, rl, tile, u % ks, &s_last, base, gbase, gbar)) {
-        switch (a.epi) {
-          case TC_EPI_FC: epilogue_fc(a, taddr, row, nb * BN, nb); break;
-          case TC_EPI_KV: epilogue_kv(a, taddr, row, nb * BN); break;
-          case TC_EPI_F16: epilogue_f16(a, taddr, row, nb * BN); break;
-          case TC_EPI_RESID: epilogue_resid(a, taddr, row, nb * BN); break;
-          case TC_EPI_SEGS: epilogue_segs(a, taddr, row, nb * BN); break;
-          default: epilogue_argmax(a, taddr, row, nb * BN, nb); break;
-        }
+      if (ks > 1) {
+        // this slice's partial tile goes to the cluster reduction below
+        store_partial(taddr, rl, half, reinterpret_cast<float *>(gbase));
+        continue;
       }
+      int mb, nb;
+      tile_coords(u, n_mb, n_nb, gm, mb, nb);
+      run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb, 0, BN);
       tc_fence_before();
       mbar_arrive(tempty(b));
     }
+  }
+  if (ks > 1) {
+    // Split-K over a cluster of the tile's ks slices (one unit per CTA): every
+    // slice's partial is in its shared memory; slice s sums its piece of the
+    // columns over all slices (slice order) and runs the epilogue there.
+    __syncwarp();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    const int u = blockIdx.x, slice = u % ks;
+    if (warp >= 2 && u < n_units) {
+      const int quad = warp & 3, rl = quad * 32 + lane, half = (warp - 2) >> 2;
+      int mb, nb;
+      tile_coords(u / ks, n_mb, n_nb, gm, mb, nb);
+      const int pieces = epilogue_pieces(a, ks);
+      if (slice < pieces) {
+        const int w = BN / pieces, c_lo = slice * w;
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
+        tc_fence_after();
+        reduce_piece(taddr, rl, half, reinterpret_cast<float *>(gbase), ks, c_lo, c_lo + w);
+        run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb * pieces + slice, c_lo, c_lo + w);
+      }
+    }
+    // no CTA leaves (or frees its shared memory) while a peer may still read its partial
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
   }
   tc_fence_before();
   __syncthreads();
@@ -630,31 +689,41 @@ bool make_tma_f16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
-size_t tc_gemm_smem_bytes() { return (size_t)ST * STAGE + 1024 + 256; }
+size_t tc_gemm_smem_bytes() { return (size_t)ST * STAGE + 1024 + 256 + sizeof(EpCols); }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs &a, int n_sm, cudaStream_t s) {
   if (a.N % BN != 0 || a.K % BK != 0 || a.M < 1) return cudaErrorInvalidValue;
   const int ks = a.ksplit > 1 ? a.ksplit : 1;
-  if (ks > a.K / BK || (ks > 1 && (!a.ws || !a.tile_tickets))) return cudaErrorInvalidValue;
   const int n_units = ((a.M + BM - 1) / BM) * (a.N / BN) * ks;
-  // a split GEMM gives each CTA one unit (the gather stages its partials in the idle operand
-  // ring: two chunks of ks - 1 blocks of 16 KB must fit)
-  if (ks > 1 && (n_units > n_sm || 2 * (ks - 1) * BM * 32 * 4 > ST * STAGE)) return cudaErrorInvalidValue;
-  const int grid = n_units < n_sm ? n_units : n_sm;
+  // K slices: a power of two up to 4 (a cluster of them per tile, 256 / ks columns each in the epilogue),
+  // one unit per CTA
+  if (ks > 1 && (ks > 4 || (ks & (ks - 1)) || ks > a.K / BK || n_units > n_sm)) return cudaErrorInvalidValue;
+  const int grid = ks > 1 ? n_units : (n_units < n_sm ? n_units : n_sm);
   const size_t smem = tc_gemm_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(fm_prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // two epilogue threads per row when each CTA has one tile (its epilogue is not overlapped)
+  const bool wide_epi = grid >= n_units;
+  auto kern = wide_epi ? fm_prefill_gemm_kernel<64 + 256> : fm_prefill_gemm_kernel<64 + 128>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(wide_epi ? 64 + 256 : 64 + 128, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 1;
+  if (ks > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = ks;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fm_prefill_gemm_kernel, a);
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 cudaError_t launch_f32_to_f16(const float *in, __half *out, size_t n, int n_sm, cudaStream_t s) {

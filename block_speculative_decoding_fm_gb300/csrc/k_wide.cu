@@ -5,9 +5,11 @@
 //   * wide_prep       every slot row starts at h0 (``init``: the jump from zero
 //                     noise), and each sequence's anchor row is gathered from
 //                     the f16 token table (the anchor_proj operand);
-//   * wide_lnmod      adaLN LayerNorm-modulate of each row (``lnMod``): two-pass
-//                     mean / population variance, * (1 + scale) + shift, f16 out
-//                     (the next product's operand);
+//   * wide_lnmod      adds the gated branch of the previous product to the
+//                     residual stream (``gateAdd``), then adaLN LayerNorm-modulate
+//                     of each row (``lnMod``): two-pass mean / population
+//                     variance, * (1 + scale) + shift, f16 out (the next
+//                     product's operand);
 //   * wide_self_attn  the block's self-attention per sequence and head (no
 //                     mask, ``attn`` over the 16 slots), f16 out;
 //   * wide_argmax     the per-row reduction of the lm_head's per-tile bests
@@ -42,22 +44,33 @@ __global__ void wide_prep_kernel(const float *__restrict__ h0, int D, int T, flo
   }
 }
 
-// one warp per row; D <= 4096, a multiple of 128
-__global__ void wide_lnmod_kernel(const float *__restrict__ X, int D, int T, const float *__restrict__ scale,
-                                  const float *__restrict__ shift, float eps, __half *__restrict__ out) {
+// one warp per row; D <= 4096, a multiple of 128.  With R: the residual stream
+// first takes the gated branch the previous product wrote (X += R, stored back).
+__global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict__ R, int D, int T,
+                                  const float *__restrict__ scale, const float *__restrict__ shift, float eps,
+                                  __half *__restrict__ out) {
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + warp;
   if (row >= T) return;
   const int per = D / 128;   // float4 per lane
-  const float4 *x = reinterpret_cast<const float4 *>(X + (size_t)row * D);
+  float4 *x = reinterpret_cast<float4 *>(X + (size_t)row * D);
+  const float4 *r = R ? reinterpret_cast<const float4 *>(R + (size_t)row * D) : nullptr;
   float4 v[32];
   float s = 0.f;
 #pragma unroll
   for (int u = 0; u < 32; ++u) {
     if (u < per) {
       v[u] = x[u * 32 + lane];
+      if (r) {
+        const float4 g = r[u * 32 + lane];
+        v[u].x += g.x;
+        v[u].y += g.y;
+        v[u].z += g.z;
+        v[u].w += g.w;
+        x[u * 32 + lane] = v[u];
+      }
       s += (v[u].x + v[u].y) + (v[u].z + v[u].w);
     }
   }
@@ -214,11 +227,12 @@ cudaError_t launch_wide_prep(const float *h0, int D, int T, float *X, const Wide
   return launch_pdl((const void *)wide_prep_kernel, dim3(grid), dim3(256), args, s);
 }
 
-cudaError_t launch_wide_lnmod(const float *X, int D, int T, const float *scale, const float *shift, float eps,
+cudaError_t launch_wide_lnmod(float *X, const float *R, int D, int T, const float *scale, const float *shift, float eps,
                               __half *out, cudaStream_t s) {
   if (D % 128 || D > 4096) return cudaErrorInvalidValue;
-  void *args[] = {(void *)&X, (void *)&D, (void *)&T, (void *)&scale, (void *)&shift, (void *)&eps, (void *)&out};
-  return launch_pdl((const void *)wide_lnmod_kernel, dim3((T + 7) / 8), dim3(256), args, s);
+  void *args[] = {(void *)&X, (void *)&R, (void *)&D, (void *)&T, (void *)&scale, (void *)&shift, (void *)&eps,
+                  (void *)&out};
+  return launch_pdl((const void *)wide_lnmod_kernel, dim3((T + 3) / 4), dim3(128), args, s);
 }
 
 cudaError_t launch_wide_self_attn(const float *qkv, int D, int B, int n_seqs, int n_heads, __half *out, cudaStream_t s) {

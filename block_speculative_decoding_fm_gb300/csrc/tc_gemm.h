@@ -15,7 +15,7 @@ enum TcEpi : int32_t {
   TC_EPI_KV = 1,      // row scale 1/rms, k_norm + RoPE on K heads, f16 stores into the head-major caches
   TC_EPI_F16 = 2,     // out16 = f16(act(acc + bias)), act = identity or exact GELU (out16 null: none);
                       // optionally out32 = acc + bias
-  TC_EPI_RESID = 3,   // X[row][n] += gate[n] * (acc + bias[n])   (gated residual, f32 in place)
+  TC_EPI_GATED = 3,   // out32[row][n] = gate[n] * (acc + bias[n])   (a gated residual branch)
   TC_EPI_SEGS = 4,    // out32: per-head RMSNorm + interleaved-pair RoPE on segments 0 / 1, plain elsewhere
   TC_EPI_ARGMAX = 5,  // per row, the best (value, lowest index) over the tile's columns < n_valid
 };
@@ -31,13 +31,12 @@ struct TcGemmArgs {
   int32_t group_m;
   int32_t *err;       // set to 1 when a bounded wait gives up
   int32_t a_row0;     // A rows start at this row of the map (rows past the map's extent read as zero)
-  // split-K: each output tile is computed as ksplit slices of the K blocks; a
-  // slice stores its partial tile into ws and takes a ticket, and the last
-  // slice to finish sums the partials in slice order (deterministic) and runs
-  // the epilogue.  ksplit 1: no workspace.
+  // split-K: each output tile is computed by a cluster of ksplit CTAs (1, 2 or
+  // 4), one K slice each; the partial tiles are summed through distributed
+  // shared memory in slice order (deterministic), slice s finishing its piece
+  // of the columns (an FC output then has ksplit row-statistics entries per
+  // 256 columns: st_ld = N / 256 * ksplit)
   int32_t ksplit;
-  float *ws;                  // [tiles][ksplit][128][256]
-  int32_t *tile_tickets;      // [tiles], zero between launches
   // FC
   const __nv_bfloat16 *colw;
   __half *out16;
@@ -60,13 +59,11 @@ struct TcGemmArgs {
   const int32_t *row_pos;
   const int32_t *row_seq;
   size_t seq_stride;
-  // F16 / RESID / FC
+  // F16 / GATED / FC
   const __nv_bfloat16 *bias;  // [N] or null
   int32_t gelu;
-  float *X;                   // RESID: [M][ldx]
-  const float *gate;          // RESID: [N]
-  int32_t ldx;
-  // SEGS (and F16's optional f32 copy)
+  const float *gate;          // GATED: [N]
+  // SEGS, GATED (and F16's optional f32 copy)
   float *out32;
   int32_t ldo32;
   const __nv_bfloat16 *nw0, *nw1;  // per-head norm weights [hd] of segments 0 and 1 (null: plain)
