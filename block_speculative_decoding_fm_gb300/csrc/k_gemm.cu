@@ -446,10 +446,12 @@ __device__ __forceinline__ int epilogue_pieces(const TcGemmArgs &a, int ks) {
   return ks;
 }
 
+// staged: the tile's columns are already in shared memory (the CTA's first tile, staged
+// before griddepcontrol.wait)
 __device__ __forceinline__ void run_epilogue(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row,
-                                             int nb, int st_col, int c_lo, int c_hi) {
+                                             int nb, int st_col, int c_lo, int c_hi, bool staged) {
   const int n0 = nb * BN;
-  if (a.epi != TC_EPI_ARGMAX) stage_cols(a, ep, n0, (int)threadIdx.x - 64);
+  if (a.epi != TC_EPI_ARGMAX && !staged) stage_cols(a, ep, n0, (int)threadIdx.x - 64);
   switch (a.epi) {
     case TC_EPI_FC: epilogue_fc(a, ep, taddr, rl, h, row, n0, st_col, c_lo, c_hi); break;
     case TC_EPI_KV: epilogue_kv(a, ep, taddr, rl, h, row, n0, c_lo, c_hi); break;
@@ -508,8 +510,6 @@ __global__ void __launch_bounds__(NT, 1) fm_prefill_gemm_kernel(const __grid_con
   const uint32_t tmem = lds32(tslot);
 
   pdl_trigger();
-  // the producer waits for the previous kernel itself, after requesting its first weight tiles
-  if (warp != 0) pdl_wait();
 
   const int n_nb = a.N / BN;
   const int n_mb = (a.M + BM - 1) / BM;
@@ -518,6 +518,14 @@ __global__ void __launch_bounds__(NT, 1) fm_prefill_gemm_kernel(const __grid_con
   const int nk = a.K / BK;
   const int ks = a.ksplit > 1 ? a.ksplit : 1;
   const int n_units = n_tiles * ks;   // unit u: tile u / ks, K slice u % ks (slices of a tile adjacent)
+  // Nothing an earlier kernel writes is read before griddepcontrol.wait: the producer requests its first
+  // weight tiles first, the epilogue warps stage the first tile's per-column operands (weights) first.
+  if (warp >= 2 && a.epi != TC_EPI_ARGMAX && (int)blockIdx.x < n_units) {
+    int mb0, nb0;
+    tile_coords(blockIdx.x / ks, n_mb, n_nb, gm, mb0, nb0);
+    stage_cols(a, ep, nb0 * BN, (int)threadIdx.x - 64);
+  }
+  if (warp != 0) pdl_wait();
   auto kslice = [&](int slice, int &kb0, int &kb1) {
     kb0 = slice * nk / ks;
     kb1 = (slice + 1) * nk / ks;
@@ -604,7 +612,7 @@ __global__ void __launch_bounds__(NT, 1) fm_prefill_gemm_kernel(const __grid_con
       }
       int mb, nb;
       tile_coords(u, n_mb, n_nb, gm, mb, nb);
-      run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb, 0, BN);
+      run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb, 0, BN, tc == 0);
       tc_fence_before();
       mbar_arrive(tempty(b));
     }
@@ -627,7 +635,7 @@ __global__ void __launch_bounds__(NT, 1) fm_prefill_gemm_kernel(const __grid_con
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
         tc_fence_after();
         reduce_piece(taddr, rl, half, reinterpret_cast<float *>(gbase), ks, c_lo, c_lo + w);
-        run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb * pieces + slice, c_lo, c_lo + w);
+        run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb * pieces + slice, c_lo, c_lo + w, true);
       }
     }
     // no CTA leaves (or frees its shared memory) while a peer may still read its partial

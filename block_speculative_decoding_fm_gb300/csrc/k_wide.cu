@@ -46,10 +46,18 @@ __global__ void wide_prep_kernel(const float *__restrict__ h0, int D, int T, flo
 
 // one warp per row; D <= 4096, a multiple of 128.  With R: the residual stream
 // first takes the gated branch the previous product wrote (X += R, stored back).
+// The modulation rows (weights, not written by earlier kernels) are staged in
+// shared memory before griddepcontrol.wait.
 __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict__ R, int D, int T,
                                   const float *__restrict__ scale, const float *__restrict__ shift, float eps,
                                   __half *__restrict__ out) {
+  extern __shared__ float4 mods[];   // [D / 4] scale, then [D / 4] shift
   pdl_trigger();
+  for (int i = threadIdx.x; i < D / 4; i += blockDim.x) {
+    mods[i] = reinterpret_cast<const float4 *>(scale)[i];
+    mods[D / 4 + i] = reinterpret_cast<const float4 *>(shift)[i];
+  }
+  __syncthreads();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -59,6 +67,7 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
   const float4 *r = R ? reinterpret_cast<const float4 *>(R + (size_t)row * D) : nullptr;
   float4 v[32];
   float s = 0.f;
+  // every load of the row is issued before any store
 #pragma unroll
   for (int u = 0; u < 32; ++u) {
     if (u < per) {
@@ -69,10 +78,14 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
         v[u].y += g.y;
         v[u].z += g.z;
         v[u].w += g.w;
-        x[u * 32 + lane] = v[u];
       }
       s += (v[u].x + v[u].y) + (v[u].z + v[u].w);
     }
+  }
+  if (r) {
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      if (u < per) x[u * 32 + lane] = v[u];
   }
   const float mean = warp_sum(s) / (float)D;
   float q = 0.f;
@@ -88,9 +101,9 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
 #pragma unroll
   for (int u = 0; u < 32; ++u) {
     if (u < per) {
-      const int c0 = (u * 32 + lane) * 4;
-      const float4 sc = *reinterpret_cast<const float4 *>(scale + c0);
-      const float4 sh = *reinterpret_cast<const float4 *>(shift + c0);
+      const int i4 = u * 32 + lane;
+      const float4 sc = mods[i4];
+      const float4 sh = mods[D / 4 + i4];
       const __half2 h01 = __floats2half2_rn((v[u].x - mean) * rstd * (1.f + sc.x) + sh.x,
                                             (v[u].y - mean) * rstd * (1.f + sc.y) + sh.y);
       const __half2 h23 = __floats2half2_rn((v[u].z - mean) * rstd * (1.f + sc.z) + sh.z,
@@ -98,7 +111,7 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
       uint2 pk;
       pk.x = *reinterpret_cast<const uint32_t *>(&h01);
       pk.y = *reinterpret_cast<const uint32_t *>(&h23);
-      *reinterpret_cast<uint2 *>(o + c0) = pk;
+      *reinterpret_cast<uint2 *>(o + 4 * i4) = pk;
     }
   }
 }
@@ -112,12 +125,26 @@ __global__ void wide_self_attn_kernel(const float *__restrict__ qkv, int D, int 
   pdl_wait();
   const int seq = blockIdx.x, head = blockIdx.y, t = threadIdx.x;
   const int r0 = seq * B;
-  for (int i = t; i < B * (HD / 4); i += blockDim.x) {
-    const int n = i / (HD / 4), c = (i % (HD / 4)) * 4;
-    const float *row = qkv + (size_t)(r0 + n) * 3 * D + head * HD + c;
-    *reinterpret_cast<float4 *>(&q[n][c]) = *reinterpret_cast<const float4 *>(row);
-    *reinterpret_cast<float4 *>(&k[n][c]) = *reinterpret_cast<const float4 *>(row + D);
-    *reinterpret_cast<float4 *>(&v[n][c]) = *reinterpret_cast<const float4 *>(row + 2 * D);
+  // 16 rows x 32 float4 per operand over 128 threads: every load issued before the shared-memory stores
+  float4 lq[4], lk[4], lv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = t + 128 * j, n = i / (HD / 4), c = (i % (HD / 4)) * 4;
+    if (n < B) {
+      const float *row = qkv + (size_t)(r0 + n) * 3 * D + head * HD + c;
+      lq[j] = *reinterpret_cast<const float4 *>(row);
+      lk[j] = *reinterpret_cast<const float4 *>(row + D);
+      lv[j] = *reinterpret_cast<const float4 *>(row + 2 * D);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = t + 128 * j, n = i / (HD / 4), c = (i % (HD / 4)) * 4;
+    if (n < B) {
+      *reinterpret_cast<float4 *>(&q[n][c]) = lq[j];
+      *reinterpret_cast<float4 *>(&k[n][c]) = lk[j];
+      *reinterpret_cast<float4 *>(&v[n][c]) = lv[j];
+    }
   }
   __syncthreads();
   const float scale = 0.08838834764831845f;   // 1 / sqrt(128)
@@ -202,10 +229,11 @@ __global__ void f16_copy_pad_kernel(const __nv_bfloat16 *__restrict__ in, int V,
     out[i] = (int)(i / H) < V ? __float2half_rn(__bfloat162float(in[i])) : __float2half_rn(0.f);
 }
 
-cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaStream_t s) {
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaStream_t s, size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -232,7 +260,7 @@ cudaError_t launch_wide_lnmod(float *X, const float *R, int D, int T, const floa
   if (D % 128 || D > 4096) return cudaErrorInvalidValue;
   void *args[] = {(void *)&X, (void *)&R, (void *)&D, (void *)&T, (void *)&scale, (void *)&shift, (void *)&eps,
                   (void *)&out};
-  return launch_pdl((const void *)wide_lnmod_kernel, dim3((T + 3) / 4), dim3(128), args, s);
+  return launch_pdl((const void *)wide_lnmod_kernel, dim3((T + 3) / 4), dim3(128), args, s, (size_t)D * 8);
 }
 
 cudaError_t launch_wide_self_attn(const float *qkv, int D, int B, int n_seqs, int n_heads, __half *out, cudaStream_t s) {
