@@ -53,9 +53,25 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
                                   __half *__restrict__ out) {
   extern __shared__ float4 mods[];   // [D / 4] scale, then [D / 4] shift
   pdl_trigger();
-  for (int i = threadIdx.x; i < D / 4; i += blockDim.x) {
-    mods[i] = reinterpret_cast<const float4 *>(scale)[i];
-    mods[D / 4 + i] = reinterpret_cast<const float4 *>(shift)[i];
+  {
+    // all of a thread's loads first, then its shared-memory stores (D / 4 <= 1024 float4 per row over 128 threads)
+    float4 sv[8], hv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = threadIdx.x + j * blockDim.x;
+      if (i < D / 4) {
+        sv[j] = reinterpret_cast<const float4 *>(scale)[i];
+        hv[j] = reinterpret_cast<const float4 *>(shift)[i];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = threadIdx.x + j * blockDim.x;
+      if (i < D / 4) {
+        mods[i] = sv[j];
+        mods[D / 4 + i] = hv[j];
+      }
+    }
   }
   __syncthreads();
   pdl_wait();
