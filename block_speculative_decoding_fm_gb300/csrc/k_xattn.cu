@@ -428,6 +428,20 @@ __global__ void __launch_bounds__(kThreads, 1) fm_xattn_kernel(const __grid_cons
           const float l = red[n] + red[16 + n] + red[32 + n] + red[48 + n];
           cml[n] = make_float2(ntiles ? m_ref[n] : -INFINITY, ntiles ? l : 0.f);
         }
+    } else if (ns == 1) {
+      // one range per head: the output directly, O / l (thread j: dim j of every query row)
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        if (n < T) {
+          const float l = red[n] + red[16 + n] + red[32 + n] + red[48 + n];
+          const float val = (o[n] + o[16 + n]) / l;
+          const size_t off = (size_t)(qrow0 + n) * a.ldo + head * HD + j;
+          if (a.out16)
+            a.out16[off] = __float2half_rn(val);
+          else
+            a.out[off] = val;
+        }
+      }
     } else {
       float *po = a.part_o + (zslot * ns + split) * 16 * HD;
       float2 *pml = a.part_ml + (zslot * ns + split) * 16;
