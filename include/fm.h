@@ -174,12 +174,16 @@ FM_API fm_status fm_context_append(fm_handle *h, int32_t seq, const float *feats
 /*
  * fm_context_append_batched -- fm_context_append for several sequences in one
  * call.  Dense appends (>= 128 rows) run one after another through the
- * tensor-core prefill; shorter appends run per sequence on that sequence's
- * own stream, concurrently (each reads the weights itself).  feats_dev holds
- * the rows of seq_ids[0], then seq_ids[1], ...; n_rows_host[i] and
- * start_host[i] are per sequence (host arrays of n_seqs).  Same checks per
- * sequence; nothing is launched if any check fails.  Sequence ids must be
- * distinct.
+ * tensor-core prefill.  The shorter appends of 4 or more sequences, on a
+ * FlashMap handle with max_seqs >= 2 and head_dim 128, share each weight
+ * read: all their rows go through one fc GEMM and one K/V GEMM (per-row
+ * sequence and position), in chunks of at most 16384 rows; otherwise each
+ * runs on its sequence's own stream, concurrently (each reading the weights
+ * itself).  feats_dev holds the rows of seq_ids[0], then seq_ids[1], ...;
+ * n_rows_host[i] and start_host[i] are per sequence (host arrays of n_seqs).
+ * Same checks per sequence; nothing is launched if any check fails.
+ * Sequence ids must be distinct.  Batched calls on one handle run in stream
+ * order on one stream (they share the handle's batched-pass buffers).
  */
 FM_API fm_status fm_context_append_batched(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids_host,
                                     const float *feats_dev, const int32_t *n_rows_host,
@@ -193,6 +197,13 @@ FM_API fm_status fm_context_append_batched(fm_handle *h, int32_t n_seqs, const i
  * page does; the length is unchanged (a later append from pos overwrites it).
  * tokens_dev: device int32 [n_seqs][block], written in stream order.
  * Host arrays: seq_ids, anchors, pos (n_seqs each; distinct seq ids).
+ * Four or more sequences on a FlashMap handle with max_seqs >= 2 and
+ * head_dim 128 draft together, in passes of up to 32: each pass runs every
+ * product over all the pass's slot rows as one tensor-core GEMM (f16
+ * operands), so each weight and the token table are read once per pass, and
+ * one attention launch per layer serves every sequence's cache.  Fewer
+ * sequences, or other handles, run one chain per sequence on the sequences'
+ * own streams.
  * Errors: FM_ERR_INVALID_ARG (anchor outside [0, vocab), bad seq id, n_seqs
  *   outside [1, max_seqs], null tokens), FM_ERR_STATE (pos != length),
  *   FM_ERR_CONTEXT_FULL (pos + block + 1 > max_ctx), FM_ERR_CUDA.
