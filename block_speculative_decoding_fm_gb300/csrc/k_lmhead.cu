@@ -224,9 +224,10 @@ __device__ __forceinline__ int my_tile_count(int n_tiles) {
 // finished tile and keep the per-row running best, warp 22 is the second MMA
 // issuer (pairs alternate between the issuers, each with its own accumulator).
 // Work moves in pairs of chunks (G = 2; G = 1 when a tile's chunk count is odd).
-// TMEM columns: A slot i < kNA (= 3, so the converters can run two pairs ahead
-// of the MMAs) at 128 i, chunk h of the pair at + 64 h, hi at + 0 and lo at
-// + 32 (16 columns per 32-column block); accumulators at 384 + 64 me + 32 db
+// TMEM columns: A slot i < kNA at kSlotW i (6 slots of 64 columns, so the
+// converters can run five pairs ahead of the MMAs; 3 of 128 with the f16
+// residual), chunk h of the pair at + kSlotW / 2 h, hi at + 0 (and lo at + 32)
+// (16 columns per 32-column block); accumulators at 384 + 64 me + 32 db
 // (issuer me, tile parity db), per group of 8 slots 8 hi then 8 lo columns.
 // Y operand: kStreamY (Y pre-split in global memory): each ring stage carries
 // the Y chunks its table chunks need, so the ring can be deep; otherwise Y is
@@ -257,8 +258,11 @@ template <bool kStreamY>
 __global__ void __launch_bounds__(kQ8Threads, 1) fm_lmhead_q8_kernel(const __grid_constant__ LmArgs a, const int S, const int U, const int NI, const int G) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int SB = kQ8Chunk;
-  constexpr int kNA = 3;
-  constexpr int kD = 128 * kNA;   // first accumulator column
+  // A slots: with the f16 residual a slot holds a pair's hi and lo halves (128 columns, 3 slots); without
+  // it a pair's two chunks take 64 columns, so 6 slots fit and the converters run five pairs ahead
+  constexpr int kNA = kWeightResidual ? 3 : 6;
+  constexpr int kSlotW = kWeightResidual ? 128 : 64, kChunkW = kSlotW / 2;
+  constexpr int kD = kSlotW * kNA;   // first accumulator column (384)
   constexpr uint32_t IDESC = umma_idesc(128, 32, false);
   const int H = a.H, kcs = H / kChunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) fm_lmhead_q8_kernel(const __gri
             // (streamed Y: the converters' afull for this chunk implies its stage has landed)
             const uint64_t bd = umma_desc_sw128(kStreamY ? ring + y2.st * SS + y2.uo * kYChunk
                                                           : ybuf + (kc + h) * kYChunk);
-            const uint32_t ah = tmem + 128 * i + 64 * h;
+            const uint32_t ah = tmem + kSlotW * i + kChunkW * h;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               umma_ts_elect(d, ah + 8 * kk, bd + 2 * kk, IDESC, (first_in_tile && h == 0 && kk == 0) ? 0u : 1u);
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) fm_lmhead_q8_kernel(const __gri
             lo[j] = *reinterpret_cast<const uint32_t *>(&pl);
           }
         }
-        const uint32_t ta = lane_base + 128 * i + 64 * h + 16 * b;
+        const uint32_t ta = lane_base + kSlotW * i + kChunkW * h + 16 * b;
         if constexpr (kWeightResidual) {
           tmem_st16(ta, hi, false);
           tmem_st16(ta + 32, lo);
