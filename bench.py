@@ -83,19 +83,24 @@ def source_digest(tag):
     return h.hexdigest()[:16]
 
 
+WORKLOAD = "flashmap4b"   # the workload of this run (a kernel tag's traffic depends on it)
+
+
 def ncu_traffic(tag):
-    """DRAM bytes (read + write) per launch of the kernel behind `tag`, from the
-    committed ncu summary profiles/ncu_dram_traffic.txt, or None when there is
-    no capture or the kernel's sources have changed since it was taken (each
-    line records source_digest() of the build the capture ran)."""
+    """DRAM bytes (read + write) per launch of the kernel behind `tag` in this
+    run's workload, from the committed ncu summary profiles/ncu_dram_traffic.txt
+    (lines `tag@workload`, or a bare `tag` for the default FlashMap-4B step), or
+    None when there is no capture or the kernel's sources have changed since it
+    was taken (each line records source_digest() of the build the capture ran)."""
     digest = source_digest(tag)
     path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
     if digest is None or not os.path.exists(path):
         return None
+    names = {f"{tag}@{WORKLOAD}"} | ({tag} if WORKLOAD == "flashmap4b" else set())
     with open(path) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 4 and not line.startswith("#") and parts[0] == tag and parts[3] == digest:
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] in names and parts[3] == digest:
                 return float(parts[1])
     return None
 
@@ -842,7 +847,9 @@ def run_ours(args):
 
 
 def main():
+    global WORKLOAD
     args = parse()
+    WORKLOAD = args.workload
     if args.impl == "reference":
         run_reference(args)
     elif args.workload != "flashmap4b":
