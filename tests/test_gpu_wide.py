@@ -189,3 +189,35 @@ def test_batched_argmax_ties_go_to_the_lowest_index():
     for s in range(4):
         check_seq(p, s, got[s], [2, 4, 6, 8][s], lens[s])
     p.close()
+
+
+def test_batched_append_ragged_then_draft():
+    """A batched append with ragged row counts: none, one, 127 (the largest that
+    takes the shared pass), 33, and 130 (dense: the prefill GEMMs on its own),
+    then a batched draft; every sequence against the oracle, the appended cache
+    rows included."""
+    import torch
+    import block_speculative_decoding_fm_gb300 as fm
+    cfg = mid_config(5, max_ctx=320)
+    p = Pair(cfg, 1405, keep_hidden=False)
+    fr = S.streams(1405)["features"]
+    base = [20, 3, 90, 1, 40]
+    for s, n in enumerate(base):
+        p.append(s, S.gen_features(fr, n, cfg.feat_dim), 0)
+    add = [0, 1, 127, 33, 130]
+    ids = [0, 1, 2, 3, 4]
+    rows = [S.gen_features(fr, n, cfg.feat_dim) for n in add]
+    fm.fm_context_append_batched(p.h, ids, torch.from_numpy(np.concatenate(rows)).cuda(), add, base)
+    for s in ids:
+        if add[s]:
+            p.oracle.context_append(p.state(s), rows[s], base[s])
+        assert fm.fm_get_length(p.h, s) == base[s] + add[s]
+        if add[s]:
+            cache_rows_match(p, s, base[s], base[s] + add[s])
+    pos = [base[s] + add[s] for s in ids]
+    anchors = [17, 170, 1700, 4000, 2]
+    got = batched_draft(p, ids, anchors, pos)
+    assert fm.fm_last_launch_count(p.h) == wide_launches(cfg, 1)
+    for s in ids:
+        check_seq(p, s, got[s], anchors[s], pos[s])
+    p.close()
