@@ -148,7 +148,8 @@ struct fm_handle {
     int rows_cap = 0;
     cudaEvent_t rows_ev[kParamSlots]{};
     int rows_next = 0;
-    std::vector<int> row_of;        // per sequence: its first row in the last batched draft, or -1
+    std::vector<int> row_of;        // per sequence: its first row in the last batched pass; -1: its last
+                                    // draft was not batched; -2: an earlier pass of the last batched call
     double keys = 0;                // the current pass's cache rows read per layer (profile bytes)
     float *dbg_logits = nullptr;    // FM_DEBUG_LOGITS of a batched draft: [block][Vn]
   } wide;
@@ -1336,7 +1337,7 @@ bool wide_wanted(const fm_handle *h) {
   const char *e = getenv("FM_NO_WIDE");
   if (e && e[0] == '1') return false;
   const double cache_rows = (double)c.max_seqs * c.n_layers * 2 * c.n_heads * c.max_ctx;
-  return c.variant == FM_VARIANT_FLASHMAP && c.max_seqs >= 2 && c.head_dim == 128 && c.dim % 256 == 0 &&
+  return c.variant == FM_VARIANT_FLASHMAP && c.max_seqs >= kWideMin && c.head_dim == 128 && c.dim % 256 == 0 &&
          c.ff_dim % 256 == 0 && c.target_dim % 256 == 0 && c.dim <= 4096 && c.max_ctx >= 128 &&
          cache_rows < 2147483647.0;
 }
@@ -1645,7 +1646,8 @@ fm_status wide_draft(fm_handle *h, int n, const int32_t *ids, const int32_t *anc
   const fm_config &c = h->cfg;
   fm_handle::Wide &w = h->wide;
   for (int i = 0; i < n; ++i) TRY(flush_pending(h, ids[i], s));
-  std::fill(w.row_of.begin(), w.row_of.end(), -1);
+  for (int &r : w.row_of)
+    if (r >= 0) r = -2;   // this call overwrites the head output of the previous batched call
   for (int p0 = 0; p0 < n; p0 += kWideSeqs) {
     const int m = n - p0 < kWideSeqs ? n - p0 : kWideSeqs;
     WideParams p;
@@ -1674,8 +1676,8 @@ fm_status wide_draft(fm_handle *h, int n, const int32_t *ids, const int32_t *anc
     for (int i = 0; i < m; ++i) w.keys += p.pos[i] + 1;
     const int xs = w.xsplits;
     TRY(run_graph(h, chain_key(6, 0, m, xs, 0), s, [&](cudaStream_t st) { return wide_chain(h, m, xs, st); }));
-    if (p0 + m == n)
-      for (int i = 0; i < m; ++i) w.row_of[ids[p0 + i]] = i * c.block;
+    // the head output of the last pass stays readable; earlier passes' rows are overwritten (-2)
+    for (int i = 0; i < m; ++i) w.row_of[ids[p0 + i]] = p0 + m == n ? i * c.block : -2;
   }
   return FM_OK;
 }
@@ -2590,11 +2592,15 @@ fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, 
       TRY(check_seq(h, seq));
       use_lane(h, seq);
       src = h->Y;
+      if (h->wide.on && h->wide.row_of[seq] == -2)
+        return fail(h, FM_ERR_UNSUPPORTED, "the head output of an earlier batched pass is not kept");
       if (h->wide.on && h->wide.row_of[seq] >= 0) src = h->wide.Y + (size_t)h->wide.row_of[seq] * c.target_dim;
       size = (int64_t)c.block * c.target_dim * 4;
       break;
     case FM_DEBUG_LOGITS: {
       TRY(check_seq(h, seq));
+      if (h->wide.on && h->wide.row_of[seq] == -2)
+        return fail(h, FM_ERR_UNSUPPORTED, "the head output of an earlier batched pass is not kept");
       if (h->wide.on && h->wide.row_of[seq] >= 0) {
         // the batched lm_head's product for this sequence's rows, stored instead of reduced
         fm_handle::Wide &w = h->wide;

@@ -367,8 +367,15 @@ FM_API fm_status fm_policy_after_plain(fm_verify_policy *p, double ms, int32_t r
 
 /*
  * fm_debug_copy -- copy nbytes of the selected buffer, starting at byte
- * offset, to dst_host.  Synchronises the stream.  Errors: FM_ERR_INVALID_ARG
- * (unknown selector, index or range outside the buffer), FM_ERR_CUDA.
+ * offset, to dst_host.  Synchronises the stream.  After a batched draft,
+ * FM_DEBUG_HEAD_OUT and FM_DEBUG_LOGITS read the sequence's rows of the last
+ * pass of the last batched call (the logits recomputed by the batched
+ * lm_head's product); a sequence of an earlier pass, or of an earlier batched
+ * call, has no kept head output until its next draft (FM_ERR_UNSUPPORTED).
+ * FM_DEBUG_HIDDEN is kept by single-sequence drafts only.
+ * Errors: FM_ERR_INVALID_ARG (unknown selector, index or range outside the
+ * buffer), FM_ERR_UNSUPPORTED (above), FM_ERR_CUDA, FM_ERR_TIMEOUT (a bounded
+ * wait gave up in an earlier call).
  */
 FM_API fm_status fm_debug_copy(fm_handle *h, int32_t what, int32_t seq, int32_t index, int64_t offset, void *dst_host,
                         int64_t nbytes, void *stream);

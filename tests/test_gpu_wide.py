@@ -161,6 +161,10 @@ def test_batched_draft_in_passes():
     pos = [lens[s] for s in ids]
     got = batched_draft(p, ids, anchors, pos)
     assert fm.fm_last_launch_count(p.h) == wide_launches(cfg, 2)
+    # the first pass's head output has been overwritten by the second pass: reading it is refused
+    with pytest.raises(fm.FmError) as e:
+        head_out(p, ids[0])
+    assert e.value.status == fm.FM_ERR_UNSUPPORTED
     for j, s in enumerate(ids):
         # only the last pass keeps its head output
         if j >= 32:
