@@ -218,9 +218,12 @@ class FlashMapStep:
         self.launches += fm.fm_last_launch_count(self.h)
 
     def step_e2e(self):
-        self.f17_dev.copy_(self.f17_host, non_blocking=True)
-        self.step()
-        self.tok_host.copy_(self.tokens, non_blocking=True)
+        # the host-buffer calls of the C ABI: rows copied in, tokens copied out, on the stream
+        fm = self.fm
+        fm.fm_context_append_host(self.h, 0, self.f17_host, 17, 1024)
+        self.launches += fm.fm_last_launch_count(self.h)
+        fm.fm_draft_host(self.h, [0], [self.anchor], [1041], self.tok_host)
+        self.launches += fm.fm_last_launch_count(self.h)
 
     e2e_h2d = 17 * 12800 * 4
     e2e_d2h = 16 * 4
@@ -412,6 +415,10 @@ class BatchedStep:
         self.ids = list(range(n_seqs))
         self.pos = [L + n for L, n in zip(self.L, self.n)]
         self.tokens = torch.zeros((n_seqs, 16), dtype=torch.int32, device="cuda")
+        self.feats_host = self.feats.cpu().pin_memory()
+        self.tok_host = torch.zeros((n_seqs, 16), dtype=torch.int32).pin_memory()
+        self.e2e_h2d = sum(self.n) * c.feat_dim * 4
+        self.e2e_d2h = n_seqs * 16 * 4
         self.launches = 0
         D, F, Ht, Ll = c.dim, c.ff_dim, c.target_dim, c.n_layers
         weights = (D * c.feat_dim + D * Ht * 2 + Ll * (4 * D * D + 4 * D * D + 2 * F * D) + Ht * D) * 2
@@ -424,6 +431,13 @@ class BatchedStep:
         fm.fm_context_append_batched(self.h, self.ids, self.feats, self.n, self.L)
         self.launches += fm.fm_last_launch_count(self.h)
         fm.fm_draft(self.h, self.ids, self.anchors, self.pos, self.tokens)
+        self.launches += fm.fm_last_launch_count(self.h)
+
+    def step_e2e(self):
+        fm = self.fm
+        fm.fm_context_append_batched_host(self.h, self.ids, self.feats_host, self.n, self.L)
+        self.launches += fm.fm_last_launch_count(self.h)
+        fm.fm_draft_host(self.h, self.ids, self.anchors, self.pos, self.tok_host)
         self.launches += fm.fm_last_launch_count(self.h)
 
 
@@ -534,6 +548,13 @@ def run_workload(args):
             extra["tokens_drafted_per_s"] = value * 32 * 16
             extra["achieved_hbm_gbs"] = w.bytes_per_step * value / 1e9
             extra["bytes_per_step"] = w.bytes_per_step
+            if not args.no_e2e:
+                # the host-buffer calls: the step's feature rows in, the drafted tokens out, inside the timed region
+                for _ in range(3):
+                    w.step_e2e()
+                ms_e2e = time_steps(torch, w.step_e2e, args.steps)
+                e2e = {"value": args.steps / (ms_e2e / 1000), "unit": "steps/s", "h2d_bytes_per_step": w.e2e_h2d,
+                       "d2h_bytes_per_step": w.e2e_d2h}
             cfgd = {"workload": f"batched: 32 FlashMap-4B sequences, contexts U[512,{args.batched_ctx}], append "
                                 "acc_i+1 rows (acc_i in 0..16) + 32 x 16-slot draft", "global_batch": 512}
         else:   # prefill
@@ -657,8 +678,9 @@ def run_workload(args):
                    "sample": f"{k} drafts in {dt:.1f} s", "blas_threads": blas_threads()}
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfgd, "gpu_launches": launches,
-            "roofline": roofline, "kernels": kernels, "clocks": clk.summary(), "cpu_baseline": cpu, **extra}
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfgd, "e2e": e2e,
+            "gpu_launches": launches, "roofline": roofline, "kernels": kernels, "clocks": clk.summary(),
+            "cpu_baseline": cpu, **extra}
     print(json.dumps(line), flush=True)
 
 

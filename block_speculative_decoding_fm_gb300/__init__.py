@@ -30,8 +30,9 @@ FM_DEBUG_PROFILE = 2
 FM_DEBUG_TRACE = 4
 
 EXPORTS = ["fm_create", "fm_time_conditioning", "fm_context_append", "fm_context_append_batched", "fm_draft",
-           "fm_draft_pruned", "fm_accept",
-           "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_synchronize", "fm_selftest_wait_timeout", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
+           "fm_context_append_host", "fm_context_append_batched_host", "fm_draft_host", "fm_draft_pruned",
+           "fm_accept", "fm_accept_batched", "fm_lm_head_argmax_noalloc", "fm_synchronize",
+           "fm_selftest_wait_timeout", "fm_debug_copy", "fm_set_debug", "fm_get_length", "fm_memory_bytes",
            "fm_last_launch_count", "fm_profile_read", "fm_status_str", "fm_last_error", "fm_destroy",
            "fm_policy_init", "fm_policy_next", "fm_policy_after_round", "fm_policy_after_plain",
            "fm_mtp_create", "fm_mtp_forward", "fm_mtp_draft", "fm_mtp_cache", "fm_mtp_last_launch_count",
@@ -99,6 +100,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fm_context_append": (I32, [P, I32, P, I32, I32, P]),
         "fm_context_append_batched": (I32, [P, I32, P, P, P, P, P]),
         "fm_draft": (I32, [P, I32, P, P, P, P, P]),
+        "fm_context_append_host": (I32, [P, I32, P, I32, I32, P]),
+        "fm_context_append_batched_host": (I32, [P, I32, P, P, P, P, P]),
+        "fm_draft_host": (I32, [P, I32, P, P, P, P, P]),
         "fm_draft_pruned": (I32, [P, I32, I32, I32, P, ctypes.c_float, P, P, P, P]),
         "fm_accept": (I32, [P, P, I32, P, P]),
         "fm_accept_batched": (I32, [P, I32, P, P, P, P, P, P]),
@@ -214,6 +218,8 @@ def fm_create(cfg, weights: Iterable[Tuple[str, object, int]], modulation=None, 
     h = ctypes.c_void_p()
     _check(lib.fm_create(ctypes.byref(c), arr, len(items), _ptr(mod), _stream(stream), ctypes.byref(h)))
     h._fm_target_dim = int(cfg.target_dim)
+    h._fm_block = int(cfg.block)
+    h._fm_feat = int(cfg.n_taps) * int(cfg.target_dim)
     return h
 
 
@@ -239,6 +245,52 @@ def fm_draft(h, seq_ids: Sequence[int], anchors: Sequence[int], pos: Sequence[in
     an = np.ascontiguousarray(anchors, np.int32)
     ps = np.ascontiguousarray(pos, np.int32)
     _check(lib.fm_draft(h, len(ids), _ptr(ids), _ptr(an), _ptr(ps), _ptr(tokens), _stream(stream)), h)
+
+
+def _host_buffer(x, dtype, what: str, need: int):
+    """A host buffer for the host-buffer calls: a C-contiguous numpy array or
+    CPU tensor of dtype with at least need elements (pinned memory keeps the
+    copy asynchronous)."""
+    if isinstance(x, np.ndarray):
+        ok, size = x.dtype == dtype and x.flags["C_CONTIGUOUS"], x.size
+    else:
+        ok = not getattr(x, "is_cuda", True) and x.is_contiguous() and str(x.dtype) == "torch." + np.dtype(dtype).name
+        size = x.numel() if ok else 0
+    if not ok:
+        raise ValueError(f"{what} must be a contiguous {np.dtype(dtype).name} host array or CPU tensor")
+    if size < need:
+        raise ValueError(f"{what} holds {size} values, fewer than the call's {need}")
+    return x
+
+
+def fm_context_append_host(h, seq: int, feats, n_rows: int, start_pos: int, stream=None) -> None:
+    """fm_context_append with the rows in host memory (copied on the stream)."""
+    lib = load_library()
+    f = None if n_rows <= 0 else _host_buffer(feats, np.float32, "feature rows", n_rows * h._fm_feat)
+    _check(lib.fm_context_append_host(h, seq, _ptr(f), n_rows, start_pos, _stream(stream)), h)
+
+
+def fm_context_append_batched_host(h, seq_ids: Sequence[int], feats, n_rows: Sequence[int], starts: Sequence[int],
+                                   stream=None) -> None:
+    lib = load_library()
+    ids = np.ascontiguousarray(seq_ids, np.int32)
+    nr = np.ascontiguousarray(n_rows, np.int32)
+    st = np.ascontiguousarray(starts, np.int32)
+    total = int(np.maximum(nr, 0).sum())
+    f = None if total == 0 else _host_buffer(feats, np.float32, "feature rows", total * h._fm_feat)
+    _check(lib.fm_context_append_batched_host(h, len(ids), _ptr(ids), _ptr(f), _ptr(nr), _ptr(st),
+                                              _stream(stream)), h)
+
+
+def fm_draft_host(h, seq_ids: Sequence[int], anchors: Sequence[int], pos: Sequence[int], tokens, stream=None) -> None:
+    """tokens: host int32 [n_seqs, block] (numpy array or CPU tensor, pinned for an
+    asynchronous copy); complete once the stream has passed the call."""
+    lib = load_library()
+    ids = np.ascontiguousarray(seq_ids, np.int32)
+    an = np.ascontiguousarray(anchors, np.int32)
+    ps = np.ascontiguousarray(pos, np.int32)
+    _host_buffer(tokens, np.int32, "tokens", len(ids) * h._fm_block)
+    _check(lib.fm_draft_host(h, len(ids), _ptr(ids), _ptr(an), _ptr(ps), _ptr(tokens), _stream(stream)), h)
 
 
 def fm_draft_pruned(h, seq: int, anchor: int, pos: int, tokens, conf=None, length=None, thresholds=None,

@@ -103,6 +103,12 @@ struct fm_handle {
 
   int32_t *dev_err = nullptr;     // raised by a device-side bounded wait that gave up
 
+  // ---- calls with host buffers: device copies of their feature rows and tokens ----
+  float *stage_feats = nullptr;   // grown on demand
+  size_t stage_cap = 0;           // floats stage_feats holds
+  int32_t *stage_tok = nullptr;   // [max_seqs][block]
+  cudaEvent_t stage_ev = nullptr; // recorded after the last host-buffer call's work
+
   // ---- the persistent draft step ----
   bool use_step = true;
   int step_attrs = 3;                 // launch attributes the device accepted (cooperative | PDL)
@@ -2221,6 +2227,31 @@ fm_status append_one(fm_handle *h, int32_t seq, const float *feats, int32_t n, i
   return FM_OK;
 }
 
+// The device copy of a host-buffer call's feature rows (n floats), made on stream s after the
+// previous host-buffer call's work: the staging buffer is grown (once that work has finished) when
+// it is too small.  Asynchronous to the host when the rows are in pinned memory.
+fm_status stage_rows(fm_handle *h, const float *host, size_t n, cudaStream_t s, const float **dev) {
+  if (!h->stage_ev) CK(cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming));
+  CK(cudaStreamWaitEvent(s, h->stage_ev, 0));
+  if (n > h->stage_cap) {
+    CK(cudaEventSynchronize(h->stage_ev));
+    if (h->stage_feats) {
+      auto it = std::find(h->allocs.begin(), h->allocs.end(), static_cast<void *>(h->stage_feats));
+      if (it != h->allocs.end()) h->allocs.erase(it);
+      h->bytes -= (int64_t)(h->stage_cap * sizeof(float));
+      cudaFree(h->stage_feats);
+      h->stage_feats = nullptr;
+      h->stage_cap = 0;
+    }
+    const size_t cap = n < ((size_t)1 << 20) ? (size_t)1 << 20 : n;
+    TRY(dalloc(h, &h->stage_feats, cap));
+    h->stage_cap = cap;
+  }
+  if (n) CK(cudaMemcpyAsync(h->stage_feats, host, n * sizeof(float), cudaMemcpyHostToDevice, s));
+  *dev = h->stage_feats;
+  return FM_OK;
+}
+
 }  // namespace
 
 // Run body(i, stream) for the n sequences ids[0..n): one sequence on the caller's
@@ -2387,6 +2418,60 @@ fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const i
   return run_lanes(h, n_seqs, seq_ids, s, [&](int i, cudaStream_t ls) {
     return draft_one(h, seq_ids[i], anchors[i], pos[i], tokens + (size_t)i * h->cfg.block, ls);
   });
+}
+
+fm_status fm_context_append_host(fm_handle *h, int32_t seq, const float *feats_host, int32_t n_rows,
+                                 int32_t start_pos, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  if (n_rows > 0 && !feats_host) return fail(h, FM_ERR_INVALID_ARG, "null feature rows");
+  TRY(check_seq(h, seq));
+  if (n_rows < 0) return fail(h, FM_ERR_INVALID_ARG, "n_rows < 0");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float *dev = nullptr;
+  TRY(stage_rows(h, feats_host, (size_t)n_rows * h->cfg.n_taps * h->cfg.target_dim, s, &dev));
+  const fm_status st = fm_context_append(h, seq, n_rows > 0 ? dev : nullptr, n_rows, start_pos, stream);
+  CK(cudaEventRecord(h->stage_ev, s));
+  return st;
+}
+
+fm_status fm_context_append_batched_host(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids,
+                                         const float *feats_host, const int32_t *n_rows, const int32_t *start,
+                                         void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  if (n_seqs < 1 || n_seqs > h->cfg.max_seqs || !seq_ids || !n_rows || !start)
+    return fail(h, FM_ERR_INVALID_ARG, "bad batched append arguments");
+  size_t total = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    if (n_rows[i] < 0) return fail(h, FM_ERR_INVALID_ARG, "n_rows < 0");
+    total += (size_t)n_rows[i];
+  }
+  if (total > 0 && !feats_host) return fail(h, FM_ERR_INVALID_ARG, "null feature rows");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float *dev = nullptr;
+  TRY(stage_rows(h, feats_host, total * h->cfg.n_taps * h->cfg.target_dim, s, &dev));
+  const fm_status st = fm_context_append_batched(h, n_seqs, seq_ids, total > 0 ? dev : nullptr, n_rows, start,
+                                                 stream);
+  CK(cudaEventRecord(h->stage_ev, s));
+  return st;
+}
+
+fm_status fm_draft_host(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids, const int32_t *anchors,
+                        const int32_t *pos, int32_t *tokens_host, void *stream) {
+  if (!h) return FM_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  if (!tokens_host) return fail(h, FM_ERR_INVALID_ARG, "null tokens");
+  if (n_seqs < 1 || n_seqs > h->cfg.max_seqs) return fail(h, FM_ERR_INVALID_ARG, "n_seqs outside [1, max_seqs]");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!h->stage_ev) CK(cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming));
+  if (!h->stage_tok) TRY(dalloc(h, &h->stage_tok, (size_t)h->cfg.max_seqs * h->cfg.block));
+  CK(cudaStreamWaitEvent(s, h->stage_ev, 0));
+  TRY(fm_draft(h, n_seqs, seq_ids, anchors, pos, h->stage_tok, stream));
+  CK(cudaMemcpyAsync(tokens_host, h->stage_tok, (size_t)n_seqs * h->cfg.block * sizeof(int32_t),
+                     cudaMemcpyDeviceToHost, s));
+  CK(cudaEventRecord(h->stage_ev, s));
+  return FM_OK;
 }
 
 fm_status fm_draft_pruned(fm_handle *h, int32_t seq, int32_t anchor, int32_t pos, const float *thresholds,
@@ -2750,6 +2835,7 @@ void fm_destroy(fm_handle *h) {
     if (L.done) cudaEventDestroy(L.done);
   }
   if (h->fork_ev) cudaEventDestroy(h->fork_ev);
+  if (h->stage_ev) cudaEventDestroy(h->stage_ev);
   if (h->wide.par_host) cudaFreeHost(h->wide.par_host);
   if (h->wide.rows_host) cudaFreeHost(h->wide.rows_host);
   for (int i = 0; i < kParamSlots; ++i) {

@@ -212,6 +212,33 @@ FM_API fm_status fm_draft(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids_h
                    const int32_t *pos_host, int32_t *tokens_dev, void *stream);
 
 /*
+ * Host-buffer forms of the three calls above, for callers whose feature rows
+ * arrive in, and whose drafted tokens go to, host memory.  Each copies on the
+ * stream with cudaMemcpyAsync: the rows into a handle-owned device staging
+ * buffer (grown when a call needs more; it waits for the previous
+ * host-buffer call's work before it is reused), then runs the device-pointer
+ * call, whose checks, behaviour and errors it shares; fm_draft_host then
+ * copies the tokens back.  With pinned host memory every copy is
+ * asynchronous to the host: the rows must stay unchanged, and tokens_host
+ * must not be read, until the stream has passed the call (fm_synchronize).
+ * With pageable memory the runtime makes the copies synchronous instead.
+ *   feats_host: host f32 rows laid out as in the device-pointer call (no
+ *     alignment requirement).
+ *   tokens_host: host int32 [n_seqs][block].
+ * Errors: those of the device-pointer call; FM_ERR_INVALID_ARG (null
+ *   feats_host with rows, null tokens_host); FM_ERR_OOM (the staging buffer
+ *   could not grow); FM_ERR_CUDA (a copy failed).
+ */
+FM_API fm_status fm_context_append_host(fm_handle *h, int32_t seq, const float *feats_host, int32_t n_rows,
+                                        int32_t start_pos, void *stream);
+FM_API fm_status fm_context_append_batched_host(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids_host,
+                                                const float *feats_host, const int32_t *n_rows_host,
+                                                const int32_t *start_host, void *stream);
+FM_API fm_status fm_draft_host(fm_handle *h, int32_t n_seqs, const int32_t *seq_ids_host,
+                               const int32_t *anchors_host, const int32_t *pos_host, int32_t *tokens_host,
+                               void *stream);
+
+/*
  * fm_draft_pruned -- [DF] the greedy draft of one sequence through the
  * sequential logit head, with the confidence head and confidence pruning
  * (module-dflash.ts: ``#markov`` (Eq 5), ``#rnn`` (Eq 6), ``#confidence`` and
