@@ -42,6 +42,20 @@ constexpr int kBfWorkers = 128;               // bf16: warps 2..5
 constexpr int kBase = 64;                     // warp 0: producer, warp 1: TMEM owner + MMA issuer
 
 
+// Four offset-binary bytes u = q + 128 (the repacked table's form) -> two f16x2
+// words holding q exactly: each byte goes into the low mantissa bits of 1024.0
+// (0x64 high byte), then 1024 + 128 is subtracted (the published "magic number"
+// int-to-float conversion).  One byte permute per pair, no sign handling.
+__device__ __forceinline__ void ob8x4_to_f16x4(uint32_t u, uint32_t &w01, uint32_t &w23) {
+  const uint32_t h01 = __byte_perm(u, 0x64646464u, 0x4140);
+  const uint32_t h23 = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  __half2 r01 = __hsub2(*reinterpret_cast<const __half2 *>(&h01), bias);
+  __half2 r23 = __hsub2(*reinterpret_cast<const __half2 *>(&h23), bias);
+  w01 = *reinterpret_cast<uint32_t *>(&r01);
+  w23 = *reinterpret_cast<uint32_t *>(&r23);
+}
+
 // tcgen05.mma with A in tensor memory (lane = A row, 32-bit columns hold K pairs),
 // issued by one elected lane of a warp that runs the issue loop together
 __device__ __forceinline__ void umma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -443,7 +457,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) fm_lmhead_q8_kernel(const __gri
       const uint32_t o0 = (uint32_t)r * 64 + (((2 * b) ^ x) << 4), o1 = (uint32_t)r * 64 + (((2 * b + 1) ^ x) << 4);
       // the row's f16 block scale (two rows per 32-bit word in the chunk's scale plane)
       const uint32_t soff = (uint32_t)kTile * 64 + (uint32_t)b * 256 + (uint32_t)(r & ~1) * 2;
-      const int sh = (r & 1) * 16;
+      const uint32_t dsel = (r & 1) ? 0x3232u : 0x1010u;   // this row's f16 scale, in both halves
       RingPos c;
       c.step(h, U, S);
       int i = 0;
@@ -456,18 +470,17 @@ __global__ void __launch_bounds__(kQ8Threads, 1) fm_lmhead_q8_kernel(const __gri
         const uint32_t buf = ring + c.st * SS + TOFF + c.uo * SB;
         const uint4 v0 = lds128(buf + o0), v1 = lds128(buf + o1);
         const uint32_t sw = lds32(buf + soff);
-        const uint32_t dd = (sw >> sh) & 0xffffu;
-        const uint32_t dpair = dd | (dd << 16);
+        const uint32_t dpair = __byte_perm(sw, 0u, dsel);
         const __half2 d2 = *reinterpret_cast<const __half2 *>(&dpair);
         uint32_t w[16];
-        i8x4_to_f16x4(v0.x, w[0], w[1]);
-        i8x4_to_f16x4(v0.y, w[2], w[3]);
-        i8x4_to_f16x4(v0.z, w[4], w[5]);
-        i8x4_to_f16x4(v0.w, w[6], w[7]);
-        i8x4_to_f16x4(v1.x, w[8], w[9]);
-        i8x4_to_f16x4(v1.y, w[10], w[11]);
-        i8x4_to_f16x4(v1.z, w[12], w[13]);
-        i8x4_to_f16x4(v1.w, w[14], w[15]);
+        ob8x4_to_f16x4(v0.x, w[0], w[1]);
+        ob8x4_to_f16x4(v0.y, w[2], w[3]);
+        ob8x4_to_f16x4(v0.z, w[4], w[5]);
+        ob8x4_to_f16x4(v0.w, w[6], w[7]);
+        ob8x4_to_f16x4(v1.x, w[8], w[9]);
+        ob8x4_to_f16x4(v1.y, w[10], w[11]);
+        ob8x4_to_f16x4(v1.z, w[12], w[13]);
+        ob8x4_to_f16x4(v1.w, w[14], w[15]);
         // last chunk of this set in the unit: the stage may be refilled after these loads
         if (c.uo + G >= U) {
           __syncwarp();

@@ -7,10 +7,11 @@ namespace fm {
 namespace {
 
 // GGUF Q8_0 rows [V][nb * 34] -> the lm_head layout: per (128-row tile, 64-column
-// chunk) 128 x 64 int8 (pre-swizzled) then the chunk's two blocks of f16 scales
+// chunk) 128 x 64 weights as offset-binary bytes q + 128 (pre-swizzled; rows past V
+// hold q = 0, the byte 0x80) then the chunk's two blocks of f16 scales
 // [2][128] (the MTP loader on ternary_bonsai_2_mtp.js splits the 34-byte blocks
 // into an int8 plane and a scale plane; here both halves of a chunk sit together
-// so one bulk copy fetches them).  Rows past V get zeros.  One thread per block.
+// so one bulk copy fetches them).  One thread per block.
 __global__ void q8_repack_kernel(const uint8_t *raw, int V, int H, uint8_t *dst) {
   const int nb = H / 32, nck = H / 64;
   const int Vpad = (V + 127) / 128 * 128;
@@ -28,7 +29,8 @@ __global__ void q8_repack_kernel(const uint8_t *raw, int V, int H, uint8_t *dst)
   } else {
     for (int i = 0; i < 32; ++i) q[i] = 0;
   }
-  for (int i = 0; i < 32; ++i) chunk[q8_slot(rr, 32 * bb + i)] = q[i];
+  // offset binary: the byte q + 128 (q ^ 0x80), so the converters place it straight into an f16 mantissa
+  for (int i = 0; i < 32; ++i) chunk[q8_slot(rr, 32 * bb + i)] = (uint8_t)(q[i] ^ 0x80u);
   *reinterpret_cast<unsigned short *>(chunk + kTile * 64 + bb * 256 + rr * 2) = d;
 }
 

@@ -211,10 +211,11 @@ __device__ __forceinline__ void stage_store(const GemvArgs &a, const float *stat
           const int rr = r & 127, kk = k & 63;
           if (a.amode == A_ROW_Q8) {
             const uint8_t *base = a.tq8 + chunk * kQ8Chunk;
-            const char4 qv = *reinterpret_cast<const char4 *>(base + q8_slot(rr, kk));
+            const uchar4 qv = *reinterpret_cast<const uchar4 *>(base + q8_slot(rr, kk));   // q + 128
             const float d = __half2float(
                 *reinterpret_cast<const __half *>(base + kTile * 64 + (kk >> 5) * 256 + rr * 2));
-            v[0] = d * qv.x; v[1] = d * qv.y; v[2] = d * qv.z; v[3] = d * qv.w;
+            v[0] = d * (float)((int)qv.x - 128); v[1] = d * (float)((int)qv.y - 128);
+            v[2] = d * (float)((int)qv.z - 128); v[3] = d * (float)((int)qv.w - 128);
           } else {
             const uint8_t *base = a.tb + chunk * 16384;
             const uint2 u = *reinterpret_cast<const uint2 *>(base + w_slot(rr, kk));
