@@ -144,6 +144,7 @@ struct fm_handle {
     float2 *xml = nullptr;
     int32_t *xtickets = nullptr;
     int xsplits = 1;                // key ranges per (sequence, head) (measured: 1 > 2 > 3 at 32 sequences)
+    bool tstore = true;             // single-output epilogues write through tensor stores (FM_WIDE_TSTORE=0: plain)
     int max_ksplit = 4;             // K slices per GEMM tile at most (1, 2 or 4)
     WideParams *par = nullptr;      // device copy of the pass's values
     WideParams *par_host = nullptr; // pinned ring
@@ -1409,6 +1410,8 @@ fm_status create_wide(fm_handle *h, cudaStream_t s) {
   if (xs && atoi(xs) >= 1 && atoi(xs) <= 8) w.xsplits = atoi(xs);
   const char *mk = getenv("FM_WIDE_MAX_KSPLIT");
   if (mk && atoi(mk) >= 1 && atoi(mk) <= 4) w.max_ksplit = atoi(mk);
+  const char *ts = getenv("FM_WIDE_TSTORE");
+  w.tstore = !(ts && ts[0] == '0');
   TRY(dalloc(h, &w.par, 1));
   CK(cudaMallocHost(&w.par_host, sizeof(WideParams) * kParamSlots));
   w.rows_cap = h->pf_rows;
@@ -1455,6 +1458,15 @@ fm_status run_tc(fm_handle *h, const TcGemmArgs &g, cudaStream_t s, const char *
   ProfScope ps(h, s, tag, 2.0 * g.M * g.N * g.K);   // GEMM records carry their FLOPs
   CK(launch_tc_gemm(g, h->n_sm, s));
   ++h->last_launches;
+  return FM_OK;
+}
+
+// A single-output product of a batched pass stores its tile through tensor copies: the output's map
+// covers the pass's rows, so a ragged last row block is clipped.
+fm_status wide_tstore(fm_handle *h, TcGemmArgs &g, const void *out, int rows, int cols, bool f32) {
+  if (!h->wide.tstore) return FM_OK;
+  if (!make_tma_out(&g.tma_o, out, rows, cols, f32)) return fail(h, FM_ERR_CUDA, "tensor map encoding failed");
+  g.tstore = 1;
   return FM_OK;
 }
 
@@ -1514,6 +1526,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.out32 = w.qkv_out;
     g.ldo32 = 3 * D;
     g.row_pos = WIDE_FIELD(h, row_pos);
+    TRY(wide_tstore(h, g, w.qkv_out, T, 3 * D, true));
     TRY(run_tc(h, g, s, "wide.gemm_qkv_self"));
     {
       ProfScope ps(h, s, "wide.attn_self", (double)T * D * 3 * 4 + (double)T * D * 2);
@@ -1524,6 +1537,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.out32 = w.br;
     g.ldo32 = D;
     g.gate = ms + 2 * D;
+    TRY(wide_tstore(h, g, w.br, T, D, true));
     TRY(run_tc(h, g, s, "wide.gemm_o_self"));
     // cross-attention over each sequence's own cache rows 0 .. pos
     TRY(run_lnmod(h, mc, T, true, s));
@@ -1533,6 +1547,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.out32 = w.qc;
     g.ldo32 = D;
     g.row_pos = WIDE_FIELD(h, row_pos);
+    TRY(wide_tstore(h, g, w.qc, T, D, true));
     TRY(run_tc(h, g, s, "wide.gemm_q_cross"));
     {
       XAttnArgs xa;
@@ -1566,6 +1581,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.out32 = w.br;
     g.ldo32 = D;
     g.gate = mc + 2 * D;
+    TRY(wide_tstore(h, g, w.br, T, D, true));
     TRY(run_tc(h, g, s, "wide.gemm_o_cross"));
     // MLP
     TRY(run_lnmod(h, mm, T, true, s));
@@ -1574,12 +1590,14 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     g.gelu = 1;
     g.out16 = w.u16;
     g.ldo = F;
+    TRY(wide_tstore(h, g, w.u16, T, F, false));
     TRY(run_tc(h, g, s, "wide.gemm_fc1"));
     g = wide_gemm(h, w.m_u16, w.t_f2[l], T, D, F, TC_EPI_GATED);
     g.bias = h->b_f2[l];
     g.out32 = w.br;
     g.ldo32 = D;
     g.gate = mm + 2 * D;
+    TRY(wide_tstore(h, g, w.br, T, D, true));
     TRY(run_tc(h, g, s, "wide.gemm_fc2"));
   }
   // the last MLP branch joins the stream; final adaLN -> head -> lm_head with the per-row argmax

@@ -131,6 +131,40 @@ __device__ __forceinline__ void store_f16x32(__half *dst, const float *v) {
   for (int j = 0; j < 32; j += 8) store_h8(dst + j, v + j);
 }
 
+// Tensor-store staging: the epilogue's columns [c_lo, c_hi) as boxes of 128 rows x 128 bytes (32 f32 or
+// 64 f16 columns, 16 KB each, one after another), each row's 16-byte units XOR-swizzled by (row & 7): the
+// layout a 128-byte-swizzle tensor copy reads (box bases 1024-byte aligned).
+constexpr int kBoxBytes = BM * 128;
+__device__ __forceinline__ void stage_f32x32(uint8_t *stage, int rel, int rl, const float *v) {
+  uint8_t *row = stage + (size_t)(rel >> 5) * kBoxBytes + rl * 128;
+  const int sw = rl & 7;
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<float4 *>(row + ((u ^ sw) << 4)) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+}
+__device__ __forceinline__ void stage_f16x32(uint8_t *stage, int rel, int rl, const float *v) {
+  uint8_t *row = stage + (size_t)(rel >> 6) * kBoxBytes + rl * 128;
+  const int sw = rl & 7, u0 = (rel & 63) >> 3;   // these 32 columns are units u0 .. u0 + 3 of the row
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float *w = v + 8 * j;
+    __half2 h0 = __floats2half2_rn(w[0], w[1]), h1 = __floats2half2_rn(w[2], w[3]);
+    __half2 h2 = __floats2half2_rn(w[4], w[5]), h3 = __floats2half2_rn(w[6], w[7]);
+    uint4 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&h0);
+    pk.y = *reinterpret_cast<uint32_t *>(&h1);
+    pk.z = *reinterpret_cast<uint32_t *>(&h2);
+    pk.w = *reinterpret_cast<uint32_t *>(&h3);
+    *reinterpret_cast<uint4 *>(row + (((u0 + j) ^ sw) << 4)) = pk;
+  }
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+
 // Per-column operands of a tile (gate, bias, norm weight), staged once per tile
 // in shared memory by the epilogue threads (one round trip for all of them),
 // and the per-row values the two threads of a row exchange.
@@ -302,21 +336,25 @@ __device__ void epilogue_kv(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int
 // q / k / v rows: segment s = n / seg_cols; segments 0 and 1 take a per-head
 // RMSNorm with their weight (when given) and RoPE at the row's position
 __device__ void epilogue_segs(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row, int n0,
-                              int c_lo, int c_hi) {
+                              int c_lo, int c_hi, uint8_t *stage) {
   const bool live = row < a.M;
   const int seg = n0 / a.seg_cols;
   const bool norm = (seg == 0 && a.nw0) || (seg == 1 && a.nw1);
   const int p = live ? (a.row_pos ? a.row_pos[row] : a.start + row) : 0;
   float *out = a.out32 + (size_t)(live ? row : 0) * a.ldo32 + n0;
   norm_rope_half(a, ep, taddr, rl, h, 1.f, norm, p, c_lo, c_hi, [&](int c0, const float *v) {
-    if (live) store_f32x32(out + c0, v);
+    if (!live) return;
+    if (stage)
+      stage_f32x32(stage, c0 - c_lo, rl, v);
+    else
+      store_f32x32(out + c0, v);
   });
 }
 
 // F16: bias (+ exact GELU) -> f16; GATED: gate * (acc + bias) -> f32 (the residual
 // stream adds it in the next kernel)
-__device__ void epilogue_f16(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int h, int row, int n0, int c_lo,
-                             int c_hi) {
+__device__ void epilogue_f16(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row, int n0,
+                             int c_lo, int c_hi, uint8_t *stage) {
   const bool live = row < a.M;
   const bool gated = a.epi == TC_EPI_GATED;
   const int w = (c_hi - c_lo) / n_halves();
@@ -330,13 +368,21 @@ __device__ void epilogue_f16(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, in
       for (int j = 0; j < 32; ++j) v[j] *= ep->gate[c0 + j];
     }
     if (!live) continue;
-    if (a.out32) store_f32x32(a.out32 + (size_t)row * a.ldo32 + n0 + c0, v);
+    if (a.out32) {
+      if (stage)   // a staged epilogue has this single output
+        stage_f32x32(stage, c0 - c_lo, rl, v);
+      else
+        store_f32x32(a.out32 + (size_t)row * a.ldo32 + n0 + c0, v);
+    }
     if (!a.out16) continue;
     if (a.gelu) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
     }
-    store_f16x32(a.out16 + (size_t)row * a.ldo + n0 + c0, v);
+    if (stage)
+      stage_f16x32(stage, c0 - c_lo, rl, v);
+    else
+      store_f16x32(a.out16 + (size_t)row * a.ldo + n0 + c0, v);
   }
 }
 
@@ -447,18 +493,30 @@ __device__ __forceinline__ int epilogue_pieces(const TcGemmArgs &a, int ks) {
 }
 
 // staged: the tile's columns are already in shared memory (the CTA's first tile, staged
-// before griddepcontrol.wait)
+// before griddepcontrol.wait).  stage: the tensor-store staging area (null: plain stores);
+// its boxes go out through a.tma_o once every epilogue thread has written its rows.
 __device__ __forceinline__ void run_epilogue(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row,
-                                             int nb, int st_col, int c_lo, int c_hi, bool staged) {
+                                             int nb, int st_col, int c_lo, int c_hi, bool staged, uint8_t *stage) {
   const int n0 = nb * BN;
   if (a.epi != TC_EPI_ARGMAX && !staged) stage_cols(a, ep, n0, (int)threadIdx.x - 64);
+  if ((a.epi != TC_EPI_SEGS && a.epi != TC_EPI_F16 && a.epi != TC_EPI_GATED) || (a.out16 && a.out32)) stage = nullptr;
   switch (a.epi) {
     case TC_EPI_FC: epilogue_fc(a, ep, taddr, rl, h, row, n0, st_col, c_lo, c_hi); break;
     case TC_EPI_KV: epilogue_kv(a, ep, taddr, rl, h, row, n0, c_lo, c_hi); break;
     case TC_EPI_F16:
-    case TC_EPI_GATED: epilogue_f16(a, ep, taddr, h, row, n0, c_lo, c_hi); break;
-    case TC_EPI_SEGS: epilogue_segs(a, ep, taddr, rl, h, row, n0, c_lo, c_hi); break;
+    case TC_EPI_GATED: epilogue_f16(a, ep, taddr, rl, h, row, n0, c_lo, c_hi, stage); break;
+    case TC_EPI_SEGS: epilogue_segs(a, ep, taddr, rl, h, row, n0, c_lo, c_hi, stage); break;
     default: epilogue_argmax(a, ep, taddr, rl, h, row, n0, nb); break;
+  }
+  if (!stage) return;
+  fence_proxy_async();            // the rows written above are visible to the tensor copies
+  named_sync(1, n_epi());
+  if (threadIdx.x == 64) {
+    const int cols = a.out16 ? 64 : 32;   // per box
+    for (int i = 0; i < (c_hi - c_lo) / cols; ++i)
+      tma_store_2d(&a.tma_o, smem_u32(stage + (size_t)i * kBoxBytes), n0 + c_lo + i * cols, row - rl);
+    asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");   // written before the CTA ends
   }
 }
 
@@ -612,7 +670,9 @@ __global__ void __launch_bounds__(NT, 1) fm_prefill_gemm_kernel(const __grid_con
       }
       int mb, nb;
       tile_coords(u, n_mb, n_nb, gm, mb, nb);
-      run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb, 0, BN, tc == 0);
+      // one tile per CTA: the operand ring is idle once its MMAs are done and stages the tensor stores
+      uint8_t *stage = a.tstore && (int)gridDim.x >= n_units ? gbase : nullptr;
+      run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb, 0, BN, tc == 0, stage);
       tc_fence_before();
       mbar_arrive(tempty(b));
     }
@@ -635,7 +695,9 @@ __global__ void __launch_bounds__(NT, 1) fm_prefill_gemm_kernel(const __grid_con
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
         tc_fence_after();
         reduce_piece(taddr, rl, half, reinterpret_cast<float *>(gbase), ks, c_lo, c_lo + w);
-        run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb * pieces + slice, c_lo, c_lo + w, true);
+        // the tensor-store staging sits behind the partial tile (8 blocks of 128 x 32 f32) that peers read
+        uint8_t *stage = a.tstore ? gbase + (size_t)(BN / 32) * BM * 32 * 4 : nullptr;
+        run_epilogue(a, ep, taddr, rl, half, mb * BM + rl, nb, nb * pieces + slice, c_lo, c_lo + w, true, stage);
       }
     }
     // no CTA leaves (or frees its shared memory) while a peer may still read its partial
@@ -694,6 +756,20 @@ bool make_tma_f16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t col
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tma_out(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, bool f32) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)BM};
+  cuuint32_t el[2] = {1, 1};
+  CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void *>(ptr), dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

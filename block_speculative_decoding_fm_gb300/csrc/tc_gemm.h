@@ -23,6 +23,12 @@ enum TcEpi : int32_t {
 struct TcGemmArgs {
   CUtensorMap tma_a;  // A [M][K] f16, box 64 x 128
   CUtensorMap tma_b;  // B [N][K] f16, box 64 x 256
+  // tensor stores (tstore = 1; SEGS / GATED / F16 with a single output, when each CTA has one tile):
+  // the epilogue writes its columns into shared memory in the 128-byte-swizzle layout and tensor
+  // copies store them through this map of the output ([M][cols], f32 box 32 x 128 or f16 box
+  // 64 x 128; rows past M are clipped).  With several tiles per CTA the plain stores run instead.
+  CUtensorMap tma_o;
+  int32_t tstore;
   int32_t M, N, K;
   int32_t epi;
   // tile order: groups of group_m consecutive 128-row blocks; inside a group
@@ -74,6 +80,8 @@ struct TcGemmArgs {
 };
 
 bool make_tma_f16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// the output map of a tensor-store epilogue: [rows][cols] f32 (box 32 x 128) or f16 (box 64 x 128)
+bool make_tma_out(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, bool f32);
 size_t tc_gemm_smem_bytes();
 // column blocks of 256 (N must be a multiple of 256), row blocks of 128
 inline int tc_gemm_tiles(int M, int N) { return ((M + 127) / 128) * (N / 256); }
