@@ -44,86 +44,81 @@ __global__ void wide_prep_kernel(const float *__restrict__ h0, int D, int T, flo
   }
 }
 
-// one warp per row; D <= 4096, a multiple of 128.  With R: the residual stream
-// first takes the gated branch the previous product wrote (X += R, stored back).
-// The modulation rows (weights, not written by earlier kernels) are staged in
-// shared memory before griddepcontrol.wait.
+// Sum over the CTA (at most 8 warps) in warp order, the same value in every thread; slot k of red
+// is this reduction's own, so two reductions need one barrier each.
+__device__ __forceinline__ float block_sum(float v, float (*red)[8], int k) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[k][warp] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int i = 0; i < nw; ++i) s += red[k][i];
+  return s;
+}
+
+// one CTA per row of D columns (a multiple of 256, at most 4096): float4 i of the row goes to thread
+// i % blockDim.x, at most 4 per thread.  With R: the residual stream first takes the gated branch the
+// previous product wrote (X += R, stored back).  A thread's modulation columns (weights, not written by
+// earlier kernels) are loaded before griddepcontrol.wait.
 __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict__ R, int D, int T,
                                   const float *__restrict__ scale, const float *__restrict__ shift, float eps,
                                   __half *__restrict__ out) {
-  extern __shared__ float4 mods[];   // [D / 4] scale, then [D / 4] shift
+  __shared__ float red[2][8];
   pdl_trigger();
-  {
-    // all of a thread's loads first, then its shared-memory stores (D / 4 <= 1024 float4 per row over 128 threads)
-    float4 sv[8], hv[8];
+  const int t = threadIdx.x, nt = blockDim.x, n4 = D / 4, row = blockIdx.x;
+  float4 sc[4], sh[4], v[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = threadIdx.x + j * blockDim.x;
-      if (i < D / 4) {
-        sv[j] = reinterpret_cast<const float4 *>(scale)[i];
-        hv[j] = reinterpret_cast<const float4 *>(shift)[i];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = threadIdx.x + j * blockDim.x;
-      if (i < D / 4) {
-        mods[i] = sv[j];
-        mods[D / 4 + i] = hv[j];
-      }
+  for (int q = 0; q < 4; ++q) {
+    if (t + q * nt < n4) {
+      sc[q] = reinterpret_cast<const float4 *>(scale)[t + q * nt];
+      sh[q] = reinterpret_cast<const float4 *>(shift)[t + q * nt];
     }
   }
-  __syncthreads();
   pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
   if (row >= T) return;
-  const int per = D / 128;   // float4 per lane
   float4 *x = reinterpret_cast<float4 *>(X + (size_t)row * D);
   const float4 *r = R ? reinterpret_cast<const float4 *>(R + (size_t)row * D) : nullptr;
-  float4 v[32];
+  float4 g[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {   // every load of the row before any store
+    if (t + q * nt < n4) {
+      v[q] = x[t + q * nt];
+      if (r) g[q] = r[t + q * nt];
+    }
+  }
   float s = 0.f;
-  // every load of the row is issued before any store
 #pragma unroll
-  for (int u = 0; u < 32; ++u) {
-    if (u < per) {
-      v[u] = x[u * 32 + lane];
+  for (int q = 0; q < 4; ++q) {
+    if (t + q * nt < n4) {
       if (r) {
-        const float4 g = r[u * 32 + lane];
-        v[u].x += g.x;
-        v[u].y += g.y;
-        v[u].z += g.z;
-        v[u].w += g.w;
+        v[q].x += g[q].x;
+        v[q].y += g[q].y;
+        v[q].z += g[q].z;
+        v[q].w += g[q].w;
+        x[t + q * nt] = v[q];
       }
-      s += (v[u].x + v[u].y) + (v[u].z + v[u].w);
+      s += (v[q].x + v[q].y) + (v[q].z + v[q].w);
     }
   }
-  if (r) {
+  const float mean = block_sum(s, red, 0) / (float)D;
+  float m2 = 0.f;
 #pragma unroll
-    for (int u = 0; u < 32; ++u)
-      if (u < per) x[u * 32 + lane] = v[u];
-  }
-  const float mean = warp_sum(s) / (float)D;
-  float q = 0.f;
-#pragma unroll
-  for (int u = 0; u < 32; ++u) {
-    if (u < per) {
-      const float a = v[u].x - mean, b = v[u].y - mean, c = v[u].z - mean, d = v[u].w - mean;
-      q += (a * a + b * b) + (c * c + d * d);
+  for (int q = 0; q < 4; ++q) {
+    if (t + q * nt < n4) {
+      const float a = v[q].x - mean, b = v[q].y - mean, c = v[q].z - mean, d = v[q].w - mean;
+      m2 += (a * a + b * b) + (c * c + d * d);
     }
   }
-  const float rstd = rsqrtf(warp_sum(q) / (float)D + eps);
+  const float rstd = rsqrtf(block_sum(m2, red, 1) / (float)D + eps);
   __half *o = out + (size_t)row * D;
 #pragma unroll
-  for (int u = 0; u < 32; ++u) {
-    if (u < per) {
-      const int i4 = u * 32 + lane;
-      const float4 sc = mods[i4];
-      const float4 sh = mods[D / 4 + i4];
-      const __half2 h01 = __floats2half2_rn((v[u].x - mean) * rstd * (1.f + sc.x) + sh.x,
-                                            (v[u].y - mean) * rstd * (1.f + sc.y) + sh.y);
-      const __half2 h23 = __floats2half2_rn((v[u].z - mean) * rstd * (1.f + sc.z) + sh.z,
-                                            (v[u].w - mean) * rstd * (1.f + sc.w) + sh.w);
+  for (int q = 0; q < 4; ++q) {
+    if (t + q * nt < n4) {
+      const int i4 = t + q * nt;
+      const __half2 h01 = __floats2half2_rn((v[q].x - mean) * rstd * (1.f + sc[q].x) + sh[q].x,
+                                            (v[q].y - mean) * rstd * (1.f + sc[q].y) + sh[q].y);
+      const __half2 h23 = __floats2half2_rn((v[q].z - mean) * rstd * (1.f + sc[q].z) + sh[q].z,
+                                            (v[q].w - mean) * rstd * (1.f + sc[q].w) + sh[q].w);
       uint2 pk;
       pk.x = *reinterpret_cast<const uint32_t *>(&h01);
       pk.y = *reinterpret_cast<const uint32_t *>(&h23);
@@ -132,10 +127,13 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
   }
 }
 
-// one CTA (128 threads) per (sequence, head): O = softmax(q k^T / sqrt(128)) v over the B slots
+// one CTA (128 threads) per (sequence, head): O = softmax(q k^T / sqrt(128)) v over the B <= 16 slots.
+// Scores: thread i takes the pairs (n, j) = (i / 16, i % 16) and (i / 16 + 8, i % 16) over the 128 dims
+// with four partial sums; softmax: a half-warp per row (lane j holds score j), maximum and sum by
+// shuffles inside the half; output: thread = dim, all rows at once (16 independent sums).
 __global__ void wide_self_attn_kernel(const float *__restrict__ qkv, int D, int B, __half *__restrict__ out) {
-  constexpr int HD = 128;
-  __shared__ float q[16][HD], k[16][HD], v[16][HD];
+  constexpr int HD = 128, KS = HD + 4;   // padded q / k rows
+  __shared__ __align__(16) float q[16][KS], k[16][KS], v[16][HD];
   __shared__ float p[16][17];
   pdl_trigger();
   pdl_wait();
@@ -164,32 +162,53 @@ __global__ void wide_self_attn_kernel(const float *__restrict__ qkv, int D, int 
   }
   __syncthreads();
   const float scale = 0.08838834764831845f;   // 1 / sqrt(128)
-  for (int pr = t; pr < B * B; pr += blockDim.x) {
-    const int n = pr / B, j = pr % B;
-    float s = 0.f;
+  {
+    const int j = t & 15;
+#pragma unroll
+    for (int y = 0; y < 2; ++y) {
+      const int n = (t >> 4) + 8 * y;
+      if (n < B && j < B) {
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll 8
-    for (int d = 0; d < HD; ++d) s += q[n][(d + j) & (HD - 1)] * k[j][(d + j) & (HD - 1)];
-    p[n][j] = s * scale;
-  }
-  __syncthreads();
-  if (t < B) {
-    float m = -INFINITY;
-    for (int j = 0; j < B; ++j) m = fmaxf(m, p[t][j]);
-    float l = 0.f;
-    for (int j = 0; j < B; ++j) {
-      const float e = expf(p[t][j] - m);
-      p[t][j] = e;
-      l += e;
+        for (int d = 0; d < HD; d += 4) {
+          const float4 a = *reinterpret_cast<const float4 *>(&q[n][d]);
+          const float4 b = *reinterpret_cast<const float4 *>(&k[j][d]);
+          s0 += a.x * b.x; s1 += a.y * b.y; s2 += a.z * b.z; s3 += a.w * b.w;
+        }
+        p[n][j] = ((s0 + s1) + (s2 + s3)) * scale;
+      }
     }
-    const float inv = 1.f / l;
-    for (int j = 0; j < B; ++j) p[t][j] *= inv;
   }
   __syncthreads();
-  for (int n = 0; n < B; ++n) {
-    float o = 0.f;
-    for (int j = 0; j < B; ++j) o += p[n][j] * v[j][t];
-    out[(size_t)(r0 + n) * D + head * HD + t] = __float2half_rn(o);
+  {
+    const int lane = t & 31, j = lane & 15;
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int n = 2 * (t >> 5) + (lane >> 4) + 8 * pass;
+      const bool on = n < B && j < B;
+      const float sc = on ? p[n][j] : -INFINITY;
+      float m = sc;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const float e = on ? expf(sc - m) : 0.f;
+      float l = e;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      if (on) p[n][j] = e / l;
+    }
   }
+  __syncthreads();
+  float o[16];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n] = 0.f;
+  for (int j = 0; j < B; ++j) {
+    const float vj = v[j][t];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n] += p[n][j] * vj;
+  }
+#pragma unroll
+  for (int n = 0; n < 16; ++n)
+    if (n < B) out[(size_t)(r0 + n) * D + head * HD + t] = __float2half_rn(o[n]);
 }
 
 // one warp per row: the best (value, index) over the row's column-block bests, in block order
@@ -273,10 +292,12 @@ cudaError_t launch_wide_prep(const float *h0, int D, int T, float *X, const Wide
 
 cudaError_t launch_wide_lnmod(float *X, const float *R, int D, int T, const float *scale, const float *shift, float eps,
                               __half *out, cudaStream_t s) {
-  if (D % 128 || D > 4096) return cudaErrorInvalidValue;
+  if (D % 256 || D > 4096 || T < 1) return cudaErrorInvalidValue;
   void *args[] = {(void *)&X, (void *)&R, (void *)&D, (void *)&T, (void *)&scale, (void *)&shift, (void *)&eps,
                   (void *)&out};
-  return launch_pdl((const void *)wide_lnmod_kernel, dim3((T + 3) / 4), dim3(128), args, s, (size_t)D * 8);
+  // D / 8 threads (two float4 each, whole warps) up to 256; wider rows give a thread up to four
+  const int nt = D / 8 < 256 ? D / 8 : 256;
+  return launch_pdl((const void *)wide_lnmod_kernel, dim3(T), dim3(nt), args, s, 0);
 }
 
 cudaError_t launch_wide_self_attn(const float *qkv, int D, int B, int n_seqs, int n_heads, __half *out, cudaStream_t s) {
