@@ -1470,6 +1470,21 @@ fm_status wide_tstore(fm_handle *h, TcGemmArgs &g, const void *out, int rows, in
   return FM_OK;
 }
 
+// A gated residual product: with tensor stores its tile is added into the residual stream X by tensor
+// reduce-add copies (each element gets its one addend); otherwise it writes the branch to br, which the
+// next adaLN adds.
+fm_status wide_gated(fm_handle *h, TcGemmArgs &g, int T) {
+  fm_handle::Wide &w = h->wide;
+  g.ldo32 = h->cfg.dim;
+  if (!w.tstore) {
+    g.out32 = w.br;
+    return FM_OK;
+  }
+  g.out32 = w.X;
+  g.treduce = 1;
+  return wide_tstore(h, g, w.X, T, h->cfg.dim, true);
+}
+
 // the residual stream takes the previous product's gated branch (when `add`), then adaLN
 fm_status run_lnmod(fm_handle *h, const float *m, int T, bool add, cudaStream_t s) {
   const int D = h->cfg.dim;
@@ -1518,7 +1533,7 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     const float *mc = h->mod + (size_t)(3 * l + 1) * 3 * D;
     const float *mm = h->mod + (size_t)(3 * l + 2) * 3 * D;
     // self-attention over each sequence's block (the previous layer's MLP branch joins the stream first)
-    TRY(run_lnmod(h, ms, T, l > 0, s));
+    TRY(run_lnmod(h, ms, T, l > 0 && !w.tstore, s));
     g = wide_gemm(h, w.m_a16, w.t_qkv[l], T, 3 * D, D, TC_EPI_SEGS);
     g.seg_cols = D;
     g.nw0 = h->w_sqn[l];
@@ -1534,13 +1549,11 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
       ++h->last_launches;
     }
     g = wide_gemm(h, w.m_o16, w.t_so[l], T, D, D, TC_EPI_GATED);
-    g.out32 = w.br;
-    g.ldo32 = D;
     g.gate = ms + 2 * D;
-    TRY(wide_tstore(h, g, w.br, T, D, true));
+    TRY(wide_gated(h, g, T));
     TRY(run_tc(h, g, s, "wide.gemm_o_self"));
     // cross-attention over each sequence's own cache rows 0 .. pos
-    TRY(run_lnmod(h, mc, T, true, s));
+    TRY(run_lnmod(h, mc, T, !w.tstore, s));
     g = wide_gemm(h, w.m_a16, w.t_cq[l], T, D, D, TC_EPI_SEGS);
     g.seg_cols = D;
     g.nw0 = h->w_cqn[l];
@@ -1578,13 +1591,11 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
       ++h->last_launches;
     }
     g = wide_gemm(h, w.m_o16, w.t_co[l], T, D, D, TC_EPI_GATED);
-    g.out32 = w.br;
-    g.ldo32 = D;
     g.gate = mc + 2 * D;
-    TRY(wide_tstore(h, g, w.br, T, D, true));
+    TRY(wide_gated(h, g, T));
     TRY(run_tc(h, g, s, "wide.gemm_o_cross"));
     // MLP
-    TRY(run_lnmod(h, mm, T, true, s));
+    TRY(run_lnmod(h, mm, T, !w.tstore, s));
     g = wide_gemm(h, w.m_a16, w.t_f1[l], T, F, D, TC_EPI_F16);
     g.bias = h->b_f1[l];
     g.gelu = 1;
@@ -1594,14 +1605,12 @@ fm_status wide_chain(fm_handle *h, int n, int xs, cudaStream_t s) {
     TRY(run_tc(h, g, s, "wide.gemm_fc1"));
     g = wide_gemm(h, w.m_u16, w.t_f2[l], T, D, F, TC_EPI_GATED);
     g.bias = h->b_f2[l];
-    g.out32 = w.br;
-    g.ldo32 = D;
     g.gate = mm + 2 * D;
-    TRY(wide_tstore(h, g, w.br, T, D, true));
+    TRY(wide_gated(h, g, T));
     TRY(run_tc(h, g, s, "wide.gemm_fc2"));
   }
   // the last MLP branch joins the stream; final adaLN -> head -> lm_head with the per-row argmax
-  TRY(run_lnmod(h, h->mod + (size_t)(3 * L) * 3 * D, T, true, s));
+  TRY(run_lnmod(h, h->mod + (size_t)(3 * L) * 3 * D, T, !w.tstore, s));
   g = wide_gemm(h, w.m_a16, w.t_head, T, Ht, D, TC_EPI_F16);
   g.bias = h->b_head;
   g.out16 = w.y16;

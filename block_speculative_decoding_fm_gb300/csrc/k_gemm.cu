@@ -158,6 +158,12 @@ __device__ __forceinline__ void stage_f16x32(uint8_t *stage, int rel, int rl, co
     *reinterpret_cast<uint4 *>(row + (((u0 + j) ^ sw) << 4)) = pk;
   }
 }
+__device__ __forceinline__ void tma_add_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -369,10 +375,16 @@ __device__ void epilogue_f16(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, in
     }
     if (!live) continue;
     if (a.out32) {
-      if (stage)   // a staged epilogue has this single output
+      float *dst = a.out32 + (size_t)row * a.ldo32 + n0 + c0;
+      if (stage) {   // a staged epilogue has this single output
         stage_f32x32(stage, c0 - c_lo, rl, v);
-      else
-        store_f32x32(a.out32 + (size_t)row * a.ldo32 + n0 + c0, v);
+      } else {
+        if (a.treduce) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += __ldcg(dst + j);
+        }
+        store_f32x32(dst, v);
+      }
     }
     if (!a.out16) continue;
     if (a.gelu) {
@@ -513,8 +525,13 @@ __device__ __forceinline__ void run_epilogue(const TcGemmArgs &a, EpCols *ep, ui
   named_sync(1, n_epi());
   if (threadIdx.x == 64) {
     const int cols = a.out16 ? 64 : 32;   // per box
-    for (int i = 0; i < (c_hi - c_lo) / cols; ++i)
-      tma_store_2d(&a.tma_o, smem_u32(stage + (size_t)i * kBoxBytes), n0 + c_lo + i * cols, row - rl);
+    for (int i = 0; i < (c_hi - c_lo) / cols; ++i) {
+      const uint32_t src = smem_u32(stage + (size_t)i * kBoxBytes);
+      if (a.treduce)
+        tma_add_2d(&a.tma_o, src, n0 + c_lo + i * cols, row - rl);
+      else
+        tma_store_2d(&a.tma_o, src, n0 + c_lo + i * cols, row - rl);
+    }
     asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
     asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");   // written before the CTA ends
   }

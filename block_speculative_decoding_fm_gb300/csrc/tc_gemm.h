@@ -15,7 +15,7 @@ enum TcEpi : int32_t {
   TC_EPI_KV = 1,      // row scale 1/rms, k_norm + RoPE on K heads, f16 stores into the head-major caches
   TC_EPI_F16 = 2,     // out16 = f16(act(acc + bias)), act = identity or exact GELU (out16 null: none);
                       // optionally out32 = acc + bias
-  TC_EPI_GATED = 3,   // out32[row][n] = gate[n] * (acc + bias[n])   (a gated residual branch)
+  TC_EPI_GATED = 3,   // out32[row][n] = gate[n] * (acc + bias[n])   (a gated residual branch; treduce: +=)
   TC_EPI_SEGS = 4,    // out32: per-head RMSNorm + interleaved-pair RoPE on segments 0 / 1, plain elsewhere
   TC_EPI_ARGMAX = 5,  // per row, the best (value, lowest index) over the tile's columns < n_valid
 };
@@ -29,6 +29,9 @@ struct TcGemmArgs {
   // 64 x 128; rows past M are clipped).  With several tiles per CTA the plain stores run instead.
   CUtensorMap tma_o;
   int32_t tstore;
+  // GATED with tstore: the tensor copies add the tile into out32 (the residual stream X += branch, one
+  // addend per element) instead of storing it; without the staged path the epilogue adds in place
+  int32_t treduce;
   int32_t M, N, K;
   int32_t epi;
   // tile order: groups of group_m consecutive 128-row blocks; inside a group
