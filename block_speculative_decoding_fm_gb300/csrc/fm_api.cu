@@ -136,7 +136,7 @@ struct fm_handle {
     CUtensorMap t_ap{}, t_head{}, t_table{}, t_cache{};
     // activations: X [rows][D] f32; q/k/v and cross q f32; the head output f32 and f16
     float *X = nullptr, *qkv_out = nullptr, *qc = nullptr, *Y = nullptr, *kst = nullptr;
-    float *br = nullptr;            // a product's gated residual branch, added by the next adaLN
+    float *br = nullptr;            // without tensor stores: a product's gated branch, added by the next adaLN
     __half *a16 = nullptr, *o16 = nullptr, *u16 = nullptr, *y16 = nullptr, *anc16 = nullptr, *kin16 = nullptr;
     CUtensorMap m_a16{}, m_o16{}, m_u16{}, m_y16{}, m_anc16{}, m_kin16{};
     float2 *amax = nullptr;         // lm_head per-row, per-column-block bests

@@ -357,8 +357,8 @@ __device__ void epilogue_segs(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, i
   });
 }
 
-// F16: bias (+ exact GELU) -> f16; GATED: gate * (acc + bias) -> f32 (the residual
-// stream adds it in the next kernel)
+// F16: bias (+ exact GELU) -> f16; GATED: gate * (acc + bias) -> f32, the residual branch
+// (treduce: added into out32, the residual stream, by the tensor reduce-add copies or in place)
 __device__ void epilogue_f16(const TcGemmArgs &a, EpCols *ep, uint32_t taddr, int rl, int h, int row, int n0,
                              int c_lo, int c_hi, uint8_t *stage) {
   const bool live = row < a.M;

@@ -6,7 +6,9 @@
 //                     noise), and each sequence's anchor row is gathered from
 //                     the f16 token table (the anchor_proj operand);
 //   * wide_lnmod      adds the gated branch of the previous product to the
-//                     residual stream (``gateAdd``), then adaLN LayerNorm-modulate
+//                     residual stream (``gateAdd``) when that product wrote it
+//                     apart (its tensor reduce-add copies otherwise added it
+//                     already), then adaLN LayerNorm-modulate
 //                     of each row (``lnMod``): two-pass mean / population
 //                     variance, * (1 + scale) + shift, f16 out (the next
 //                     product's operand);
