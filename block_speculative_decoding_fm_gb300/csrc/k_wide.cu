@@ -62,15 +62,17 @@ __device__ __forceinline__ float block_sum(float v, float (*red)[8], int k) {
 // i % blockDim.x, at most 4 per thread.  With R: the residual stream first takes the gated branch the
 // previous product wrote (X += R, stored back).  A thread's modulation columns (weights, not written by
 // earlier kernels) are loaded before griddepcontrol.wait.
-__global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict__ R, int D, int T,
-                                  const float *__restrict__ scale, const float *__restrict__ shift, float eps,
-                                  __half *__restrict__ out) {
+template <int Q>   // float4 per thread at most (2 for rows up to 2048 columns, else 4): the register budget
+__global__ void __launch_bounds__(256) wide_lnmod_kernel(float *__restrict__ X, const float *__restrict__ R, int D,
+                                                          int T, const float *__restrict__ scale,
+                                                          const float *__restrict__ shift, float eps,
+                                                          __half *__restrict__ out) {
   __shared__ float red[2][8];
   pdl_trigger();
   const int t = threadIdx.x, nt = blockDim.x, n4 = D / 4, row = blockIdx.x;
-  float4 sc[4], sh[4], v[4];
+  float4 sc[Q], sh[Q], v[Q];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < Q; ++q) {
     if (t + q * nt < n4) {
       sc[q] = reinterpret_cast<const float4 *>(scale)[t + q * nt];
       sh[q] = reinterpret_cast<const float4 *>(shift)[t + q * nt];
@@ -80,9 +82,9 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
   if (row >= T) return;
   float4 *x = reinterpret_cast<float4 *>(X + (size_t)row * D);
   const float4 *r = R ? reinterpret_cast<const float4 *>(R + (size_t)row * D) : nullptr;
-  float4 g[4];
+  float4 g[Q];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {   // every load of the row before any store
+  for (int q = 0; q < Q; ++q) {   // every load of the row before any store
     if (t + q * nt < n4) {
       v[q] = x[t + q * nt];
       if (r) g[q] = r[t + q * nt];
@@ -90,7 +92,7 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
   }
   float s = 0.f;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < Q; ++q) {
     if (t + q * nt < n4) {
       if (r) {
         v[q].x += g[q].x;
@@ -105,7 +107,7 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
   const float mean = block_sum(s, red, 0) / (float)D;
   float m2 = 0.f;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < Q; ++q) {
     if (t + q * nt < n4) {
       const float a = v[q].x - mean, b = v[q].y - mean, c = v[q].z - mean, d = v[q].w - mean;
       m2 += (a * a + b * b) + (c * c + d * d);
@@ -114,7 +116,7 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
   const float rstd = rsqrtf(block_sum(m2, red, 1) / (float)D + eps);
   __half *o = out + (size_t)row * D;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < Q; ++q) {
     if (t + q * nt < n4) {
       const int i4 = t + q * nt;
       const __half2 h01 = __floats2half2_rn((v[q].x - mean) * rstd * (1.f + sc[q].x) + sh[q].x,
@@ -132,7 +134,7 @@ __global__ void wide_lnmod_kernel(float *__restrict__ X, const float *__restrict
 // one CTA (128 threads) per (sequence, head): O = softmax(q k^T / sqrt(128)) v over the B <= 16 slots.
 // Scores: thread i takes the pairs (n, j) = (i / 16, i % 16) and (i / 16 + 8, i % 16) over the 128 dims
 // with four partial sums; softmax: a half-warp per row (lane j holds score j), maximum and sum by
-// shuffles inside the half; output: thread = dim, all rows at once (16 independent sums).
+// shuffles inside the half; output: a warp per four rows, a lane per four dims.
 __global__ void wide_self_attn_kernel(const float *__restrict__ qkv, int D, int B, __half *__restrict__ out) {
   constexpr int HD = 128, KS = HD + 4;   // padded q / k rows
   __shared__ __align__(16) float q[16][KS], k[16][KS], v[16][HD];
@@ -200,17 +202,27 @@ __global__ void wide_self_attn_kernel(const float *__restrict__ qkv, int D, int 
     }
   }
   __syncthreads();
-  float o[16];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n] = 0.f;
+  // warp w forms rows 4w .. 4w + 3, lane l dims 4l .. 4l + 3: one float4 of v and four probabilities per key
+  const int lane = t & 31, n0 = 4 * (t >> 5);
+  float o[4][4] = {};
   for (int j = 0; j < B; ++j) {
-    const float vj = v[j][t];
+    const float4 vj = *reinterpret_cast<const float4 *>(&v[j][4 * lane]);
 #pragma unroll
-    for (int n = 0; n < 16; ++n) o[n] += p[n][j] * vj;
+    for (int y = 0; y < 4; ++y) {
+      const float pj = p[n0 + y][j];
+      o[y][0] += pj * vj.x; o[y][1] += pj * vj.y; o[y][2] += pj * vj.z; o[y][3] += pj * vj.w;
+    }
   }
 #pragma unroll
-  for (int n = 0; n < 16; ++n)
-    if (n < B) out[(size_t)(r0 + n) * D + head * HD + t] = __float2half_rn(o[n]);
+  for (int y = 0; y < 4; ++y) {
+    if (n0 + y < B) {
+      const __half2 a = __floats2half2_rn(o[y][0], o[y][1]), b = __floats2half2_rn(o[y][2], o[y][3]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t *>(&a);
+      pk.y = *reinterpret_cast<const uint32_t *>(&b);
+      *reinterpret_cast<uint2 *>(out + (size_t)(r0 + n0 + y) * D + head * HD + 4 * lane) = pk;
+    }
+  }
 }
 
 // one warp per row: the best (value, index) over the row's column-block bests, in block order
@@ -299,7 +311,8 @@ cudaError_t launch_wide_lnmod(float *X, const float *R, int D, int T, const floa
                   (void *)&out};
   // D / 8 threads (two float4 each, whole warps) up to 256; wider rows give a thread up to four
   const int nt = D / 8 < 256 ? D / 8 : 256;
-  return launch_pdl((const void *)wide_lnmod_kernel, dim3(T), dim3(nt), args, s, 0);
+  return launch_pdl(D <= 2048 ? (const void *)wide_lnmod_kernel<2> : (const void *)wide_lnmod_kernel<4>, dim3(T),
+                    dim3(nt), args, s, 0);
 }
 
 cudaError_t launch_wide_self_attn(const float *qkv, int D, int B, int n_seqs, int n_heads, __half *out, cudaStream_t s) {
