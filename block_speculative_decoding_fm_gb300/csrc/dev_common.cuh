@@ -94,19 +94,6 @@ __device__ __forceinline__ void split2_f16(float a, float b, uint32_t &hi, uint3
   lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// Four signed bytes -> two f16x2 words (exact): bias to unsigned, place each
-// byte in the mantissa of 1024.0 and subtract 1024 + 128.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t v, uint32_t &w01, uint32_t &w23) {
-  const uint32_t u = v ^ 0x80808080u;
-  const uint32_t h01 = __byte_perm(u, 0x64646464u, 0x4140);
-  const uint32_t h23 = __byte_perm(u, 0x64646464u, 0x4342);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-  __half2 r01 = __hsub2(*reinterpret_cast<const __half2 *>(&h01), bias);
-  __half2 r23 = __hsub2(*reinterpret_cast<const __half2 *>(&h23), bias);
-  w01 = *reinterpret_cast<uint32_t *>(&r01);
-  w23 = *reinterpret_cast<uint32_t *>(&r23);
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
