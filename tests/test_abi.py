@@ -94,8 +94,28 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.fm_context_append(None, 0, None, 0, 0, None) == fm.FM_ERR_INVALID_ARG
     assert lib.fm_draft(None, 1, None, None, None, None, None) == fm.FM_ERR_INVALID_ARG
     assert lib.fm_debug_copy(None, 0, 0, 0, 0, None, 0, None) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_context_append_host(None, 0, None, 0, 0, None) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_context_append_batched_host(None, 1, None, None, None, None, None) == fm.FM_ERR_INVALID_ARG
+    assert lib.fm_draft_host(None, 1, None, None, None, None, None) == fm.FM_ERR_INVALID_ARG
     lib.fm_destroy(None)
     assert lib.fm_last_error(None) is not None
+
+
+def test_host_buffer_binding_checks():
+    """The binding's checks of a host-buffer call's rows and tokens (before any
+    library call): dtype, a host (not CUDA) buffer, C order, enough values."""
+    import torch
+    ok = [np.zeros(12, np.float32), torch.zeros(12), torch.zeros((3, 4))]
+    for x in ok:
+        assert fm._host_buffer(x, np.float32, "rows", 12) is x
+    assert fm._host_buffer(torch.zeros(8, dtype=torch.int32), np.int32, "tokens", 8) is not None
+    bad = [np.zeros(12, np.float64), torch.zeros(12, dtype=torch.float64), np.zeros((4, 3), np.float32).T,
+           torch.zeros((4, 3)).t(), np.zeros(12, np.int32)]
+    for x in bad:
+        with pytest.raises(ValueError):
+            fm._host_buffer(x, np.float32, "rows", 12)
+    with pytest.raises(ValueError):
+        fm._host_buffer(np.zeros(11, np.float32), np.float32, "rows", 12)
 
 
 def test_verify_policy_matches_the_oracle_step_for_step(lib):
