@@ -738,6 +738,13 @@ def blas_threads():
 
 # ----------------------------------------------------------------- arms
 
+def step_config(n_gpus):
+    """The default workload's config, the same on both arms."""
+    return {"workload": "flashmap4b_step: append 17 rows at 1024 + 16-slot draft at 1041 (L=1042), Q8_0 vocab 151936",
+            "global_batch": 16 * n_gpus, "seq_len": 1042, "parallelism": "replicas" if n_gpus > 1 else "single",
+            "l2": "inputs > L2 (1.35 GB/step)"}
+
+
 def run_reference(args):
     ws, rank, _ = dist()
     if rank != 0:
@@ -770,8 +777,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "flashmap4b_step: append 17 rows at 1024 + 16-slot draft at 1041 (L=1042)",
-                       "global_batch": 16, "seq_len": 1042, "parallelism": "replicas", "l2": "inputs > L2"},
+            "config": step_config(args.gpus),
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} full steps after {args.warmup} warm-up steps",
                              "blas_threads": blas_threads()},
@@ -857,9 +863,7 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "dtype_note": "bf16 / Q8_0 weights on bf16/f16 tensor cores with split (hi + lo) activations, "
                               "f32 accumulate", "data": "synthetic",
-                "config": {"workload": "flashmap4b_step: append 17 rows at 1024 + 16-slot draft at 1041 (L=1042), "
-                                       "Q8_0 vocab 151936", "global_batch": 16 * ws, "seq_len": 1042,
-                           "parallelism": "replicas" if ws > 1 else "single", "l2": "inputs > L2 (1.35 GB/step)"},
+                "config": step_config(ws),
                 "achieved_hbm_gbs": hbm_gbs, "bytes_per_step": w.bytes_per_step,
                 "e2e": e2e, "gpu_launches": launches, "roofline": roofline, "kernels": kernels,
                 "clocks": clk.summary(), "cpu_baseline": cpu, **extra}
